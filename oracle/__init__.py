@@ -1,0 +1,293 @@
+"""qlin oracle -- TEST INFRASTRUCTURE ONLY.
+
+A plain CPU statement (C, fp64 accumulation) of the quantized linear layer
+Y = X . deq(W)^T in its two variants, used to check the CUDA library.  Only
+``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import it; the product package never does, and the two
+share no code.  Every function cites the passage of the source pages it
+follows (see ``qlin_oracle.c`` for the list):
+
+  [LP] "Low-precision LLM inference: FP8/INT8/INT4/FP4 kernels and
+       calibration" -- S2 uniform quantisation, S3 symmetric/asymmetric,
+       S4 granularity, S5 effective bits, S7 E4M3, S8 FP8 current scaling,
+       S22 accumulator precision.
+  [TP] "Quantization throughput by batch size: why W4A16 is overtaken by
+       W8A8" -- the arithmetic-intensity roofline (``roofline_*`` below).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
+against closed forms, brute force, exhaustive code tables and library
+routines; no function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qlin_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liborc.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (IEEE rounding: no fast-math, no FMA contraction)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.orc_f16_to_f64.restype = ctypes.c_double
+        lib.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.orc_f32_to_f16_rn.restype = ctypes.c_uint16
+        lib.orc_f32_to_f16_rn.argtypes = [ctypes.c_float]
+        lib.orc_e4m3_to_f64.restype = ctypes.c_double
+        lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.orc_f32_to_e4m3_rn_sat.restype = ctypes.c_uint8
+        lib.orc_f32_to_e4m3_rn_sat.argtypes = [ctypes.c_float]
+        lib.orc_quantize_w4.restype = ctypes.c_int
+        lib.orc_quantize_w4.argtypes = [_p, _i64, _i64, ctypes.c_int, ctypes.c_int, _p, _p, _p]
+        lib.orc_dequant_w4.restype = None
+        lib.orc_dequant_w4.argtypes = [_p, _p, _p, _i64, _i64, ctypes.c_int, _p]
+        lib.orc_pack_canonical.restype = None
+        lib.orc_pack_canonical.argtypes = [_p, _p, _i64, _i64, ctypes.c_int, _p, _p]
+        lib.orc_pack_tile.restype = None
+        lib.orc_pack_tile.argtypes = [_p, _p, _p, _i64, _i64, _p, _p, _p]
+        lib.orc_quant_fp8_rows.restype = None
+        lib.orc_quant_fp8_rows.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.orc_quant_fp8_tensor.restype = None
+        lib.orc_quant_fp8_tensor.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.orc_gemm_nt_f64.restype = None
+        lib.orc_gemm_nt_f64.argtypes = [_p, _p, _i64, _i64, _i64, _p]
+        lib.orc_w4a16_at.restype = None
+        lib.orc_w4a16_at.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int,
+                                     _p, _p, _i64, _p]
+        lib.orc_w8a8_at.restype = None
+        lib.orc_w8a8_at.argtypes = [_p, _p, _p, ctypes.c_float, _i64, _i64, _i64,
+                                    _p, _p, _i64, _p]
+        lib.orc_num_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+# ---------------------------------------------------------------- formats
+
+def bf16_bits_to_f32(u16: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float32 values (bf16 is the top half of binary32)."""
+    return (np.ascontiguousarray(u16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f16_to_f64(h: int) -> float:
+    return float(_load().orc_f16_to_f64(int(h)))
+
+
+def f32_to_f16_rn(x: float) -> int:
+    return int(_load().orc_f32_to_f16_rn(float(x)))
+
+
+def e4m3_to_f64(c: int) -> float:
+    """[LP] S7: E4M3 (OCP fn variant) decode."""
+    return float(_load().orc_e4m3_to_f64(int(c)))
+
+
+def f32_to_e4m3(x: float) -> int:
+    """[LP] S7/S8: round-to-nearest-even encode with saturation to +-448."""
+    return int(_load().orc_f32_to_e4m3_rn_sat(float(x)))
+
+
+def e4m3_table() -> np.ndarray:
+    """Value of each of the 256 E4M3 codes (NaN for the two NaN codes)."""
+    return np.array([e4m3_to_f64(c) for c in range(256)], dtype=np.float64)
+
+
+def f16_bits_to_f64(h: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.ascontiguousarray(h, dtype=np.uint16).ravel()
+    uniq, inv = np.unique(flat, return_inverse=True)
+    vals = np.array([lib.orc_f16_to_f64(int(u)) for u in uniq], dtype=np.float64)
+    return vals[inv].reshape(np.shape(h))
+
+
+# ---------------------------------------------------------------- INT4 W4A16
+
+class W4Quant:
+    """Result of the per-group INT4 quantiser: one code per weight, unpacked."""
+
+    def __init__(self, q, s, z, G, symmetric, overflow):
+        self.q = q            # [N, K] uint8, stored code 0..15
+        self.s = s            # [N, K/G] uint16, binary16 bits
+        self.z = z            # [N, K/G] uint8, stored zero nibble
+        self.G = G
+        self.symmetric = symmetric
+        self.overflow = overflow
+
+
+def quantize_w4(W_bf16: np.ndarray, G: int = 128, symmetric: bool = False) -> W4Quant:
+    """[LP] S2-S4: q = clamp(round(x/s)+z, 0, 15) per group of G weights along K."""
+    W = np.ascontiguousarray(W_bf16, dtype=np.uint16)
+    N, K = W.shape
+    assert K % G == 0
+    q = np.empty((N, K), np.uint8)
+    s = np.empty((N, K // G), np.uint16)
+    z = np.empty((N, K // G), np.uint8)
+    ov = _load().orc_quantize_w4(_ptr(W), N, K, G, int(bool(symmetric)), _ptr(q), _ptr(s), _ptr(z))
+    return W4Quant(q, s, z, G, bool(symmetric), int(ov))
+
+
+def dequant_w4(wq: W4Quant) -> np.ndarray:
+    """[LP] S2: x_hat = s (q - z), exact in double."""
+    N, K = wq.q.shape
+    out = np.empty((N, K), np.float64)
+    _load().orc_dequant_w4(_ptr(wq.q), _ptr(wq.s), _ptr(wq.z), N, K, wq.G, _ptr(out))
+    return out
+
+
+def pack_canonical(wq: W4Quant):
+    """Canonical layout: codes [N][K/2] (low nibble = even k), zeros [N][K/2G]."""
+    N, K = wq.q.shape
+    ng = K // wq.G
+    codes = np.empty((N, K // 2), np.uint8)
+    zeros = np.empty(((N * ng + 1) // 2,), np.uint8)
+    _load().orc_pack_canonical(_ptr(wq.q), _ptr(wq.z), N, K, wq.G, _ptr(codes), _ptr(zeros))
+    return codes, wq.s.copy(), zeros
+
+
+def pack_tile(wq: W4Quant):
+    """Tile layout v1 (128 x 64 tiles, G = 128): codes, scales, zeros as flat arrays."""
+    N, K = wq.q.shape
+    assert wq.G == 128 and N % 128 == 0 and K % 128 == 0
+    codes = np.empty((N * K // 2,), np.uint8)
+    scales = np.empty((N * K // 128,), np.uint16)
+    zeros = np.empty((N * K // 256,), np.uint8)
+    _load().orc_pack_tile(_ptr(wq.q), _ptr(wq.s), _ptr(wq.z), N, K,
+                          _ptr(codes), _ptr(scales), _ptr(zeros))
+    return codes, scales, zeros
+
+
+def w4a16_full(X_bf16: np.ndarray, wq: W4Quant) -> np.ndarray:
+    """Y = X . deq(W)^T in double: dequantise, then a plain fp64 GEMM."""
+    X = bf16_bits_to_f32(X_bf16).astype(np.float64)
+    Wd = dequant_w4(wq)
+    return gemm_nt_f64(X, Wd)
+
+
+def w4a16_at(X_bf16: np.ndarray, wq: W4Quant, ms: np.ndarray, ns: np.ndarray) -> np.ndarray:
+    """Y[m_i, n_i] for sampled pairs, each an fp64 dot product over K."""
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    M, K = X.shape
+    N = wq.q.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape, np.float64)
+    _load().orc_w4a16_at(_ptr(X), _ptr(wq.q), _ptr(wq.s), _ptr(wq.z), M, N, K, wq.G,
+                         _ptr(ms), _ptr(ns), ms.size, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- FP8 W8A8
+
+def quant_fp8_rows(X_bf16: np.ndarray):
+    """[LP] S4 per-token + S8 current scaling: s_x[m] = amax_m / 448, Xq = E4M3(X / s_x)."""
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    M, K = X.shape
+    Xq = np.empty((M, K), np.uint8)
+    sx = np.empty((M,), np.float32)
+    _load().orc_quant_fp8_rows(_ptr(X), M, K, _ptr(Xq), _ptr(sx))
+    return Xq, sx
+
+
+def quant_fp8_tensor(W_bf16: np.ndarray):
+    """[LP] S4 per-tensor + S8: s_w = amax(W) / 448, Wq = E4M3(W / s_w)."""
+    W = np.ascontiguousarray(W_bf16, dtype=np.uint16)
+    N, K = W.shape
+    Wq = np.empty((N, K), np.uint8)
+    sw = np.empty((1,), np.float32)
+    _load().orc_quant_fp8_tensor(_ptr(W), N, K, _ptr(Wq), _ptr(sw))
+    return Wq, float(sw[0])
+
+
+def e4m3_decode_array(c: np.ndarray) -> np.ndarray:
+    return e4m3_table()[np.asarray(c, dtype=np.uint8)]
+
+
+def w8a8_full(Xq, sx, Wq, sw) -> np.ndarray:
+    """Y = diag(s_x) (dec(Xq) . dec(Wq)^T) s_w in double."""
+    tab = e4m3_table()
+    A = tab[Xq]
+    B = tab[Wq]
+    Y = gemm_nt_f64(np.ascontiguousarray(A), np.ascontiguousarray(B))
+    return Y * np.asarray(sx, np.float64)[:, None] * float(sw)
+
+
+def w8a8_at(Xq, sx, Wq, sw, ms, ns) -> np.ndarray:
+    Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape, np.float64)
+    _load().orc_w8a8_at(_ptr(Xq), _ptr(sx), _ptr(Wq), float(sw), M, N, K,
+                        _ptr(ms), _ptr(ns), ms.size, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- GEMM
+
+def gemm_nt_f64(A: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """[LP] S22: Y = A . B^T accumulated in double (plain loops in C)."""
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    B = np.ascontiguousarray(B, dtype=np.float64)
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2
+    Y = np.empty((M, N), np.float64)
+    _load().orc_gemm_nt_f64(_ptr(A), _ptr(B), M, N, K, _ptr(Y))
+    return Y
+
+
+# ---------------------------------------------------------------- bytes and roofline
+
+def w4_bits_per_weight(N: int, K: int, G: int = 128, with_zeros: bool = False) -> float:
+    """[LP] S5: effective bits from the packed buffer sizes (codes + scales [+ zeros])."""
+    codes = N * K // 2
+    scales = N * (K // G) * 2
+    zeros = (N * (K // G) + 1) // 2
+    total = codes + scales + (zeros if with_zeros else 0)
+    return 8.0 * total / (N * K)
+
+
+def roofline_transition_batch(ridge_flop_per_byte: float, bytes_per_weight: float) -> float:
+    """[TP] arithmetic intensity of a decode GEMM, AI(B) = 2B / bytes_per_weight;
+    the compute-bound transition is the batch where AI reaches the ridge."""
+    return ridge_flop_per_byte * bytes_per_weight / 2.0

@@ -1,0 +1,399 @@
+/*
+ * qlin oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU statement of what the quantized linear
+ * layer computes.  Only the test-suite, the smoke check and the CPU-baseline
+ * leg of the benchmark may load this library; the product path never does.
+ * It shares no code, header or table with the CUDA library.
+ *
+ * Sources (web pages; section names as printed on each page):
+ *  [LP]  "Low-precision LLM inference: FP8/INT8/INT4/FP4 kernels and
+ *         calibration" (blog.ruahverce.com, post 68)
+ *        S1  precision manifest: accumulate in a wider type, output BF16
+ *        S2  Uniform Integer Quantization: q = clamp(round(x/s)+z, qmin, qmax),
+ *            x_hat = s(q - z)
+ *        S3  Symmetric (z = 0, s = max|x|/qmax) and Asymmetric (range from the
+ *            observed min/max)
+ *        S4  granularity: per-tensor, per-token/row, per-group (128 weights)
+ *        S5  effective bits b + m/G
+ *        S7  FP8 E4M3 = 1 sign, 4 exponent, 3 mantissa bits
+ *        S8  current scaling: scale = amax / max_representable_fp8
+ *        S22 accumulator precision
+ *  [TP]  "Quantization throughput by batch size: why W4A16 is overtaken by
+ *         W8A8" (hrletsgo.me) -- roofline arithmetic only (not in this file).
+ *
+ * Readings of points the pages leave open (each also listed in the design
+ * notes): asymmetric s = (hi-lo)/15 with the range widened to include 0,
+ * z = clamp(rint(-lo/s),0,15); round() is round-half-to-even; x/s is an IEEE
+ * binary32 division by the stored FP16 scale; a group whose FP16 scale
+ * rounds to 0 stores s = 1, z = 0; E4M3 is the OCP "fn" variant (max 448,
+ * no infinities) with round-to-nearest-even and saturation; an all-zero FP8
+ * row or tensor takes scale 1.
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -fPIC -shared
+ * (no -ffast-math: every rounding here is the IEEE one).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* Number formats, written from their definitions.                      */
+/* ------------------------------------------------------------------ */
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* IEEE binary16 -> value. */
+double orc_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+/* binary32 -> IEEE binary16, round to nearest, ties to even; overflow to inf. */
+uint16_t orc_f32_to_f16_rn(float f)
+{
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    double a = fabs((double)f);
+    int e2;
+    if (isnan(f))
+        return sign | 0x7e00;
+    if (isinf(f))
+        return sign | 0x7c00;
+    if (a == 0.0)
+        return sign;
+    frexp(a, &e2);          /* a = frac * 2^e2, frac in [0.5, 1) */
+    int E = e2 - 1;         /* a = 1.xxx * 2^E */
+    if (E < -14) {          /* subnormal range: quantum 2^-24 */
+        double r = rint(ldexp(a, 24));
+        return sign | (uint16_t)r;       /* r == 1024 is the smallest normal */
+    }
+    double r = rint(ldexp(a, 10 - E));  /* 11-bit significand in [1024, 2048] */
+    if (r == 2048.0) {
+        r = 1024.0;
+        E += 1;
+    }
+    if (E > 15)
+        return sign | 0x7c00;
+    return sign | (uint16_t)((E + 15) << 10) | (uint16_t)(r - 1024.0);
+}
+
+/* OCP FP8 E4M3 ("fn"): bias 7, no infinities, S.1111.111 is NaN, max 448. */
+double orc_e4m3_to_f64(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 15;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(8 + m), e - 10);
+    return sign ? -v : v;
+}
+
+/* binary32 -> E4M3, round to nearest even, then saturate to +-448. */
+uint8_t orc_f32_to_e4m3_rn_sat(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x))
+        return sign | 0x7f;
+    if (isinf(x))
+        return sign | 0x7e;
+    double a = fabs((double)x);
+    if (a == 0.0)
+        return sign;
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1;
+    if (E < -6) {                          /* subnormal quantum 2^-9 */
+        double r = rint(ldexp(a, 9));      /* 0..8; 8 is the smallest normal */
+        return sign | (uint8_t)r;
+    }
+    double r = rint(ldexp(a, 3 - E));      /* 4-bit significand in [8, 16] */
+    if (r == 16.0) {
+        r = 8.0;
+        E += 1;
+    }
+    if (E + 7 > 15)
+        return sign | 0x7e;
+    int code = ((E + 7) << 3) | (int)(r - 8.0);
+    if (code > 0x7e)                       /* would be the NaN pattern: saturate */
+        code = 0x7e;
+    return sign | (uint8_t)code;
+}
+
+/* ------------------------------------------------------------------ */
+/* INT4 weight quantisation, one group of G weights along K per scale.  */
+/* [LP] S2 (formula), S3 (symmetric / asymmetric), S4 (per-group).      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * W    : [N][K] bfloat16 bits
+ * q    : [N][K] stored code per weight, one per byte, 0..15
+ * s    : [N][K/G] IEEE binary16 bits of the scale
+ * z    : [N][K/G] stored zero-point nibble, 0..15
+ * Asymmetric: q = clamp(rint(w/s) + z, 0, 15), x_hat = s (q - z).
+ * Symmetric : signed code c = clamp(rint(w/s), -8, 7) stored as q = c + 8
+ *             with stored zero 8, so that s (q - z) = s c (logical z = 0).
+ * Returns the number of groups whose scale overflowed binary16.
+ */
+int orc_quantize_w4(const uint16_t *W, int64_t N, int64_t K, int G, int symmetric,
+                    uint8_t *q, uint16_t *s, uint8_t *z)
+{
+    int64_t ng = K / G;
+    int overflow = 0;
+#pragma omp parallel for reduction(+ : overflow) schedule(static)
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t g = 0; g < ng; g++) {
+            const uint16_t *w = W + n * K + g * G;
+            float lo = 0.0f, hi = 0.0f, amax = 0.0f;   /* range widened to include 0 */
+            for (int i = 0; i < G; i++) {
+                float v = bf16_to_f32(w[i]);
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+                if (fabsf(v) > amax) amax = fabsf(v);
+            }
+            float s32 = symmetric ? amax / 7.0f : (hi - lo) / 15.0f;
+            uint16_t s16 = orc_f32_to_f16_rn(s32);
+            float sc = (float)orc_f16_to_f64(s16);
+            int zp;
+            if (sc == 0.0f) {            /* degenerate group */
+                s16 = 0x3c00;            /* 1.0 */
+                sc = 1.0f;
+                zp = symmetric ? 8 : 0;
+            } else if (symmetric) {
+                zp = 8;
+            } else {
+                float zf = rintf(-lo / sc);
+                if (zf < 0.0f) zf = 0.0f;
+                if (zf > 15.0f) zf = 15.0f;
+                zp = (int)zf;
+            }
+            if (isinf(sc))
+                overflow += 1;
+            s[n * ng + g] = s16;
+            z[n * ng + g] = (uint8_t)zp;
+            for (int i = 0; i < G; i++) {
+                float v = bf16_to_f32(w[i]);
+                float r = rintf(v / sc);
+                int c;
+                if (symmetric) {
+                    if (r < -8.0f) r = -8.0f;
+                    if (r > 7.0f) r = 7.0f;
+                    c = (int)r + 8;
+                } else {
+                    r = r + (float)zp;
+                    if (r < 0.0f) r = 0.0f;
+                    if (r > 15.0f) r = 15.0f;
+                    c = (int)r;
+                }
+                q[n * K + g * G + i] = (uint8_t)c;
+            }
+        }
+    }
+    return overflow;
+}
+
+/* x_hat = s (q - z) for every weight, as double (exact). [LP] S2. */
+void orc_dequant_w4(const uint8_t *q, const uint16_t *s, const uint8_t *z,
+                    int64_t N, int64_t K, int G, double *Wdeq)
+{
+    int64_t ng = K / G;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) {
+            double sc = orc_f16_to_f64(s[n * ng + k / G]);
+            Wdeq[n * K + k] = sc * ((double)q[n * K + k] - (double)z[n * ng + k / G]);
+        }
+}
+
+/*
+ * Canonical packed layout (format version 1):
+ *   codes [N][K/2]   byte n*K/2 + k/2, low nibble = even k
+ *   zeros [N][K/2G]  byte n*(K/G)/2 + g/2, low nibble = even g
+ *   scales are already [N][K/G] binary16.
+ */
+void orc_pack_canonical(const uint8_t *q, const uint8_t *z, int64_t N, int64_t K, int G,
+                        uint8_t *codes, uint8_t *zeros)
+{
+    int64_t ng = K / G;
+    memset(codes, 0, (size_t)(N * K / 2));
+    memset(zeros, 0, (size_t)((N * ng + 1) / 2));
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t k = 0; k < K; k++) {
+            uint8_t v = q[n * K + k] & 15;
+            codes[n * (K / 2) + k / 2] |= (k % 2 == 0) ? v : (uint8_t)(v << 4);
+        }
+        for (int64_t g = 0; g < ng; g++) {
+            uint8_t v = z[n * ng + g] & 15;
+            int64_t idx = n * ng + g;
+            zeros[idx / 2] |= (idx % 2 == 0) ? v : (uint8_t)(v << 4);
+        }
+    }
+}
+
+/*
+ * Tile layout (format version 1), restated from its written description:
+ * tiles of 128 rows (n) by 64 columns (k); G must be 128.
+ *   codes : tile (nb = n/128, kb = k/64) is 4096 bytes at
+ *           (nb * (K/64) + kb) * 4096; inside it, half h = (k%64)/32 and row
+ *           r = n%128 own the 16 bytes at h*2048 + r*16.  Those 16 bytes are
+ *           four little-endian 32-bit words; word j = (k%32)/8 holds the eight
+ *           columns 8j..8j+7 of that half, column e = k%8 in nibble position
+ *           p = e/2 for even e and p = 4 + e/2 for odd e (bits 4p..4p+3).
+ *   scales: binary16 at element (nb * (K/128) + g) * 128 + r.
+ *   zeros : byte (nb * (K/128) + g) * 64 + r/2, low nibble for even r.
+ */
+void orc_pack_tile(const uint8_t *q, const uint16_t *s, const uint8_t *z,
+                   int64_t N, int64_t K, uint8_t *codes, uint16_t *scales, uint8_t *zeros)
+{
+    int64_t ng = K / 128;
+    memset(codes, 0, (size_t)(N * K / 2));
+    memset(zeros, 0, (size_t)(N * ng / 2));
+    for (int64_t n = 0; n < N; n++) {
+        int64_t nb = n / 128, r = n % 128;
+        for (int64_t k = 0; k < K; k++) {
+            int64_t kb = k / 64, h = (k % 64) / 32, j = (k % 32) / 8, e = k % 8;
+            int64_t p = (e % 2 == 0) ? e / 2 : 4 + e / 2;
+            int64_t byte = (nb * (K / 64) + kb) * 4096 + h * 2048 + r * 16 + j * 4 + p / 2;
+            uint8_t v = q[n * K + k] & 15;
+            codes[byte] |= (p % 2 == 0) ? v : (uint8_t)(v << 4);
+        }
+        for (int64_t g = 0; g < ng; g++) {
+            scales[(nb * ng + g) * 128 + r] = s[n * ng + g];
+            uint8_t v = z[n * ng + g] & 15;
+            zeros[(nb * ng + g) * 64 + r / 2] |= (r % 2 == 0) ? v : (uint8_t)(v << 4);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* FP8 E4M3 quantisation with current (amax) scaling.                   */
+/* [LP] S4 per-token and per-tensor, S7 E4M3, S8 scale = amax / 448.    */
+/* ------------------------------------------------------------------ */
+
+static float amax_scale(float amax)
+{
+    return amax == 0.0f ? 1.0f : amax / 448.0f;
+}
+
+/* Per-row (per-token) scales: X [M][K] bf16 -> Xq [M][K] e4m3, sx [M]. */
+void orc_quant_fp8_rows(const uint16_t *X, int64_t M, int64_t K, uint8_t *Xq, float *sx)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; k++) {
+            float a = fabsf(bf16_to_f32(X[m * K + k]));
+            if (a > amax) amax = a;
+        }
+        float sc = amax_scale(amax);
+        sx[m] = sc;
+        for (int64_t k = 0; k < K; k++)
+            Xq[m * K + k] = orc_f32_to_e4m3_rn_sat(bf16_to_f32(X[m * K + k]) / sc);
+    }
+}
+
+/* One scale for the whole tensor: W [N][K] bf16 -> Wq [N][K] e4m3, *sw. */
+void orc_quant_fp8_tensor(const uint16_t *W, int64_t N, int64_t K, uint8_t *Wq, float *sw)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < N * K; i++) {
+        float a = fabsf(bf16_to_f32(W[i]));
+        if (a > amax) amax = a;
+    }
+    float sc = amax_scale(amax);
+    *sw = sc;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < N * K; i++)
+        Wq[i] = orc_f32_to_e4m3_rn_sat(bf16_to_f32(W[i]) / sc);
+}
+
+/* ------------------------------------------------------------------ */
+/* The linear layer Y = A . B^T, accumulated in double, no rounding of Y. */
+/* [LP] S1 / S22: wide accumulation; the double result is the exact      */
+/* target that the device's FP32-accumulated, BF16-rounded Y is held to. */
+/* ------------------------------------------------------------------ */
+
+void orc_gemm_nt_f64(const double *A, const double *B, int64_t M, int64_t N, int64_t K, double *Y)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; k++)
+                acc += A[m * K + k] * B[n * K + k];
+            Y[m * N + n] = acc;
+        }
+}
+
+/* W4A16: Y[m][n] = sum_k X[m][k] * s[n][k/G] * (q[n][k] - z[n][k/G]).   */
+/* Evaluated at `cnt` (m, n) pairs; every term in double.  [LP] S2, S11. */
+void orc_w4a16_at(const uint16_t *X, const uint8_t *q, const uint16_t *s, const uint8_t *z,
+                  int64_t M, int64_t N, int64_t K, int G,
+                  const int64_t *ms, const int64_t *ns, int64_t cnt, double *out)
+{
+    int64_t ng = K / G;
+    (void)M;
+    (void)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < cnt; i++) {
+        int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            double sc = orc_f16_to_f64(s[n * ng + k / G]);
+            double w = sc * ((double)q[n * K + k] - (double)z[n * ng + k / G]);
+            acc += (double)bf16_to_f32(X[m * K + k]) * w;
+        }
+        out[i] = acc;
+    }
+}
+
+/* W8A8: Y[m][n] = sx[m] * sw * sum_k e4m3(Xq[m][k]) * e4m3(Wq[n][k]).   */
+void orc_w8a8_at(const uint8_t *Xq, const float *sx, const uint8_t *Wq, float sw,
+                 int64_t M, int64_t N, int64_t K,
+                 const int64_t *ms, const int64_t *ns, int64_t cnt, double *out)
+{
+    (void)M;
+    (void)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < cnt; i++) {
+        int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; k++)
+            acc += orc_e4m3_to_f64(Xq[m * K + k]) * orc_e4m3_to_f64(Wq[n * K + k]);
+        out[i] = acc * (double)sx[m] * (double)sw;
+    }
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,409 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests needs a GPU.  Each pin is independent of the oracle's own
+code: closed forms, exhaustive code tables, brute force on tiny inputs,
+library routines (numpy / torch casts and matmul) and values printed on the
+pages (``tests/golden/page_values.json``).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_quantized_linear_gb300 import synthetic as syn
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_values.json")))
+
+
+def _bf16(vals):
+    return syn.f32_to_bf16_bits(np.asarray(vals, dtype=np.float32))
+
+
+# ------------------------------------------------------------------ formats
+
+def test_f16_encode_matches_numpy_rne():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * 1e-3,
+        rng.standard_normal(20000).astype(np.float32) * 1e4,
+        (rng.random(5000).astype(np.float32) * 6.1e-5),        # subnormal range
+        np.float32([0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6, 5.96e-8, 2.98e-8, 2.99e-8]),
+    ])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    ours = np.array([oracle.f32_to_f16_rn(v) for v in x], dtype=np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_f16_decode_all_codes():
+    codes = np.arange(65536, dtype=np.uint16)
+    ours = oracle.f16_bits_to_f64(codes)
+    ref = codes.view(np.float16).astype(np.float64)
+    finite = np.isfinite(ref)
+    assert np.array_equal(ours[finite], ref[finite])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+
+
+def test_e4m3_decode_all_codes_vs_torch():
+    tab = oracle.e4m3_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(tab), np.isnan(ref))
+    assert np.array_equal(tab[~np.isnan(tab)], ref[~np.isnan(ref)])
+    # the format facts: max 448, smallest subnormal 2^-9, NaN only at S.1111.111
+    assert np.nanmax(tab) == 448.0 and tab[0x7E] == 448.0
+    assert tab[1] == 2.0 ** -9
+    assert set(np.flatnonzero(np.isnan(tab))) == {0x7F, 0xFF}
+
+
+def test_e4m3_roundtrip_every_code():
+    tab = oracle.e4m3_table()
+    for c in range(256):
+        if np.isnan(tab[c]):
+            continue
+        assert oracle.f32_to_e4m3(tab[c]) == c, c
+
+
+def test_e4m3_midpoints_round_to_even_and_saturate():
+    tab = oracle.e4m3_table()
+    pos = sorted({(tab[c], c) for c in range(0x7F)})
+    for (v0, c0), (v1, c1) in zip(pos[:-1], pos[1:]):
+        mid = np.float32((v0 + v1) / 2)
+        if float(mid) != (v0 + v1) / 2:
+            continue
+        want = c0 if (c0 & 1) == 0 else c1
+        assert oracle.f32_to_e4m3(mid) == want, (v0, v1)
+        assert oracle.f32_to_e4m3(-mid) == want | 0x80
+    for big in (448.0, 463.9, 464.0, 480.0, 1e4, 3e38):
+        assert oracle.f32_to_e4m3(big) == 0x7E
+        assert oracle.f32_to_e4m3(-big) == 0xFE
+
+
+def test_e4m3_encode_is_nearest_code_brute_force():
+    tab = oracle.e4m3_table()
+    finite_pos = np.array([tab[c] for c in range(0x7F)])
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(3000) * 50, rng.standard_normal(3000) * 0.01]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    for v in x:
+        c = oracle.f32_to_e4m3(v)
+        d = np.abs(finite_pos - abs(float(v)))
+        best = d.min()
+        assert abs(tab[c & 0x7F] - abs(float(v))) == best
+        if v != 0:
+            assert (c >> 7) == (1 if v < 0 else 0)
+
+
+def test_e4m3_encode_matches_torch_cast_in_range():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(50000) * 60).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    ours = np.array([oracle.f32_to_e4m3(v) for v in x], dtype=np.uint8)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+# ------------------------------------------------------------------ INT4 quantiser
+
+def _group_grid_ok(Wf, wq, G):
+    """Round-trip bound |x - x_hat| <= s/2 for every weight whose code is not clamped."""
+    deq = oracle.dequant_w4(wq)
+    s = oracle.f16_bits_to_f64(wq.s)
+    N, K = Wf.shape
+    s_full = np.repeat(s, G, axis=1)
+    err = np.abs(Wf.astype(np.float64) - deq)
+    return err, s_full, deq
+
+
+def test_asymmetric_all_16_codes_and_exact_grid():
+    G = 128
+    # one group per row spanning a different range; linspace hits every code
+    rows = []
+    # the first two ranges are exact multiples of s = range/15 (every code appears);
+    # the others leave z to rounding, so one end code may go unused
+    for lo, hi in [(-3.0, 4.5), (-0.25, 0.125), (-1.0, 2.0), (-0.003, 0.001), (-50.0, 10.0),
+                   (0.5, 3.0), (-4.0, -1.0)]:
+        rows.append(np.linspace(lo, hi, G, dtype=np.float32))
+    W = _bf16(np.stack(rows))
+    Wf = syn.bf16_bits_to_f32(W)
+    wq = oracle.quantize_w4(W, G=G, symmetric=False)
+    for r in range(len(rows)):
+        lo = min(Wf[r].min(), 0.0)
+        hi = max(Wf[r].max(), 0.0)
+        used = set(wq.q[r].tolist())
+        if r < 2:
+            assert used == set(range(16))
+        elif lo < 0.0 < hi:
+            assert len(used) >= 15
+        else:
+            assert len(used) >= 8
+        # dequantised values lie exactly on the grid s (c - z), c in 0..15
+        s = oracle.f16_to_f64(int(wq.s[r, 0]))
+        z = int(wq.z[r, 0])
+        deq = oracle.dequant_w4(wq)[r]
+        grid = s * (np.arange(16) - z)
+        assert np.all(np.isin(deq, grid))
+        # zero is exactly representable: the grid contains 0
+        assert 0.0 in grid
+    err, s_full, _ = _group_grid_ok(Wf, wq, G)
+    assert np.all(err <= s_full / 2 * (1 + 2 ** -20))
+
+
+def test_asymmetric_round_trip_bound_random_groups():
+    G = 128
+    rng = np.random.default_rng(3)
+    N, K = 16, 1024
+    w = rng.standard_normal((N, K)).astype(np.float32) * 0.02
+    # groups of very different magnitude catch a wrong group index
+    w *= (10.0 ** rng.integers(-2, 3, size=(N, K // G))).repeat(G, axis=1).astype(np.float32)
+    W = _bf16(w)
+    Wf = syn.bf16_bits_to_f32(W)
+    wq = oracle.quantize_w4(W, G=G)
+    err, s_full, deq = _group_grid_ok(Wf, wq, G)
+    assert np.all(err <= s_full / 2 * (1 + 2 ** -20))
+    # the nearest grid point is chosen: no other code is strictly closer
+    s = s_full
+    zf = np.repeat(wq.z.astype(np.float64), G, axis=1)
+    for c in range(16):
+        alt = s * (c - zf)
+        assert np.all(np.abs(Wf - alt) >= err - s * 2 ** -20)
+
+
+def test_symmetric_zero_point_and_extremes():
+    G = 128
+    rng = np.random.default_rng(4)
+    W = _bf16(rng.standard_normal((8, 256)).astype(np.float32) * 0.05)
+    Wf = syn.bf16_bits_to_f32(W).reshape(8, 2, G)
+    wq = oracle.quantize_w4(W, G=G, symmetric=True)
+    assert np.all(wq.z == 8)                       # logical zero-point 0, offset-binary storage
+    codes = wq.q.reshape(8, 2, G).astype(int) - 8  # signed codes
+    amax_pos = np.abs(Wf).argmax(axis=2)
+    for n in range(8):
+        for g in range(2):
+            c = codes[n, g, amax_pos[n, g]]
+            v = Wf[n, g, amax_pos[n, g]]
+            assert c == (7 if v > 0 else -7)      # max|x| maps to +-qmax
+    err, s_full, _ = _group_grid_ok(syn.bf16_bits_to_f32(W), wq, G)
+    assert np.all(err <= s_full / 2 * (1 + 2 ** -20))
+
+
+def test_degenerate_group_zero():
+    W = _bf16(np.zeros((2, 128), np.float32))
+    for sym in (False, True):
+        wq = oracle.quantize_w4(W, G=128, symmetric=sym)
+        assert np.all(wq.s == 0x3C00)
+        assert np.all(oracle.dequant_w4(wq) == 0.0)
+
+
+def test_scale_is_fp16_of_range_over_15():
+    # one closed-form value: range [-1.5, 6.0] -> s = 7.5/15 = 0.5, z = 3
+    v = np.zeros(128, np.float32)
+    v[0], v[1] = -1.5, 6.0
+    wq = oracle.quantize_w4(_bf16(v[None, :]), G=128)
+    assert oracle.f16_to_f64(int(wq.s[0, 0])) == 0.5
+    assert wq.z[0, 0] == 3
+    assert wq.q[0, 0] == 0 and wq.q[0, 1] == 15 and wq.q[0, 2] == 3
+
+
+# ------------------------------------------------------------------ packing
+
+def test_canonical_pack_nibble_order():
+    rng = np.random.default_rng(1)
+    W = syn.make_weight(4, 256, seed=9, outlier_frac=0.0)
+    wq = oracle.quantize_w4(W, G=128)
+    codes, scales, zeros = oracle.pack_canonical(wq)
+    lo = codes & 15
+    hi = codes >> 4
+    assert np.array_equal(lo, wq.q[:, 0::2])
+    assert np.array_equal(hi, wq.q[:, 1::2])
+    zflat = wq.z.ravel()
+    assert np.array_equal(zeros & 15, zflat[0::2])
+    assert np.array_equal(zeros >> 4, zflat[1::2])
+
+
+def test_tile_pack_is_a_bijection_and_hand_positions():
+    N, K = 256, 256
+    # distinct code per (n, k) position modulo 16 is not unique; use single-hot probes
+    q = np.zeros((N, K), np.uint8)
+    s = np.full((N, K // 128), 0x3C00, np.uint16)
+    z = np.zeros((N, K // 128), np.uint8)
+    wq = oracle.W4Quant(q, s, z, 128, False, 0)
+    seen = np.zeros(N * K, bool)
+    rng = np.random.default_rng(2)
+    for (n, k) in [(0, 0), (0, 1), (0, 2), (0, 7), (0, 8), (0, 32), (0, 63), (0, 64),
+                   (1, 0), (127, 255), (128, 0), (255, 255)] + [tuple(x) for x in rng.integers(0, 256, (40, 2))]:
+        q[:] = 0
+        q[n, k] = 0xF
+        codes, _, _ = oracle.pack_tile(wq)
+        nz = np.flatnonzero(codes)
+        assert nz.size == 1
+        byte = nz[0]
+        nib = 0 if codes[byte] == 0x0F else 1
+        assert codes[byte] in (0x0F, 0xF0)
+        pos = byte * 2 + nib
+        assert not seen[pos]
+        seen[pos] = True
+        if (n, k) == (0, 0):
+            assert (byte, nib) == (0, 0)
+        if (n, k) == (0, 1):            # odd column 1 -> nibble position 4 -> byte 2, low
+            assert (byte, nib) == (2, 0)
+        if (n, k) == (0, 2):            # even column 2 -> nibble position 1 -> byte 0, high
+            assert (byte, nib) == (0, 1)
+        if (n, k) == (0, 7):            # position 7 -> byte 3, high
+            assert (byte, nib) == (3, 1)
+        if (n, k) == (0, 8):            # next 32-bit word
+            assert (byte, nib) == (4, 0)
+        if (n, k) == (0, 32):           # second half of the 64-column tile
+            assert (byte, nib) == (2048, 0)
+        if (n, k) == (1, 0):            # next row: 16 bytes on
+            assert (byte, nib) == (16, 0)
+        if (n, k) == (0, 64):           # next k tile of the same row tile
+            assert (byte, nib) == (4096, 0)
+        if (n, k) == (128, 0):          # next row tile: after K/64 = 4 tiles
+            assert (byte, nib) == (4 * 4096, 0)
+
+
+def test_tile_pack_roundtrip_full():
+    N, K = 256, 512
+    W = syn.make_weight(N, K, seed=3)
+    wq = oracle.quantize_w4(W, G=128)
+    codes, scales, zeros = oracle.pack_tile(wq)
+    # unpack by the written description and compare with the unpacked codes
+    c = codes.reshape(N // 128, K // 64, 2, 128, 4, 4)          # nb, kb, h, r, word j, byte
+    nib = np.stack([c & 15, c >> 4], axis=-1).reshape(N // 128, K // 64, 2, 128, 4, 8)  # position p
+    order = [0, 4, 1, 5, 2, 6, 3, 7]                             # column e -> position p
+    e_of_p = np.argsort(order)
+    cols = nib[..., order]                                       # now indexed by column e
+    un = cols.transpose(0, 3, 1, 2, 4, 5).reshape(N, K)
+    assert np.array_equal(un, wq.q)
+    sc = scales.reshape(N // 128, K // 128, 128).transpose(0, 2, 1).reshape(N, K // 128)
+    assert np.array_equal(sc, wq.s)
+    zz = zeros.reshape(N // 128, K // 128, 64)
+    zz = np.stack([zz & 15, zz >> 4], axis=-1).reshape(N // 128, K // 128, 128)
+    assert np.array_equal(zz.transpose(0, 2, 1).reshape(N, K // 128), wq.z)
+    assert e_of_p.tolist() == [0, 2, 4, 6, 1, 3, 5, 7]
+
+
+def test_effective_bits_from_buffers():
+    gold = GOLDEN["effective_bits_int4_fp16_scale_g128"]
+    N, K = 256, 512
+    wq = oracle.quantize_w4(syn.make_weight(N, K, seed=1), G=128)
+    codes, scales, zeros = oracle.pack_tile(wq)
+    bits = 8.0 * (codes.nbytes + scales.nbytes) / (N * K)
+    assert bits == gold["value"] == gold["b"] + gold["m"] / gold["G"]
+    assert 8.0 * (codes.nbytes + scales.nbytes + zeros.nbytes) / (N * K) == 4.15625
+    assert oracle.w4_bits_per_weight(N, K) == 4.125
+
+
+def test_8b_bytes_thought_experiment():
+    gold = GOLDEN["model_8b_weight_gb"]
+    p = gold["params"]
+    assert p * 2 / 1e9 == gold["bf16"] and p * 1 / 1e9 == gold["int8"] and p * 0.5 / 1e9 == gold["int4"]
+    # with FP16 scales per 128 and 4-bit zeros the resident bytes are above the ideal 4 GB
+    packed = p * oracle.w4_bits_per_weight(4096, 4096, with_zeros=True) / 8 / 1e9
+    assert 4.0 < packed < 4.2
+
+
+# ------------------------------------------------------------------ FP8 quantisation
+
+def test_fp8_per_token_scale_and_max_code():
+    X = syn.make_act(9, 512, seed=4, token_outlier_frac=0.2)
+    X[3, :] = 0                                   # all-zero row -> scale 1, codes 0
+    Xq, sx = oracle.quant_fp8_rows(X)
+    Xf = syn.bf16_bits_to_f32(X)
+    tab = oracle.e4m3_table()
+    for m in range(9):
+        amax = np.abs(Xf[m]).max()
+        if amax == 0:
+            assert sx[m] == 1.0 and np.all(Xq[m] == 0)
+            continue
+        assert sx[m] == np.float32(amax) / np.float32(448.0)
+        i = np.abs(Xf[m]).argmax()
+        assert Xq[m, i] in (0x7E, 0xFE)
+        dec = tab[Xq[m]] * sx[m]
+        normal = np.abs(tab[Xq[m]]) >= 2.0 ** -6
+        rel = np.abs(dec - Xf[m])[normal] / np.abs(Xf[m])[normal]
+        assert rel.max() <= 2.0 ** -4 * (1 + 1e-6)
+
+
+def test_fp8_per_tensor_scale():
+    W = syn.make_weight(64, 256, seed=2)
+    Wq, sw = oracle.quant_fp8_tensor(W)
+    Wf = syn.bf16_bits_to_f32(W)
+    assert sw == np.float32(np.abs(Wf).max()) / np.float32(448.0)
+    assert np.sum((Wq & 0x7F) == 0x7E) >= 1
+    # exact power-of-two case: amax = 448 -> scale 1, codes equal the direct cast
+    v = np.zeros((1, 128), np.float32)
+    v[0, :] = np.linspace(-448, 448, 128, dtype=np.float32)
+    Wq2, sw2 = oracle.quant_fp8_tensor(_bf16(v))
+    assert sw2 == 1.0
+    ref = torch.from_numpy(syn.bf16_bits_to_f32(_bf16(v))).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(Wq2, ref)
+
+
+# ------------------------------------------------------------------ GEMM
+
+def test_gemm_identity_pins_layout():
+    K = 256
+    W = syn.make_weight(384, K, seed=6)
+    wq = oracle.quantize_w4(W, G=128)
+    X = _bf16(np.eye(K, dtype=np.float32))
+    Y = oracle.w4a16_full(X, wq)
+    assert np.array_equal(Y, oracle.dequant_w4(wq).T)
+
+
+def test_gemm_brute_force_tiny():
+    M, N, K = 3, 8, 128
+    W = syn.make_weight(N, K, seed=8)
+    X = syn.make_act(M, K, seed=8)
+    wq = oracle.quantize_w4(W, G=128)
+    Y = oracle.w4a16_full(X, wq)
+    Xf = syn.bf16_bits_to_f32(X).astype(np.float64)
+    s = oracle.f16_bits_to_f64(wq.s)
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += Xf[m, k] * (s[n, k // 128] * (int(wq.q[n, k]) - int(wq.z[n, k // 128])))
+            assert abs(acc - Y[m, n]) <= 1e-12 * (1 + abs(acc))
+
+
+def test_gemm_matches_library_matmul_and_sampled_path():
+    M, N, K = 5, 256, 512
+    W = syn.make_weight(N, K, seed=10)
+    X = syn.make_act(M, K, seed=10)
+    wq = oracle.quantize_w4(W, G=128)
+    Y = oracle.w4a16_full(X, wq)
+    ref = syn.bf16_bits_to_f32(X).astype(np.float64) @ oracle.dequant_w4(wq).T
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+    ms = np.array([0, 4, 2, 1]), np.array([0, 255, 17, 128])
+    assert np.allclose(oracle.w4a16_at(X, wq, *ms), Y[ms], rtol=1e-12, atol=1e-12)
+
+
+def test_w8a8_reference_matches_library_and_sampled_path():
+    M, N, K = 6, 128, 384
+    X = syn.make_act(M, K, seed=12, token_outlier_frac=0.2)
+    W = syn.make_weight(N, K, seed=12)
+    Xq, sx = oracle.quant_fp8_rows(X)
+    Wq, sw = oracle.quant_fp8_tensor(W)
+    Y = oracle.w8a8_full(Xq, sx, Wq, sw)
+    A = torch.from_numpy(Xq).view(torch.float8_e4m3fn).to(torch.float64)
+    B = torch.from_numpy(Wq).view(torch.float8_e4m3fn).to(torch.float64)
+    ref = (A @ B.T).numpy() * sx.astype(np.float64)[:, None] * sw
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-15)
+    ms, ns = np.array([0, 5, 3]), np.array([7, 0, 127])
+    assert np.allclose(oracle.w8a8_at(Xq, sx, Wq, sw, ms, ns), Y[ms, ns], rtol=1e-12, atol=1e-15)
+
+
+# ------------------------------------------------------------------ roofline arithmetic
+
+def test_roofline_transition_from_page_numbers():
+    ridge = GOLDEN["ridge_h100_sxm_flop_per_byte"]["value"]
+    t = GOLDEN["w4a16_transition_batch_h100"]
+    b = oracle.roofline_transition_batch(ridge, t["bytes_per_weight"])
+    assert b == 73.75 and round(b) == t["value"]
+    d = GOLDEN["decode_bf16_ai_flop_per_byte"]
+    assert 2 * d["batch"] / d["bytes_per_weight"] == d["value"]
