@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized linear layer on GB300.
+
+Default workload (one "step"): the four linear layers of a Llama-3-8B block
+(qkv K=4096 N=6144, o_proj 4096x4096, gate_up K=4096 N=28672, down K=14336
+N=4096) as W4A16 (G=128 asymmetric INT4, FP16 scale, 4-bit zero-point) at
+decode batches M = 1, 4 and 16: 12 GEMM calls per step, weights resident in
+HBM.  The metric is quantized-linear weight GB/s: packed weight bytes
+(codes + scales + zeros) read per step / step time.
+
+Timing: CUDA graphs of one step each over 4 rotating copies of the packed
+weights (452 MB > 3x L2), CUDA events on the launching stream, W warm-up
+steps, K timed steps.  Under torchrun every rank runs the same workload on
+its own GPU (replicas, weak scaling) and the slowest rank's time is used.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+    python bench.py --sweep crossover|prefill|70b   (tables, not the bench line)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS_8B = [("qkv", 4096, 6144), ("o_proj", 4096, 4096), ("gate_up", 4096, 28672), ("down", 14336, 4096)]
+MS_DECODE = (1, 4, 16)
+ROTATE = 4
+WORKLOAD = "llama3-8b W4A16 decode layers (qkv/o/gate_up/down) at M=1,4,16"
+
+
+def w4_weight_bytes(N, K):
+    return N * K // 2 + 2 * N * (K // 128) + N * (K // 128) // 2
+
+
+def w4_alg_bytes(M, N, K):
+    return w4_weight_bytes(N, K) + 2 * M * K + 2 * M * N
+
+
+def w8_alg_bytes(M, N, K):
+    return N * K + M * K + 4 * M + 4 + 2 * M * N
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def make_event(external: bool):
+    import torch
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+    return torch.cuda.Event(enable_timing=True)
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def build_workload(rank: int):
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+    from precision_quantized_linear_gb300 import synthetic as syn
+    from precision_quantized_linear_gb300.layers import W4A16Linear
+
+    layers = []
+    for i, (name, K, N) in enumerate(LAYERS_8B):
+        W = syn.make_weight(N, K, seed=1000 * (rank + 1) + i)
+        lin = W4A16Linear(torch.from_numpy(W.view(np.int16)).cuda())
+        sets = [(lin.codes, lin.scales, lin.zeros)]
+        for r in range(1, ROTATE):
+            sets.append((lin.codes.clone(), lin.scales.clone(), lin.zeros.clone()))
+        layers.append({"name": name, "K": K, "N": N, "lin": lin, "sets": sets})
+    xs, ys = {}, {}
+    for M in MS_DECODE:
+        for K in sorted({K for _, K, _ in LAYERS_8B}):
+            xs[(M, K)] = torch.from_numpy(syn.make_act(M, K, seed=77 + M + K).view(np.int16)).cuda()
+        for L in layers:
+            ys[(M, L["name"])] = torch.empty((M, L["N"]), dtype=torch.int16, device="cuda")
+    ws_bytes = max(q.qlin_workspace_size(q.OP_W4A16_GEMM, M, L["N"], L["K"]) for M in MS_DECODE for L in layers)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    calls = []  # (M, layer) in step order
+    for M in MS_DECODE:
+        for L in layers:
+            calls.append((M, L))
+    return layers, xs, ys, ws, calls
+
+
+def kernel_of(M):
+    import precision_quantized_linear_gb300 as q
+    return "w4a16_gemv" if M <= q.qlin_gemv_max_m(q.OP_W4A16_GEMM) else "w4a16_tc"
+
+
+def run_ours(args):
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+
+    world, rank, local = dist_setup(args)
+    q.build()
+    q.load()
+    layers, xs, ys, ws, calls = build_workload(rank)
+    stream = torch.cuda.Stream()
+    peaks = load_peaks()
+
+    def issue(r, events=None):
+        for i, (M, L) in enumerate(calls):
+            c, s, z = L["sets"][r]
+            if events:
+                events[i][0].record(stream)
+            q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
+                              ws.numel(), stream)
+            if events:
+                events[i][1].record(stream)
+
+    # correctness of the launch configuration before timing
+    with torch.cuda.stream(stream):
+        issue(0)
+    torch.cuda.synchronize()
+    err = q.qlin_get_device_error(stream)
+    if err:
+        raise RuntimeError("device error %d before timing" % err)
+
+    # one CUDA graph per rotation set, with timing events around each kernel
+    ext_ok = make_event(True) is not None
+    graphs, gevents = [], []
+    for r in range(ROTATE):
+        evs = [(make_event(True), make_event(True)) for _ in calls] if ext_ok else None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            issue(r, evs)
+        graphs.append(g)
+        gevents.append(evs)
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        graphs[i % ROTATE].replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = make_event(False), make_event(False)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[(args.warmup + i) % ROTATE].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms_local = e0.elapsed_time(e1) / args.steps
+    step_ms = dist_max(step_ms_local, world)
+
+    weight_bytes = sum(w4_weight_bytes(L["N"], L["K"]) for M, L in calls)
+    alg_bytes = sum(w4_alg_bytes(M, L["N"], L["K"]) for M, L in calls)
+    value = world * weight_bytes / (step_ms * 1e-3) / 1e9
+
+    # per-kernel device time in the timed region (last replay of every graph)
+    per_kernel = {}
+    per_call = []
+    if ext_ok and args.steps >= ROTATE:
+        for r in range(ROTATE):
+            for i, (M, L) in enumerate(calls):
+                a, b = gevents[r][i]
+                per_call.append((M, L, a.elapsed_time(b)))
+    else:  # fallback: a graph of each call alone, timed with events
+        for M, L in calls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(ROTATE):
+                    c, s, z = L["sets"][r]
+                    q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
+                                      ws.numel(), stream)
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = make_event(False), make_event(False)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(5):
+                    g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            per_call.append((M, L, a.elapsed_time(b) / (5 * ROTATE)))
+    for M, L, ms in per_call:
+        k = kernel_of(M)
+        d = per_kernel.setdefault(k, {"ms": 0.0, "launches": 0, "bytes": 0})
+        d["ms"] += ms
+        d["launches"] += 1
+        d["bytes"] += w4_alg_bytes(M, L["N"], L["K"])
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
+    dk = per_kernel[dom]
+    achieved = dk["bytes"] / (dk["ms"] * 1e-3) / 1e9
+    per_m = {}
+    for M, L, ms in per_call:
+        e = per_m.setdefault(M, [0.0, 0])
+        e[0] += ms
+        e[1] += w4_weight_bytes(L["N"], L["K"])
+    # t and b are both summed over the same launches
+    per_m_gbs = {str(M): round(b / (t * 1e-3) / 1e9, 1) for M, (t, b) in per_m.items()}
+
+    e2e = run_e2e(args, layers, xs, ys, ws, calls, stream, world)
+
+    out = {
+        "metric": "quantized-linear weight GB/s (decode) & TFLOPS (prefill) vs batch M, % of roofline",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4 weights x bf16 activations, fp32 accumulate", "data": "synthetic (seeded N(0,0.02) weights with 1% x20 outlier channels, N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "layers_KxN": [[K, N] for _, K, N in LAYERS_8B], "M": list(MS_DECODE),
+                   "G": 128, "calls_per_step": len(calls), "weight_bytes_per_step": weight_bytes,
+                   "alg_bytes_per_step": alg_bytes, "l2": "4 rotating weight copies (%.0f MB > 3x L2)" %
+                   (ROTATE * weight_bytes / 1e6 / len(MS_DECODE)), "timing": "CUDA graph per step, CUDA events"},
+        "per_M_weight_gbs": per_m_gbs,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": peaks["source"], "launches_timed": dk["launches"],
+                     "share_of_step": round(dk["ms"] / sum(v["ms"] for v in per_kernel.values()), 3)},
+        "kernels": {k: {"ms_per_launch": round(v["ms"] / v["launches"], 5), "launches": v["launches"],
+                        "GBps": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)} for k, v in per_kernel.items()},
+        "gpu_launches": len(calls) * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, layers, xs, ys, ws, calls, stream, world):
+    """Same metric through the public API, host buffers in and out every step."""
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+    hx = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu()) for k, v in xs.items()}
+    hy = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in ys.items()}
+    h2d = sum(t.numel() * 2 for t in hx.values())
+    d2h = sum(t.numel() * 2 for t in hy.values())
+
+    def step(r):
+        with torch.cuda.stream(stream):
+            for k in hx:
+                xs[k].copy_(hx[k], non_blocking=True)
+            for M, L in calls:
+                c, s, z = L["sets"][r]
+                q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
+                                  ws.numel(), stream)
+            for k in hy:
+                hy[k].copy_(ys[k], non_blocking=True)
+
+    for i in range(max(1, args.warmup)):
+        step(i % ROTATE)
+    torch.cuda.synchronize()
+    barrier(world)
+    n = max(1, args.steps)
+    e0, e1 = make_event(False), make_event(False)
+    e0.record(stream)
+    for i in range(n):
+        step(i % ROTATE)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_max(e0.elapsed_time(e1) / n, world)
+    wbytes = sum(w4_weight_bytes(L["N"], L["K"]) for M, L in calls)
+    return {"value": round(world * wbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "how": "per step: pinned host X -> device, 12 qlin_w4a16_gemm calls (no graph), Y -> pinned host"}
+
+
+# ---------------------------------------------------------------------------- oracle (CPU) arms
+
+def _oracle_sample():
+    import oracle
+    from precision_quantized_linear_gb300 import synthetic as syn
+    name, K, N = LAYERS_8B[1]           # o_proj, 4096 x 4096
+    W = syn.make_weight(N, K, seed=1001)
+    wq = oracle.quantize_w4(W)
+    xs = {M: syn.make_act(M, K, seed=77 + M + K) for M in MS_DECODE}
+    return oracle, wq, xs, N, K
+
+
+def cpu_baseline(seconds: float = 10.0):
+    """The oracle as it stands, on the host cores, over a bounded sample."""
+    oracle, wq, xs, N, K = _oracle_sample()
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        for M in MS_DECODE:
+            oracle.w4a16_full(xs[M], wq)
+            calls += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(calls * w4_weight_bytes(N, K) / dt / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "oracle W4A16 GEMM (dequantise + fp64 GEMM) on the o_proj layer K=N=4096 at M=1,4,16, "
+                      "%d calls in %.1f s" % (calls, dt)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle, wq, xs, N, K = _oracle_sample()
+    for _ in range(args.warmup):
+        oracle.w4a16_full(xs[1], wq)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for M in MS_DECODE:
+            oracle.w4a16_full(xs[M], wq)
+    dt = time.perf_counter() - t0
+    value = args.steps * len(MS_DECODE) * w4_weight_bytes(N, K) / dt / 1e9
+    ms = dt * 1e3 / args.steps
+    sample = "each step: oracle W4A16 GEMM on o_proj K=N=4096 at M=1,4,16 (a bounded sample of the 8B decode set)"
+    out = {"impl": "reference", "metric": "quantized-linear weight GB/s (decode) & TFLOPS (prefill) vs batch M, % of roofline",
+           "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64", "data": "synthetic", "config": {"workload": WORKLOAD},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sweep", default=None, choices=["crossover", "prefill", "70b", "decode"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.sweep:
+        from precision_quantized_linear_gb300 import sweep
+        sweep.run(args.sweep, args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/*
+ * qlin -- quantized linear layers Y = X . deq(W)^T for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libqlin.so.  Two variants of the linear layer of LLM serving:
+ *
+ *  W4A16  INT4 weights, q = clamp(round(w/s) + z, 0, 15), one FP16 scale s
+ *         and one 4-bit zero-point z per group of G = 128 weights along K
+ *         (4.125 bits/weight for codes + scales); BF16 activations; the
+ *         dequantisation x_hat = s (q - z) happens inside the GEMM kernel.
+ *  W8A8   FP8 E4M3 weights with one FP32 scale for the whole tensor and E4M3
+ *         activations with one FP32 scale per token (row), both "current"
+ *         scales amax / 448; FP32 accumulation, BF16 output.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [LP] "Low-precision LLM inference: FP8/INT8/INT4/FP4 kernels and
+ *        calibration" (blog.ruahverce.com): S1 precision manifest, S2 uniform
+ *        integer quantisation, S3 symmetric/asymmetric, S4 scale granularity,
+ *        S5 effective bits, S7 FP8 formats, S8 FP8 scale recipes, S11 W4A16
+ *        pipeline, S22 accumulator precision, S23 fused kernels, S24 kernel
+ *        eligibility checklist, S25 padding, S28 CUDA graphs and dynamic scale,
+ *        S31 artifact manifest (fail-closed fallback policy).
+ *  [TP] "Quantization throughput by batch size: why W4A16 is overtaken by
+ *        W8A8" (hrletsgo.me): small batches are bound by weight bytes, large
+ *        batches by tensor-core throughput.
+ *
+ * Conventions for every call
+ *  - X is [M][K] row-major, W is [N][K] row-major (the nn.Linear layout),
+ *    Y is [M][N] row-major.  BF16/FP16 buffers hold raw 16-bit patterns.
+ *  - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned;
+ *    `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Every call is asynchronous on `stream`, allocates nothing, never reads a
+ *    device value on the host, and can be captured in a CUDA graph ([LP] S28).
+ *  - Arguments are validated before anything is launched; a call that returns
+ *    an error launched nothing and wrote nothing.  There is no fallback path,
+ *    no CPU path and no silent padding ([LP] S24, S25, S31 "fail-closed").
+ *  - Errors found by a kernel while it runs (a scale that overflows FP16, a
+ *    pipeline wait that gave up) are recorded in a per-device error word read
+ *    by qlin_get_device_error().
+ *  - M = 0 is a valid empty call: it returns QLIN_OK and launches nothing.
+ *
+ * Eligibility ([LP] S24): device sm_103 (compute capability 10.3); G = 128;
+ * N % 128 == 0; K % 128 == 0; 1 <= N, K; 0 <= M <= 2^24.
+ */
+#ifndef QLIN_H
+#define QLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QLIN_OK = 0,
+  QLIN_ERR_INVALID_VALUE = 1,      /* null pointer, bad flag, bad value found on device */
+  QLIN_ERR_UNSUPPORTED_SHAPE = 2,  /* M/N/K/G outside the eligibility rules above */
+  QLIN_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+  QLIN_ERR_WORKSPACE_TOO_SMALL = 4,
+  QLIN_ERR_ARCH = 5,               /* current device is not compute capability 10.3 */
+  QLIN_ERR_CUDA = 6,               /* a CUDA runtime call or a launch failed */
+  QLIN_ERR_TIMEOUT = 7             /* a kernel's bounded pipeline wait gave up */
+} qlin_status_t;
+
+/* Version of the packed INT4 tile layout written by qlin_pack_w4 ([LP] S31
+ * "kernel_pack_format").  A consumer must reject any other version. */
+#define QLIN_PACK_FORMAT_VERSION 1
+
+/* Operation ids for qlin_workspace_size. */
+#define QLIN_OP_W4A16_GEMM 1
+#define QLIN_OP_W8A8_GEMM 2
+#define QLIN_OP_QUANT_W_FP8 3
+
+/* Kernel selection for the *_ex GEMM calls (measurement and ablation). */
+#define QLIN_PATH_AUTO 0   /* choose by M (the default of the plain calls) */
+#define QLIN_PATH_GEMV 1   /* CUDA-core split-K GEMV, small M              */
+#define QLIN_PATH_TC 2     /* TMA + tcgen05 tensor-core kernel             */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qlin_status_string(int status);
+
+/* QLIN_PACK_FORMAT_VERSION of the library that is loaded. */
+int qlin_pack_format_version(void);
+
+/* Byte sizes of the three packed-weight buffers for an [N][K] weight.
+ * codes = N*K/2, scales = 2*N*K/G, zeros = N*K/(2G) ([LP] S5: codes + scales
+ * give exactly 4 + 16/G bits per weight; the zeros add 4/G). */
+int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros);
+
+/* Scratch bytes a call of `op` needs for these sizes (0 if none).  The
+ * workspace must be zero-filled before its first use with this library and
+ * is left zero-filled by every call that completes; calls that share one
+ * workspace must not overlap in time (use one per stream). */
+int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/*
+ * Quantise and pack BF16 weights W[N][K] ([LP] S2-S5, run once at load).
+ *  Per row n and group g (columns gG .. gG+G-1), in IEEE binary32:
+ *   asymmetric (symmetric = 0): lo = min(min w, 0), hi = max(max w, 0),
+ *     s = fp16(( hi - lo) / 15), z = clamp(rint(-lo / s), 0, 15),
+ *     q = clamp(rint(w / s) + z, 0, 15);
+ *   symmetric (symmetric = 1): s = fp16(max|w| / 7), q = clamp(rint(w/s),-8,7)
+ *     stored offset-binary as q + 8 with stored zero-point 8 (logical z = 0).
+ *   rint rounds half to even; a group whose scale rounds to 0 stores s = 1,
+ *   z = 0 (symmetric: 8).  A scale that overflows FP16 sets the device error
+ *   word to QLIN_ERR_INVALID_VALUE.
+ *  Outputs, in tile layout version 1 (tiles of 128 rows x 64 columns):
+ *   codes  (N*K/2 bytes): tile (n/128, k/64) is 4096 bytes at
+ *          ((n/128)*(K/64) + k/64) * 4096; in it, half h = (k%64)/32 of row
+ *          r = n%128 is the 16 bytes at h*2048 + r*16: four little-endian
+ *          32-bit words, word j = (k%32)/8 holding columns 8j..8j+7 of the
+ *          half with column e = k%8 in nibble position p = e/2 (e even) or
+ *          4 + e/2 (e odd), i.e. bits 4p..4p+3.
+ *   scales (2*N*K/128 bytes): FP16 of (n, g) at element
+ *          ((n/128)*(K/128) + g) * 128 + n%128.
+ *   zeros  (N*K/256 bytes): nibble of (n, g) in byte
+ *          ((n/128)*(K/128) + g) * 64 + (n%128)/2, low nibble for even n.
+ *  Requires G == 128, N % 128 == 0, K % 128 == 0.
+ */
+int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes,
+                 void* scales_f16, void* zeros_u4, void* stream);
+
+/*
+ * W4A16 linear layer ([LP] S11, S23): Y = bf16( sum_k X[m][k] s (q - z) ),
+ * accumulated in FP32 ([LP] S22), from the packed buffers of qlin_pack_w4.
+ * Kernel choice by M ([LP] S24 "different kernels for small batch and
+ * large prefill"): a split-K CUDA-core GEMV for small M, a TMA + tcgen05
+ * BF16 tensor-core kernel (weights dequantised to BF16 in shared memory)
+ * otherwise.  Split-K partial sums are reduced in a fixed order, so results
+ * are deterministic.  workspace: qlin_workspace_size(QLIN_OP_W4A16_GEMM, ...)
+ * bytes (may be NULL when that is 0).
+ */
+int qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                    void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
+                    void* stream);
+
+/* Same, with the kernel path forced (QLIN_PATH_*). */
+int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                       void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
+                       int path, void* stream);
+
+/*
+ * Per-token FP8 activation quantisation ([LP] S4 per-token, S8 current
+ * scaling), one fused kernel: for each row m, amax_m = max_k |X[m][k]|,
+ * sx[m] = amax_m / 448 (1 if amax_m = 0), Xq[m][k] = e4m3_rn_satfinite(
+ * X[m][k] / sx[m]) with an IEEE binary32 division.  Outputs: Xq [M][K] E4M3
+ * bytes, sx [M] FP32.  The scale never leaves the device ([LP] S28).
+ */
+int qlin_quant_act_fp8(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream);
+
+/*
+ * Per-tensor FP8 weight quantisation ([LP] S4 per-tensor, S8), run once at
+ * load: sw = amax(W)/448 (1 if 0), Wq = e4m3_rn_satfinite(W / sw).
+ * Outputs Wq [N][K] E4M3 bytes and *sw (one FP32, device memory).
+ * workspace: qlin_workspace_size(QLIN_OP_QUANT_W_FP8, ...) bytes (holds the
+ * grid-wide amax).
+ */
+int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* workspace,
+                     size_t ws_bytes, void* stream);
+
+/*
+ * W8A8 FP8 linear layer ([LP] S8, S9, S22): Y[m][n] = bf16( acc[m][n] *
+ * sx[m] * sw ) with acc = sum_k e4m3(Xq[m][k]) e4m3(Wq[n][k]) in FP32.
+ * Kernel choice by M as for W4A16 (CUDA-core GEMV or tcgen05 kind::f8f6f4).
+ * workspace: qlin_workspace_size(QLIN_OP_W8A8_GEMM, ...) bytes.
+ */
+int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                       void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                       void* stream);
+
+int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                          void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                          int path, void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word: QLIN_OK, or the first error a kernel recorded since the last call. */
+int qlin_get_device_error(void* stream);
+
+/* The M at or below which the AUTO path of each GEMM uses the GEMV kernel. */
+int qlin_gemv_max_m(int op);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLIN_H */

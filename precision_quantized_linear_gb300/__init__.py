@@ -1,0 +1,176 @@
+"""qlin: GB300-native quantized linear layers (W4A16 INT4 and W8A8 FP8-E4M3).
+
+Thin ctypes binding over ``libqlin.so`` (the C ABI declared in
+``include/qlin.h``).  The ``qlin_*`` functions take the same arguments as the
+C calls, with torch CUDA tensors in place of device pointers, and raise
+``QlinError`` on a non-zero status; every step of the computation runs in the
+library's CUDA kernels.  PyTorch is only used for device memory and streams.
+
+If the shared library is missing the first call raises: there is no other
+implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build_mod
+
+__all__ = [
+    "QlinError", "load", "build",
+    "qlin_status_string", "qlin_pack_format_version", "qlin_w4_packed_sizes", "qlin_workspace_size",
+    "qlin_pack_w4", "qlin_w4a16_gemm", "qlin_w4a16_gemm_ex", "qlin_quant_act_fp8", "qlin_quant_w_fp8",
+    "qlin_w8a8_fp8_gemm", "qlin_w8a8_fp8_gemm_ex", "qlin_get_device_error", "qlin_gemv_max_m",
+    "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "PATH_AUTO", "PATH_GEMV", "PATH_TC",
+    "PACK_FORMAT_VERSION",
+]
+
+OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8 = 1, 2, 3
+PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+PACK_FORMAT_VERSION = 1
+
+_lock = threading.Lock()
+_lib = None
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_int = ctypes.c_int
+
+# name -> argtypes (restype is int for all but qlin_status_string)
+_SIGS = {
+    "qlin_status_string": [_int],
+    "qlin_pack_format_version": [],
+    "qlin_gemv_max_m": [_int],
+    "qlin_w4_packed_sizes": [_i64, _i64, _int, ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
+    "qlin_workspace_size": [_int, _i64, _i64, _i64, ctypes.POINTER(_sz)],
+    "qlin_pack_w4": [_p, _i64, _i64, _int, _int, _p, _p, _p, _p],
+    "qlin_w4a16_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _sz, _p],
+    "qlin_w4a16_gemm_ex": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _sz, _int, _p],
+    "qlin_quant_act_fp8": [_p, _i64, _i64, _p, _p, _p],
+    "qlin_quant_w_fp8": [_p, _i64, _i64, _p, _p, _p, _sz, _p],
+    "qlin_w8a8_fp8_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
+    "qlin_w8a8_fp8_gemm_ex": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _int, _p],
+    "qlin_get_device_error": [_p],
+}
+
+
+class QlinError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__("%s failed: %s (%d)" % (where, qlin_status_string(status), status))
+
+
+def build(force: bool = False) -> str:
+    return _build_mod.build(force=force)
+
+
+def lib_path() -> str:
+    return _build_mod.LIB
+
+
+def load():
+    """Load libqlin.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build_mod.LIB
+        if not os.path.exists(path):
+            raise RuntimeError("libqlin.so is not built (%s); run precision_quantized_linear_gb300.build()" % path)
+        lib = ctypes.CDLL(path)
+        for name, args in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_char_p if name == "qlin_status_string" else _int
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, where: str) -> int:
+    if st != 0:
+        raise QlinError(st, where)
+    return st
+
+
+def qlin_status_string(status: int) -> str:
+    return load().qlin_status_string(int(status)).decode()
+
+
+def qlin_pack_format_version() -> int:
+    return load().qlin_pack_format_version()
+
+
+def qlin_gemv_max_m(op: int) -> int:
+    return load().qlin_gemv_max_m(op)
+
+
+def qlin_w4_packed_sizes(N: int, K: int, G: int = 128):
+    a, b, c = _sz(), _sz(), _sz()
+    _check(load().qlin_w4_packed_sizes(N, K, G, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+           "qlin_w4_packed_sizes")
+    return a.value, b.value, c.value
+
+
+def qlin_workspace_size(op: int, M: int, N: int, K: int) -> int:
+    b = _sz()
+    _check(load().qlin_workspace_size(op, M, N, K, ctypes.byref(b)), "qlin_workspace_size")
+    return b.value
+
+
+def qlin_pack_w4(W, N, K, G, symmetric, codes, scales, zeros, stream=None):
+    return _check(load().qlin_pack_w4(_ptr(W), N, K, G, int(symmetric), _ptr(codes), _ptr(scales), _ptr(zeros),
+                                      _stream(stream)), "qlin_pack_w4")
+
+
+def qlin_w4a16_gemm(X, codes, scales, zeros, Y, M, N, K, G, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_w4a16_gemm(_ptr(X), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(Y), M, N, K, G,
+                                         _ptr(workspace), ws_bytes, _stream(stream)), "qlin_w4a16_gemm")
+
+
+def qlin_w4a16_gemm_ex(X, codes, scales, zeros, Y, M, N, K, G, workspace, ws_bytes, path, stream=None):
+    return _check(load().qlin_w4a16_gemm_ex(_ptr(X), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(Y), M, N, K, G,
+                                            _ptr(workspace), ws_bytes, path, _stream(stream)), "qlin_w4a16_gemm_ex")
+
+
+def qlin_quant_act_fp8(X, M, K, Xq, sx, stream=None):
+    return _check(load().qlin_quant_act_fp8(_ptr(X), M, K, _ptr(Xq), _ptr(sx), _stream(stream)),
+                  "qlin_quant_act_fp8")
+
+
+def qlin_quant_w_fp8(W, N, K, Wq, sw, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_quant_w_fp8(_ptr(W), N, K, _ptr(Wq), _ptr(sw), _ptr(workspace), ws_bytes,
+                                          _stream(stream)), "qlin_quant_w_fp8")
+
+
+def qlin_w8a8_fp8_gemm(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_w8a8_fp8_gemm(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
+                                            _ptr(workspace), ws_bytes, _stream(stream)), "qlin_w8a8_fp8_gemm")
+
+
+def qlin_w8a8_fp8_gemm_ex(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, path, stream=None):
+    return _check(load().qlin_w8a8_fp8_gemm_ex(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
+                                               _ptr(workspace), ws_bytes, path, _stream(stream)),
+                  "qlin_w8a8_fp8_gemm_ex")
+
+
+def qlin_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    return load().qlin_get_device_error(_stream(stream))

@@ -1,0 +1,293 @@
+// Host side of libqlin: argument validation ([LP] S24 eligibility checklist,
+// S31 fail-closed), kernel choice by M ([LP] S24, [TP] small vs large batch),
+// tensor-map encoding and the per-device error word.  Nothing here allocates
+// per call, synchronises (except qlin_get_device_error) or reads device data.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "qlin_internal.cuh"
+
+namespace qlin {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxM = int64_t(1) << 24;
+
+// Error word of each device (first error wins; cleared by qlin_get_device_error).
+__device__ int g_error_word;
+
+struct DeviceState {
+  bool ready = false;
+  int status = QLIN_OK;
+  int num_sms = 0;
+  int* err = nullptr;  // device address of g_error_word on this device
+};
+
+static DeviceState g_dev[kMaxDevices];
+static std::mutex g_mu;
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QLIN_ERR_CUDA;
+  DeviceState& d = g_dev[dev];
+  if (d.ready) {
+    *out = &d;
+    return d.status;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      d.status = QLIN_ERR_CUDA;
+    } else if (major != 10 || minor != 3) {
+      d.status = QLIN_ERR_ARCH;  // the library holds sm_103a code only
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_error_word) != cudaSuccess) {
+      d.status = QLIN_ERR_CUDA;
+    } else {
+      if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+          d.status = QLIN_ERR_CUDA;
+        } else {
+          g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+      }
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return d.status;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  (void)elem_bytes;
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// M at or below which the GEMV kernels are chosen (measured crossover).
+static int g_gemv_max_m_w4 = 4;
+static int g_gemv_max_m_w8 = 4;
+
+}  // namespace qlin
+
+using namespace qlin;
+
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_shape(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || M > kMaxM || N <= 0 || K <= 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (N % kTileN != 0 || K % kGroup != 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  return QLIN_OK;
+}
+
+static int launch_status(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA; }
+
+extern "C" {
+
+const char* qlin_status_string(int status) {
+  switch (status) {
+    case QLIN_OK: return "QLIN_OK";
+    case QLIN_ERR_INVALID_VALUE: return "QLIN_ERR_INVALID_VALUE";
+    case QLIN_ERR_UNSUPPORTED_SHAPE: return "QLIN_ERR_UNSUPPORTED_SHAPE";
+    case QLIN_ERR_MISALIGNED: return "QLIN_ERR_MISALIGNED";
+    case QLIN_ERR_WORKSPACE_TOO_SMALL: return "QLIN_ERR_WORKSPACE_TOO_SMALL";
+    case QLIN_ERR_ARCH: return "QLIN_ERR_ARCH";
+    case QLIN_ERR_CUDA: return "QLIN_ERR_CUDA";
+    case QLIN_ERR_TIMEOUT: return "QLIN_ERR_TIMEOUT";
+    default: return "QLIN_ERR_UNKNOWN";
+  }
+}
+
+int qlin_pack_format_version(void) { return QLIN_PACK_FORMAT_VERSION; }
+
+int qlin_gemv_max_m(int op) { return op == QLIN_OP_W8A8_GEMM ? g_gemv_max_m_w8 : g_gemv_max_m_w4; }
+
+int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros) {
+  if (!codes || !scales || !zeros) return QLIN_ERR_INVALID_VALUE;
+  if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  int st = check_shape(0, N, K);
+  if (st != QLIN_OK) return st;
+  *codes = static_cast<size_t>(N * K / 2);
+  *scales = static_cast<size_t>(N * (K / G) * 2);
+  *zeros = static_cast<size_t>(N * (K / G) / 2);
+  return QLIN_OK;
+}
+
+static size_t ws_w4(int64_t M, int64_t N, int64_t K, int sms) {
+  const size_t a = plan_w4a16_gemv(M, N, K, sms).ws_bytes;
+  const size_t b = plan_w4a16_tc(M, N, K, sms).split.ws_bytes;
+  return a > b ? a : b;
+}
+static size_t ws_w8(int64_t M, int64_t N, int64_t K, int sms) {
+  const size_t a = plan_w8a8_gemv(M, N, K, sms).ws_bytes;
+  const size_t b = plan_w8a8_tc(M, N, K, sms).split.ws_bytes;
+  return a > b ? a : b;
+}
+
+int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes) {
+  if (!bytes) return QLIN_ERR_INVALID_VALUE;
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  switch (op) {
+    case QLIN_OP_W4A16_GEMM: *bytes = M == 0 ? 0 : ws_w4(M, N, K, d->num_sms); return QLIN_OK;
+    case QLIN_OP_W8A8_GEMM: *bytes = M == 0 ? 0 : ws_w8(M, N, K, d->num_sms); return QLIN_OK;
+    case QLIN_OP_QUANT_W_FP8: *bytes = 256; return QLIN_OK;
+    default: return QLIN_ERR_INVALID_VALUE;
+  }
+}
+
+int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes, void* scales_f16,
+                 void* zeros_u4, void* stream) {
+  if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  int st = check_shape(0, N, K);
+  if (st != QLIN_OK) return st;
+  if (symmetric != 0 && symmetric != 1) return QLIN_ERR_INVALID_VALUE;
+  if (!W_bf16 || !codes || !scales_f16 || !zeros_u4) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(W_bf16) || !aligned16(codes) || !aligned16(scales_f16) || !aligned16(zeros_u4))
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_pack_w4(static_cast<const uint16_t*>(W_bf16), N, K, symmetric,
+                                      static_cast<uint8_t*>(codes), static_cast<uint16_t*>(scales_f16),
+                                      static_cast<uint8_t*>(zeros_u4), d->err, d->num_sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                       void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
+                       int path, void* stream) {
+  if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  int st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;
+  if (M == 0) return QLIN_OK;
+  if (!X_bf16 || !codes || !scales_f16 || !zeros_u4 || !Y_bf16) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(X_bf16) || !aligned16(codes) || !aligned16(scales_f16) || !aligned16(zeros_u4) ||
+      !aligned16(Y_bf16) || (workspace && !aligned16(workspace)))
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  if (path == QLIN_PATH_AUTO) path = M <= g_gemv_max_m_w4 ? QLIN_PATH_GEMV : QLIN_PATH_TC;
+  const auto* X = static_cast<const uint16_t*>(X_bf16);
+  const auto* c = static_cast<const uint8_t*>(codes);
+  const auto* s = static_cast<const uint16_t*>(scales_f16);
+  const auto* z = static_cast<const uint8_t*>(zeros_u4);
+  auto* Y = static_cast<uint16_t*>(Y_bf16);
+  auto cs = static_cast<cudaStream_t>(stream);
+  if (path == QLIN_PATH_GEMV) {
+    const SplitPlan p = plan_w4a16_gemv(M, N, K, d->num_sms);
+    if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+    return launch_status(launch_w4a16_gemv(X, c, s, z, Y, M, N, K, p, workspace, cs));
+  }
+  const TcPlan p = plan_w4a16_tc(M, N, K, d->num_sms);
+  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, p, workspace, d->err, cs));
+}
+
+int qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                    void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  return qlin_w4a16_gemm_ex(X_bf16, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, workspace, ws_bytes,
+                            QLIN_PATH_AUTO, stream);
+}
+
+int qlin_quant_act_fp8(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream) {
+  if (M < 0 || M > kMaxM || K <= 0 || K % kGroup != 0 || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return QLIN_OK;
+  if (!X_bf16 || !Xq_e4m3 || !sx) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(X_bf16) || !aligned16(Xq_e4m3) || !aligned16(sx)) return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_quant_act_fp8(static_cast<const uint16_t*>(X_bf16), M, K,
+                                            static_cast<uint8_t*>(Xq_e4m3), sx, static_cast<cudaStream_t>(stream)));
+}
+
+int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  int st = check_shape(0, N, K);
+  if (st != QLIN_OK) return st;
+  if (!W_bf16 || !Wq_e4m3 || !sw || !workspace) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(W_bf16) || !aligned16(Wq_e4m3) || !aligned16(sw) || !aligned16(workspace))
+    return QLIN_ERR_MISALIGNED;
+  if (ws_bytes < 256) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_quant_w_fp8(static_cast<const uint16_t*>(W_bf16), N, K, static_cast<uint8_t*>(Wq_e4m3),
+                                          sw, static_cast<uint32_t*>(workspace), d->num_sms,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
+                          int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, int path,
+                          void* stream) {
+  int st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;
+  if (M == 0) return QLIN_OK;
+  if (!Xq_e4m3 || !sx || !Wq_e4m3 || !sw || !Y_bf16) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(Xq_e4m3) || !aligned16(Wq_e4m3) || !aligned16(Y_bf16) || (workspace && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(sx) & 3u) || (reinterpret_cast<uintptr_t>(sw) & 3u))
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  if (path == QLIN_PATH_AUTO) path = M <= g_gemv_max_m_w8 ? QLIN_PATH_GEMV : QLIN_PATH_TC;
+  const auto* xq = static_cast<const uint8_t*>(Xq_e4m3);
+  const auto* wq = static_cast<const uint8_t*>(Wq_e4m3);
+  auto* Y = static_cast<uint16_t*>(Y_bf16);
+  auto cs = static_cast<cudaStream_t>(stream);
+  if (path == QLIN_PATH_GEMV) {
+    const SplitPlan p = plan_w8a8_gemv(M, N, K, d->num_sms);
+    if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+    return launch_status(launch_w8a8_gemv(xq, sx, wq, sw, Y, M, N, K, p, workspace, cs));
+  }
+  const TcPlan p = plan_w8a8_tc(M, N, K, d->num_sms);
+  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_w8a8_tc(xq, sx, wq, sw, Y, M, N, K, p, workspace, d->err, cs));
+}
+
+int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
+                       int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, void* stream) {
+  return qlin_w8a8_fp8_gemm_ex(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, workspace, ws_bytes, QLIN_PATH_AUTO,
+                               stream);
+}
+
+int qlin_get_device_error(void* stream) {
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  auto cs = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return QLIN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QLIN_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QLIN_ERR_CUDA;
+  return word;
+}
+
+}  // extern "C"

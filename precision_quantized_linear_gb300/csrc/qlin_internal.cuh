@@ -1,0 +1,86 @@
+// Declarations shared by the translation units of libqlin (host side).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/qlin.h"
+
+namespace qlin {
+
+constexpr int kTileN = 128;   // weight rows per tile
+constexpr int kTileK = 64;    // columns per tile (one 128-byte BF16 row)
+constexpr int kGroup = 128;   // quantisation group along K
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Device error word: first error wins.
+__device__ __forceinline__ void set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Split-K workspace: [counters: one uint32 per output tile, padded to 256 B]
+// [partials: splits x M x N float].
+struct SplitPlan {
+  int splits = 1;        // K ranges per output tile
+  int kb_per_split = 0;  // 64-column blocks per range (last range may be shorter)
+  int64_t tiles = 0;     // output tiles (m blocks x n tiles)
+  size_t ws_bytes = 0;   // workspace needed (0 when splits == 1)
+};
+
+// cudaFuncSetAttribute once per (kernel, device), so that no such call is made
+// while a stream is being captured into a CUDA graph.
+template <typename F>
+inline cudaError_t set_smem_once(F* kernel, int bytes) {
+  static unsigned long long done = 0;  // bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
+inline size_t counters_bytes(int64_t tiles) { return static_cast<size_t>((tiles * 4 + 255) / 256 * 256); }
+
+// ---- launchers (return cudaError_t of the launch)
+cudaError_t launch_pack_w4(const uint16_t* W, int64_t N, int64_t K, int symmetric, uint8_t* codes,
+                           uint16_t* scales, uint8_t* zeros, int* err, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_act_fp8(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx,
+                                 cudaStream_t st);
+cudaError_t launch_quant_w_fp8(const uint16_t* W, int64_t N, int64_t K, uint8_t* Wq, float* sw, uint32_t* amax_ws,
+                               int num_sms, cudaStream_t st);
+
+SplitPlan plan_w4a16_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
+                              uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws,
+                              cudaStream_t st);
+
+SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
+                             int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st);
+
+// tcgen05 kernels: swap-AB (weights are the 128-row MMA operand, tokens the N side)
+struct TcPlan {
+  int bn = 16;           // tokens per tile (MMA N)
+  int64_t mblocks = 1;   // token blocks
+  SplitPlan split;
+};
+TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms);
+TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
+
+cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
+                            uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
+                            cudaStream_t st);
+cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
+                           int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
+                           cudaStream_t st);
+
+// Tensor-map encoding through the driver entry point (no libcuda link).
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+}  // namespace qlin

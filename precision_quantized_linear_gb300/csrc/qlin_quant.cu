@@ -1,0 +1,229 @@
+// Load-time and per-call quantisation kernels:
+//  * pack_w4        -- per-group INT4 quantiser + tile-layout packing
+//  * quant_act_fp8  -- fused per-token amax + E4M3 cast
+//  * quant_w_fp8    -- per-tensor amax (grid reduction) + E4M3 cast
+// Rounding follows IEEE binary32 throughout (no fast-math): divisions are
+// __fdiv_rn, round() is rintf (half to even), FP16 is __float2half_rn and
+// E4M3 is cvt.rn.satfinite.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qlin_internal.cuh"
+
+namespace qlin {
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Nibble position of column e (0..7) inside its 32-bit word: even columns in
+// positions 0..3, odd columns in 4..7, so that one AND with 0x000F000F pulls
+// out two adjacent columns as the two halves of a 32-bit register.
+__device__ __forceinline__ int nibble_pos(int e) { return (e & 1) ? 4 + (e >> 1) : (e >> 1); }
+
+// [LP] S2-S4: one warp per (pair of rows, group of 128 columns).  Lane l owns
+// columns 4l..4l+3 of the group; the group's min/max are warp reductions.
+__global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K,
+                                                      int symmetric, uint8_t* __restrict__ codes,
+                                                      uint16_t* __restrict__ scales, uint8_t* __restrict__ zeros,
+                                                      int* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t ng = K / kGroup;
+  const int64_t total = (N / 2) * ng;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; item < total;
+       item += nwarps) {
+    const int64_t pair = item / ng, g = item % ng;
+    uint32_t zbyte = 0;
+    const int64_t nb = (pair * 2) / kTileN;
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      const int64_t n = pair * 2 + sub;
+      const int r = static_cast<int>(n % kTileN);
+      const uint2 raw = *reinterpret_cast<const uint2*>(W + n * K + g * kGroup + 4 * lane);
+      const float v[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+      float lo = 0.0f, hi = 0.0f, amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        lo = fminf(lo, v[i]);
+        hi = fmaxf(hi, v[i]);
+        amax = fmaxf(amax, fabsf(v[i]));
+      }
+      lo = warp_min(lo);
+      hi = warp_max(hi);
+      amax = warp_max(amax);
+      const float s32 = symmetric ? __fdiv_rn(amax, 7.0f) : __fdiv_rn(hi - lo, 15.0f);
+      __half s16 = __float2half_rn(s32);
+      float sc = __half2float(s16);
+      int zp;
+      if (sc == 0.0f) {  // degenerate group: s = 1, logical zero-point 0
+        s16 = __float2half_rn(1.0f);
+        sc = 1.0f;
+        zp = symmetric ? 8 : 0;
+      } else if (symmetric) {
+        zp = 8;
+      } else {
+        float zf = rintf(__fdiv_rn(-lo, sc));
+        zf = fminf(fmaxf(zf, 0.0f), 15.0f);
+        zp = static_cast<int>(zf);
+      }
+      if (isinf(sc) && lane == 0) set_error(err, QLIN_ERR_INVALID_VALUE);
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float rq = rintf(__fdiv_rn(v[i], sc));
+        int c;
+        if (symmetric) {
+          rq = fminf(fmaxf(rq, -8.0f), 7.0f);
+          c = static_cast<int>(rq) + 8;
+        } else {
+          rq = fminf(fmaxf(rq + static_cast<float>(zp), 0.0f), 15.0f);
+          c = static_cast<int>(rq);
+        }
+        const int e = (lane & 1) * 4 + i;  // column within the 8-column word
+        word |= static_cast<uint32_t>(c) << (4 * nibble_pos(e));
+      }
+      word |= __shfl_xor_sync(0xffffffffu, word, 1);
+      if ((lane & 1) == 0) {
+        const int64_t k = g * kGroup + 4 * lane;  // first column of the word
+        const int64_t kb = k / kTileK;
+        const int h = static_cast<int>((k % kTileK) / 32);
+        const int j = static_cast<int>((k % 32) / 8);
+        *reinterpret_cast<uint32_t*>(codes + (nb * (K / kTileK) + kb) * 4096 + h * 2048 + r * 16 + j * 4) = word;
+      }
+      if (lane == 0) {
+        scales[(nb * ng + g) * kTileN + r] = __half_as_ushort(s16);
+        zbyte |= static_cast<uint32_t>(zp) << (4 * sub);
+      }
+    }
+    if (lane == 0) zeros[(nb * ng + g) * (kTileN / 2) + ((pair * 2) % kTileN) / 2] = static_cast<uint8_t>(zbyte);
+  }
+}
+
+cudaError_t launch_pack_w4(const uint16_t* W, int64_t N, int64_t K, int symmetric, uint8_t* codes, uint16_t* scales,
+                           uint8_t* zeros, int* err, int num_sms, cudaStream_t st) {
+  const int64_t items = (N / 2) * (K / kGroup);
+  const int64_t want = (items + 7) / 8;
+  const int blocks = static_cast<int>(want < static_cast<int64_t>(num_sms) * 16 ? want : num_sms * 16);
+  pack_w4_kernel<<<blocks, 256, 0, st>>>(W, N, K, symmetric, codes, scales, zeros, err);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ FP8
+
+// E4M3 pair: `lo` goes to the lower byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int THREADS>
+__device__ __forceinline__ float block_max(float v, float* red) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < THREADS / 32 ? red[lane] : 0.0f;
+    v = warp_max(v);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = red[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ uint2 quant8(uint4 v, float s) {
+  const uint32_t b0 = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s));
+  const uint32_t b1 = e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s));
+  const uint32_t b2 = e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s));
+  const uint32_t b3 = e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s));
+  return make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+}
+
+__device__ __forceinline__ float amax8(uint4 v, float a) {
+  a = fmaxf(a, fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))));
+  a = fmaxf(a, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+  a = fmaxf(a, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
+  a = fmaxf(a, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
+  return a;
+}
+
+// [LP] S4 per-token, S8 current scaling: one CTA per row; the row is read
+// once from HBM (the second pass hits L1/L2), amax is a block reduction.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) quant_act_fp8_kernel(const uint16_t* __restrict__ X, int64_t K,
+                                                                uint8_t* __restrict__ Xq, float* __restrict__ sx) {
+  __shared__ float red[32];
+  const int64_t m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(X + m * K);
+  const int64_t n8 = K / 8;
+  float a = 0.0f;
+  for (int64_t i = threadIdx.x; i < n8; i += THREADS) a = amax8(row[i], a);
+  a = block_max<THREADS>(a, red);
+  const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+  if (threadIdx.x == 0) sx[m] = s;
+  uint2* out = reinterpret_cast<uint2*>(Xq + m * K);
+  for (int64_t i = threadIdx.x; i < n8; i += THREADS) out[i] = quant8(row[i], s);
+}
+
+cudaError_t launch_quant_act_fp8(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx, cudaStream_t st) {
+  if (K >= 4096)
+    quant_act_fp8_kernel<512><<<static_cast<unsigned>(M), 512, 0, st>>>(X, K, Xq, sx);
+  else
+    quant_act_fp8_kernel<128><<<static_cast<unsigned>(M), 128, 0, st>>>(X, K, Xq, sx);
+  return cudaGetLastError();
+}
+
+// [LP] S4 per-tensor: grid-wide amax via atomicMax on the IEEE bits of a
+// non-negative float (integer order equals float order there).
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ W, int64_t n8,
+                                                   uint32_t* __restrict__ amax_bits) {
+  __shared__ float red[32];
+  float a = 0.0f;
+  const uint4* p = reinterpret_cast<const uint4*>(W);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n8; i += static_cast<int64_t>(gridDim.x) * 256)
+    a = amax8(p[i], a);
+  a = block_max<256>(a, red);
+  if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(a));
+}
+
+__global__ void __launch_bounds__(256) cast_w_fp8_kernel(const uint16_t* __restrict__ W, int64_t n8,
+                                                         const uint32_t* __restrict__ amax_bits,
+                                                         uint8_t* __restrict__ Wq, float* __restrict__ sw) {
+  const float a = __uint_as_float(*amax_bits);
+  const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sw = s;
+  const uint4* p = reinterpret_cast<const uint4*>(W);
+  uint2* out = reinterpret_cast<uint2*>(Wq);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n8; i += static_cast<int64_t>(gridDim.x) * 256)
+    out[i] = quant8(p[i], s);
+}
+
+cudaError_t launch_quant_w_fp8(const uint16_t* W, int64_t N, int64_t K, uint8_t* Wq, float* sw, uint32_t* amax_ws,
+                               int num_sms, cudaStream_t st) {
+  const int64_t n8 = N * K / 8;
+  cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  const int64_t want = (n8 + 255) / 256;
+  const int blocks = static_cast<int>(want < static_cast<int64_t>(num_sms) * 8 ? want : num_sms * 8);
+  amax_kernel<<<blocks, 256, 0, st>>>(W, n8, amax_ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cast_w_fp8_kernel<<<blocks, 256, 0, st>>>(W, n8, amax_ws, Wq, sw);
+  return cudaGetLastError();
+}
+
+}  // namespace qlin

@@ -1,0 +1,98 @@
+"""Layer objects that own the packed weights and the split-K workspace.
+
+``W4A16Linear`` packs BF16 weights once at construction ([LP] S18 "pack once,
+reuse") and runs ``qlin_w4a16_gemm`` per call; ``W8A8Linear`` quantises the
+weights to E4M3 once and runs the fused per-token activation quantiser plus
+``qlin_w8a8_fp8_gemm`` per call.  Device memory comes from torch; every
+computation is a libqlin kernel.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_pack_w4, qlin_quant_act_fp8,
+               qlin_quant_w_fp8, qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w8a8_fp8_gemm_ex,
+               qlin_workspace_size)
+
+
+def _as_u16(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16)
+    assert t.dtype in (torch.int16, torch.uint16)
+    return t
+
+
+class Workspace:
+    """Zero-filled split-K scratch, grown on demand (the library leaves it zeroed)."""
+
+    def __init__(self, device):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        if nbytes == 0:
+            return None, 0
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf, self.buf.numel()
+
+
+class W4A16Linear:
+    def __init__(self, W_bf16: torch.Tensor, G: int = 128, symmetric: bool = False, stream=None):
+        N, K = W_bf16.shape
+        self.N, self.K, self.G = N, K, G
+        dev = W_bf16.device
+        nc, ns, nz = qlin_w4_packed_sizes(N, K, G)
+        self.codes = torch.empty(nc, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(ns // 2, dtype=torch.int16, device=dev)
+        self.zeros = torch.empty(nz, dtype=torch.uint8, device=dev)
+        qlin_pack_w4(_as_u16(W_bf16.contiguous()), N, K, G, symmetric, self.codes, self.scales, self.zeros,
+                     stream)
+        self.ws = Workspace(dev)
+
+    def packed_bytes(self) -> int:
+        return self.codes.numel() + 2 * self.scales.numel() + self.zeros.numel()
+
+    def __call__(self, X_bf16: torch.Tensor, Y: torch.Tensor = None, path: int = PATH_AUTO, stream=None):
+        M = X_bf16.shape[0]
+        if Y is None:
+            Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=X_bf16.device)
+        buf, nb = self.ws.get(qlin_workspace_size(OP_W4A16_GEMM, M, self.N, self.K))
+        qlin_w4a16_gemm_ex(_as_u16(X_bf16), self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N,
+                           self.K, self.G, buf, nb, path, stream)
+        return Y
+
+
+class W8A8Linear:
+    def __init__(self, W_bf16: torch.Tensor, stream=None):
+        N, K = W_bf16.shape
+        self.N, self.K = N, K
+        dev = W_bf16.device
+        self.Wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        self.sw = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.zeros(qlin_workspace_size(OP_QUANT_W_FP8, 1, N, K), dtype=torch.uint8, device=dev)
+        qlin_quant_w_fp8(_as_u16(W_bf16.contiguous()), N, K, self.Wq, self.sw, ws, ws.numel(), stream)
+        self.ws = Workspace(dev)
+        self._amax_ws = ws
+
+    def quant_act(self, X_bf16: torch.Tensor, Xq=None, sx=None, stream=None):
+        M, K = X_bf16.shape
+        if Xq is None:
+            Xq = torch.empty((M, K), dtype=torch.uint8, device=X_bf16.device)
+        if sx is None:
+            sx = torch.empty(max(M, 1), dtype=torch.float32, device=X_bf16.device)
+        qlin_quant_act_fp8(_as_u16(X_bf16), M, K, Xq, sx, stream)
+        return Xq, sx
+
+    def gemm(self, Xq, sx, Y=None, path: int = PATH_AUTO, stream=None):
+        M = Xq.shape[0]
+        if Y is None:
+            Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
+        buf, nb = self.ws.get(qlin_workspace_size(OP_W8A8_GEMM, M, self.N, self.K))
+        qlin_w8a8_fp8_gemm_ex(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, buf, nb, path,
+                              stream)
+        return Y
+
+    def __call__(self, X_bf16, Y=None, path: int = PATH_AUTO, stream=None):
+        Xq, sx = self.quant_act(X_bf16, stream=stream)
+        return self.gemm(Xq, sx, Y, path, stream)

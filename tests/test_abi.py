@@ -1,0 +1,84 @@
+"""The C ABI library loads and exports every symbol the header declares, and
+argument validation rejects bad calls before touching the GPU (no compute)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import precision_quantized_linear_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qlin.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    q.build()
+    return q.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qlin_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared()
+    for n in ("qlin_pack_w4", "qlin_w4a16_gemm", "qlin_quant_act_fp8", "qlin_w8a8_fp8_gemm", "qlin_quant_w_fp8",
+              "qlin_get_device_error", "qlin_workspace_size", "qlin_w4_packed_sizes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(q._SIGS), "binding misses a declared call"
+
+
+def test_status_strings_and_version(lib):
+    assert q.qlin_status_string(0) == "QLIN_OK"
+    assert q.qlin_status_string(7) == "QLIN_ERR_TIMEOUT"
+    assert q.qlin_status_string(99) == "QLIN_ERR_UNKNOWN"
+    assert q.qlin_pack_format_version() == q.PACK_FORMAT_VERSION == 1
+
+
+def test_packed_sizes_give_4_125_bits(lib):
+    c, s, z = q.qlin_w4_packed_sizes(4096, 14336, 128)
+    assert 8 * (c + s) / (4096 * 14336) == 4.125
+    assert 8 * (c + s + z) / (4096 * 14336) == 4.15625
+    with pytest.raises(q.QlinError) as e:
+        q.qlin_w4_packed_sizes(4096, 4096, 64)
+    assert e.value.status == 2
+
+
+# Validation happens before any CUDA call: these return without a device.
+def _w4(lib, X=16, codes=16, s=16, z=16, Y=16, M=1, N=128, K=128, G=128, ws=None, wsb=0, path=0):
+    return lib.qlin_w4a16_gemm_ex(X, codes, s, z, Y, M, N, K, G, ws, wsb, path, None)
+
+
+def test_w4a16_rejects_bad_arguments(lib):
+    assert _w4(lib, G=64) == 2
+    assert _w4(lib, N=100) == 2
+    assert _w4(lib, K=192) == 2
+    assert _w4(lib, M=-1) == 2
+    assert _w4(lib, M=(1 << 24) + 1) == 2
+    assert _w4(lib, path=3) == 1
+    assert _w4(lib, X=None) == 1
+    assert _w4(lib, Y=None) == 1
+    assert _w4(lib, codes=24) == 3
+    assert _w4(lib, ws=8) == 3
+    assert _w4(lib, M=0, X=None) == 0          # empty call: nothing to do
+
+
+def test_fp8_and_pack_reject_bad_arguments(lib):
+    assert lib.qlin_quant_act_fp8(16, 1, 100, 16, 16, None) == 2
+    assert lib.qlin_quant_act_fp8(None, 1, 128, 16, 16, None) == 1
+    assert lib.qlin_quant_act_fp8(16, 1, 128, 17, 16, None) == 3
+    assert lib.qlin_quant_act_fp8(None, 0, 128, None, None, None) == 0
+    assert lib.qlin_w8a8_fp8_gemm_ex(16, 16, 16, 16, 16, 1, 96, 128, None, 0, 0, None) == 2
+    assert lib.qlin_w8a8_fp8_gemm_ex(16, 18, 16, 16, 16, 1, 128, 128, None, 0, 0, None) == 3
+    assert lib.qlin_pack_w4(16, 128, 128, 128, 2, 16, 16, 16, None) == 1
+    assert lib.qlin_pack_w4(16, 128, 128, 32, 0, 16, 16, 16, None) == 2
+    assert lib.qlin_quant_w_fp8(16, 128, 128, 16, 16, None, 0, None) == 1
