@@ -431,6 +431,142 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------------------------- sweeps
+
+def fp8_peak_probe():
+    """Dense E4M3 GEMM throughput of the vendor library (torch._scaled_mm), TFLOP/s."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device="cuda")
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        e0, e1 = make_event(False), make_event(False)
+        e0.record()
+        for _ in range(20):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        e1.record()
+        torch.cuda.synchronize()
+        return 2 * n ** 3 * 20 / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    except Exception as ex:  # noqa: BLE001
+        print("fp8 probe failed:", ex, file=sys.stderr)
+        return None
+
+
+def time_launches(launches, reps=10, warm=3):
+    """Average device time of one launch: a CUDA graph holding the given
+    launch closures (one per rotating weight copy), replayed `reps` times."""
+    import torch
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for f in launches:
+            f(st)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for f in launches:
+            f(st)
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = make_event(False), make_event(False)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(reps):
+            g.replay()
+        e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * len(launches)) * 1e3   # microseconds
+
+
+def run_sweep(args):
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+    from precision_quantized_linear_gb300 import synthetic as syn
+    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8Linear
+
+    torch.cuda.set_device(0)
+    q.build()
+    q.load()
+    peaks = load_peaks()
+    p8 = fp8_peak_probe()
+    p16 = peaks["bf16_tflops"]
+    bw = peaks["hbm_gbs"]
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size if hasattr(torch.cuda.get_device_properties(0), "L2_cache_size") else 126 * 2 ** 20
+    print(json.dumps({"peaks": peaks, "fp8_probe_tflops": p8, "l2_bytes": l2}), flush=True)
+    p8_use = p8 if p8 else 2 * p16
+
+    if args.sweep == "crossover":
+        shapes = [(4096, 14336), (14336, 4096)]
+        plan = [("w4", M) for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)] + \
+               [("w8", M) for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)]
+    elif args.sweep == "prefill":
+        shapes = [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]
+        plan = [("w8", M) for M in (2048, 8192)] + [("w4", M) for M in (2048, 8192)]
+    elif args.sweep == "70b":
+        shapes = [(8192, 10240), (8192, 8192), (8192, 57344), (28672, 8192)]
+        plan = [("w4", M) for M in (1, 64, 256)] + [("w8", M) for M in (256, 4096)]
+    else:  # decode: GEMV vs tensor-core path per M, for the dispatch threshold
+        shapes = [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]
+        plan = [(v, M) for M in (1, 2, 3, 4, 5, 8, 16) for v in ("w4gemv", "w4tc", "w8gemv", "w8tc")]
+
+    for (K, N) in shapes:
+        W = torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda()
+        lin4 = W4A16Linear(W)
+        lin8 = W8A8Linear(W)
+        del W
+        w4b, w8b = w4_weight_bytes(N, K), N * K
+        r4 = max(1, int(np.ceil(3 * l2 / w4b)))
+        r8 = max(1, int(np.ceil(3 * l2 / w8b)))
+        sets4 = [(lin4.codes, lin4.scales, lin4.zeros)] + [
+            (lin4.codes.clone(), lin4.scales.clone(), lin4.zeros.clone()) for _ in range(r4 - 1)]
+        sets8 = [lin8.Wq] + [lin8.Wq.clone() for _ in range(r8 - 1)]
+        for (v, M) in plan:
+            X = torch.from_numpy(syn.make_act(M, K, seed=M + 7, token_outlier_frac=0.001).view(np.int16)).cuda()
+            Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+            Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+            sx = torch.empty(M, dtype=torch.float32, device="cuda")
+            row = {"K": K, "N": N, "M": M, "variant": v}
+            flops = 2 * M * N * K
+            if v.startswith("w4"):
+                path = {"w4": q.PATH_AUTO, "w4gemv": q.PATH_GEMV, "w4tc": q.PATH_TC}[v]
+                nb = q.qlin_workspace_size(q.OP_W4A16_GEMM, M, N, K)
+                ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+                fns = [lambda st, c=c, s=s, z=z: q.qlin_w4a16_gemm_ex(X, c, s, z, Y, M, N, K, 128, ws, ws.numel(),
+                                                                     path, st) for (c, s, z) in sets4]
+                us = time_launches(fns)
+                alg = w4_alg_bytes(M, N, K)
+                t_roof = max(flops / (p16 * 1e12), alg / (bw * 1e9)) * 1e6
+                row.update(us=round(us, 2), weight_GBps=round(w4b / (us * 1e-6) / 1e9, 1),
+                           TFLOPS=round(flops / (us * 1e-6) / 1e12, 2), roof_us=round(t_roof, 2),
+                           roof_frac=round(t_roof / us, 3),
+                           bound="hbm" if alg / (bw * 1e9) > flops / (p16 * 1e12) else "tensor")
+            else:
+                path = {"w8": q.PATH_AUTO, "w8gemv": q.PATH_GEMV, "w8tc": q.PATH_TC}[v]
+                nb = q.qlin_workspace_size(q.OP_W8A8_GEMM, M, N, K)
+                ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+                q.qlin_quant_act_fp8(X, M, K, Xq, sx)
+                fns = [lambda st, wq=wq: q.qlin_w8a8_fp8_gemm_ex(Xq, sx, wq, lin8.sw, Y, M, N, K, ws, ws.numel(),
+                                                                 path, st) for wq in sets8]
+                us = time_launches(fns)
+                qus = time_launches([lambda st: q.qlin_quant_act_fp8(X, M, K, Xq, sx, st)])
+                alg = w8_alg_bytes(M, N, K)
+                t_roof = max(flops / (p8_use * 1e12), alg / (bw * 1e9)) * 1e6
+                row.update(us=round(us, 2), quant_us=round(qus, 2), weight_GBps=round(w8b / (us * 1e-6) / 1e9, 1),
+                           TFLOPS=round(flops / (us * 1e-6) / 1e12, 2), roof_us=round(t_roof, 2),
+                           roof_frac=round(t_roof / us, 3),
+                           bound="hbm" if alg / (bw * 1e9) > flops / (p8_use * 1e12) else "tensor",
+                           fp8_peak="probe" if p8 else "2x bf16 (assumed)")
+            assert q.qlin_get_device_error() == 0
+            print(json.dumps(row), flush=True)
+        del lin4, lin8, sets4, sets8
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,8 +583,7 @@ def main():
         run_reference(args)
         return
     if args.sweep:
-        from precision_quantized_linear_gb300 import sweep
-        sweep.run(args.sweep, args)
+        run_sweep(args)
         return
     run_ours(args)
 

@@ -305,13 +305,20 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols) {
   p.mblocks = (M + p.bn - 1) / p.bn;
   const int64_t tiles = (N / kTileN) * p.mblocks;
   const int64_t KB = K / cols;
-  // one CTA per SM: split K until about one wave of CTAs covers the SMs,
-  // keeping at least 8 blocks of K per CTA
+  // One CTA per SM.  Pick the split count whose CTAs fill whole waves best
+  // (busy SM-slots / all slots of the waves), with at least 4 blocks of K per
+  // CTA; on a tie take fewer splits (less partial-sum traffic).
   int s = 1;
-  if (tiles < num_sms) {
-    s = static_cast<int>((num_sms + tiles - 1) / tiles);
-    const int64_t max_s = KB / 8 > 0 ? KB / 8 : 1;
-    if (s > max_s) s = static_cast<int>(max_s);
+  double best = -1.0;
+  const int64_t max_s = KB / 4 > 0 ? (KB / 4 < 32 ? KB / 4 : 32) : 1;
+  for (int c = 1; c <= max_s; ++c) {
+    const int64_t ctas = tiles * c;
+    const int64_t waves = (ctas + num_sms - 1) / num_sms;
+    const double eff = static_cast<double>(ctas) / static_cast<double>(waves * num_sms);
+    if (eff > best + 0.02) {
+      best = eff;
+      s = c;
+    }
   }
   const int per = static_cast<int>((KB + s - 1) / s);
   s = static_cast<int>((KB + per - 1) / per);
