@@ -133,12 +133,12 @@ def dist_setup(args):
     return world, rank, local
 
 
-def dist_max(x: float, world: int) -> float:
+def dist_max(x: float, world: int, device: str = "cuda") -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -567,6 +567,42 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_case(args):
+    """A few launches of one GEMM configuration (small ncu captures)."""
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+    from precision_quantized_linear_gb300 import synthetic as syn
+    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8Linear
+
+    torch.cuda.set_device(0)
+    q.build()
+    q.load()
+    M, N, K = args.M, args.N, args.K
+    path = {"auto": q.PATH_AUTO, "gemv": q.PATH_GEMV, "tc": q.PATH_TC}[args.path]
+    W = torch.from_numpy(syn.make_weight(N, K, seed=5).view(np.int16)).cuda()
+    X = torch.from_numpy(syn.make_act(M, K, seed=6).view(np.int16)).cuda()
+    if args.case == "w4a16":
+        lin = W4A16Linear(W)
+        fn = lambda: lin(X, path=path)  # noqa: E731
+    else:
+        lin = W8A8Linear(W)
+        Xq, sx = lin.quant_act(X)
+        fn = lambda: lin.gemm(Xq, sx, path=path)  # noqa: E731
+    del W
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = make_event(False), make_event(False)
+    e0.record()
+    for _ in range(args.reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    assert q.qlin_get_device_error() == 0
+    print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "path": args.path,
+                      "us_per_call": round(e0.elapsed_time(e1) * 1e3 / args.reps, 2)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -576,6 +612,12 @@ def main():
     ap.add_argument("--sweep", default=None, choices=["crossover", "prefill", "70b", "decode"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, choices=["w4a16", "w8a8"])
+    ap.add_argument("--M", type=int, default=16)
+    ap.add_argument("--N", type=int, default=28672)
+    ap.add_argument("--K", type=int, default=4096)
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"])
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -584,6 +626,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.case:
+        run_case(args)
         return
     run_ours(args)
 

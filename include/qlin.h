@@ -176,6 +176,14 @@ int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e
  * word: QLIN_OK, or the first error a kernel recorded since the last call. */
 int qlin_get_device_error(void* stream);
 
+/* Failure-detection self-test: launches one CTA that waits, with the same
+ * bounded mbarrier wait the tensor-core kernels use, on a barrier that nothing
+ * completes.  After `limit_us` microseconds of device time the wait gives up
+ * and records QLIN_ERR_TIMEOUT in the error word, and the kernel returns; the
+ * context stays usable.  Returns the launch status; read the recorded error
+ * with qlin_get_device_error().  limit_us must be in 1..1000000. */
+int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
 /* The M at or below which the AUTO path of each GEMM uses the GEMV kernel. */
 int qlin_gemv_max_m(int op);
 

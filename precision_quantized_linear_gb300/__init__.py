@@ -22,7 +22,7 @@ __all__ = [
     "qlin_status_string", "qlin_pack_format_version", "qlin_w4_packed_sizes", "qlin_workspace_size",
     "qlin_pack_w4", "qlin_w4a16_gemm", "qlin_w4a16_gemm_ex", "qlin_quant_act_fp8", "qlin_quant_w_fp8",
     "qlin_w8a8_fp8_gemm", "qlin_w8a8_fp8_gemm_ex", "qlin_get_device_error", "qlin_gemv_max_m",
-    "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "PATH_AUTO", "PATH_GEMV", "PATH_TC",
+    "qlin_selftest_wait_timeout", "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "PATH_AUTO", "PATH_GEMV", "PATH_TC",
     "PACK_FORMAT_VERSION",
 ]
 
@@ -52,6 +52,7 @@ _SIGS = {
     "qlin_w8a8_fp8_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
     "qlin_w8a8_fp8_gemm_ex": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _int, _p],
     "qlin_get_device_error": [_p],
+    "qlin_selftest_wait_timeout": [ctypes.c_uint32, _p],
 }
 
 
@@ -174,3 +175,8 @@ def qlin_w8a8_fp8_gemm_ex(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, path,
 def qlin_get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error word."""
     return load().qlin_get_device_error(_stream(stream))
+
+
+def qlin_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    """Launch the bounded-wait self-test kernel (see include/qlin.h)."""
+    return _check(load().qlin_selftest_wait_timeout(int(limit_us), _stream(stream)), "qlin_selftest_wait_timeout")

@@ -277,6 +277,15 @@ int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3
                                stream);
 }
 
+int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return QLIN_ERR_INVALID_VALUE;
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_wait_timeout(static_cast<uint64_t>(limit_us) * 1000ull, d->err,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int qlin_get_device_error(void* stream) {
   DeviceState* d = nullptr;
   int st = device_state(&d);

@@ -79,6 +79,8 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
                            int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
                            cudaStream_t st);
 
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int* err, cudaStream_t st);
+
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);

@@ -289,6 +289,24 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ------------------------------------------------------------------ self-test
+
+// A barrier nobody arrives on: the bounded wait must give up and report.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) set_error(err, QLIN_ERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int* err, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ planning
 
 static int pick_bn(int64_t M) {
