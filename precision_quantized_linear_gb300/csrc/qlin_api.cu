@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <unordered_map>
 
 #include "qlin_internal.cuh"
 
@@ -79,6 +80,21 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+cudaError_t set_smem_once_impl(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, unsigned long long> done;  // kernel -> bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = done.find(kernel);
+  if (it != done.end() && (it->second & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[kernel] |= bit;
+  return e;
 }
 
 // M at or below which the GEMV kernels are chosen (measured crossover).

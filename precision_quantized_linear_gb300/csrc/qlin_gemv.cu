@@ -119,13 +119,28 @@ __global__ void __launch_bounds__(128) w4a16_gemv_kernel(const uint16_t* __restr
     for (int i = 0; i < 4; ++i) y[m][i] = 0.0f;
 
   const int64_t ng = K / kGroup;
+  const uint8_t* tbase = codes + static_cast<int64_t>(nt) * KB * 4096;
+  uint4 cn[4][2];
+  if (kb0 + warp < kb1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        cn[i][h] = ldg_stream(tbase + static_cast<int64_t>(kb0 + warp) * 4096 + h * 2048 + (lane + 32 * i) * 16);
+  }
   for (int kb = kb0 + warp; kb < kb1; kb += 4) {
-    const uint8_t* tile = codes + (static_cast<int64_t>(nt) * KB + kb) * 4096;
     uint4 c[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) c[i][h] = ldg_stream(tile + h * 2048 + (lane + 32 * i) * 16);
+      for (int h = 0; h < 2; ++h) c[i][h] = cn[i][h];
+    if (kb + 4 < kb1) {  // software pipelining: next block's codes are in flight during this block's math
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          cn[i][h] = ldg_stream(tbase + static_cast<int64_t>(kb + 4) * 4096 + h * 2048 + (lane + 32 * i) * 16);
+    }
     const int64_t sz = static_cast<int64_t>(nt) * ng + kb / 2;
     float sc[4], cz[4];
 #pragma unroll

@@ -30,18 +30,12 @@ struct SplitPlan {
 };
 
 // cudaFuncSetAttribute once per (kernel, device), so that no such call is made
-// while a stream is being captured into a CUDA graph.
+// while a stream is being captured into a CUDA graph.  Keyed by the kernel's
+// address: template instantiations share a type but not an address.
+cudaError_t set_smem_once_impl(const void* kernel, int bytes);
 template <typename F>
 inline cudaError_t set_smem_once(F* kernel, int bytes) {
-  static unsigned long long done = 0;  // bit per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
-  return e;
+  return set_smem_once_impl(reinterpret_cast<const void*>(kernel), bytes);
 }
 
 inline size_t counters_bytes(int64_t tiles) { return static_cast<size_t>((tiles * 4 + 255) / 256 * 256); }
