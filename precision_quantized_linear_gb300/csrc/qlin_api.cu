@@ -68,6 +68,13 @@ static int device_state(DeviceState** out) {
   return d.status;
 }
 
+int device_num_sms(int* out) {
+  DeviceState* d = nullptr;
+  const int st = device_state(&d);
+  if (st == QLIN_OK) *out = d->num_sms;
+  return st;
+}
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
   (void)elem_bytes;
@@ -220,7 +227,7 @@ int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales
   }
   const TcPlan p = plan_w4a16_tc(M, N, K, d->num_sms);
   if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, p, workspace, d->err, cs));
+  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, p, workspace, d->err, d->num_sms, cs));
 }
 
 int qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
@@ -284,7 +291,7 @@ int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e
   }
   const TcPlan p = plan_w8a8_tc(M, N, K, d->num_sms);
   if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_w8a8_tc(xq, sx, wq, sw, Y, M, N, K, p, workspace, d->err, cs));
+  return launch_status(launch_w8a8_tc(xq, sx, wq, sw, Y, M, N, K, p, workspace, d->err, d->num_sms, cs));
 }
 
 int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,

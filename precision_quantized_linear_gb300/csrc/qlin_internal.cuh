@@ -68,12 +68,16 @@ TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
-                            cudaStream_t st);
+                            int num_sms, cudaStream_t st);
 cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
-                           int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
+                           int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
                            cudaStream_t st);
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* err, cudaStream_t st);
+
+// SM count of the current device after the library's device checks
+// (returns a qlin status).
+int device_num_sms(int* out);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,

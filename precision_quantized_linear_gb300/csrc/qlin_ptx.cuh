@@ -49,14 +49,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait on the phase with the given parity.  Returns false when the
-// wait gave up (after `limit_ns` of global time), so that the caller can
-// record an error and leave instead of hanging the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+// wait gave up -- after `limit_ns` of global time, or at once when `abort`
+// (a flag in shared memory set by a role that already gave up) is set -- so
+// that the caller can record an error and leave instead of hanging the GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                          const volatile int* abort = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    if (abort && *abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
