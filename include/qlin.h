@@ -184,6 +184,31 @@ int qlin_get_device_error(void* stream);
  * with qlin_get_device_error().  limit_us must be in 1..1000000. */
 int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
 
+/*
+ * W4A16 split-K GEMV that allocates nothing (no counterpart on the pages: it
+ * exists for callers that cannot allocate device memory when they run the
+ * layer -- code inside a memory pool it does not own, a runtime that forbids
+ * allocation after start-up, a host that must keep a fixed footprint).
+ * Same arguments and result as qlin_w4a16_gemm_ex(..., QLIN_PATH_GEMV, ...)
+ * but without a workspace: the split-K partial sums live in one scratch array
+ * of 4 MiB inside the library image (a file-scope __device__ array that every
+ * GPU which loads the library holds until the process exits).
+ *  - Sizes whose split-K partial sums need more than 4 MiB are rejected with
+ *    QLIN_ERR_WORKSPACE_TOO_SMALL before anything is launched.  With the
+ *    current split choice this accepts every M <= 16 on the Llama-3-8B layer
+ *    shapes and every M <= 4 on the Llama-3-70B shapes.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents:
+ *    the call clears the per-tile counters itself (an asynchronous memset on
+ *    `stream`), so calls that overlap on the GPU -- on different streams, or
+ *    from different threads -- race and must not be issued.
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                            void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* stream);
+
 /* The M at or below which the AUTO path of each GEMM uses the GEMV kernel. */
 int qlin_gemv_max_m(int op);
 

@@ -22,7 +22,7 @@ __all__ = [
     "qlin_status_string", "qlin_pack_format_version", "qlin_w4_packed_sizes", "qlin_workspace_size",
     "qlin_pack_w4", "qlin_w4a16_gemm", "qlin_w4a16_gemm_ex", "qlin_quant_act_fp8", "qlin_quant_w_fp8",
     "qlin_w8a8_fp8_gemm", "qlin_w8a8_fp8_gemm_ex", "qlin_get_device_error", "qlin_gemv_max_m",
-    "qlin_selftest_wait_timeout", "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "PATH_AUTO", "PATH_GEMV", "PATH_TC",
+    "qlin_selftest_wait_timeout", "qlin_w4a16_gemv_noalloc", "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "PATH_AUTO", "PATH_GEMV", "PATH_TC",
     "PACK_FORMAT_VERSION",
 ]
 
@@ -53,6 +53,7 @@ _SIGS = {
     "qlin_w8a8_fp8_gemm_ex": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _int, _p],
     "qlin_get_device_error": [_p],
     "qlin_selftest_wait_timeout": [ctypes.c_uint32, _p],
+    "qlin_w4a16_gemv_noalloc": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p],
 }
 
 
@@ -180,3 +181,10 @@ def qlin_get_device_error(stream=None) -> int:
 def qlin_selftest_wait_timeout(limit_us: int, stream=None) -> int:
     """Launch the bounded-wait self-test kernel (see include/qlin.h)."""
     return _check(load().qlin_selftest_wait_timeout(int(limit_us), _stream(stream)), "qlin_selftest_wait_timeout")
+
+
+def qlin_w4a16_gemv_noalloc(X, codes, scales, zeros, Y, M, N, K, G, stream=None):
+    """W4A16 GEMV whose scratch is a fixed array inside the library (no workspace
+    argument, nothing allocated): for callers that cannot allocate device memory."""
+    return _check(load().qlin_w4a16_gemv_noalloc(_ptr(X), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(Y), M, N, K,
+                                                 G, _stream(stream)), "qlin_w4a16_gemv_noalloc")
