@@ -195,8 +195,8 @@ int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
  * GPU which loads the library holds until the process exits).
  *  - Sizes whose split-K partial sums need more than 4 MiB are rejected with
  *    QLIN_ERR_WORKSPACE_TOO_SMALL before anything is launched.  With the
- *    current split choice this accepts every M <= 16 on the Llama-3-8B layer
- *    shapes and every M <= 4 on the Llama-3-70B shapes.
+ *    current split choice this accepts every M <= 16 on the Llama-3-8B and
+ *    Llama-3-70B layer shapes.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.

@@ -75,6 +75,11 @@ int device_num_sms(int* out) {
   return st;
 }
 
+int* device_error_word() {
+  DeviceState* d = nullptr;
+  return device_state(&d) == QLIN_OK ? d->err : nullptr;
+}
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
   (void)elem_bytes;
@@ -105,7 +110,7 @@ cudaError_t set_smem_once_impl(const void* kernel, int bytes) {
 }
 
 // M at or below which the GEMV kernels are chosen (measured crossover).
-static int g_gemv_max_m_w4 = 4;
+static int g_gemv_max_m_w4 = 16;
 static int g_gemv_max_m_w8 = 4;
 
 }  // namespace qlin
@@ -155,7 +160,7 @@ int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* sca
 }
 
 static size_t ws_w4(int64_t M, int64_t N, int64_t K, int sms) {
-  const size_t a = plan_w4a16_gemv(M, N, K, sms).ws_bytes;
+  size_t a = mma_path_ok(M, K) ? plan_w4a16_mma(M, N, K, sms).ws_bytes : plan_w4a16_gemv(M, N, K, sms).ws_bytes;
   const size_t b = plan_w4a16_tc(M, N, K, sms).split.ws_bytes;
   return a > b ? a : b;
 }
@@ -221,6 +226,11 @@ int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales
   auto* Y = static_cast<uint16_t*>(Y_bf16);
   auto cs = static_cast<cudaStream_t>(stream);
   if (path == QLIN_PATH_GEMV) {
+    if (mma_path_ok(M, K)) {
+      const SplitPlan p = plan_w4a16_mma(M, N, K, d->num_sms);
+      if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+      return launch_status(launch_w4a16_mma(X, c, s, z, Y, M, N, K, p, workspace, d->err, cs));
+    }
     const SplitPlan p = plan_w4a16_gemv(M, N, K, d->num_sms);
     if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
     return launch_status(launch_w4a16_gemv(X, c, s, z, Y, M, N, K, p, workspace, cs));

@@ -10,6 +10,7 @@
 #include <cuda_fp16.h>
 
 #include "qlin_internal.cuh"
+#include "qlin_ptx.cuh"
 
 namespace qlin {
 
@@ -92,6 +93,21 @@ __global__ void __launch_bounds__(128) w4a16_gemv_kernel(const uint16_t* __restr
   float* red = xsum + MT * ((nkb + 3) & ~3);  // [4][MT][128]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // the packed weights never depend on the previous kernel on the stream:
+  // start streaming them before waiting for it
+  const int64_t ng = K / kGroup;
+  const uint8_t* tbase = codes + static_cast<int64_t>(nt) * KB * 4096;
+  uint4 cn[4][2];
+  if (kb0 + warp < kb1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        cn[i][h] = ldg_stream(tbase + static_cast<int64_t>(kb0 + warp) * 4096 + h * 2048 + (lane + 32 * i) * 16);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+
   for (int idx = threadIdx.x; idx < MT * (KR / 8); idx += 128) {
     const int m = idx / (KR / 8), i8 = idx % (KR / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -118,16 +134,6 @@ __global__ void __launch_bounds__(128) w4a16_gemv_kernel(const uint16_t* __restr
 #pragma unroll
     for (int i = 0; i < 4; ++i) y[m][i] = 0.0f;
 
-  const int64_t ng = K / kGroup;
-  const uint8_t* tbase = codes + static_cast<int64_t>(nt) * KB * 4096;
-  uint4 cn[4][2];
-  if (kb0 + warp < kb1) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        cn[i][h] = ldg_stream(tbase + static_cast<int64_t>(kb0 + warp) * 4096 + h * 2048 + (lane + 32 * i) * 16);
-  }
   for (int kb = kb0 + warp; kb < kb1; kb += 4) {
     uint4 c[4][2];
 #pragma unroll
@@ -214,6 +220,24 @@ __global__ void __launch_bounds__(128) w4a16_gemv_kernel(const uint16_t* __restr
                     [&](int64_t m, int64_t nn, float v) { Y[m * N + nn] = f32_to_bf16_rn(v); });
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream finishes; it waits for that kernel (grid
+// dependency) before touching activations or outputs.
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 static size_t w4_gemv_smem(int mt, int kb_per_split) {
   const int KR = kb_per_split * kTileK;
   return sizeof(float) * (static_cast<size_t>(mt) * KR + mt * ((kb_per_split + 3) & ~3) + 4 * mt * kTileN);
@@ -261,15 +285,15 @@ cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uin
   case MTV:                                                                                              \
     e = set_smem_once(w4a16_gemv_kernel<MTV>, 64 * 1024);                                                \
     if (e != cudaSuccess) return e;                                                                      \
-    w4a16_gemv_kernel<MTV><<<grid, 128, smem, st>>>(X, codes, scales, zeros, Y, M, N, K, plan.kb_per_split, \
-                                                    plan.splits, partials, counters);                    \
+    e = launch_pdl(w4a16_gemv_kernel<MTV>, grid, smem, st, X, codes, scales, zeros, Y, M, N, K,            \
+                   plan.kb_per_split, plan.splits, partials, counters);                                  \
     break;
     QLIN_W4GEMV(1)
     QLIN_W4GEMV(2)
     QLIN_W4GEMV(4)
 #undef QLIN_W4GEMV
   }
-  return cudaGetLastError();
+  return e;
 }
 
 // ------------------------------------------------------------------ W8A8 FP8
@@ -301,6 +325,8 @@ __global__ void __launch_bounds__(128) w8a8_gemv_kernel(const uint8_t* __restric
   const int KR = (kb1 - kb0) * kTileK;
   const int64_t kbase = static_cast<int64_t>(kb0) * kTileK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_wait();
+  grid_dep_launch();
 
   for (int idx = threadIdx.x; idx < MT * (KR / 8); idx += 128) {
     const int m = idx / (KR / 8), i8 = idx % (KR / 8);
@@ -389,15 +415,15 @@ cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* 
   case MTV:                                                                                                \
     e = set_smem_once(w8a8_gemv_kernel<MTV>, 64 * 1024);                                                   \
     if (e != cudaSuccess) return e;                                                                        \
-    w8a8_gemv_kernel<MTV><<<grid, 128, smem, st>>>(Xq, sx, Wq, sw, Y, M, N, K, plan.kb_per_split, plan.splits, \
-                                                   partials, counters);                                    \
+    e = launch_pdl(w8a8_gemv_kernel<MTV>, grid, smem, st, Xq, sx, Wq, sw, Y, M, N, K, plan.kb_per_split,     \
+                   plan.splits, partials, counters);                                                       \
     break;
     QLIN_W8GEMV(1)
     QLIN_W8GEMV(2)
     QLIN_W8GEMV(4)
 #undef QLIN_W8GEMV
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace qlin

@@ -53,6 +53,14 @@ cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uin
                               uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws,
                               cudaStream_t st);
 
+// W4A16 small-M kernel with register-level dequantisation feeding mma.sync
+// (M <= 16, K % 256 == 0); kb_per_split counts 256-column stages.
+bool mma_path_ok(int64_t M, int64_t K);
+SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
+                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, int* err,
+                             cudaStream_t st);
+
 SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                              int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st);
@@ -60,6 +68,7 @@ cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* 
 // tcgen05 kernels: swap-AB (weights are the 128-row MMA operand, tokens the N side)
 struct TcPlan {
   int bn = 16;           // tokens per tile (MMA N)
+  int kps = 1;           // K blocks per pipeline stage
   int64_t mblocks = 1;   // token blocks
   SplitPlan split;
 };
@@ -78,6 +87,8 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, int* err, cudaStream_t st);
 // SM count of the current device after the library's device checks
 // (returns a qlin status).
 int device_num_sms(int* out);
+// Device address of the current device's error word (valid after device_num_sms succeeded).
+int* device_error_word();
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,

@@ -1,0 +1,316 @@
+// W4A16 for small M (decode): split-K GEMV-style kernel whose inner product
+// runs on the tensor cores through register-level mma.sync, so that the CUDA
+// cores only unpack nibbles.
+//
+// [LP] S11 (packed INT4 -> unpack/dequantise -> multiply with BF16 activations
+// -> accumulate) and S22 (FP32 accumulation).  Per group g of 128 columns the
+// kernel uses
+//     sum_k x_k s (q_k - z) = s ( sum_k x_k (128 + q_k) - (128 + z) sum_k x_k ),
+// where 128 + q_k is exact in BF16 and comes out of the packed word with one
+// shift and one LOP3 per pair of columns; the MMA accumulates
+// sum_k x_k (128 + q_k) in FP32 and the scale / zero-point are applied once
+// per group and row in FP32 registers.
+//
+// One CTA = one 128-row tile x one K range.  Warp 4 streams, per stage of 256
+// columns, the tile's packed codes (16 KB), scales and zero-points and the
+// activation slice of every token into a ring of shared-memory stages with
+// bulk copies (weights first, before waiting for the previous kernel on the
+// stream).  Warps 0-3 each own 32 rows (two m16 blocks) and every token (one
+// or two n8 blocks).  The per-group activation sums come from the tensor core
+// too: one extra m16 block whose A fragment is all ones yields sum_k x_k for
+// exactly the tokens each thread folds.  Split-K partial sums use the same
+// deterministic last-arriver reduction as the other kernels.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qlin_internal.cuh"
+#include "qlin_ptx.cuh"
+
+namespace qlin {
+
+constexpr int kMmaStageCols = 256;                 // K columns per stage (4 code tiles)
+constexpr int kMmaCodeBytes = 4 * 4096;            // codes of one stage
+constexpr int kMmaMetaOff = kMmaCodeBytes;         // 2 groups x 128 FP16 scales, then 2 x 64 B zeros
+constexpr int kMmaXOff = kMmaCodeBytes + 1024;     // activation rows
+constexpr int kMmaXRow = kMmaStageCols * 2 + 16;   // 528 B per token row (conflict-free B fragments)
+constexpr int kMmaStages = 4;
+constexpr int kMmaConsumers = 8;                   // consumer warps, 16 rows (one m16 block) each
+constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
+constexpr uint64_t kMmaWaitNs = 2000000000ull;
+
+template <int NT>
+struct MmaCfg {
+  static constexpr int kTok = 8 * NT;
+  static constexpr int kStage = ((kMmaXOff + kTok * kMmaXRow) + 1023) / 1024 * 1024;
+  static constexpr int kSmem = 1024 + kMmaStages * kStage + 256;
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Pair (2p, 2p+1) of a packed word as BF16x2 (128 + q): nibble positions p and
+// 4 + p hold the two columns (tile layout v1).
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
+  return ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+}
+
+template <int NT>  // n8 token blocks: M <= 8 * NT
+__global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
+    const uint16_t* __restrict__ X, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+    const uint8_t* __restrict__ zeros, uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K, int stages_per_split,
+    int splits, float* partials, uint32_t* counters, int* err) {
+  using C = MmaCfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kMmaStages * C::kStage);
+  uint64_t* empty = full + kMmaStages;
+  __shared__ int s_last;
+  __shared__ volatile int s_abort;
+
+  const int nt = blockIdx.x, split = blockIdx.y;
+  const int64_t KS = K / kMmaStageCols;
+  const int s0 = split * stages_per_split;
+  const int nst = static_cast<int>(imin64(KS, s0 + stages_per_split)) - s0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ngK = K / kGroup;
+  const int64_t KB = K / kTileK;
+  const int mrows = static_cast<int>(imin64(M, C::kTok));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMmaStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMmaConsumers);
+    }
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+
+  const uint32_t tx = kMmaCodeBytes + 2 * 256 + 2 * 64 + mrows * kMmaStageCols * 2;
+  auto issue_w = [&](int i) {  // weights of stage i (ring slot i % kMmaStages)
+    uint8_t* st = ring + (i % kMmaStages) * C::kStage;
+    uint64_t* bar = &full[i % kMmaStages];
+    const int64_t kb = static_cast<int64_t>(s0 + i) * 4;  // first 64-column block
+    const int64_t g0 = kb / 2;
+    mbar_arrive_expect_tx(bar, tx);
+    bulk_load(st, codes + (static_cast<int64_t>(nt) * KB + kb) * 4096, kMmaCodeBytes, bar);
+    bulk_load(st + kMmaMetaOff, scales + (static_cast<int64_t>(nt) * ngK + g0) * kTileN, 2 * 256, bar);
+    bulk_load(st + kMmaMetaOff + 512, zeros + (static_cast<int64_t>(nt) * ngK + g0) * (kTileN / 2), 2 * 64, bar);
+  };
+  auto issue_x = [&](int i) {  // activation rows of stage i
+    uint8_t* st = ring + (i % kMmaStages) * C::kStage;
+    const int64_t k0 = static_cast<int64_t>(s0 + i) * kMmaStageCols;
+    for (int m = 0; m < mrows; ++m)
+      bulk_load(st + kMmaXOff + m * kMmaXRow, X + m * K + k0, kMmaStageCols * 2, &full[i % kMmaStages]);
+  };
+  // weights never depend on the previous kernel on the stream: start them first
+  if (warp == kMmaConsumers && lane == 0)
+    for (int i = 0; i < nst && i < kMmaStages; ++i) issue_w(i);
+  grid_dep_wait();
+  grid_dep_launch();
+
+  const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
+  float acc[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
+
+  if (warp == kMmaConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int i = 0; i < nst && i < kMmaStages; ++i) issue_x(i);
+      for (int i = kMmaStages; i < nst; ++i) {
+        if (!mbar_wait(&empty[i % kMmaStages], ((i / kMmaStages) & 1) ^ 1, kMmaWaitNs, &s_abort)) {
+          set_error(err, QLIN_ERR_TIMEOUT);
+          s_abort = 1;
+          break;
+        }
+        issue_w(i);
+        issue_x(i);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers: rows 16*warp .. 16*warp + 15
+    const int r0 = warp * 16 + gq;  // this thread's rows: r0 and r0 + 8
+    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // BF16 1.0 pairs
+    for (int i = 0; i < nst; ++i) {
+      const int slot = i % kMmaStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / kMmaStages) & 1, kMmaWaitNs, &s_abort))) {
+        set_error(err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      const uint8_t* st = ring + slot * C::kStage;
+      const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kMmaMetaOff);
+      const uint8_t* zp = st + kMmaMetaOff + 512;
+#pragma unroll 1
+      for (int grp = 0; grp < 2; ++grp) {
+        // two accumulators (one per 64-column block) keep two MMA chains in flight
+        float c[2][NT][4];
+        float xs[2][NT][4];  // sum_k x over each block, from the ones block (rows all equal)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              c[h2][j][e] = 0.0f;
+              xs[h2][j][e] = 0.0f;
+            }
+#pragma unroll
+        for (int kb2 = 0; kb2 < 2; ++kb2) {
+          const int kbl = grp * 2 + kb2;  // 64-column block within the stage
+          const uint8_t* tile = st + kbl * 4096;
+          const uint4 w00 = *reinterpret_cast<const uint4*>(tile + r0 * 16);         // half 0, row r0
+          const uint4 w01 = *reinterpret_cast<const uint4*>(tile + (r0 + 8) * 16);   // half 0, row r0+8
+          const uint4 w10 = *reinterpret_cast<const uint4*>(tile + 2048 + r0 * 16);  // half 1
+          const uint4 w11 = *reinterpret_cast<const uint4*>(tile + 2048 + (r0 + 8) * 16);
+          const uint32_t wr0[8] = {w00.x, w00.y, w00.z, w00.w, w10.x, w10.y, w10.z, w10.w};
+          const uint32_t wr1[8] = {w01.x, w01.y, w01.z, w01.w, w11.x, w11.y, w11.z, w11.w};
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {  // words 2ks, 2ks+1 hold columns 16ks .. 16ks+15
+            uint32_t b[NT][2];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              const int tok = j * 8 + gq;
+              if (tok < mrows) {
+                const uint8_t* xr = st + kMmaXOff + tok * kMmaXRow + (kbl * 64 + ks * 16 + 2 * tq) * 2;
+                b[j][0] = *reinterpret_cast<const uint32_t*>(xr);
+                b[j][1] = *reinterpret_cast<const uint32_t*>(xr + 16);
+              } else {
+                b[j][0] = 0u;
+                b[j][1] = 0u;
+              }
+            }
+            uint32_t a[4];
+            a[0] = nib_pair_bf16(wr0[2 * ks], tq);      // row r0,   columns 2t, 2t+1
+            a[1] = nib_pair_bf16(wr1[2 * ks], tq);      // row r0+8, columns 2t, 2t+1
+            a[2] = nib_pair_bf16(wr0[2 * ks + 1], tq);  // row r0,   columns 2t+8, 2t+9
+            a[3] = nib_pair_bf16(wr1[2 * ks + 1], tq);  // row r0+8, columns 2t+8, 2t+9
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              mma_bf16_16816(c[kb2][j], a, b[j][0], b[j][1]);
+              mma_bf16_16816(xs[kb2][j], ones, b[j][0], b[j][1]);
+            }
+          }
+        }
+        // fold: y += s (sum x (128 + q) - (128 + z) sum x); rows r0, r0+8; tokens 8j+2t, +1
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = r0 + hr * 8;
+          const float s = __half2float(__ushort_as_half(sc[grp * kTileN + r]));
+          const uint32_t zb = zp[grp * (kTileN / 2) + r / 2];
+          const float cz = 128.0f + static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float cs = c[0][j][hr * 2 + e] + c[1][j][hr * 2 + e];
+              const float xv = xs[0][j][e] + xs[1][j][e];
+              acc[j][hr * 2 + e] = fmaf(s, fmaf(-cz, xv, cs), acc[j][hr * 2 + e]);
+            }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+  }
+
+  // ---------------------------------------------------------------- outputs
+  if (warp < kMmaConsumers) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int64_t n = static_cast<int64_t>(nt) * kTileN + warp * 16 + gq + hr * 8;
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int64_t m = j * 8 + 2 * tq + e;
+          if (m < M) {
+            const float v = acc[j][hr * 2 + e];
+            if (splits == 1)
+              Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            else
+              __stcg(partials + (static_cast<int64_t>(split) * M + m) * N + n, v);
+          }
+        }
+    }
+  }
+  if (splits == 1) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    s_last = !s_abort && (atomicAdd(counters + nt, 1u) == static_cast<uint32_t>(splits - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // the last CTA of the tile adds the K ranges in split order (deterministic)
+  const int total = static_cast<int>(M) * kTileN;
+  for (int idx = threadIdx.x; idx < total; idx += kMmaThreads) {
+    const int64_t m = idx / kTileN;
+    const int64_t n = static_cast<int64_t>(nt) * kTileN + idx % kTileN;
+    const float* p = partials + m * N + n;
+    float v = 0.0f;
+#pragma unroll 4
+    for (int s = 0; s < splits; ++s) v += __ldcg(p + static_cast<int64_t>(s) * M * N);
+    Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  if (threadIdx.x == 0) counters[nt] = 0u;
+}
+
+// Split K only for parallelism: about two CTAs per SM.
+SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
+  SplitPlan p;
+  (void)M;
+  const int64_t tiles = N / kTileN;
+  const int64_t KS = K / kMmaStageCols;
+  int64_t s = (2LL * num_sms + tiles - 1) / tiles;
+  if (s > KS) s = KS;
+  if (s < 1) s = 1;
+  const int64_t per = (KS + s - 1) / s;
+  s = (KS + per - 1) / per;
+  p.splits = static_cast<int>(s);
+  p.kb_per_split = static_cast<int>(per);  // here: stages of 256 columns per split
+  p.tiles = tiles;
+  p.ws_bytes = s > 1 ? counters_bytes(tiles) + sizeof(float) * static_cast<size_t>(s) * M * N : 0;
+  return p;
+}
+
+bool mma_path_ok(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K % kMmaStageCols == 0; }
+
+template <int NT>
+static cudaError_t launch_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
+                              uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, float* partials,
+                              uint32_t* counters, int* err, cudaStream_t st) {
+  cudaError_t e = set_smem_once(w4a16_mma_kernel<NT>, MmaCfg<NT>::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(N / kTileN), plan.splits);
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = MmaCfg<NT>::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a16_mma_kernel<NT>, X, codes, scales, zeros, Y, M, N, K, plan.kb_per_split,
+                            plan.splits, partials, counters, err);
+}
+
+cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
+                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, int* err,
+                             cudaStream_t st) {
+  uint32_t* counters = static_cast<uint32_t*>(ws);
+  float* partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.tiles)) : nullptr;
+  if (M <= 8) return launch_mma<1>(X, codes, scales, zeros, Y, M, N, K, plan, partials, counters, err, st);
+  return launch_mma<2>(X, codes, scales, zeros, Y, M, N, K, plan, partials, counters, err, st);
+}
+
+}  // namespace qlin

@@ -56,7 +56,9 @@ extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, co
   int num_sms = 0;
   int st = device_num_sms(&num_sms);
   if (st != QLIN_OK) return st;
-  const SplitPlan plan = plan_w4a16_gemv(M, N, K, num_sms);
+  // same kernel choice as qlin_w4a16_gemm_ex(..., QLIN_PATH_GEMV, ...)
+  const bool mma = mma_path_ok(M, K);
+  const SplitPlan plan = mma ? plan_w4a16_mma(M, N, K, num_sms) : plan_w4a16_gemv(M, N, K, num_sms);
   if (plan.ws_bytes > kNoAllocScratchBytes) return QLIN_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
@@ -66,9 +68,13 @@ extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, co
   // start at zero, the partial sums are overwritten before they are read.
   if (plan.splits > 1 && cudaMemsetAsync(scratch, 0, counters_bytes(plan.tiles), cs) != cudaSuccess)
     return QLIN_ERR_CUDA;
-  const cudaError_t e = launch_w4a16_gemv(static_cast<const uint16_t*>(X_bf16), static_cast<const uint8_t*>(codes),
-                                          static_cast<const uint16_t*>(scales_f16),
-                                          static_cast<const uint8_t*>(zeros_u4), static_cast<uint16_t*>(Y_bf16), M,
-                                          N, K, plan, plan.splits > 1 ? scratch : nullptr, cs);
+  void* ws = plan.splits > 1 ? scratch : nullptr;
+  const auto* Xp = static_cast<const uint16_t*>(X_bf16);
+  const auto* cp = static_cast<const uint8_t*>(codes);
+  const auto* sp = static_cast<const uint16_t*>(scales_f16);
+  const auto* zp = static_cast<const uint8_t*>(zeros_u4);
+  auto* Yp = static_cast<uint16_t*>(Y_bf16);
+  const cudaError_t e = mma ? launch_w4a16_mma(Xp, cp, sp, zp, Yp, M, N, K, plan, ws, device_error_word(), cs)
+                            : launch_w4a16_gemv(Xp, cp, sp, zp, Yp, M, N, K, plan, ws, cs);
   return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA;
 }

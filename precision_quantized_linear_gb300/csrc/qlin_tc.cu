@@ -31,26 +31,39 @@ namespace qlin {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kSmemBudget = 225 * 1024;
 
-template <int BN, bool W4>
+template <int BN, bool W4, int KPS>
 struct TcCfg {
-  static constexpr int kBlkBytes = 128;                        // bytes of one row of a K block
-  static constexpr int kCols = W4 ? 64 : 128;                  // K columns per block
-  static constexpr int kXBytes = BN * kBlkBytes;               // token tile
-  static constexpr int kWBytes = W4 ? 4096 : 128 * kBlkBytes;  // packed codes / E4M3 weight tile
-  static constexpr int kMetaBytes = W4 ? 1024 : 0;             // scales (256) + zeros (64), padded
-  static constexpr int kStage = kXBytes + kWBytes + kMetaBytes;
-  static constexpr int kAStage = W4 ? 128 * kBlkBytes : 0;     // dequantised BF16 weight tile
-  static constexpr int kAStages = W4 ? 4 : 0;
+  static constexpr int kBlkBytes = 128;                         // bytes of one row of a K block
+  static constexpr int kCols = W4 ? 64 : 128;                   // K columns per block
+  static constexpr int kXBlk = BN * kBlkBytes;                  // token tile of one K block
+  static constexpr int kWBlk = W4 ? 4096 : 128 * kBlkBytes;     // packed codes / E4M3 tile of one K block
+  static constexpr int kGroupsPerStage = W4 ? (KPS >= 2 ? KPS / 2 : 1) : 0;
+  static constexpr int kScaleOff = KPS * kXBlk + KPS * kWBlk;   // scales, then zero-points (W4A16)
+  static constexpr int kZeroOff = kScaleOff + kGroupsPerStage * 256;
+  static constexpr int kMetaBytes = W4 ? ((kGroupsPerStage * 320 + 1023) / 1024) * 1024 : 0;
+  static constexpr int kStage = KPS * kXBlk + KPS * kWBlk + kMetaBytes;
+  static constexpr int kTxBytes = KPS * kXBlk + KPS * kWBlk + kGroupsPerStage * 320;
+  // dequantised BF16 weight tiles: in TMEM (tcgen05.st, read by the MMA as
+  // its A operand) when the accumulators leave room, else in shared memory
+  static constexpr bool kATmem = W4 && BN <= 128;
+  static constexpr int kAStages = W4 ? 4 : 0;                   // A slots (one 64-column block each)
+  static constexpr int kAStage = (W4 && !kATmem) ? 128 * kBlkBytes : 0;  // shared-memory bytes per slot
+  static constexpr int kASlotCols = 32;                         // TMEM columns per slot (64 BF16 per lane)
   static constexpr int kStagesRaw = (kSmemBudget - 2048 - kAStages * kAStage) / kStage;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
-  static constexpr int kAccCols = BN;                          // one accumulator
-  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+  static constexpr int kAccCols = BN;                           // one accumulator
+  static constexpr int kAColBase = 2 * BN;                      // first TMEM column of the A slots
+  static constexpr int kTmemNeed = 2 * BN + (kATmem ? kAStages * kASlotCols : 0);
+  static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                 : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kDqWarps = W4 ? 8 : 0;
   static constexpr int kEpiWarp0 = 2 + kDqWarps;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStage + kAStages * kAStage + 1024 /*barriers*/;
   static_assert(kStages >= 2, "pipeline too shallow");
-  static_assert(kXBytes % 1024 == 0 && kStage % 1024 == 0, "1024-byte alignment of swizzled tiles");
+  static_assert(kXBlk % 1024 == 0 && kStage % 1024 == 0, "1024-byte alignment of swizzled tiles");
+  static_assert(W4 || KPS == 1, "E4M3 stages hold one K block");
+  static_assert(kTmemNeed <= 512, "TMEM budget");
 };
 
 struct TcArgs {
@@ -67,7 +80,7 @@ struct TcArgs {
   int ntiles;        // N / 128
   int mblocks;       // token blocks
   int splits;        // K ranges per output tile
-  int kb_per_split;  // K blocks per range
+  int kb_per_split;  // K blocks per range (a multiple of the blocks per stage)
   int units;         // ntiles * mblocks * splits
 };
 
@@ -107,11 +120,11 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
   return r;
 }
 
-template <int BN, bool W4>
-__global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
+template <int BN, bool W4, int KPS>
+__global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ TcArgs a) {
-  using C = TcCfg<BN, W4>;
+  using C = TcCfg<BN, W4, KPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -158,6 +171,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) grid_dep_launch();  // the next kernel may start its prologue
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -165,29 +179,57 @@ __global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
       const int64_t ng = a.K / kGroup;
+      // weights never depend on the previous kernel: the first pass over the
+      // ring is filled with weight tiles before waiting for that kernel; the
+      // activation tiles follow once it has finished
+      auto load_w = [&](int s, const Unit& un, int j) {
+        uint8_t* st = ring + s * C::kStage;
+        const int kb = un.kb0 + j * KPS;
+        if constexpr (W4) {
+          const int64_t g0 = kb / 2;
+          bulk_load_hint(st + KPS * C::kXBlk, a.codes + (static_cast<int64_t>(un.nt) * KB + kb) * 4096,
+                         KPS * 4096, &full[s], pol_stream);
+          bulk_load(st + C::kScaleOff, a.scales + (static_cast<int64_t>(un.nt) * ng + g0) * kTileN,
+                    C::kGroupsPerStage * 256, &full[s]);
+          bulk_load(st + C::kZeroOff, a.zeros + (static_cast<int64_t>(un.nt) * ng + g0) * (kTileN / 2),
+                    C::kGroupsPerStage * 64, &full[s]);
+        } else {
+          tma_load_2d_hint(st + C::kXBlk, &tmap_w, &full[s], kb * C::kCols, un.nt * kTileN, pol_stream);
+        }
+      };
+      auto load_x = [&](int s, const Unit& un, int j) {
+        uint8_t* st = ring + s * C::kStage;
+        const int kb = un.kb0 + j * KPS;
+#pragma unroll
+        for (int i = 0; i < KPS; ++i)
+          tma_load_2d_hint(st + i * C::kXBlk, &tmap_x, &full[s], (kb + i) * C::kCols, un.mb * BN, pol_keep);
+      };
       int it = 0;
+      // phase 1: weights of the first ring pass
+      for (int u = blockIdx.x; u < a.units && it < C::kStages; u += gridDim.x) {
+        const Unit un = unit_of(a, u, KB);
+        for (int j = 0; j < un.nkb / KPS && it < C::kStages; ++j, ++it) {
+          mbar_arrive_expect_tx(&full[it], C::kTxBytes);
+          load_w(it, un, j);
+        }
+      }
+      const int prefilled = it;
+      grid_dep_wait();
+      it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         const Unit un = unit_of(a, u, KB);
-        for (int j = 0; j < un.nkb; ++j, ++it) {
+        for (int j = 0; j < un.nkb / KPS; ++j, ++it) {
           const int s = it % C::kStages;
-          if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
-            ok = false;
-            break;
+          if (it >= prefilled) {
+            if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+            load_w(s, un, j);
           }
-          uint8_t* st = ring + s * C::kStage;
-          const int kb = un.kb0 + j;
-          mbar_arrive_expect_tx(&full[s], C::kXBytes + (W4 ? 4096 + 256 + 64 : C::kWBytes));
-          tma_load_2d_hint(st, &tmap_x, &full[s], kb * C::kCols, un.mb * BN, pol_keep);
-          if constexpr (W4) {
-            const int64_t meta = static_cast<int64_t>(un.nt) * ng + kb / 2;
-            bulk_load_hint(st + C::kXBytes, a.codes + (static_cast<int64_t>(un.nt) * KB + kb) * 4096, 4096,
-                           &full[s], pol_stream);
-            bulk_load(st + C::kXBytes + 4096, a.scales + meta * kTileN, 256, &full[s]);
-            bulk_load(st + C::kXBytes + 4096 + 256, a.zeros + meta * (kTileN / 2), 64, &full[s]);
-          } else {
-            tma_load_2d_hint(st + C::kXBytes, &tmap_w, &full[s], kb * C::kCols, un.nt * kTileN, pol_stream);
-          }
+          load_x(s, un, j);
         }
       }
       if (!ok) {
@@ -199,7 +241,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = W4 ? idesc_make(1, 1, 128, BN) : idesc_make(0, 0, 128, BN);
-      int it = 0, ua = 0;
+      int it = 0, ait = 0, ua = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++ua) {
         const Unit un = unit_of(a, u, KB);
@@ -210,36 +252,41 @@ __global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + acc * C::kAccCols;
-        for (int j = 0; j < un.nkb; ++j, ++it) {
+        for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
             ok = false;
             break;
           }
-          uint32_t a_addr;
-          const int ai = W4 ? it % C::kAStages : 0;
-          if constexpr (W4) {
-            if (!mbar_wait(&a_full[ai], (it / C::kAStages) & 1, kWaitLimitNs, &s_abort)) {
-              ok = false;
-              break;
-            }
-            a_addr = smem_u32(aring + ai * C::kAStage);
-          } else {
-            a_addr = smem_u32(ring + s * C::kStage + C::kXBytes);
-          }
-          tc_fence_after();
-          const uint32_t b_addr = smem_u32(ring + s * C::kStage);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per MMA
-            const uint64_t ad = sdesc_sw128(a_addr + kk * 32);
-            const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
-            if constexpr (W4)
-              mma_f16(tmem_d, ad, bd, idesc, (j | kk) != 0);
-            else
-              mma_f8(tmem_d, ad, bd, idesc, (j | kk) != 0);
+          for (int i = 0; i < KPS; ++i, ++ait) {
+            uint32_t a_addr;
+            const int ai = W4 ? ait % C::kAStages : 0;
+            if constexpr (W4) {
+              if (!mbar_wait(&a_full[ai], (ait / C::kAStages) & 1, kWaitLimitNs, &s_abort)) {
+                ok = false;
+                break;
+              }
+              a_addr = C::kATmem ? tmem_base + C::kAColBase + ai * C::kASlotCols : smem_u32(aring + ai * C::kAStage);
+            } else {
+              a_addr = smem_u32(ring + s * C::kStage + KPS * C::kXBlk);
+            }
+            tc_fence_after();
+            const uint32_t b_addr = smem_u32(ring + s * C::kStage + i * C::kXBlk);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per MMA
+              const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
+              const uint32_t accum = (j | i | kk) != 0;
+              if constexpr (C::kATmem)
+                mma_f16_tmem_a(tmem_d, a_addr + kk * 8, bd, idesc, accum);  // 16 BF16 of K = 8 columns
+              else if constexpr (W4)
+                mma_f16(tmem_d, sdesc_sw128(a_addr + kk * 32), bd, idesc, accum);
+              else
+                mma_f8(tmem_d, sdesc_sw128(a_addr + kk * 32), bd, idesc, accum);
+            }
+            if constexpr (W4) mma_commit(&a_empty[ai]);
           }
           mma_commit(&empty[s]);
-          if constexpr (W4) mma_commit(&a_empty[ai]);
         }
         mma_commit(&acc_full[acc]);  // arrives when this unit's MMAs are done
       }
@@ -251,41 +298,70 @@ __global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
   } else if (warp < C::kEpiWarp0) {
     // ---------------------------------------------------------------- dequantisation (W4A16)
     if constexpr (W4) {
-      const int t = threadIdx.x - 64;  // 0..255
-      const int r = t & 127;           // weight row of the tile
-      const int h = t >> 7;            // which 32-column half of the 64-column block
-      int it = 0;
+      const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+      const int r = quad * 32 + lane;            // weight row of the tile
+      const int h = (warp - 2) >> 2;             // which 32-column half of each 64-column block
+      int it = 0, ait = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         const Unit un = unit_of(a, u, KB);
-        for (int j = 0; j < un.nkb; ++j, ++it) {
+        for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
           const int s = it % C::kStages;
-          const int ai = it % C::kAStages;
-          const bool got = mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort) &&
-                           mbar_wait(&a_empty[ai], ((it / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort);
-          if (!__all_sync(0xffffffffu, got)) {  // leave as a whole warp
-            ok = false;
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort))) {
+            ok = false;  // leave as a whole warp
             break;
           }
-          const uint8_t* st = ring + s * C::kStage + C::kXBytes;
-          const uint4 c = *reinterpret_cast<const uint4*>(st + h * 2048 + r * 16);
-          const float scale = __half2float(*reinterpret_cast<const __half*>(st + 4096 + r * 2));
-          const uint32_t zb = st[4096 + 256 + r / 2];
-          const float zq = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);  // this warp's codes are in registers
-          const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq);
-          const __nv_bfloat162 s2 = __float2bfloat162_rn(scale);
-          uint8_t* arow = aring + ai * C::kAStage + r * 128;
-          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+          const uint8_t* st = ring + s * C::kStage;
+          const int kb = un.kb0 + j * KPS;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 16-byte chunk cc holds columns 8cc..8cc+7
-            const int cc = h * 4 + q;
-            *reinterpret_cast<uint4*>(arow + ((cc ^ (r & 7)) << 4)) = dequant8(words[q], zoff, s2);
+          for (int i = 0; i < KPS; ++i, ++ait) {
+            const int ai = ait % C::kAStages;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&a_empty[ai], ((ait / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
+              ok = false;
+              break;
+            }
+            const uint4 c = *reinterpret_cast<const uint4*>(st + KPS * C::kXBlk + i * 4096 + h * 2048 + r * 16);
+            const int gi = (kb + i) / 2 - kb / 2;  // group of this block within the stage
+            const float scale = __half2float(*reinterpret_cast<const __half*>(st + C::kScaleOff + gi * 256 + r * 2));
+            const uint32_t zb = st[C::kZeroOff + gi * 64 + r / 2];
+            const float zq = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
+            if (i == KPS - 1) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
+            }
+            const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq);
+            const __nv_bfloat162 s2 = __float2bfloat162_rn(scale);
+            const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+            if constexpr (C::kATmem) {
+              // lane r of the slot holds row r: 32 columns x two BF16 = the 64 columns of the block
+              tc_fence_after();
+              uint32_t v[16];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 d = dequant8(words[q], zoff, s2);
+                v[4 * q + 0] = d.x;
+                v[4 * q + 1] = d.y;
+                v[4 * q + 2] = d.z;
+                v[4 * q + 3] = d.w;
+              }
+              tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
+                            h * 16,
+                        v);
+              tmem_st_wait();
+              tc_fence_before();
+            } else {
+              uint8_t* arow = aring + ai * C::kAStage + r * 128;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {  // 16-byte chunk cc holds columns 8cc..8cc+7
+                const int cc = h * 4 + q;
+                *reinterpret_cast<uint4*>(arow + ((cc ^ (r & 7)) << 4)) = dequant8(words[q], zoff, s2);
+              }
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[ai]);
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[ai]);
         }
       }
       if (!ok) {
@@ -295,6 +371,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
+    grid_dep_wait();  // outputs and the workspace may still be in use by the previous kernel
     const int t = threadIdx.x - C::kEpiWarp0 * 32;  // 0..127
     const int quad = warp & 3;                       // TMEM lane quadrant of this warp
     const float s_w = W4 ? 1.0f : *a.sw;
@@ -343,15 +420,27 @@ __global__ void __launch_bounds__(TcCfg<BN, W4>::kThreads, 1)
         const int64_t tile = static_cast<int64_t>(un.mb) * a.ntiles + un.nt;
         if (t == 0) s_last = !s_abort && (atomicAdd(a.counters + tile, 1u) == static_cast<uint32_t>(a.splits - 1));
         named_bar_epi();
-        const bool last = s_last != 0;
-        if (last) {
+        if (s_last) {
           __threadfence();
-          const int64_t mend = imin64(a.M, mbase + BN);
-          for (int64_t m = mbase; m < mend; ++m) {
-            float x = 0.0f;
-            for (int s = 0; s < a.splits; ++s)
-              x += __ldcg(a.partials + (static_cast<int64_t>(s) * a.M + m) * a.N + n);
-            a.Y[m * a.N + n] = W4 ? to_bf16(x) : to_bf16((x * __ldg(a.sx + m)) * s_w);
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            if (mbase + c0 >= a.M) break;
+            float acc_v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc_v[i] = 0.0f;
+            // 16 tokens x several splits of independent loads in flight per thread
+#pragma unroll 4
+            for (int s = 0; s < a.splits; ++s) {
+              const float* p = a.partials + (static_cast<int64_t>(s) * a.M + mbase + c0) * a.N + n;
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (mbase + c0 + i < a.M) acc_v[i] += __ldcg(p + static_cast<int64_t>(i) * a.N);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t m = mbase + c0 + i;
+              if (m < a.M) a.Y[m * a.N + n] = W4 ? to_bf16(acc_v[i]) : to_bf16((acc_v[i] * __ldg(a.sx + m)) * s_w);
+            }
           }
           if (t == 0) a.counters[tile] = 0u;
         }
@@ -397,19 +486,29 @@ static int pick_bn(int64_t M) {
   return 256;
 }
 
-static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols) {
+static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4) {
   TcPlan p;
   p.bn = pick_bn(M);
   p.mblocks = (M + p.bn - 1) / p.bn;
   const int64_t tiles = (N / kTileN) * p.mblocks;
   const int64_t KB = K / cols;
+  // K blocks per pipeline stage: small token tiles carry little activation
+  // data, so W4A16 stages bundle several 4 KB code blocks to keep enough bytes
+  // in flight per SM
+  p.kps = 1;
+  if (w4 && p.bn <= 32 && KB % 4 == 0) p.kps = 4;
+  else if (w4 && p.bn <= 64 && KB % 2 == 0) p.kps = 2;
+  const int64_t KS = KB / p.kps;  // stages along K
   // One persistent CTA per SM walks units round-robin.  Pick the split count
   // whose units spread most evenly over the SMs (units / (rounds x SMs)), with
   // at least 4 blocks of K per unit; on a tie take fewer splits (less
   // partial-sum traffic).
   int s = 1;
   double best = -1.0;
-  const int64_t max_s = KB / 4 > 0 ? (KB / 4 < 32 ? KB / 4 : 32) : 1;
+  const int64_t min_stages = (4 + p.kps - 1) / p.kps;
+  int64_t max_s = KS / min_stages;
+  if (max_s < 1) max_s = 1;
+  if (max_s > 32) max_s = 32;
   for (int c = 1; c <= max_s; ++c) {
     const int64_t units = tiles * c;
     const int64_t rounds = (units + num_sms - 1) / num_sms;
@@ -419,23 +518,23 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols) {
       s = c;
     }
   }
-  const int per = static_cast<int>((KB + s - 1) / s);
-  s = static_cast<int>((KB + per - 1) / per);
+  const int per = static_cast<int>((KS + s - 1) / s);  // stages per split
+  s = static_cast<int>((KS + per - 1) / per);
   p.split.splits = s;
-  p.split.kb_per_split = per;
+  p.split.kb_per_split = per * p.kps;
   p.split.tiles = tiles;
   p.split.ws_bytes = s > 1 ? counters_bytes(tiles) + sizeof(float) * static_cast<size_t>(s) * M * N : 0;
   return p;
 }
 
-TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 64); }
-TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128); }
+TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 64, true); }
+TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false); }
 
-template <int BN, bool W4>
+template <int BN, bool W4, int KPS>
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, TcArgs args, const TcPlan& plan,
                              void* ws, int num_sms, cudaStream_t st) {
-  using C = TcCfg<BN, W4>;
-  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4>, C::kSmemBytes);
+  using C = TcCfg<BN, W4, KPS>;
+  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   args.counters = static_cast<uint32_t*>(ws);
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.split.tiles)) : nullptr;
@@ -445,8 +544,39 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, TcArg
   args.kb_per_split = plan.split.kb_per_split;
   args.units = static_cast<int>(plan.split.tiles * plan.split.splits);
   const int grid = args.units < num_sms ? args.units : num_sms;
-  tc_gemm_kernel<BN, W4><<<grid, C::kThreads, C::kSmemBytes, st>>>(tx, tw, args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the previous kernel's tail
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS>, tx, tw, args);
+}
+
+template <bool W4>
+static cudaError_t launch_tc_bn(const CUtensorMap& tx, const CUtensorMap& tw, const TcArgs& a, const TcPlan& plan,
+                                void* ws, int num_sms, cudaStream_t st) {
+  if constexpr (W4) {
+    if (plan.bn == 16) return plan.kps == 4 ? launch_tc<16, true, 4>(tx, tw, a, plan, ws, num_sms, st)
+                                            : launch_tc<16, true, 2>(tx, tw, a, plan, ws, num_sms, st);
+    if (plan.bn == 32) return plan.kps == 4 ? launch_tc<32, true, 4>(tx, tw, a, plan, ws, num_sms, st)
+                                            : launch_tc<32, true, 2>(tx, tw, a, plan, ws, num_sms, st);
+    if (plan.bn == 64) return launch_tc<64, true, 2>(tx, tw, a, plan, ws, num_sms, st);
+    if (plan.bn == 128) return launch_tc<128, true, 1>(tx, tw, a, plan, ws, num_sms, st);
+    return launch_tc<256, true, 1>(tx, tw, a, plan, ws, num_sms, st);
+  } else {
+    switch (plan.bn) {
+      case 16: return launch_tc<16, false, 1>(tx, tw, a, plan, ws, num_sms, st);
+      case 32: return launch_tc<32, false, 1>(tx, tw, a, plan, ws, num_sms, st);
+      case 64: return launch_tc<64, false, 1>(tx, tw, a, plan, ws, num_sms, st);
+      case 128: return launch_tc<128, false, 1>(tx, tw, a, plan, ws, num_sms, st);
+      default: return launch_tc<256, false, 1>(tx, tw, a, plan, ws, num_sms, st);
+    }
+  }
 }
 
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
@@ -464,13 +594,7 @@ cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint1
   a.M = M;
   a.N = N;
   a.K = K;
-  switch (plan.bn) {
-    case 16: return launch_tc<16, true>(tx, tx, a, plan, ws, num_sms, st);
-    case 32: return launch_tc<32, true>(tx, tx, a, plan, ws, num_sms, st);
-    case 64: return launch_tc<64, true>(tx, tx, a, plan, ws, num_sms, st);
-    case 128: return launch_tc<128, true>(tx, tx, a, plan, ws, num_sms, st);
-    default: return launch_tc<256, true>(tx, tx, a, plan, ws, num_sms, st);
-  }
+  return launch_tc_bn<true>(tx, tx, a, plan, ws, num_sms, st);
 }
 
 cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
@@ -487,13 +611,7 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
   a.M = M;
   a.N = N;
   a.K = K;
-  switch (plan.bn) {
-    case 16: return launch_tc<16, false>(tx, tw, a, plan, ws, num_sms, st);
-    case 32: return launch_tc<32, false>(tx, tw, a, plan, ws, num_sms, st);
-    case 64: return launch_tc<64, false>(tx, tw, a, plan, ws, num_sms, st);
-    case 128: return launch_tc<128, false>(tx, tw, a, plan, ws, num_sms, st);
-    default: return launch_tc<256, false>(tx, tw, a, plan, ws, num_sms, st);
-  }
+  return launch_tc_bn<false>(tx, tw, a, plan, ws, num_sms, st);
 }
 
 }  // namespace qlin
