@@ -33,7 +33,6 @@ constexpr int kMmaCodeBytes = 4 * 4096;            // codes of one stage
 constexpr int kMmaMetaOff = kMmaCodeBytes;         // 2 groups x 128 FP16 scales, then 2 x 64 B zeros
 constexpr int kMmaXOff = kMmaCodeBytes + 1024;     // activation rows
 constexpr int kMmaXRow = kMmaStageCols * 2 + 16;   // 528 B per token row (conflict-free B fragments)
-constexpr int kMmaStages = 4;
 constexpr int kMmaConsumers = 8;                   // consumer warps, 16 rows (one m16 block) each
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 constexpr uint64_t kMmaWaitNs = 2000000000ull;
@@ -42,7 +41,8 @@ template <int NT>
 struct MmaCfg {
   static constexpr int kTok = 8 * NT;
   static constexpr int kStage = ((kMmaXOff + kTok * kMmaXRow) + 1023) / 1024 * 1024;
-  static constexpr int kSmem = 1024 + kMmaStages * kStage + 256;
+  static constexpr int kStages = NT == 1 ? 3 : 4;  // M <= 8: three CTAs fit per SM
+  static constexpr int kSmem = 1024 + kStages * kStage + 256;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -54,9 +54,9 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 }
 
 // Pair (2p, 2p+1) of a packed word as BF16x2 (128 + q): nibble positions p and
-// 4 + p hold the two columns (tile layout v1).
-__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
-  return ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+// 4 + p hold the two columns (tile layout v1); `sh` = 4p.
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, uint32_t sh) {
+  return ((w >> sh) & 0x000F000Fu) | 0x43004300u;
 }
 
 template <int NT>  // n8 token blocks: M <= 8 * NT
@@ -67,8 +67,8 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
   using C = MmaCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kMmaStages * C::kStage);
-  uint64_t* empty = full + kMmaStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kStages * C::kStage);
+  uint64_t* empty = full + C::kStages;
   __shared__ int s_last;
   __shared__ volatile int s_abort;
 
@@ -82,19 +82,26 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
   const int mrows = static_cast<int>(imin64(M, C::kTok));
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kMmaStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kMmaConsumers);
     }
     fence_mbar_init();
     s_abort = 0;
   }
+  // token rows >= M are never copied: zero them once so B fragments need no bounds test
+  for (int idx = threadIdx.x; idx < C::kStages * (C::kTok - mrows) * (kMmaXRow / 16); idx += kMmaThreads) {
+    const int per = (C::kTok - mrows) * (kMmaXRow / 16);
+    const int stg = idx / per, rem = idx % per;
+    const int row = mrows + rem / (kMmaXRow / 16), c16 = rem % (kMmaXRow / 16);
+    *reinterpret_cast<uint4*>(ring + stg * C::kStage + kMmaXOff + row * kMmaXRow + c16 * 16) = make_uint4(0, 0, 0, 0);
+  }
   __syncthreads();
 
   const uint32_t tx = kMmaCodeBytes + 2 * 256 + 2 * 64 + mrows * kMmaStageCols * 2;
-  auto issue_w = [&](int i) {  // weights of stage i (ring slot i % kMmaStages)
-    uint8_t* st = ring + (i % kMmaStages) * C::kStage;
-    uint64_t* bar = &full[i % kMmaStages];
+  auto issue_w = [&](int i) {  // weights of stage i (ring slot i % C::kStages)
+    uint8_t* st = ring + (i % C::kStages) * C::kStage;
+    uint64_t* bar = &full[i % C::kStages];
     const int64_t kb = static_cast<int64_t>(s0 + i) * 4;  // first 64-column block
     const int64_t g0 = kb / 2;
     mbar_arrive_expect_tx(bar, tx);
@@ -103,14 +110,14 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
     bulk_load(st + kMmaMetaOff + 512, zeros + (static_cast<int64_t>(nt) * ngK + g0) * (kTileN / 2), 2 * 64, bar);
   };
   auto issue_x = [&](int i) {  // activation rows of stage i
-    uint8_t* st = ring + (i % kMmaStages) * C::kStage;
+    uint8_t* st = ring + (i % C::kStages) * C::kStage;
     const int64_t k0 = static_cast<int64_t>(s0 + i) * kMmaStageCols;
     for (int m = 0; m < mrows; ++m)
-      bulk_load(st + kMmaXOff + m * kMmaXRow, X + m * K + k0, kMmaStageCols * 2, &full[i % kMmaStages]);
+      bulk_load(st + kMmaXOff + m * kMmaXRow, X + m * K + k0, kMmaStageCols * 2, &full[i % C::kStages]);
   };
   // weights never depend on the previous kernel on the stream: start them first
   if (warp == kMmaConsumers && lane == 0)
-    for (int i = 0; i < nst && i < kMmaStages; ++i) issue_w(i);
+    for (int i = 0; i < nst && i < C::kStages; ++i) issue_w(i);
   grid_dep_wait();
   grid_dep_launch();
 
@@ -124,9 +131,9 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
   if (warp == kMmaConsumers) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int i = 0; i < nst && i < kMmaStages; ++i) issue_x(i);
-      for (int i = kMmaStages; i < nst; ++i) {
-        if (!mbar_wait(&empty[i % kMmaStages], ((i / kMmaStages) & 1) ^ 1, kMmaWaitNs, &s_abort)) {
+      for (int i = 0; i < nst && i < C::kStages; ++i) issue_x(i);
+      for (int i = C::kStages; i < nst; ++i) {
+        if (!mbar_wait(&empty[i % C::kStages], ((i / C::kStages) & 1) ^ 1, kMmaWaitNs, &s_abort)) {
           set_error(err, QLIN_ERR_TIMEOUT);
           s_abort = 1;
           break;
@@ -138,10 +145,12 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
   } else {
     // ------------------------------------------------------------ consumers: rows 16*warp .. 16*warp + 15
     const int r0 = warp * 16 + gq;  // this thread's rows: r0 and r0 + 8
+    const uint32_t sh = 4u * static_cast<uint32_t>(tq);
+    const int xoff = kMmaXOff + gq * kMmaXRow + 4 * tq;  // B fragment of token gq, columns 2t, 2t+1
     const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // BF16 1.0 pairs
     for (int i = 0; i < nst; ++i) {
-      const int slot = i % kMmaStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / kMmaStages) & 1, kMmaWaitNs, &s_abort))) {
+      const int slot = i % C::kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort))) {
         set_error(err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
         break;
@@ -178,21 +187,15 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
             uint32_t b[NT][2];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-              const int tok = j * 8 + gq;
-              if (tok < mrows) {
-                const uint8_t* xr = st + kMmaXOff + tok * kMmaXRow + (kbl * 64 + ks * 16 + 2 * tq) * 2;
-                b[j][0] = *reinterpret_cast<const uint32_t*>(xr);
-                b[j][1] = *reinterpret_cast<const uint32_t*>(xr + 16);
-              } else {
-                b[j][0] = 0u;
-                b[j][1] = 0u;
-              }
+              const uint8_t* xr = st + xoff + j * 8 * kMmaXRow + (kbl * 64 + ks * 16) * 2;
+              b[j][0] = *reinterpret_cast<const uint32_t*>(xr);
+              b[j][1] = *reinterpret_cast<const uint32_t*>(xr + 16);
             }
             uint32_t a[4];
-            a[0] = nib_pair_bf16(wr0[2 * ks], tq);      // row r0,   columns 2t, 2t+1
-            a[1] = nib_pair_bf16(wr1[2 * ks], tq);      // row r0+8, columns 2t, 2t+1
-            a[2] = nib_pair_bf16(wr0[2 * ks + 1], tq);  // row r0,   columns 2t+8, 2t+9
-            a[3] = nib_pair_bf16(wr1[2 * ks + 1], tq);  // row r0+8, columns 2t+8, 2t+9
+            a[0] = nib_pair_bf16(wr0[2 * ks], sh);      // row r0,   columns 2t, 2t+1
+            a[1] = nib_pair_bf16(wr1[2 * ks], sh);      // row r0+8, columns 2t, 2t+1
+            a[2] = nib_pair_bf16(wr0[2 * ks + 1], sh);  // row r0,   columns 2t+8, 2t+9
+            a[3] = nib_pair_bf16(wr1[2 * ks + 1], sh);  // row r0+8, columns 2t+8, 2t+9
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
               mma_bf16_16816(c[kb2][j], a, b[j][0], b[j][1]);
@@ -264,13 +267,16 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
   if (threadIdx.x == 0) counters[nt] = 0u;
 }
 
-// Split K only for parallelism: about two CTAs per SM.
+// Split K only for parallelism: about as many CTAs as fit on the SMs at once.
 SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
   SplitPlan p;
-  (void)M;
   const int64_t tiles = N / kTileN;
   const int64_t KS = K / kMmaStageCols;
-  int64_t s = (2LL * num_sms + tiles - 1) / tiles;
+  const int64_t per_sm = M <= 8 ? 3 : 2;
+  int64_t s = (per_sm * num_sms + tiles - 1) / tiles;
+  // FP32 partial sums (written and read back once) at most a quarter of the weight bytes
+  const int64_t cap = static_cast<int64_t>(0.25 * 0.51953125 * static_cast<double>(K) / (8.0 * static_cast<double>(M)));
+  if (s > cap) s = cap;
   if (s > KS) s = KS;
   if (s < 1) s = 1;
   const int64_t per = (KS + s - 1) / s;

@@ -20,6 +20,9 @@
 // dequantisation warps (W4A16) fill a second ring with BF16 weight tiles; four
 // epilogue warps drain the other accumulator meanwhile.  Every wait is bounded
 // in time; on expiry the kernel records QLIN_ERR_TIMEOUT and leaves.
+#include <cmath>
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -82,6 +85,8 @@ struct TcArgs {
   int splits;        // K ranges per output tile
   int kb_per_split;  // K blocks per range (a multiple of the blocks per stage)
   int units;         // ntiles * mblocks * splits
+  int mb_fast;       // unit order: token block fastest (weights streamed once) or weight tile fastest
+  int x_keep;        // keep activation tiles in L2 (evict-last) when they are small
 };
 
 __device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
@@ -103,8 +108,12 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 zoff, __nv_
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Work unit u -> (n tile, token block, K range); the n tile varies fastest so
-// that the CTAs working at the same time share one activation block.
+// Work unit u -> (n tile, token block, K range).  When the weights fit in L2
+// the weight tile varies fastest (the weights stay resident and each
+// activation block is streamed once); otherwise tiles are taken in groups of
+// kRasterN weight tiles x every token block, token block fastest, so that the
+// activations stay resident and each weight tile is streamed once.
+constexpr int kRasterN = 16;
 struct Unit {
   int nt, mb, split, kb0, nkb;
 };
@@ -112,8 +121,16 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
   Unit r;
   r.split = u % a.splits;
   const int tile = u / a.splits;
-  r.nt = tile % a.ntiles;
-  r.mb = tile / a.ntiles;
+  if (a.mb_fast) {
+    const int gsz = kRasterN * a.mblocks;
+    const int g = tile / gsz, rem = tile % gsz;
+    const int gn = a.ntiles - g * kRasterN < kRasterN ? a.ntiles - g * kRasterN : kRasterN;  // tiles in this group
+    r.mb = rem % a.mblocks;
+    r.nt = g * kRasterN + (rem / a.mblocks) % gn;
+  } else {
+    r.nt = tile % a.ntiles;
+    r.mb = tile / a.ntiles;
+  }
   r.kb0 = r.split * a.kb_per_split;
   const int64_t end = imin64(KB, static_cast<int64_t>(r.kb0) + a.kb_per_split);
   r.nkb = static_cast<int>(end - r.kb0);
@@ -177,7 +194,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();
+      const uint64_t pol_keep = a.x_keep ? policy_evict_last() : policy_evict_normal();
       const int64_t ng = a.K / kGroup;
       // weights never depend on the previous kernel: the first pass over the
       // ring is filled with weight tiles before waiting for that kernel; the
@@ -499,22 +516,36 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bo
   if (w4 && p.bn <= 32 && KB % 4 == 0) p.kps = 4;
   else if (w4 && p.bn <= 64 && KB % 2 == 0) p.kps = 2;
   const int64_t KS = KB / p.kps;  // stages along K
-  // One persistent CTA per SM walks units round-robin.  Pick the split count
-  // whose units spread most evenly over the SMs (units / (rounds x SMs)), with
-  // at least 4 blocks of K per unit; on a tie take fewer splits (less
-  // partial-sum traffic).
-  int s = 1;
-  double best = -1.0;
+  // Split K by a small cost model: the time of a split count c is the larger
+  // of the memory time (all bytes at the HBM rate, or one unit's bytes at a
+  // single SM's streaming rate, times the rounds of units per SM) and the MMA
+  // time (rounds x one unit's FLOPs at one SM's rate), plus a fixed cost for
+  // the partial-sum fix-up when c > 1.  Partial sums are FP32, written and read
+  // back once.  At least 4 blocks of K per unit; fewer splits on a tie.
+  const double wbytes = static_cast<double>(N) * static_cast<double>(K) * (w4 ? 0.51953125 : 1.0);
+  const double xbytes = static_cast<double>(M) * static_cast<double>(K) * (w4 ? 2.0 : 1.0);
+  const double ybytes = 2.0 * static_cast<double>(M) * static_cast<double>(N);
+  const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
+  const double hbm = 6.5e12, sm_stream = 80e9;
+  const double sm_mma = (w4 ? 1.9e15 : 3.9e15) * 0.7 / num_sms;
   const int64_t min_stages = (4 + p.kps - 1) / p.kps;
   int64_t max_s = KS / min_stages;
   if (max_s < 1) max_s = 1;
   if (max_s > 32) max_s = 32;
+  if (p.bn >= 128 && max_s > 2) max_s = 2;  // wide token tiles: the fix-up of many partials costs more than it gains
+  if (tiles >= num_sms) max_s = 1;          // enough tiles for every SM: splitting only adds partial-sum traffic
+  int s = 1;
+  double best = 1e30;
   for (int c = 1; c <= max_s; ++c) {
-    const int64_t units = tiles * c;
-    const int64_t rounds = (units + num_sms - 1) / num_sms;
-    const double eff = static_cast<double>(units) / static_cast<double>(rounds * num_sms);
-    if (eff > best + 0.02) {
-      best = eff;
+    const double units = static_cast<double>(tiles) * c;
+    const double rounds = std::ceil(units / num_sms);
+    const double partial = c > 1 ? 8.0 * c * static_cast<double>(M) * static_cast<double>(N) : 0.0;
+    const double bytes = wbytes * static_cast<double>(p.mblocks > 4 ? 1 : p.mblocks) + xbytes + ybytes + partial;
+    const double t_mem = std::max(bytes / hbm, rounds * (bytes / units) / sm_stream);
+    const double t_mma = rounds * (flops / units) / sm_mma;
+    const double t = std::max(t_mem, t_mma) + (c > 1 ? 2e-6 : 0.0);
+    if (t < best * 0.97) {
+      best = t;
       s = c;
     }
   }
@@ -543,6 +574,13 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, TcArg
   args.splits = plan.split.splits;
   args.kb_per_split = plan.split.kb_per_split;
   args.units = static_cast<int>(plan.split.tiles * plan.split.splits);
+  {
+    const double l2_half = 63.0 * 1024 * 1024;  // half of the 126 MB L2
+    const double wb = static_cast<double>(args.N) * static_cast<double>(args.K) * (W4 ? 0.51953125 : 1.0);
+    const double xb = static_cast<double>(args.M) * static_cast<double>(args.K) * (W4 ? 2.0 : 1.0);
+    args.mb_fast = (wb > l2_half && xb < wb) ? 1 : 0;
+    args.x_keep = xb <= l2_half / 2 ? 1 : 0;
+  }
   const int grid = args.units < num_sms ? args.units : num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
