@@ -50,6 +50,15 @@ def w8_alg_bytes(M, N, K):
     return N * K + M * K + 4 * M + 4 + 2 * M * N
 
 
+# DRAM traffic of the small-M W4A16 kernel from one ncu capture (profiles/
+# w4a16_mma_splitk_m1_gateup_4096x28672.md): dram__bytes_read.sum + dram__bytes_write.sum
+# for M = 1, K = 4096, N = 28672, against that launch's algorithmic bytes.  The
+# traffic of a bench launch is scaled from it by its algorithmic bytes (traffic grows
+# in proportion: the weights are streamed once).
+TRAFFIC_CAPTURE = {"kernel": "w4a16_mma_splitk", "dram_bytes": 61046272 + 121856,
+                   "alg_bytes": 28672 * 4096 // 2 + 2 * 28672 * 32 + 28672 * 32 // 2 + 2 * 4096 + 2 * 28672}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -330,7 +339,11 @@ def run_ours(args):
                    (ROTATE * weight_bytes / 1e6 / len(MS_DECODE)), "timing": "CUDA graph per step, CUDA events; per-kernel times from an event-instrumented replay of the same graphs"},
         "per_M_weight_gbs": per_m_gbs,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": (round(TRAFFIC_CAPTURE["dram_bytes"] / TRAFFIC_CAPTURE["alg_bytes"]
+                                       * dk["bytes"] / dk["launches"])
+                                 if dom == TRAFFIC_CAPTURE["kernel"] else None),
+                     "traffic_note": "bytes per launch, scaled from one ncu capture (M=1, 4096x28672)",
                      "peak_source": peaks["source"], "launches_timed": dk["launches"],
                      "share_of_step": round(dk["ms"] / sum(v["ms"] for v in per_kernel.values()), 3)},
         "kernels": {k: {"ms_per_launch": round(v["ms"] / v["launches"], 5), "launches": v["launches"],
@@ -494,6 +507,33 @@ def time_launches(launches, reps=10, warm=3):
     return e0.elapsed_time(e1) / (reps * len(launches)) * 1e3   # microseconds
 
 
+def crossover_summary(rows, p16_tf, p8_tf, bw_gbs):
+    """Measured W4A16-vs-W8A8 crossover M (W8A8 counted as activation quantisation + GEMM)
+    beside the roofline predictions of the arithmetic-intensity argument."""
+    out = {"crossover": []}
+    for (K, N) in sorted({(r["K"], r["N"]) for r in rows}):
+        w4 = {r["M"]: r["us"] for r in rows if (r["K"], r["N"]) == (K, N) and r["variant"] == "w4"}
+        w8 = {r["M"]: r["us"] + r.get("quant_us", 0.0) for r in rows if (r["K"], r["N"]) == (K, N) and r["variant"] == "w8"}
+        ms = sorted(set(w4) & set(w8))
+        measured = next((m for m in ms if w8[m] <= w4[m] and all(w8[x] <= w4[x] for x in ms if x >= m)), None)
+
+        def t4(m):
+            return max(2 * m * N * K / (p16_tf * 1e12), w4_alg_bytes(m, N, K) / (bw_gbs * 1e9))
+
+        def t8(m, with_quant):
+            t = max(2 * m * N * K / (p8_tf * 1e12), w8_alg_bytes(m, N, K) / (bw_gbs * 1e9))
+            return t + (3 * m * K + 4 * m) / (bw_gbs * 1e9) if with_quant else t
+        pred_gemm = next((m for m in range(1, 8193) if t8(m, False) <= t4(m)), None)
+        pred_quant = next((m for m in range(1, 8193) if t8(m, True) <= t4(m)), None)
+        out["crossover"].append({
+            "K": K, "N": N, "measured_M": measured,
+            "measured_us": {str(m): [round(w4[m], 2), round(w8[m], 2)] for m in ms},
+            "roofline_M_gemm_only": pred_gemm, "roofline_M_with_act_quant": pred_quant,
+            "simplified_P16_over_2BW": round(p16_tf * 1e12 / (2 * bw_gbs * 1e9), 1),
+            "w4a16_transition_M": round((p16_tf * 1e12 / (bw_gbs * 1e9)) * 0.51953125 / 2, 1)})
+    return out
+
+
 def run_sweep(args):
     import torch
 
@@ -512,6 +552,7 @@ def run_sweep(args):
     print(json.dumps({"peaks": peaks, "fp8_probe_tflops": p8, "l2_bytes": l2}), flush=True)
     p8_use = p8 if p8 else 2 * p16
 
+    results = []
     if args.sweep == "crossover":
         shapes = [(4096, 14336), (14336, 4096)]
         plan = [("w4", M) for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)] + \
@@ -575,8 +616,11 @@ def run_sweep(args):
                            fp8_peak="probe" if p8 else "2x bf16 (assumed)")
             assert q.qlin_get_device_error() == 0
             print(json.dumps(row), flush=True)
+            results.append(row)
         del lin4, lin8, sets4, sets8
         torch.cuda.empty_cache()
+    if args.sweep == "crossover":
+        print(json.dumps(crossover_summary(results, p16, p8_use, bw)), flush=True)
 
 
 def run_case(args):

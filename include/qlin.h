@@ -191,9 +191,9 @@ int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
  * allocation after start-up, a host that must keep a fixed footprint).
  * Same arguments and result as qlin_w4a16_gemm_ex(..., QLIN_PATH_GEMV, ...)
  * but without a workspace: the split-K partial sums live in one scratch array
- * of 4 MiB inside the library image (a file-scope __device__ array that every
+ * of 8 MiB inside the library image (a file-scope __device__ array that every
  * GPU which loads the library holds until the process exits).
- *  - Sizes whose split-K partial sums need more than 4 MiB are rejected with
+ *  - Sizes whose split-K partial sums need more than 8 MiB are rejected with
  *    QLIN_ERR_WORKSPACE_TOO_SMALL before anything is launched.  With the
  *    current split choice this accepts every M <= 16 on the Llama-3-8B and
  *    Llama-3-70B layer shapes.

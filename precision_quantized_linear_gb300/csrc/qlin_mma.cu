@@ -53,6 +53,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Same with a zero accumulator (starts a chain without clearing registers).
+__device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 // Pair (2p, 2p+1) of a packed word as BF16x2 (128 + q): nibble positions p and
 // 4 + p hold the two columns (tile layout v1); `sh` = 4p.
 __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, uint32_t sh) {
@@ -146,6 +155,9 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
     // ------------------------------------------------------------ consumers: rows 16*warp .. 16*warp + 15
     const int r0 = warp * 16 + gq;  // this thread's rows: r0 and r0 + 8
     const uint32_t sh = 4u * static_cast<uint32_t>(tq);
+    // zero-point nibble of rows r0, r0+8 (same parity): moved to bits 16..19 of an FP32
+    // whose exponent is 2^7, which reads as 128 + z exactly
+    const uint32_t zsh = (r0 & 1) ? 12u : 16u;
     const int xoff = kMmaXOff + gq * kMmaXRow + 4 * tq;  // B fragment of token gq, columns 2t, 2t+1
     const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // BF16 1.0 pairs
     for (int i = 0; i < nst; ++i) {
@@ -155,31 +167,22 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
         s_abort = 1;
         break;
       }
-      const uint8_t* st = ring + slot * C::kStage;
-      const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kMmaMetaOff);
-      const uint8_t* zp = st + kMmaMetaOff + 512;
+      const uint32_t st = smem_u32(ring + slot * C::kStage);  // shared-space address of the stage
+      const uint32_t sc = st + kMmaMetaOff;                   // FP16 scales [2][128]
+      const uint32_t zp = st + kMmaMetaOff + 512;             // zero nibbles [2][64]
 #pragma unroll 1
       for (int grp = 0; grp < 2; ++grp) {
         // two accumulators (one per 64-column block) keep two MMA chains in flight
         float c[2][NT][4];
         float xs[2][NT][4];  // sum_k x over each block, from the ones block (rows all equal)
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-          for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              c[h2][j][e] = 0.0f;
-              xs[h2][j][e] = 0.0f;
-            }
-#pragma unroll
         for (int kb2 = 0; kb2 < 2; ++kb2) {
           const int kbl = grp * 2 + kb2;  // 64-column block within the stage
-          const uint8_t* tile = st + kbl * 4096;
-          const uint4 w00 = *reinterpret_cast<const uint4*>(tile + r0 * 16);         // half 0, row r0
-          const uint4 w01 = *reinterpret_cast<const uint4*>(tile + (r0 + 8) * 16);   // half 0, row r0+8
-          const uint4 w10 = *reinterpret_cast<const uint4*>(tile + 2048 + r0 * 16);  // half 1
-          const uint4 w11 = *reinterpret_cast<const uint4*>(tile + 2048 + (r0 + 8) * 16);
+          const uint32_t tile = st + kbl * 4096;
+          const uint4 w00 = lds128(tile + r0 * 16);          // half 0, row r0
+          const uint4 w01 = lds128(tile + (r0 + 8) * 16);    // half 0, row r0+8
+          const uint4 w10 = lds128(tile + 2048 + r0 * 16);   // half 1
+          const uint4 w11 = lds128(tile + 2048 + (r0 + 8) * 16);
           const uint32_t wr0[8] = {w00.x, w00.y, w00.z, w00.w, w10.x, w10.y, w10.z, w10.w};
           const uint32_t wr1[8] = {w01.x, w01.y, w01.z, w01.w, w11.x, w11.y, w11.z, w11.w};
 #pragma unroll
@@ -187,9 +190,9 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
             uint32_t b[NT][2];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-              const uint8_t* xr = st + xoff + j * 8 * kMmaXRow + (kbl * 64 + ks * 16) * 2;
-              b[j][0] = *reinterpret_cast<const uint32_t*>(xr);
-              b[j][1] = *reinterpret_cast<const uint32_t*>(xr + 16);
+              const uint32_t xr = st + xoff + j * 8 * kMmaXRow + (kbl * 64 + ks * 16) * 2;
+              b[j][0] = lds32(xr);
+              b[j][1] = lds32(xr + 16);
             }
             uint32_t a[4];
             a[0] = nib_pair_bf16(wr0[2 * ks], sh);      // row r0,   columns 2t, 2t+1
@@ -198,25 +201,34 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
             a[3] = nib_pair_bf16(wr1[2 * ks + 1], sh);  // row r0+8, columns 2t+8, 2t+9
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-              mma_bf16_16816(c[kb2][j], a, b[j][0], b[j][1]);
-              mma_bf16_16816(xs[kb2][j], ones, b[j][0], b[j][1]);
+              if (ks == 0) {  // first k-step of the block starts both chains from zero
+                mma_bf16_16816_z(c[kb2][j], a, b[j][0], b[j][1]);
+                mma_bf16_16816_z(xs[kb2][j], ones, b[j][0], b[j][1]);
+              } else {
+                mma_bf16_16816(c[kb2][j], a, b[j][0], b[j][1]);
+                mma_bf16_16816(xs[kb2][j], ones, b[j][0], b[j][1]);
+              }
             }
           }
         }
         // fold: y += s (sum x (128 + q) - (128 + z) sum x); rows r0, r0+8; tokens 8j+2t, +1
+        float xv[NT][2];
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) xv[j][e] = xs[0][j][e] + xs[1][j][e];
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = r0 + hr * 8;
-          const float s = __half2float(__ushort_as_half(sc[grp * kTileN + r]));
-          const uint32_t zb = zp[grp * (kTileN / 2) + r / 2];
-          const float cz = 128.0f + static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
+          const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(sc + (grp * kTileN + r) * 2))));
+          const uint32_t zb = lds8(zp + grp * (kTileN / 2) + r / 2);
+          const float cz = __uint_as_float(((zb << zsh) & 0x000F0000u) | 0x43000000u);
 #pragma unroll
           for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const float cs = c[0][j][hr * 2 + e] + c[1][j][hr * 2 + e];
-              const float xv = xs[0][j][e] + xs[1][j][e];
-              acc[j][hr * 2 + e] = fmaf(s, fmaf(-cz, xv, cs), acc[j][hr * 2 + e]);
+              acc[j][hr * 2 + e] = fmaf(s, fmaf(-cz, xv[j][e], cs), acc[j][hr * 2 + e]);
             }
         }
       }
@@ -267,18 +279,32 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
   if (threadIdx.x == 0) counters[nt] = 0u;
 }
 
-// Split K only for parallelism: about as many CTAs as fit on the SMs at once.
+// Split K only for parallelism: the split count whose CTAs fill whole waves of
+// the resident CTA slots best (three per SM for M <= 8, two otherwise), with
+// the FP32 partial sums (written and read back once) at most a quarter of the
+// weight bytes; fewer splits on a near tie.
 SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
   SplitPlan p;
   const int64_t tiles = N / kTileN;
   const int64_t KS = K / kMmaStageCols;
-  const int64_t per_sm = M <= 8 ? 3 : 2;
-  int64_t s = (per_sm * num_sms + tiles - 1) / tiles;
-  // FP32 partial sums (written and read back once) at most a quarter of the weight bytes
-  const int64_t cap = static_cast<int64_t>(0.25 * 0.51953125 * static_cast<double>(K) / (8.0 * static_cast<double>(M)));
-  if (s > cap) s = cap;
-  if (s > KS) s = KS;
-  if (s < 1) s = 1;
+  const int64_t slots = (M <= 8 ? 3 : 2) * static_cast<int64_t>(num_sms);
+  int64_t cap = static_cast<int64_t>(0.25 * 0.51953125 * static_cast<double>(K) / (8.0 * static_cast<double>(M)));
+  if (cap > KS) cap = KS;
+  if (cap > 32) cap = 32;
+  if (cap < 1) cap = 1;
+  int64_t s = 1;
+  double best = -1.0;
+  for (int64_t c = 1; c <= cap; ++c) {
+    const int64_t per = (KS + c - 1) / c;
+    const int64_t real = (KS + per - 1) / per;  // splits actually formed
+    const int64_t ctas = tiles * real;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const double eff = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+    if (eff > best + 0.02) {
+      best = eff;
+      s = real;
+    }
+  }
   const int64_t per = (KS + s - 1) / s;
   s = (KS + per - 1) / per;
   p.splits = static_cast<int>(s);

@@ -14,7 +14,7 @@ namespace qlin {
 
 // Fixed scratch of the no-allocation entry point.  Every GPU that loads the
 // library holds these bytes until the process exits.
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 static std::mutex g_noalloc_mu;

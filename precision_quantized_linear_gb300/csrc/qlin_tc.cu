@@ -338,10 +338,12 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
               ok = false;
               break;
             }
-            const uint4 c = *reinterpret_cast<const uint4*>(st + KPS * C::kXBlk + i * 4096 + h * 2048 + r * 16);
+            const uint32_t sts = smem_u32(st);
+            const uint4 c = lds128(sts + KPS * C::kXBlk + i * 4096 + h * 2048 + r * 16);
             const int gi = (kb + i) / 2 - kb / 2;  // group of this block within the stage
-            const float scale = __half2float(*reinterpret_cast<const __half*>(st + C::kScaleOff + gi * 256 + r * 2));
-            const uint32_t zb = st[C::kZeroOff + gi * 64 + r / 2];
+            const float scale =
+                __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
+            const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
             const float zq = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
             if (i == KPS - 1) {
               __syncwarp();
