@@ -64,7 +64,7 @@ typedef enum {
 
 /* Version of the packed INT4 tile layout written by qlin_pack_w4 ([LP] S31
  * "kernel_pack_format").  A consumer must reject any other version. */
-#define QLIN_PACK_FORMAT_VERSION 1
+#define QLIN_PACK_FORMAT_VERSION 2
 
 /* Operation ids for qlin_workspace_size. */
 #define QLIN_OP_W4A16_GEMM 1
@@ -104,13 +104,16 @@ int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes);
  *   rint rounds half to even; a group whose scale rounds to 0 stores s = 1,
  *   z = 0 (symmetric: 8).  A scale that overflows FP16 sets the device error
  *   word to QLIN_ERR_INVALID_VALUE.
- *  Outputs, in tile layout version 1 (tiles of 128 rows x 64 columns):
+ *  Outputs, in tile layout version 2 (tiles of 128 rows x 64 columns):
  *   codes  (N*K/2 bytes): tile (n/128, k/64) is 4096 bytes at
  *          ((n/128)*(K/64) + k/64) * 4096; in it, half h = (k%64)/32 of row
  *          r = n%128 is the 16 bytes at h*2048 + r*16: four little-endian
- *          32-bit words, word j = (k%32)/8 holding columns 8j..8j+7 of the
- *          half with column e = k%8 in nibble position p = e/2 (e even) or
- *          4 + e/2 (e odd), i.e. bits 4p..4p+3.
+ *          32-bit words.  Writing the column within the half as
+ *          c = k%32 = 16a + 8b + 2t + e (a, b, e in {0,1}; t in 0..3), column
+ *          c is in word t at nibble position p = 2a + b + 4e, i.e. bits
+ *          4p..4p+3.  Word t thus holds what lane t of an mma.sync quad needs
+ *          for two 16-column k-steps, and the pair (c, c+1) is the two halves
+ *          of (word >> 4(2a + b)) & 0x000F000F.
  *   scales (2*N*K/128 bytes): FP16 of (n, g) at element
  *          ((n/128)*(K/128) + g) * 128 + n%128.
  *   zeros  (N*K/256 bytes): nibble of (n, g) in byte

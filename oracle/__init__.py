@@ -182,7 +182,7 @@ def pack_canonical(wq: W4Quant):
 
 
 def pack_tile(wq: W4Quant):
-    """Tile layout v1 (128 x 64 tiles, G = 128): codes, scales, zeros as flat arrays."""
+    """Tile layout, format version 2 (128 x 64 tiles, G = 128): codes, scales, zeros as flat arrays."""
     N, K = wq.q.shape
     assert wq.G == 128 and N % 128 == 0 and K % 128 == 0
     codes = np.empty((N * K // 2,), np.uint8)

@@ -256,14 +256,15 @@ void orc_pack_canonical(const uint8_t *q, const uint8_t *z, int64_t N, int64_t K
 }
 
 /*
- * Tile layout (format version 1), restated from its written description:
+ * Tile layout (format version 2), restated from its written description:
  * tiles of 128 rows (n) by 64 columns (k); G must be 128.
  *   codes : tile (nb = n/128, kb = k/64) is 4096 bytes at
  *           (nb * (K/64) + kb) * 4096; inside it, half h = (k%64)/32 and row
- *           r = n%128 own the 16 bytes at h*2048 + r*16.  Those 16 bytes are
- *           four little-endian 32-bit words; word j = (k%32)/8 holds the eight
- *           columns 8j..8j+7 of that half, column e = k%8 in nibble position
- *           p = e/2 for even e and p = 4 + e/2 for odd e (bits 4p..4p+3).
+ *           r = n%128 own the 16 bytes at h*2048 + r*16, the 32 columns
+ *           c = k%32 of that half.  Those 16 bytes are four little-endian
+ *           32-bit words.  With c = 16a + 8b + 2t + e (a, b, e in {0,1},
+ *           t in 0..3), column c sits in word t at nibble position
+ *           p = 2a + b + 4e (bits 4p..4p+3).
  *   scales: binary16 at element (nb * (K/128) + g) * 128 + r.
  *   zeros : byte (nb * (K/128) + g) * 64 + r/2, low nibble for even r.
  */
@@ -276,9 +277,10 @@ void orc_pack_tile(const uint8_t *q, const uint16_t *s, const uint8_t *z,
     for (int64_t n = 0; n < N; n++) {
         int64_t nb = n / 128, r = n % 128;
         for (int64_t k = 0; k < K; k++) {
-            int64_t kb = k / 64, h = (k % 64) / 32, j = (k % 32) / 8, e = k % 8;
-            int64_t p = (e % 2 == 0) ? e / 2 : 4 + e / 2;
-            int64_t byte = (nb * (K / 64) + kb) * 4096 + h * 2048 + r * 16 + j * 4 + p / 2;
+            int64_t kb = k / 64, h = (k % 64) / 32, c = k % 32;
+            int64_t a = c / 16, b = (c % 16) / 8, t = (c % 8) / 2, e = c % 2;
+            int64_t p = 2 * a + b + 4 * e;
+            int64_t byte = (nb * (K / 64) + kb) * 4096 + h * 2048 + r * 16 + t * 4 + p / 2;
             uint8_t v = q[n * K + k] & 15;
             codes[byte] |= (p % 2 == 0) ? v : (uint8_t)(v << 4);
         }

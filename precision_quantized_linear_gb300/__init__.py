@@ -28,7 +28,7 @@ __all__ = [
 
 OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8 = 1, 2, 3
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
-PACK_FORMAT_VERSION = 1
+PACK_FORMAT_VERSION = 2
 
 _lock = threading.Lock()
 _lib = None

@@ -168,13 +168,10 @@ __global__ void __launch_bounds__(128) w4a16_gemv_kernel(const uint16_t* __restr
       for (int j = 0; j < 4; ++j) {
         float2 xv[MT][4];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const float4* xp = reinterpret_cast<const float4*>(xs + m * KR + kl + h * 32 + j * 8);
-          const float4 a = xp[0], b = xp[1];
-          xv[m][0] = make_float2(a.x, a.y);
-          xv[m][1] = make_float2(a.z, a.w);
-          xv[m][2] = make_float2(b.x, b.y);
-          xv[m][3] = make_float2(b.z, b.w);
+        for (int m = 0; m < MT; ++m) {  // word j, position pair p: columns 16(p/2) + 8(p%2) + 2j, +1
+          const float2* xp = reinterpret_cast<const float2*>(xs + m * KR + kl + h * 32 + j * 2);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) xv[m][p] = xp[4 * p];
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {

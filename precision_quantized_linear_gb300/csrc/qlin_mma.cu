@@ -6,20 +6,22 @@
 // -> accumulate) and S22 (FP32 accumulation).  Per group g of 128 columns the
 // kernel uses
 //     sum_k x_k s (q_k - z) = s ( sum_k x_k (128 + q_k) - (128 + z) sum_k x_k ),
-// where 128 + q_k is exact in BF16 and comes out of the packed word with one
-// shift and one LOP3 per pair of columns; the MMA accumulates
+// where 128 + q_k is exact in BF16.  The packed layout gives each lane of an
+// mma.sync quad its own 32-bit word per record (four A-fragment pairs), so a
+// pair comes out with one LOP3 (ALU pipe) after a right shift by a constant,
+// done as a high multiply on the otherwise idle FMA pipe; the MMA accumulates
 // sum_k x_k (128 + q_k) in FP32 and the scale / zero-point are applied once
 // per group and row in FP32 registers.
 //
-// One CTA = one 128-row tile x one K range.  Warp 4 streams, per stage of 256
+// One CTA = one 128-row tile x one K range.  Warp 8 streams, per stage of 256
 // columns, the tile's packed codes (16 KB), scales and zero-points and the
 // activation slice of every token into a ring of shared-memory stages with
 // bulk copies (weights first, before waiting for the previous kernel on the
-// stream).  Warps 0-3 each own 32 rows (two m16 blocks) and every token (one
-// or two n8 blocks).  The per-group activation sums come from the tensor core
-// too: one extra m16 block whose A fragment is all ones yields sum_k x_k for
-// exactly the tokens each thread folds.  Split-K partial sums use the same
-// deterministic last-arriver reduction as the other kernels.
+// stream).  Warps 0-7 each own 16 rows (one m16 block) and every token (one
+// or two n8 blocks).  Warp 9 forms the per-group activation sums sum_k x_k of
+// each stage once for the whole CTA, on the tensor core (an m16 A operand of
+// all ones), and leaves them in the stage for the folds.  Split-K partial sums
+// use the same deterministic last-arriver reduction as the other kernels.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -31,10 +33,13 @@ namespace qlin {
 constexpr int kMmaStageCols = 256;                 // K columns per stage (4 code tiles)
 constexpr int kMmaCodeBytes = 4 * 4096;            // codes of one stage
 constexpr int kMmaMetaOff = kMmaCodeBytes;         // 2 groups x 128 FP16 scales, then 2 x 64 B zeros
+constexpr int kMmaSumOff = kMmaMetaOff + 640;      // FP32 activation sums [2 groups][16 tokens]
 constexpr int kMmaXOff = kMmaCodeBytes + 1024;     // activation rows
 constexpr int kMmaXRow = kMmaStageCols * 2 + 16;   // 528 B per token row (conflict-free B fragments)
 constexpr int kMmaConsumers = 8;                   // consumer warps, 16 rows (one m16 block) each
-constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
+constexpr int kMmaProducer = kMmaConsumers;        // bulk-copy warp
+constexpr int kMmaSummer = kMmaConsumers + 1;      // activation-sum warp
+constexpr int kMmaThreads = (kMmaConsumers + 2) * 32;
 constexpr uint64_t kMmaWaitNs = 2000000000ull;
 
 template <int NT>
@@ -43,10 +48,11 @@ struct MmaCfg {
   static constexpr int kStage = ((kMmaXOff + kTok * kMmaXRow) + 1023) / 1024 * 1024;
   static constexpr int kStages = NT == 1 ? 3 : 4;  // M <= 8: three CTAs fit per SM
   static constexpr int kSmem = 1024 + kStages * kStage + 256;
+  static constexpr int kMinBlocks = NT == 1 ? 3 : 2;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -55,21 +61,39 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 
 // Same with a zero accumulator (starts a chain without clearing registers).
 __device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%10, %10, %10, %10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// Pair (2p, 2p+1) of a packed word as BF16x2 (128 + q): nibble positions p and
-// 4 + p hold the two columns (tile layout v1); `sh` = 4p.
-__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, uint32_t sh) {
-  return ((w >> sh) & 0x000F000Fu) | 0x43004300u;
+// BF16x2 (128 + q) of the pair in the low nibbles of each half of v:
+// (v & mask) | magic with mask = 0x000F000F and magic = 0x43004300 (a BF16
+// with exponent 2^7 whose low mantissa bits take the nibble), as one logic op.
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t v, uint32_t mask, uint32_t magic) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(magic));
+  return r;
+}
+
+// B fragments of two consecutive 16-column k-steps for tokens 8j .. 8j+7 of an
+// activation block whose rows are `row_bytes` apart: lanes 8i .. 8i+7 address
+// the rows at column offset 8i (x4 matrices = k-steps (0: cols 0-7, 8-15), (1: 16-23, 24-31)).
+__device__ __forceinline__ void ldsm_b2(uint32_t addr, uint32_t (&b)[2][2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(b[0][0]), "=r"(b[0][1]), "=r"(b[1][0]), "=r"(b[1][1])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
 }
 
 template <int NT>  // n8 token blocks: M <= 8 * NT
-__global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
+__global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma_kernel(
     const uint16_t* __restrict__ X, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
     const uint8_t* __restrict__ zeros, uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K, int stages_per_split,
     int splits, float* partials, uint32_t* counters, int* err) {
@@ -78,8 +102,14 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kStages * C::kStage);
   uint64_t* empty = full + C::kStages;
+  uint64_t* summed = empty + C::kStages;  // activation sums of the stage are in place
   __shared__ int s_last;
   __shared__ volatile int s_abort;
+  // extraction constants, read back from shared memory so that the compiler
+  // keeps them in registers: the nibble mask and BF16 magic as the two register
+  // operands of one LOP3, and the multipliers 2^28, 2^24, 2^20 whose high
+  // products are the right shifts by 4, 8, 12 on the FMA pipe
+  __shared__ volatile uint32_t s_kc[5];
 
   const int nt = blockIdx.x, split = blockIdx.y;
   const int64_t KS = K / kMmaStageCols;
@@ -94,9 +124,15 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kMmaConsumers);
+      mbar_init(&summed[i], 4);
     }
     fence_mbar_init();
     s_abort = 0;
+    s_kc[0] = 0x000F000Fu;
+    s_kc[1] = 0x43004300u;
+    s_kc[2] = 1u << 28;
+    s_kc[3] = 1u << 24;
+    s_kc[4] = 1u << 20;
   }
   // token rows >= M are never copied: zero them once so B fragments need no bounds test
   for (int idx = threadIdx.x; idx < C::kStages * (C::kTok - mrows) * (kMmaXRow / 16); idx += kMmaThreads) {
@@ -125,7 +161,7 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
       bulk_load(st + kMmaXOff + m * kMmaXRow, X + m * K + k0, kMmaStageCols * 2, &full[i % C::kStages]);
   };
   // weights never depend on the previous kernel on the stream: start them first
-  if (warp == kMmaConsumers && lane == 0)
+  if (warp == kMmaProducer && lane == 0)
     for (int i = 0; i < nst && i < C::kStages; ++i) issue_w(i);
   grid_dep_wait();
   grid_dep_launch();
@@ -137,7 +173,7 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
 
-  if (warp == kMmaConsumers) {
+  if (warp == kMmaProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       for (int i = 0; i < nst && i < C::kStages; ++i) issue_x(i);
@@ -151,15 +187,55 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
         issue_x(i);
       }
     }
+  } else if (warp == kMmaSummer) {
+    // ------------------------------------------------------------ activation sums per group and token
+    // C = ones(16 x 128) * X_g^T: every row of C holds sum_k x_k of the n8 block's
+    // tokens; lanes 0-3 (row 0) write tokens 8j + 2t, 8j + 2t + 1.
+    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // BF16 1.0 pairs
+    for (int i = 0; i < nst; ++i) {
+      const int slot = i % C::kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort))) {
+        set_error(err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      const uint32_t st = smem_u32(ring + slot * C::kStage);
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          float cs[2][4];  // two chains of four k-steps
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t bb[2][2];
+            ldsm_b2(st + kMmaXOff + (j * 8 + (lane & 7)) * kMmaXRow + (grp * 128 + q * 32 + (lane >> 3) * 8) * 2, bb);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (q == 0)
+                mma_bf16_16816_z(cs[h], ones, bb[h][0], bb[h][1]);
+              else
+                mma_bf16_16816(cs[h], ones, bb[h][0], bb[h][1]);
+            }
+          }
+          if (lane < 4) {
+            float2 v = make_float2(cs[0][0] + cs[1][0], cs[0][1] + cs[1][1]);
+            *reinterpret_cast<float2*>(ring + slot * C::kStage + kMmaSumOff + (grp * 16 + j * 8 + 2 * lane) * 4) = v;
+          }
+        }
+      if (lane < 4) mbar_arrive(&summed[slot]);
+    }
   } else {
     // ------------------------------------------------------------ consumers: rows 16*warp .. 16*warp + 15
     const int r0 = warp * 16 + gq;  // this thread's rows: r0 and r0 + 8
-    const uint32_t sh = 4u * static_cast<uint32_t>(tq);
+    const uint32_t kmask = s_kc[0], kmagic = s_kc[1];
+    const uint32_t kshr[3] = {s_kc[2], s_kc[3], s_kc[4]};
+    // pair in nibble positions i, i + 4 of w, as BF16x2 (128 + q)
+    auto pair_at = [&](uint32_t w, int i) {
+      return nib_pair_bf16(i == 0 ? w : __umulhi(w, kshr[i - 1]), kmask, kmagic);
+    };
     // zero-point nibble of rows r0, r0+8 (same parity): moved to bits 16..19 of an FP32
     // whose exponent is 2^7, which reads as 128 + z exactly
     const uint32_t zsh = (r0 & 1) ? 12u : 16u;
-    const int xoff = kMmaXOff + gq * kMmaXRow + 4 * tq;  // B fragment of token gq, columns 2t, 2t+1
-    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // BF16 1.0 pairs
     for (int i = 0; i < nst; ++i) {
       const int slot = i % C::kStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort))) {
@@ -170,53 +246,60 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
       const uint32_t st = smem_u32(ring + slot * C::kStage);  // shared-space address of the stage
       const uint32_t sc = st + kMmaMetaOff;                   // FP16 scales [2][128]
       const uint32_t zp = st + kMmaMetaOff + 512;             // zero nibbles [2][64]
-#pragma unroll 1
+      // word t (this lane's) of the records of rows r0, r0+8 in both halves of a
+      // 64-column tile; each tile's words are loaded one tile ahead so that the
+      // shared-memory latency is hidden
+      uint32_t cw[4];
+      auto load_codes = [&](int kbl, uint32_t (&w)[4]) {
+        const uint32_t tile = st + kbl * 4096 + tq * 4;
+        w[0] = lds32(tile + r0 * 16);               // half 0, row r0
+        w[1] = lds32(tile + (r0 + 8) * 16);         // half 0, row r0+8
+        w[2] = lds32(tile + 2048 + r0 * 16);        // half 1, row r0
+        w[3] = lds32(tile + 2048 + (r0 + 8) * 16);  // half 1, row r0+8
+      };
+      load_codes(0, cw);
+      bool sums_ok = true;
+#pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
-        // two accumulators (one per 64-column block) keep two MMA chains in flight
+        // two accumulators (one per 64-column tile) keep two MMA chains in flight
         float c[2][NT][4];
-        float xs[2][NT][4];  // sum_k x over each block, from the ones block (rows all equal)
 #pragma unroll
         for (int kb2 = 0; kb2 < 2; ++kb2) {
-          const int kbl = grp * 2 + kb2;  // 64-column block within the stage
-          const uint32_t tile = st + kbl * 4096;
-          const uint4 w00 = lds128(tile + r0 * 16);          // half 0, row r0
-          const uint4 w01 = lds128(tile + (r0 + 8) * 16);    // half 0, row r0+8
-          const uint4 w10 = lds128(tile + 2048 + r0 * 16);   // half 1
-          const uint4 w11 = lds128(tile + 2048 + (r0 + 8) * 16);
-          const uint32_t wr0[8] = {w00.x, w00.y, w00.z, w00.w, w10.x, w10.y, w10.z, w10.w};
-          const uint32_t wr1[8] = {w01.x, w01.y, w01.z, w01.w, w11.x, w11.y, w11.z, w11.w};
+          const int kbl = grp * 2 + kb2;  // 64-column tile within the stage
+          const uint32_t cur[4] = {cw[0], cw[1], cw[2], cw[3]};
+          if (kbl < 3) load_codes(kbl + 1, cw);
+          // B fragments: one ldmatrix.x4 per token block covers two 16-column k-steps
+          uint32_t b[2][NT][2][2];
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {  // words 2ks, 2ks+1 hold columns 16ks .. 16ks+15
-            uint32_t b[NT][2];
+          for (int half = 0; half < 2; ++half)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              const uint32_t xr = st + xoff + j * 8 * kMmaXRow + (kbl * 64 + ks * 16) * 2;
-              b[j][0] = lds32(xr);
-              b[j][1] = lds32(xr + 16);
-            }
+            for (int j = 0; j < NT; ++j)
+              ldsm_b2(st + kMmaXOff + (j * 8 + (lane & 7)) * kMmaXRow + (kbl * 64 + half * 32 + (lane >> 3) * 8) * 2,
+                      b[half][j]);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {  // k-step = columns 16a .. 16a+15 of half h
+            const int h = ks >> 1, ia = 2 * (ks & 1);
             uint32_t a[4];
-            a[0] = nib_pair_bf16(wr0[2 * ks], sh);      // row r0,   columns 2t, 2t+1
-            a[1] = nib_pair_bf16(wr1[2 * ks], sh);      // row r0+8, columns 2t, 2t+1
-            a[2] = nib_pair_bf16(wr0[2 * ks + 1], sh);  // row r0,   columns 2t+8, 2t+9
-            a[3] = nib_pair_bf16(wr1[2 * ks + 1], sh);  // row r0+8, columns 2t+8, 2t+9
+            a[0] = pair_at(cur[2 * h], ia);          // row r0,   columns 2t, 2t+1
+            a[1] = pair_at(cur[2 * h + 1], ia);      // row r0+8, columns 2t, 2t+1
+            a[2] = pair_at(cur[2 * h], ia + 1);      // row r0,   columns 2t+8, 2t+9
+            a[3] = pair_at(cur[2 * h + 1], ia + 1);  // row r0+8, columns 2t+8, 2t+9
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-              if (ks == 0) {  // first k-step of the block starts both chains from zero
-                mma_bf16_16816_z(c[kb2][j], a, b[j][0], b[j][1]);
-                mma_bf16_16816_z(xs[kb2][j], ones, b[j][0], b[j][1]);
-              } else {
-                mma_bf16_16816(c[kb2][j], a, b[j][0], b[j][1]);
-                mma_bf16_16816(xs[kb2][j], ones, b[j][0], b[j][1]);
-              }
+              const uint32_t(&bk)[2] = b[h][j][ks & 1];
+              if (ks == 0)  // first k-step of the tile starts the chain from zero
+                mma_bf16_16816_z(c[kb2][j], a, bk[0], bk[1]);
+              else
+                mma_bf16_16816(c[kb2][j], a, bk[0], bk[1]);
             }
           }
         }
         // fold: y += s (sum x (128 + q) - (128 + z) sum x); rows r0, r0+8; tokens 8j+2t, +1
-        float xv[NT][2];
+        if (grp == 0)
+          sums_ok = __all_sync(0xffffffffu, mbar_wait(&summed[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort));
+        float2 xv[NT];
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) xv[j][e] = xs[0][j][e] + xs[1][j][e];
+        for (int j = 0; j < NT; ++j) xv[j] = lds64f(st + kMmaSumOff + (grp * 16 + j * 8 + 2 * tq) * 4);
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = r0 + hr * 8;
@@ -224,13 +307,18 @@ __global__ void __launch_bounds__(kMmaThreads) w4a16_mma_kernel(
           const uint32_t zb = lds8(zp + grp * (kTileN / 2) + r / 2);
           const float cz = __uint_as_float(((zb << zsh) & 0x000F0000u) | 0x43000000u);
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float cs = c[0][j][hr * 2 + e] + c[1][j][hr * 2 + e];
-              acc[j][hr * 2 + e] = fmaf(s, fmaf(-cz, xv[j][e], cs), acc[j][hr * 2 + e]);
-            }
+          for (int j = 0; j < NT; ++j) {
+            const float c0 = c[0][j][hr * 2] + c[1][j][hr * 2];
+            const float c1 = c[0][j][hr * 2 + 1] + c[1][j][hr * 2 + 1];
+            acc[j][hr * 2] = fmaf(s, fmaf(-cz, xv[j].x, c0), acc[j][hr * 2]);
+            acc[j][hr * 2 + 1] = fmaf(s, fmaf(-cz, xv[j].y, c1), acc[j][hr * 2 + 1]);
+          }
         }
+      }
+      if (!sums_ok) {
+        set_error(err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+        break;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);

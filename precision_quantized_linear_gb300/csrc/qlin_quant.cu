@@ -26,13 +26,18 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Nibble position of column e (0..7) inside its 32-bit word: even columns in
-// positions 0..3, odd columns in 4..7, so that one AND with 0x000F000F pulls
-// out two adjacent columns as the two halves of a 32-bit register.
-__device__ __forceinline__ int nibble_pos(int e) { return (e & 1) ? 4 + (e >> 1) : (e >> 1); }
+// Packed layout (format version 2): in each 16-byte record (one row, 32
+// columns c = 16a + 8b + 2t + e of a 64-column tile) word t holds the eight
+// columns a lane t of an mma.sync quad needs for two 16-column k-steps, column
+// c in nibble position 2a + b + 4e.  Pair (c, c+1) is then the two halves of
+// (word >> 4(2a + b)) & 0x000F000F: one shift by a constant and one logic op.
 
 // [LP] S2-S4: one warp per (pair of rows, group of 128 columns).  Lane l owns
 // columns 4l..4l+3 of the group; the group's min/max are warp reductions.
+// Lane l = 8R + u covers record R of the group (tile R/2, half R%2); its
+// columns 4u, 4u+1 go to word 2(u%2) and 4u+2, 4u+3 to word 2(u%2)+1, both at
+// nibble positions u/2 and u/2 + 4, so each word is the OR of the lanes u,
+// u^2, u^4, u^6.
 __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K,
                                                       int symmetric, uint8_t* __restrict__ codes,
                                                       uint16_t* __restrict__ scales, uint8_t* __restrict__ zeros,
@@ -78,7 +83,7 @@ __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict
         zp = static_cast<int>(zf);
       }
       if (isinf(sc) && lane == 0) set_error(err, QLIN_ERR_INVALID_VALUE);
-      uint32_t word = 0;
+      uint32_t cq[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float rq = rintf(__fdiv_rn(v[i], sc));
@@ -90,16 +95,21 @@ __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict
           rq = fminf(fmaxf(rq + static_cast<float>(zp), 0.0f), 15.0f);
           c = static_cast<int>(rq);
         }
-        const int e = (lane & 1) * 4 + i;  // column within the 8-column word
-        word |= static_cast<uint32_t>(c) << (4 * nibble_pos(e));
+        cq[i] = static_cast<uint32_t>(c);
       }
-      word |= __shfl_xor_sync(0xffffffffu, word, 1);
-      if ((lane & 1) == 0) {
-        const int64_t k = g * kGroup + 4 * lane;  // first column of the word
-        const int64_t kb = k / kTileK;
-        const int h = static_cast<int>((k % kTileK) / 32);
-        const int j = static_cast<int>((k % 32) / 8);
-        *reinterpret_cast<uint32_t*>(codes + (nb * (K / kTileK) + kb) * 4096 + h * 2048 + r * 16 + j * 4) = word;
+      const int u = lane & 7, R = lane >> 3;
+      const uint32_t pos = 4u * static_cast<uint32_t>(u >> 1);
+      uint32_t wa = (cq[0] << pos) | (cq[1] << (pos + 16));  // word 2(u%2)
+      uint32_t wb = (cq[2] << pos) | (cq[3] << (pos + 16));  // word 2(u%2) + 1
+      wa |= __shfl_xor_sync(0xffffffffu, wa, 2);
+      wb |= __shfl_xor_sync(0xffffffffu, wb, 2);
+      wa |= __shfl_xor_sync(0xffffffffu, wa, 4);
+      wb |= __shfl_xor_sync(0xffffffffu, wb, 4);
+      if (u < 2) {
+        const int64_t kb = g * 2 + (R >> 1);
+        const int h = R & 1;
+        *reinterpret_cast<uint2*>(codes + (nb * (K / kTileK) + kb) * 4096 + h * 2048 + r * 16 + u * 8) =
+            make_uint2(wa, wb);
       }
       if (lane == 0) {
         scales[(nb * ng + g) * kTileN + r] = __half_as_ushort(s16);

@@ -95,7 +95,9 @@ __device__ __forceinline__ void named_bar_epi() { asm volatile("bar.sync 1, 128;
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
-// Eight columns of one 32-bit code word -> eight BF16 values bf16(s) (q - z), 16 bytes.
+// Eight columns of one 32-bit code word -> four BF16 pairs bf16(s) (q - z);
+// component i is the pair in nibble positions i and i + 4.  Word t of a
+// 32-column record holds pairs (columns 8i + 2t, +1) for i = 0..3.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 zoff, __nv_bfloat162 s2) {
   uint32_t o[4];
 #pragma unroll
@@ -355,14 +357,14 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
             if constexpr (C::kATmem) {
               // lane r of the slot holds row r: 32 columns x two BF16 = the 64 columns of the block
               tc_fence_after();
-              uint32_t v[16];
+              uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 d = dequant8(words[q], zoff, s2);
-                v[4 * q + 0] = d.x;
-                v[4 * q + 1] = d.y;
-                v[4 * q + 2] = d.z;
-                v[4 * q + 3] = d.w;
+              for (int t = 0; t < 4; ++t) {
+                const uint4 d = dequant8(words[t], zoff, s2);
+                v[t] = d.x;
+                v[4 + t] = d.y;
+                v[8 + t] = d.z;
+                v[12 + t] = d.w;
               }
               tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
                             h * 16,
@@ -371,11 +373,14 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
               tc_fence_before();
             } else {
               uint8_t* arow = aring + ai * C::kAStage + r * 128;
+              uint4 d[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {  // 16-byte chunk cc holds columns 8cc..8cc+7
-                const int cc = h * 4 + q;
-                *reinterpret_cast<uint4*>(arow + ((cc ^ (r & 7)) << 4)) = dequant8(words[q], zoff, s2);
-              }
+              for (int t = 0; t < 4; ++t) d[t] = dequant8(words[t], zoff, s2);
+              // 16-byte chunk cc = 4h + i holds columns 8cc..8cc+7: position i of words 0..3
+              *reinterpret_cast<uint4*>(arow + (((h * 4 + 0) ^ (r & 7)) << 4)) = make_uint4(d[0].x, d[1].x, d[2].x, d[3].x);
+              *reinterpret_cast<uint4*>(arow + (((h * 4 + 1) ^ (r & 7)) << 4)) = make_uint4(d[0].y, d[1].y, d[2].y, d[3].y);
+              *reinterpret_cast<uint4*>(arow + (((h * 4 + 2) ^ (r & 7)) << 4)) = make_uint4(d[0].z, d[1].z, d[2].z, d[3].z);
+              *reinterpret_cast<uint4*>(arow + (((h * 4 + 3) ^ (r & 7)) << 4)) = make_uint4(d[0].w, d[1].w, d[2].w, d[3].w);
               fence_proxy_async_smem();
             }
             __syncwarp();

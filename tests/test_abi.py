@@ -41,7 +41,7 @@ def test_status_strings_and_version(lib):
     assert q.qlin_status_string(0) == "QLIN_OK"
     assert q.qlin_status_string(7) == "QLIN_ERR_TIMEOUT"
     assert q.qlin_status_string(99) == "QLIN_ERR_UNKNOWN"
-    assert q.qlin_pack_format_version() == q.PACK_FORMAT_VERSION == 1
+    assert q.qlin_pack_format_version() == q.PACK_FORMAT_VERSION == 2
 
 
 def test_packed_sizes_give_4_125_bits(lib):

@@ -233,7 +233,7 @@ def test_tile_pack_is_a_bijection_and_hand_positions():
     wq = oracle.W4Quant(q, s, z, 128, False, 0)
     seen = np.zeros(N * K, bool)
     rng = np.random.default_rng(2)
-    for (n, k) in [(0, 0), (0, 1), (0, 2), (0, 7), (0, 8), (0, 32), (0, 63), (0, 64),
+    for (n, k) in [(0, 0), (0, 1), (0, 2), (0, 7), (0, 8), (0, 16), (0, 25), (0, 32), (0, 63), (0, 64),
                    (1, 0), (127, 255), (128, 0), (255, 255)] + [tuple(x) for x in rng.integers(0, 256, (40, 2))]:
         q[:] = 0
         q[n, k] = 0xF
@@ -250,12 +250,16 @@ def test_tile_pack_is_a_bijection_and_hand_positions():
             assert (byte, nib) == (0, 0)
         if (n, k) == (0, 1):            # odd column 1 -> nibble position 4 -> byte 2, low
             assert (byte, nib) == (2, 0)
-        if (n, k) == (0, 2):            # even column 2 -> nibble position 1 -> byte 0, high
-            assert (byte, nib) == (0, 1)
-        if (n, k) == (0, 7):            # position 7 -> byte 3, high
-            assert (byte, nib) == (3, 1)
-        if (n, k) == (0, 8):            # next 32-bit word
+        if (n, k) == (0, 2):            # column 2 = 2t with t = 1 -> word 1, position 0
             assert (byte, nib) == (4, 0)
+        if (n, k) == (0, 7):            # column 7 = 2*3 + 1 -> word 3, position 4 -> byte 14, low
+            assert (byte, nib) == (14, 0)
+        if (n, k) == (0, 8):            # column 8 = 8b -> word 0, position 1 -> byte 0, high
+            assert (byte, nib) == (0, 1)
+        if (n, k) == (0, 16):           # column 16 = 16a -> word 0, position 2 -> byte 1, low
+            assert (byte, nib) == (1, 0)
+        if (n, k) == (0, 25):           # column 25 = 16 + 8 + 1 -> word 0, position 7 -> byte 3, high
+            assert (byte, nib) == (3, 1)
         if (n, k) == (0, 32):           # second half of the 64-column tile
             assert (byte, nib) == (2048, 0)
         if (n, k) == (1, 0):            # next row: 16 bytes on
@@ -272,19 +276,21 @@ def test_tile_pack_roundtrip_full():
     wq = oracle.quantize_w4(W, G=128)
     codes, scales, zeros = oracle.pack_tile(wq)
     # unpack by the written description and compare with the unpacked codes
-    c = codes.reshape(N // 128, K // 64, 2, 128, 4, 4)          # nb, kb, h, r, word j, byte
+    c = codes.reshape(N // 128, K // 64, 2, 128, 4, 4)          # nb, kb, h, r, word t, byte
     nib = np.stack([c & 15, c >> 4], axis=-1).reshape(N // 128, K // 64, 2, 128, 4, 8)  # position p
-    order = [0, 4, 1, 5, 2, 6, 3, 7]                             # column e -> position p
-    e_of_p = np.argsort(order)
-    cols = nib[..., order]                                       # now indexed by column e
-    un = cols.transpose(0, 3, 1, 2, 4, 5).reshape(N, K)
+    # position p = 2a + b + 4e of word t holds column c = 16a + 8b + 2t + e of the half
+    cols = np.zeros((N // 128, K // 64, 2, 128, 32), np.uint8)
+    for t in range(4):
+        for p in range(8):
+            a, b, e = (p & 3) >> 1, p & 1, p >> 2
+            cols[..., 16 * a + 8 * b + 2 * t + e] = nib[..., t, p]
+    un = cols.transpose(0, 3, 1, 2, 4).reshape(N, K)
     assert np.array_equal(un, wq.q)
     sc = scales.reshape(N // 128, K // 128, 128).transpose(0, 2, 1).reshape(N, K // 128)
     assert np.array_equal(sc, wq.s)
     zz = zeros.reshape(N // 128, K // 128, 64)
     zz = np.stack([zz & 15, zz >> 4], axis=-1).reshape(N // 128, K // 128, 128)
     assert np.array_equal(zz.transpose(0, 2, 1).reshape(N, K // 128), wq.z)
-    assert e_of_p.tolist() == [0, 2, 4, 6, 1, 3, 5, 7]
 
 
 def test_effective_bits_from_buffers():
