@@ -89,8 +89,12 @@ int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* sca
 
 /* Scratch bytes a call of `op` needs for these sizes (0 if none).  The
  * workspace must be zero-filled before its first use with this library and
- * is left zero-filled by every call that completes; calls that share one
- * workspace must not overlap in time (use one per stream). */
+ * is left zero-filled by every call that completes (split-K counters, the
+ * small-M kernel's work-queue word and the partial sums are all cleared by the
+ * call that used them), so one workspace may serve calls of any shapes in
+ * turn; calls that share one workspace must not overlap in time (use one per
+ * stream).  After a call whose kernel reported a device error (see
+ * qlin_get_device_error) its contents are undefined: zero it again. */
 int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 /*

@@ -94,7 +94,7 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t set_smem_once_impl(const void* kernel, int bytes) {
+cudaError_t set_smem_once_impl(const void* kernel, int bytes, bool wide_clusters) {
   static std::mutex mu;
   static std::unordered_map<const void*, unsigned long long> done;  // kernel -> bit per device
   int dev = 0;
@@ -105,6 +105,7 @@ cudaError_t set_smem_once_impl(const void* kernel, int bytes) {
   auto it = done.find(kernel);
   if (it != done.end() && (it->second & bit)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && wide_clusters) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[kernel] |= bit;
   return e;
 }

@@ -52,7 +52,11 @@ __device__ __forceinline__ void splitk_finish(const float (&mine)[MT], int mcoun
   for (int m = 0; m < MT; ++m) {
     if (m >= mcount) continue;
     float acc = 0.0f;
-    for (int s = 0; s < splits; ++s) acc += __ldcg(partials + (static_cast<int64_t>(s) * M + m0 + m) * N + n);
+    for (int s = 0; s < splits; ++s) {  // read and clear: the workspace is left zero-filled
+      float* p = partials + (static_cast<int64_t>(s) * M + m0 + m) * N + n;
+      acc += __ldcg(p);
+      __stcg(p, 0.0f);
+    }
     epi(m0 + m, n, acc);
   }
   if (threadIdx.x == 0) counters[tile] = 0u;
@@ -264,7 +268,10 @@ SplitPlan plan_w4a16_gemv(int64_t M, int64_t N, int64_t K, int num_sms) {
   const int mt = gemv_mt(M);
   const int64_t tiles = (N / kTileN) * ((M + mt - 1) / mt);
   SplitPlan p = plan_splits(tiles, K / kTileK, num_sms, 8192 / mt / kTileK);
-  if (p.splits > 1) p.ws_bytes = counters_bytes(tiles) + sizeof(float) * static_cast<size_t>(p.splits) * M * N;
+  if (p.splits > 1) {
+    p.ws_bytes = counters_bytes(tiles) + sizeof(float) * static_cast<size_t>(p.splits) * M * N;
+    p.zero_bytes = counters_bytes(tiles);
+  }
   return p;
 }
 
@@ -395,7 +402,10 @@ SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms) {
   const int mt = gemv_mt(M);
   const int64_t tiles = (N / kTileN) * ((M + mt - 1) / mt);
   SplitPlan p = plan_splits(tiles, K / kTileK, num_sms, 8192 / mt / kTileK);
-  if (p.splits > 1) p.ws_bytes = counters_bytes(tiles) + sizeof(float) * static_cast<size_t>(p.splits) * M * N;
+  if (p.splits > 1) {
+    p.ws_bytes = counters_bytes(tiles) + sizeof(float) * static_cast<size_t>(p.splits) * M * N;
+    p.zero_bytes = counters_bytes(tiles);
+  }
   return p;
 }
 

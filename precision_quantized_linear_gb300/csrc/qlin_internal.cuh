@@ -27,15 +27,17 @@ struct SplitPlan {
   int kb_per_split = 0;  // 64-column blocks per range (last range may be shorter)
   int64_t tiles = 0;     // output tiles (m blocks x n tiles)
   size_t ws_bytes = 0;   // workspace needed (0 when splits == 1)
+  size_t zero_bytes = 0; // leading workspace bytes (counters) that must be zero at launch
 };
 
 // cudaFuncSetAttribute once per (kernel, device), so that no such call is made
 // while a stream is being captured into a CUDA graph.  Keyed by the kernel's
 // address: template instantiations share a type but not an address.
-cudaError_t set_smem_once_impl(const void* kernel, int bytes);
+cudaError_t set_smem_once_impl(const void* kernel, int bytes, bool wide_clusters);
+// wide_clusters: also allow thread-block clusters of up to 16 CTAs.
 template <typename F>
-inline cudaError_t set_smem_once(F* kernel, int bytes) {
-  return set_smem_once_impl(reinterpret_cast<const void*>(kernel), bytes);
+inline cudaError_t set_smem_once(F* kernel, int bytes, bool wide_clusters = false) {
+  return set_smem_once_impl(reinterpret_cast<const void*>(kernel), bytes, wide_clusters);
 }
 
 inline size_t counters_bytes(int64_t tiles) { return static_cast<size_t>((tiles * 4 + 255) / 256 * 256); }

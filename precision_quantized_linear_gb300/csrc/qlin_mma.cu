@@ -20,10 +20,15 @@
 // stream).  Warps 0-7 each own 16 rows (one m16 block) and every token (one
 // or two n8 blocks).  Warp 9 forms the per-group activation sums sum_k x_k of
 // each stage once for the whole CTA, on the tensor core (an m16 A operand of
-// all ones), and leaves them in the stage for the folds.  Split-K partial sums
-// use the same deterministic last-arriver reduction as the other kernels.
+// all ones), and leaves them in the stage for the folds.  The K ranges of one
+// tile run as a thread-block cluster and add their partial sums through
+// distributed shared memory, in rank order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <array>
+#include <mutex>
+#include <unordered_map>
 
 #include "qlin_internal.cuh"
 #include "qlin_ptx.cuh"
@@ -41,6 +46,7 @@ constexpr int kMmaProducer = kMmaConsumers;        // bulk-copy warp
 constexpr int kMmaSummer = kMmaConsumers + 1;      // activation-sum warp
 constexpr int kMmaThreads = (kMmaConsumers + 2) * 32;
 constexpr uint64_t kMmaWaitNs = 2000000000ull;
+constexpr int kMmaMaxCluster = 16;                 // CTAs of one tile's split-K cluster (non-portable above 8)
 
 template <int NT>
 struct MmaCfg {
@@ -96,14 +102,13 @@ template <int NT>  // n8 token blocks: M <= 8 * NT
 __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma_kernel(
     const uint16_t* __restrict__ X, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
     const uint8_t* __restrict__ zeros, uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K, int stages_per_split,
-    int splits, float* partials, uint32_t* counters, int* err) {
+    int splits, int* err) {
   using C = MmaCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kStages * C::kStage);
   uint64_t* empty = full + C::kStages;
   uint64_t* summed = empty + C::kStages;  // activation sums of the stage are in place
-  __shared__ int s_last;
   __shared__ volatile int s_abort;
   // extraction constants, read back from shared memory so that the compiler
   // keeps them in registers: the nibble mask and BF16 magic as the two register
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   // products are the right shifts by 4, 8, 12 on the FMA pipe
   __shared__ volatile uint32_t s_kc[5];
 
-  const int nt = blockIdx.x, split = blockIdx.y;
+  const int split = blockIdx.x, nt = blockIdx.y;  // the K ranges of a tile form one cluster (rank = split)
   const int64_t KS = K / kMmaStageCols;
   const int s0 = split * stages_per_split;
   const int nst = static_cast<int>(imin64(KS, s0 + stages_per_split)) - s0;
@@ -326,79 +331,135 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   }
 
   // ---------------------------------------------------------------- outputs
+  if (splits == 1) {
+    if (warp < kMmaConsumers) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int64_t n = static_cast<int64_t>(nt) * kTileN + warp * 16 + gq + hr * 8;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int64_t m = j * 8 + 2 * tq + e;
+            if (m < M) Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j][hr * 2 + e]));
+          }
+      }
+    }
+    return;
+  }
+  // Split K: the CTAs of the tile's cluster add their partial sums through
+  // distributed shared memory.  Each leaves its FP32 sums [token][row] in its
+  // own ring (every stage has been consumed and no copy is in flight); after a
+  // cluster barrier, rank q adds rows [q R, q R + R) over ranks 0, 1, ... in
+  // order (deterministic) and writes them; a second barrier keeps every CTA's
+  // shared memory alive until all ranks have read it.  Every thread of every
+  // CTA reaches both barriers, also after a timed-out wait.
+  float* red = reinterpret_cast<float*>(ring);
+  __syncthreads();  // every warp is done with the ring
   if (warp < kMmaConsumers) {
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int64_t n = static_cast<int64_t>(nt) * kTileN + warp * 16 + gq + hr * 8;
+    for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int64_t m = j * 8 + 2 * tq + e;
-          if (m < M) {
-            const float v = acc[j][hr * 2 + e];
-            if (splits == 1)
-              Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-            else
-              __stcg(partials + (static_cast<int64_t>(split) * M + m) * N + n, v);
-          }
-        }
+        for (int e = 0; e < 2; ++e) red[(j * 8 + 2 * tq + e) * kTileN + warp * 16 + gq + hr * 8] = acc[j][hr * 2 + e];
+  }
+  __syncwarp();
+  cluster_sync();
+  const int R = (kTileN + splits - 1) / splits;
+  const int r_lo = split * R, r_n = static_cast<int>(imin64(kTileN, r_lo + R)) - r_lo;
+  if (r_n > 0) {
+    const uint32_t red_u32 = smem_u32(red);
+    for (int idx = threadIdx.x; idx < r_n * mrows; idx += kMmaThreads) {
+      const int m = idx / r_n, r = r_lo + idx % r_n;
+      const uint32_t off = red_u32 + static_cast<uint32_t>(m * kTileN + r) * 4u;
+      float v = 0.0f;
+      for (int q = 0; q < splits; ++q) v += ld_cluster_f32(cluster_map(off, static_cast<uint32_t>(q)));
+      Y[static_cast<int64_t>(m) * N + static_cast<int64_t>(nt) * kTileN + r] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
   }
-  if (splits == 1) return;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0)
-    s_last = !s_abort && (atomicAdd(counters + nt, 1u) == static_cast<uint32_t>(splits - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // the last CTA of the tile adds the K ranges in split order (deterministic)
-  const int total = static_cast<int>(M) * kTileN;
-  for (int idx = threadIdx.x; idx < total; idx += kMmaThreads) {
-    const int64_t m = idx / kTileN;
-    const int64_t n = static_cast<int64_t>(nt) * kTileN + idx % kTileN;
-    const float* p = partials + m * N + n;
-    float v = 0.0f;
-#pragma unroll 4
-    for (int s = 0; s < splits; ++s) v += __ldcg(p + static_cast<int64_t>(s) * M * N);
-    Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  }
-  if (threadIdx.x == 0) counters[nt] = 0u;
+  __syncwarp();
+  cluster_sync();
 }
 
-// Split K only for parallelism: the split count whose CTAs fill whole waves of
-// the resident CTA slots best (three per SM for M <= 8, two otherwise), with
-// the FP32 partial sums (written and read back once) at most a quarter of the
-// weight bytes; fewer splits on a near tie.
+// Clusters of `cs` CTAs of w4a16_mma_kernel<NT> that fit on the GPU at once
+// (cudaOccupancyMaxActiveClusters; wide clusters pack the GPCs less densely),
+// for cs = 1 .. kMmaMaxCluster, queried once per device.
+template <int NT>
+static int max_active_clusters(int cs) {
+  static std::mutex mu;
+  static std::unordered_map<int, std::array<int, kMmaMaxCluster + 1>> table;  // device -> count per size
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = table.find(dev);
+  if (it == table.end()) {
+    std::array<int, kMmaMaxCluster + 1> t{};
+    if (set_smem_once(w4a16_mma_kernel<NT>, MmaCfg<NT>::kSmem, true) == cudaSuccess) {
+      for (int c = 1; c <= kMmaMaxCluster; ++c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(c), 1);
+        cfg.blockDim = dim3(kMmaThreads);
+        cfg.dynamicSmemBytes = MmaCfg<NT>::kSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, w4a16_mma_kernel<NT>, &cfg) != cudaSuccess) n = 0;
+        t[c] = n;
+      }
+    }
+    (void)cudaGetLastError();
+    it = table.emplace(dev, t).first;
+  }
+  return it->second[cs];
+}
+
+// Split K only for parallelism.  Time model per split count s (a cluster of s
+// CTAs per tile): waves x (start-up + stages per CTA x the time one CTA takes
+// for a stage), where a wave holds as many clusters as fit at once and the
+// CTAs of a wave share the HBM bandwidth, or less when they are too few to
+// keep enough bytes in flight (each has at most a ring of stages in flight for
+// a loaded memory latency).  Fewer splits on a near tie.  The split-K sums
+// never leave the GPC: no workspace.
 SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
+  (void)num_sms;  // the cluster occupancy table already counts the SMs
   SplitPlan p;
   const int64_t tiles = N / kTileN;
   const int64_t KS = K / kMmaStageCols;
-  const int64_t slots = (M <= 8 ? 3 : 2) * static_cast<int64_t>(num_sms);
-  int64_t cap = static_cast<int64_t>(0.25 * 0.51953125 * static_cast<double>(K) / (8.0 * static_cast<double>(M)));
-  if (cap > KS) cap = KS;
-  if (cap > 32) cap = 32;
-  if (cap < 1) cap = 1;
-  int64_t s = 1;
-  double best = -1.0;
+  const bool nt1 = M <= 8;
+  const double bw = 6.5e12, latency = 2.5e-6, startup = 3e-6;
+  const int ring = nt1 ? MmaCfg<1>::kStages : MmaCfg<2>::kStages;
+  const double stage_bytes = kMmaCodeBytes + 640.0 + 2.0 * kMmaStageCols * static_cast<double>(M);
+  const int64_t cap = KS < kMmaMaxCluster ? KS : kMmaMaxCluster;
+  int64_t best_s = 1;
+  double best_t = 1e30;
   for (int64_t c = 1; c <= cap; ++c) {
     const int64_t per = (KS + c - 1) / c;
-    const int64_t real = (KS + per - 1) / per;  // splits actually formed
-    const int64_t ctas = tiles * real;
-    const int64_t waves = (ctas + slots - 1) / slots;
-    const double eff = static_cast<double>(ctas) / static_cast<double>(waves * slots);
-    if (eff > best + 0.02) {
-      best = eff;
-      s = real;
+    const int64_t s = (KS + per - 1) / per;  // splits actually formed
+    if (s != c) continue;
+    const int64_t fit = nt1 ? max_active_clusters<1>(static_cast<int>(s)) : max_active_clusters<2>(static_cast<int>(s));
+    if (fit <= 0) continue;
+    const int64_t waves = (tiles + fit - 1) / fit;
+    const double conc = static_cast<double>((tiles < fit ? tiles : fit) * s);  // CTAs running together
+    const double inflight = conc * ring * stage_bytes / latency;
+    const double bw_eff = inflight < bw ? inflight : bw;
+    const double t = static_cast<double>(waves) * (startup + static_cast<double>(per) * stage_bytes * conc / bw_eff);
+    if (t < best_t * 0.98) {
+      best_t = t;
+      best_s = s;
     }
   }
-  const int64_t per = (KS + s - 1) / s;
-  s = (KS + per - 1) / per;
-  p.splits = static_cast<int>(s);
+  const int64_t per = (KS + best_s - 1) / best_s;
+  p.splits = static_cast<int>(best_s);
   p.kb_per_split = static_cast<int>(per);  // here: stages of 256 columns per split
   p.tiles = tiles;
-  p.ws_bytes = s > 1 ? counters_bytes(tiles) + sizeof(float) * static_cast<size_t>(s) * M * N : 0;
+  p.ws_bytes = 0;
   return p;
 }
 
@@ -406,31 +467,34 @@ bool mma_path_ok(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K % kMmaSta
 
 template <int NT>
 static cudaError_t launch_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
-                              uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, float* partials,
-                              uint32_t* counters, int* err, cudaStream_t st) {
-  cudaError_t e = set_smem_once(w4a16_mma_kernel<NT>, MmaCfg<NT>::kSmem);
+                              uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, int* err,
+                              cudaStream_t st) {
+  cudaError_t e = set_smem_once(w4a16_mma_kernel<NT>, MmaCfg<NT>::kSmem, true);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(N / kTileN), plan.splits);
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.splits), static_cast<unsigned>(N / kTileN));
   cfg.blockDim = dim3(kMmaThreads);
   cfg.dynamicSmemBytes = MmaCfg<NT>::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(plan.splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, w4a16_mma_kernel<NT>, X, codes, scales, zeros, Y, M, N, K, plan.kb_per_split,
-                            plan.splits, partials, counters, err);
+                            plan.splits, err);
 }
 
 cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                              uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, int* err,
                              cudaStream_t st) {
-  uint32_t* counters = static_cast<uint32_t*>(ws);
-  float* partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.tiles)) : nullptr;
-  if (M <= 8) return launch_mma<1>(X, codes, scales, zeros, Y, M, N, K, plan, partials, counters, err, st);
-  return launch_mma<2>(X, codes, scales, zeros, Y, M, N, K, plan, partials, counters, err, st);
+  (void)ws;  // the split-K reduction runs in distributed shared memory
+  if (M <= 8) return launch_mma<1>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
+  return launch_mma<2>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
 }
 
 }  // namespace qlin

@@ -64,11 +64,10 @@ extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, co
   st = noalloc_scratch(&scratch);
   if (st != QLIN_OK) return st;
   auto cs = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents: the per-tile counters must
-  // start at zero, the partial sums are overwritten before they are read.
-  if (plan.splits > 1 && cudaMemsetAsync(scratch, 0, counters_bytes(plan.tiles), cs) != cudaSuccess)
-    return QLIN_ERR_CUDA;
-  void* ws = plan.splits > 1 ? scratch : nullptr;
+  // The array keeps the previous call's contents: the counters must start at
+  // zero, the partial sums are overwritten before they are read.
+  if (plan.zero_bytes > 0 && cudaMemsetAsync(scratch, 0, plan.zero_bytes, cs) != cudaSuccess) return QLIN_ERR_CUDA;
+  void* ws = plan.ws_bytes > 0 ? scratch : nullptr;
   const auto* Xp = static_cast<const uint16_t*>(X_bf16);
   const auto* cp = static_cast<const uint8_t*>(codes);
   const auto* sp = static_cast<const uint16_t*>(scales_f16);

@@ -455,10 +455,13 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
             // 16 tokens x several splits of independent loads in flight per thread
 #pragma unroll 4
             for (int s = 0; s < a.splits; ++s) {
-              const float* p = a.partials + (static_cast<int64_t>(s) * a.M + mbase + c0) * a.N + n;
+              float* p = a.partials + (static_cast<int64_t>(s) * a.M + mbase + c0) * a.N + n;
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                if (mbase + c0 + i < a.M) acc_v[i] += __ldcg(p + static_cast<int64_t>(i) * a.N);
+                if (mbase + c0 + i < a.M) {  // read and clear: the workspace is left zero-filled
+                  acc_v[i] += __ldcg(p + static_cast<int64_t>(i) * a.N);
+                  __stcg(p + static_cast<int64_t>(i) * a.N, 0.0f);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {

@@ -200,16 +200,62 @@ def test_w8a8_prefill_sampled(M, K, N):
 
 # ------------------------------------------------------------------ boundary on device
 
+def test_shared_workspace_mixed_shapes():
+    """One workspace shared by calls of different shapes and kernels, twice over:
+    each output equals the one computed with a private workspace, and the shared
+    buffer is left all zero (the split-K counters, the work queue and the
+    partial sums are all cleared by the calls that used them)."""
+    w4 = [(1, 28672, 4096), (16, 4096, 14336), (4, 6144, 4096), (3, 512, 640), (64, 4096, 4096)]
+    cases = []
+    for i, (M, N, K) in enumerate(w4):
+        lin = W4A16Linear(to_dev(syn.make_weight(N, K, seed=40 + i)))
+        X = to_dev(syn.make_act(M, K, seed=50 + i))
+        cases.append(("w4", M, N, K, lin, X, lin(X).clone()))
+    lin8 = W8A8Linear(to_dev(syn.make_weight(4096, 4096, seed=60)))
+    X8 = to_dev(syn.make_act(4, 4096, seed=61))
+    Xq8, sx8 = lin8.quant_act(X8)
+    cases.append(("w8", 4, 4096, 4096, lin8, (Xq8, sx8), lin8.gemm(Xq8, sx8).clone()))
+    need = max(q.qlin_workspace_size(q.OP_W4A16_GEMM if c[0] == "w4" else q.OP_W8A8_GEMM, c[1], c[2], c[3])
+               for c in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        outs = []
+        for kind, M, N, K, lin, X, _ in cases:
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            if kind == "w4":
+                q.qlin_w4a16_gemm(X, lin.codes, lin.scales, lin.zeros, Y.view(torch.int16), M, N, K, 128, ws,
+                                  ws.numel())
+            else:
+                q.qlin_w8a8_fp8_gemm(X[0], X[1], lin.Wq, lin.sw, Y.view(torch.int16), M, N, K, ws, ws.numel())
+            outs.append(Y)
+        torch.cuda.synchronize()
+        for (kind, M, N, K, _, _, ref), Y in zip(cases, outs):
+            assert torch.equal(Y, ref), (kind, M, N, K)
+        assert int(torch.count_nonzero(ws)) == 0
+    assert q.qlin_get_device_error() == 0
+
+
 def test_workspace_too_small_and_empty():
-    W = syn.make_weight(4096, 4096, seed=1)
+    # K = 4224 is not a multiple of 256: the CUDA-core GEMV serves M = 4 and
+    # keeps its split-K partial sums in the workspace
+    K = 4224
+    W = syn.make_weight(4096, K, seed=1)
     layer = W4A16Linear(to_dev(W))
-    X = to_dev(syn.make_act(4, 4096, seed=2))
+    X = to_dev(syn.make_act(4, K, seed=2))
     Y = torch.empty((4, 4096), dtype=torch.bfloat16, device="cuda")
-    need = q.qlin_workspace_size(q.OP_W4A16_GEMM, 4, 4096, 4096)
+    need = q.qlin_workspace_size(q.OP_W4A16_GEMM, 4, 4096, K)
     assert need > 0
     with pytest.raises(q.QlinError) as e:
-        q.qlin_w4a16_gemm(X, layer.codes, layer.scales, layer.zeros, Y.view(torch.int16), 4, 4096, 4096, 128,
+        q.qlin_w4a16_gemm(X, layer.codes, layer.scales, layer.zeros, Y.view(torch.int16), 4, 4096, K, 128,
                           None, 0)
     assert e.value.status == 4
-    q.qlin_w4a16_gemm(X, layer.codes, layer.scales, layer.zeros, Y.view(torch.int16), 0, 4096, 4096, 128, None, 0)
+    q.qlin_w4a16_gemm(X, layer.codes, layer.scales, layer.zeros, Y.view(torch.int16), 0, 4096, K, 128, None, 0)
+    # the small-M tensor-core kernel adds its split-K sums in distributed shared memory: no workspace
+    X4 = to_dev(syn.make_act(4, 4096, seed=3))
+    lin = W4A16Linear(to_dev(syn.make_weight(4096, 4096, seed=4)))
+    Y4 = torch.empty((4, 4096), dtype=torch.bfloat16, device="cuda")
+    q.qlin_w4a16_gemm_ex(X4, lin.codes, lin.scales, lin.zeros, Y4.view(torch.int16), 4, 4096, 4096, 128, None, 0,
+                         q.PATH_GEMV)
+    torch.cuda.synchronize()
+    assert torch.equal(Y4, lin(X4, path=q.PATH_GEMV))
     assert q.qlin_get_device_error() == 0
