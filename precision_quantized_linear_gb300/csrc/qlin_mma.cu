@@ -8,19 +8,21 @@
 //     sum_k x_k s (q_k - z) = s ( sum_k x_k (128 + q_k) - (128 + z) sum_k x_k ),
 // where 128 + q_k is exact in BF16.  The packed layout gives each lane of an
 // mma.sync quad its own 32-bit word per record (four A-fragment pairs), so a
-// pair comes out with one LOP3 (ALU pipe) after a right shift by a constant,
-// done as a high multiply on the otherwise idle FMA pipe; the MMA accumulates
+// pair comes out with one LOP3 after a right shift by a constant (a high
+// multiply on the FMA pipe instead of the shift measured slower: it stalls
+// dispatch); the MMA accumulates
 // sum_k x_k (128 + q_k) in FP32 and the scale / zero-point are applied once
 // per group and row in FP32 registers.
 //
-// One CTA = one 128-row tile x one K range.  Warp 8 streams, per stage of 256
+// One CTA = one 128-row tile x one K range.  Warp 4 streams, per stage of 256
 // columns, the tile's packed codes (16 KB), scales and zero-points and the
 // activation slice of every token into a ring of shared-memory stages with
 // bulk copies (weights first, before waiting for the previous kernel on the
-// stream).  Warps 0-7 each own 16 rows (one m16 block) and every token (one
-// or two n8 blocks).  Warp 9 forms the per-group activation sums sum_k x_k of
-// each stage once for the whole CTA, on the tensor core (an m16 A operand of
-// all ones), and leaves them in the stage for the folds.  The K ranges of one
+// stream).  Warps 0-3 each own 32 rows (two m16 blocks that share every B
+// fragment) and every token (one or two n8 blocks).  Warp 5 forms the
+// per-group activation sums sum_k x_k of each stage once for the whole CTA,
+// on the tensor core (an m16 A operand of all ones), and leaves them in the
+// stage for the folds.  The K ranges of one
 // tile run as a thread-block cluster and add their partial sums through
 // distributed shared memory, in rank order.
 #include <cuda_bf16.h>
@@ -41,7 +43,8 @@ constexpr int kMmaMetaOff = kMmaCodeBytes;         // 2 groups x 128 FP16 scales
 constexpr int kMmaSumOff = kMmaMetaOff + 640;      // FP32 activation sums [2 groups][16 tokens]
 constexpr int kMmaXOff = kMmaCodeBytes + 1024;     // activation rows
 constexpr int kMmaXRow = kMmaStageCols * 2 + 16;   // 528 B per token row (conflict-free B fragments)
-constexpr int kMmaConsumers = 8;                   // consumer warps, 16 rows (one m16 block) each
+constexpr int kMmaRowBlocks = 2;                   // m16 row blocks per consumer warp
+constexpr int kMmaConsumers = kTileN / (16 * kMmaRowBlocks);  // consumer warps, 32 rows each
 constexpr int kMmaProducer = kMmaConsumers;        // bulk-copy warp
 constexpr int kMmaSummer = kMmaConsumers + 1;      // activation-sum warp
 constexpr int kMmaThreads = (kMmaConsumers + 2) * 32;
@@ -111,10 +114,9 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   uint64_t* summed = empty + C::kStages;  // activation sums of the stage are in place
   __shared__ volatile int s_abort;
   // extraction constants, read back from shared memory so that the compiler
-  // keeps them in registers: the nibble mask and BF16 magic as the two register
-  // operands of one LOP3, and the multipliers 2^28, 2^24, 2^20 whose high
-  // products are the right shifts by 4, 8, 12 on the FMA pipe
-  __shared__ volatile uint32_t s_kc[5];
+  // keeps them in registers: the nibble mask and the BF16 magic become the two
+  // register operands of one LOP3
+  __shared__ volatile uint32_t s_kc[2];
 
   const int split = blockIdx.x, nt = blockIdx.y;  // the K ranges of a tile form one cluster (rank = split)
   const int64_t KS = K / kMmaStageCols;
@@ -135,9 +137,6 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     s_abort = 0;
     s_kc[0] = 0x000F000Fu;
     s_kc[1] = 0x43004300u;
-    s_kc[2] = 1u << 28;
-    s_kc[3] = 1u << 24;
-    s_kc[4] = 1u << 20;
   }
   // token rows >= M are never copied: zero them once so B fragments need no bounds test
   for (int idx = threadIdx.x; idx < C::kStages * (C::kTok - mrows) * (kMmaXRow / 16); idx += kMmaThreads) {
@@ -172,11 +171,13 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   grid_dep_launch();
 
   const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
-  float acc[NT][4];
+  float acc[kMmaRowBlocks][NT][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j)
+  for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[rb][j][e] = 0.0f;
 
   if (warp == kMmaProducer) {
     // ------------------------------------------------------------ producer
@@ -230,17 +231,19 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
       if (lane < 4) mbar_arrive(&summed[slot]);
     }
   } else {
-    // ------------------------------------------------------------ consumers: rows 16*warp .. 16*warp + 15
-    const int r0 = warp * 16 + gq;  // this thread's rows: r0 and r0 + 8
+    // ------------------------------------------------------------ consumers: rows 32*warp .. 32*warp + 31
+    // row block rb (m16) of this warp: rows 32 warp + 16 rb + (0..15); this
+    // thread's rows in it are rr(rb) and rr(rb) + 8.  Both blocks share every B
+    // fragment and activation sum.
+    const int rbase = warp * 16 * kMmaRowBlocks + gq;
+    auto rr = [&](int rb) { return rbase + 16 * rb; };
     const uint32_t kmask = s_kc[0], kmagic = s_kc[1];
-    const uint32_t kshr[3] = {s_kc[2], s_kc[3], s_kc[4]};
-    // pair in nibble positions i, i + 4 of w, as BF16x2 (128 + q)
-    auto pair_at = [&](uint32_t w, int i) {
-      return nib_pair_bf16(i == 0 ? w : __umulhi(w, kshr[i - 1]), kmask, kmagic);
-    };
-    // zero-point nibble of rows r0, r0+8 (same parity): moved to bits 16..19 of an FP32
-    // whose exponent is 2^7, which reads as 128 + z exactly
-    const uint32_t zsh = (r0 & 1) ? 12u : 16u;
+    // pair in nibble positions i, i + 4 of w, as BF16x2 (128 + q): a constant
+    // shift and one LOP3
+    auto pair_at = [&](uint32_t w, int i) { return nib_pair_bf16(w >> (4 * i), kmask, kmagic); };
+    // zero-point nibble of this thread's rows (all of the same parity): moved to
+    // bits 16..19 of an FP32 whose exponent is 2^7, which reads as 128 + z exactly
+    const uint32_t zsh = (rbase & 1) ? 12u : 16u;
     for (int i = 0; i < nst; ++i) {
       const int slot = i % C::kStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort))) {
@@ -251,27 +254,34 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
       const uint32_t st = smem_u32(ring + slot * C::kStage);  // shared-space address of the stage
       const uint32_t sc = st + kMmaMetaOff;                   // FP16 scales [2][128]
       const uint32_t zp = st + kMmaMetaOff + 512;             // zero nibbles [2][64]
-      // word t (this lane's) of the records of rows r0, r0+8 in both halves of a
-      // 64-column tile; each tile's words are loaded one tile ahead so that the
-      // shared-memory latency is hidden
-      uint32_t cw[4];
-      auto load_codes = [&](int kbl, uint32_t (&w)[4]) {
+      // word t (this lane's) of the records of each of this thread's rows in both
+      // halves of a 64-column tile: w[rb][2h + e] = half h, row rr(rb) + 8e.  Each
+      // tile's words are loaded one tile ahead to hide the shared-memory latency.
+      uint32_t cw[kMmaRowBlocks][4];
+      auto load_codes = [&](int kbl, uint32_t (&w)[kMmaRowBlocks][4]) {
         const uint32_t tile = st + kbl * 4096 + tq * 4;
-        w[0] = lds32(tile + r0 * 16);               // half 0, row r0
-        w[1] = lds32(tile + (r0 + 8) * 16);         // half 0, row r0+8
-        w[2] = lds32(tile + 2048 + r0 * 16);        // half 1, row r0
-        w[3] = lds32(tile + 2048 + (r0 + 8) * 16);  // half 1, row r0+8
+#pragma unroll
+        for (int rb = 0; rb < kMmaRowBlocks; ++rb) {
+          w[rb][0] = lds32(tile + rr(rb) * 16);
+          w[rb][1] = lds32(tile + (rr(rb) + 8) * 16);
+          w[rb][2] = lds32(tile + 2048 + rr(rb) * 16);
+          w[rb][3] = lds32(tile + 2048 + (rr(rb) + 8) * 16);
+        }
       };
       load_codes(0, cw);
       bool sums_ok = true;
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
-        // two accumulators (one per 64-column tile) keep two MMA chains in flight
-        float c[2][NT][4];
+        // one accumulator per 64-column tile and row block: independent MMA chains
+        float c[2][kMmaRowBlocks][NT][4];
 #pragma unroll
         for (int kb2 = 0; kb2 < 2; ++kb2) {
           const int kbl = grp * 2 + kb2;  // 64-column tile within the stage
-          const uint32_t cur[4] = {cw[0], cw[1], cw[2], cw[3]};
+          uint32_t cur[kMmaRowBlocks][4];
+#pragma unroll
+          for (int rb = 0; rb < kMmaRowBlocks; ++rb)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) cur[rb][q] = cw[rb][q];
           if (kbl < 3) load_codes(kbl + 1, cw);
           // B fragments: one ldmatrix.x4 per token block covers two 16-column k-steps
           uint32_t b[2][NT][2][2];
@@ -284,41 +294,47 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {  // k-step = columns 16a .. 16a+15 of half h
             const int h = ks >> 1, ia = 2 * (ks & 1);
-            uint32_t a[4];
-            a[0] = pair_at(cur[2 * h], ia);          // row r0,   columns 2t, 2t+1
-            a[1] = pair_at(cur[2 * h + 1], ia);      // row r0+8, columns 2t, 2t+1
-            a[2] = pair_at(cur[2 * h], ia + 1);      // row r0,   columns 2t+8, 2t+9
-            a[3] = pair_at(cur[2 * h + 1], ia + 1);  // row r0+8, columns 2t+8, 2t+9
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              const uint32_t(&bk)[2] = b[h][j][ks & 1];
-              if (ks == 0)  // first k-step of the tile starts the chain from zero
-                mma_bf16_16816_z(c[kb2][j], a, bk[0], bk[1]);
-              else
-                mma_bf16_16816(c[kb2][j], a, bk[0], bk[1]);
+            for (int rb = 0; rb < kMmaRowBlocks; ++rb) {
+              uint32_t a[4];
+              a[0] = pair_at(cur[rb][2 * h], ia);          // row rr,   columns 2t, 2t+1
+              a[1] = pair_at(cur[rb][2 * h + 1], ia);      // row rr+8, columns 2t, 2t+1
+              a[2] = pair_at(cur[rb][2 * h], ia + 1);      // row rr,   columns 2t+8, 2t+9
+              a[3] = pair_at(cur[rb][2 * h + 1], ia + 1);  // row rr+8, columns 2t+8, 2t+9
+#pragma unroll
+              for (int j = 0; j < NT; ++j) {
+                const uint32_t(&bk)[2] = b[h][j][ks & 1];
+                if (ks == 0)  // first k-step of the tile starts the chain from zero
+                  mma_bf16_16816_z(c[kb2][rb][j], a, bk[0], bk[1]);
+                else
+                  mma_bf16_16816(c[kb2][rb][j], a, bk[0], bk[1]);
+              }
             }
           }
         }
-        // fold: y += s (sum x (128 + q) - (128 + z) sum x); rows r0, r0+8; tokens 8j+2t, +1
+        // fold: y += s (sum x (128 + q) - (128 + z) sum x); tokens 8j+2t, +1
         if (grp == 0)
           sums_ok = __all_sync(0xffffffffu, mbar_wait(&summed[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort));
         float2 xv[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) xv[j] = lds64f(st + kMmaSumOff + (grp * 16 + j * 8 + 2 * tq) * 4);
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = r0 + hr * 8;
-          const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(sc + (grp * kTileN + r) * 2))));
-          const uint32_t zb = lds8(zp + grp * (kTileN / 2) + r / 2);
-          const float cz = __uint_as_float(((zb << zsh) & 0x000F0000u) | 0x43000000u);
+        for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const float c0 = c[0][j][hr * 2] + c[1][j][hr * 2];
-            const float c1 = c[0][j][hr * 2 + 1] + c[1][j][hr * 2 + 1];
-            acc[j][hr * 2] = fmaf(s, fmaf(-cz, xv[j].x, c0), acc[j][hr * 2]);
-            acc[j][hr * 2 + 1] = fmaf(s, fmaf(-cz, xv[j].y, c1), acc[j][hr * 2 + 1]);
+          for (int hr = 0; hr < 2; ++hr) {
+            const int r = rr(rb) + hr * 8;
+            const float s =
+                __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(sc + (grp * kTileN + r) * 2))));
+            const uint32_t zb = lds8(zp + grp * (kTileN / 2) + r / 2);
+            const float cz = __uint_as_float(((zb << zsh) & 0x000F0000u) | 0x43000000u);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              const float c0 = c[0][rb][j][hr * 2] + c[1][rb][j][hr * 2];
+              const float c1 = c[0][rb][j][hr * 2 + 1] + c[1][rb][j][hr * 2 + 1];
+              acc[rb][j][hr * 2] = fmaf(s, fmaf(-cz, xv[j].x, c0), acc[rb][j][hr * 2]);
+              acc[rb][j][hr * 2 + 1] = fmaf(s, fmaf(-cz, xv[j].y, c1), acc[rb][j][hr * 2 + 1]);
+            }
           }
-        }
       }
       if (!sums_ok) {
         set_error(err, QLIN_ERR_TIMEOUT);
@@ -331,19 +347,22 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   }
 
   // ---------------------------------------------------------------- outputs
+  // this thread's outputs: row 32 warp + 16 rb + gq + 8 hr, token 8 j + 2 tq + e
   if (splits == 1) {
     if (warp < kMmaConsumers) {
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int64_t n = static_cast<int64_t>(nt) * kTileN + warp * 16 + gq + hr * 8;
+      for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+        for (int hr = 0; hr < 2; ++hr) {
+          const int64_t n = static_cast<int64_t>(nt) * kTileN + warp * 16 * kMmaRowBlocks + 16 * rb + gq + hr * 8;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int64_t m = j * 8 + 2 * tq + e;
-            if (m < M) Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j][hr * 2 + e]));
-          }
-      }
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int64_t m = j * 8 + 2 * tq + e;
+              if (m < M) Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[rb][j][hr * 2 + e]));
+            }
+        }
     }
     return;
   }
@@ -358,11 +377,15 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   __syncthreads();  // every warp is done with the ring
   if (warp < kMmaConsumers) {
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr)
+    for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
+      for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) red[(j * 8 + 2 * tq + e) * kTileN + warp * 16 + gq + hr * 8] = acc[j][hr * 2 + e];
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            red[(j * 8 + 2 * tq + e) * kTileN + warp * 16 * kMmaRowBlocks + 16 * rb + gq + hr * 8] =
+                acc[rb][j][hr * 2 + e];
   }
   __syncwarp();
   cluster_sync();
