@@ -25,6 +25,7 @@
 // stage for the folds.  The K ranges of one
 // tile run as a thread-block cluster and add their partial sums through
 // distributed shared memory, in rank order.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,6 +37,8 @@
 #include "qlin_ptx.cuh"
 
 namespace qlin {
+
+namespace cg = cooperative_groups;
 
 constexpr int kMmaStageCols = 256;                 // K columns per stage (4 code tiles)
 constexpr int kMmaCodeBytes = 4 * 4096;            // codes of one stage
@@ -50,13 +53,17 @@ constexpr int kMmaSummer = kMmaConsumers + 1;      // activation-sum warp
 constexpr int kMmaThreads = (kMmaConsumers + 2) * 32;
 constexpr uint64_t kMmaWaitNs = 2000000000ull;
 constexpr int kMmaMaxCluster = 16;                 // CTAs of one tile's split-K cluster (non-portable above 8)
+constexpr int kMmaRedRows = 144;                   // >= splits x ceil(128 / splits) for splits <= 16
 
 template <int NT>
 struct MmaCfg {
   static constexpr int kTok = 8 * NT;
   static constexpr int kStage = ((kMmaXOff + kTok * kMmaXRow) + 1023) / 1024 * 1024;
-  static constexpr int kStages = NT == 1 ? 3 : 4;  // M <= 8: three CTAs fit per SM
-  static constexpr int kSmem = 1024 + kStages * kStage + 256;
+  static constexpr int kStages = 3;  // three CTAs fit per SM for M <= 8, two otherwise
+  // split-K receive buffer: [token][source rank][row within the owner's slice];
+  // ranks x slice rows <= 140 for every split count up to 16
+  static constexpr int kRedFloats = kTok * kMmaRedRows;
+  static constexpr int kSmem = 1024 + kStages * kStage + 256 + kRedFloats * 4;
   static constexpr int kMinBlocks = NT == 1 ? 3 : 2;
 };
 
@@ -112,6 +119,8 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kStages * C::kStage);
   uint64_t* empty = full + C::kStages;
   uint64_t* summed = empty + C::kStages;  // activation sums of the stage are in place
+  uint64_t* red_bar = summed + C::kStages;  // split-K: every rank's partial rows have arrived
+  float* red = reinterpret_cast<float*>(ring + C::kStages * C::kStage + 256);
   __shared__ volatile int s_abort;
   // extraction constants, read back from shared memory so that the compiler
   // keeps them in registers: the nibble mask and the BF16 magic become the two
@@ -133,6 +142,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
       mbar_init(&empty[i], kMmaConsumers);
       mbar_init(&summed[i], 4);
     }
+    mbar_init(red_bar, static_cast<uint32_t>(splits));
     fence_mbar_init();
     s_abort = 0;
     s_kc[0] = 0x000F000Fu;
@@ -146,6 +156,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     *reinterpret_cast<uint4*>(ring + stg * C::kStage + kMmaXOff + row * kMmaXRow + c16 * 16) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
+  if (splits > 1) cluster_arrive_relaxed();  // waited for before the split-K exchange
 
   const uint32_t tx = kMmaCodeBytes + 2 * 256 + 2 * 64 + mrows * kMmaStageCols * 2;
   auto issue_w = [&](int i) {  // weights of stage i (ring slot i % C::kStages)
@@ -366,44 +377,51 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     }
     return;
   }
-  // Split K: the CTAs of the tile's cluster add their partial sums through
-  // distributed shared memory.  Each leaves its FP32 sums [token][row] in its
-  // own ring (every stage has been consumed and no copy is in flight); after a
-  // cluster barrier, rank q adds rows [q R, q R + R) over ranks 0, 1, ... in
-  // order (deterministic) and writes them; a second barrier keeps every CTA's
-  // shared memory alive until all ranks have read it.  Every thread of every
-  // CTA reaches both barriers, also after a timed-out wait.
-  float* red = reinterpret_cast<float*>(ring);
-  __syncthreads();  // every warp is done with the ring
+  // Split K: rank q of the tile's cluster owns rows [q R, q R + R).  Every CTA
+  // stores its partial sums of each row into the owner's receive buffer
+  // (distributed shared memory) and arrives once on each owner's red_bar with
+  // cluster-scope release; each owner waits for all ranks, adds the slots in
+  // rank order (deterministic) from its own shared memory and writes Y.  No
+  // CTA reads another's shared memory, so none waits for the others to exit.
+  const int R = (kTileN + splits - 1) / splits;
+  const int r_lo = split * R, r_n = static_cast<int>(imin64(kTileN, r_lo + R)) - r_lo;
+  cg::cluster_group cluster = cg::this_cluster();
+  __syncwarp();
+  cluster_wait();  // pairs with the arrival after the barrier set-up: every red_bar is initialised
   if (warp < kMmaConsumers) {
 #pragma unroll
     for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr)
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = warp * 16 * kMmaRowBlocks + 16 * rb + gq + hr * 8;
+        const int q = r / R;
+        float* dst = cluster.map_shared_rank(red, static_cast<unsigned>(q));
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            red[(j * 8 + 2 * tq + e) * kTileN + warp * 16 * kMmaRowBlocks + 16 * rb + gq + hr * 8] =
-                acc[rb][j][hr * 2 + e];
+          for (int e = 0; e < 2; ++e) {
+            const int m = j * 8 + 2 * tq + e;
+            if (m < mrows) dst[(m * splits + split) * R + (r - q * R)] = acc[rb][j][hr * 2 + e];
+          }
+      }
   }
-  __syncwarp();
-  cluster_sync();
-  const int R = (kTileN + splits - 1) / splits;
-  const int r_lo = split * R, r_n = static_cast<int>(imin64(kTileN, r_lo + R)) - r_lo;
+  __syncthreads();  // this CTA's stores precede the releasing arrivals below
+  if (threadIdx.x < static_cast<unsigned>(splits) && static_cast<int>(threadIdx.x) * R < kTileN)
+    mbar_arrive_remote(red_bar, threadIdx.x);
   if (r_n > 0) {
-    const uint32_t red_u32 = smem_u32(red);
+    if (!mbar_wait_cluster(red_bar, 0, kMmaWaitNs)) {
+      set_error(err, QLIN_ERR_TIMEOUT);
+      return;
+    }
     for (int idx = threadIdx.x; idx < r_n * mrows; idx += kMmaThreads) {
-      const int m = idx / r_n, r = r_lo + idx % r_n;
-      const uint32_t off = red_u32 + static_cast<uint32_t>(m * kTileN + r) * 4u;
+      const int m = idx / r_n, rl = idx % r_n;
+      const float* src = red + m * splits * R + rl;
       float v = 0.0f;
-      for (int q = 0; q < splits; ++q) v += ld_cluster_f32(cluster_map(off, static_cast<uint32_t>(q)));
-      Y[static_cast<int64_t>(m) * N + static_cast<int64_t>(nt) * kTileN + r] =
+      for (int p = 0; p < splits; ++p) v += src[p * R];
+      Y[static_cast<int64_t>(m) * N + static_cast<int64_t>(nt) * kTileN + r_lo + rl] =
           __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
   }
-  __syncwarp();
-  cluster_sync();
 }
 
 // Clusters of `cs` CTAs of w4a16_mma_kernel<NT> that fit on the GPU at once
