@@ -25,7 +25,6 @@
 // stage for the folds.  The K ranges of one
 // tile run as a thread-block cluster and add their partial sums through
 // distributed shared memory, in rank order.
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -37,8 +36,6 @@
 #include "qlin_ptx.cuh"
 
 namespace qlin {
-
-namespace cg = cooperative_groups;
 
 constexpr int kMmaStageCols = 256;                 // K columns per stage (4 code tiles)
 constexpr int kMmaCodeBytes = 4 * 4096;            // codes of one stage
@@ -60,8 +57,8 @@ struct MmaCfg {
   static constexpr int kTok = 8 * NT;
   static constexpr int kStage = ((kMmaXOff + kTok * kMmaXRow) + 1023) / 1024 * 1024;
   static constexpr int kStages = 3;  // three CTAs fit per SM for M <= 8, two otherwise
-  // split-K receive buffer: [token][source rank][row within the owner's slice];
-  // ranks x slice rows <= 140 for every split count up to 16
+  // split-K receive buffer: [source rank][row within the owner's slice][token
+  // slot]; ranks x slice rows <= 140 for every split count up to 16
   static constexpr int kRedFloats = kTok * kMmaRedRows;
   static constexpr int kSmem = 1024 + kStages * kStage + 256 + kRedFloats * 4;
   static constexpr int kMinBlocks = NT == 1 ? 3 : 2;
@@ -136,27 +133,14 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   const int64_t KB = K / kTileK;
   const int mrows = static_cast<int>(imin64(M, C::kTok));
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kMmaConsumers);
-      mbar_init(&summed[i], 4);
-    }
-    mbar_init(red_bar, static_cast<uint32_t>(splits));
-    fence_mbar_init();
-    s_abort = 0;
-    s_kc[0] = 0x000F000Fu;
-    s_kc[1] = 0x43004300u;
-  }
-  // token rows >= M are never copied: zero them once so B fragments need no bounds test
-  for (int idx = threadIdx.x; idx < C::kStages * (C::kTok - mrows) * (kMmaXRow / 16); idx += kMmaThreads) {
-    const int per = (C::kTok - mrows) * (kMmaXRow / 16);
-    const int stg = idx / per, rem = idx % per;
-    const int row = mrows + rem / (kMmaXRow / 16), c16 = rem % (kMmaXRow / 16);
-    *reinterpret_cast<uint4*>(ring + stg * C::kStage + kMmaXOff + row * kMmaXRow + c16 * 16) = make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
-  if (splits > 1) cluster_arrive_relaxed();  // waited for before the split-K exchange
+  // split K: rank q of the tile's cluster owns rows [lo(q), lo(q + 1)), lo(q) = 128 q / splits
+  // (at least eight rows for every split count up to 16)
+  auto row_lo = [&](int q) { return q * kTileN / splits; };
+  const int r_lo = row_lo(split), r_n = row_lo(split + 1) - r_lo;
+  const int rstride = (kTileN + splits - 1) / splits;  // slice rows of the receive buffer
+  // token groups a source sends per row: lane tq holds tokens 2tq, 2tq+1 (and
+  // 8+2tq, 9+2tq); groups whose first token is >= M are all zero and not sent
+  const int groups = NT == 1 ? (mrows + 1) / 2 : 4;
 
   const uint32_t tx = kMmaCodeBytes + 2 * 256 + 2 * 64 + mrows * kMmaStageCols * 2;
   auto issue_w = [&](int i) {  // weights of stage i (ring slot i % C::kStages)
@@ -175,9 +159,31 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     for (int m = 0; m < mrows; ++m)
       bulk_load(st + kMmaXOff + m * kMmaXRow, X + m * K + k0, kMmaStageCols * 2, &full[i % C::kStages]);
   };
-  // weights never depend on the previous kernel on the stream: start them first
-  if (warp == kMmaProducer && lane == 0)
+  if (warp == kMmaProducer && lane == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMmaConsumers);
+      mbar_init(&summed[i], 4);
+    }
+    mbar_init(red_bar, 1);
+    fence_mbar_init();
+    // the owner's one arrival, with the bytes every rank will store into its slice
+    if (splits > 1) mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(splits * r_n * groups * 2 * NT * 4));
+    s_abort = 0;
+    s_kc[0] = 0x000F000Fu;
+    s_kc[1] = 0x43004300u;
+    // weights never depend on the previous kernel on the stream: start them first
     for (int i = 0; i < nst && i < C::kStages; ++i) issue_w(i);
+  }
+  // token rows >= M are never copied: zero them once so B fragments need no bounds test
+  for (int idx = threadIdx.x; idx < C::kStages * (C::kTok - mrows) * (kMmaXRow / 16); idx += kMmaThreads) {
+    const int per = (C::kTok - mrows) * (kMmaXRow / 16);
+    const int stg = idx / per, rem = idx % per;
+    const int row = mrows + rem / (kMmaXRow / 16), c16 = rem % (kMmaXRow / 16);
+    *reinterpret_cast<uint4*>(ring + stg * C::kStage + kMmaXOff + row * kMmaXRow + c16 * 16) = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  if (splits > 1) cluster_arrive_relaxed();  // waited for before the first access to another CTA
   grid_dep_wait();
   grid_dep_launch();
 
@@ -255,6 +261,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     // zero-point nibble of this thread's rows (all of the same parity): moved to
     // bits 16..19 of an FP32 whose exponent is 2^7, which reads as 128 + z exactly
     const uint32_t zsh = (rbase & 1) ? 12u : 16u;
+    if (splits > 1) cluster_wait();  // overlaps the first stage's load
     for (int i = 0; i < nst; ++i) {
       const int slot = i % C::kStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort))) {
@@ -377,50 +384,44 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     }
     return;
   }
-  // Split K: rank q of the tile's cluster owns rows [q R, q R + R).  Every CTA
-  // stores its partial sums of each row into the owner's receive buffer
-  // (distributed shared memory) and arrives once on each owner's red_bar with
-  // cluster-scope release; each owner waits for all ranks, adds the slots in
-  // rank order (deterministic) from its own shared memory and writes Y.  No
-  // CTA reads another's shared memory, so none waits for the others to exit.
-  const int R = (kTileN + splits - 1) / splits;
-  const int r_lo = split * R, r_n = static_cast<int>(imin64(kTileN, r_lo + R)) - r_lo;
-  cg::cluster_group cluster = cg::this_cluster();
+  // Split K: every CTA sends each row's token values to the row's owner with
+  // one asynchronous remote store (8 or 16 bytes: the tokens this lane holds,
+  // slot tq * 2NT + 2j + e for token 8j + 2tq + e) that completes its bytes on
+  // the owner's red_bar, so no fence or barrier among the CTAs is needed.  Each
+  // owner, once every rank's values have landed, adds the slots in rank order
+  // (deterministic) from its own shared memory and writes Y.
   __syncwarp();
-  cluster_wait();  // pairs with the arrival after the barrier set-up: every red_bar is initialised
-  if (warp < kMmaConsumers) {
+  if (warp >= kMmaConsumers) cluster_wait();  // the consumers waited at their start
+  if (warp < kMmaConsumers && tq < groups) {
+    const uint32_t red_u32 = smem_u32(red), bar_u32 = smem_u32(red_bar);
 #pragma unroll
     for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int r = warp * 16 * kMmaRowBlocks + 16 * rb + gq + hr * 8;
-        const int q = r / R;
-        float* dst = cluster.map_shared_rank(red, static_cast<unsigned>(q));
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int m = j * 8 + 2 * tq + e;
-            if (m < mrows) dst[(m * splits + split) * R + (r - q * R)] = acc[rb][j][hr * 2 + e];
-          }
+        const int q = (r * splits + splits - 1) / kTileN;  // owner: the last rank with lo(q) <= r
+        const uint32_t dst = cluster_map(red_u32, static_cast<uint32_t>(q)) +
+                             static_cast<uint32_t>(((split * rstride + r - row_lo(q)) * C::kTok + tq * 2 * NT) * 4);
+        const uint32_t dbar = cluster_map(bar_u32, static_cast<uint32_t>(q));
+        if constexpr (NT == 1)
+          st_async_v2(dst, acc[rb][0][hr * 2], acc[rb][0][hr * 2 + 1], dbar);
+        else
+          st_async_v4(dst, acc[rb][0][hr * 2], acc[rb][0][hr * 2 + 1], acc[rb][NT - 1][hr * 2],
+                      acc[rb][NT - 1][hr * 2 + 1], dbar);
       }
   }
-  __syncthreads();  // this CTA's stores precede the releasing arrivals below
-  if (threadIdx.x < static_cast<unsigned>(splits) && static_cast<int>(threadIdx.x) * R < kTileN)
-    mbar_arrive_remote(red_bar, threadIdx.x);
-  if (r_n > 0) {
-    if (!mbar_wait_cluster(red_bar, 0, kMmaWaitNs)) {
-      set_error(err, QLIN_ERR_TIMEOUT);
-      return;
-    }
-    for (int idx = threadIdx.x; idx < r_n * mrows; idx += kMmaThreads) {
-      const int m = idx / r_n, rl = idx % r_n;
-      const float* src = red + m * splits * R + rl;
-      float v = 0.0f;
-      for (int p = 0; p < splits; ++p) v += src[p * R];
-      Y[static_cast<int64_t>(m) * N + static_cast<int64_t>(nt) * kTileN + r_lo + rl] =
-          __bfloat16_as_ushort(__float2bfloat16_rn(v));
-    }
+  if (!mbar_wait_cluster(red_bar, 0, kMmaWaitNs)) {
+    set_error(err, QLIN_ERR_TIMEOUT);
+    return;
+  }
+  for (int idx = threadIdx.x; idx < r_n * mrows; idx += kMmaThreads) {
+    const int m = idx / r_n, rl = idx % r_n;
+    const int slot = NT == 1 ? m : ((m & 7) >> 1) * 4 + (m >> 3) * 2 + (m & 1);
+    const float* src = red + rl * C::kTok + slot;
+    float v = 0.0f;
+    for (int p = 0; p < splits; ++p) v += src[p * rstride * C::kTok];
+    Y[static_cast<int64_t>(m) * N + static_cast<int64_t>(nt) * kTileN + r_lo + rl] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(v));
   }
 }
 
