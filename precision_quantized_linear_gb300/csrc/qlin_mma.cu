@@ -212,8 +212,10 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     }
   } else if (warp == kMmaSummer) {
     // ------------------------------------------------------------ activation sums per group and token
-    // C = ones(16 x 128) * X_g^T: every row of C holds sum_k x_k of the n8 block's
-    // tokens; lanes 0-3 (row 0) write tokens 8j + 2t, 8j + 2t + 1.
+    // M <= 8: C = ones(16 x 128) * X_g^T, every row of C holds sum_k x_k of the
+    // n8 token block; lanes 0-3 (row 0) write tokens 2t, 2t + 1.
+    // M <= 16: C = X_g (16 tokens x 128) * ones(128 x 8), one MMA per k-step for
+    // all 16 tokens; lanes 4g (column 0) write tokens g and g + 8.
     const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // BF16 1.0 pairs
     for (int i = 0; i < nst; ++i) {
       const int slot = i % C::kStages;
@@ -223,15 +225,15 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
         break;
       }
       const uint32_t st = smem_u32(ring + slot * C::kStage);
+      float* sums = reinterpret_cast<float*>(ring + slot * C::kStage + kMmaSumOff);  // [group][16 tokens]
 #pragma unroll
-      for (int grp = 0; grp < 2; ++grp)
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          float cs[2][4];  // two chains of four k-steps
+      for (int grp = 0; grp < 2; ++grp) {
+        float cs[2][4];  // two chains of four k-steps
+        if constexpr (NT == 1) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t bb[2][2];
-            ldsm_b2(st + kMmaXOff + (j * 8 + (lane & 7)) * kMmaXRow + (grp * 128 + q * 32 + (lane >> 3) * 8) * 2, bb);
+            ldsm_b2(st + kMmaXOff + (lane & 7) * kMmaXRow + (grp * 128 + q * 32 + (lane >> 3) * 8) * 2, bb);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (q == 0)
@@ -240,11 +242,30 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
                 mma_bf16_16816(cs[h], ones, bb[h][0], bb[h][1]);
             }
           }
-          if (lane < 4) {
-            float2 v = make_float2(cs[0][0] + cs[1][0], cs[0][1] + cs[1][1]);
-            *reinterpret_cast<float2*>(ring + slot * C::kStage + kMmaSumOff + (grp * 16 + j * 8 + 2 * lane) * 4) = v;
+          if (lane < 4)
+            *reinterpret_cast<float2*>(sums + grp * 16 + 2 * lane) =
+                make_float2(cs[0][0] + cs[1][0], cs[0][1] + cs[1][1]);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            // A fragment of tokens 0-15 x columns 16ks..16ks+15: lanes 0-15 address
+            // token rows (lane & 15) at column 16ks, lanes 16-31 at 16ks + 8
+            uint32_t a[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                         : "r"(st + kMmaXOff + (lane & 15) * kMmaXRow + (grp * 128 + ks * 16 + (lane >> 4) * 8) * 2));
+            if (ks < 2)
+              mma_bf16_16816_z(cs[ks & 1], a, ones[0], ones[1]);
+            else
+              mma_bf16_16816(cs[ks & 1], a, ones[0], ones[1]);
+          }
+          if (tq == 0) {
+            sums[grp * 16 + gq] = cs[0][0] + cs[1][0];
+            sums[grp * 16 + gq + 8] = cs[0][2] + cs[1][2];
           }
         }
+      }
+      __syncwarp();
       if (lane < 4) mbar_arrive(&summed[slot]);
     }
   } else {
