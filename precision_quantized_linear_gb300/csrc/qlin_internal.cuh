@@ -93,7 +93,9 @@ int device_num_sms(int* out);
 int* device_error_word();
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
+// swizzle128: 128-byte swizzled shared-memory tiles (MMA operands), else a plain row-major box.
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t inner,
-                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                    bool swizzle128 = true);
 
 }  // namespace qlin

@@ -52,7 +52,9 @@ struct TcCfg {
   static constexpr int kAStages = W4 ? 4 : 0;                   // A slots (one 64-column block each)
   static constexpr int kAStage = (W4 && !kATmem) ? 128 * kBlkBytes : 0;  // shared-memory bytes per slot
   static constexpr int kASlotCols = 32;                         // TMEM columns per slot (64 BF16 per lane)
-  static constexpr int kStagesRaw = (kSmemBudget - 2048 - kAStages * kAStage) / kStage;
+  // output staging: two boxes of 16 tokens x 128 rows of BF16 for the tensor stores
+  static constexpr int kEpiBox = 16 * kTileN * 2;
+  static constexpr int kStagesRaw = (kSmemBudget - 2048 - kAStages * kAStage - 2 * kEpiBox) / kStage;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kAccCols = BN;                           // one accumulator
   static constexpr int kAColBase = 2 * BN;                      // first TMEM column of the A slots
@@ -62,7 +64,8 @@ struct TcCfg {
   static constexpr int kDqWarps = W4 ? 8 : 0;
   static constexpr int kEpiWarp0 = 2 + kDqWarps;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStage + kAStages * kAStage + 1024 /*barriers*/;
+  static constexpr int kSmemBytes =
+      1024 /*align slack*/ + kStages * kStage + kAStages * kAStage + 2 * kEpiBox + 1024 /*barriers*/;
   static_assert(kStages >= 2, "pipeline too shallow");
   static_assert(kXBlk % 1024 == 0 && kStage % 1024 == 0, "1024-byte alignment of swizzled tiles");
   static_assert(W4 || KPS == 1, "E4M3 stages hold one K block");
@@ -142,13 +145,14 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
 template <int BN, bool W4, int KPS>
 __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                   const __grid_constant__ TcArgs a) {
+                   const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ TcArgs a) {
   using C = TcCfg<BN, W4, KPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint8_t* aring = ring + C::kStages * C::kStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(aring + C::kAStages * C::kAStage);
+  uint8_t* epi_box = aring + C::kAStages * C::kAStage;  // [2][16 tokens][128 rows] BF16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_box + 2 * C::kEpiBox);
   uint64_t* full = bars;                       // [kStages]  producer -> consumers (tx bytes)
   uint64_t* empty = full + C::kStages;         // [kStages]  consumers -> producer
   uint64_t* a_full = empty + C::kStages;       // [kAStages] dequant -> MMA
@@ -181,6 +185,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmap_x);
     if constexpr (!W4) prefetch_tensormap(&tmap_w);
+    prefetch_tensormap(&tmap_y);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -400,6 +405,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
     const int quad = warp & 3;                       // TMEM lane quadrant of this warp
     const float s_w = W4 ? 1.0f : *a.sw;
     int ua = 0;
+    uint32_t epi_n = 0;  // staging boxes used so far
     for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++ua) {
       const Unit un = unit_of(a, u, KB);
       const int acc = ua & 1;
@@ -416,24 +422,44 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
       const uint32_t tmem_d = tmem_base + acc * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const bool direct = a.splits == 1;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN && have; c0 += 16) {
+      for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem_d + c0, v);
-        tmem_ld_wait();
-        if (c0 + 16 >= BN) {  // the whole accumulator has been read: hand it back to the MMA
+        if (have) {
+          tmem_ld16(tmem_d + c0, v);
+          tmem_ld_wait();
+        }
+        if (have && c0 + 16 >= BN) {  // the whole accumulator has been read: hand it back to the MMA
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
+        if (direct) {
+          // 16 tokens x 128 rows as BF16 into a staging box, then one tensor store
+          // (rows past M are clipped by the tensor map); the two boxes alternate
+          // over the stores issued.  Whether this block of tokens exists is the
+          // same for all 128 threads, so they skip the barriers together.
+          if (mbase + c0 < a.M) {
+            uint16_t* box = reinterpret_cast<uint16_t*>(epi_box + (epi_n & 1) * C::kEpiBox);
+            if (t == 0) bulk_wait_read<1>();  // the store before last, from this box, has read it
+            named_bar_epi();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int64_t m = mbase + c0 + i;
-          if (m < a.M) {
-            const float x = __uint_as_float(v[i]);
-            if (direct)
-              a.Y[m * a.N + n] = W4 ? to_bf16(x) : to_bf16((x * __ldg(a.sx + m)) * s_w);
-            else
-              __stcg(a.partials + (static_cast<int64_t>(un.split) * a.M + m) * a.N + n, x);
+            for (int i = 0; i < 16; ++i) {
+              const int64_t m = mbase + c0 + i;
+              const float x = have ? __uint_as_float(v[i]) : 0.0f;
+              box[i * kTileN + quad * 32 + lane] =  // this thread's row of the tile: TMEM lane quad * 32 + lane
+                  W4 ? to_bf16(x) : to_bf16(m < a.M ? (x * __ldg(a.sx + m)) * s_w : 0.0f);
+            }
+            fence_proxy_async_smem();
+            named_bar_epi();
+            if (t == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(mbase + c0));
+            ++epi_n;
+          }
+        } else if (have) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int64_t m = mbase + c0 + i;
+            if (m < a.M)
+              __stcg(a.partials + (static_cast<int64_t>(un.split) * a.M + m) * a.N + n, __uint_as_float(v[i]));
           }
         }
       }
@@ -474,6 +500,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
         named_bar_epi();  // s_last is read by all before the next unit rewrites it
       }
     }
+    if (t == 0) bulk_wait_all();  // every tensor store has written its box
   }
 
   tc_fence_before();
@@ -572,8 +599,8 @@ TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan
 TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false); }
 
 template <int BN, bool W4, int KPS>
-static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, TcArgs args, const TcPlan& plan,
-                             void* ws, int num_sms, cudaStream_t st) {
+static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
+                             const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   using C = TcCfg<BN, W4, KPS>;
   cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -602,27 +629,27 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, TcArg
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS>, tx, tw, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS>, tx, tw, ty, args);
 }
 
 template <bool W4>
-static cudaError_t launch_tc_bn(const CUtensorMap& tx, const CUtensorMap& tw, const TcArgs& a, const TcPlan& plan,
-                                void* ws, int num_sms, cudaStream_t st) {
+static cudaError_t launch_tc_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const TcArgs& a,
+                                const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   if constexpr (W4) {
-    if (plan.bn == 16) return plan.kps == 4 ? launch_tc<16, true, 4>(tx, tw, a, plan, ws, num_sms, st)
-                                            : launch_tc<16, true, 2>(tx, tw, a, plan, ws, num_sms, st);
-    if (plan.bn == 32) return plan.kps == 4 ? launch_tc<32, true, 4>(tx, tw, a, plan, ws, num_sms, st)
-                                            : launch_tc<32, true, 2>(tx, tw, a, plan, ws, num_sms, st);
-    if (plan.bn == 64) return launch_tc<64, true, 2>(tx, tw, a, plan, ws, num_sms, st);
-    if (plan.bn == 128) return launch_tc<128, true, 1>(tx, tw, a, plan, ws, num_sms, st);
-    return launch_tc<256, true, 1>(tx, tw, a, plan, ws, num_sms, st);
+    if (plan.bn == 16) return plan.kps == 4 ? launch_tc<16, true, 4>(tx, tw, ty, a, plan, ws, num_sms, st)
+                                            : launch_tc<16, true, 2>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 32) return plan.kps == 4 ? launch_tc<32, true, 4>(tx, tw, ty, a, plan, ws, num_sms, st)
+                                            : launch_tc<32, true, 2>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 64) return launch_tc<64, true, 2>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 128) return launch_tc<128, true, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
+    return launch_tc<256, true, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
   } else {
     switch (plan.bn) {
-      case 16: return launch_tc<16, false, 1>(tx, tw, a, plan, ws, num_sms, st);
-      case 32: return launch_tc<32, false, 1>(tx, tw, a, plan, ws, num_sms, st);
-      case 64: return launch_tc<64, false, 1>(tx, tw, a, plan, ws, num_sms, st);
-      case 128: return launch_tc<128, false, 1>(tx, tw, a, plan, ws, num_sms, st);
-      default: return launch_tc<256, false, 1>(tx, tw, a, plan, ws, num_sms, st);
+      case 16: return launch_tc<16, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
+      case 32: return launch_tc<32, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
+      case 64: return launch_tc<64, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
+      case 128: return launch_tc<128, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
+      default: return launch_tc<256, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
     }
   }
 }
@@ -630,8 +657,10 @@ static cudaError_t launch_tc_bn(const CUtensorMap& tx, const CUtensorMap& tw, co
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
                             int num_sms, cudaStream_t st) {
-  CUtensorMap tx;
+  CUtensorMap tx, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, K * 2, 64, plan.bn))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, N * 2, kTileN, 16, false))
     return cudaErrorInvalidValue;
   TcArgs a{};
   a.codes = codes;
@@ -642,15 +671,17 @@ cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint1
   a.M = M;
   a.N = N;
   a.K = K;
-  return launch_tc_bn<true>(tx, tx, a, plan, ws, num_sms, st);
+  return launch_tc_bn<true>(tx, tx, ty, a, plan, ws, num_sms, st);
 }
 
 cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                            int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
                            cudaStream_t st) {
-  CUtensorMap tx, tw;
+  CUtensorMap tx, tw, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, K, N, K, 128, 128)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, N * 2, kTileN, 16, false))
+    return cudaErrorInvalidValue;
   TcArgs a{};
   a.sx = sx;
   a.sw = sw;
@@ -659,7 +690,7 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
   a.M = M;
   a.N = N;
   a.K = K;
-  return launch_tc_bn<false>(tx, tw, a, plan, ws, num_sms, st);
+  return launch_tc_bn<false>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
 }  // namespace qlin
