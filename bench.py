@@ -217,15 +217,11 @@ def run_ours(args):
     stream = torch.cuda.Stream()
     peaks = load_peaks()
 
-    def issue(r, events=None):
-        for i, (M, L) in enumerate(calls):
+    def issue(r):
+        for M, L in calls:
             c, s, z = L["sets"][r]
-            if events:
-                events[i][0].record(stream)
             q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
                               ws.numel(), stream)
-            if events:
-                events[i][1].record(stream)
 
     # correctness of the launch configuration before timing
     with torch.cuda.stream(stream):
@@ -235,23 +231,14 @@ def run_ours(args):
     if err:
         raise RuntimeError("device error %d before timing" % err)
 
-    # one CUDA graph per rotation set; the timed graphs hold only the kernels
-    # (programmatic launches of consecutive kernels may overlap), a second set
-    # with CUDA events around each kernel attributes device time per kernel
-    ext_ok = make_event(True) is not None
-    graphs, ev_graphs, gevents = [], [], []
+    # one CUDA graph per rotation set, holding only the kernels (programmatic
+    # launches of consecutive kernels may overlap)
+    graphs = []
     for r in range(ROTATE):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             issue(r)
         graphs.append(g)
-        if ext_ok:
-            evs = [(make_event(True), make_event(True)) for _ in calls]
-            ge = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(ge, stream=stream):
-                issue(r, evs)
-            ev_graphs.append(ge)
-            gevents.append(evs)
     torch.cuda.synchronize()
 
     for i in range(args.warmup):
@@ -273,42 +260,34 @@ def run_ours(args):
     clk = clocks.stop()
     step_ms_local = e0.elapsed_time(e1) / args.steps
     step_ms = dist_max(step_ms_local, world)
-    if ext_ok:  # attribution pass: each instrumented graph once, right after the timed region
-        with torch.cuda.stream(stream):
-            for r in range(ROTATE):
-                ev_graphs[r].replay()
-        torch.cuda.synchronize()
 
     weight_bytes = sum(w4_weight_bytes(L["N"], L["K"]) for M, L in calls)
     alg_bytes = sum(w4_alg_bytes(M, L["N"], L["K"]) for M, L in calls)
     value = world * weight_bytes / (step_ms * 1e-3) / 1e9
 
-    # per-kernel device time in the timed region (last replay of every graph)
+    # per-kernel device time, right after the timed region: a graph of each call's
+    # launches over the rotating weight copies (consecutive launches overlap as in
+    # the step), replayed and timed with CUDA events; events between the launches
+    # of the step itself would serialise them and add their own gaps
     per_kernel = {}
     per_call = []
-    if ext_ok:
-        for r in range(ROTATE):
-            for i, (M, L) in enumerate(calls):
-                a, b = gevents[r][i]
-                per_call.append((M, L, a.elapsed_time(b)))
-    else:  # fallback: a graph of each call alone, timed with events
-        for M, L in calls:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for r in range(ROTATE):
-                    c, s, z = L["sets"][r]
-                    q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
-                                      ws.numel(), stream)
-            g.replay()
-            torch.cuda.synchronize()
-            a, b = make_event(False), make_event(False)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                for _ in range(5):
-                    g.replay()
-                b.record(stream)
-            torch.cuda.synchronize()
-            per_call.append((M, L, a.elapsed_time(b) / (5 * ROTATE)))
+    for M, L in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(ROTATE):
+                c, s, z = L["sets"][r]
+                q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
+                                  ws.numel(), stream)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = make_event(False), make_event(False)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(5):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        per_call.append((M, L, a.elapsed_time(b) / (5 * ROTATE)))
     for M, L, ms in per_call:
         k = kernel_of(M)
         d = per_kernel.setdefault(k, {"ms": 0.0, "launches": 0, "bytes": 0})
@@ -336,10 +315,11 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "layers_KxN": [[K, N] for _, K, N in LAYERS_8B], "M": list(MS_DECODE),
                    "G": 128, "calls_per_step": len(calls), "weight_bytes_per_step": weight_bytes,
                    "alg_bytes_per_step": alg_bytes, "l2": "4 rotating weight copies (%.0f MB > 3x L2)" %
-                   (ROTATE * weight_bytes / 1e6 / len(MS_DECODE)), "timing": "CUDA graph per step, CUDA events; per-kernel times from an event-instrumented replay of the same graphs"},
+                   (ROTATE * weight_bytes / 1e6 / len(MS_DECODE)), "timing": "CUDA graph per step, CUDA events; per-kernel times from a graph of each call's launches over the rotating weight copies, timed with CUDA events after the timed region"},
         "per_M_weight_gbs": per_m_gbs,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "frac_in_step": round(alg_bytes / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                      "traffic": (round(TRAFFIC_CAPTURE["dram_bytes"] / TRAFFIC_CAPTURE["alg_bytes"]
                                        * dk["bytes"] / dk["launches"])
                                  if dom == TRAFFIC_CAPTURE["kernel"] else None),
