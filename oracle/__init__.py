@@ -77,6 +77,12 @@ def _load():
         lib.orc_quant_fp8_rows.argtypes = [_p, _i64, _i64, _p, _p]
         lib.orc_quant_fp8_tensor.restype = None
         lib.orc_quant_fp8_tensor.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.orc_quant_fp8_act_blocks.restype = None
+        lib.orc_quant_fp8_act_blocks.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.orc_quant_fp8_weight_blocks.restype = None
+        lib.orc_quant_fp8_weight_blocks.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.orc_w8a8_blocks_at.restype = None
+        lib.orc_w8a8_blocks_at.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p]
         lib.orc_gemm_nt_f64.restype = None
         lib.orc_gemm_nt_f64.argtypes = [_p, _p, _i64, _i64, _i64, _p]
         lib.orc_w4a16_at.restype = None
@@ -291,3 +297,59 @@ def roofline_transition_batch(ridge_flop_per_byte: float, bytes_per_weight: floa
     """[TP] arithmetic intensity of a decode GEMM, AI(B) = 2B / bytes_per_weight;
     the compute-bound transition is the batch where AI reaches the ridge."""
     return ridge_flop_per_byte * bytes_per_weight / 2.0
+
+
+# ---------------------------------------------------------------- FP8 block scaling
+
+def quant_fp8_act_blocks(X_bf16: np.ndarray):
+    """[LP] S8 block scaling, 1 x 128 activation blocks: Xq [M][K] E4M3 and
+    sx [K/128][M] (block-major), each block's scale amax / 448."""
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    M, K = X.shape
+    assert K % 128 == 0
+    Xq = np.empty((M, K), np.uint8)
+    sx = np.empty((K // 128, M), np.float32)
+    _load().orc_quant_fp8_act_blocks(_ptr(X), M, K, _ptr(Xq), _ptr(sx))
+    return Xq, sx
+
+
+def quant_fp8_weight_blocks(W_bf16: np.ndarray):
+    """[LP] S8 block scaling, 128 x 128 weight blocks: Wq [N][K] E4M3 and
+    sw [N/128][K/128]."""
+    W = np.ascontiguousarray(W_bf16, dtype=np.uint16)
+    N, K = W.shape
+    assert N % 128 == 0 and K % 128 == 0
+    Wq = np.empty((N, K), np.uint8)
+    sw = np.empty((N // 128, K // 128), np.float32)
+    _load().orc_quant_fp8_weight_blocks(_ptr(W), N, K, _ptr(Wq), _ptr(sw))
+    return Wq, sw
+
+
+def w8a8_blocks_full(Xq, sx, Wq, sw) -> np.ndarray:
+    """Y = sum over K blocks b of diag(sx[b]) (dec(Xq_b) . dec(Wq_b)^T) sw[:, b] in double."""
+    tab = e4m3_table()
+    A = tab[Xq]
+    B = tab[Wq]
+    M, K = A.shape
+    N = B.shape[0]
+    Y = np.zeros((M, N), np.float64)
+    for b in range(K // 128):
+        part = gemm_nt_f64(np.ascontiguousarray(A[:, b * 128:(b + 1) * 128]),
+                           np.ascontiguousarray(B[:, b * 128:(b + 1) * 128]))
+        Y += part * np.asarray(sx[b], np.float64)[:, None] * np.repeat(np.asarray(sw[:, b], np.float64), 128)[None, :]
+    return Y
+
+
+def w8a8_blocks_at(Xq, sx, Wq, sw, ms, ns) -> np.ndarray:
+    Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape, np.float64)
+    _load().orc_w8a8_blocks_at(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), M, N, K, _ptr(ms), _ptr(ns), ms.size,
+                               _ptr(out))
+    return out

@@ -335,6 +335,78 @@ void orc_quant_fp8_tensor(const uint16_t *W, int64_t N, int64_t K, uint8_t *Wq, 
 }
 
 /* ------------------------------------------------------------------ */
+/* FP8 block scaling ([LP] S8 "Block Scaling": every block has its own    */
+/* scale, x ~ x_fp8 * scale_block, scale_block = amax_block / max_fp8).   */
+/* Blocks: 1 x 128 for activations (token m, columns 128b .. 128b+127),   */
+/* 128 x 128 for weights (rows 128i.., columns 128b..).  Scales FP32,     */
+/* the same amax / 448 (1 for an all-zero block) and E4M3 RNE-saturating  */
+/* cast of x / scale (binary32 division) as the per-token recipe.         */
+/* Activation scales are stored block-major: sx[b][m], b = k / 128.       */
+/* ------------------------------------------------------------------ */
+
+void orc_quant_fp8_act_blocks(const uint16_t *X, int64_t M, int64_t K, uint8_t *Xq, float *sx)
+{
+    int64_t nb = K / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < nb; b++) {
+            float amax = 0.0f;
+            for (int64_t k = b * 128; k < b * 128 + 128; k++) {
+                float a = fabsf(bf16_to_f32(X[m * K + k]));
+                if (a > amax) amax = a;
+            }
+            float sc = amax_scale(amax);
+            sx[b * M + m] = sc;
+            for (int64_t k = b * 128; k < b * 128 + 128; k++)
+                Xq[m * K + k] = orc_f32_to_e4m3_rn_sat(bf16_to_f32(X[m * K + k]) / sc);
+        }
+}
+
+/* Weight blocks: W [N][K] -> Wq [N][K], sw[i][b] for rows 128i.., columns 128b... */
+void orc_quant_fp8_weight_blocks(const uint16_t *W, int64_t N, int64_t K, uint8_t *Wq, float *sw)
+{
+    int64_t nr = N / 128, nb = K / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t i = 0; i < nr; i++)
+        for (int64_t b = 0; b < nb; b++) {
+            float amax = 0.0f;
+            for (int64_t n = i * 128; n < i * 128 + 128; n++)
+                for (int64_t k = b * 128; k < b * 128 + 128; k++) {
+                    float a = fabsf(bf16_to_f32(W[n * K + k]));
+                    if (a > amax) amax = a;
+                }
+            float sc = amax_scale(amax);
+            sw[i * nb + b] = sc;
+            for (int64_t n = i * 128; n < i * 128 + 128; n++)
+                for (int64_t k = b * 128; k < b * 128 + 128; k++)
+                    Wq[n * K + k] = orc_f32_to_e4m3_rn_sat(bf16_to_f32(W[n * K + k]) / sc);
+        }
+}
+
+/* Block-scaled W8A8: Y[m][n] = sum_b sx[b][m] * sw[n/128][b] *            */
+/* sum_{k in block b} e4m3(Xq[m][k]) * e4m3(Wq[n][k]), in double, at       */
+/* `cnt` (m, n) pairs.                                                     */
+void orc_w8a8_blocks_at(const uint8_t *Xq, const float *sx, const uint8_t *Wq, const float *sw,
+                        int64_t M, int64_t N, int64_t K,
+                        const int64_t *ms, const int64_t *ns, int64_t cnt, double *out)
+{
+    int64_t nb = K / 128;
+    (void)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < cnt; i++) {
+        int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t b = 0; b < nb; b++) {
+            double part = 0.0;
+            for (int64_t k = b * 128; k < b * 128 + 128; k++)
+                part += orc_e4m3_to_f64(Xq[m * K + k]) * orc_e4m3_to_f64(Wq[n * K + k]);
+            acc += part * (double)sx[b * M + m] * (double)sw[(n / 128) * nb + b];
+        }
+        out[i] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* The linear layer Y = A . B^T, accumulated in double, no rounding of Y. */
 /* [LP] S1 / S22: wide accumulation; the double result is the exact      */
 /* target that the device's FP32-accumulated, BF16-rounded Y is held to. */

@@ -413,3 +413,92 @@ def test_roofline_transition_from_page_numbers():
     assert b == 73.75 and round(b) == t["value"]
     d = GOLDEN["decode_bf16_ai_flop_per_byte"]
     assert 2 * d["batch"] / d["bytes_per_weight"] == d["value"]
+
+
+# ---------------------------------------------------------------- FP8 block scaling ([LP] S8)
+
+def test_fp8_act_blocks_reduce_to_per_token():
+    """Each 1 x 128 block is quantised exactly as the per-token recipe would
+    quantise a 128-column row holding just that block."""
+    X = syn.make_act(5, 512, seed=21, token_outlier_frac=0.2)
+    X[1, 128:256] = 0                       # an all-zero block: scale 1, codes 0
+    Xq, sx = oracle.quant_fp8_act_blocks(X)
+    assert sx.shape == (4, 5)
+    for b in range(4):
+        q_ref, s_ref = oracle.quant_fp8_rows(np.ascontiguousarray(X[:, b * 128:(b + 1) * 128]))
+        assert np.array_equal(Xq[:, b * 128:(b + 1) * 128], q_ref)
+        assert np.array_equal(sx[b], s_ref)
+    assert sx[1, 1] == 1.0 and not Xq[1, 128:256].any()
+
+
+def test_fp8_weight_blocks_reduce_to_per_tensor():
+    """Each 128 x 128 block is quantised exactly as the per-tensor recipe would
+    quantise that block as a tensor of its own."""
+    W = syn.make_weight(256, 384, seed=22)
+    W[128:, :128] = 0
+    Wq, sw = oracle.quant_fp8_weight_blocks(W)
+    assert sw.shape == (2, 3)
+    for i in range(2):
+        for b in range(3):
+            blk = np.ascontiguousarray(W[i * 128:(i + 1) * 128, b * 128:(b + 1) * 128])
+            q_ref, s_ref = oracle.quant_fp8_tensor(blk)
+            assert np.array_equal(Wq[i * 128:(i + 1) * 128, b * 128:(b + 1) * 128], q_ref)
+            assert sw[i, b] == s_ref
+    assert sw[1, 0] == 1.0
+
+
+def test_w8a8_blocks_reduce_to_per_token_per_tensor():
+    """With every block scale of a token equal and one weight scale, the
+    block-scaled product is the per-token / per-tensor W8A8 product."""
+    rng = np.random.default_rng(23)
+    M, N, K = 3, 256, 384
+    Xq = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    Wq = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    Xq[(Xq & 0x7F) == 0x7F] = 0             # no NaN codes
+    Wq[(Wq & 0x7F) == 0x7F] = 0
+    sx_tok = np.array([0.5, 0.125, 2.0], np.float32)
+    sx = np.repeat(sx_tok[None, :], K // 128, axis=0)
+    sw = np.full((N // 128, K // 128), 0.25, np.float32)
+    ref = oracle.w8a8_full(Xq, sx_tok, Wq, 0.25)
+    ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    got = oracle.w8a8_blocks_at(Xq, sx, Wq, sw, ms.ravel(), ns.ravel()).reshape(M, N)
+    assert np.allclose(got, ref, rtol=1e-12, atol=0)
+    full = oracle.w8a8_blocks_full(Xq, sx, Wq, sw)
+    assert np.allclose(full, ref, rtol=1e-12, atol=0)
+
+
+def test_w8a8_blocks_scales_enter_per_block():
+    """Different scales per block: doubling one block's scale adds exactly that
+    block's partial product once more (checked on a brute-force sum)."""
+    rng = np.random.default_rng(24)
+    M, N, K = 2, 128, 256
+    Xq = rng.integers(0, 0x70, (M, K), dtype=np.uint8)
+    Wq = rng.integers(0, 0x70, (N, K), dtype=np.uint8)
+    sx = np.array([[1.0, 1.0], [1.0, 1.0]], np.float32)
+    sw = np.array([[1.0, 1.0]], np.float32)
+    base = oracle.w8a8_blocks_full(Xq, sx, Wq, sw)
+    sx2 = sx.copy()
+    sx2[1, 0] = 2.0                           # block 1, token 0
+    got = oracle.w8a8_blocks_full(Xq, sx2, Wq, sw)
+    tab = oracle.e4m3_table()
+    part = np.array([[sum(tab[Xq[m, k]] * tab[Wq[n, k]] for k in range(128, 256)) for n in range(N)] for m in range(M)])
+    assert np.allclose(got[0] - base[0], part[0], rtol=1e-12)
+    assert np.array_equal(got[1], base[1])
+
+
+def test_block_scaling_confines_an_outlier():
+    """The reason for block scaling ([LP] S8): an outlier only coarsens its own
+    block.  With one channel x4000, the per-token scale flushes some non-zero
+    values of the other blocks to code 0 (below E4M3's smallest subnormal at
+    that scale); the 1 x 128 block scales keep every one of them."""
+    X = syn.make_act(4, 1024, seed=25)
+    X32 = syn.bf16_bits_to_f32(X).astype(np.float64)
+    X32[:, 5] *= 4000.0
+    X = syn.f32_to_bf16_bits(X32.astype(np.float32))
+    nonzero = syn.bf16_bits_to_f32(X)[:, 128:] != 0
+    q1, _ = oracle.quant_fp8_rows(X)
+    qb, _ = oracle.quant_fp8_act_blocks(X)
+    flushed_tok = ((q1[:, 128:] & 0x7F) == 0) & nonzero
+    flushed_blk = ((qb[:, 128:] & 0x7F) == 0) & nonzero
+    assert flushed_tok.sum() > 0
+    assert flushed_blk.sum() == 0
