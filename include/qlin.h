@@ -70,6 +70,7 @@ typedef enum {
 #define QLIN_OP_W4A16_GEMM 1
 #define QLIN_OP_W8A8_GEMM 2
 #define QLIN_OP_QUANT_W_FP8 3
+#define QLIN_OP_W8A8_BLOCK_GEMM 4
 
 /* Kernel selection for the *_ex GEMM calls (measurement and ablation). */
 #define QLIN_PATH_AUTO 0   /* choose by M (the default of the plain calls) */
@@ -178,6 +179,33 @@ int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3
 int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                           void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                           int path, void* stream);
+
+/* ---- FP8 block scaling ([LP] S8 "Block Scaling": each block of the tensor
+ * has its own scale, x ~ x_fp8 * scale_block, scale_block = amax_block /
+ * max_fp8).  The pages leave the block shape and scale type open: here
+ * activations use 1 x 128 blocks (one token, 128 columns) and weights 128 x 128
+ * blocks, with FP32 scales computed exactly as the per-token recipe does
+ * (amax / 448, 1 for an all-zero block; E4M3 RNE with saturation of x / scale,
+ * binary32 division). */
+
+/* X [M][K] BF16 -> Xq [M][K] E4M3 and sx [K/128][M] FP32 (block-major: the
+ * scales of one K block of all tokens are contiguous).  K % 128 == 0.  sx
+ * 4-byte aligned, X and Xq 16-byte aligned.  Asynchronous, no workspace. */
+int qlin_quant_act_fp8_blocks(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream);
+
+/* W [N][K] BF16 -> Wq [N][K] E4M3 and sw [N/128][K/128] FP32 (row-block major).
+ * N % 128 == 0, K % 128 == 0.  Asynchronous, no workspace. */
+int qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* stream);
+
+/* Block-scaled W8A8: Y[m][n] = bf16( sum_b sx[b][m] * sw[n/128][b] *
+ * sum_{k in block b} Xq[m][k] * Wq[n][k] ), every block's product accumulated
+ * in FP32 on the tensor cores and promoted with its two scales into an FP32
+ * sum in block order.  Shapes and alignment as qlin_w8a8_fp8_gemm;
+ * workspace: qlin_workspace_size(QLIN_OP_W8A8_BLOCK_GEMM, ...) bytes (0 when the
+ * K range is not split), zero-filled, left zero-filled.  Deterministic. */
+int qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                             void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                             void* stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QLIN_OK, or the first error a kernel recorded since the last call. */

@@ -22,11 +22,13 @@ __all__ = [
     "qlin_status_string", "qlin_pack_format_version", "qlin_w4_packed_sizes", "qlin_workspace_size",
     "qlin_pack_w4", "qlin_w4a16_gemm", "qlin_w4a16_gemm_ex", "qlin_quant_act_fp8", "qlin_quant_w_fp8",
     "qlin_w8a8_fp8_gemm", "qlin_w8a8_fp8_gemm_ex", "qlin_get_device_error", "qlin_gemv_max_m",
-    "qlin_selftest_wait_timeout", "qlin_w4a16_gemv_noalloc", "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "PATH_AUTO", "PATH_GEMV", "PATH_TC",
+    "qlin_selftest_wait_timeout", "qlin_w4a16_gemv_noalloc", "qlin_quant_act_fp8_blocks", "qlin_quant_w_fp8_blocks",
+    "qlin_w8a8_fp8_block_gemm", "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "OP_W8A8_BLOCK_GEMM",
+    "PATH_AUTO", "PATH_GEMV", "PATH_TC",
     "PACK_FORMAT_VERSION",
 ]
 
-OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8 = 1, 2, 3
+OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM = 1, 2, 3, 4
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 PACK_FORMAT_VERSION = 2
 
@@ -54,6 +56,9 @@ _SIGS = {
     "qlin_get_device_error": [_p],
     "qlin_selftest_wait_timeout": [ctypes.c_uint32, _p],
     "qlin_w4a16_gemv_noalloc": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p],
+    "qlin_quant_act_fp8_blocks": [_p, _i64, _i64, _p, _p, _p],
+    "qlin_quant_w_fp8_blocks": [_p, _i64, _i64, _p, _p, _p],
+    "qlin_w8a8_fp8_block_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
 }
 
 
@@ -171,6 +176,22 @@ def qlin_w8a8_fp8_gemm_ex(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, path,
     return _check(load().qlin_w8a8_fp8_gemm_ex(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
                                                _ptr(workspace), ws_bytes, path, _stream(stream)),
                   "qlin_w8a8_fp8_gemm_ex")
+
+
+def qlin_quant_act_fp8_blocks(X, M, K, Xq, sx, stream=None):
+    return _check(load().qlin_quant_act_fp8_blocks(_ptr(X), M, K, _ptr(Xq), _ptr(sx), _stream(stream)),
+                  "qlin_quant_act_fp8_blocks")
+
+
+def qlin_quant_w_fp8_blocks(W, N, K, Wq, sw, stream=None):
+    return _check(load().qlin_quant_w_fp8_blocks(_ptr(W), N, K, _ptr(Wq), _ptr(sw), _stream(stream)),
+                  "qlin_quant_w_fp8_blocks")
+
+
+def qlin_w8a8_fp8_block_gemm(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_w8a8_fp8_block_gemm(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
+                                                  _ptr(workspace), ws_bytes, _stream(stream)),
+                  "qlin_w8a8_fp8_block_gemm")
 
 
 def qlin_get_device_error(stream=None) -> int:

@@ -185,6 +185,9 @@ int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes) 
     case QLIN_OP_W4A16_GEMM: *bytes = M == 0 ? 0 : ws_w4(M, N, K, d->num_sms); return QLIN_OK;
     case QLIN_OP_W8A8_GEMM: *bytes = M == 0 ? 0 : ws_w8(M, N, K, d->num_sms); return QLIN_OK;
     case QLIN_OP_QUANT_W_FP8: *bytes = 256; return QLIN_OK;
+    case QLIN_OP_W8A8_BLOCK_GEMM:
+      *bytes = M == 0 ? 0 : plan_w8a8_block_tc(M, N, K, d->num_sms).split.ws_bytes;
+      return QLIN_OK;
     default: return QLIN_ERR_INVALID_VALUE;
   }
 }
@@ -312,6 +315,52 @@ int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3
                        int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, void* stream) {
   return qlin_w8a8_fp8_gemm_ex(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, workspace, ws_bytes, QLIN_PATH_AUTO,
                                stream);
+}
+
+int qlin_quant_act_fp8_blocks(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream) {
+  if (M < 0 || M > kMaxM || K <= 0 || K % kGroup != 0 || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return QLIN_OK;
+  if (!X_bf16 || !Xq_e4m3 || !sx) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(X_bf16) || !aligned16(Xq_e4m3) || (reinterpret_cast<uintptr_t>(sx) & 3u)) return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_quant_act_fp8_blocks(static_cast<const uint16_t*>(X_bf16), M, K,
+                                                   static_cast<uint8_t*>(Xq_e4m3), sx,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+int qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* stream) {
+  int st = check_shape(0, N, K);
+  if (st != QLIN_OK) return st;
+  if (!W_bf16 || !Wq_e4m3 || !sw) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(W_bf16) || !aligned16(Wq_e4m3) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_quant_w_fp8_blocks(static_cast<const uint16_t*>(W_bf16), N, K,
+                                                 static_cast<uint8_t*>(Wq_e4m3), sw, static_cast<cudaStream_t>(stream)));
+}
+
+int qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                             void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  int st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  if (!Xq_e4m3 || !sx || !Wq_e4m3 || !sw || !Y_bf16) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(Xq_e4m3) || !aligned16(Wq_e4m3) || !aligned16(Y_bf16) || (workspace && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(sx) & 3u) || (reinterpret_cast<uintptr_t>(sw) & 3u))
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  const TcPlan p = plan_w8a8_block_tc(M, N, K, d->num_sms);
+  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_w8a8_block_tc(static_cast<const uint8_t*>(Xq_e4m3), sx,
+                                            static_cast<const uint8_t*>(Wq_e4m3), sw, static_cast<uint16_t*>(Y_bf16),
+                                            M, N, K, p, workspace, d->err, d->num_sms,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream) {

@@ -76,6 +76,7 @@ struct TcPlan {
 };
 TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
+TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
@@ -83,6 +84,14 @@ cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint1
 cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                            int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
                            cudaStream_t st);
+// FP8 block scaling: sx = [K/128][M], sw = [N/128][K/128] FP32 block scales.
+cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
+                                 int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
+                                 cudaStream_t st);
+cudaError_t launch_quant_act_fp8_blocks(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx,
+                                        cudaStream_t st);
+cudaError_t launch_quant_w_fp8_blocks(const uint16_t* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,
+                                      cudaStream_t st);
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* err, cudaStream_t st);
 

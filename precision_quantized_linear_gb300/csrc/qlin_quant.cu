@@ -236,4 +236,64 @@ cudaError_t launch_quant_w_fp8(const uint16_t* W, int64_t N, int64_t K, uint8_t*
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ FP8 block scaling
+
+// [LP] S8 block scaling, 1 x 128 activation blocks: one warp per (token m,
+// block b); lanes 0-15 hold eight columns each.  sx is block-major, sx[b][m].
+__global__ void __launch_bounds__(256) quant_act_fp8_blocks_kernel(const uint16_t* __restrict__ X, int64_t M,
+                                                                   int64_t K, uint8_t* __restrict__ Xq,
+                                                                   float* __restrict__ sx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nb = K / 128;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= M * nb) return;  // whole warps only
+  const int64_t m = item / nb, b = item % nb;
+  const uint4* src = reinterpret_cast<const uint4*>(X + m * K + b * 128);
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (lane < 16) v = src[lane];
+  const float a = warp_max(amax8(v, 0.0f));
+  const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+  if (lane == 0) sx[b * M + m] = s;
+  if (lane < 16) reinterpret_cast<uint2*>(Xq + m * K + b * 128)[lane] = quant8(v, s);
+}
+
+// 128 x 128 weight blocks: one CTA per block, eight 8-column pieces per thread.
+__global__ void __launch_bounds__(256) quant_w_fp8_blocks_kernel(const uint16_t* __restrict__ W, int64_t K,
+                                                                 uint8_t* __restrict__ Wq, float* __restrict__ sw) {
+  __shared__ float red[32];
+  const int64_t nb = K / 128;
+  const int64_t i = blockIdx.y, b = blockIdx.x;
+  uint4 v[8];
+  float a = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int idx = threadIdx.x + 256 * j;  // row idx / 16, columns 8 (idx % 16) ..
+    v[j] = reinterpret_cast<const uint4*>(W + (i * 128 + idx / 16) * K + b * 128)[idx % 16];
+    a = amax8(v[j], a);
+  }
+  a = block_max<256>(a, red);
+  const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+  if (threadIdx.x == 0) sw[i * nb + b] = s;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int idx = threadIdx.x + 256 * j;
+    reinterpret_cast<uint2*>(Wq + (i * 128 + idx / 16) * K + b * 128)[idx % 16] = quant8(v[j], s);
+  }
+}
+
+cudaError_t launch_quant_act_fp8_blocks(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx,
+                                        cudaStream_t st) {
+  const int64_t warps = M * (K / 128);
+  const int64_t blocks = (warps + 7) / 8;
+  quant_act_fp8_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, M, K, Xq, sx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_w_fp8_blocks(const uint16_t* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,
+                                      cudaStream_t st) {
+  quant_w_fp8_blocks_kernel<<<dim3(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128)), 256, 0, st>>>(
+      W, K, Wq, sw);
+  return cudaGetLastError();
+}
+
 }  // namespace qlin

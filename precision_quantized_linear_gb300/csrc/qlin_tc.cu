@@ -34,7 +34,7 @@ namespace qlin {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kSmemBudget = 225 * 1024;
 
-template <int BN, bool W4, int KPS>
+template <int BN, bool W4, int KPS, bool BS = false>
 struct TcCfg {
   static constexpr int kBlkBytes = 128;                         // bytes of one row of a K block
   static constexpr int kCols = W4 ? 64 : 128;                   // K columns per block
@@ -70,6 +70,7 @@ struct TcCfg {
   static_assert(kXBlk % 1024 == 0 && kStage % 1024 == 0, "1024-byte alignment of swizzled tiles");
   static_assert(W4 || KPS == 1, "E4M3 stages hold one K block");
   static_assert(kTmemNeed <= 512, "TMEM budget");
+  static_assert(!BS || (!W4 && BN <= 128), "block scaling: E4M3 operands, at most 128 tokens (running sums in registers)");
 };
 
 struct TcArgs {
@@ -77,7 +78,7 @@ struct TcArgs {
   const uint16_t* scales;
   const uint8_t* zeros;
   const float* sx;
-  const float* sw;
+  const float* sw;  // W8A8 block scaling: sx = [K/128][M], sw = [N/128][K/128]
   uint16_t* Y;
   float* partials;
   uint32_t* counters;
@@ -142,11 +143,11 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
   return r;
 }
 
-template <int BN, bool W4, int KPS>
-__global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
+template <int BN, bool W4, int KPS, bool BS>
+__global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ TcArgs a) {
-  using C = TcCfg<BN, W4, KPS>;
+  using C = TcCfg<BN, W4, KPS, BS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -263,7 +264,41 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && BS) {
+      // block scaling: every K block of 128 goes to its own partial product, in
+      // one of two TMEM buffers; the epilogue promotes it with the block scales
+      constexpr uint32_t idesc = idesc_make(0, 0, 128, BN);
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        const Unit un = unit_of(a, u, KB);
+        for (int j = 0; j < un.nkb && ok; ++j, ++it) {
+          const int pb = it & 1;
+          if (!mbar_wait(&acc_empty[pb], ((it >> 1) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+            ok = false;
+            break;
+          }
+          const int s = it % C::kStages;
+          if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tmem_d = tmem_base + pb * C::kAccCols;
+          const uint32_t a_addr = smem_u32(ring + s * C::kStage + C::kXBlk);
+          const uint32_t b_addr = smem_u32(ring + s * C::kStage);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8(tmem_d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc, kk != 0);
+          mma_commit(&empty[s]);
+          mma_commit(&acc_full[pb]);
+        }
+      }
+      if (!ok) {
+        set_error(a.err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+      }
+    } else if (lane == 0) {
       constexpr uint32_t idesc = W4 ? idesc_make(1, 1, 128, BN) : idesc_make(0, 0, 128, BN);
       int it = 0, ait = 0, ua = 0;
       bool ok = true;
@@ -403,10 +438,99 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS>::kThreads, 1)
     grid_dep_wait();  // outputs and the workspace may still be in use by the previous kernel
     const int t = threadIdx.x - C::kEpiWarp0 * 32;  // 0..127
     const int quad = warp & 3;                       // TMEM lane quadrant of this warp
-    const float s_w = W4 ? 1.0f : *a.sw;
+    const float s_w = (W4 || BS) ? 1.0f : *a.sw;
     int ua = 0;
     uint32_t epi_n = 0;  // staging boxes used so far
+    int kbi = 0;         // K blocks promoted so far (block scaling)
     for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++ua) {
+      if constexpr (BS) {
+        // ---- block scaling: promote every K block's partial product into FP32
+        // running sums, r[c] += P[c] * sx[kb][m_c] * sw[nt][kb], in K-block order
+        const Unit un = unit_of(a, u, KB);
+        const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
+        const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
+        const bool direct = a.splits == 1;
+        float r[BN];
+#pragma unroll
+        for (int c = 0; c < BN; ++c) r[c] = 0.0f;
+        bool have = true;
+        for (int j = 0; j < un.nkb; ++j, ++kbi) {
+          const int pb = kbi & 1;
+          if (have && !__all_sync(0xffffffffu, mbar_wait(&acc_full[pb], (kbi >> 1) & 1, kWaitLimitNs, &s_abort))) {
+            have = false;
+            set_error(a.err, QLIN_ERR_TIMEOUT);
+            s_abort = 1;
+          }
+          if (!have) continue;
+          tc_fence_after();
+          const int64_t kb = un.kb0 + j;
+          const float swb = __ldg(a.sw + static_cast<int64_t>(un.nt) * KB + kb);
+          const float* sxk = a.sx + kb * a.M;
+          const uint32_t tmem_d = tmem_base + pb * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem_d + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t m = mbase + c0 + i;
+              const float f = m < a.M ? __ldg(sxk + m) * swb : 0.0f;
+              r[c0 + i] = fmaf(__uint_as_float(v[i]), f, r[c0 + i]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[pb]);  // the partial buffer may take the next K block
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          if (direct) {
+            if (mbase + c0 < a.M) {  // the same for all 128 threads: they skip the barriers together
+              uint16_t* box = reinterpret_cast<uint16_t*>(epi_box + (epi_n & 1) * C::kEpiBox);
+              if (t == 0) bulk_wait_read<1>();
+              named_bar_epi();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) box[i * kTileN + quad * 32 + lane] = to_bf16(r[c0 + i]);
+              fence_proxy_async_smem();
+              named_bar_epi();
+              if (t == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(mbase + c0));
+              ++epi_n;
+            }
+          } else if (have) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t m = mbase + c0 + i;
+              if (m < a.M) __stcg(a.partials + (static_cast<int64_t>(un.split) * a.M + m) * a.N + n, r[c0 + i]);
+            }
+          }
+        }
+        if (!direct) {
+          // last-arriver reduction of the K ranges, in split order (deterministic)
+          __threadfence();
+          named_bar_epi();
+          const int64_t tile = static_cast<int64_t>(un.mb) * a.ntiles + un.nt;
+          if (t == 0) s_last = !s_abort && (atomicAdd(a.counters + tile, 1u) == static_cast<uint32_t>(a.splits - 1));
+          named_bar_epi();
+          if (s_last) {
+            __threadfence();
+            for (int c = 0; c < BN; ++c) {
+              const int64_t m = mbase + c;
+              if (m >= a.M) break;
+              float* p = a.partials + m * a.N + n;
+              float acc_v = 0.0f;
+              for (int sp = 0; sp < a.splits; ++sp) {  // read and clear: the workspace is left zero-filled
+                acc_v += __ldcg(p + static_cast<int64_t>(sp) * a.M * a.N);
+                __stcg(p + static_cast<int64_t>(sp) * a.M * a.N, 0.0f);
+              }
+              a.Y[m * a.N + n] = to_bf16(acc_v);
+            }
+            if (t == 0) a.counters[tile] = 0u;
+          }
+          named_bar_epi();
+        }
+        continue;
+      }
       const Unit un = unit_of(a, u, KB);
       const int acc = ua & 1;
       // A warp whose wait gave up skips this unit's data but keeps taking part
@@ -540,9 +664,9 @@ static int pick_bn(int64_t M) {
   return 256;
 }
 
-static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4) {
+static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn = 256) {
   TcPlan p;
-  p.bn = pick_bn(M);
+  p.bn = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
   p.mblocks = (M + p.bn - 1) / p.bn;
   const int64_t tiles = (N / kTileN) * p.mblocks;
   const int64_t KB = K / cols;
@@ -597,12 +721,16 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bo
 
 TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 64, true); }
 TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false); }
+// block scaling keeps the running sums of a 128-token tile in registers
+TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
+  return plan_tc(M, N, K, num_sms, 128, false, 128);
+}
 
-template <int BN, bool W4, int KPS>
+template <int BN, bool W4, int KPS, bool BS = false>
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
                              const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
-  using C = TcCfg<BN, W4, KPS>;
-  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS>, C::kSmemBytes);
+  using C = TcCfg<BN, W4, KPS, BS>;
+  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   args.counters = static_cast<uint32_t*>(ws);
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.split.tiles)) : nullptr;
@@ -629,7 +757,7 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS>, tx, tw, ty, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS>, tx, tw, ty, args);
 }
 
 template <bool W4>
@@ -691,6 +819,30 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
   a.N = N;
   a.K = K;
   return launch_tc_bn<false>(tx, tw, ty, a, plan, ws, num_sms, st);
+}
+
+cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
+                                 int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
+                                 cudaStream_t st) {
+  CUtensorMap tx, tw, ty;
+  if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, K, N, K, 128, 128)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, N * 2, kTileN, 16, false))
+    return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.sx = sx;
+  a.sw = sw;
+  a.Y = Y;
+  a.err = err;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  switch (plan.bn) {
+    case 16: return launch_tc<16, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 32: return launch_tc<32, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 64: return launch_tc<64, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default: return launch_tc<128, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+  }
 }
 
 }  // namespace qlin

@@ -10,8 +10,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_pack_w4, qlin_quant_act_fp8,
-               qlin_quant_w_fp8, qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w8a8_fp8_gemm_ex,
+from . import (OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_pack_w4,
+               qlin_quant_act_fp8, qlin_quant_act_fp8_blocks, qlin_quant_w_fp8, qlin_quant_w_fp8_blocks,
+               qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w8a8_fp8_block_gemm, qlin_w8a8_fp8_gemm_ex,
                qlin_workspace_size)
 
 
@@ -96,3 +97,37 @@ class W8A8Linear:
     def __call__(self, X_bf16, Y=None, path: int = PATH_AUTO, stream=None):
         Xq, sx = self.quant_act(X_bf16, stream=stream)
         return self.gemm(Xq, sx, Y, path, stream)
+
+
+class W8A8BlockLinear:
+    """FP8 W8A8 with block scaling: 128 x 128 weight blocks, 1 x 128 activation blocks."""
+
+    def __init__(self, W_bf16: torch.Tensor, stream=None):
+        N, K = W_bf16.shape
+        self.N, self.K = N, K
+        dev = W_bf16.device
+        self.Wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        self.sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+        qlin_quant_w_fp8_blocks(_as_u16(W_bf16.contiguous()), N, K, self.Wq, self.sw, stream)
+        self.ws = Workspace(dev)
+
+    def quant_act(self, X_bf16: torch.Tensor, Xq=None, sx=None, stream=None):
+        M, K = X_bf16.shape
+        if Xq is None:
+            Xq = torch.empty((M, K), dtype=torch.uint8, device=X_bf16.device)
+        if sx is None:
+            sx = torch.empty((K // 128, max(M, 1)), dtype=torch.float32, device=X_bf16.device)
+        qlin_quant_act_fp8_blocks(_as_u16(X_bf16), M, K, Xq, sx, stream)
+        return Xq, sx
+
+    def gemm(self, Xq, sx, Y=None, stream=None):
+        M = Xq.shape[0]
+        if Y is None:
+            Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
+        buf, nb = self.ws.get(qlin_workspace_size(OP_W8A8_BLOCK_GEMM, M, self.N, self.K))
+        qlin_w8a8_fp8_block_gemm(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        return Y
+
+    def __call__(self, X_bf16, Y=None, stream=None):
+        Xq, sx = self.quant_act(X_bf16, stream=stream)
+        return self.gemm(Xq, sx, Y, stream)

@@ -259,3 +259,74 @@ def test_workspace_too_small_and_empty():
     torch.cuda.synchronize()
     assert torch.equal(Y4, lin(X4, path=q.PATH_GEMV))
     assert q.qlin_get_device_error() == 0
+
+
+# ------------------------------------------------------------------ FP8 block scaling
+
+from precision_quantized_linear_gb300.layers import W8A8BlockLinear  # noqa: E402
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (7, 512), (300, 4096)])
+def test_quant_act_fp8_blocks_bit_exact(M, K):
+    X = syn.make_act(M, K, seed=M + K, token_outlier_frac=0.01)
+    X[0, :128] = 0                                # an all-zero block
+    q_ref, s_ref = oracle.quant_fp8_act_blocks(X)
+    Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+    q.qlin_quant_act_fp8_blocks(to_dev(X), M, K, Xq, sx)
+    torch.cuda.synchronize()
+    assert np.array_equal(Xq.cpu().numpy(), q_ref)
+    assert np.array_equal(sx.cpu().numpy(), s_ref)
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (384, 1024), (4096, 4096)])
+def test_quant_w_fp8_blocks_bit_exact(N, K):
+    W = syn.make_weight(N, K, seed=N + K)
+    W[:128, :128] = 0
+    q_ref, s_ref = oracle.quant_fp8_weight_blocks(W)
+    lin = W8A8BlockLinear(to_dev(W))
+    torch.cuda.synchronize()
+    assert np.array_equal(lin.Wq.cpu().numpy(), q_ref)
+    assert np.array_equal(lin.sw.cpu().numpy(), s_ref)
+
+
+def _w8b_case(M, N, K, seed, nsamp=None):
+    W = syn.make_weight(N, K, seed=seed)
+    X = syn.make_act(M, K, seed=seed + 1, token_outlier_frac=0.001)
+    Xq_r, sx_r = oracle.quant_fp8_act_blocks(X)
+    Wq_r, sw_r = oracle.quant_fp8_weight_blocks(W)
+    lin = W8A8BlockLinear(to_dev(W))
+    Xq, sx = lin.quant_act(to_dev(X))
+    Y = bf16_out(lin.gemm(Xq, sx))
+    assert np.array_equal(Xq.cpu().numpy(), Xq_r) and np.array_equal(sx.cpu().numpy()[:, :M], sx_r)
+    tab = oracle.e4m3_table()
+    xd = tab[Xq_r] * np.repeat(sx_r.T.astype(np.float64), 128, axis=1)
+    wd = tab[Wq_r] * np.repeat(np.repeat(sw_r.astype(np.float64), 128, axis=0), 128, axis=1)
+    xn, wn = np.linalg.norm(xd, axis=1), np.linalg.norm(wd, axis=1)
+    if nsamp is None:
+        ref = oracle.w8a8_blocks_full(Xq_r, sx_r, Wq_r, sw_r)
+        return norm_err(Y, ref, xn, wn)
+    rng = np.random.default_rng(seed)
+    ms, ns = rng.integers(0, M, nsamp), rng.integers(0, N, nsamp)
+    ref = oracle.w8a8_blocks_at(Xq_r, sx_r, Wq_r, sw_r, ms, ns)
+    err = np.abs(Y[ms, ns] - ref) / (xn[ms] * wn[ns])
+    return float(err.max())
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 64, 100, 129, 300])
+def test_w8a8_block_gemm_m_sweep(M):
+    assert _w8b_case(M, 512, 1024, seed=M + 31) <= TOL
+
+
+@pytest.mark.parametrize("M,N,K", [(4, 4096, 4096), (16, 4096, 14336), (2048, 4096, 4096)])
+def test_w8a8_block_gemm_llama_sampled(M, N, K):
+    assert _w8b_case(M, N, K, seed=M + N, nsamp=1500) <= TOL
+
+
+def test_w8a8_block_gemm_deterministic():
+    W = syn.make_weight(512, 4096, seed=5)
+    X = syn.make_act(3, 4096, seed=6)
+    lin = W8A8BlockLinear(to_dev(W))
+    a = lin(to_dev(X)).clone()
+    b = lin(to_dev(X)).clone()
+    assert torch.equal(a, b)
