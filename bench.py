@@ -519,7 +519,7 @@ def run_sweep(args):
 
     import precision_quantized_linear_gb300 as q
     from precision_quantized_linear_gb300 import synthetic as syn
-    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8Linear
+    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8BlockLinear, W8A8Linear
 
     torch.cuda.set_device(0)
     q.build()
@@ -543,6 +543,9 @@ def run_sweep(args):
     elif args.sweep == "70b":
         shapes = [(8192, 10240), (8192, 8192), (8192, 57344), (28672, 8192)]
         plan = [("w4", M) for M in (1, 64, 256)] + [("w8", M) for M in (256, 4096)]
+    elif args.sweep == "blocks":  # FP8 block scaling beside per-tensor FP8, decode to prefill
+        shapes = [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]
+        plan = [(v, M) for M in (1, 16, 2048, 8192) for v in ("w8", "w8b")]
     else:  # decode: GEMV vs tensor-core path per M, for the dispatch threshold
         shapes = [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]
         plan = [(v, M) for M in (1, 2, 3, 4, 5, 8, 16) for v in ("w4gemv", "w4tc", "w8gemv", "w8tc")]
@@ -551,6 +554,7 @@ def run_sweep(args):
         W = torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda()
         lin4 = W4A16Linear(W)
         lin8 = W8A8Linear(W)
+        lin8b = W8A8BlockLinear(W) if args.sweep == "blocks" else None
         del W
         w4b, w8b = w4_weight_bytes(N, K), N * K
         r4 = max(1, int(np.ceil(3 * l2 / w4b)))
@@ -558,6 +562,8 @@ def run_sweep(args):
         sets4 = [(lin4.codes, lin4.scales, lin4.zeros)] + [
             (lin4.codes.clone(), lin4.scales.clone(), lin4.zeros.clone()) for _ in range(r4 - 1)]
         sets8 = [lin8.Wq] + [lin8.Wq.clone() for _ in range(r8 - 1)]
+        sets8b = ([(lin8b.Wq, lin8b.sw)] + [(lin8b.Wq.clone(), lin8b.sw.clone()) for _ in range(r8 - 1)]
+                  if lin8b is not None else [])
         for (v, M) in plan:
             X = torch.from_numpy(syn.make_act(M, K, seed=M + 7, token_outlier_frac=0.001).view(np.int16)).cuda()
             Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
@@ -578,6 +584,22 @@ def run_sweep(args):
                            TFLOPS=round(flops / (us * 1e-6) / 1e12, 2), roof_us=round(t_roof, 2),
                            roof_frac=round(t_roof / us, 3),
                            bound="hbm" if alg / (bw * 1e9) > flops / (p16 * 1e12) else "tensor")
+            elif v == "w8b":
+                nb = q.qlin_workspace_size(q.OP_W8A8_BLOCK_GEMM, M, N, K)
+                ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+                sxb = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+                q.qlin_quant_act_fp8_blocks(X, M, K, Xq, sxb)
+                fns = [lambda st, wq=wq, sw=sw: q.qlin_w8a8_fp8_block_gemm(Xq, sxb, wq, sw, Y, M, N, K, ws, ws.numel(),
+                                                                          st) for (wq, sw) in sets8b]
+                us = time_launches(fns)
+                qus = time_launches([lambda st: q.qlin_quant_act_fp8_blocks(X, M, K, Xq, sxb, st)])
+                alg = w8_alg_bytes(M, N, K) + 4 * M * (K // 128) + 4 * (N // 128) * (K // 128)
+                t_roof = max(flops / (p8_use * 1e12), alg / (bw * 1e9)) * 1e6
+                row.update(us=round(us, 2), quant_us=round(qus, 2), weight_GBps=round(w8b / (us * 1e-6) / 1e9, 1),
+                           TFLOPS=round(flops / (us * 1e-6) / 1e12, 2), roof_us=round(t_roof, 2),
+                           roof_frac=round(t_roof / us, 3),
+                           bound="hbm" if alg / (bw * 1e9) > flops / (p8_use * 1e12) else "tensor",
+                           fp8_peak="probe" if p8 else "2x bf16 (assumed)")
             else:
                 path = {"w8": q.PATH_AUTO, "w8gemv": q.PATH_GEMV, "w8tc": q.PATH_TC}[v]
                 nb = q.qlin_workspace_size(q.OP_W8A8_GEMM, M, N, K)
@@ -597,7 +619,7 @@ def run_sweep(args):
             assert q.qlin_get_device_error() == 0
             print(json.dumps(row), flush=True)
             results.append(row)
-        del lin4, lin8, sets4, sets8
+        del lin4, lin8, lin8b, sets4, sets8, sets8b
         torch.cuda.empty_cache()
     if args.sweep == "crossover":
         print(json.dumps(crossover_summary(results, p16, p8_use, bw)), flush=True)
@@ -609,7 +631,7 @@ def run_case(args):
 
     import precision_quantized_linear_gb300 as q
     from precision_quantized_linear_gb300 import synthetic as syn
-    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8Linear
+    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8BlockLinear, W8A8Linear
 
     torch.cuda.set_device(0)
     q.build()
@@ -621,6 +643,10 @@ def run_case(args):
     if args.case == "w4a16":
         lin = W4A16Linear(W)
         fn = lambda: lin(X, path=path)  # noqa: E731
+    elif args.case == "w8a8b":
+        lin = W8A8BlockLinear(W)
+        Xq, sx = lin.quant_act(X)
+        fn = lambda: lin.gemm(Xq, sx)  # noqa: E731
     else:
         lin = W8A8Linear(W)
         Xq, sx = lin.quant_act(X)
@@ -645,10 +671,10 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sweep", default=None, choices=["crossover", "prefill", "70b", "decode"])
+    ap.add_argument("--sweep", default=None, choices=["crossover", "prefill", "70b", "decode", "blocks"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default=None, choices=["w4a16", "w8a8"])
+    ap.add_argument("--case", default=None, choices=["w4a16", "w8a8", "w8a8b"])
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--N", type=int, default=28672)
     ap.add_argument("--K", type=int, default=4096)

@@ -83,6 +83,15 @@ const char* qlin_status_string(int status);
 /* QLIN_PACK_FORMAT_VERSION of the library that is loaded. */
 int qlin_pack_format_version(void);
 
+/* The cudaError_t (as int) behind the most recent QLIN_ERR_CUDA returned by a
+ * call on the calling thread; 0 if there was none.  A call that returns
+ * QLIN_ERR_CUDA has also cleared the runtime's last-error state, so a failed
+ * launch is not reported again by a later, unrelated call. */
+int qlin_last_cuda_error(void);
+
+/* The CUDA runtime's name for an error code (static string, never NULL). */
+const char* qlin_cuda_error_name(int code);
+
 /* Byte sizes of the three packed-weight buffers for an [N][K] weight.
  * codes = N*K/2, scales = 2*N*K/G, zeros = N*K/(2G) ([LP] S5: codes + scales
  * give exactly 4 + 16/G bits per weight; the zeros add 4/G). */

@@ -19,7 +19,8 @@ from . import build as _build_mod
 
 __all__ = [
     "QlinError", "load", "build",
-    "qlin_status_string", "qlin_pack_format_version", "qlin_w4_packed_sizes", "qlin_workspace_size",
+    "qlin_status_string", "qlin_pack_format_version", "qlin_last_cuda_error", "qlin_cuda_error_name",
+    "qlin_w4_packed_sizes", "qlin_workspace_size",
     "qlin_pack_w4", "qlin_w4a16_gemm", "qlin_w4a16_gemm_ex", "qlin_quant_act_fp8", "qlin_quant_w_fp8",
     "qlin_w8a8_fp8_gemm", "qlin_w8a8_fp8_gemm_ex", "qlin_get_device_error", "qlin_gemv_max_m",
     "qlin_selftest_wait_timeout", "qlin_w4a16_gemv_noalloc", "qlin_quant_act_fp8_blocks", "qlin_quant_w_fp8_blocks",
@@ -43,6 +44,8 @@ _int = ctypes.c_int
 _SIGS = {
     "qlin_status_string": [_int],
     "qlin_pack_format_version": [],
+    "qlin_last_cuda_error": [],
+    "qlin_cuda_error_name": [_int],
     "qlin_gemv_max_m": [_int],
     "qlin_w4_packed_sizes": [_i64, _i64, _int, ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
     "qlin_workspace_size": [_int, _i64, _i64, _i64, ctypes.POINTER(_sz)],
@@ -65,7 +68,12 @@ _SIGS = {
 class QlinError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
-        super().__init__("%s failed: %s (%d)" % (where, qlin_status_string(status), status))
+        self.cuda_error = 0
+        msg = "%s failed: %s (%d)" % (where, qlin_status_string(status), status)
+        if self.status == 6:  # QLIN_ERR_CUDA: name the CUDA error behind it
+            self.cuda_error = qlin_last_cuda_error()
+            msg += " [%s]" % qlin_cuda_error_name(self.cuda_error)
+        super().__init__(msg)
 
 
 def build(force: bool = False) -> str:
@@ -89,7 +97,7 @@ def load():
         for name, args in _SIGS.items():
             fn = getattr(lib, name)
             fn.argtypes = args
-            fn.restype = ctypes.c_char_p if name == "qlin_status_string" else _int
+            fn.restype = ctypes.c_char_p if name in ("qlin_status_string", "qlin_cuda_error_name") else _int
         _lib = lib
         return lib
 
@@ -119,6 +127,14 @@ def _check(st: int, where: str) -> int:
 
 def qlin_status_string(status: int) -> str:
     return load().qlin_status_string(int(status)).decode()
+
+
+def qlin_last_cuda_error() -> int:
+    return load().qlin_last_cuda_error()
+
+
+def qlin_cuda_error_name(code: int) -> str:
+    return load().qlin_cuda_error_name(int(code)).decode()
 
 
 def qlin_pack_format_version() -> int:

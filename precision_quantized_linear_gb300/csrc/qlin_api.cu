@@ -130,7 +130,19 @@ static int check_shape(int64_t M, int64_t N, int64_t K) {
   return QLIN_OK;
 }
 
-static int launch_status(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA; }
+// The CUDA error behind the last QLIN_ERR_CUDA returned on this thread.
+static thread_local int g_last_cuda_error = 0;
+
+namespace qlin {
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return QLIN_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  (void)cudaGetLastError();  // a launch error must not be reported again by the next call
+  return QLIN_ERR_CUDA;
+}
+}  // namespace qlin
+
+static int launch_status(cudaError_t e) { return cuda_status(e); }
 
 extern "C" {
 
@@ -149,6 +161,10 @@ const char* qlin_status_string(int status) {
 }
 
 int qlin_pack_format_version(void) { return QLIN_PACK_FORMAT_VERSION; }
+
+int qlin_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* qlin_cuda_error_name(int code) { return cudaGetErrorName(static_cast<cudaError_t>(code)); }
 
 int qlin_gemv_max_m(int op) { return op == QLIN_OP_W8A8_GEMM ? g_gemv_max_m_w8 : g_gemv_max_m_w4; }
 
@@ -377,11 +393,14 @@ int qlin_get_device_error(void* stream) {
   int st = device_state(&d);
   if (st != QLIN_OK) return st;
   auto cs = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(cs) != cudaSuccess) return QLIN_ERR_CUDA;
+  st = cuda_status(cudaStreamSynchronize(cs));
+  if (st != QLIN_OK) return st;
   int word = 0;
-  if (cudaMemcpy(&word, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QLIN_ERR_CUDA;
+  st = cuda_status(cudaMemcpy(&word, d->err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (st != QLIN_OK) return st;
   const int zero = 0;
-  if (cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QLIN_ERR_CUDA;
+  st = cuda_status(cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  if (st != QLIN_OK) return st;
   return word;
 }
 

@@ -34,6 +34,9 @@ struct SplitPlan {
 // while a stream is being captured into a CUDA graph.  Keyed by the kernel's
 // address: template instantiations share a type but not an address.
 cudaError_t set_smem_once_impl(const void* kernel, int bytes, bool wide_clusters);
+// QLIN_OK for cudaSuccess; otherwise records e for qlin_last_cuda_error(),
+// clears the runtime's last-error state and returns QLIN_ERR_CUDA.
+int cuda_status(cudaError_t e);
 // wide_clusters: also allow thread-block clusters of up to 16 CTAs.
 template <typename F>
 inline cudaError_t set_smem_once(F* kernel, int bytes, bool wide_clusters = false) {
@@ -70,6 +73,7 @@ cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* 
 // tcgen05 kernels: swap-AB (weights are the 128-row MMA operand, tokens the N side)
 struct TcPlan {
   int bn = 16;           // tokens per tile (MMA N)
+  int wn = 128;          // weight rows per tile (256: block-scaled token-major tiles)
   int kps = 1;           // K blocks per pipeline stage
   int64_t mblocks = 1;   // token blocks
   SplitPlan split;

@@ -66,7 +66,10 @@ extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, co
   auto cs = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the counters must start at
   // zero, the partial sums are overwritten before they are read.
-  if (plan.zero_bytes > 0 && cudaMemsetAsync(scratch, 0, plan.zero_bytes, cs) != cudaSuccess) return QLIN_ERR_CUDA;
+  if (plan.zero_bytes > 0) {
+    st = cuda_status(cudaMemsetAsync(scratch, 0, plan.zero_bytes, cs));
+    if (st != QLIN_OK) return st;
+  }
   void* ws = plan.ws_bytes > 0 ? scratch : nullptr;
   const auto* Xp = static_cast<const uint16_t*>(X_bf16);
   const auto* cp = static_cast<const uint8_t*>(codes);
@@ -75,5 +78,5 @@ extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, co
   auto* Yp = static_cast<uint16_t*>(Y_bf16);
   const cudaError_t e = mma ? launch_w4a16_mma(Xp, cp, sp, zp, Yp, M, N, K, plan, ws, device_error_word(), cs)
                             : launch_w4a16_gemv(Xp, cp, sp, zp, Yp, M, N, K, plan, ws, cs);
-  return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA;
+  return cuda_status(e);
 }

@@ -343,6 +343,14 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Ties 16 registers filled by tmem_ld16 to a point after tmem_ld_wait: the
+// empty volatile statements stay in order behind the wait and appear to
+// rewrite the values, so no arithmetic on them can be scheduled earlier.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
 // swizzle layout: rows of 128 bytes, 8-row atoms 1024 bytes apart (atoms
 // start 1024-byte aligned).  Leading-byte offset is unused for this layout.

@@ -34,12 +34,12 @@ namespace qlin {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kSmemBudget = 225 * 1024;
 
-template <int BN, bool W4, int KPS, bool BS = false>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128>
 struct TcCfg {
   static constexpr int kBlkBytes = 128;                         // bytes of one row of a K block
   static constexpr int kCols = W4 ? 64 : 128;                   // K columns per block
   static constexpr int kXBlk = BN * kBlkBytes;                  // token tile of one K block
-  static constexpr int kWBlk = W4 ? 4096 : 128 * kBlkBytes;     // packed codes / E4M3 tile of one K block
+  static constexpr int kWBlk = W4 ? 4096 : WN * kBlkBytes;      // packed codes / E4M3 tile of one K block
   static constexpr int kGroupsPerStage = W4 ? (KPS >= 2 ? KPS / 2 : 1) : 0;
   static constexpr int kScaleOff = KPS * kXBlk + KPS * kWBlk;   // scales, then zero-points (W4A16)
   static constexpr int kZeroOff = kScaleOff + kGroupsPerStage * 256;
@@ -53,24 +53,45 @@ struct TcCfg {
   static constexpr int kAStage = (W4 && !kATmem) ? 128 * kBlkBytes : 0;  // shared-memory bytes per slot
   static constexpr int kASlotCols = 32;                         // TMEM columns per slot (64 BF16 per lane)
   // output staging: two boxes of 16 tokens x 128 rows of BF16 for the tensor stores
+  // Block scaling with 128-token tiles runs token-major: the token tile is the
+  // MMA's A operand (TMEM lane = token) and the weight tile of WN rows (one or
+  // two 128-row scale blocks) its B operand, so the promotion factor
+  // sx[kb][m] * sw[n / 128][kb] is one scalar per thread and 128 columns.
+  static constexpr bool kTokM = BS && BN == 128;
+  // epilogue warps: four (one per TMEM lane quadrant); with block scaling and
+  // at least 32 tokens, eight, two per quadrant, each taking half the columns
+  static constexpr int kEpiWarps = (BS && BN >= 32) ? 8 : 4;
+  static constexpr int kEpiHalves = kEpiWarps / 4;
   static constexpr int kEpiBox = 16 * kTileN * 2;
-  static constexpr int kStagesRaw = (kSmemBudget - 2048 - kAStages * kAStage - 2 * kEpiBox) / kStage;
+  static constexpr int kEpiBoxes = kTokM ? 0 : 2 * kEpiHalves;  // token-major writes rows straight to Y
+  static constexpr int kScaleVec = (BS && !kTokM) ? 2 * 128 * 4 : 0;  // sx * sw of one K block, two buffers
+  static constexpr int kStagesRaw =
+      (kSmemBudget - 2048 - kAStages * kAStage - kEpiBoxes * kEpiBox - kScaleVec) / kStage;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
-  static constexpr int kAccCols = BN;                           // one accumulator
+  static constexpr int kAccCols = kTokM ? WN : BN;              // one accumulator
+  // accumulators in TMEM: two (one unit while the epilogue drains the other);
+  // block scaling keeps up to four K-block partial products in flight
+  static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : 2;
   static constexpr int kAColBase = 2 * BN;                      // first TMEM column of the A slots
-  static constexpr int kTmemNeed = 2 * BN + (kATmem ? kAStages * kASlotCols : 0);
+  static constexpr int kTmemNeed = kAccBufs * BN + (kATmem ? kAStages * kASlotCols : 0);
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                  : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kDqWarps = W4 ? 8 : 0;
   static constexpr int kEpiWarp0 = 2 + kDqWarps;
-  static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
-  static constexpr int kSmemBytes =
-      1024 /*align slack*/ + kStages * kStage + kAStages * kAStage + 2 * kEpiBox + 1024 /*barriers*/;
+  static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+  // Register cap per thread.  Each of the SM's four sub-partitions holds 16 K
+  // registers and takes every fourth warp, so the cap is set by the
+  // sub-partition with the most warps: 14 warps (W4A16) -> 4 -> 128;
+  // 10 warps -> 3 -> 168; 6 warps -> 2 -> 255 (232 kept).
+  static constexpr int kMaxRegs = W4 ? 128 : kThreads > 256 ? 168 : 232;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStage + kAStages * kAStage +
+                                    kEpiBoxes * kEpiBox + kScaleVec + 1024 /*barriers*/;
   static_assert(kStages >= 2, "pipeline too shallow");
   static_assert(kXBlk % 1024 == 0 && kStage % 1024 == 0, "1024-byte alignment of swizzled tiles");
   static_assert(W4 || KPS == 1, "E4M3 stages hold one K block");
   static_assert(kTmemNeed <= 512, "TMEM budget");
   static_assert(!BS || (!W4 && BN <= 128), "block scaling: E4M3 operands, at most 128 tokens (running sums in registers)");
+  static_assert(WN == 128 || (kTokM && WN == 256), "256-row weight tiles only token-major");
 };
 
 struct TcArgs {
@@ -96,6 +117,9 @@ struct TcArgs {
 __device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
 __device__ __forceinline__ void named_bar_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
@@ -143,24 +167,25 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
   return r;
 }
 
-template <int BN, bool W4, int KPS, bool BS>
-__global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
+template <int BN, bool W4, int KPS, bool BS, int WN>
+__global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ TcArgs a) {
-  using C = TcCfg<BN, W4, KPS, BS>;
+  using C = TcCfg<BN, W4, KPS, BS, WN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint8_t* aring = ring + C::kStages * C::kStage;
-  uint8_t* epi_box = aring + C::kAStages * C::kAStage;  // [2][16 tokens][128 rows] BF16
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_box + 2 * C::kEpiBox);
+  uint8_t* epi_box = aring + C::kAStages * C::kAStage;  // [kEpiBoxes][16 tokens][128 rows] BF16
+  float* scale_vec = reinterpret_cast<float*>(epi_box + C::kEpiBoxes * C::kEpiBox);  // [2][128] (block scaling)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_box + C::kEpiBoxes * C::kEpiBox + C::kScaleVec);
   uint64_t* full = bars;                       // [kStages]  producer -> consumers (tx bytes)
   uint64_t* empty = full + C::kStages;         // [kStages]  consumers -> producer
   uint64_t* a_full = empty + C::kStages;       // [kAStages] dequant -> MMA
   uint64_t* a_empty = a_full + C::kAStages;    // [kAStages] MMA -> dequant
-  uint64_t* acc_full = a_empty + C::kAStages;  // [2] MMA -> epilogue
-  uint64_t* acc_empty = acc_full + 2;          // [2] epilogue -> MMA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_full = a_empty + C::kAStages;  // [kAccBufs] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + C::kAccBufs;  // [kAccBufs] epilogue -> MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + C::kAccBufs);
   __shared__ int s_last;
   __shared__ volatile int s_abort;  // set by the first role whose wait gave up
 
@@ -176,9 +201,9 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
       mbar_init(&a_full[i], C::kDqWarps);
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], C::kEpiWarps);
     }
     fence_mbar_init();
     s_abort = 0;
@@ -219,7 +244,10 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
           bulk_load(st + C::kZeroOff, a.zeros + (static_cast<int64_t>(un.nt) * ng + g0) * (kTileN / 2),
                     C::kGroupsPerStage * 64, &full[s]);
         } else {
-          tma_load_2d_hint(st + C::kXBlk, &tmap_w, &full[s], kb * C::kCols, un.nt * kTileN, pol_stream);
+#pragma unroll
+          for (int h = 0; h < WN / kTileN; ++h)  // one box of 128 rows per scale block
+            tma_load_2d_hint(st + C::kXBlk + h * kTileN * C::kBlkBytes, &tmap_w, &full[s], kb * C::kCols,
+                             un.nt * WN + h * kTileN, pol_stream);
         }
       };
       auto load_x = [&](int s, const Unit& un, int j) {
@@ -266,15 +294,15 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && BS) {
       // block scaling: every K block of 128 goes to its own partial product, in
-      // one of two TMEM buffers; the epilogue promotes it with the block scales
-      constexpr uint32_t idesc = idesc_make(0, 0, 128, BN);
+      // one of kAccBufs TMEM buffers; the epilogue promotes it with the block scales
+      constexpr uint32_t idesc = idesc_make(0, 0, 128, C::kTokM ? WN : BN);
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         const Unit un = unit_of(a, u, KB);
         for (int j = 0; j < un.nkb && ok; ++j, ++it) {
-          const int pb = it & 1;
-          if (!mbar_wait(&acc_empty[pb], ((it >> 1) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+          const int pb = it % C::kAccBufs;
+          if (!mbar_wait(&acc_empty[pb], ((it / C::kAccBufs) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
             ok = false;
             break;
           }
@@ -285,8 +313,9 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t tmem_d = tmem_base + pb * C::kAccCols;
-          const uint32_t a_addr = smem_u32(ring + s * C::kStage + C::kXBlk);
-          const uint32_t b_addr = smem_u32(ring + s * C::kStage);
+          // weight-major: A = weight tile, B = token tile; token-major: swapped
+          const uint32_t a_addr = smem_u32(ring + s * C::kStage + (C::kTokM ? 0 : C::kXBlk));
+          const uint32_t b_addr = smem_u32(ring + s * C::kStage + (C::kTokM ? C::kXBlk : 0));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8(tmem_d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc, kk != 0);
@@ -436,71 +465,210 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     grid_dep_wait();  // outputs and the workspace may still be in use by the previous kernel
-    const int t = threadIdx.x - C::kEpiWarp0 * 32;  // 0..127
+    const int t = threadIdx.x - C::kEpiWarp0 * 32;  // 0 .. kEpiWarps * 32 - 1
     const int quad = warp & 3;                       // TMEM lane quadrant of this warp
     const float s_w = (W4 || BS) ? 1.0f : *a.sw;
     int ua = 0;
     uint32_t epi_n = 0;  // staging boxes used so far
     int kbi = 0;         // K blocks promoted so far (block scaling)
     for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++ua) {
-      if constexpr (BS) {
-        // ---- block scaling: promote every K block's partial product into FP32
-        // running sums, r[c] += P[c] * sx[kb][m_c] * sw[nt][kb], in K-block order
+      if constexpr (C::kTokM) {
+        // ---- block scaling, token-major: thread = token m (TMEM lane quad * 32 +
+        // lane), columns [cbase, cbase + 64) of the weight tile; every K block's
+        // partial product is promoted as r[c] += P[c] * (sx[kb][m] * sw[nt][kb])
+        constexpr int kCw = WN / C::kEpiHalves;
+        constexpr int kChunk = kCw > 64 ? 16 : kCw;  // TMEM columns loaded per wait
+        constexpr int kAll = C::kEpiWarps * 32;
+        const int te = threadIdx.x - C::kEpiWarp0 * 32;
+        const int cbase = (te >> 7) * kCw;
         const Unit un = unit_of(a, u, KB);
-        const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
-        const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
+        const int64_t m = static_cast<int64_t>(un.mb) * BN + quad * 32 + lane;
+        const int64_t n0 = static_cast<int64_t>(un.nt) * WN + cbase;
+        const bool mok = m < a.M;
         const bool direct = a.splits == 1;
-        float r[BN];
+        // the next K block's scales are loaded while the current one is promoted
+        const float* swp = a.sw + (n0 / kTileN) * KB;  // this thread's columns lie in one scale block
+        float sxn = 0.0f, swn = 0.0f;
+        if (un.nkb > 0) {
+          swn = __ldg(swp + un.kb0);
+          if (mok) sxn = __ldg(a.sx + un.kb0 * a.M + m);
+        }
+        float r[kCw];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) r[c] = 0.0f;
+        for (int c = 0; c < kCw; ++c) r[c] = 0.0f;
         bool have = true;
         for (int j = 0; j < un.nkb; ++j, ++kbi) {
-          const int pb = kbi & 1;
-          if (have && !__all_sync(0xffffffffu, mbar_wait(&acc_full[pb], (kbi >> 1) & 1, kWaitLimitNs, &s_abort))) {
+          const int pb = kbi % C::kAccBufs;
+          const float f = sxn * swn;
+          if (j + 1 < un.nkb) {
+            const int64_t kb1 = un.kb0 + j + 1;
+            swn = __ldg(swp + kb1);
+            if (mok) sxn = __ldg(a.sx + kb1 * a.M + m);
+          }
+          if (have && !__all_sync(0xffffffffu, mbar_wait(&acc_full[pb], (kbi / C::kAccBufs) & 1, kWaitLimitNs,
+                                                           &s_abort))) {
             have = false;
             set_error(a.err, QLIN_ERR_TIMEOUT);
             s_abort = 1;
           }
           if (!have) continue;
           tc_fence_after();
-          const int64_t kb = un.kb0 + j;
-          const float swb = __ldg(a.sw + static_cast<int64_t>(un.nt) * KB + kb);
-          const float* sxk = a.sx + kb * a.M;
-          const uint32_t tmem_d = tmem_base + pb * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+          const uint32_t tmem_d =
+              tmem_base + pb * C::kAccCols + cbase + (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll
-          for (int c0 = 0; c0 < BN; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem_d + c0, v);
+          for (int c0 = 0; c0 < kCw; c0 += kChunk) {
+            uint32_t v[kChunk / 16][16];
+#pragma unroll
+            for (int q = 0; q < kChunk / 16; ++q) tmem_ld16(tmem_d + c0 + q * 16, v[q]);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int64_t m = mbase + c0 + i;
-              const float f = m < a.M ? __ldg(sxk + m) * swb : 0.0f;
-              r[c0 + i] = fmaf(__uint_as_float(v[i]), f, r[c0 + i]);
+            for (int q = 0; q < kChunk / 16; ++q) reg_fence16(v[q]);  // no use of v is hoisted above the wait
+            if (c0 + kChunk == kCw) {  // all in registers: the buffer may take the next K block
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[pb]);
+            }
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) r[c0 + c] = fmaf(__uint_as_float(v[c >> 4][c & 15]), f, r[c0 + c]);
+          }
+        }
+        if (direct) {
+          if (have && mok) {
+            uint4* yrow = reinterpret_cast<uint4*>(a.Y + m * a.N + n0);
+#pragma unroll
+            for (int c = 0; c < kCw; c += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                w[i] = static_cast<uint32_t>(to_bf16(r[c + 2 * i])) | (static_cast<uint32_t>(to_bf16(r[c + 2 * i + 1])) << 16);
+              yrow[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
+        } else {
+          if (have && mok) {
+            float4* prow = reinterpret_cast<float4*>(a.partials + (static_cast<int64_t>(un.split) * a.M + m) * a.N + n0);
+#pragma unroll
+            for (int c = 0; c < kCw; c += 4) __stcg(prow + c / 4, make_float4(r[c], r[c + 1], r[c + 2], r[c + 3]));
+          }
+          // last-arriver reduction of the K ranges, in split order (deterministic)
+          __threadfence();
+          named_bar(1, kAll);
+          const int64_t tile = static_cast<int64_t>(un.mb) * a.ntiles + un.nt;
+          if (te == 0) s_last = !s_abort && (atomicAdd(a.counters + tile, 1u) == static_cast<uint32_t>(a.splits - 1));
+          named_bar(1, kAll);
+          if (s_last) {
+            __threadfence();
+            if (mok) {
+              for (int c = 0; c < kCw; c += 4) {
+                float4 acc_v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int sp = 0; sp < a.splits; ++sp) {  // read and clear: the workspace is left zero-filled
+                  float4* pp = reinterpret_cast<float4*>(a.partials + (static_cast<int64_t>(sp) * a.M + m) * a.N + n0 + c);
+                  const float4 x = __ldcg(pp);
+                  acc_v.x += x.x;
+                  acc_v.y += x.y;
+                  acc_v.z += x.z;
+                  acc_v.w += x.w;
+                  __stcg(pp, make_float4(0.0f, 0.0f, 0.0f, 0.0f));
+                }
+                const uint32_t lo = static_cast<uint32_t>(to_bf16(acc_v.x)) | (static_cast<uint32_t>(to_bf16(acc_v.y)) << 16);
+                const uint32_t hi = static_cast<uint32_t>(to_bf16(acc_v.z)) | (static_cast<uint32_t>(to_bf16(acc_v.w)) << 16);
+                *reinterpret_cast<uint2*>(a.Y + m * a.N + n0 + c) = make_uint2(lo, hi);
+              }
+            }
+            if (te == 0) a.counters[tile] = 0u;
+          }
+          named_bar(1, kAll);
+        }
+        continue;
+      } else if constexpr (BS) {
+        // ---- block scaling: promote every K block's partial product into FP32
+        // running sums, r[c] += P[c] * sx[kb][m_c] * sw[nt][kb], in K-block order.
+        // Epilogue warp e owns TMEM lanes quad * 32.. (its rows of the tile) and
+        // token columns [cbase, cbase + kCw) of the token block.
+        constexpr int kCw = BN / C::kEpiHalves;
+        constexpr int kAll = C::kEpiWarps * 32;
+        const int te = threadIdx.x - C::kEpiWarp0 * 32;  // 0 .. kAll - 1
+        const int half = te >> 7, th = te & 127;
+        const int cbase = half * kCw;
+        const Unit un = unit_of(a, u, KB);
+        const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
+        const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
+        const bool direct = a.splits == 1;
+        // thread te < BN stages the factor of token mbase + te; the next K
+        // block's factor is loaded while the current one is promoted
+        const int64_t mt = mbase + te;
+        const bool stager = te < BN && mt < a.M && un.nkb > 0;
+        const float* swp = a.sw + static_cast<int64_t>(un.nt) * KB;
+        // raw scales, multiplied only where they are stored: the product does
+        // not wait for the loads right after they are issued
+        float sxn = 0.0f, swn = 0.0f;
+        if (stager) {
+          sxn = __ldg(a.sx + un.kb0 * a.M + mt);
+          swn = __ldg(swp + un.kb0);
+        }
+        float r[kCw];
+#pragma unroll
+        for (int c = 0; c < kCw; ++c) r[c] = 0.0f;
+        bool have = true;
+        for (int j = 0; j < un.nkb; ++j, ++kbi) {
+          const int pb = kbi % C::kAccBufs;
+          float* fv = scale_vec + (kbi & 1) * 128;
+          if (te < BN) fv[te] = sxn * swn;
+          if (stager && j + 1 < un.nkb) {
+            const int64_t kb1 = un.kb0 + j + 1;
+            sxn = __ldg(a.sx + kb1 * a.M + mt);
+            swn = __ldg(swp + kb1);
+          }
+          if (have && !__all_sync(0xffffffffu, mbar_wait(&acc_full[pb], (kbi / C::kAccBufs) & 1, kWaitLimitNs,
+                                                           &s_abort))) {
+            have = false;
+            set_error(a.err, QLIN_ERR_TIMEOUT);
+            s_abort = 1;
+          }
+          // every epilogue warp takes part, also one whose wait gave up
+          named_bar(1, kAll);
+          if (!have) continue;
+          tc_fence_after();
+          const uint32_t tmem_d =
+              tmem_base + pb * C::kAccCols + cbase + (static_cast<uint32_t>(quad * 32) << 16);
+          uint32_t v[kCw / 16][16];
+#pragma unroll
+          for (int q = 0; q < kCw / 16; ++q) tmem_ld16(tmem_d + q * 16, v[q]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < kCw / 16; ++q) reg_fence16(v[q]);  // no use of v is hoisted above the wait
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[pb]);  // the partial buffer may take the next K block
+          if (lane == 0) mbar_arrive(&acc_empty[pb]);  // in registers: the buffer may take the next K block
+          const float4* f4 = reinterpret_cast<const float4*>(fv + cbase);
+#pragma unroll
+          for (int q = 0; q < kCw / 4; ++q) {
+            const float4 x = f4[q];
+            r[4 * q] = fmaf(__uint_as_float(v[q >> 2][(4 * q) & 15]), x.x, r[4 * q]);
+            r[4 * q + 1] = fmaf(__uint_as_float(v[q >> 2][(4 * q + 1) & 15]), x.y, r[4 * q + 1]);
+            r[4 * q + 2] = fmaf(__uint_as_float(v[q >> 2][(4 * q + 2) & 15]), x.z, r[4 * q + 2]);
+            r[4 * q + 3] = fmaf(__uint_as_float(v[q >> 2][(4 * q + 3) & 15]), x.w, r[4 * q + 3]);
+          }
         }
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = 0; c0 < kCw; c0 += 16) {
+          const int64_t m0 = mbase + cbase + c0;
           if (direct) {
-            if (mbase + c0 < a.M) {  // the same for all 128 threads: they skip the barriers together
-              uint16_t* box = reinterpret_cast<uint16_t*>(epi_box + (epi_n & 1) * C::kEpiBox);
-              if (t == 0) bulk_wait_read<1>();
-              named_bar_epi();
+            if (m0 < a.M) {  // the same for the 128 threads of this half: they skip the barriers together
+              uint16_t* box = reinterpret_cast<uint16_t*>(epi_box + (half * 2 + (epi_n & 1)) * C::kEpiBox);
+              if (th == 0) bulk_wait_read<1>();
+              named_bar(2 + half, 128);
 #pragma unroll
               for (int i = 0; i < 16; ++i) box[i * kTileN + quad * 32 + lane] = to_bf16(r[c0 + i]);
               fence_proxy_async_smem();
-              named_bar_epi();
-              if (t == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(mbase + c0));
+              named_bar(2 + half, 128);
+              if (th == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(m0));
               ++epi_n;
             }
           } else if (have) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int64_t m = mbase + c0 + i;
+              const int64_t m = m0 + i;
               if (m < a.M) __stcg(a.partials + (static_cast<int64_t>(un.split) * a.M + m) * a.N + n, r[c0 + i]);
             }
           }
@@ -508,26 +676,38 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
         if (!direct) {
           // last-arriver reduction of the K ranges, in split order (deterministic)
           __threadfence();
-          named_bar_epi();
+          named_bar(1, kAll);
           const int64_t tile = static_cast<int64_t>(un.mb) * a.ntiles + un.nt;
-          if (t == 0) s_last = !s_abort && (atomicAdd(a.counters + tile, 1u) == static_cast<uint32_t>(a.splits - 1));
-          named_bar_epi();
+          if (te == 0) s_last = !s_abort && (atomicAdd(a.counters + tile, 1u) == static_cast<uint32_t>(a.splits - 1));
+          named_bar(1, kAll);
           if (s_last) {
             __threadfence();
-            for (int c = 0; c < BN; ++c) {
-              const int64_t m = mbase + c;
-              if (m >= a.M) break;
-              float* p = a.partials + m * a.N + n;
-              float acc_v = 0.0f;
-              for (int sp = 0; sp < a.splits; ++sp) {  // read and clear: the workspace is left zero-filled
-                acc_v += __ldcg(p + static_cast<int64_t>(sp) * a.M * a.N);
-                __stcg(p + static_cast<int64_t>(sp) * a.M * a.N, 0.0f);
+#pragma unroll 1
+            for (int c0 = cbase; c0 < cbase + kCw; c0 += 16) {
+              if (mbase + c0 >= a.M) break;
+              float acc_v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc_v[i] = 0.0f;
+              // 16 tokens x several splits of independent loads in flight per thread
+#pragma unroll 4
+              for (int sp = 0; sp < a.splits; ++sp) {
+                float* p = a.partials + (static_cast<int64_t>(sp) * a.M + mbase + c0) * a.N + n;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (mbase + c0 + i < a.M) {  // read and clear: the workspace is left zero-filled
+                    acc_v[i] += __ldcg(p + static_cast<int64_t>(i) * a.N);
+                    __stcg(p + static_cast<int64_t>(i) * a.N, 0.0f);
+                  }
               }
-              a.Y[m * a.N + n] = to_bf16(acc_v);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int64_t m = mbase + c0 + i;
+                if (m < a.M) a.Y[m * a.N + n] = to_bf16(acc_v[i]);
+              }
             }
-            if (t == 0) a.counters[tile] = 0u;
+            if (te == 0) a.counters[tile] = 0u;
           }
-          named_bar_epi();
+          named_bar(1, kAll);
         }
         continue;
       }
@@ -624,7 +804,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W4, KPS, BS>::kThreads, 1)
         named_bar_epi();  // s_last is read by all before the next unit rewrites it
       }
     }
-    if (t == 0) bulk_wait_all();  // every tensor store has written its box
+    if ((t & 127) == 0) bulk_wait_all();  // every tensor store has written its box (one issuer per half)
   }
 
   tc_fence_before();
@@ -664,11 +844,13 @@ static int pick_bn(int64_t M) {
   return 256;
 }
 
-static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn = 256) {
+static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn = 256,
+                      int tile_n = kTileN) {
   TcPlan p;
   p.bn = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
+  p.wn = tile_n;
   p.mblocks = (M + p.bn - 1) / p.bn;
-  const int64_t tiles = (N / kTileN) * p.mblocks;
+  const int64_t tiles = (N / tile_n) * p.mblocks;
   const int64_t KB = K / cols;
   // K blocks per pipeline stage: small token tiles carry little activation
   // data, so W4A16 stages bundle several 4 KB code blocks to keep enough bytes
@@ -721,20 +903,26 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bo
 
 TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 64, true); }
 TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false); }
-// block scaling keeps the running sums of a 128-token tile in registers
+// Block scaling keeps the running sums of a 128-token tile in registers.  With
+// 128-token tiles the weight tile is 256 rows (two scale blocks) when N allows
+// and there are still enough tiles for every SM: a wider MMA moves fewer
+// shared-memory bytes per FLOP.
 TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
-  return plan_tc(M, N, K, num_sms, 128, false, 128);
+  const int bn = pick_bn(M) < 128 ? pick_bn(M) : 128;
+  const int64_t mblocks = (M + bn - 1) / bn;
+  const int wn = (bn == 128 && N % 256 == 0 && (N / 256) * mblocks >= num_sms) ? 256 : 128;
+  return plan_tc(M, N, K, num_sms, 128, false, 128, wn);
 }
 
-template <int BN, bool W4, int KPS, bool BS = false>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128>
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
                              const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
-  using C = TcCfg<BN, W4, KPS, BS>;
-  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS>, C::kSmemBytes);
+  using C = TcCfg<BN, W4, KPS, BS, WN>;
+  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   args.counters = static_cast<uint32_t*>(ws);
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.split.tiles)) : nullptr;
-  args.ntiles = static_cast<int>(args.N / kTileN);
+  args.ntiles = static_cast<int>(args.N / WN);
   args.mblocks = static_cast<int>(plan.mblocks);
   args.splits = plan.split.splits;
   args.kb_per_split = plan.split.kb_per_split;
@@ -757,7 +945,7 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS>, tx, tw, ty, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS, WN>, tx, tw, ty, args);
 }
 
 template <bool W4>
@@ -841,7 +1029,9 @@ cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8
     case 16: return launch_tc<16, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
     case 32: return launch_tc<32, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
     case 64: return launch_tc<64, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    default: return launch_tc<128, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default:
+      return plan.wn == 256 ? launch_tc<128, false, 1, true, 256>(tx, tw, ty, a, plan, ws, num_sms, st)
+                            : launch_tc<128, false, 1, true, 128>(tx, tw, ty, a, plan, ws, num_sms, st);
   }
 }
 

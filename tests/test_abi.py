@@ -42,6 +42,9 @@ def test_status_strings_and_version(lib):
     assert q.qlin_status_string(7) == "QLIN_ERR_TIMEOUT"
     assert q.qlin_status_string(99) == "QLIN_ERR_UNKNOWN"
     assert q.qlin_pack_format_version() == q.PACK_FORMAT_VERSION == 2
+    assert q.qlin_last_cuda_error() == 0  # nothing has failed on this thread
+    assert q.qlin_cuda_error_name(0) == "cudaSuccess"
+    assert q.qlin_cuda_error_name(2) == "cudaErrorMemoryAllocation"
 
 
 def test_packed_sizes_give_4_125_bits(lib):
