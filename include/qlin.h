@@ -74,7 +74,7 @@ typedef enum {
 
 /* Kernel selection for the *_ex GEMM calls (measurement and ablation). */
 #define QLIN_PATH_AUTO 0   /* choose by M (the default of the plain calls) */
-#define QLIN_PATH_GEMV 1   /* CUDA-core split-K GEMV, small M              */
+#define QLIN_PATH_GEMV 1   /* small-M split-K kernel (see qlin_w4a16_gemm)  */
 #define QLIN_PATH_TC 2     /* TMA + tcgen05 tensor-core kernel             */
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -141,9 +141,11 @@ int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric,
  * W4A16 linear layer ([LP] S11, S23): Y = bf16( sum_k X[m][k] s (q - z) ),
  * accumulated in FP32 ([LP] S22), from the packed buffers of qlin_pack_w4.
  * Kernel choice by M ([LP] S24 "different kernels for small batch and
- * large prefill"): a split-K CUDA-core GEMV for small M, a TMA + tcgen05
- * BF16 tensor-core kernel (weights dequantised to BF16 in shared memory)
- * otherwise.  Split-K partial sums are reduced in a fixed order, so results
+ * large prefill"): for M <= qlin_gemv_max_m (32) a split-K kernel that
+ * unpacks the nibbles in registers and multiplies on the tensor cores with
+ * register-level MMA (M <= 32 and K % 256 == 0; a CUDA-core GEMV otherwise on
+ * QLIN_PATH_GEMV), above it a TMA + tcgen05 BF16 tensor-core kernel (weights
+ * dequantised to BF16 in tensor or shared memory).  Split-K partial sums are reduced in a fixed order, so results
  * are deterministic.  workspace: qlin_workspace_size(QLIN_OP_W4A16_GEMM, ...)
  * bytes (may be NULL when that is 0).
  */
@@ -239,8 +241,8 @@ int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
  * GPU which loads the library holds until the process exits).
  *  - Sizes whose split-K partial sums need more than 8 MiB are rejected with
  *    QLIN_ERR_WORKSPACE_TOO_SMALL before anything is launched.  With the
- *    current split choice this accepts every M <= 16 on the Llama-3-8B and
- *    Llama-3-70B layer shapes.
+ *    current split choice this accepts every M <= 32 on the Llama-3-8B and
+ *    Llama-3-70B layer shapes (their split-K sums stay in on-chip memory).
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.

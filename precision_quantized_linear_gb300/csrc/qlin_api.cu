@@ -114,7 +114,7 @@ cudaError_t set_smem_once_impl(const void* kernel, int bytes, bool wide_clusters
 }
 
 // M at or below which the GEMV kernels are chosen (measured crossover).
-static int g_gemv_max_m_w4 = 16;
+static int g_gemv_max_m_w4 = 32;
 static int g_gemv_max_m_w8 = 0;  // the tcgen05 path was faster at every measured M
 
 }  // namespace qlin

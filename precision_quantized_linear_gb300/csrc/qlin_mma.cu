@@ -40,7 +40,6 @@ namespace qlin {
 constexpr int kMmaStageCols = 256;                 // K columns per stage (4 code tiles)
 constexpr int kMmaCodeBytes = 4 * 4096;            // codes of one stage
 constexpr int kMmaMetaOff = kMmaCodeBytes;         // 2 groups x 128 FP16 scales, then 2 x 64 B zeros
-constexpr int kMmaSumOff = kMmaMetaOff + 640;      // FP32 activation sums [2 groups][16 tokens]
 constexpr int kMmaXOff = kMmaCodeBytes + 1024;     // activation rows
 constexpr int kMmaXRow = kMmaStageCols * 2 + 16;   // 528 B per token row (conflict-free B fragments)
 constexpr int kMmaRowBlocks = 2;                   // m16 row blocks per consumer warp
@@ -55,13 +54,18 @@ constexpr int kMmaRedRows = 144;                   // >= splits x ceil(128 / spl
 template <int NT>
 struct MmaCfg {
   static constexpr int kTok = 8 * NT;
-  static constexpr int kStage = ((kMmaXOff + kTok * kMmaXRow) + 1023) / 1024 * 1024;
-  static constexpr int kStages = 3;  // three CTAs fit per SM for M <= 8, two otherwise
+  static constexpr int kSumOff = kMmaXOff + kTok * kMmaXRow;  // FP32 activation sums [2 groups][kTok tokens]
+  static constexpr int kStage = ((kSumOff + 2 * kTok * 4) + 1023) / 1024 * 1024;
+  // three CTAs fit per SM for M <= 8, two up to 32 (a ring of two stages at 32 tokens)
+  static constexpr int kStages = NT == 4 ? 2 : 3;
   // split-K receive buffer: [source rank][row within the owner's slice][token
   // slot]; ranks x slice rows <= 140 for every split count up to 16
   static constexpr int kRedFloats = kTok * kMmaRedRows;
   static constexpr int kSmem = 1024 + kStages * kStage + 256 + kRedFloats * 4;
   static constexpr int kMinBlocks = NT == 1 ? 3 : 2;
+  // independent MMA chains per group: one per 64-column tile up to 16
+  // tokens; with more token blocks there is enough independent work per warp
+  static constexpr int kChains = NT <= 2 ? 2 : 1;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -105,7 +109,7 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   return v;
 }
 
-template <int NT>  // n8 token blocks: M <= 8 * NT
+template <int NT>  // n8 token blocks: M <= 8 * NT (NT = 1, 2, 4)
 __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma_kernel(
     const uint16_t* __restrict__ X, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
     const uint8_t* __restrict__ zeros, uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K, int stages_per_split,
@@ -214,8 +218,8 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     // ------------------------------------------------------------ activation sums per group and token
     // M <= 8: C = ones(16 x 128) * X_g^T, every row of C holds sum_k x_k of the
     // n8 token block; lanes 0-3 (row 0) write tokens 2t, 2t + 1.
-    // M <= 16: C = X_g (16 tokens x 128) * ones(128 x 8), one MMA per k-step for
-    // all 16 tokens; lanes 4g (column 0) write tokens g and g + 8.
+    // M > 8: C = X_g (16 tokens x 128) * ones(128 x 8) per block of 16 tokens,
+    // one MMA per k-step; lanes 4g (column 0) write tokens g and g + 8.
     const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // BF16 1.0 pairs
     for (int i = 0; i < nst; ++i) {
       const int slot = i % C::kStages;
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
         break;
       }
       const uint32_t st = smem_u32(ring + slot * C::kStage);
-      float* sums = reinterpret_cast<float*>(ring + slot * C::kStage + kMmaSumOff);  // [group][16 tokens]
+      float* sums = reinterpret_cast<float*>(ring + slot * C::kStage + C::kSumOff);  // [group][kTok tokens]
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
         float cs[2][4];  // two chains of four k-steps
@@ -243,25 +247,29 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
             }
           }
           if (lane < 4)
-            *reinterpret_cast<float2*>(sums + grp * 16 + 2 * lane) =
+            *reinterpret_cast<float2*>(sums + grp * C::kTok + 2 * lane) =
                 make_float2(cs[0][0] + cs[1][0], cs[0][1] + cs[1][1]);
         } else {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            // A fragment of tokens 0-15 x columns 16ks..16ks+15: lanes 0-15 address
-            // token rows (lane & 15) at column 16ks, lanes 16-31 at 16ks + 8
-            uint32_t a[4];
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
-                         : "r"(st + kMmaXOff + (lane & 15) * kMmaXRow + (grp * 128 + ks * 16 + (lane >> 4) * 8) * 2));
-            if (ks < 2)
-              mma_bf16_16816_z(cs[ks & 1], a, ones[0], ones[1]);
-            else
-              mma_bf16_16816(cs[ks & 1], a, ones[0], ones[1]);
-          }
-          if (tq == 0) {
-            sums[grp * 16 + gq] = cs[0][0] + cs[1][0];
-            sums[grp * 16 + gq + 8] = cs[0][2] + cs[1][2];
+          for (int tb = 0; tb < NT / 2; ++tb) {  // 16 tokens per block
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              // A fragment of tokens 16tb .. 16tb+15 x columns 16ks..16ks+15: lanes
+              // 0-15 address token rows (lane & 15) at column 16ks, lanes 16-31 at 16ks + 8
+              uint32_t a[4];
+              asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                           : "r"(st + kMmaXOff + (tb * 16 + (lane & 15)) * kMmaXRow +
+                                 (grp * 128 + ks * 16 + (lane >> 4) * 8) * 2));
+              if (ks < 2)
+                mma_bf16_16816_z(cs[ks & 1], a, ones[0], ones[1]);
+              else
+                mma_bf16_16816(cs[ks & 1], a, ones[0], ones[1]);
+            }
+            if (tq == 0) {
+              sums[grp * C::kTok + tb * 16 + gq] = cs[0][0] + cs[1][0];
+              sums[grp * C::kTok + tb * 16 + gq + 8] = cs[0][2] + cs[1][2];
+            }
           }
         }
       }
@@ -311,28 +319,35 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
       bool sums_ok = true;
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
-        // one accumulator per 64-column tile and row block: independent MMA chains
-        float c[2][kMmaRowBlocks][NT][4];
+        // accumulators per row block and token block: one chain per 64-column
+        // tile (kChains = 2) or one for the group
+        float c[C::kChains][kMmaRowBlocks][NT][4];
 #pragma unroll
         for (int kb2 = 0; kb2 < 2; ++kb2) {
           const int kbl = grp * 2 + kb2;  // 64-column tile within the stage
+          const int ch = C::kChains == 2 ? kb2 : 0;
           uint32_t cur[kMmaRowBlocks][4];
 #pragma unroll
           for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
             for (int q = 0; q < 4; ++q) cur[rb][q] = cw[rb][q];
           if (kbl < 3) load_codes(kbl + 1, cw);
-          // B fragments: one ldmatrix.x4 per token block covers two 16-column k-steps
-          uint32_t b[2][NT][2][2];
-#pragma unroll
-          for (int half = 0; half < 2; ++half)
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-              ldsm_b2(st + kMmaXOff + (j * 8 + (lane & 7)) * kMmaXRow + (kbl * 64 + half * 32 + (lane >> 3) * 8) * 2,
-                      b[half][j]);
+          // B fragments: one ldmatrix.x4 per token block covers two 16-column
+          // k-steps; up to 16 tokens both halves of the tile are loaded up front
+          constexpr int kBH = NT <= 2 ? 2 : 1;  // halves of B fragments held at once
+          uint32_t b[kBH][NT][2][2];
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {  // k-step = columns 16a .. 16a+15 of half h
             const int h = ks >> 1, ia = 2 * (ks & 1);
+            if (ks == 0 || (kBH == 1 && ks == 2)) {
+#pragma unroll
+              for (int hb = 0; hb < kBH; ++hb)
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+                  ldsm_b2(st + kMmaXOff + (j * 8 + (lane & 7)) * kMmaXRow +
+                              (kbl * 64 + (h + hb) * 32 + (lane >> 3) * 8) * 2,
+                          b[hb][j]);
+            }
 #pragma unroll
             for (int rb = 0; rb < kMmaRowBlocks; ++rb) {
               uint32_t a[4];
@@ -342,11 +357,11 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
               a[3] = pair_at(cur[rb][2 * h + 1], ia + 1);  // row rr+8, columns 2t+8, 2t+9
 #pragma unroll
               for (int j = 0; j < NT; ++j) {
-                const uint32_t(&bk)[2] = b[h][j][ks & 1];
-                if (ks == 0)  // first k-step of the tile starts the chain from zero
-                  mma_bf16_16816_z(c[kb2][rb][j], a, bk[0], bk[1]);
+                const uint32_t(&bk)[2] = b[kBH == 2 ? h : 0][j][ks & 1];
+                if (ks == 0 && (C::kChains == 2 || kb2 == 0))  // the chain starts from zero
+                  mma_bf16_16816_z(c[ch][rb][j], a, bk[0], bk[1]);
                 else
-                  mma_bf16_16816(c[kb2][rb][j], a, bk[0], bk[1]);
+                  mma_bf16_16816(c[ch][rb][j], a, bk[0], bk[1]);
               }
             }
           }
@@ -356,7 +371,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
           sums_ok = __all_sync(0xffffffffu, mbar_wait(&summed[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort));
         float2 xv[NT];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) xv[j] = lds64f(st + kMmaSumOff + (grp * 16 + j * 8 + 2 * tq) * 4);
+        for (int j = 0; j < NT; ++j) xv[j] = lds64f(st + C::kSumOff + (grp * C::kTok + j * 8 + 2 * tq) * 4);
 #pragma unroll
         for (int rb = 0; rb < kMmaRowBlocks; ++rb)
 #pragma unroll
@@ -368,8 +383,9 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
             const float cz = __uint_as_float(((zb << zsh) & 0x000F0000u) | 0x43000000u);
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-              const float c0 = c[0][rb][j][hr * 2] + c[1][rb][j][hr * 2];
-              const float c1 = c[0][rb][j][hr * 2 + 1] + c[1][rb][j][hr * 2 + 1];
+              const float c0 = C::kChains == 2 ? c[0][rb][j][hr * 2] + c[C::kChains - 1][rb][j][hr * 2] : c[0][rb][j][hr * 2];
+              const float c1 = C::kChains == 2 ? c[0][rb][j][hr * 2 + 1] + c[C::kChains - 1][rb][j][hr * 2 + 1]
+                                               : c[0][rb][j][hr * 2 + 1];
               acc[rb][j][hr * 2] = fmaf(s, fmaf(-cz, xv[j].x, c0), acc[rb][j][hr * 2]);
               acc[rb][j][hr * 2 + 1] = fmaf(s, fmaf(-cz, xv[j].y, c1), acc[rb][j][hr * 2 + 1]);
             }
@@ -424,11 +440,14 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
         const uint32_t dst = cluster_map(red_u32, static_cast<uint32_t>(q)) +
                              static_cast<uint32_t>(((split * rstride + r - row_lo(q)) * C::kTok + tq * 2 * NT) * 4);
         const uint32_t dbar = cluster_map(bar_u32, static_cast<uint32_t>(q));
-        if constexpr (NT == 1)
+        if constexpr (NT == 1) {
           st_async_v2(dst, acc[rb][0][hr * 2], acc[rb][0][hr * 2 + 1], dbar);
-        else
-          st_async_v4(dst, acc[rb][0][hr * 2], acc[rb][0][hr * 2 + 1], acc[rb][NT - 1][hr * 2],
-                      acc[rb][NT - 1][hr * 2 + 1], dbar);
+        } else {
+#pragma unroll
+          for (int j = 0; j < NT; j += 2)  // slots 2j .. 2j + 3: token blocks j and j + 1
+            st_async_v4(dst + j * 8, acc[rb][j][hr * 2], acc[rb][j][hr * 2 + 1], acc[rb][j + 1][hr * 2],
+                        acc[rb][j + 1][hr * 2 + 1], dbar);
+        }
       }
   }
   if (!mbar_wait_cluster(red_bar, 0, kMmaWaitNs)) {
@@ -437,7 +456,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   }
   for (int idx = threadIdx.x; idx < r_n * mrows; idx += kMmaThreads) {
     const int m = idx / r_n, rl = idx % r_n;
-    const int slot = NT == 1 ? m : ((m & 7) >> 1) * 4 + (m >> 3) * 2 + (m & 1);
+    const int slot = NT == 1 ? m : ((m & 7) >> 1) * 2 * NT + (m >> 3) * 2 + (m & 1);
     const float* src = red + rl * C::kTok + slot;
     float v = 0.0f;
     for (int p = 0; p < splits; ++p) v += src[p * rstride * C::kTok];
@@ -495,9 +514,9 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
   SplitPlan p;
   const int64_t tiles = N / kTileN;
   const int64_t KS = K / kMmaStageCols;
-  const bool nt1 = M <= 8;
+  const int ntb = M <= 8 ? 1 : M <= 16 ? 2 : 4;  // n8 token blocks
   const double bw = 6.5e12, latency = 2.5e-6, startup = 3e-6;
-  const int ring = nt1 ? MmaCfg<1>::kStages : MmaCfg<2>::kStages;
+  const int ring = ntb == 1 ? MmaCfg<1>::kStages : ntb == 2 ? MmaCfg<2>::kStages : MmaCfg<4>::kStages;
   const double stage_bytes = kMmaCodeBytes + 640.0 + 2.0 * kMmaStageCols * static_cast<double>(M);
   const int64_t cap = KS < kMmaMaxCluster ? KS : kMmaMaxCluster;
   int64_t best_s = 1;
@@ -506,7 +525,10 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t per = (KS + c - 1) / c;
     const int64_t s = (KS + per - 1) / per;  // splits actually formed
     if (s != c) continue;
-    const int64_t fit = nt1 ? max_active_clusters<1>(static_cast<int>(s)) : max_active_clusters<2>(static_cast<int>(s));
+    const int cs = static_cast<int>(s);
+    const int64_t fit = ntb == 1   ? max_active_clusters<1>(cs)
+                        : ntb == 2 ? max_active_clusters<2>(cs)
+                                   : max_active_clusters<4>(cs);
     if (fit <= 0) continue;
     const int64_t waves = (tiles + fit - 1) / fit;
     const double conc = static_cast<double>((tiles < fit ? tiles : fit) * s);  // CTAs running together
@@ -526,7 +548,7 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
   return p;
 }
 
-bool mma_path_ok(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K % kMmaStageCols == 0; }
+bool mma_path_ok(int64_t M, int64_t K) { return M >= 1 && M <= 32 && K % kMmaStageCols == 0; }
 
 template <int NT>
 static cudaError_t launch_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
@@ -557,7 +579,8 @@ cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint
                              cudaStream_t st) {
   (void)ws;  // the split-K reduction runs in distributed shared memory
   if (M <= 8) return launch_mma<1>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
-  return launch_mma<2>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
+  if (M <= 16) return launch_mma<2>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
+  return launch_mma<4>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
 }
 
 }  // namespace qlin

@@ -49,7 +49,7 @@ struct TcCfg {
   // dequantised BF16 weight tiles: in TMEM (tcgen05.st, read by the MMA as
   // its A operand) when the accumulators leave room, else in shared memory
   static constexpr bool kATmem = W4 && BN <= 128;
-  static constexpr int kAStages = W4 ? 4 : 0;                   // A slots (one 64-column block each)
+  static constexpr int kAStages = W4 ? (kATmem ? 8 : 4) : 0;  // A slots (one 64-column block each)
   static constexpr int kAStage = (W4 && !kATmem) ? 128 * kBlkBytes : 0;  // shared-memory bytes per slot
   static constexpr int kASlotCols = 32;                         // TMEM columns per slot (64 BF16 per lane)
   // output staging: two boxes of 16 tokens x 128 rows of BF16 for the tensor stores
@@ -198,7 +198,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
       mbar_init(&empty[s], W4 ? 1 + C::kDqWarps : 1);
     }
     for (int i = 0; i < C::kAStages; ++i) {
-      mbar_init(&a_full[i], C::kDqWarps);
+      mbar_init(&a_full[i], C::kDqWarps / 2);  // one group of four warps fills a slot
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < C::kAccBufs; ++i) {
@@ -386,9 +386,13 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
   } else if (warp < C::kEpiWarp0) {
     // ---------------------------------------------------------------- dequantisation (W4A16)
     if constexpr (W4) {
+      // Two groups of four warps take the 64-column blocks in turn (group g the
+      // blocks with ait % 2 == g), so that two blocks are dequantised at once;
+      // within a group, the warp of TMEM lane quadrant q does rows 32q..32q+31,
+      // all 64 columns.
       const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
       const int r = quad * 32 + lane;            // weight row of the tile
-      const int h = (warp - 2) >> 2;             // which 32-column half of each 64-column block
+      const int grp = (warp - 2) >> 2;
       int it = 0, ait = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
@@ -403,53 +407,67 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
           const int kb = un.kb0 + j * KPS;
 #pragma unroll
           for (int i = 0; i < KPS; ++i, ++ait) {
+            const bool mine = (ait & 1) == grp;
             const int ai = ait % C::kAStages;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(&a_empty[ai], ((ait / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
-              ok = false;
-              break;
+            uint4 c[2];
+            float scale = 0.0f, zq = 0.0f;
+            if (mine) {
+              if (!__all_sync(0xffffffffu,
+                              mbar_wait(&a_empty[ai], ((ait / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
+                ok = false;
+                break;
+              }
+              const uint32_t sts = smem_u32(st);
+              c[0] = lds128(sts + KPS * C::kXBlk + i * 4096 + r * 16);         // columns 0..31
+              c[1] = lds128(sts + KPS * C::kXBlk + i * 4096 + 2048 + r * 16);  // columns 32..63
+              const int gi = (kb + i) / 2 - kb / 2;  // group of this block within the stage
+              scale = __half2float(
+                  __ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
+              const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
+              zq = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
             }
-            const uint32_t sts = smem_u32(st);
-            const uint4 c = lds128(sts + KPS * C::kXBlk + i * 4096 + h * 2048 + r * 16);
-            const int gi = (kb + i) / 2 - kb / 2;  // group of this block within the stage
-            const float scale =
-                __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
-            const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
-            const float zq = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
             if (i == KPS - 1) {
               __syncwarp();
               if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
             }
+            if (!mine) continue;
             const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq);
             const __nv_bfloat162 s2 = __float2bfloat162_rn(scale);
-            const uint32_t words[4] = {c.x, c.y, c.z, c.w};
             if constexpr (C::kATmem) {
               // lane r of the slot holds row r: 32 columns x two BF16 = the 64 columns of the block
               tc_fence_after();
-              uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const uint4 d = dequant8(words[t], zoff, s2);
-                v[t] = d.x;
-                v[4 + t] = d.y;
-                v[8 + t] = d.z;
-                v[12 + t] = d.w;
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
+                uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const uint4 d = dequant8(words[t], zoff, s2);
+                  v[t] = d.x;
+                  v[4 + t] = d.y;
+                  v[8 + t] = d.z;
+                  v[12 + t] = d.w;
+                }
+                tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
+                              h * 16,
+                          v);
               }
-              tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
-                            h * 16,
-                        v);
               tmem_st_wait();
               tc_fence_before();
             } else {
               uint8_t* arow = aring + ai * C::kAStage + r * 128;
-              uint4 d[4];
 #pragma unroll
-              for (int t = 0; t < 4; ++t) d[t] = dequant8(words[t], zoff, s2);
-              // 16-byte chunk cc = 4h + i holds columns 8cc..8cc+7: position i of words 0..3
-              *reinterpret_cast<uint4*>(arow + (((h * 4 + 0) ^ (r & 7)) << 4)) = make_uint4(d[0].x, d[1].x, d[2].x, d[3].x);
-              *reinterpret_cast<uint4*>(arow + (((h * 4 + 1) ^ (r & 7)) << 4)) = make_uint4(d[0].y, d[1].y, d[2].y, d[3].y);
-              *reinterpret_cast<uint4*>(arow + (((h * 4 + 2) ^ (r & 7)) << 4)) = make_uint4(d[0].z, d[1].z, d[2].z, d[3].z);
-              *reinterpret_cast<uint4*>(arow + (((h * 4 + 3) ^ (r & 7)) << 4)) = make_uint4(d[0].w, d[1].w, d[2].w, d[3].w);
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
+                uint4 d[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) d[t] = dequant8(words[t], zoff, s2);
+                // 16-byte chunk cc = 4h + i holds columns 8cc..8cc+7: position i of words 0..3
+                *reinterpret_cast<uint4*>(arow + (((h * 4 + 0) ^ (r & 7)) << 4)) = make_uint4(d[0].x, d[1].x, d[2].x, d[3].x);
+                *reinterpret_cast<uint4*>(arow + (((h * 4 + 1) ^ (r & 7)) << 4)) = make_uint4(d[0].y, d[1].y, d[2].y, d[3].y);
+                *reinterpret_cast<uint4*>(arow + (((h * 4 + 2) ^ (r & 7)) << 4)) = make_uint4(d[0].z, d[1].z, d[2].z, d[3].z);
+                *reinterpret_cast<uint4*>(arow + (((h * 4 + 3) ^ (r & 7)) << 4)) = make_uint4(d[0].w, d[1].w, d[2].w, d[3].w);
+              }
               fence_proxy_async_smem();
             }
             __syncwarp();

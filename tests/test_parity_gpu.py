@@ -152,6 +152,14 @@ def test_w4a16_llama8b_decode_sampled(K, N, M):
     assert err <= TOL
 
 
+@pytest.mark.parametrize("K,N", [(4096, 14336), (14336, 4096), (8192, 10240)])
+@pytest.mark.parametrize("M", [17, 24, 32])
+def test_w4a16_mid_m_small_kernel_sampled(K, N, M):
+    # 17 <= M <= 32 on the register-level MMA kernel (four token blocks), split-K clusters
+    err, _, _ = _sampled_w4(M, N, K, q.PATH_GEMV, seed=K + N + M)
+    assert err <= TOL
+
+
 def test_w4a16_deterministic_split_k():
     _, layer, X = _sampled_w4(4, 4096, 14336, q.PATH_AUTO, seed=9, nsamp=10)
     Xd = to_dev(X)
