@@ -862,11 +862,76 @@ static int pick_bn(int64_t M) {
   return 256;
 }
 
+// Cost of a unit on one SM in cycles at 2.07 GHz, measured on GB300 per token
+// tile (64 / 128 / 256 tokens) with the split count forced: cycles per K block
+// (64 columns W4A16, 128 E4M3), a start-up and drain cost paid once per CTA,
+// and the split-K fix-up of a unit (partial sums written, the last arriver's
+// reduction), which grows with the tile and, by half again per extra split,
+// with the split count.
+struct TcCost {
+  double kb, once, fix;
+};
+static TcCost tc_cost(bool w4, int bn) {
+  const int i = bn >= 256 ? 2 : bn >= 128 ? 1 : 0;
+  static const double kb8[3] = {590, 594, 657}, once8[3] = {10.5e3, 15e3, 24.5e3};
+  static const double kb4[3] = {713, 906, 924}, once4[3] = {11e3, 8.9e3, 16.7e3};
+  static const double fix[3] = {23e3, 40e3, 70e3};
+  return TcCost{w4 ? kb4[i] : kb8[i], w4 ? once4[i] : once8[i], fix[i]};
+}
+
+// Token tile and split count for M > 32 (tiles of 64 tokens or more), chosen
+// together to minimise max(memory time, rounds of units x unit cost + once).
+// Ties keep the wider tile (fewer re-reads of the weights).
+static void plan_tc_joint(TcPlan& p, int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn) {
+  const int64_t KB = K / cols;
+  const double wbytes = static_cast<double>(N) * static_cast<double>(K) * (w4 ? 0.51953125 : 1.0);
+  const double xbytes = static_cast<double>(M) * static_cast<double>(K) * (w4 ? 2.0 : 1.0);
+  const double ybytes = 2.0 * static_cast<double>(M) * static_cast<double>(N);
+  double best = 1e30;
+  const int top = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
+  for (int bn = top; bn >= 64; bn /= 2) {
+    const TcCost cost = tc_cost(w4, bn);
+    const int kps = (w4 && bn <= 64 && KB % 2 == 0) ? 2 : 1;
+    const int64_t KS = KB / kps;
+    const int64_t mblocks = (M + bn - 1) / bn;
+    const int64_t tiles = (N / kTileN) * mblocks;
+    const int64_t min_stages = (4 + kps - 1) / kps;
+    int64_t max_s = KS / min_stages;
+    if (max_s < 1) max_s = 1;
+    if (max_s > 8) max_s = 8;
+    const double t_mem = (wbytes * static_cast<double>(mblocks > 4 ? 4 : mblocks) + xbytes + ybytes) / 6.5e12;
+    for (int c = 1; c <= max_s; ++c) {
+      const int64_t per = (KS + c - 1) / c;
+      if ((KS + per - 1) / per != c) continue;  // that many splits would not form
+      const double rounds = std::ceil(static_cast<double>(tiles * c) / num_sms);
+      const double fix = c > 1 ? cost.fix * (1.0 + 0.5 * (c - 2)) : 0.0;
+      const double cyc = rounds * (static_cast<double>(per * kps) * cost.kb + fix) + cost.once;
+      const double t = std::max(cyc / 2.07e9, t_mem);
+      if (t < best) {
+        best = t;
+        p.bn = bn;
+        p.kps = kps;
+        p.mblocks = mblocks;
+        p.split.splits = c;
+        p.split.kb_per_split = static_cast<int>(per) * kps;
+        p.split.tiles = tiles;
+      }
+    }
+  }
+  p.split.ws_bytes = p.split.splits > 1 ? counters_bytes(p.split.tiles) +
+                                              sizeof(float) * static_cast<size_t>(p.split.splits) * M * N
+                                        : 0;
+}
+
 static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn = 256,
-                      int tile_n = kTileN) {
+                      int tile_n = kTileN, bool joint = true) {
   TcPlan p;
   p.bn = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
   p.wn = tile_n;
+  if (joint && p.bn >= 64 && tile_n == kTileN) {
+    plan_tc_joint(p, M, N, K, num_sms, cols, w4, max_bn);
+    return p;
+  }
   p.mblocks = (M + p.bn - 1) / p.bn;
   const int64_t tiles = (N / tile_n) * p.mblocks;
   const int64_t KB = K / cols;
@@ -929,7 +994,7 @@ TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   const int bn = pick_bn(M) < 128 ? pick_bn(M) : 128;
   const int64_t mblocks = (M + bn - 1) / bn;
   const int wn = (bn == 128 && N % 256 == 0 && (N / 256) * mblocks >= num_sms) ? 256 : 128;
-  return plan_tc(M, N, K, num_sms, 128, false, 128, wn);
+  return plan_tc(M, N, K, num_sms, 128, false, 128, wn, false);
 }
 
 template <int BN, bool W4, int KPS, bool BS = false, int WN = 128>
