@@ -72,6 +72,12 @@ typedef enum {
 #define QLIN_OP_QUANT_W_FP8 3
 #define QLIN_OP_W8A8_BLOCK_GEMM 4
 
+/* Activation of the fused output epilogue (qlin_*_gemm_fused). */
+#define QLIN_ACT_NONE 0
+#define QLIN_ACT_RELU 1 /* max(v, 0)                                   */
+#define QLIN_ACT_SILU 2 /* v / (1 + exp(-v))                           */
+#define QLIN_ACT_GELU 3 /* v * Phi(v) = 0.5 v (1 + erf(v / sqrt 2))    */
+
 /* Kernel selection for the *_ex GEMM calls (measurement and ablation). */
 #define QLIN_PATH_AUTO 0   /* choose by M (the default of the plain calls) */
 #define QLIN_PATH_GEMV 1   /* small-M split-K kernel (see qlin_w4a16_gemm)  */
@@ -158,6 +164,17 @@ int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales
                        void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
                        int path, void* stream);
 
+/* W4A16 with a fused output epilogue ([LP] S23 "fused epilogue ... write
+ * output once", S24 "bias / activation epilogue"):
+ *     Y[m][n] = bf16( act( acc[m][n] + bias[n] ) )
+ * acc the FP32 result of qlin_w4a16_gemm, bias BF16 [N] (NULL: none, else
+ * 16-byte aligned), act one of QLIN_ACT_*; bias and activation are applied in
+ * FP32 and Y is rounded once.  Every kernel path applies it where it writes Y
+ * (also after a split-K reduction), so no extra pass over Y is made. */
+int qlin_w4a16_gemm_fused(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                          void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const void* bias_bf16, int act,
+                          void* workspace, size_t ws_bytes, int path, void* stream);
+
 /*
  * Per-token FP8 activation quantisation ([LP] S4 per-token, S8 current
  * scaling), one fused kernel: for each row m, amax_m = max_k |X[m][k]|,
@@ -190,6 +207,12 @@ int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3
 int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                           void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                           int path, void* stream);
+
+/* W8A8 with the fused output epilogue of qlin_w4a16_gemm_fused:
+ * Y[m][n] = bf16( act( (acc[m][n] * sx[m]) * sw + bias[n] ) ). */
+int qlin_w8a8_fp8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                             void* Y_bf16, int64_t M, int64_t N, int64_t K, const void* bias_bf16, int act,
+                             void* workspace, size_t ws_bytes, int path, void* stream);
 
 /* ---- FP8 block scaling ([LP] S8 "Block Scaling": each block of the tensor
  * has its own scale, x ~ x_fp8 * scale_block, scale_block = amax_block /

@@ -10,7 +10,8 @@ follows (see ``qlin_oracle.c`` for the list):
   [LP] "Low-precision LLM inference: FP8/INT8/INT4/FP4 kernels and
        calibration" -- S2 uniform quantisation, S3 symmetric/asymmetric,
        S4 granularity, S5 effective bits, S7 E4M3, S8 FP8 current scaling,
-       S22 accumulator precision.
+       S22 accumulator precision, S23/S24 fused bias / activation
+       epilogue (``epilogue`` below).
   [TP] "Quantization throughput by batch size: why W4A16 is overtaken by
        W8A8" -- the arithmetic-intensity roofline (``roofline_*`` below).
 
@@ -353,3 +354,29 @@ def w8a8_blocks_at(Xq, sx, Wq, sw, ms, ns) -> np.ndarray:
     _load().orc_w8a8_blocks_at(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), M, N, K, _ptr(ms), _ptr(ns), ms.size,
                                _ptr(out))
     return out
+
+
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = 0, 1, 2, 3
+
+
+def epilogue(Y: np.ndarray, bias_bf16, act: int) -> np.ndarray:
+    """[LP] S23/S24 fused epilogue, in double: act(Y[m][n] + bias[n]).
+
+    bias_bf16: BF16 bit patterns [N] or None.  act: ReLU max(v, 0); SiLU
+    v * sigmoid(v) = v / (1 + e^-v); GELU v * Phi(v), Phi the standard normal
+    distribution function, Phi(v) = (1 + erf(v / sqrt 2)) / 2.
+    """
+    import math
+
+    V = np.array(Y, dtype=np.float64, copy=True)
+    if bias_bf16 is not None:
+        V = V + bf16_bits_to_f32(np.asarray(bias_bf16, np.uint16)).astype(np.float64)[None, :]
+    if act == ACT_RELU:
+        return np.maximum(V, 0.0)
+    if act == ACT_SILU:
+        return V / (1.0 + np.exp(-V))
+    if act == ACT_GELU:
+        phi = np.vectorize(lambda v: 0.5 * (1.0 + math.erf(v / math.sqrt(2.0))))(V) if V.size else V
+        return V * phi
+    assert act == ACT_NONE
+    return V

@@ -25,12 +25,14 @@ __all__ = [
     "qlin_w8a8_fp8_gemm", "qlin_w8a8_fp8_gemm_ex", "qlin_get_device_error", "qlin_gemv_max_m",
     "qlin_selftest_wait_timeout", "qlin_w4a16_gemv_noalloc", "qlin_quant_act_fp8_blocks", "qlin_quant_w_fp8_blocks",
     "qlin_w8a8_fp8_block_gemm", "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "OP_W8A8_BLOCK_GEMM",
-    "PATH_AUTO", "PATH_GEMV", "PATH_TC",
+    "PATH_AUTO", "PATH_GEMV", "PATH_TC", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU",
+    "qlin_w4a16_gemm_fused", "qlin_w8a8_fp8_gemm_fused",
     "PACK_FORMAT_VERSION",
 ]
 
 OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM = 1, 2, 3, 4
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = 0, 1, 2, 3
 PACK_FORMAT_VERSION = 2
 
 _lock = threading.Lock()
@@ -56,6 +58,8 @@ _SIGS = {
     "qlin_quant_w_fp8": [_p, _i64, _i64, _p, _p, _p, _sz, _p],
     "qlin_w8a8_fp8_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
     "qlin_w8a8_fp8_gemm_ex": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _int, _p],
+    "qlin_w4a16_gemm_fused": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _int, _p, _sz, _int, _p],
+    "qlin_w8a8_fp8_gemm_fused": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _int, _p],
     "qlin_get_device_error": [_p],
     "qlin_selftest_wait_timeout": [ctypes.c_uint32, _p],
     "qlin_w4a16_gemv_noalloc": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p],
@@ -173,6 +177,13 @@ def qlin_w4a16_gemm_ex(X, codes, scales, zeros, Y, M, N, K, G, workspace, ws_byt
                                             _ptr(workspace), ws_bytes, path, _stream(stream)), "qlin_w4a16_gemm_ex")
 
 
+def qlin_w4a16_gemm_fused(X, codes, scales, zeros, Y, M, N, K, G, bias, act, workspace, ws_bytes, path,
+                          stream=None):
+    return _check(load().qlin_w4a16_gemm_fused(_ptr(X), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(Y), M, N, K,
+                                               G, _ptr(bias), act, _ptr(workspace), ws_bytes, path,
+                                               _stream(stream)), "qlin_w4a16_gemm_fused")
+
+
 def qlin_quant_act_fp8(X, M, K, Xq, sx, stream=None):
     return _check(load().qlin_quant_act_fp8(_ptr(X), M, K, _ptr(Xq), _ptr(sx), _stream(stream)),
                   "qlin_quant_act_fp8")
@@ -192,6 +203,12 @@ def qlin_w8a8_fp8_gemm_ex(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, path,
     return _check(load().qlin_w8a8_fp8_gemm_ex(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
                                                _ptr(workspace), ws_bytes, path, _stream(stream)),
                   "qlin_w8a8_fp8_gemm_ex")
+
+
+def qlin_w8a8_fp8_gemm_fused(Xq, sx, Wq, sw, Y, M, N, K, bias, act, workspace, ws_bytes, path, stream=None):
+    return _check(load().qlin_w8a8_fp8_gemm_fused(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
+                                                  _ptr(bias), act, _ptr(workspace), ws_bytes, path,
+                                                  _stream(stream)), "qlin_w8a8_fp8_gemm_fused")
 
 
 def qlin_quant_act_fp8_blocks(X, M, K, Xq, sx, stream=None):

@@ -144,6 +144,15 @@ int cuda_status(cudaError_t e) {
 
 static int launch_status(cudaError_t e) { return cuda_status(e); }
 
+// Validated output epilogue of the *_fused calls.
+static int make_epi(const void* bias_bf16, int act, Epi* epi) {
+  if (act < QLIN_ACT_NONE || act > QLIN_ACT_GELU) return QLIN_ERR_INVALID_VALUE;
+  if (bias_bf16 && !aligned16(bias_bf16)) return QLIN_ERR_MISALIGNED;
+  epi->bias = static_cast<const uint16_t*>(bias_bf16);
+  epi->act = act;
+  return QLIN_OK;
+}
+
 extern "C" {
 
 const char* qlin_status_string(int status) {
@@ -226,9 +235,9 @@ int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric,
                                       static_cast<cudaStream_t>(stream)));
 }
 
-int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
-                       void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
-                       int path, void* stream) {
+static int w4a16_impl(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                      void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const Epi& epi, void* workspace,
+                      size_t ws_bytes, int path, void* stream) {
   if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
   int st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
@@ -252,15 +261,31 @@ int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales
     if (mma_path_ok(M, K)) {
       const SplitPlan p = plan_w4a16_mma(M, N, K, d->num_sms);
       if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-      return launch_status(launch_w4a16_mma(X, c, s, z, Y, M, N, K, p, workspace, d->err, cs));
+      return launch_status(launch_w4a16_mma(X, c, s, z, Y, M, N, K, p, workspace, d->err, cs, epi));
     }
     const SplitPlan p = plan_w4a16_gemv(M, N, K, d->num_sms);
     if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-    return launch_status(launch_w4a16_gemv(X, c, s, z, Y, M, N, K, p, workspace, cs));
+    return launch_status(launch_w4a16_gemv(X, c, s, z, Y, M, N, K, p, workspace, cs, epi));
   }
   const TcPlan p = plan_w4a16_tc(M, N, K, d->num_sms);
   if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, p, workspace, d->err, d->num_sms, cs));
+  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, p, workspace, d->err, d->num_sms, cs, epi));
+}
+
+int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                       void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
+                       int path, void* stream) {
+  return w4a16_impl(X_bf16, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, Epi{}, workspace, ws_bytes, path,
+                    stream);
+}
+
+int qlin_w4a16_gemm_fused(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+                          void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const void* bias_bf16, int act,
+                          void* workspace, size_t ws_bytes, int path, void* stream) {
+  Epi epi;
+  const int st = make_epi(bias_bf16, act, &epi);
+  if (st != QLIN_OK) return st;
+  return w4a16_impl(X_bf16, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, epi, workspace, ws_bytes, path, stream);
 }
 
 int qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
@@ -298,9 +323,9 @@ int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, fl
                                           static_cast<cudaStream_t>(stream)));
 }
 
-int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
-                          int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, int path,
-                          void* stream) {
+static int w8a8_impl(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
+                     int64_t M, int64_t N, int64_t K, const Epi& epi, void* workspace, size_t ws_bytes, int path,
+                     void* stream) {
   int st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;
@@ -320,11 +345,26 @@ int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e
   if (path == QLIN_PATH_GEMV) {
     const SplitPlan p = plan_w8a8_gemv(M, N, K, d->num_sms);
     if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-    return launch_status(launch_w8a8_gemv(xq, sx, wq, sw, Y, M, N, K, p, workspace, cs));
+    return launch_status(launch_w8a8_gemv(xq, sx, wq, sw, Y, M, N, K, p, workspace, cs, epi));
   }
   const TcPlan p = plan_w8a8_tc(M, N, K, d->num_sms);
   if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_w8a8_tc(xq, sx, wq, sw, Y, M, N, K, p, workspace, d->err, d->num_sms, cs));
+  return launch_status(launch_w8a8_tc(xq, sx, wq, sw, Y, M, N, K, p, workspace, d->err, d->num_sms, cs, epi));
+}
+
+int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
+                          int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, int path,
+                          void* stream) {
+  return w8a8_impl(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, Epi{}, workspace, ws_bytes, path, stream);
+}
+
+int qlin_w8a8_fp8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                             void* Y_bf16, int64_t M, int64_t N, int64_t K, const void* bias_bf16, int act,
+                             void* workspace, size_t ws_bytes, int path, void* stream) {
+  Epi epi;
+  const int st = make_epi(bias_bf16, act, &epi);
+  if (st != QLIN_OK) return st;
+  return w8a8_impl(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, epi, workspace, ws_bytes, path, stream);
 }
 
 int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,

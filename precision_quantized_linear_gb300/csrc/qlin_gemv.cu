@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(128) w4a16_gemv_kernel(const uint16_t* __restr
                                                          const uint16_t* __restrict__ scales,
                                                          const uint8_t* __restrict__ zeros, uint16_t* __restrict__ Y,
                                                          int64_t M, int64_t N, int64_t K, int kb_per_split, int splits,
-                                                         float* partials, uint32_t* counters) {
+                                                         float* partials, uint32_t* counters, Epi epi) {
   extern __shared__ float4 smem_f4[];
   float* smem = reinterpret_cast<float*>(smem_f4);
   const int nt = blockIdx.x, split = blockIdx.y;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(128) w4a16_gemv_kernel(const uint16_t* __restr
   const int64_t n = static_cast<int64_t>(nt) * kTileN + threadIdx.x;
   const int64_t tile = static_cast<int64_t>(blockIdx.z) * gridDim.x + nt;
   splitk_finish<MT>(mine, mcount, m0, n, M, N, split, splits, tile, partials, counters,
-                    [&](int64_t m, int64_t nn, float v) { Y[m * N + nn] = f32_to_bf16_rn(v); });
+                    [&](int64_t m, int64_t nn, float v) { Y[m * N + nn] = f32_to_bf16_rn(epi_apply(epi, v, nn)); });
 }
 
 // Launch with programmatic stream serialisation: the kernel may start while
@@ -277,7 +277,7 @@ SplitPlan plan_w4a16_gemv(int64_t M, int64_t N, int64_t K, int num_sms) {
 
 cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                               uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, const Epi& epi) {
   const int mt = gemv_mt(M);
   dim3 grid(static_cast<unsigned>(N / kTileN), plan.splits, static_cast<unsigned>((M + mt - 1) / mt));
   const size_t smem = w4_gemv_smem(mt, plan.kb_per_split);
@@ -290,7 +290,7 @@ cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uin
     e = set_smem_once(w4a16_gemv_kernel<MTV>, 64 * 1024);                                                \
     if (e != cudaSuccess) return e;                                                                      \
     e = launch_pdl(w4a16_gemv_kernel<MTV>, grid, smem, st, X, codes, scales, zeros, Y, M, N, K,            \
-                   plan.kb_per_split, plan.splits, partials, counters);                                  \
+                   plan.kb_per_split, plan.splits, partials, counters, epi);                             \
     break;
     QLIN_W4GEMV(1)
     QLIN_W4GEMV(2)
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(128) w8a8_gemv_kernel(const uint8_t* __restric
                                                         const uint8_t* __restrict__ Wq, const float* __restrict__ sw,
                                                         uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K,
                                                         int kb_per_split, int splits, float* partials,
-                                                        uint32_t* counters) {
+                                                        uint32_t* counters, Epi epi) {
   extern __shared__ float4 smem_f4[];
   float* xs = reinterpret_cast<float*>(smem_f4);  // [MT][KR]
   __shared__ float acc_s[MT][kTileN];
@@ -395,7 +395,9 @@ __global__ void __launch_bounds__(128) w8a8_gemv_kernel(const uint8_t* __restric
   const int64_t n = static_cast<int64_t>(nt) * kTileN + threadIdx.x;
   const int64_t tile = static_cast<int64_t>(blockIdx.z) * gridDim.x + nt;
   splitk_finish<MT>(mine, mcount, m0, n, M, N, split, splits, tile, partials, counters,
-                    [&](int64_t m, int64_t nn, float v) { Y[m * N + nn] = f32_to_bf16_rn((v * sx[m]) * s_w); });
+                    [&](int64_t m, int64_t nn, float v) {
+                      Y[m * N + nn] = f32_to_bf16_rn(epi_apply(epi, (v * sx[m]) * s_w, nn));
+                    });
 }
 
 SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -410,7 +412,8 @@ SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms) {
 }
 
 cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
-                             int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st) {
+                             int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st,
+                             const Epi& epi) {
   const int mt = gemv_mt(M);
   dim3 grid(static_cast<unsigned>(N / kTileN), plan.splits, static_cast<unsigned>((M + mt - 1) / mt));
   const size_t smem = sizeof(float) * static_cast<size_t>(mt) * plan.kb_per_split * kTileK;
@@ -423,7 +426,7 @@ cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* 
     e = set_smem_once(w8a8_gemv_kernel<MTV>, 64 * 1024);                                                   \
     if (e != cudaSuccess) return e;                                                                        \
     e = launch_pdl(w8a8_gemv_kernel<MTV>, grid, smem, st, Xq, sx, Wq, sw, Y, M, N, K, plan.kb_per_split,     \
-                   plan.splits, partials, counters);                                                       \
+                   plan.splits, partials, counters, epi);                                                  \
     break;
     QLIN_W8GEMV(1)
     QLIN_W8GEMV(2)

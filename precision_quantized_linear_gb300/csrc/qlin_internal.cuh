@@ -20,6 +20,57 @@ __device__ __forceinline__ void set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Output epilogue of the GEMMs ([LP] S23 "fused epilogue", S24 "bias /
+// activation epilogue fused"): Y = bf16(act(acc + bias[n])), acc the FP32
+// result after the quantisation scales; bias BF16 [N] or null, act QLIN_ACT_*.
+struct Epi {
+  const uint16_t* bias = nullptr;
+  int act = QLIN_ACT_NONE;
+};
+// bias[n] as FP32 (0 without a bias); load it early, it is needed only at the end
+__device__ __forceinline__ float epi_bias(const Epi& e, int64_t n) {
+  return e.bias ? __uint_as_float(static_cast<uint32_t>(__ldg(e.bias + n)) << 16) : 0.0f;
+}
+// SiLU as v / (1 + e^-v) with the hardware exponential and the fast divide
+// (relative error ~2^-21, far below the BF16 output's 2^-9; 0 once e^-v
+// overflows, i.e. for v < -88, where |silu(v)| < 2^-120); GELU as v * Phi(v)
+// with CUDA's normcdff.
+__device__ __forceinline__ float epi_silu(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+__device__ __forceinline__ float epi_gelu(float v) { return v * normcdff(v); }
+// act(v + b)
+__device__ __forceinline__ float epi_act(int act, float v, float b) {
+  v += b;
+  switch (act) {
+    case QLIN_ACT_RELU: return fmaxf(v, 0.0f);
+    case QLIN_ACT_SILU: return epi_silu(v);
+    case QLIN_ACT_GELU: return epi_gelu(v);
+    default: return v;
+  }
+}
+__device__ __forceinline__ float epi_apply(const Epi& e, float v, int64_t n) { return epi_act(e.act, v, epi_bias(e, n)); }
+// act(o[i] + b) for a run of values of one output column: one branch on the
+// activation for the whole run, so that each loop stays straight-line code
+template <int L>
+__device__ __forceinline__ void epi_run(int act, float (&o)[L], float b) {
+  switch (act) {
+    case QLIN_ACT_RELU:
+#pragma unroll
+      for (int i = 0; i < L; ++i) o[i] = epi_act(QLIN_ACT_RELU, o[i], b);
+      break;
+    case QLIN_ACT_SILU:
+#pragma unroll
+      for (int i = 0; i < L; ++i) o[i] = epi_act(QLIN_ACT_SILU, o[i], b);
+      break;
+    case QLIN_ACT_GELU:
+#pragma unroll
+      for (int i = 0; i < L; ++i) o[i] = epi_act(QLIN_ACT_GELU, o[i], b);
+      break;
+    default:
+#pragma unroll
+      for (int i = 0; i < L; ++i) o[i] += b;
+  }
+}
+
 // Split-K workspace: [counters: one uint32 per output tile, padded to 256 B]
 // [partials: splits x M x N float].
 struct SplitPlan {
@@ -56,19 +107,20 @@ cudaError_t launch_quant_w_fp8(const uint16_t* W, int64_t N, int64_t K, uint8_t*
 SplitPlan plan_w4a16_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                               uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, const Epi& epi = Epi{});
 
 // W4A16 small-M kernel with register-level dequantisation feeding mma.sync
-// (M <= 16, K % 256 == 0); kb_per_split counts 256-column stages.
+// (M <= 32, K % 256 == 0); kb_per_split counts 256-column stages.
 bool mma_path_ok(int64_t M, int64_t K);
 SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                              uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, int* err,
-                             cudaStream_t st);
+                             cudaStream_t st, const Epi& epi = Epi{});
 
 SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
-                             int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st);
+                             int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st,
+                             const Epi& epi = Epi{});
 
 // tcgen05 kernels: swap-AB (weights are the 128-row MMA operand, tokens the N side)
 struct TcPlan {
@@ -84,10 +136,10 @@ TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
-                            int num_sms, cudaStream_t st);
+                            int num_sms, cudaStream_t st, const Epi& epi = Epi{});
 cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                            int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
-                           cudaStream_t st);
+                           cudaStream_t st, const Epi& epi = Epi{});
 // FP8 block scaling: sx = [K/128][M], sw = [N/128][K/128] FP32 block scales.
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                                  int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,

@@ -29,6 +29,7 @@
 #include <cuda_fp16.h>
 
 #include <array>
+#include <type_traits>
 #include <mutex>
 #include <unordered_map>
 
@@ -109,11 +110,11 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   return v;
 }
 
-template <int NT>  // n8 token blocks: M <= 8 * NT (NT = 1, 2, 4)
+template <int NT, bool EPI>  // n8 token blocks: M <= 8 * NT (NT = 1, 2, 4); EPI: bias / activation epilogue
 __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma_kernel(
     const uint16_t* __restrict__ X, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
     const uint8_t* __restrict__ zeros, uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K, int stages_per_split,
-    int splits, int* err) {
+    int splits, int* err, Epi epi) {
   using C = MmaCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -192,6 +193,18 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   grid_dep_launch();
 
   const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
+  // bias of this thread's output rows (direct path), loaded now and used at the end
+  float bias_r[kMmaRowBlocks][2] = {};
+  if constexpr (EPI) {
+    if (splits == 1 && warp < kMmaConsumers) {
+#pragma unroll
+      for (int rb = 0; rb < kMmaRowBlocks; ++rb)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+          bias_r[rb][hr] =
+              epi_bias(epi, static_cast<int64_t>(nt) * kTileN + warp * 16 * kMmaRowBlocks + 16 * rb + gq + hr * 8);
+    }
+  }
   float acc[kMmaRowBlocks][NT][4];
 #pragma unroll
   for (int rb = 0; rb < kMmaRowBlocks; ++rb)
@@ -410,12 +423,18 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int64_t n = static_cast<int64_t>(nt) * kTileN + warp * 16 * kMmaRowBlocks + 16 * rb + gq + hr * 8;
+          float o[2 * NT];  // tokens 8j + 2tq + e of row n
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) o[2 * j + e] = acc[rb][j][hr * 2 + e];
+          if constexpr (EPI) epi_run(epi.act, o, bias_r[rb][hr]);
 #pragma unroll
           for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int64_t m = j * 8 + 2 * tq + e;
-              if (m < M) Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[rb][j][hr * 2 + e]));
+              if (m < M) Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o[2 * j + e]));
             }
         }
     }
@@ -460,12 +479,13 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     const float* src = red + rl * C::kTok + slot;
     float v = 0.0f;
     for (int p = 0; p < splits; ++p) v += src[p * rstride * C::kTok];
-    Y[static_cast<int64_t>(m) * N + static_cast<int64_t>(nt) * kTileN + r_lo + rl] =
-        __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    const int64_t n = static_cast<int64_t>(nt) * kTileN + r_lo + rl;
+    if constexpr (EPI) v = epi_apply(epi, v, n);
+    Y[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   }
 }
 
-// Clusters of `cs` CTAs of w4a16_mma_kernel<NT> that fit on the GPU at once
+// Clusters of `cs` CTAs of w4a16_mma_kernel<NT, *> that fit on the GPU at once
 // (cudaOccupancyMaxActiveClusters; wide clusters pack the GPCs less densely),
 // for cs = 1 .. kMmaMaxCluster, queried once per device.
 template <int NT>
@@ -478,7 +498,7 @@ static int max_active_clusters(int cs) {
   auto it = table.find(dev);
   if (it == table.end()) {
     std::array<int, kMmaMaxCluster + 1> t{};
-    if (set_smem_once(w4a16_mma_kernel<NT>, MmaCfg<NT>::kSmem, true) == cudaSuccess) {
+    if (set_smem_once(w4a16_mma_kernel<NT, false>, MmaCfg<NT>::kSmem, true) == cudaSuccess) {
       for (int c = 1; c <= kMmaMaxCluster; ++c) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(c), 1);
@@ -492,7 +512,7 @@ static int max_active_clusters(int cs) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, w4a16_mma_kernel<NT>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, w4a16_mma_kernel<NT, false>, &cfg) != cudaSuccess) n = 0;
         t[c] = n;
       }
     }
@@ -550,11 +570,11 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
 
 bool mma_path_ok(int64_t M, int64_t K) { return M >= 1 && M <= 32 && K % kMmaStageCols == 0; }
 
-template <int NT>
+template <int NT, bool EPI>
 static cudaError_t launch_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                               uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, int* err,
-                              cudaStream_t st) {
-  cudaError_t e = set_smem_once(w4a16_mma_kernel<NT>, MmaCfg<NT>::kSmem, true);
+                              cudaStream_t st, const Epi& epi) {
+  cudaError_t e = set_smem_once(w4a16_mma_kernel<NT, EPI>, MmaCfg<NT>::kSmem, true);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan.splits), static_cast<unsigned>(N / kTileN));
@@ -570,17 +590,24 @@ static cudaError_t launch_mma(const uint16_t* X, const uint8_t* codes, const uin
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, w4a16_mma_kernel<NT>, X, codes, scales, zeros, Y, M, N, K, plan.kb_per_split,
-                            plan.splits, err);
+  return cudaLaunchKernelEx(&cfg, w4a16_mma_kernel<NT, EPI>, X, codes, scales, zeros, Y, M, N, K, plan.kb_per_split,
+                            plan.splits, err, epi);
 }
 
 cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                              uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, int* err,
-                             cudaStream_t st) {
+                             cudaStream_t st, const Epi& epi) {
   (void)ws;  // the split-K reduction runs in distributed shared memory
-  if (M <= 8) return launch_mma<1>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
-  if (M <= 16) return launch_mma<2>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
-  return launch_mma<4>(X, codes, scales, zeros, Y, M, N, K, plan, err, st);
+  const bool fused = epi.bias != nullptr || epi.act != QLIN_ACT_NONE;
+  auto go = [&](auto nt, auto ep) {
+    return launch_mma<decltype(nt)::value, decltype(ep)::value>(X, codes, scales, zeros, Y, M, N, K, plan, err, st,
+                                                                 epi);
+  };
+  using F = std::false_type;
+  using T = std::true_type;
+  if (M <= 8) return fused ? go(std::integral_constant<int, 1>{}, T{}) : go(std::integral_constant<int, 1>{}, F{});
+  if (M <= 16) return fused ? go(std::integral_constant<int, 2>{}, T{}) : go(std::integral_constant<int, 2>{}, F{});
+  return fused ? go(std::integral_constant<int, 4>{}, T{}) : go(std::integral_constant<int, 4>{}, F{});
 }
 
 }  // namespace qlin

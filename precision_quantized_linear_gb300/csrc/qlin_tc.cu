@@ -112,6 +112,7 @@ struct TcArgs {
   int units;         // ntiles * mblocks * splits
   int mb_fast;       // unit order: token block fastest (weights streamed once) or weight tile fastest
   int x_keep;        // keep activation tiles in L2 (evict-last) when they are small
+  Epi epi;           // output epilogue (bias, activation); not used by block scaling
 };
 
 __device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
@@ -167,7 +168,8 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
   return r;
 }
 
-template <int BN, bool W4, int KPS, bool BS, int WN>
+// EPI: the output epilogue (bias, activation) of the *_gemm_fused calls is compiled in
+template <int BN, bool W4, int KPS, bool BS, int WN, bool EPI>
 __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ TcArgs a) {
@@ -731,6 +733,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
       }
       const Unit un = unit_of(a, u, KB);
       const int acc = ua & 1;
+      const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
+      const float bias_n = EPI ? epi_bias(a.epi, n) : 0.0f;  // loaded while the MMAs run
       // A warp whose wait gave up skips this unit's data but keeps taking part
       // in the named barriers below, so that they always see all 128 threads.
       const bool have = __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (ua >> 1) & 1, kWaitLimitNs, &s_abort));
@@ -739,7 +743,6 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
         s_abort = 1;
       }
       tc_fence_after();
-      const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
       const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
       const uint32_t tmem_d = tmem_base + acc * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const bool direct = a.splits == 1;
@@ -764,13 +767,17 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
             uint16_t* box = reinterpret_cast<uint16_t*>(epi_box + (epi_n & 1) * C::kEpiBox);
             if (t == 0) bulk_wait_read<1>();  // the store before last, from this box, has read it
             named_bar_epi();
+            float o[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int64_t m = mbase + c0 + i;
               const float x = have ? __uint_as_float(v[i]) : 0.0f;
-              box[i * kTileN + quad * 32 + lane] =  // this thread's row of the tile: TMEM lane quad * 32 + lane
-                  W4 ? to_bf16(x) : to_bf16(m < a.M ? (x * __ldg(a.sx + m)) * s_w : 0.0f);
+              o[i] = W4 ? x : (m < a.M ? (x * __ldg(a.sx + m)) * s_w : 0.0f);
             }
+            if constexpr (EPI) epi_run(a.epi.act, o, bias_n);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)  // this thread's row of the tile: TMEM lane quad * 32 + lane
+              box[i * kTileN + quad * 32 + lane] = mbase + c0 + i < a.M ? to_bf16(o[i]) : uint16_t(0);
             fence_proxy_async_smem();
             named_bar_epi();
             if (t == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(mbase + c0));
@@ -811,10 +818,18 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
                   __stcg(p + static_cast<int64_t>(i) * a.N, 0.0f);
                 }
             }
+            if constexpr (!W4) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int64_t m = mbase + c0 + i;
+                acc_v[i] = m < a.M ? (acc_v[i] * __ldg(a.sx + m)) * s_w : 0.0f;
+              }
+            }
+            if constexpr (EPI) epi_run(a.epi.act, acc_v, bias_n);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int64_t m = mbase + c0 + i;
-              if (m < a.M) a.Y[m * a.N + n] = W4 ? to_bf16(acc_v[i]) : to_bf16((acc_v[i] * __ldg(a.sx + m)) * s_w);
+              if (m < a.M) a.Y[m * a.N + n] = to_bf16(acc_v[i]);
             }
           }
           if (t == 0) a.counters[tile] = 0u;
@@ -997,11 +1012,11 @@ TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   return plan_tc(M, N, K, num_sms, 128, false, 128, wn, false);
 }
 
-template <int BN, bool W4, int KPS, bool BS = false, int WN = 128>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = false>
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
                              const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   using C = TcCfg<BN, W4, KPS, BS, WN>;
-  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN>, C::kSmemBytes);
+  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   args.counters = static_cast<uint32_t*>(ws);
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.split.tiles)) : nullptr;
@@ -1028,34 +1043,34 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS, WN>, tx, tw, ty, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI>, tx, tw, ty, args);
 }
 
-template <bool W4>
+template <bool W4, bool EPI>
 static cudaError_t launch_tc_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const TcArgs& a,
                                 const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   if constexpr (W4) {
-    if (plan.bn == 16) return plan.kps == 4 ? launch_tc<16, true, 4>(tx, tw, ty, a, plan, ws, num_sms, st)
-                                            : launch_tc<16, true, 2>(tx, tw, ty, a, plan, ws, num_sms, st);
-    if (plan.bn == 32) return plan.kps == 4 ? launch_tc<32, true, 4>(tx, tw, ty, a, plan, ws, num_sms, st)
-                                            : launch_tc<32, true, 2>(tx, tw, ty, a, plan, ws, num_sms, st);
-    if (plan.bn == 64) return launch_tc<64, true, 2>(tx, tw, ty, a, plan, ws, num_sms, st);
-    if (plan.bn == 128) return launch_tc<128, true, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
-    return launch_tc<256, true, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 16) return plan.kps == 4 ? launch_tc<16, true, 4, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st)
+                                            : launch_tc<16, true, 2, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 32) return plan.kps == 4 ? launch_tc<32, true, 4, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st)
+                                            : launch_tc<32, true, 2, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 64) return launch_tc<64, true, 2, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 128) return launch_tc<128, true, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    return launch_tc<256, true, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
   } else {
     switch (plan.bn) {
-      case 16: return launch_tc<16, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
-      case 32: return launch_tc<32, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
-      case 64: return launch_tc<64, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
-      case 128: return launch_tc<128, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
-      default: return launch_tc<256, false, 1>(tx, tw, ty, a, plan, ws, num_sms, st);
+      case 16: return launch_tc<16, false, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+      case 32: return launch_tc<32, false, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+      case 64: return launch_tc<64, false, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+      case 128: return launch_tc<128, false, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+      default: return launch_tc<256, false, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
     }
   }
 }
 
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
-                            int num_sms, cudaStream_t st) {
+                            int num_sms, cudaStream_t st, const Epi& epi) {
   CUtensorMap tx, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, K * 2, 64, plan.bn))
     return cudaErrorInvalidValue;
@@ -1070,12 +1085,14 @@ cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint1
   a.M = M;
   a.N = N;
   a.K = K;
-  return launch_tc_bn<true>(tx, tx, ty, a, plan, ws, num_sms, st);
+  a.epi = epi;
+  return (epi.bias || epi.act) ? launch_tc_bn<true, true>(tx, tx, ty, a, plan, ws, num_sms, st)
+                                : launch_tc_bn<true, false>(tx, tx, ty, a, plan, ws, num_sms, st);
 }
 
 cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                            int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
-                           cudaStream_t st) {
+                           cudaStream_t st, const Epi& epi) {
   CUtensorMap tx, tw, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, K, N, K, 128, 128)) return cudaErrorInvalidValue;
@@ -1089,7 +1106,9 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
   a.M = M;
   a.N = N;
   a.K = K;
-  return launch_tc_bn<false>(tx, tw, ty, a, plan, ws, num_sms, st);
+  a.epi = epi;
+  return (epi.bias || epi.act) ? launch_tc_bn<false, true>(tx, tw, ty, a, plan, ws, num_sms, st)
+                                : launch_tc_bn<false, false>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,

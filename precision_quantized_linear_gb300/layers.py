@@ -3,17 +3,19 @@
 ``W4A16Linear`` packs BF16 weights once at construction ([LP] S18 "pack once,
 reuse") and runs ``qlin_w4a16_gemm`` per call; ``W8A8Linear`` quantises the
 weights to E4M3 once and runs the fused per-token activation quantiser plus
-``qlin_w8a8_fp8_gemm`` per call.  Device memory comes from torch; every
+``qlin_w8a8_fp8_gemm`` per call.  A layer built with a bias, or called with an
+activation, runs the ``*_gemm_fused`` calls instead: bias and activation are
+applied where the kernel writes Y.  Device memory comes from torch; every
 computation is a libqlin kernel.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_pack_w4,
+from . import (ACT_NONE, OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_pack_w4,
                qlin_quant_act_fp8, qlin_quant_act_fp8_blocks, qlin_quant_w_fp8, qlin_quant_w_fp8_blocks,
-               qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w8a8_fp8_block_gemm, qlin_w8a8_fp8_gemm_ex,
-               qlin_workspace_size)
+               qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w4a16_gemm_fused, qlin_w8a8_fp8_block_gemm,
+               qlin_w8a8_fp8_gemm_ex, qlin_w8a8_fp8_gemm_fused, qlin_workspace_size)
 
 
 def _as_u16(t: torch.Tensor) -> torch.Tensor:
@@ -38,10 +40,18 @@ class Workspace:
         return self.buf, self.buf.numel()
 
 
+def _bias_bf16(bias, N):
+    if bias is None:
+        return None
+    assert bias.shape == (N,) and bias.dtype == torch.bfloat16
+    return bias.contiguous()
+
+
 class W4A16Linear:
-    def __init__(self, W_bf16: torch.Tensor, G: int = 128, symmetric: bool = False, stream=None):
+    def __init__(self, W_bf16: torch.Tensor, G: int = 128, symmetric: bool = False, stream=None, bias=None):
         N, K = W_bf16.shape
         self.N, self.K, self.G = N, K, G
+        self.bias = _bias_bf16(bias, N)
         dev = W_bf16.device
         nc, ns, nz = qlin_w4_packed_sizes(N, K, G)
         self.codes = torch.empty(nc, dtype=torch.uint8, device=dev)
@@ -54,20 +64,26 @@ class W4A16Linear:
     def packed_bytes(self) -> int:
         return self.codes.numel() + 2 * self.scales.numel() + self.zeros.numel()
 
-    def __call__(self, X_bf16: torch.Tensor, Y: torch.Tensor = None, path: int = PATH_AUTO, stream=None):
+    def __call__(self, X_bf16: torch.Tensor, Y: torch.Tensor = None, path: int = PATH_AUTO, stream=None,
+                 act: int = ACT_NONE):
         M = X_bf16.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=X_bf16.device)
         buf, nb = self.ws.get(qlin_workspace_size(OP_W4A16_GEMM, M, self.N, self.K))
-        qlin_w4a16_gemm_ex(_as_u16(X_bf16), self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N,
-                           self.K, self.G, buf, nb, path, stream)
+        if self.bias is None and act == ACT_NONE:
+            qlin_w4a16_gemm_ex(_as_u16(X_bf16), self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N,
+                               self.K, self.G, buf, nb, path, stream)
+        else:
+            qlin_w4a16_gemm_fused(_as_u16(X_bf16), self.codes, self.scales, self.zeros, Y.view(torch.int16), M,
+                                  self.N, self.K, self.G, self.bias, act, buf, nb, path, stream)
         return Y
 
 
 class W8A8Linear:
-    def __init__(self, W_bf16: torch.Tensor, stream=None):
+    def __init__(self, W_bf16: torch.Tensor, stream=None, bias=None):
         N, K = W_bf16.shape
         self.N, self.K = N, K
+        self.bias = _bias_bf16(bias, N)
         dev = W_bf16.device
         self.Wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
         self.sw = torch.empty(1, dtype=torch.float32, device=dev)
@@ -85,18 +101,22 @@ class W8A8Linear:
         qlin_quant_act_fp8(_as_u16(X_bf16), M, K, Xq, sx, stream)
         return Xq, sx
 
-    def gemm(self, Xq, sx, Y=None, path: int = PATH_AUTO, stream=None):
+    def gemm(self, Xq, sx, Y=None, path: int = PATH_AUTO, stream=None, act: int = ACT_NONE):
         M = Xq.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
         buf, nb = self.ws.get(qlin_workspace_size(OP_W8A8_GEMM, M, self.N, self.K))
-        qlin_w8a8_fp8_gemm_ex(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, buf, nb, path,
-                              stream)
+        if self.bias is None and act == ACT_NONE:
+            qlin_w8a8_fp8_gemm_ex(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, buf, nb, path,
+                                  stream)
+        else:
+            qlin_w8a8_fp8_gemm_fused(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, self.bias,
+                                     act, buf, nb, path, stream)
         return Y
 
-    def __call__(self, X_bf16, Y=None, path: int = PATH_AUTO, stream=None):
+    def __call__(self, X_bf16, Y=None, path: int = PATH_AUTO, stream=None, act: int = ACT_NONE):
         Xq, sx = self.quant_act(X_bf16, stream=stream)
-        return self.gemm(Xq, sx, Y, path, stream)
+        return self.gemm(Xq, sx, Y, path, stream, act)
 
 
 class W8A8BlockLinear:

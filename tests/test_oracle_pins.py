@@ -502,3 +502,43 @@ def test_block_scaling_confines_an_outlier():
     flushed_blk = ((qb[:, 128:] & 0x7F) == 0) & nonzero
     assert flushed_tok.sum() > 0
     assert flushed_blk.sum() == 0
+
+
+# ---- fused epilogue ([LP] S23 / S24): act(Y + bias[n])
+
+def test_epilogue_activations_at_closed_form_points():
+    ln3 = math.log(3.0)  # sigmoid(ln 3) = 3/4 exactly
+    z975 = 1.959963984540054  # the standard normal 0.975 quantile: Phi(z) = 0.975
+    v = np.array([[ln3, -ln3, z975, -z975, 1.0, 0.0, 40.0, -40.0, 2.5, -2.5]])
+    silu = oracle.epilogue(v, None, oracle.ACT_SILU)[0]
+    gelu = oracle.epilogue(v, None, oracle.ACT_GELU)[0]
+    relu = oracle.epilogue(v, None, oracle.ACT_RELU)[0]
+    assert silu[0] == pytest.approx(0.75 * ln3, rel=1e-15) and silu[1] == pytest.approx(-0.25 * ln3, rel=1e-15)
+    assert gelu[2] == pytest.approx(0.975 * z975, rel=1e-14) and gelu[3] == pytest.approx(-0.025 * z975, rel=1e-12)
+    assert gelu[4] == pytest.approx(0.8413447460685429, rel=1e-15)  # Phi(1) from the normal table
+    assert silu[5] == 0.0 and gelu[5] == 0.0 and relu[5] == 0.0
+    assert silu[6] == pytest.approx(40.0, rel=1e-15) and abs(silu[7]) < 1e-15
+    assert list(relu) == [ln3, 0.0, z975, 0.0, 1.0, 0.0, 40.0, 0.0, 2.5, 0.0]
+    np.testing.assert_array_equal(oracle.epilogue(v, None, oracle.ACT_NONE), v)
+
+
+def test_epilogue_odd_part_identities():
+    # x sigmoid(x) - (-x) sigmoid(-x) = x and x Phi(x) - (-x) Phi(-x) = x for every x
+    v = np.random.default_rng(3).normal(0.0, 3.0, (4, 64))
+    for act in (oracle.ACT_SILU, oracle.ACT_GELU):
+        d = oracle.epilogue(v, None, act) - oracle.epilogue(-v, None, act)
+        np.testing.assert_allclose(d, v, rtol=0, atol=1e-12)
+
+
+def test_epilogue_bias_is_per_output_column_and_precedes_the_activation():
+    # [X, 1] . [W, b]^T = X W^T + b: the library matmul on augmented operands
+    X = syn.make_act(5, 256, seed=21)
+    W = syn.make_weight(128, 256, seed=22)
+    wq = oracle.quantize_w4(W)
+    bias = syn.make_act(1, 128, seed=23)[0]
+    Y = oracle.epilogue(oracle.w4a16_full(X, wq), bias, oracle.ACT_NONE)
+    xa = np.hstack([syn.bf16_bits_to_f32(X).astype(np.float64), np.ones((5, 1))])
+    wa = np.hstack([oracle.dequant_w4(wq), syn.bf16_bits_to_f32(bias).astype(np.float64)[:, None]])
+    np.testing.assert_allclose(Y, xa @ wa.T, rtol=1e-12, atol=1e-12)
+    two = np.array([0x4000], np.uint16)  # BF16 2.0
+    assert oracle.epilogue(np.array([[-1.0]]), two, oracle.ACT_RELU)[0, 0] == 1.0  # relu(-1 + 2), not relu(-1) + 2
