@@ -14,7 +14,7 @@ steps, K timed steps.  Under torchrun every rank runs the same workload on
 its own GPU (replicas, weak scaling) and the slowest rank's time is used.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
-    python bench.py --sweep crossover|prefill|70b   (tables, not the bench line)
+    python bench.py --sweep crossover|prefill|70b|decode|blocks|epilogue   (tables, not the bench line)
 """
 from __future__ import annotations
 
@@ -543,6 +543,9 @@ def run_sweep(args):
     elif args.sweep == "70b":
         shapes = [(8192, 10240), (8192, 8192), (8192, 57344), (28672, 8192)]
         plan = [("w4", M) for M in (1, 64, 256)] + [("w8", M) for M in (256, 4096)]
+    elif args.sweep == "epilogue":  # fused bias + SiLU / GELU beside the plain calls
+        shapes = [(4096, 4096), (4096, 28672)]
+        plan = [(v, M) for M in (1, 16, 256, 2048) for v in ("w4", "w4:silu", "w4:gelu", "w8", "w8:silu")]
     elif args.sweep == "blocks":  # FP8 block scaling beside per-tensor FP8, decode to prefill
         shapes = [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]
         plan = [(v, M) for M in (1, 16, 2048, 8192) for v in ("w8", "w8b")]
@@ -564,19 +567,26 @@ def run_sweep(args):
         sets8 = [lin8.Wq] + [lin8.Wq.clone() for _ in range(r8 - 1)]
         sets8b = ([(lin8b.Wq, lin8b.sw)] + [(lin8b.Wq.clone(), lin8b.sw.clone()) for _ in range(r8 - 1)]
                   if lin8b is not None else [])
+        bias = torch.from_numpy(syn.make_act(1, N, seed=N)[0].view(np.int16)).cuda()
         for (v, M) in plan:
+            v, _, actname = v.partition(":")
+            act = {"": q.ACT_NONE, "silu": q.ACT_SILU, "gelu": q.ACT_GELU}[actname]
             X = torch.from_numpy(syn.make_act(M, K, seed=M + 7, token_outlier_frac=0.001).view(np.int16)).cuda()
             Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
             Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
             sx = torch.empty(M, dtype=torch.float32, device="cuda")
-            row = {"K": K, "N": N, "M": M, "variant": v}
+            row = {"K": K, "N": N, "M": M, "variant": v + (":bias+" + actname if actname else "")}
             flops = 2 * M * N * K
             if v.startswith("w4"):
                 path = {"w4": q.PATH_AUTO, "w4gemv": q.PATH_GEMV, "w4tc": q.PATH_TC}[v]
                 nb = q.qlin_workspace_size(q.OP_W4A16_GEMM, M, N, K)
                 ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
-                fns = [lambda st, c=c, s=s, z=z: q.qlin_w4a16_gemm_ex(X, c, s, z, Y, M, N, K, 128, ws, ws.numel(),
-                                                                     path, st) for (c, s, z) in sets4]
+                if act == q.ACT_NONE:
+                    fns = [lambda st, c=c, s=s, z=z: q.qlin_w4a16_gemm_ex(X, c, s, z, Y, M, N, K, 128, ws, ws.numel(),
+                                                                         path, st) for (c, s, z) in sets4]
+                else:
+                    fns = [lambda st, c=c, s=s, z=z: q.qlin_w4a16_gemm_fused(X, c, s, z, Y, M, N, K, 128, bias, act, ws,
+                                                                            ws.numel(), path, st) for (c, s, z) in sets4]
                 us = time_launches(fns)
                 alg = w4_alg_bytes(M, N, K)
                 t_roof = max(flops / (p16 * 1e12), alg / (bw * 1e9)) * 1e6
@@ -605,8 +615,12 @@ def run_sweep(args):
                 nb = q.qlin_workspace_size(q.OP_W8A8_GEMM, M, N, K)
                 ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
                 q.qlin_quant_act_fp8(X, M, K, Xq, sx)
-                fns = [lambda st, wq=wq: q.qlin_w8a8_fp8_gemm_ex(Xq, sx, wq, lin8.sw, Y, M, N, K, ws, ws.numel(),
-                                                                 path, st) for wq in sets8]
+                if act == q.ACT_NONE:
+                    fns = [lambda st, wq=wq: q.qlin_w8a8_fp8_gemm_ex(Xq, sx, wq, lin8.sw, Y, M, N, K, ws, ws.numel(),
+                                                                     path, st) for wq in sets8]
+                else:
+                    fns = [lambda st, wq=wq: q.qlin_w8a8_fp8_gemm_fused(Xq, sx, wq, lin8.sw, Y, M, N, K, bias, act, ws,
+                                                                        ws.numel(), path, st) for wq in sets8]
                 us = time_launches(fns)
                 qus = time_launches([lambda st: q.qlin_quant_act_fp8(X, M, K, Xq, sx, st)])
                 alg = w8_alg_bytes(M, N, K)
@@ -671,7 +685,7 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sweep", default=None, choices=["crossover", "prefill", "70b", "decode", "blocks"])
+    ap.add_argument("--sweep", default=None, choices=["crossover", "prefill", "70b", "decode", "blocks", "epilogue"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None, choices=["w4a16", "w8a8", "w8a8b"])

@@ -73,7 +73,7 @@ def _load():
         lib.orc_pack_canonical.restype = None
         lib.orc_pack_canonical.argtypes = [_p, _p, _i64, _i64, ctypes.c_int, _p, _p]
         lib.orc_pack_tile.restype = None
-        lib.orc_pack_tile.argtypes = [_p, _p, _p, _i64, _i64, _p, _p, _p]
+        lib.orc_pack_tile.argtypes = [_p, _p, _p, _i64, _i64, _i64, _p, _p, _p]
         lib.orc_quant_fp8_rows.restype = None
         lib.orc_quant_fp8_rows.argtypes = [_p, _i64, _i64, _p, _p]
         lib.orc_quant_fp8_tensor.restype = None
@@ -189,13 +189,14 @@ def pack_canonical(wq: W4Quant):
 
 
 def pack_tile(wq: W4Quant):
-    """Tile layout, format version 2 (128 x 64 tiles, G = 128): codes, scales, zeros as flat arrays."""
+    """Tile layout, format version 2 (128 x 64 tiles, G = 32, 64 or 128): codes, scales, zeros as flat arrays."""
     N, K = wq.q.shape
-    assert wq.G == 128 and N % 128 == 0 and K % 128 == 0
+    G = wq.G
+    assert G in (32, 64, 128) and N % 128 == 0 and K % 128 == 0
     codes = np.empty((N * K // 2,), np.uint8)
-    scales = np.empty((N * K // 128,), np.uint16)
-    zeros = np.empty((N * K // 256,), np.uint8)
-    _load().orc_pack_tile(_ptr(wq.q), _ptr(wq.s), _ptr(wq.z), N, K,
+    scales = np.empty((N * K // G,), np.uint16)
+    zeros = np.empty((N * K // G // 2,), np.uint8)
+    _load().orc_pack_tile(_ptr(wq.q), _ptr(wq.s), _ptr(wq.z), N, K, G,
                           _ptr(codes), _ptr(scales), _ptr(zeros))
     return codes, scales, zeros
 

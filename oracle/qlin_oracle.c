@@ -257,7 +257,7 @@ void orc_pack_canonical(const uint8_t *q, const uint8_t *z, int64_t N, int64_t K
 
 /*
  * Tile layout (format version 2), restated from its written description:
- * tiles of 128 rows (n) by 64 columns (k); G must be 128.
+ * tiles of 128 rows (n) by 64 columns (k); G is 32, 64 or 128.
  *   codes : tile (nb = n/128, kb = k/64) is 4096 bytes at
  *           (nb * (K/64) + kb) * 4096; inside it, half h = (k%64)/32 and row
  *           r = n%128 own the 16 bytes at h*2048 + r*16, the 32 columns
@@ -265,13 +265,13 @@ void orc_pack_canonical(const uint8_t *q, const uint8_t *z, int64_t N, int64_t K
  *           32-bit words.  With c = 16a + 8b + 2t + e (a, b, e in {0,1},
  *           t in 0..3), column c sits in word t at nibble position
  *           p = 2a + b + 4e (bits 4p..4p+3).
- *   scales: binary16 at element (nb * (K/128) + g) * 128 + r.
- *   zeros : byte (nb * (K/128) + g) * 64 + r/2, low nibble for even r.
+ *   scales: binary16 at element (nb * (K/G) + g) * 128 + r, g = k / G.
+ *   zeros : byte (nb * (K/G) + g) * 64 + r/2, low nibble for even r.
  */
 void orc_pack_tile(const uint8_t *q, const uint16_t *s, const uint8_t *z,
-                   int64_t N, int64_t K, uint8_t *codes, uint16_t *scales, uint8_t *zeros)
+                   int64_t N, int64_t K, int64_t G, uint8_t *codes, uint16_t *scales, uint8_t *zeros)
 {
-    int64_t ng = K / 128;
+    int64_t ng = K / G;
     memset(codes, 0, (size_t)(N * K / 2));
     memset(zeros, 0, (size_t)(N * ng / 2));
     for (int64_t n = 0; n < N; n++) {

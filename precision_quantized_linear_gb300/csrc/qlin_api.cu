@@ -144,6 +144,9 @@ int cuda_status(cudaError_t e) {
 
 static int launch_status(cudaError_t e) { return cuda_status(e); }
 
+// W4A16 quantisation groups the kernels take ([LP] S4 per-group, S5 b_eff = 4 + 16 / G)
+static bool group_ok(int G) { return G == 32 || G == 64 || G == 128; }
+
 // Validated output epilogue of the *_fused calls.
 static int make_epi(const void* bias_bf16, int act, Epi* epi) {
   if (act < QLIN_ACT_NONE || act > QLIN_ACT_GELU) return QLIN_ERR_INVALID_VALUE;
@@ -179,7 +182,7 @@ int qlin_gemv_max_m(int op) { return op == QLIN_OP_W8A8_GEMM ? g_gemv_max_m_w8 :
 
 int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros) {
   if (!codes || !scales || !zeros) return QLIN_ERR_INVALID_VALUE;
-  if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   int st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   *codes = static_cast<size_t>(N * K / 2);
@@ -219,7 +222,7 @@ int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes) 
 
 int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes, void* scales_f16,
                  void* zeros_u4, void* stream) {
-  if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   int st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   if (symmetric != 0 && symmetric != 1) return QLIN_ERR_INVALID_VALUE;
@@ -229,7 +232,7 @@ int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric,
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != QLIN_OK) return st;
-  return launch_status(launch_pack_w4(static_cast<const uint16_t*>(W_bf16), N, K, symmetric,
+  return launch_status(launch_pack_w4(static_cast<const uint16_t*>(W_bf16), N, K, G, symmetric,
                                       static_cast<uint8_t*>(codes), static_cast<uint16_t*>(scales_f16),
                                       static_cast<uint8_t*>(zeros_u4), d->err, d->num_sms,
                                       static_cast<cudaStream_t>(stream)));
@@ -238,7 +241,7 @@ int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric,
 static int w4a16_impl(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                       void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const Epi& epi, void* workspace,
                       size_t ws_bytes, int path, void* stream) {
-  if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   int st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;
@@ -259,17 +262,18 @@ static int w4a16_impl(const void* X_bf16, const void* codes, const void* scales_
   auto cs = static_cast<cudaStream_t>(stream);
   if (path == QLIN_PATH_GEMV) {
     if (mma_path_ok(M, K)) {
-      const SplitPlan p = plan_w4a16_mma(M, N, K, d->num_sms);
+      const SplitPlan p = plan_w4a16_mma(M, N, K, d->num_sms, G);
       if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-      return launch_status(launch_w4a16_mma(X, c, s, z, Y, M, N, K, p, workspace, d->err, cs, epi));
+      return launch_status(launch_w4a16_mma(X, c, s, z, Y, M, N, K, G, p, workspace, d->err, cs, epi));
     }
+    if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;  // the CUDA-core GEMV takes G = 128 only
     const SplitPlan p = plan_w4a16_gemv(M, N, K, d->num_sms);
     if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
     return launch_status(launch_w4a16_gemv(X, c, s, z, Y, M, N, K, p, workspace, cs, epi));
   }
   const TcPlan p = plan_w4a16_tc(M, N, K, d->num_sms);
   if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, p, workspace, d->err, d->num_sms, cs, epi));
+  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, G, p, workspace, d->err, d->num_sms, cs, epi));
 }
 
 int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,

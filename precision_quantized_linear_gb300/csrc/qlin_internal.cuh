@@ -97,7 +97,7 @@ inline cudaError_t set_smem_once(F* kernel, int bytes, bool wide_clusters = fals
 inline size_t counters_bytes(int64_t tiles) { return static_cast<size_t>((tiles * 4 + 255) / 256 * 256); }
 
 // ---- launchers (return cudaError_t of the launch)
-cudaError_t launch_pack_w4(const uint16_t* W, int64_t N, int64_t K, int symmetric, uint8_t* codes,
+cudaError_t launch_pack_w4(const uint16_t* W, int64_t N, int64_t K, int G, int symmetric, uint8_t* codes,
                            uint16_t* scales, uint8_t* zeros, int* err, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_act_fp8(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx,
                                  cudaStream_t st);
@@ -112,10 +112,10 @@ cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uin
 // W4A16 small-M kernel with register-level dequantisation feeding mma.sync
 // (M <= 32, K % 256 == 0); kb_per_split counts 256-column stages.
 bool mma_path_ok(int64_t M, int64_t K);
-SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms);
+SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms, int G = 128);
 cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
-                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, int* err,
-                             cudaStream_t st, const Epi& epi = Epi{});
+                             uint16_t* Y, int64_t M, int64_t N, int64_t K, int G, const SplitPlan& plan, void* ws,
+                             int* err, cudaStream_t st, const Epi& epi = Epi{});
 
 SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
@@ -135,8 +135,8 @@ TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
-                            uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
-                            int num_sms, cudaStream_t st, const Epi& epi = Epi{});
+                            uint16_t* Y, int64_t M, int64_t N, int64_t K, int G, const TcPlan& plan, void* ws,
+                            int* err, int num_sms, cudaStream_t st, const Epi& epi = Epi{});
 cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                            int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
                            cudaStream_t st, const Epi& epi = Epi{});

@@ -40,8 +40,7 @@ namespace qlin {
 
 constexpr int kMmaStageCols = 256;                 // K columns per stage (4 code tiles)
 constexpr int kMmaCodeBytes = 4 * 4096;            // codes of one stage
-constexpr int kMmaMetaOff = kMmaCodeBytes;         // 2 groups x 128 FP16 scales, then 2 x 64 B zeros
-constexpr int kMmaXOff = kMmaCodeBytes + 1024;     // activation rows
+constexpr int kMmaMetaOff = kMmaCodeBytes;         // group scales (128 FP16 each), then zeros (64 B each)
 constexpr int kMmaXRow = kMmaStageCols * 2 + 16;   // 528 B per token row (conflict-free B fragments)
 constexpr int kMmaRowBlocks = 2;                   // m16 row blocks per consumer warp
 constexpr int kMmaConsumers = kTileN / (16 * kMmaRowBlocks);  // consumer warps, 32 rows each
@@ -52,11 +51,14 @@ constexpr uint64_t kMmaWaitNs = 2000000000ull;
 constexpr int kMmaMaxCluster = 16;                 // CTAs of one tile's split-K cluster (non-portable above 8)
 constexpr int kMmaRedRows = 144;                   // >= splits x ceil(128 / splits) for splits <= 16
 
-template <int NT>
+template <int NT, int G = 128>
 struct MmaCfg {
   static constexpr int kTok = 8 * NT;
-  static constexpr int kSumOff = kMmaXOff + kTok * kMmaXRow;  // FP32 activation sums [2 groups][kTok tokens]
-  static constexpr int kStage = ((kSumOff + 2 * kTok * 4) + 1023) / 1024 * 1024;
+  static constexpr int kGps = kMmaStageCols / G;  // quantisation groups per stage
+  static constexpr int kZeroOff = kMmaMetaOff + kGps * 256;
+  static constexpr int kXOff = kMmaCodeBytes + (kGps * 320 + 1023) / 1024 * 1024;  // activation rows
+  static constexpr int kSumOff = kXOff + kTok * kMmaXRow;  // FP32 activation sums [kGps groups][kTok tokens]
+  static constexpr int kStage = ((kSumOff + kGps * kTok * 4) + 1023) / 1024 * 1024;
   // three CTAs fit per SM for M <= 8, two up to 32 (a ring of two stages at 32 tokens)
   static constexpr int kStages = NT == 4 ? 2 : 3;
   // split-K receive buffer: [source rank][row within the owner's slice][token
@@ -110,12 +112,14 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   return v;
 }
 
-template <int NT, bool EPI>  // n8 token blocks: M <= 8 * NT (NT = 1, 2, 4); EPI: bias / activation epilogue
+// NT: n8 token blocks, M <= 8 * NT (NT = 1, 2, 4); EPI: bias / activation
+// epilogue; G: quantisation group (32, 64, 128 columns)
+template <int NT, bool EPI, int G>
 __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma_kernel(
     const uint16_t* __restrict__ X, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
     const uint8_t* __restrict__ zeros, uint16_t* __restrict__ Y, int64_t M, int64_t N, int64_t K, int stages_per_split,
     int splits, int* err, Epi epi) {
-  using C = MmaCfg<NT>;
+  using C = MmaCfg<NT, G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kStages * C::kStage);
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   const int s0 = split * stages_per_split;
   const int nst = static_cast<int>(imin64(KS, s0 + stages_per_split)) - s0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ngK = K / kGroup;
+  const int64_t ngK = K / G;
   const int64_t KB = K / kTileK;
   const int mrows = static_cast<int>(imin64(M, C::kTok));
 
@@ -147,22 +151,22 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   // 8+2tq, 9+2tq); groups whose first token is >= M are all zero and not sent
   const int groups = NT == 1 ? (mrows + 1) / 2 : 4;
 
-  const uint32_t tx = kMmaCodeBytes + 2 * 256 + 2 * 64 + mrows * kMmaStageCols * 2;
+  const uint32_t tx = kMmaCodeBytes + C::kGps * 320 + mrows * kMmaStageCols * 2;
   auto issue_w = [&](int i) {  // weights of stage i (ring slot i % C::kStages)
     uint8_t* st = ring + (i % C::kStages) * C::kStage;
     uint64_t* bar = &full[i % C::kStages];
     const int64_t kb = static_cast<int64_t>(s0 + i) * 4;  // first 64-column block
-    const int64_t g0 = kb / 2;
+    const int64_t g0 = kb * 64 / G;  // first group
     mbar_arrive_expect_tx(bar, tx);
     bulk_load(st, codes + (static_cast<int64_t>(nt) * KB + kb) * 4096, kMmaCodeBytes, bar);
-    bulk_load(st + kMmaMetaOff, scales + (static_cast<int64_t>(nt) * ngK + g0) * kTileN, 2 * 256, bar);
-    bulk_load(st + kMmaMetaOff + 512, zeros + (static_cast<int64_t>(nt) * ngK + g0) * (kTileN / 2), 2 * 64, bar);
+    bulk_load(st + kMmaMetaOff, scales + (static_cast<int64_t>(nt) * ngK + g0) * kTileN, C::kGps * 256, bar);
+    bulk_load(st + C::kZeroOff, zeros + (static_cast<int64_t>(nt) * ngK + g0) * (kTileN / 2), C::kGps * 64, bar);
   };
   auto issue_x = [&](int i) {  // activation rows of stage i
     uint8_t* st = ring + (i % C::kStages) * C::kStage;
     const int64_t k0 = static_cast<int64_t>(s0 + i) * kMmaStageCols;
     for (int m = 0; m < mrows; ++m)
-      bulk_load(st + kMmaXOff + m * kMmaXRow, X + m * K + k0, kMmaStageCols * 2, &full[i % C::kStages]);
+      bulk_load(st + C::kXOff + m * kMmaXRow, X + m * K + k0, kMmaStageCols * 2, &full[i % C::kStages]);
   };
   if (warp == kMmaProducer && lane == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     const int per = (C::kTok - mrows) * (kMmaXRow / 16);
     const int stg = idx / per, rem = idx % per;
     const int row = mrows + rem / (kMmaXRow / 16), c16 = rem % (kMmaXRow / 16);
-    *reinterpret_cast<uint4*>(ring + stg * C::kStage + kMmaXOff + row * kMmaXRow + c16 * 16) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(ring + stg * C::kStage + C::kXOff + row * kMmaXRow + c16 * 16) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   if (splits > 1) cluster_arrive_relaxed();  // waited for before the first access to another CTA
@@ -244,13 +248,13 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
       const uint32_t st = smem_u32(ring + slot * C::kStage);
       float* sums = reinterpret_cast<float*>(ring + slot * C::kStage + C::kSumOff);  // [group][kTok tokens]
 #pragma unroll
-      for (int grp = 0; grp < 2; ++grp) {
-        float cs[2][4];  // two chains of four k-steps
+      for (int grp = 0; grp < C::kGps; ++grp) {
+        float cs[2][4];  // two chains of G / 32 k-steps
         if constexpr (NT == 1) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < G / 32; ++q) {
             uint32_t bb[2][2];
-            ldsm_b2(st + kMmaXOff + (lane & 7) * kMmaXRow + (grp * 128 + q * 32 + (lane >> 3) * 8) * 2, bb);
+            ldsm_b2(st + C::kXOff + (lane & 7) * kMmaXRow + (grp * G + q * 32 + (lane >> 3) * 8) * 2, bb);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (q == 0)
@@ -266,14 +270,14 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
 #pragma unroll
           for (int tb = 0; tb < NT / 2; ++tb) {  // 16 tokens per block
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+            for (int ks = 0; ks < G / 16; ++ks) {
               // A fragment of tokens 16tb .. 16tb+15 x columns 16ks..16ks+15: lanes
               // 0-15 address token rows (lane & 15) at column 16ks, lanes 16-31 at 16ks + 8
               uint32_t a[4];
               asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                            : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
-                           : "r"(st + kMmaXOff + (tb * 16 + (lane & 15)) * kMmaXRow +
-                                 (grp * 128 + ks * 16 + (lane >> 4) * 8) * 2));
+                           : "r"(st + C::kXOff + (tb * 16 + (lane & 15)) * kMmaXRow +
+                                 (grp * G + ks * 16 + (lane >> 4) * 8) * 2));
               if (ks < 2)
                 mma_bf16_16816_z(cs[ks & 1], a, ones[0], ones[1]);
               else
@@ -312,8 +316,8 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
         break;
       }
       const uint32_t st = smem_u32(ring + slot * C::kStage);  // shared-space address of the stage
-      const uint32_t sc = st + kMmaMetaOff;                   // FP16 scales [2][128]
-      const uint32_t zp = st + kMmaMetaOff + 512;             // zero nibbles [2][64]
+      const uint32_t sc = st + kMmaMetaOff;                   // FP16 scales [kGps][128]
+      const uint32_t zp = st + C::kZeroOff;                   // zero nibbles [kGps][64]
       // word t (this lane's) of the records of each of this thread's rows in both
       // halves of a 64-column tile: w[rb][2h + e] = half h, row rr(rb) + 8e.  Each
       // tile's words are loaded one tile ahead to hide the shared-memory latency.
@@ -330,15 +334,44 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
       };
       load_codes(0, cw);
       bool sums_ok = true;
+      // Groups: G = 128 spans two 64-column tiles (one MMA chain per tile up to
+      // 16 tokens, summed at the fold), G = 64 one tile, G = 32 one half of a
+      // tile (two k-steps).  The fold of group g:
+      //   y += s (sum x (128 + q) - (128 + z) sum x); tokens 8j+2t, +1
+      constexpr int kTpg = G >= 64 ? G / 64 : 1;      // tiles per outer step
+      constexpr int kCh = G == 128 ? C::kChains : 1;  // MMA chains per group
+      auto fold = [&](int g, const float (&cc)[kCh][kMmaRowBlocks][NT][4]) {
+        if (g == 0)
+          sums_ok = __all_sync(0xffffffffu, mbar_wait(&summed[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort));
+        float2 xv[NT];
 #pragma unroll
-      for (int grp = 0; grp < 2; ++grp) {
-        // accumulators per row block and token block: one chain per 64-column
-        // tile (kChains = 2) or one for the group
-        float c[C::kChains][kMmaRowBlocks][NT][4];
+        for (int j = 0; j < NT; ++j) xv[j] = lds64f(st + C::kSumOff + (g * C::kTok + j * 8 + 2 * tq) * 4);
 #pragma unroll
-        for (int kb2 = 0; kb2 < 2; ++kb2) {
-          const int kbl = grp * 2 + kb2;  // 64-column tile within the stage
-          const int ch = C::kChains == 2 ? kb2 : 0;
+        for (int rb = 0; rb < kMmaRowBlocks; ++rb)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int r = rr(rb) + hr * 8;
+            const float s =
+                __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(sc + (g * kTileN + r) * 2))));
+            const uint32_t zb = lds8(zp + g * (kTileN / 2) + r / 2);
+            const float cz = __uint_as_float(((zb << zsh) & 0x000F0000u) | 0x43000000u);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              const float c0 = kCh == 2 ? cc[0][rb][j][hr * 2] + cc[kCh - 1][rb][j][hr * 2] : cc[0][rb][j][hr * 2];
+              const float c1 =
+                  kCh == 2 ? cc[0][rb][j][hr * 2 + 1] + cc[kCh - 1][rb][j][hr * 2 + 1] : cc[0][rb][j][hr * 2 + 1];
+              acc[rb][j][hr * 2] = fmaf(s, fmaf(-cz, xv[j].x, c0), acc[rb][j][hr * 2]);
+              acc[rb][j][hr * 2 + 1] = fmaf(s, fmaf(-cz, xv[j].y, c1), acc[rb][j][hr * 2 + 1]);
+            }
+          }
+      };
+#pragma unroll
+      for (int ob = 0; ob < 4 / kTpg; ++ob) {
+        float c[kCh][kMmaRowBlocks][NT][4];
+#pragma unroll
+        for (int kb2 = 0; kb2 < kTpg; ++kb2) {
+          const int kbl = ob * kTpg + kb2;  // 64-column tile within the stage
+          const int ch = kCh == 2 ? kb2 : 0;
           uint32_t cur[kMmaRowBlocks][4];
 #pragma unroll
           for (int rb = 0; rb < kMmaRowBlocks; ++rb)
@@ -357,10 +390,12 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
               for (int hb = 0; hb < kBH; ++hb)
 #pragma unroll
                 for (int j = 0; j < NT; ++j)
-                  ldsm_b2(st + kMmaXOff + (j * 8 + (lane & 7)) * kMmaXRow +
+                  ldsm_b2(st + C::kXOff + (j * 8 + (lane & 7)) * kMmaXRow +
                               (kbl * 64 + (h + hb) * 32 + (lane >> 3) * 8) * 2,
                           b[hb][j]);
             }
+            // the chain starts from zero at the first k-step of its group (or tile)
+            const bool start = G == 32 ? (ks & 1) == 0 : (ks == 0 && (kCh == 2 || kb2 == 0));
 #pragma unroll
             for (int rb = 0; rb < kMmaRowBlocks; ++rb) {
               uint32_t a[4];
@@ -371,38 +406,16 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
 #pragma unroll
               for (int j = 0; j < NT; ++j) {
                 const uint32_t(&bk)[2] = b[kBH == 2 ? h : 0][j][ks & 1];
-                if (ks == 0 && (C::kChains == 2 || kb2 == 0))  // the chain starts from zero
+                if (start)
                   mma_bf16_16816_z(c[ch][rb][j], a, bk[0], bk[1]);
                 else
                   mma_bf16_16816(c[ch][rb][j], a, bk[0], bk[1]);
               }
             }
+            if (G == 32 && (ks & 1)) fold(kbl * 2 + h, c);  // end of a 32-column group
           }
         }
-        // fold: y += s (sum x (128 + q) - (128 + z) sum x); tokens 8j+2t, +1
-        if (grp == 0)
-          sums_ok = __all_sync(0xffffffffu, mbar_wait(&summed[slot], (i / C::kStages) & 1, kMmaWaitNs, &s_abort));
-        float2 xv[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) xv[j] = lds64f(st + C::kSumOff + (grp * C::kTok + j * 8 + 2 * tq) * 4);
-#pragma unroll
-        for (int rb = 0; rb < kMmaRowBlocks; ++rb)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int r = rr(rb) + hr * 8;
-            const float s =
-                __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(sc + (grp * kTileN + r) * 2))));
-            const uint32_t zb = lds8(zp + grp * (kTileN / 2) + r / 2);
-            const float cz = __uint_as_float(((zb << zsh) & 0x000F0000u) | 0x43000000u);
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              const float c0 = C::kChains == 2 ? c[0][rb][j][hr * 2] + c[C::kChains - 1][rb][j][hr * 2] : c[0][rb][j][hr * 2];
-              const float c1 = C::kChains == 2 ? c[0][rb][j][hr * 2 + 1] + c[C::kChains - 1][rb][j][hr * 2 + 1]
-                                               : c[0][rb][j][hr * 2 + 1];
-              acc[rb][j][hr * 2] = fmaf(s, fmaf(-cz, xv[j].x, c0), acc[rb][j][hr * 2]);
-              acc[rb][j][hr * 2 + 1] = fmaf(s, fmaf(-cz, xv[j].y, c1), acc[rb][j][hr * 2 + 1]);
-            }
-          }
+        if (G >= 64) fold(ob, c);
       }
       if (!sums_ok) {
         set_error(err, QLIN_ERR_TIMEOUT);
@@ -485,10 +498,10 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   }
 }
 
-// Clusters of `cs` CTAs of w4a16_mma_kernel<NT, *> that fit on the GPU at once
-// (cudaOccupancyMaxActiveClusters; wide clusters pack the GPCs less densely),
-// for cs = 1 .. kMmaMaxCluster, queried once per device.
-template <int NT>
+// Clusters of `cs` CTAs of w4a16_mma_kernel<NT, *, G> that fit on the GPU at
+// once (cudaOccupancyMaxActiveClusters; wide clusters pack the GPCs less
+// densely), for cs = 1 .. kMmaMaxCluster, queried once per device.
+template <int NT, int G>
 static int max_active_clusters(int cs) {
   static std::mutex mu;
   static std::unordered_map<int, std::array<int, kMmaMaxCluster + 1>> table;  // device -> count per size
@@ -498,12 +511,12 @@ static int max_active_clusters(int cs) {
   auto it = table.find(dev);
   if (it == table.end()) {
     std::array<int, kMmaMaxCluster + 1> t{};
-    if (set_smem_once(w4a16_mma_kernel<NT, false>, MmaCfg<NT>::kSmem, true) == cudaSuccess) {
+    if (set_smem_once(w4a16_mma_kernel<NT, false, G>, MmaCfg<NT, G>::kSmem, true) == cudaSuccess) {
       for (int c = 1; c <= kMmaMaxCluster; ++c) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(c), 1);
         cfg.blockDim = dim3(kMmaThreads);
-        cfg.dynamicSmemBytes = MmaCfg<NT>::kSmem;
+        cfg.dynamicSmemBytes = MmaCfg<NT, G>::kSmem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(c);
@@ -512,7 +525,7 @@ static int max_active_clusters(int cs) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, w4a16_mma_kernel<NT, false>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, w4a16_mma_kernel<NT, false, G>, &cfg) != cudaSuccess) n = 0;
         t[c] = n;
       }
     }
@@ -529,7 +542,13 @@ static int max_active_clusters(int cs) {
 // keep enough bytes in flight (each has at most a ring of stages in flight for
 // a loaded memory latency).  Fewer splits on a near tie.  The split-K sums
 // never leave the GPC: no workspace.
-SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
+template <int G>
+static int active_clusters(int ntb, int cs) {
+  return ntb == 1 ? max_active_clusters<1, G>(cs) : ntb == 2 ? max_active_clusters<2, G>(cs)
+                                                               : max_active_clusters<4, G>(cs);
+}
+
+SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms, int G) {
   (void)num_sms;  // the cluster occupancy table already counts the SMs
   SplitPlan p;
   const int64_t tiles = N / kTileN;
@@ -537,7 +556,7 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
   const int ntb = M <= 8 ? 1 : M <= 16 ? 2 : 4;  // n8 token blocks
   const double bw = 6.5e12, latency = 2.5e-6, startup = 3e-6;
   const int ring = ntb == 1 ? MmaCfg<1>::kStages : ntb == 2 ? MmaCfg<2>::kStages : MmaCfg<4>::kStages;
-  const double stage_bytes = kMmaCodeBytes + 640.0 + 2.0 * kMmaStageCols * static_cast<double>(M);
+  const double stage_bytes = kMmaCodeBytes + 320.0 * (kMmaStageCols / G) + 2.0 * kMmaStageCols * static_cast<double>(M);
   const int64_t cap = KS < kMmaMaxCluster ? KS : kMmaMaxCluster;
   int64_t best_s = 1;
   double best_t = 1e30;
@@ -546,9 +565,8 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t s = (KS + per - 1) / per;  // splits actually formed
     if (s != c) continue;
     const int cs = static_cast<int>(s);
-    const int64_t fit = ntb == 1   ? max_active_clusters<1>(cs)
-                        : ntb == 2 ? max_active_clusters<2>(cs)
-                                   : max_active_clusters<4>(cs);
+    const int64_t fit = G == 32 ? active_clusters<32>(ntb, cs) : G == 64 ? active_clusters<64>(ntb, cs)
+                                                               : active_clusters<128>(ntb, cs);
     if (fit <= 0) continue;
     const int64_t waves = (tiles + fit - 1) / fit;
     const double conc = static_cast<double>((tiles < fit ? tiles : fit) * s);  // CTAs running together
@@ -570,16 +588,16 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms) {
 
 bool mma_path_ok(int64_t M, int64_t K) { return M >= 1 && M <= 32 && K % kMmaStageCols == 0; }
 
-template <int NT, bool EPI>
+template <int NT, bool EPI, int G>
 static cudaError_t launch_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                               uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, int* err,
                               cudaStream_t st, const Epi& epi) {
-  cudaError_t e = set_smem_once(w4a16_mma_kernel<NT, EPI>, MmaCfg<NT>::kSmem, true);
+  cudaError_t e = set_smem_once(w4a16_mma_kernel<NT, EPI, G>, MmaCfg<NT, G>::kSmem, true);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan.splits), static_cast<unsigned>(N / kTileN));
   cfg.blockDim = dim3(kMmaThreads);
-  cfg.dynamicSmemBytes = MmaCfg<NT>::kSmem;
+  cfg.dynamicSmemBytes = MmaCfg<NT, G>::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -590,24 +608,28 @@ static cudaError_t launch_mma(const uint16_t* X, const uint8_t* codes, const uin
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, w4a16_mma_kernel<NT, EPI>, X, codes, scales, zeros, Y, M, N, K, plan.kb_per_split,
+  return cudaLaunchKernelEx(&cfg, w4a16_mma_kernel<NT, EPI, G>, X, codes, scales, zeros, Y, M, N, K, plan.kb_per_split,
                             plan.splits, err, epi);
 }
 
 cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
-                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, int* err,
-                             cudaStream_t st, const Epi& epi) {
+                             uint16_t* Y, int64_t M, int64_t N, int64_t K, int G, const SplitPlan& plan, void* ws,
+                             int* err, cudaStream_t st, const Epi& epi) {
   (void)ws;  // the split-K reduction runs in distributed shared memory
   const bool fused = epi.bias != nullptr || epi.act != QLIN_ACT_NONE;
-  auto go = [&](auto nt, auto ep) {
-    return launch_mma<decltype(nt)::value, decltype(ep)::value>(X, codes, scales, zeros, Y, M, N, K, plan, err, st,
-                                                                 epi);
+  auto go = [&](auto nt, auto ep, auto g) {
+    return launch_mma<decltype(nt)::value, decltype(ep)::value, decltype(g)::value>(X, codes, scales, zeros, Y, M, N,
+                                                                                      K, plan, err, st, epi);
   };
-  using F = std::false_type;
-  using T = std::true_type;
-  if (M <= 8) return fused ? go(std::integral_constant<int, 1>{}, T{}) : go(std::integral_constant<int, 1>{}, F{});
-  if (M <= 16) return fused ? go(std::integral_constant<int, 2>{}, T{}) : go(std::integral_constant<int, 2>{}, F{});
-  return fused ? go(std::integral_constant<int, 4>{}, T{}) : go(std::integral_constant<int, 4>{}, F{});
+  auto by_group = [&](auto nt, auto ep) {
+    if (G == 32) return go(nt, ep, std::integral_constant<int, 32>{});
+    if (G == 64) return go(nt, ep, std::integral_constant<int, 64>{});
+    return go(nt, ep, std::integral_constant<int, 128>{});
+  };
+  auto by_epi = [&](auto nt) { return fused ? by_group(nt, std::true_type{}) : by_group(nt, std::false_type{}); };
+  if (M <= 8) return by_epi(std::integral_constant<int, 1>{});
+  if (M <= 16) return by_epi(std::integral_constant<int, 2>{});
+  return by_epi(std::integral_constant<int, 4>{});
 }
 
 }  // namespace qlin

@@ -76,7 +76,7 @@ extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, co
   const auto* sp = static_cast<const uint16_t*>(scales_f16);
   const auto* zp = static_cast<const uint8_t*>(zeros_u4);
   auto* Yp = static_cast<uint16_t*>(Y_bf16);
-  const cudaError_t e = mma ? launch_w4a16_mma(Xp, cp, sp, zp, Yp, M, N, K, plan, ws, device_error_word(), cs)
+  const cudaError_t e = mma ? launch_w4a16_mma(Xp, cp, sp, zp, Yp, M, N, K, kGroup, plan, ws, device_error_word(), cs)
                             : launch_w4a16_gemv(Xp, cp, sp, zp, Yp, M, N, K, plan, ws, cs);
   return cuda_status(e);
 }

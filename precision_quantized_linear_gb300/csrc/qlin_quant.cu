@@ -25,6 +25,15 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+// min / max over aligned segments of `seg` lanes (seg = 8, 16 or 32)
+__device__ __forceinline__ float seg_min(float v, int seg) {
+  for (int o = seg >> 1; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float seg_max(float v, int seg) {
+  for (int o = seg >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
 
 // Packed layout (format version 2): in each 16-byte record (one row, 32
 // columns c = 16a + 8b + 2t + e of a 64-column tile) word t holds the eight
@@ -32,18 +41,21 @@ __device__ __forceinline__ float warp_max(float v) {
 // c in nibble position 2a + b + 4e.  Pair (c, c+1) is then the two halves of
 // (word >> 4(2a + b)) & 0x000F000F: one shift by a constant and one logic op.
 
-// [LP] S2-S4: one warp per (pair of rows, group of 128 columns).  Lane l owns
-// columns 4l..4l+3 of the group; the group's min/max are warp reductions.
+// [LP] S2-S4: one warp per (pair of rows, chunk of 128 columns).  Lane l owns
+// columns 4l..4l+3 of the chunk; a group of G columns (G = 32, 64, 128) is a
+// segment of G/4 lanes, and its min/max are segment reductions.
 // Lane l = 8R + u covers record R of the group (tile R/2, half R%2); its
 // columns 4u, 4u+1 go to word 2(u%2) and 4u+2, 4u+3 to word 2(u%2)+1, both at
 // nibble positions u/2 and u/2 + 4, so each word is the OR of the lanes u,
 // u^2, u^4, u^6.
 __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K,
-                                                      int symmetric, uint8_t* __restrict__ codes,
+                                                      int G, int symmetric, uint8_t* __restrict__ codes,
                                                       uint16_t* __restrict__ scales, uint8_t* __restrict__ zeros,
                                                       int* err) {
   const int lane = threadIdx.x & 31;
-  const int64_t ng = K / kGroup;
+  const int seg = G / 4;                    // lanes per group
+  const int64_t ng = K / 128;               // chunks per row
+  const int64_t ngk = K / G;                // groups per row
   const int64_t total = (N / 2) * ng;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; item < total;
@@ -64,9 +76,9 @@ __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict
         hi = fmaxf(hi, v[i]);
         amax = fmaxf(amax, fabsf(v[i]));
       }
-      lo = warp_min(lo);
-      hi = warp_max(hi);
-      amax = warp_max(amax);
+      lo = seg_min(lo, seg);
+      hi = seg_max(hi, seg);
+      amax = seg_max(amax, seg);
       const float s32 = symmetric ? __fdiv_rn(amax, 7.0f) : __fdiv_rn(hi - lo, 15.0f);
       __half s16 = __float2half_rn(s32);
       float sc = __half2float(s16);
@@ -111,21 +123,24 @@ __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict
         *reinterpret_cast<uint2*>(codes + (nb * (K / kTileK) + kb) * 4096 + h * 2048 + r * 16 + u * 8) =
             make_uint2(wa, wb);
       }
-      if (lane == 0) {
-        scales[(nb * ng + g) * kTileN + r] = __half_as_ushort(s16);
+      const int64_t gg = g * (128 / G) + lane / seg;  // group of this lane's segment
+      if (lane % seg == 0) {
+        scales[(nb * ngk + gg) * kTileN + r] = __half_as_ushort(s16);
         zbyte |= static_cast<uint32_t>(zp) << (4 * sub);
       }
     }
-    if (lane == 0) zeros[(nb * ng + g) * (kTileN / 2) + ((pair * 2) % kTileN) / 2] = static_cast<uint8_t>(zbyte);
+    if (lane % seg == 0)
+      zeros[(nb * ngk + g * (128 / G) + lane / seg) * (kTileN / 2) + ((pair * 2) % kTileN) / 2] =
+          static_cast<uint8_t>(zbyte);
   }
 }
 
-cudaError_t launch_pack_w4(const uint16_t* W, int64_t N, int64_t K, int symmetric, uint8_t* codes, uint16_t* scales,
-                           uint8_t* zeros, int* err, int num_sms, cudaStream_t st) {
-  const int64_t items = (N / 2) * (K / kGroup);
+cudaError_t launch_pack_w4(const uint16_t* W, int64_t N, int64_t K, int G, int symmetric, uint8_t* codes,
+                           uint16_t* scales, uint8_t* zeros, int* err, int num_sms, cudaStream_t st) {
+  const int64_t items = (N / 2) * (K / 128);
   const int64_t want = (items + 7) / 8;
   const int blocks = static_cast<int>(want < static_cast<int64_t>(num_sms) * 16 ? want : num_sms * 16);
-  pack_w4_kernel<<<blocks, 256, 0, st>>>(W, N, K, symmetric, codes, scales, zeros, err);
+  pack_w4_kernel<<<blocks, 256, 0, st>>>(W, N, K, G, symmetric, codes, scales, zeros, err);
   return cudaGetLastError();
 }
 

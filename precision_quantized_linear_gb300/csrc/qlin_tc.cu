@@ -40,12 +40,14 @@ struct TcCfg {
   static constexpr int kCols = W4 ? 64 : 128;                   // K columns per block
   static constexpr int kXBlk = BN * kBlkBytes;                  // token tile of one K block
   static constexpr int kWBlk = W4 ? 4096 : WN * kBlkBytes;      // packed codes / E4M3 tile of one K block
-  static constexpr int kGroupsPerStage = W4 ? (KPS >= 2 ? KPS / 2 : 1) : 0;
+  // group scales and zero-points of a stage: room for G = 32 (two groups per
+  // 64-column block); G = 64 / 128 use the front of each region
+  static constexpr int kGroupsMax = W4 ? 2 * KPS : 0;
   static constexpr int kScaleOff = KPS * kXBlk + KPS * kWBlk;   // scales, then zero-points (W4A16)
-  static constexpr int kZeroOff = kScaleOff + kGroupsPerStage * 256;
-  static constexpr int kMetaBytes = W4 ? ((kGroupsPerStage * 320 + 1023) / 1024) * 1024 : 0;
+  static constexpr int kZeroOff = kScaleOff + kGroupsMax * 256;
+  static constexpr int kMetaBytes = W4 ? ((kGroupsMax * 320 + 1023) / 1024) * 1024 : 0;
   static constexpr int kStage = KPS * kXBlk + KPS * kWBlk + kMetaBytes;
-  static constexpr int kTxBytes = KPS * kXBlk + KPS * kWBlk + kGroupsPerStage * 320;
+  static constexpr int kTxBase = KPS * kXBlk + KPS * kWBlk;    // plus 320 bytes per group loaded
   // dequantised BF16 weight tiles: in TMEM (tcgen05.st, read by the MMA as
   // its A operand) when the accumulators leave room, else in shared memory
   static constexpr bool kATmem = W4 && BN <= 128;
@@ -112,6 +114,7 @@ struct TcArgs {
   int units;         // ntiles * mblocks * splits
   int mb_fast;       // unit order: token block fastest (weights streamed once) or weight tile fastest
   int x_keep;        // keep activation tiles in L2 (evict-last) when they are small
+  int G;             // W4A16 quantisation group (32, 64, 128)
   Epi epi;           // output epilogue (bias, activation); not used by block scaling
 };
 
@@ -230,7 +233,11 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = a.x_keep ? policy_evict_last() : policy_evict_normal();
-      const int64_t ng = a.K / kGroup;
+      const int64_t ng = W4 ? a.K / a.G : 0;  // groups per weight row (W4A16)
+      // groups whose scales a stage loads: those of its KPS blocks (a G = 128
+      // group spans two blocks, so a one-block stage loads the group it is in)
+      const int gps = W4 ? (KPS * 64 >= a.G ? KPS * 64 / a.G : 1) : 0;
+      const uint32_t tx_bytes = C::kTxBase + gps * 320;
       // weights never depend on the previous kernel: the first pass over the
       // ring is filled with weight tiles before waiting for that kernel; the
       // activation tiles follow once it has finished
@@ -238,13 +245,13 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
         uint8_t* st = ring + s * C::kStage;
         const int kb = un.kb0 + j * KPS;
         if constexpr (W4) {
-          const int64_t g0 = kb / 2;
+          const int64_t g0 = static_cast<int64_t>(kb) * 64 / a.G;
           bulk_load_hint(st + KPS * C::kXBlk, a.codes + (static_cast<int64_t>(un.nt) * KB + kb) * 4096,
                          KPS * 4096, &full[s], pol_stream);
-          bulk_load(st + C::kScaleOff, a.scales + (static_cast<int64_t>(un.nt) * ng + g0) * kTileN,
-                    C::kGroupsPerStage * 256, &full[s]);
-          bulk_load(st + C::kZeroOff, a.zeros + (static_cast<int64_t>(un.nt) * ng + g0) * (kTileN / 2),
-                    C::kGroupsPerStage * 64, &full[s]);
+          bulk_load(st + C::kScaleOff, a.scales + (static_cast<int64_t>(un.nt) * ng + g0) * kTileN, gps * 256,
+                    &full[s]);
+          bulk_load(st + C::kZeroOff, a.zeros + (static_cast<int64_t>(un.nt) * ng + g0) * (kTileN / 2), gps * 64,
+                    &full[s]);
         } else {
 #pragma unroll
           for (int h = 0; h < WN / kTileN; ++h)  // one box of 128 rows per scale block
@@ -264,7 +271,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
       for (int u = blockIdx.x; u < a.units && it < C::kStages; u += gridDim.x) {
         const Unit un = unit_of(a, u, KB);
         for (int j = 0; j < un.nkb / KPS && it < C::kStages; ++j, ++it) {
-          mbar_arrive_expect_tx(&full[it], C::kTxBytes);
+          mbar_arrive_expect_tx(&full[it], tx_bytes);
           load_w(it, un, j);
         }
       }
@@ -281,7 +288,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+            mbar_arrive_expect_tx(&full[s], tx_bytes);
             load_w(s, un, j);
           }
           load_x(s, un, j);
@@ -412,7 +419,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
             const bool mine = (ait & 1) == grp;
             const int ai = ait % C::kAStages;
             uint4 c[2];
-            float scale = 0.0f, zq = 0.0f;
+            float scale[2] = {0.0f, 0.0f}, zq[2] = {0.0f, 0.0f};  // per 32-column half (they differ for G = 32)
             if (mine) {
               if (!__all_sync(0xffffffffu,
                               mbar_wait(&a_empty[ai], ((ait / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
@@ -422,24 +429,27 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
               const uint32_t sts = smem_u32(st);
               c[0] = lds128(sts + KPS * C::kXBlk + i * 4096 + r * 16);         // columns 0..31
               c[1] = lds128(sts + KPS * C::kXBlk + i * 4096 + 2048 + r * 16);  // columns 32..63
-              const int gi = (kb + i) / 2 - kb / 2;  // group of this block within the stage
-              scale = __half2float(
-                  __ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
-              const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
-              zq = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {  // group of this half within the stage
+                const int gi = ((kb + i) * 64 + h * 32) / a.G - (kb * 64) / a.G;
+                scale[h] = __half2float(
+                    __ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
+                const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
+                zq[h] = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
+              }
             }
             if (i == KPS - 1) {
               __syncwarp();
               if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
             }
             if (!mine) continue;
-            const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq);
-            const __nv_bfloat162 s2 = __float2bfloat162_rn(scale);
             if constexpr (C::kATmem) {
               // lane r of the slot holds row r: 32 columns x two BF16 = the 64 columns of the block
               tc_fence_after();
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
+                const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[h]);
+                const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[h]);
                 const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
                 uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
 #pragma unroll
@@ -460,6 +470,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
               uint8_t* arow = aring + ai * C::kAStage + r * 128;
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
+                const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[h]);
+                const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[h]);
                 const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
                 uint4 d[4];
 #pragma unroll
@@ -1069,8 +1081,8 @@ static cudaError_t launch_tc_bn(const CUtensorMap& tx, const CUtensorMap& tw, co
 }
 
 cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
-                            uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
-                            int num_sms, cudaStream_t st, const Epi& epi) {
+                            uint16_t* Y, int64_t M, int64_t N, int64_t K, int G, const TcPlan& plan, void* ws,
+                            int* err, int num_sms, cudaStream_t st, const Epi& epi) {
   CUtensorMap tx, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, K * 2, 64, plan.bn))
     return cudaErrorInvalidValue;
@@ -1080,6 +1092,7 @@ cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint1
   a.codes = codes;
   a.scales = scales;
   a.zeros = zeros;
+  a.G = G;
   a.Y = Y;
   a.err = err;
   a.M = M;

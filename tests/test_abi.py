@@ -51,9 +51,13 @@ def test_packed_sizes_give_4_125_bits(lib):
     c, s, z = q.qlin_w4_packed_sizes(4096, 14336, 128)
     assert 8 * (c + s) / (4096 * 14336) == 4.125
     assert 8 * (c + s + z) / (4096 * 14336) == 4.15625
-    with pytest.raises(q.QlinError) as e:
-        q.qlin_w4_packed_sizes(4096, 4096, 64)
-    assert e.value.status == 2
+    for G, bits in ((64, 4.25), (32, 4.5)):  # b + m / G at the other group sizes
+        c, s_, z = q.qlin_w4_packed_sizes(4096, 4096, G)
+        assert 8 * (c + s_) / (4096 * 4096) == bits and 8 * z / (4096 * 4096) == 4 / G
+    for G in (16, 48, 256):
+        with pytest.raises(q.QlinError) as e:
+            q.qlin_w4_packed_sizes(4096, 4096, G)
+        assert e.value.status == 2
 
 
 # Validation happens before any CUDA call: these return without a device.
@@ -62,7 +66,8 @@ def _w4(lib, X=16, codes=16, s=16, z=16, Y=16, M=1, N=128, K=128, G=128, ws=None
 
 
 def test_w4a16_rejects_bad_arguments(lib):
-    assert _w4(lib, G=64) == 2
+    assert _w4(lib, G=48) == 2
+    assert _w4(lib, G=256) == 2
     assert _w4(lib, N=100) == 2
     assert _w4(lib, K=192) == 2
     assert _w4(lib, M=-1) == 2
@@ -83,5 +88,5 @@ def test_fp8_and_pack_reject_bad_arguments(lib):
     assert lib.qlin_w8a8_fp8_gemm_ex(16, 16, 16, 16, 16, 1, 96, 128, None, 0, 0, None) == 2
     assert lib.qlin_w8a8_fp8_gemm_ex(16, 18, 16, 16, 16, 1, 128, 128, None, 0, 0, None) == 3
     assert lib.qlin_pack_w4(16, 128, 128, 128, 2, 16, 16, 16, None) == 1
-    assert lib.qlin_pack_w4(16, 128, 128, 32, 0, 16, 16, 16, None) == 2
+    assert lib.qlin_pack_w4(16, 128, 128, 48, 0, 16, 16, 16, None) == 2
     assert lib.qlin_quant_w_fp8(16, 128, 128, 16, 16, None, 0, None) == 1

@@ -270,10 +270,11 @@ def test_tile_pack_is_a_bijection_and_hand_positions():
             assert (byte, nib) == (4 * 4096, 0)
 
 
-def test_tile_pack_roundtrip_full():
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_tile_pack_roundtrip_full(G):
     N, K = 256, 512
     W = syn.make_weight(N, K, seed=3)
-    wq = oracle.quantize_w4(W, G=128)
+    wq = oracle.quantize_w4(W, G=G)
     codes, scales, zeros = oracle.pack_tile(wq)
     # unpack by the written description and compare with the unpacked codes
     c = codes.reshape(N // 128, K // 64, 2, 128, 4, 4)          # nb, kb, h, r, word t, byte
@@ -286,11 +287,12 @@ def test_tile_pack_roundtrip_full():
             cols[..., 16 * a + 8 * b + 2 * t + e] = nib[..., t, p]
     un = cols.transpose(0, 3, 1, 2, 4).reshape(N, K)
     assert np.array_equal(un, wq.q)
-    sc = scales.reshape(N // 128, K // 128, 128).transpose(0, 2, 1).reshape(N, K // 128)
+    ng = K // G
+    sc = scales.reshape(N // 128, ng, 128).transpose(0, 2, 1).reshape(N, ng)
     assert np.array_equal(sc, wq.s)
-    zz = zeros.reshape(N // 128, K // 128, 64)
-    zz = np.stack([zz & 15, zz >> 4], axis=-1).reshape(N // 128, K // 128, 128)
-    assert np.array_equal(zz.transpose(0, 2, 1).reshape(N, K // 128), wq.z)
+    zz = zeros.reshape(N // 128, ng, 64)
+    zz = np.stack([zz & 15, zz >> 4], axis=-1).reshape(N // 128, ng, 128)
+    assert np.array_equal(zz.transpose(0, 2, 1).reshape(N, ng), wq.z)
 
 
 def test_effective_bits_from_buffers():
@@ -302,6 +304,16 @@ def test_effective_bits_from_buffers():
     assert bits == gold["value"] == gold["b"] + gold["m"] / gold["G"]
     assert 8.0 * (codes.nbytes + scales.nbytes + zeros.nbytes) / (N * K) == 4.15625
     assert oracle.w4_bits_per_weight(N, K) == 4.125
+
+
+@pytest.mark.parametrize("G", [32, 64])
+def test_effective_bits_other_group_sizes(G):
+    # the page's b_eff = b + m / G with its b and m, at the other group sizes
+    gold = GOLDEN["effective_bits_int4_fp16_scale_g128"]
+    N, K = 128, 512
+    codes, scales, zeros = oracle.pack_tile(oracle.quantize_w4(syn.make_weight(N, K, seed=2), G=G))
+    assert 8.0 * (codes.nbytes + scales.nbytes) / (N * K) == gold["b"] + gold["m"] / G
+    assert 8.0 * zeros.nbytes / (N * K) == 4.0 / G
 
 
 def test_8b_bytes_thought_experiment():
