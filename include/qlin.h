@@ -197,7 +197,9 @@ int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, fl
 /*
  * W8A8 FP8 linear layer ([LP] S8, S9, S22): Y[m][n] = bf16( acc[m][n] *
  * sx[m] * sw ) with acc = sum_k e4m3(Xq[m][k]) e4m3(Wq[n][k]) in FP32.
- * Kernel choice by M as for W4A16 (CUDA-core GEMV or tcgen05 kind::f8f6f4).
+ * Kernel choice by M: for M <= qlin_gemv_max_m (16) a split-K kernel on
+ * register-level E4M3 MMA (mma.sync m16n8k32, K % 256 == 0; a CUDA-core GEMV
+ * otherwise on QLIN_PATH_GEMV), above it TMA + tcgen05 kind::f8f6f4.
  * workspace: qlin_workspace_size(QLIN_OP_W8A8_GEMM, ...) bytes.
  */
 int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,

@@ -115,7 +115,7 @@ cudaError_t set_smem_once_impl(const void* kernel, int bytes, bool wide_clusters
 
 // M at or below which the GEMV kernels are chosen (measured crossover).
 static int g_gemv_max_m_w4 = 32;
-static int g_gemv_max_m_w8 = 0;  // the tcgen05 path was faster at every measured M
+static int g_gemv_max_m_w8 = 16;  // the E4M3 mma.sync kernel beats the tcgen05 path up to M = 16
 
 }  // namespace qlin
 
@@ -347,6 +347,10 @@ static int w8a8_impl(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, 
   auto* Y = static_cast<uint16_t*>(Y_bf16);
   auto cs = static_cast<cudaStream_t>(stream);
   if (path == QLIN_PATH_GEMV) {
+    if (mma8_path_ok(M, K)) {  // register-level E4M3 MMA; split-K inside clusters, no workspace
+      const SplitPlan p = plan_w8a8_mma(M, N, K, d->num_sms);
+      return launch_status(launch_w8a8_mma(xq, sx, wq, sw, Y, M, N, K, p, d->err, cs, epi));
+    }
     const SplitPlan p = plan_w8a8_gemv(M, N, K, d->num_sms);
     if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
     return launch_status(launch_w8a8_gemv(xq, sx, wq, sw, Y, M, N, K, p, workspace, cs, epi));

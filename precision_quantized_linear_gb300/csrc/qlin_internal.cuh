@@ -117,6 +117,13 @@ cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint
                              uint16_t* Y, int64_t M, int64_t N, int64_t K, int G, const SplitPlan& plan, void* ws,
                              int* err, cudaStream_t st, const Epi& epi = Epi{});
 
+// W8A8 small-M kernel on register-level E4M3 mma.sync (M <= 16, K % 256 == 0);
+// kb_per_split counts 256-column stages.
+bool mma8_path_ok(int64_t M, int64_t K);
+SplitPlan plan_w8a8_mma(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w8a8_mma(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
+                            int64_t M, int64_t N, int64_t K, const SplitPlan& plan, int* err, cudaStream_t st,
+                            const Epi& epi = Epi{});
 SplitPlan plan_w8a8_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                              int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st,

@@ -201,6 +201,13 @@ def test_w8a8_m_sweep(path, M):
     assert _w8_case(M, 256, 1024, path, seed=300 + M) <= TOL
 
 
+@pytest.mark.parametrize("K,N", [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+def test_w8a8_small_m_mma_kernel_sampled(K, N, M):
+    # the register-level E4M3 MMA kernel (one or two token blocks, split-K clusters)
+    assert _w8_case(M, N, K, q.PATH_GEMV, seed=K + N + M, nsamp=1500) <= TOL
+
+
 @pytest.mark.parametrize("M,K,N", [(2048, 4096, 6144), (2048, 14336, 4096)])
 def test_w8a8_prefill_sampled(M, K, N):
     assert _w8_case(M, N, K, q.PATH_AUTO, seed=M + K + N, nsamp=1500) <= TOL
