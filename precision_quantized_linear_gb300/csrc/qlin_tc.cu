@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "qlin_internal.cuh"
 #include "qlin_ptx.cuh"
 
@@ -245,7 +247,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
         uint8_t* st = ring + s * C::kStage;
         const int kb = un.kb0 + j * KPS;
         if constexpr (W4) {
-          const int64_t g0 = static_cast<int64_t>(kb) * 64 / a.G;
+          const int64_t g0 = (static_cast<int64_t>(kb) * 64) >> (31 - __clz(a.G));
           bulk_load_hint(st + KPS * C::kXBlk, a.codes + (static_cast<int64_t>(un.nt) * KB + kb) * 4096,
                          KPS * 4096, &full[s], pol_stream);
           bulk_load(st + C::kScaleOff, a.scales + (static_cast<int64_t>(un.nt) * ng + g0) * kTileN, gps * 256,
@@ -404,91 +406,103 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
       const int grp = (warp - 2) >> 2;
       int it = 0, ait = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        const Unit un = unit_of(a, u, KB);
-        for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
-          const int s = it % C::kStages;
-          if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort))) {
-            ok = false;  // leave as a whole warp
-            break;
-          }
-          const uint8_t* st = ring + s * C::kStage;
-          const int kb = un.kb0 + j * KPS;
-#pragma unroll
-          for (int i = 0; i < KPS; ++i, ++ait) {
-            const bool mine = (ait & 1) == grp;
-            const int ai = ait % C::kAStages;
-            uint4 c[2];
-            float scale[2] = {0.0f, 0.0f}, zq[2] = {0.0f, 0.0f};  // per 32-column half (they differ for G = 32)
-            if (mine) {
-              if (!__all_sync(0xffffffffu,
-                              mbar_wait(&a_empty[ai], ((ait / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
-                ok = false;
-                break;
-              }
-              const uint32_t sts = smem_u32(st);
-              c[0] = lds128(sts + KPS * C::kXBlk + i * 4096 + r * 16);         // columns 0..31
-              c[1] = lds128(sts + KPS * C::kXBlk + i * 4096 + 2048 + r * 16);  // columns 32..63
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {  // group of this half within the stage
-                const int gi = ((kb + i) * 64 + h * 32) / a.G - (kb * 64) / a.G;
-                scale[h] = __half2float(
-                    __ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
-                const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
-                zq[h] = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
-              }
+      // the whole loop per group size, so that the group arithmetic is constant
+      auto dq_loop = [&](auto gconst) {
+        constexpr int gshift = decltype(gconst)::value;  // log2 G
+        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+          const Unit un = unit_of(a, u, KB);
+          for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
+            const int s = it % C::kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort))) {
+              ok = false;  // leave as a whole warp
+              break;
             }
-            if (i == KPS - 1) {
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
-            }
-            if (!mine) continue;
-            if constexpr (C::kATmem) {
-              // lane r of the slot holds row r: 32 columns x two BF16 = the 64 columns of the block
-              tc_fence_after();
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[h]);
-                const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[h]);
-                const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
-                uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                  const uint4 d = dequant8(words[t], zoff, s2);
-                  v[t] = d.x;
-                  v[4 + t] = d.y;
-                  v[8 + t] = d.z;
-                  v[12 + t] = d.w;
+            const uint8_t* st = ring + s * C::kStage;
+            const int kb = un.kb0 + j * KPS;
+  #pragma unroll
+            for (int i = 0; i < KPS; ++i, ++ait) {
+              const bool mine = (ait & 1) == grp;
+              const int ai = ait % C::kAStages;
+              uint4 c[2];
+              float scale[2] = {0.0f, 0.0f}, zq[2] = {0.0f, 0.0f};  // per 32-column half (they differ for G = 32)
+              if (mine) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&a_empty[ai], ((ait / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
+                  ok = false;
+                  break;
                 }
-                tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
-                              h * 16,
-                          v);
+                const uint32_t sts = smem_u32(st);
+                c[0] = lds128(sts + KPS * C::kXBlk + i * 4096 + r * 16);         // columns 0..31
+                c[1] = lds128(sts + KPS * C::kXBlk + i * 4096 + 2048 + r * 16);  // columns 32..63
+  #pragma unroll
+                for (int h = 0; h < 2; ++h) {  // group of this half within the stage (one group for G >= 64)
+                  if (h == 1 && gshift > 5) {  // G >= 64: both halves in one group
+                    scale[1] = scale[0];
+                    zq[1] = zq[0];
+                    break;
+                  }
+                  const int gi = (((kb + i) * 64 + h * 32) >> gshift) - ((kb * 64) >> gshift);
+                  scale[h] = __half2float(
+                      __ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
+                  const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
+                  zq[h] = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
+                }
               }
-              tmem_st_wait();
-              tc_fence_before();
-            } else {
-              uint8_t* arow = aring + ai * C::kAStage + r * 128;
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[h]);
-                const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[h]);
-                const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
-                uint4 d[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) d[t] = dequant8(words[t], zoff, s2);
-                // 16-byte chunk cc = 4h + i holds columns 8cc..8cc+7: position i of words 0..3
-                *reinterpret_cast<uint4*>(arow + (((h * 4 + 0) ^ (r & 7)) << 4)) = make_uint4(d[0].x, d[1].x, d[2].x, d[3].x);
-                *reinterpret_cast<uint4*>(arow + (((h * 4 + 1) ^ (r & 7)) << 4)) = make_uint4(d[0].y, d[1].y, d[2].y, d[3].y);
-                *reinterpret_cast<uint4*>(arow + (((h * 4 + 2) ^ (r & 7)) << 4)) = make_uint4(d[0].z, d[1].z, d[2].z, d[3].z);
-                *reinterpret_cast<uint4*>(arow + (((h * 4 + 3) ^ (r & 7)) << 4)) = make_uint4(d[0].w, d[1].w, d[2].w, d[3].w);
+              if (i == KPS - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
               }
-              fence_proxy_async_smem();
+              if (!mine) continue;
+              if constexpr (C::kATmem) {
+                // lane r of the slot holds row r: 32 columns x two BF16 = the 64 columns of the block
+                tc_fence_after();
+  #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[h]);
+                  const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[h]);
+                  const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
+                  uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
+  #pragma unroll
+                  for (int t = 0; t < 4; ++t) {
+                    const uint4 d = dequant8(words[t], zoff, s2);
+                    v[t] = d.x;
+                    v[4 + t] = d.y;
+                    v[8 + t] = d.z;
+                    v[12 + t] = d.w;
+                  }
+                  tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
+                                h * 16,
+                            v);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+              } else {
+                uint8_t* arow = aring + ai * C::kAStage + r * 128;
+  #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[h]);
+                  const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[h]);
+                  const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
+                  uint4 d[4];
+  #pragma unroll
+                  for (int t = 0; t < 4; ++t) d[t] = dequant8(words[t], zoff, s2);
+                  // 16-byte chunk cc = 4h + i holds columns 8cc..8cc+7: position i of words 0..3
+                  *reinterpret_cast<uint4*>(arow + (((h * 4 + 0) ^ (r & 7)) << 4)) = make_uint4(d[0].x, d[1].x, d[2].x, d[3].x);
+                  *reinterpret_cast<uint4*>(arow + (((h * 4 + 1) ^ (r & 7)) << 4)) = make_uint4(d[0].y, d[1].y, d[2].y, d[3].y);
+                  *reinterpret_cast<uint4*>(arow + (((h * 4 + 2) ^ (r & 7)) << 4)) = make_uint4(d[0].z, d[1].z, d[2].z, d[3].z);
+                  *reinterpret_cast<uint4*>(arow + (((h * 4 + 3) ^ (r & 7)) << 4)) = make_uint4(d[0].w, d[1].w, d[2].w, d[3].w);
+                }
+                fence_proxy_async_smem();
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&a_full[ai]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[ai]);
           }
         }
-      }
+      };
+      if (a.G == 32) dq_loop(std::integral_constant<int, 5>{});
+      else if (a.G == 64) dq_loop(std::integral_constant<int, 6>{});
+      else dq_loop(std::integral_constant<int, 7>{});
       if (!ok) {
         set_error(a.err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
