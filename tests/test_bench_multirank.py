@@ -40,3 +40,18 @@ def test_two_rank_max_and_barrier():
         p.join(timeout=120)
         assert p.exitcode == 0
     assert out[0] == 5.0 and out[1] == 5.0
+
+
+def test_crossover_summary_finds_the_first_m_from_which_w8a8_stays_faster():
+    import bench
+
+    rows = []
+    for M, t4, t8 in [(1, 10.0, 15.0), (16, 14.0, 18.0), (32, 20.0, 19.0), (64, 18.0, 21.0), (128, 30.0, 25.0),
+                      (256, 40.0, 30.0)]:
+        rows.append({"K": 4096, "N": 14336, "M": M, "variant": "w4", "us": t4})
+        rows.append({"K": 4096, "N": 14336, "M": M, "variant": "w8", "us": t8 - 1.0, "quant_us": 1.0})
+    out = bench.crossover_summary(rows, 1900.0, 3800.0, 6800.0)["crossover"][0]
+    assert out["measured_M"] == 128  # 32 is not the crossover: W4A16 wins again at 64
+    assert out["measured_us"]["32"] == [20.0, 19.0]
+    # the roofline crossover with FP8 at twice the BF16 rate sits near P16 / (2 BW)
+    assert abs(out["roofline_M_gemm_only"] - out["simplified_P16_over_2BW"]) < 0.15 * out["simplified_P16_over_2BW"]
