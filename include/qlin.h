@@ -5,7 +5,8 @@
  *
  *  W4A16  INT4 weights, q = clamp(round(w/s) + z, 0, 15), one FP16 scale s
  *         and one 4-bit zero-point z per group of G = 128 weights along K
- *         (4.125 bits/weight for codes + scales); BF16 activations; the
+ *         (4.125 bits/weight for codes + scales; G = 32 and 64 are also
+ *         taken, at 4.5 and 4.25 bits); BF16 activations; the
  *         dequantisation x_hat = s (q - z) happens inside the GEMM kernel.
  *  W8A8   FP8 E4M3 weights with one FP32 scale for the whole tensor and E4M3
  *         activations with one FP32 scale per token (row), both "current"
@@ -38,8 +39,10 @@
  *    by qlin_get_device_error().
  *  - M = 0 is a valid empty call: it returns QLIN_OK and launches nothing.
  *
- * Eligibility ([LP] S24): device sm_103 (compute capability 10.3); G = 128;
- * N % 128 == 0; K % 128 == 0; 1 <= N, K; 0 <= M <= 2^24.
+ * Eligibility ([LP] S24): device sm_103 (compute capability 10.3);
+ * G in {32, 64, 128} (the CUDA-core GEMV that serves small M when K % 256 != 0
+ * and qlin_w4a16_gemv_noalloc take G = 128 only); N % 128 == 0; K % 128 == 0;
+ * 1 <= N, K; 0 <= M <= 2^24.
  */
 #ifndef QLIN_H
 #define QLIN_H

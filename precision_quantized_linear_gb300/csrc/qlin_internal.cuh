@@ -129,7 +129,8 @@ cudaError_t launch_w8a8_gemv(const uint8_t* Xq, const float* sx, const uint8_t* 
                              int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws, cudaStream_t st,
                              const Epi& epi = Epi{});
 
-// tcgen05 kernels: swap-AB (weights are the 128-row MMA operand, tokens the N side)
+// tcgen05 kernels: swap-AB (weights are the 128-row MMA operand, tokens the N
+// side), except block-scaled FP8 with 128-token tiles, which is token-major
 struct TcPlan {
   int bn = 16;           // tokens per tile (MMA N)
   int wn = 128;          // weight rows per tile (256: block-scaled token-major tiles)

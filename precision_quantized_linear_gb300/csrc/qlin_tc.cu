@@ -5,6 +5,9 @@
 // and the tokens are its N side (16..256), so that a decode batch of a few
 // tokens still fills the 128-row MMA and every weight is read once per token
 // block.  D[n][m] = sum_k W[n][k] X[m][k] lands in TMEM lane n, column m.
+// The one exception is FP8 block scaling with 128-token tiles, which runs
+// token-major (tokens as M, 128 or 256 weight rows as N) so that its per-K-block
+// promotion factor is one scalar per TMEM lane.
 //
 // W4A16 ([LP] S11, S23 "fast path"): the packed INT4 tile and its scales /
 // zero-points are bulk-copied into shared memory; eight dequantisation warps
@@ -18,8 +21,9 @@
 // ring of shared-memory stages, so HBM traffic does not pause between units;
 // warp 1 owns TMEM and issues the MMAs into one of two accumulators; the
 // dequantisation warps (W4A16) fill a second ring with BF16 weight tiles; four
-// epilogue warps drain the other accumulator meanwhile.  Every wait is bounded
-// in time; on expiry the kernel records QLIN_ERR_TIMEOUT and leaves.
+// epilogue warps (eight for block scaling from 32 tokens) drain the other
+// accumulator meanwhile.  Every wait is bounded in time; on expiry the kernel
+// records QLIN_ERR_TIMEOUT and leaves.
 #include <cmath>
 #include <algorithm>
 
