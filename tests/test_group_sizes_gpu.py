@@ -94,3 +94,21 @@ def test_other_groups_rejected_where_unsupported():
     with pytest.raises(q.QlinError) as e:
         q.qlin_w4_packed_sizes(N, 4096, 48)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("G", [32, 64])
+@pytest.mark.parametrize("M,path", [(3, q.PATH_GEMV), (24, q.PATH_GEMV), (100, q.PATH_TC)])
+def test_w4a16_other_groups_with_fused_epilogue(G, M, path):
+    N, K = 256, 1024
+    W = syn.make_weight(N, K, seed=M + 3 * G)
+    X = syn.make_act(M, K, seed=M + 3 * G + 1)
+    wq = oracle.quantize_w4(W, G=G)
+    b32 = np.random.default_rng(G).normal(0.0, 0.5, N).astype(np.float32)
+    bias = (b32.view(np.uint32) >> 16).astype(np.uint16)  # BF16 by truncation: any BF16 values will do
+    lin = W4A16Linear(to_dev(W), G=G, bias=to_dev(bias).view(torch.bfloat16))
+    Y = lin(to_dev(X).view(torch.bfloat16), path=path, act=q.ACT_SILU).float().cpu().numpy().astype(np.float64)
+    Yref = oracle.epilogue(oracle.w4a16_full(X, wq), bias, oracle.ACT_SILU)
+    xn = np.linalg.norm(syn.bf16_bits_to_f32(X).astype(np.float64), axis=1)
+    wn = np.linalg.norm(oracle.dequant_w4(wq), axis=1)
+    bound = 1.13 * TOL * xn[:, None] * wn[None, :] + 2.0 ** -8 * np.abs(Yref)
+    assert (np.abs(Y - Yref) <= bound).all()
