@@ -10,8 +10,9 @@ follows (see ``qlin_oracle.c`` for the list):
   [LP] "Low-precision LLM inference: FP8/INT8/INT4/FP4 kernels and
        calibration" -- S2 uniform quantisation, S3 symmetric/asymmetric,
        S4 granularity, S5 effective bits, S7 E4M3, S8 FP8 current scaling,
-       S22 accumulator precision, S23/S24 fused bias / activation
-       epilogue (``epilogue`` below).
+       S10 MX block formats (MXFP8 after the OCP Microscaling spec v1.0,
+       ``quant_mxfp8_rows`` below), S22 accumulator precision, S23/S24 fused
+       bias / activation epilogue (``epilogue`` below).
   [TP] "Quantization throughput by batch size: why W4A16 is overtaken by
        W8A8" -- the arithmetic-intensity roofline (``roofline_*`` below).
 
@@ -72,6 +73,10 @@ def _load():
         lib.orc_dequant_w4.argtypes = [_p, _p, _p, _i64, _i64, ctypes.c_int, _p]
         lib.orc_pack_canonical.restype = None
         lib.orc_pack_canonical.argtypes = [_p, _p, _i64, _i64, ctypes.c_int, _p, _p]
+        lib.orc_quant_mxfp8_rows.restype = None
+        lib.orc_quant_mxfp8_rows.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.orc_w8a8_mx_at.restype = None
+        lib.orc_w8a8_mx_at.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p]
         lib.orc_pack_tile.restype = None
         lib.orc_pack_tile.argtypes = [_p, _p, _p, _i64, _i64, _i64, _p, _p, _p]
         lib.orc_quant_fp8_rows.restype = None
@@ -381,3 +386,38 @@ def epilogue(Y: np.ndarray, bias_bf16, act: int) -> np.ndarray:
         return V * phi
     assert act == ACT_NONE
     return V
+
+
+def quant_mxfp8_rows(X_bf16: np.ndarray):
+    """MXFP8 (OCP MX v1.0, named in [LP] S10): per row, blocks of 32 elements share a
+    power-of-two scale 2^e (E8M0 byte e + 127, e = floor(log2 amax) - 8, clamped to
+    [-127, 127]); codes E4M3(v / 2^e), RNE, saturating.  Returns codes [R][K] uint8 and
+    scales [R][K/32] uint8."""
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    R, K = X.shape
+    assert K % 32 == 0
+    codes = np.empty((R, K), np.uint8)
+    scales = np.empty((R, K // 32), np.uint8)
+    _load().orc_quant_mxfp8_rows(_ptr(X), R, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mx_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Dequantised MX values in double: e4m3(code) * 2^(scale - 127) per 32-block."""
+    tab = e4m3_table()
+    return tab[codes] * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)
+
+
+def w8a8_mx_at(Xq, xs, Wq, ws, ms, ns) -> np.ndarray:
+    """Y[m_i, n_i] = sum over 32-blocks of both block scales times the block's E4M3 dot product, in double."""
+    Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    xs = np.ascontiguousarray(xs, dtype=np.uint8)
+    ws = np.ascontiguousarray(ws, dtype=np.uint8)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape, np.float64)
+    _load().orc_w8a8_mx_at(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws), M, N, K, _ptr(ms), _ptr(ns), ms.size, _ptr(out))
+    return out

@@ -471,3 +471,64 @@ int orc_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------ */
+/* MXFP8 (the OCP Microscaling Formats specification v1.0, which [LP]  */
+/* S10 names for the MX block formats): blocks of 32 consecutive       */
+/* elements along a row share one power-of-two scale X = 2^e, stored   */
+/* as an E8M0 byte e + 127.  e = floor(log2(amax)) - 8, 8 being the     */
+/* exponent of the largest E4M3 normal (448 = 1.75 * 2^8), clamped to   */
+/* [-127, 127]; an all-zero block takes e = -127.  Each element becomes */
+/* E4M3(v / X), round to nearest even, saturating at +-448.             */
+/* ------------------------------------------------------------------ */
+
+static int mx_exponent(float amax)
+{
+    if (amax == 0.0f) return -127;
+    int ex;
+    frexpf(amax, &ex);          /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+    int e = (ex - 1) - 8;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* X [R][K] bf16 -> codes [R][K] e4m3 and scales [R][K/32] e8m0 */
+void orc_quant_mxfp8_rows(const uint16_t *X, int64_t R, int64_t K, uint8_t *codes, uint8_t *scales)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; r++) {
+        for (int64_t b = 0; b < K / 32; b++) {
+            float amax = 0.0f;
+            for (int64_t k = b * 32; k < b * 32 + 32; k++) {
+                float a = fabsf(bf16_to_f32(X[r * K + k]));
+                if (a > amax) amax = a;
+            }
+            int e = mx_exponent(amax);
+            scales[r * (K / 32) + b] = (uint8_t)(e + 127);
+            double xs = ldexp(1.0, e);
+            for (int64_t k = b * 32; k < b * 32 + 32; k++)
+                codes[r * K + k] = orc_f32_to_e4m3_rn_sat((float)((double)bf16_to_f32(X[r * K + k]) / xs));
+        }
+    }
+}
+
+/* Y[m][n] = sum over 32-blocks b of 2^(xs[m][b]-127) 2^(ws[n][b]-127)
+ *           * sum_{k in b} e4m3(Xq[m][k]) e4m3(Wq[n][k]), in double, for sampled (m, n) */
+void orc_w8a8_mx_at(const uint8_t *Xq, const uint8_t *xs, const uint8_t *Wq, const uint8_t *ws,
+                    int64_t M, int64_t N, int64_t K, const int64_t *ms, const int64_t *ns, int64_t cnt, double *out)
+{
+    (void)M; (void)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < cnt; i++) {
+        int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t b = 0; b < K / 32; b++) {
+            double part = 0.0;
+            for (int64_t k = b * 32; k < b * 32 + 32; k++)
+                part += orc_e4m3_to_f64(Xq[m * K + k]) * orc_e4m3_to_f64(Wq[n * K + k]);
+            acc += part * ldexp(1.0, (int)xs[m * (K / 32) + b] - 127) * ldexp(1.0, (int)ws[n * (K / 32) + b] - 127);
+        }
+        out[i] = acc;
+    }
+}

@@ -554,3 +554,57 @@ def test_epilogue_bias_is_per_output_column_and_precedes_the_activation():
     np.testing.assert_allclose(Y, xa @ wa.T, rtol=1e-12, atol=1e-12)
     two = np.array([0x4000], np.uint16)  # BF16 2.0
     assert oracle.epilogue(np.array([[-1.0]]), two, oracle.ACT_RELU)[0, 0] == 1.0  # relu(-1 + 2), not relu(-1) + 2
+
+
+# ---- MXFP8 (OCP Microscaling v1.0, named in [LP] S10): 32-element blocks, E8M0 scale
+
+def _bf16_bits(vals):
+    return (np.asarray(vals, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_mxfp8_shared_exponent_at_closed_form_points():
+    K = 32
+    rows = np.zeros((5, K), np.float32)
+    rows[0, 0] = 1.0          # floor(log2 1) = 0 -> e = -8, code 119; 1.0 / 2^-8 = 256 = E4M3 0x78
+    rows[1, 0] = 480.0        # e = 0, code 127; 480 saturates to 448 (0x7E)
+    rows[2, 0] = 300.0        # e = 0; 300 lies between 288 and 320 -> 288 (nearest)
+    rows[3, :] = 0.0          # all-zero block: e = -127 (code 0), codes 0
+    rows[4, 0] = 2.0 ** -126  # e would be -134: clamped to -127 (code 0); 2^-126 / 2^-127 = 2 exactly
+    codes, scales = oracle.quant_mxfp8_rows(_bf16_bits(rows))
+    assert list(scales[:, 0]) == [119, 127, 127, 0, 0]
+    tab = oracle.e4m3_table()
+    assert codes[0, 0] == 0x78 and tab[codes[0, 0]] == 256.0
+    assert codes[1, 0] == 0x7E and tab[codes[1, 0]] == 448.0
+    assert tab[codes[2, 0]] == 288.0
+    assert not codes[3].any()
+    assert tab[codes[4, 0]] == 2.0
+    deq = oracle.mx_dequant(codes, scales)
+    assert deq[0, 0] == 1.0 and deq[1, 0] == 448.0 and deq[4, 0] == 2.0 ** -126
+
+
+def test_mxfp8_round_trip_error_bound():
+    rng = np.random.default_rng(11)
+    X = (rng.standard_normal((16, 256)) * np.exp2(rng.integers(-20, 20, (16, 1)))).astype(np.float32)
+    Xb = _bf16_bits(X)
+    v = syn.bf16_bits_to_f32(Xb).astype(np.float64)
+    codes, scales = oracle.quant_mxfp8_rows(Xb)
+    deq = oracle.mx_dequant(codes, scales)
+    step = np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)  # X = 2^e of each element
+    sat = np.abs(v) >= 448.0 * step
+    # E4M3 keeps 3 mantissa bits: half an ulp is 2^-4 relative; below its normal range the step is 2^-9 X
+    ok = np.abs(v - deq) <= 2.0 ** -4 * np.abs(v) + 2.0 ** -10 * step
+    assert ok[~sat].all()
+    assert (np.abs(deq[sat]) == 448.0 * step[sat]).all()   # only the top of each block's range saturates
+    assert (np.abs(v[sat]) < 512.0 * step[sat]).all()
+
+
+def test_mxfp8_product_applies_each_block_scale_to_its_own_block():
+    rng = np.random.default_rng(12)
+    X = (rng.standard_normal((6, 128)) * np.exp2(rng.integers(-6, 6, (6, 4)).repeat(32, axis=1))).astype(np.float32)
+    W = (rng.standard_normal((8, 128)) * np.exp2(rng.integers(-6, 6, (8, 4)).repeat(32, axis=1))).astype(np.float32)
+    Xq, xs = oracle.quant_mxfp8_rows(_bf16_bits(X))
+    Wq, ws = oracle.quant_mxfp8_rows(_bf16_bits(W))
+    ms, ns = np.repeat(np.arange(6), 8), np.tile(np.arange(8), 6)
+    got = oracle.w8a8_mx_at(Xq, xs, Wq, ws, ms, ns)
+    want = (oracle.mx_dequant(Xq, xs) @ oracle.mx_dequant(Wq, ws).T)[ms, ns]  # dense product of the dequantised operands
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=0)
