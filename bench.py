@@ -8,9 +8,14 @@ decode batches M = 1, 4 and 16: 12 GEMM calls per step, weights resident in
 HBM.  The metric is quantized-linear weight GB/s: packed weight bytes
 (codes + scales + zeros) read per step / step time.
 
-Timing: CUDA graphs of one step each over 4 rotating copies of the packed
-weights (452 MB > 3x L2), CUDA events on the launching stream, W warm-up
-steps, K timed steps.  Under torchrun every rank runs the same workload on
+Timing: CUDA graphs of one step each over 5 rotating copies of the packed
+weights (pass p of the step sequence reads copy p % 5, so 4 passes = 452 MB of
+other weights, > 3x L2, stream between two reads of one copy), CUDA events on
+the launching stream, W warm-up steps, K timed steps.  The same line carries
+``prefill`` (W8A8 FP8 at M = 2048 / 8192 on the four layers, TFLOP/s and
+fraction of the FP8 peak) and ``crossover`` (W4A16 vs W8A8 on the two
+crossover shapes at M = 1 ... 512: measured crossover M beside the roofline
+prediction), each with operands rotated past L2 the same way.  Under torchrun every rank runs the same workload on
 its own GPU (replicas, weak scaling) and the slowest rank's time is used.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
@@ -34,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 LAYERS_8B = [("qkv", 4096, 6144), ("o_proj", 4096, 4096), ("gate_up", 4096, 28672), ("down", 14336, 4096)]
 MS_DECODE = (1, 4, 16)
-ROTATE = 4
+ROTATE = 5
 WORKLOAD = "llama3-8b W4A16 decode layers (qkv/o/gate_up/down) at M=1,4,16"
 
 
@@ -193,11 +198,22 @@ def build_workload(rank: int):
             ys[(M, L["name"])] = torch.empty((M, L["N"]), dtype=torch.int16, device="cuda")
     ws_bytes = max(q.qlin_workspace_size(q.OP_W4A16_GEMM, M, L["N"], L["K"]) for M in MS_DECODE for L in layers)
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
-    calls = []  # (M, layer) in step order
-    for M in MS_DECODE:
-        for L in layers:
-            calls.append((M, L))
-    return layers, xs, ys, ws, calls
+    return layers, xs, ys, ws
+
+
+def pass_calls(M, layers, copy):
+    """One pass over the four layers at batch M, all on weight copy `copy`."""
+    return [(M, L, copy) for L in layers]
+
+
+def step_calls(step, layers):
+    """The calls of step `step`: passes M = 1, 4, 16; pass p (counted over all
+    steps) reads weight copy p % ROTATE, so between two reads of one copy of a
+    layer ROTATE - 1 whole passes (>= 3 x L2 of other weights) are streamed."""
+    out = []
+    for i, M in enumerate(MS_DECODE):
+        out += pass_calls(M, layers, (step * len(MS_DECODE) + i) % ROTATE)
+    return out
 
 
 def kernel_of(M):
@@ -213,31 +229,35 @@ def run_ours(args):
     world, rank, local = dist_setup(args)
     q.build()
     q.load()
-    layers, xs, ys, ws, calls = build_workload(rank)
+    layers, xs, ys, ws = build_workload(rank)
     stream = torch.cuda.Stream()
     peaks = load_peaks()
+    l2 = l2_bytes()
+    pass_bytes = sum(w4_weight_bytes(L["N"], L["K"]) for L in layers)
+    assert (ROTATE - 1) * pass_bytes >= 3 * l2, "weight rotation too short to defeat L2"
 
-    def issue(r):
-        for M, L in calls:
+    def issue(calls):
+        for M, L, r in calls:
             c, s, z = L["sets"][r]
             q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
                               ws.numel(), stream)
 
     # correctness of the launch configuration before timing
     with torch.cuda.stream(stream):
-        issue(0)
+        issue(step_calls(0, layers))
     torch.cuda.synchronize()
     err = q.qlin_get_device_error(stream)
     if err:
         raise RuntimeError("device error %d before timing" % err)
 
-    # one CUDA graph per rotation set, holding only the kernels (programmatic
-    # launches of consecutive kernels may overlap)
+    # one CUDA graph per step of the rotation (the copy pattern repeats every
+    # ROTATE steps), holding only the kernels (programmatic launches of
+    # consecutive kernels may overlap)
     graphs = []
-    for r in range(ROTATE):
+    for st in range(ROTATE):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            issue(r)
+            issue(step_calls(st, layers))
         graphs.append(g)
     torch.cuda.synchronize()
 
@@ -261,23 +281,26 @@ def run_ours(args):
     step_ms_local = e0.elapsed_time(e1) / args.steps
     step_ms = dist_max(step_ms_local, world)
 
-    weight_bytes = sum(w4_weight_bytes(L["N"], L["K"]) for M, L in calls)
-    alg_bytes = sum(w4_alg_bytes(M, L["N"], L["K"]) for M, L in calls)
+    calls = step_calls(0, layers)
+    weight_bytes = sum(w4_weight_bytes(L["N"], L["K"]) for M, L, _ in calls)
+    alg_bytes = sum(w4_alg_bytes(M, L["N"], L["K"]) for M, L, _ in calls)
     value = world * weight_bytes / (step_ms * 1e-3) / 1e9
+    # every launch of the step is the small-M W4A16 kernel: its average launch
+    # duration is the timed region over the launches in it (consecutive
+    # launches overlap through programmatic dependent launch, as in serving)
+    kernels = {kernel_of(M) for M, _, _ in calls}
+    assert len(kernels) == 1
+    dom = kernels.pop()
+    launch_ms = step_ms / len(calls)
+    achieved = alg_bytes / len(calls) / (launch_ms * 1e-3) / 1e9
 
-    # per-kernel device time, right after the timed region: a graph of each call's
-    # launches over the rotating weight copies (consecutive launches overlap as in
-    # the step), replayed and timed with CUDA events; events between the launches
-    # of the step itself would serialise them and add their own gaps
-    per_kernel = {}
-    per_call = []
-    for M, L in calls:
+    # per batch size: a graph of ROTATE passes at that M over the rotating copies
+    per_m_gbs = {}
+    for M in MS_DECODE:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for r in range(ROTATE):
-                c, s, z = L["sets"][r]
-                q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
-                                  ws.numel(), stream)
+                issue(pass_calls(M, layers, r))
         g.replay()
         torch.cuda.synchronize()
         a, b = make_event(False), make_event(False)
@@ -287,25 +310,20 @@ def run_ours(args):
                 g.replay()
             b.record(stream)
         torch.cuda.synchronize()
-        per_call.append((M, L, a.elapsed_time(b) / (5 * ROTATE)))
-    for M, L, ms in per_call:
-        k = kernel_of(M)
-        d = per_kernel.setdefault(k, {"ms": 0.0, "launches": 0, "bytes": 0})
-        d["ms"] += ms
-        d["launches"] += 1
-        d["bytes"] += w4_alg_bytes(M, L["N"], L["K"])
-    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
-    dk = per_kernel[dom]
-    achieved = dk["bytes"] / (dk["ms"] * 1e-3) / 1e9
-    per_m = {}
-    for M, L, ms in per_call:
-        e = per_m.setdefault(M, [0.0, 0])
-        e[0] += ms
-        e[1] += w4_weight_bytes(L["N"], L["K"])
-    # t and b are both summed over the same launches
-    per_m_gbs = {str(M): round(b / (t * 1e-3) / 1e9, 1) for M, (t, b) in per_m.items()}
+        t = a.elapsed_time(b) / (5 * ROTATE)
+        per_m_gbs[str(M)] = round(pass_bytes / (t * 1e-3) / 1e9, 1)
 
-    e2e = run_e2e(args, layers, xs, ys, ws, calls, stream, world)
+    e2e = run_e2e(args, layers, xs, ys, ws, stream, world)
+    extra = {}
+    if not args.no_sweeps and world == 1:
+        clk2 = ClockSampler(local)
+        clk2.start()
+        p8_probe = fp8_peak_probe()
+        extra["prefill"] = measure_prefill(peaks, l2)
+        extra["crossover"] = measure_crossover(peaks, l2)
+        extra["prefill"]["fp8_probe_tflops"] = round(p8_probe, 1) if p8_probe else None
+        extra["sweep_clocks"] = clk2.stop()
+    traffic_per_launch = round(TRAFFIC_CAPTURE["dram_bytes"] / TRAFFIC_CAPTURE["alg_bytes"] * alg_bytes / len(calls))
 
     out = {
         "metric": "quantized-linear weight GB/s (decode) & TFLOPS (prefill) vs batch M, % of roofline",
@@ -314,24 +332,24 @@ def run_ours(args):
         "dtype": "int4 weights x bf16 activations, fp32 accumulate", "data": "synthetic (seeded N(0,0.02) weights with 1% x20 outlier channels, N(0,1) activations)",
         "config": {"workload": WORKLOAD, "layers_KxN": [[K, N] for _, K, N in LAYERS_8B], "M": list(MS_DECODE),
                    "G": 128, "calls_per_step": len(calls), "weight_bytes_per_step": weight_bytes,
-                   "alg_bytes_per_step": alg_bytes, "l2": "4 rotating weight copies (%.0f MB > 3x L2)" %
-                   (ROTATE * weight_bytes / 1e6 / len(MS_DECODE)), "timing": "CUDA graph per step, CUDA events; per-kernel times from a graph of each call's launches over the rotating weight copies, timed with CUDA events after the timed region"},
+                   "alg_bytes_per_step": alg_bytes,
+                   "l2": "inputs larger than L2: %d rotating weight copies; pass p reads copy p %% %d, so %.0f MB "
+                         "of other weights (%.1f x L2) stream between two reads of one copy" %
+                         (ROTATE, ROTATE, (ROTATE - 1) * pass_bytes / 1e6, (ROTATE - 1) * pass_bytes / l2),
+                   "timing": "CUDA graph per step, CUDA events on the launching stream around the timed steps"},
         "per_M_weight_gbs": per_m_gbs,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "frac_in_step": round(alg_bytes / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                     "traffic": (round(TRAFFIC_CAPTURE["dram_bytes"] / TRAFFIC_CAPTURE["alg_bytes"]
-                                       * dk["bytes"] / dk["launches"])
-                                 if dom == TRAFFIC_CAPTURE["kernel"] else None),
-                     "traffic_note": "bytes per launch, scaled from one ncu capture (M=1, 4096x28672)",
-                     "peak_source": peaks["source"], "launches_timed": dk["launches"],
-                     "share_of_step": round(dk["ms"] / sum(v["ms"] for v in per_kernel.values()), 3)},
-        "kernels": {k: {"ms_per_launch": round(v["ms"] / v["launches"], 5), "launches": v["launches"],
-                        "GBps": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)} for k, v in per_kernel.items()},
+                     "traffic": traffic_per_launch,
+                     "traffic_note": "bytes per launch, scaled from one ncu capture (M=1, 4096x28672) by "
+                                     "algorithmic bytes",
+                     "peak_source": peaks["source"], "launches_timed": len(calls) * args.steps,
+                     "ms_per_launch": round(launch_ms, 5), "share_of_step": 1.0},
         "gpu_launches": len(calls) * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }
+    out.update(extra)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
@@ -341,7 +359,106 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, layers, xs, ys, ws, calls, stream, world):
+def l2_bytes():
+    import torch
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+
+
+def rotation(bytes_per_copy, l2):
+    """Copies of an operand so that one copy is read again only after >= 3 x L2 of others."""
+    return max(2, int(np.ceil(3 * l2 / bytes_per_copy)) + 1)
+
+
+def measure_prefill(peaks, l2):
+    """W8A8 FP8 prefill (M = 2048 and 8192 on the four Llama-3-8B shapes, 0.1 % of
+    tokens x50): TFLOP/s of the GEMM and of activation quantisation + GEMM,
+    against the FP8 dense peak (the measured BF16 peak x 2, the nominal ratio)."""
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+    from precision_quantized_linear_gb300 import synthetic as syn
+    from precision_quantized_linear_gb300.layers import W8A8Linear
+
+    p8 = 2.0 * peaks["bf16_tflops_sustained"]
+    rows = []
+    for K, N in [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]:
+        lin = W8A8Linear(torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda())
+        sets = [lin.Wq] + [lin.Wq.clone() for _ in range(rotation(N * K, l2) - 1)]
+        for M in (2048, 8192):
+            X = torch.from_numpy(syn.make_act(M, K, seed=M + 7, token_outlier_frac=0.001).view(np.int16)).cuda()
+            Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+            Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+            sx = torch.empty(M, dtype=torch.float32, device="cuda")
+            nb = q.qlin_workspace_size(q.OP_W8A8_GEMM, M, N, K)
+            ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+            q.qlin_quant_act_fp8(X, M, K, Xq, sx)
+            us = time_launches([lambda st, wq=wq: q.qlin_w8a8_fp8_gemm(Xq, sx, wq, lin.sw, Y, M, N, K, ws, ws.numel(),
+                                                                      st) for wq in sets])
+            qus = time_launches([lambda st: q.qlin_quant_act_fp8(X, M, K, Xq, sx, st)])
+            flops = 2 * M * N * K
+            t_roof = max(flops / (p8 * 1e12), w8_alg_bytes(M, N, K) / (peaks["hbm_gbs"] * 1e9)) * 1e6
+            rows.append({"K": K, "N": N, "M": M, "us": round(us, 2), "TFLOPS": round(flops / (us * 1e-6) / 1e12, 1),
+                         "frac": round(t_roof / us, 3), "quant_us": round(qus, 2),
+                         "TFLOPS_with_quant": round(flops / ((us + qus) * 1e-6) / 1e12, 1)})
+            assert q.qlin_get_device_error() == 0
+            del X, Y, Xq, sx, ws
+        del lin, sets
+        torch.cuda.empty_cache()
+    tot_flops = sum(2 * r["M"] * r["N"] * r["K"] for r in rows)
+    tot_us = sum(r["us"] for r in rows)
+    return {"workload": "W8A8 FP8 prefill M=2048/8192 on the Llama-3-8B shapes (tcgen05 kind::f8f6f4)",
+            "peak_tflops": round(p8, 1), "peak_source": "measured bf16 sustained x 2 (nominal FP8/BF16 ratio)",
+            "TFLOPS": round(tot_flops / (tot_us * 1e-6) / 1e12, 1),
+            "frac": round(tot_flops / (tot_us * 1e-6) / 1e12 / p8, 3), "cases": rows}
+
+
+def measure_crossover(peaks, l2):
+    """W4A16 vs W8A8 (activation quantisation + GEMM) on K=4096 N=14336 and
+    K=14336 N=4096 at M = 1 ... 512, both through the default dispatch: the
+    measured crossover M beside the roofline prediction."""
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+    from precision_quantized_linear_gb300 import synthetic as syn
+    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8Linear
+
+    rows = []
+    for K, N in [(4096, 14336), (14336, 4096)]:
+        W = torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda()
+        lin4, lin8 = W4A16Linear(W), W8A8Linear(W)
+        del W
+        sets4 = [(lin4.codes, lin4.scales, lin4.zeros)] + [
+            (lin4.codes.clone(), lin4.scales.clone(), lin4.zeros.clone())
+            for _ in range(rotation(w4_weight_bytes(N, K), l2) - 1)]
+        sets8 = [lin8.Wq] + [lin8.Wq.clone() for _ in range(rotation(N * K, l2) - 1)]
+        for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):
+            X = torch.from_numpy(syn.make_act(M, K, seed=M + 7).view(np.int16)).cuda()
+            Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+            Xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+            sx = torch.empty(M, dtype=torch.float32, device="cuda")
+            nb = max(q.qlin_workspace_size(q.OP_W4A16_GEMM, M, N, K), q.qlin_workspace_size(q.OP_W8A8_GEMM, M, N, K))
+            ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+            us4 = time_launches([lambda st, c=c, s=s, z=z: q.qlin_w4a16_gemm(X, c, s, z, Y, M, N, K, 128, ws,
+                                                                            ws.numel(), st) for (c, s, z) in sets4])
+
+            def w8(st, wq):
+                q.qlin_quant_act_fp8(X, M, K, Xq, sx, st)
+                q.qlin_w8a8_fp8_gemm(Xq, sx, wq, lin8.sw, Y, M, N, K, ws, ws.numel(), st)
+            us8 = time_launches([lambda st, wq=wq: w8(st, wq) for wq in sets8])
+            rows.append({"K": K, "N": N, "M": M, "variant": "w4", "us": us4})
+            rows.append({"K": K, "N": N, "M": M, "variant": "w8", "us": us8})
+            assert q.qlin_get_device_error() == 0
+        del lin4, lin8, sets4, sets8
+        torch.cuda.empty_cache()
+    summary = crossover_summary(rows, peaks["bf16_tflops"], 2.0 * peaks["bf16_tflops"], peaks["hbm_gbs"],
+                                quant_in_w8=True)
+    summary["how"] = ("W8A8 time = qlin_quant_act_fp8 + qlin_w8a8_fp8_gemm; both through the default dispatch; "
+                      "roofline with the measured HBM and BF16 peaks, FP8 = 2 x BF16")
+    return summary
+
+
+def run_e2e(args, layers, xs, ys, ws, stream, world):
     """Same metric through the public API, host buffers in and out every step."""
     import torch
 
@@ -351,11 +468,11 @@ def run_e2e(args, layers, xs, ys, ws, calls, stream, world):
     h2d = sum(t.numel() * 2 for t in hx.values())
     d2h = sum(t.numel() * 2 for t in hy.values())
 
-    def step(r):
+    def step(i):
         with torch.cuda.stream(stream):
             for k in hx:
                 xs[k].copy_(hx[k], non_blocking=True)
-            for M, L in calls:
+            for M, L, r in step_calls(i, layers):
                 c, s, z = L["sets"][r]
                 q.qlin_w4a16_gemm(xs[(M, L["K"])], c, s, z, ys[(M, L["name"])], M, L["N"], L["K"], 128, ws,
                                   ws.numel(), stream)
@@ -363,18 +480,18 @@ def run_e2e(args, layers, xs, ys, ws, calls, stream, world):
                 hy[k].copy_(ys[k], non_blocking=True)
 
     for i in range(max(1, args.warmup)):
-        step(i % ROTATE)
+        step(i)
     torch.cuda.synchronize()
     barrier(world)
     n = max(1, args.steps)
     e0, e1 = make_event(False), make_event(False)
     e0.record(stream)
     for i in range(n):
-        step(i % ROTATE)
+        step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = dist_max(e0.elapsed_time(e1) / n, world)
-    wbytes = sum(w4_weight_bytes(L["N"], L["K"]) for M, L in calls)
+    wbytes = sum(w4_weight_bytes(L["N"], L["K"]) for M, L, _ in step_calls(0, layers))
     return {"value": round(world * wbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "how": "per step: pinned host X -> device, 12 qlin_w4a16_gemm calls (no graph), Y -> pinned host"}
@@ -383,49 +500,83 @@ def run_e2e(args, layers, xs, ys, ws, calls, stream, world):
 # ---------------------------------------------------------------------------- oracle (CPU) arms
 
 def _oracle_sample():
+    """The decode workload for the oracle: the four Llama-3-8B layers (quantised
+    once) and the activations at M = 1, 4, 16, as the GPU arm draws them."""
     import oracle
     from precision_quantized_linear_gb300 import synthetic as syn
-    name, K, N = LAYERS_8B[1]           # o_proj, 4096 x 4096
-    W = syn.make_weight(N, K, seed=1001)
-    wq = oracle.quantize_w4(W)
-    xs = {M: syn.make_act(M, K, seed=77 + M + K) for M in MS_DECODE}
-    return oracle, wq, xs, N, K
+    wqs = {}
+    for i, (name, K, N) in enumerate(LAYERS_8B):
+        wqs[name] = oracle.quantize_w4(syn.make_weight(N, K, seed=1000 + i))
+    xs = {(M, K): syn.make_act(M, K, seed=77 + M + K) for M in MS_DECODE for K in {K for _, K, _ in LAYERS_8B}}
+    calls = [(M, name, K, N) for M in MS_DECODE for name, K, N in LAYERS_8B]
+    return oracle, wqs, xs, calls
 
 
 def cpu_baseline(seconds: float = 10.0):
-    """The oracle as it stands, on the host cores, over a bounded sample."""
-    oracle, wq, xs, N, K = _oracle_sample()
+    """The oracle as it stands, on the host cores, over a bounded sample of the
+    decode step (its twelve calls in step order, as many as fit in `seconds`),
+    plus the tiny configuration (M=1, K=N=512) on one core."""
+    from precision_quantized_linear_gb300 import synthetic as syn
+    oracle, wqs, xs, calls = _oracle_sample()
     t0 = time.perf_counter()
-    calls = 0
+    done, wbytes = 0, 0
     while True:
-        for M in MS_DECODE:
-            oracle.w4a16_full(xs[M], wq)
-            calls += 1
-        if time.perf_counter() - t0 >= seconds:
+        M, name, K, N = calls[done % len(calls)]
+        oracle.w4a16_full(xs[(M, K)], wqs[name])
+        done += 1
+        wbytes += w4_weight_bytes(N, K)
+        if time.perf_counter() - t0 >= seconds and done >= len(calls):
             break
     dt = time.perf_counter() - t0
-    return {"value": round(calls * w4_weight_bytes(N, K) / dt / 1e9, 4), "unit": "GB/s",
-            "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "oracle W4A16 GEMM (dequantise + fp64 GEMM) on the o_proj layer K=N=4096 at M=1,4,16, "
-                      "%d calls in %.1f s" % (calls, dt)}
+    cores = oracle.num_threads()
+    # the tiny configuration single-threaded: quantise + pack, then the GEMM
+    oracle.set_num_threads(1)
+    W1 = syn.make_weight(512, 512, seed=0, outlier_frac=0.0)
+    X1 = syn.make_act(1, 512, seed=0)
+    t1 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t1 < 1.0:
+        wq1 = oracle.quantize_w4(W1)
+        oracle.pack_tile(wq1)
+        reps += 1
+    t_pack = (time.perf_counter() - t1) / reps
+    t2 = time.perf_counter()
+    reps2 = 0
+    while time.perf_counter() - t2 < 1.0:
+        oracle.w4a16_full(X1, wq1)
+        reps2 += 1
+    t_gemm = (time.perf_counter() - t2) / reps2
+    oracle.set_num_threads(cores)
+    return {"value": round(wbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "oracle W4A16 GEMM (dequantise + fp64 GEMM) over the decode step's calls in order "
+                      "(4 Llama-3-8B layers x M=1,4,16): %d calls in %.1f s" % (done, dt),
+            "tiny_single_thread": {"config": "M=1 K=N=512 G=128", "cores": 1,
+                                   "quantise_pack_ms": round(t_pack * 1e3, 3), "gemm_ms": round(t_gemm * 1e3, 3),
+                                   "gemm_GFLOPS": round(2 * 512 * 512 / t_gemm / 1e9, 3)}}
 
 
 def run_reference(args):
+    """The oracle as the reference arm: step i runs call i of the decode step
+    (cycling over its twelve calls), a bounded sample of the workload."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    oracle, wq, xs, N, K = _oracle_sample()
-    for _ in range(args.warmup):
-        oracle.w4a16_full(xs[1], wq)
+    oracle, wqs, xs, calls = _oracle_sample()
+    for i in range(args.warmup):
+        M, name, K, N = calls[i % len(calls)]
+        oracle.w4a16_full(xs[(M, K)], wqs[name])
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        for M in MS_DECODE:
-            oracle.w4a16_full(xs[M], wq)
+    wbytes = 0
+    for i in range(args.steps):
+        M, name, K, N = calls[(args.warmup + i) % len(calls)]
+        oracle.w4a16_full(xs[(M, K)], wqs[name])
+        wbytes += w4_weight_bytes(N, K)
     dt = time.perf_counter() - t0
-    value = args.steps * len(MS_DECODE) * w4_weight_bytes(N, K) / dt / 1e9
+    value = wbytes / dt / 1e9
     ms = dt * 1e3 / args.steps
-    sample = "each step: oracle W4A16 GEMM on o_proj K=N=4096 at M=1,4,16 (a bounded sample of the 8B decode set)"
+    sample = ("step i: oracle W4A16 GEMM (dequantise + fp64 GEMM) of call i of the decode step "
+              "(4 Llama-3-8B layers x M=1,4,16, cycled)")
     out = {"impl": "reference", "metric": "quantized-linear weight GB/s (decode) & TFLOPS (prefill) vs batch M, % of roofline",
            "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -487,13 +638,14 @@ def time_launches(launches, reps=10, warm=3):
     return e0.elapsed_time(e1) / (reps * len(launches)) * 1e3   # microseconds
 
 
-def crossover_summary(rows, p16_tf, p8_tf, bw_gbs):
+def crossover_summary(rows, p16_tf, p8_tf, bw_gbs, quant_in_w8=False):
     """Measured W4A16-vs-W8A8 crossover M (W8A8 counted as activation quantisation + GEMM)
     beside the roofline predictions of the arithmetic-intensity argument."""
     out = {"crossover": []}
     for (K, N) in sorted({(r["K"], r["N"]) for r in rows}):
         w4 = {r["M"]: r["us"] for r in rows if (r["K"], r["N"]) == (K, N) and r["variant"] == "w4"}
-        w8 = {r["M"]: r["us"] + r.get("quant_us", 0.0) for r in rows if (r["K"], r["N"]) == (K, N) and r["variant"] == "w8"}
+        w8 = {r["M"]: r["us"] + (0.0 if quant_in_w8 else r.get("quant_us", 0.0))
+              for r in rows if (r["K"], r["N"]) == (K, N) and r["variant"] == "w8"}
         ms = sorted(set(w4) & set(w8))
         measured = next((m for m in ms if w8[m] <= w4[m] and all(w8[x] <= w4[x] for x in ms if x >= m)), None)
 
@@ -688,6 +840,7 @@ def main():
     ap.add_argument("--sweep", default=None, choices=["crossover", "prefill", "70b", "decode", "blocks", "epilogue"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweeps", action="store_true", help="decode line only (no prefill / crossover objects)")
     ap.add_argument("--case", default=None, choices=["w4a16", "w8a8", "w8a8b"])
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--N", type=int, default=28672)

@@ -42,7 +42,10 @@
  * Eligibility ([LP] S24): device sm_103 (compute capability 10.3);
  * G in {32, 64, 128} (the CUDA-core GEMV that serves small M when K % 256 != 0
  * and qlin_w4a16_gemv_noalloc take G = 128 only); N % 128 == 0; K % 128 == 0;
- * 1 <= N, K; 0 <= M <= 2^24.
+ * 1 <= N, K; 0 <= M <= 2^24, and M <= 262140 (4 x 65535 token blocks of its
+ * launch grid) wherever a call runs the CUDA-core GEMV (QLIN_PATH_GEMV with
+ * K % 256 != 0, and qlin_w4a16_gemv_noalloc in that case); larger M returns
+ * QLIN_ERR_UNSUPPORTED_SHAPE there.
  */
 #ifndef QLIN_H
 #define QLIN_H
@@ -87,7 +90,7 @@ typedef enum {
 #define QLIN_PATH_TC 2     /* TMA + tcgen05 tensor-core kernel             */
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char* qlin_status_string(int status);
+const char* qlin_status_string(qlin_status_t status);
 
 /* QLIN_PACK_FORMAT_VERSION of the library that is loaded. */
 int qlin_pack_format_version(void);
@@ -104,9 +107,11 @@ const char* qlin_cuda_error_name(int code);
 /* Byte sizes of the three packed-weight buffers for an [N][K] weight.
  * codes = N*K/2, scales = 2*N*K/G, zeros = N*K/(2G) ([LP] S5: codes + scales
  * give exactly 4 + 16/G bits per weight; the zeros add 4/G). */
-int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros);
+qlin_status_t qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros);
 
-/* Scratch bytes a call of `op` needs for these sizes (0 if none).  The
+/* Scratch bytes a call of `op` needs for these sizes (0 if none).  G is the
+ * W4A16 quantisation group (checked as qlin_w4a16_gemm checks it) for
+ * QLIN_OP_W4A16_GEMM and ignored by the other operations.  The
  * workspace must be zero-filled before its first use with this library and
  * is left zero-filled by every call that completes (split-K counters, the
  * small-M kernel's work-queue word and the partial sums are all cleared by the
@@ -114,7 +119,7 @@ int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* sca
  * turn; calls that share one workspace must not overlap in time (use one per
  * stream).  After a call whose kernel reported a device error (see
  * qlin_get_device_error) its contents are undefined: zero it again. */
-int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes);
+qlin_status_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, int G, size_t* bytes);
 
 /*
  * Quantise and pack BF16 weights W[N][K] ([LP] S2-S5, run once at load).
@@ -137,13 +142,13 @@ int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes);
  *          4p..4p+3.  Word t thus holds what lane t of an mma.sync quad needs
  *          for two 16-column k-steps, and the pair (c, c+1) is the two halves
  *          of (word >> 4(2a + b)) & 0x000F000F.
- *   scales (2*N*K/128 bytes): FP16 of (n, g) at element
- *          ((n/128)*(K/128) + g) * 128 + n%128.
- *   zeros  (N*K/256 bytes): nibble of (n, g) in byte
- *          ((n/128)*(K/128) + g) * 64 + (n%128)/2, low nibble for even n.
- *  Requires G == 128, N % 128 == 0, K % 128 == 0.
+ *   scales (2*N*K/G bytes): FP16 of (n, g) at element
+ *          ((n/128)*(K/G) + g) * 128 + n%128.
+ *   zeros  (N*K/(2G) bytes): nibble of (n, g) in byte
+ *          ((n/128)*(K/G) + g) * 64 + (n%128)/2, low nibble for even n.
+ *  Requires G in {32, 64, 128}, N % 128 == 0, K % 128 == 0.
  */
-int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes,
+qlin_status_t qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes,
                  void* scales_f16, void* zeros_u4, void* stream);
 
 /*
@@ -158,12 +163,12 @@ int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric,
  * are deterministic.  workspace: qlin_workspace_size(QLIN_OP_W4A16_GEMM, ...)
  * bytes (may be NULL when that is 0).
  */
-int qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+qlin_status_t qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                     void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
                     void* stream);
 
 /* Same, with the kernel path forced (QLIN_PATH_*). */
-int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+qlin_status_t qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                        void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
                        int path, void* stream);
 
@@ -174,7 +179,7 @@ int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales
  * 16-byte aligned), act one of QLIN_ACT_*; bias and activation are applied in
  * FP32 and Y is rounded once.  Every kernel path applies it where it writes Y
  * (also after a split-K reduction), so no extra pass over Y is made. */
-int qlin_w4a16_gemm_fused(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+qlin_status_t qlin_w4a16_gemm_fused(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                           void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const void* bias_bf16, int act,
                           void* workspace, size_t ws_bytes, int path, void* stream);
 
@@ -185,7 +190,7 @@ int qlin_w4a16_gemm_fused(const void* X_bf16, const void* codes, const void* sca
  * X[m][k] / sx[m]) with an IEEE binary32 division.  Outputs: Xq [M][K] E4M3
  * bytes, sx [M] FP32.  The scale never leaves the device ([LP] S28).
  */
-int qlin_quant_act_fp8(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream);
+qlin_status_t qlin_quant_act_fp8(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream);
 
 /*
  * Per-tensor FP8 weight quantisation ([LP] S4 per-tensor, S8), run once at
@@ -194,7 +199,7 @@ int qlin_quant_act_fp8(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, 
  * workspace: qlin_workspace_size(QLIN_OP_QUANT_W_FP8, ...) bytes (holds the
  * grid-wide amax).
  */
-int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* workspace,
+qlin_status_t qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* workspace,
                      size_t ws_bytes, void* stream);
 
 /*
@@ -205,17 +210,17 @@ int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, fl
  * otherwise on QLIN_PATH_GEMV), above it TMA + tcgen05 kind::f8f6f4.
  * workspace: qlin_workspace_size(QLIN_OP_W8A8_GEMM, ...) bytes.
  */
-int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+qlin_status_t qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                        void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                        void* stream);
 
-int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+qlin_status_t qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                           void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                           int path, void* stream);
 
 /* W8A8 with the fused output epilogue of qlin_w4a16_gemm_fused:
  * Y[m][n] = bf16( act( (acc[m][n] * sx[m]) * sw + bias[n] ) ). */
-int qlin_w8a8_fp8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+qlin_status_t qlin_w8a8_fp8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                              void* Y_bf16, int64_t M, int64_t N, int64_t K, const void* bias_bf16, int act,
                              void* workspace, size_t ws_bytes, int path, void* stream);
 
@@ -230,11 +235,11 @@ int qlin_w8a8_fp8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* W
 /* X [M][K] BF16 -> Xq [M][K] E4M3 and sx [K/128][M] FP32 (block-major: the
  * scales of one K block of all tokens are contiguous).  K % 128 == 0.  sx
  * 4-byte aligned, X and Xq 16-byte aligned.  Asynchronous, no workspace. */
-int qlin_quant_act_fp8_blocks(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream);
+qlin_status_t qlin_quant_act_fp8_blocks(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream);
 
 /* W [N][K] BF16 -> Wq [N][K] E4M3 and sw [N/128][K/128] FP32 (row-block major).
  * N % 128 == 0, K % 128 == 0.  Asynchronous, no workspace. */
-int qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* stream);
+qlin_status_t qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* stream);
 
 /* Block-scaled W8A8: Y[m][n] = bf16( sum_b sx[b][m] * sw[n/128][b] *
  * sum_{k in block b} Xq[m][k] * Wq[n][k] ), every block's product accumulated
@@ -242,13 +247,13 @@ int qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e
  * sum in block order.  Shapes and alignment as qlin_w8a8_fp8_gemm;
  * workspace: qlin_workspace_size(QLIN_OP_W8A8_BLOCK_GEMM, ...) bytes (0 when the
  * K range is not split), zero-filled, left zero-filled.  Deterministic. */
-int qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                              void* stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QLIN_OK, or the first error a kernel recorded since the last call. */
-int qlin_get_device_error(void* stream);
+qlin_status_t qlin_get_device_error(void* stream);
 
 /* Failure-detection self-test: launches one CTA that waits, with the same
  * bounded mbarrier wait the tensor-core kernels use, on a barrier that nothing
@@ -256,7 +261,7 @@ int qlin_get_device_error(void* stream);
  * and records QLIN_ERR_TIMEOUT in the error word, and the kernel returns; the
  * context stays usable.  Returns the launch status; read the recorded error
  * with qlin_get_device_error().  limit_us must be in 1..1000000. */
-int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
+qlin_status_t qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
 
 /*
  * W4A16 split-K GEMV that allocates nothing (no counterpart on the pages: it
@@ -280,11 +285,42 @@ int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream);
  *    from different threads -- race and must not be issued.
  *  - Calls no cudaMalloc, cudaFree or allocating library routine.
  */
-int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+qlin_status_t qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                             void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* stream);
 
 /* The M at or below which the AUTO path of each GEMM uses the GEMV kernel. */
 int qlin_gemv_max_m(int op);
+
+/* Kernels a GEMM call can launch (qlin_plan_info, info[0]). */
+#define QLIN_KERNEL_W4A16_MMA 1   /* small-M W4A16: register dequantisation + mma.sync, split-K in a cluster */
+#define QLIN_KERNEL_W4A16_GEMV 2  /* small-M W4A16 on the CUDA cores (K % 256 != 0), split-K in the workspace */
+#define QLIN_KERNEL_W4A16_TC 3    /* W4A16 TMA + tcgen05 BF16 MMA */
+#define QLIN_KERNEL_W8A8_MMA 4    /* small-M W8A8: E4M3 mma.sync, split-K in a cluster */
+#define QLIN_KERNEL_W8A8_GEMV 5   /* small-M W8A8 on the CUDA cores (K % 256 != 0) */
+#define QLIN_KERNEL_W8A8_TC 6     /* W8A8 TMA + tcgen05 kind::f8f6f4 */
+#define QLIN_KERNEL_W8A8_BLOCK_TC 7 /* block-scaled W8A8 on tcgen05 with FP32 promotion */
+
+/*
+ * Dispatch query (for tests and measurement tools; launches nothing, reads
+ * no device memory): the kernel and tiling a call of `op`
+ * (QLIN_OP_W4A16_GEMM, QLIN_OP_W8A8_GEMM or QLIN_OP_W8A8_BLOCK_GEMM) with
+ * these sizes and `path` (QLIN_PATH_*; ignored by the block-scaled GEMM)
+ * would launch.  num_sms is the SM count to plan for, 0 for the current
+ * device's (the small-M kernels always read the current device's cluster
+ * occupancy).  Writes 8 values:
+ *   info[0] kernel (QLIN_KERNEL_*)
+ *   info[1] tokens per tile (the MMA's N side; 8 x n8 blocks for mma.sync)
+ *   info[2] weight rows per tile
+ *   info[3] K blocks per pipeline stage (tcgen05 kernels; 1 otherwise)
+ *   info[4] split-K ranges per output tile
+ *   info[5] workspace bytes of that launch
+ *   info[6] 1 when the tcgen05 W4A16 kernel keeps its dequantised BF16 tile in
+ *           tensor memory, 0 when in shared memory (0 for other kernels)
+ *   info[7] token blocks (tiles along M)
+ * The returned status is the one the GEMM call would return for the sizes
+ * (shape, group and path checks); pointers are not checked.
+ */
+qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int path, int num_sms, int64_t* info);
 
 #ifdef __cplusplus
 }

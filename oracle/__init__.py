@@ -98,6 +98,8 @@ def _load():
         lib.orc_w8a8_at.argtypes = [_p, _p, _p, ctypes.c_float, _i64, _i64, _i64,
                                     _p, _p, _i64, _p]
         lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_set_num_threads.restype = None
+        lib.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
         return lib
 
@@ -109,6 +111,11 @@ def _ptr(a: np.ndarray) -> int:
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (n >= 1)."""
+    _load().orc_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- formats

@@ -463,6 +463,18 @@ void orc_w8a8_at(const uint8_t *Xq, const float *sx, const uint8_t *Wq, float sw
     }
 }
 
+/* Thread count of the parallel loops (the CPU baseline times the oracle on
+ * one core as well as on all of them); n <= 0 leaves it unchanged. */
+void orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int orc_num_threads(void)
 {
 #ifdef _OPENMP

@@ -27,11 +27,15 @@ __all__ = [
     "qlin_w8a8_fp8_block_gemm", "OP_W4A16_GEMM", "OP_W8A8_GEMM", "OP_QUANT_W_FP8", "OP_W8A8_BLOCK_GEMM",
     "PATH_AUTO", "PATH_GEMV", "PATH_TC", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU",
     "qlin_w4a16_gemm_fused", "qlin_w8a8_fp8_gemm_fused",
-    "PACK_FORMAT_VERSION",
+    "PACK_FORMAT_VERSION", "qlin_plan_info", "PLAN_FIELDS",
+    "KERNEL_W4A16_MMA", "KERNEL_W4A16_GEMV", "KERNEL_W4A16_TC", "KERNEL_W8A8_MMA", "KERNEL_W8A8_GEMV",
+    "KERNEL_W8A8_TC", "KERNEL_W8A8_BLOCK_TC",
 ]
 
 OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM = 1, 2, 3, 4
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+(KERNEL_W4A16_MMA, KERNEL_W4A16_GEMV, KERNEL_W4A16_TC, KERNEL_W8A8_MMA, KERNEL_W8A8_GEMV, KERNEL_W8A8_TC,
+ KERNEL_W8A8_BLOCK_TC) = 1, 2, 3, 4, 5, 6, 7
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = 0, 1, 2, 3
 PACK_FORMAT_VERSION = 2
 
@@ -50,7 +54,8 @@ _SIGS = {
     "qlin_cuda_error_name": [_int],
     "qlin_gemv_max_m": [_int],
     "qlin_w4_packed_sizes": [_i64, _i64, _int, ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
-    "qlin_workspace_size": [_int, _i64, _i64, _i64, ctypes.POINTER(_sz)],
+    "qlin_workspace_size": [_int, _i64, _i64, _i64, _int, ctypes.POINTER(_sz)],
+    "qlin_plan_info": [_int, _i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(_i64)],
     "qlin_pack_w4": [_p, _i64, _i64, _int, _int, _p, _p, _p, _p],
     "qlin_w4a16_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _sz, _p],
     "qlin_w4a16_gemm_ex": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _sz, _int, _p],
@@ -156,10 +161,21 @@ def qlin_w4_packed_sizes(N: int, K: int, G: int = 128):
     return a.value, b.value, c.value
 
 
-def qlin_workspace_size(op: int, M: int, N: int, K: int) -> int:
+def qlin_workspace_size(op: int, M: int, N: int, K: int, G: int = 128) -> int:
     b = _sz()
-    _check(load().qlin_workspace_size(op, M, N, K, ctypes.byref(b)), "qlin_workspace_size")
+    _check(load().qlin_workspace_size(op, M, N, K, G, ctypes.byref(b)), "qlin_workspace_size")
     return b.value
+
+
+PLAN_FIELDS = ("kernel", "tokens_per_tile", "rows_per_tile", "kblocks_per_stage", "splits", "ws_bytes",
+               "a_in_tmem", "token_blocks")
+
+
+def qlin_plan_info(op: int, M: int, N: int, K: int, G: int = 128, path: int = 0, num_sms: int = 0) -> dict:
+    """Kernel and tiling a GEMM call would launch (launches nothing): a dict of PLAN_FIELDS."""
+    info = (_i64 * 8)()
+    _check(load().qlin_plan_info(op, M, N, K, G, path, num_sms, info), "qlin_plan_info")
+    return dict(zip(PLAN_FIELDS, (int(v) for v in info)))
 
 
 def qlin_pack_w4(W, N, K, G, symmetric, codes, scales, zeros, stream=None):

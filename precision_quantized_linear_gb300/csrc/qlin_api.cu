@@ -21,7 +21,7 @@ __device__ int g_error_word;
 
 struct DeviceState {
   bool ready = false;
-  int status = QLIN_OK;
+  qlin_status_t status = QLIN_OK;
   int num_sms = 0;
   int* err = nullptr;  // device address of g_error_word on this device
 };
@@ -30,7 +30,7 @@ static DeviceState g_dev[kMaxDevices];
 static std::mutex g_mu;
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-static int device_state(DeviceState** out) {
+static qlin_status_t device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QLIN_ERR_CUDA;
   DeviceState& d = g_dev[dev];
@@ -68,9 +68,9 @@ static int device_state(DeviceState** out) {
   return d.status;
 }
 
-int device_num_sms(int* out) {
+qlin_status_t device_num_sms(int* out) {
   DeviceState* d = nullptr;
-  const int st = device_state(&d);
+  const qlin_status_t st = device_state(&d);
   if (st == QLIN_OK) *out = d->num_sms;
   return st;
 }
@@ -123,7 +123,7 @@ using namespace qlin;
 
 static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static int check_shape(int64_t M, int64_t N, int64_t K) {
+static qlin_status_t check_shape(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || M > kMaxM || N <= 0 || K <= 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
   if (N % kTileN != 0 || K % kGroup != 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
   if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
@@ -134,7 +134,7 @@ static int check_shape(int64_t M, int64_t N, int64_t K) {
 static thread_local int g_last_cuda_error = 0;
 
 namespace qlin {
-int cuda_status(cudaError_t e) {
+qlin_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return QLIN_OK;
   g_last_cuda_error = static_cast<int>(e);
   (void)cudaGetLastError();  // a launch error must not be reported again by the next call
@@ -142,13 +142,13 @@ int cuda_status(cudaError_t e) {
 }
 }  // namespace qlin
 
-static int launch_status(cudaError_t e) { return cuda_status(e); }
+static qlin_status_t launch_status(cudaError_t e) { return cuda_status(e); }
 
 // W4A16 quantisation groups the kernels take ([LP] S4 per-group, S5 b_eff = 4 + 16 / G)
 static bool group_ok(int G) { return G == 32 || G == 64 || G == 128; }
 
 // Validated output epilogue of the *_fused calls.
-static int make_epi(const void* bias_bf16, int act, Epi* epi) {
+static qlin_status_t make_epi(const void* bias_bf16, int act, Epi* epi) {
   if (act < QLIN_ACT_NONE || act > QLIN_ACT_GELU) return QLIN_ERR_INVALID_VALUE;
   if (bias_bf16 && !aligned16(bias_bf16)) return QLIN_ERR_MISALIGNED;
   epi->bias = static_cast<const uint16_t*>(bias_bf16);
@@ -158,7 +158,7 @@ static int make_epi(const void* bias_bf16, int act, Epi* epi) {
 
 extern "C" {
 
-const char* qlin_status_string(int status) {
+const char* qlin_status_string(qlin_status_t status) {
   switch (status) {
     case QLIN_OK: return "QLIN_OK";
     case QLIN_ERR_INVALID_VALUE: return "QLIN_ERR_INVALID_VALUE";
@@ -180,10 +180,10 @@ const char* qlin_cuda_error_name(int code) { return cudaGetErrorName(static_cast
 
 int qlin_gemv_max_m(int op) { return op == QLIN_OP_W8A8_GEMM ? g_gemv_max_m_w8 : g_gemv_max_m_w4; }
 
-int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros) {
+qlin_status_t qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros) {
   if (!codes || !scales || !zeros) return QLIN_ERR_INVALID_VALUE;
   if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
-  int st = check_shape(0, N, K);
+  qlin_status_t st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   *codes = static_cast<size_t>(N * K / 2);
   *scales = static_cast<size_t>(N * (K / G) * 2);
@@ -191,8 +191,61 @@ int qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* sca
   return QLIN_OK;
 }
 
-static size_t ws_w4(int64_t M, int64_t N, int64_t K, int sms) {
-  size_t a = mma_path_ok(M, K) ? plan_w4a16_mma(M, N, K, sms).ws_bytes : plan_w4a16_gemv(M, N, K, sms).ws_bytes;
+// Which kernel and plan a W4A16 / W8A8 GEMM call launches.  The launch path
+// and qlin_plan_info both use these, so that the query reports what runs.
+struct Dispatch {
+  int kernel = 0;  // QLIN_KERNEL_*
+  SplitPlan sp;    // small-M kernels
+  TcPlan tp;       // tcgen05 kernels
+  size_t ws = 0;   // workspace bytes of the launch
+};
+
+static qlin_status_t dispatch_w4(int64_t M, int64_t N, int64_t K, int G, int path, int sms, Dispatch* d) {
+  if (path == QLIN_PATH_AUTO) path = M <= g_gemv_max_m_w4 ? QLIN_PATH_GEMV : QLIN_PATH_TC;
+  if (path == QLIN_PATH_GEMV) {
+    if (mma_path_ok(M, K)) {
+      d->kernel = QLIN_KERNEL_W4A16_MMA;
+      d->sp = plan_w4a16_mma(M, N, K, sms, G);
+      d->ws = d->sp.ws_bytes;
+      return QLIN_OK;
+    }
+    if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;  // the CUDA-core GEMV takes G = 128 only
+    if (!gemv_m_ok(M)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+    d->kernel = QLIN_KERNEL_W4A16_GEMV;
+    d->sp = plan_w4a16_gemv(M, N, K, sms);
+    d->ws = d->sp.ws_bytes;
+    return QLIN_OK;
+  }
+  d->kernel = QLIN_KERNEL_W4A16_TC;
+  d->tp = plan_w4a16_tc(M, N, K, sms);
+  d->ws = d->tp.split.ws_bytes;
+  return QLIN_OK;
+}
+
+static qlin_status_t dispatch_w8(int64_t M, int64_t N, int64_t K, int path, int sms, Dispatch* d) {
+  if (path == QLIN_PATH_AUTO) path = M <= g_gemv_max_m_w8 ? QLIN_PATH_GEMV : QLIN_PATH_TC;
+  if (path == QLIN_PATH_GEMV) {
+    if (mma8_path_ok(M, K)) {  // register-level E4M3 MMA; split-K inside clusters, no workspace
+      d->kernel = QLIN_KERNEL_W8A8_MMA;
+      d->sp = plan_w8a8_mma(M, N, K, sms);
+      d->ws = 0;
+      return QLIN_OK;
+    }
+    if (!gemv_m_ok(M)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+    d->kernel = QLIN_KERNEL_W8A8_GEMV;
+    d->sp = plan_w8a8_gemv(M, N, K, sms);
+    d->ws = d->sp.ws_bytes;
+    return QLIN_OK;
+  }
+  d->kernel = QLIN_KERNEL_W8A8_TC;
+  d->tp = plan_w8a8_tc(M, N, K, sms);
+  d->ws = d->tp.split.ws_bytes;
+  return QLIN_OK;
+}
+
+// Workspace of any path the AUTO or forced calls may take for these sizes.
+static size_t ws_w4(int64_t M, int64_t N, int64_t K, int G, int sms) {
+  size_t a = mma_path_ok(M, K) ? plan_w4a16_mma(M, N, K, sms, G).ws_bytes : plan_w4a16_gemv(M, N, K, sms).ws_bytes;
   const size_t b = plan_w4a16_tc(M, N, K, sms).split.ws_bytes;
   return a > b ? a : b;
 }
@@ -202,15 +255,18 @@ static size_t ws_w8(int64_t M, int64_t N, int64_t K, int sms) {
   return a > b ? a : b;
 }
 
-int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes) {
+qlin_status_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, int G, size_t* bytes) {
   if (!bytes) return QLIN_ERR_INVALID_VALUE;
   DeviceState* d = nullptr;
-  int st = device_state(&d);
+  qlin_status_t st = device_state(&d);
   if (st != QLIN_OK) return st;
   st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   switch (op) {
-    case QLIN_OP_W4A16_GEMM: *bytes = M == 0 ? 0 : ws_w4(M, N, K, d->num_sms); return QLIN_OK;
+    case QLIN_OP_W4A16_GEMM:
+      if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+      *bytes = M == 0 ? 0 : ws_w4(M, N, K, G, d->num_sms);
+      return QLIN_OK;
     case QLIN_OP_W8A8_GEMM: *bytes = M == 0 ? 0 : ws_w8(M, N, K, d->num_sms); return QLIN_OK;
     case QLIN_OP_QUANT_W_FP8: *bytes = 256; return QLIN_OK;
     case QLIN_OP_W8A8_BLOCK_GEMM:
@@ -220,10 +276,61 @@ int qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes) 
   }
 }
 
-int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes, void* scales_f16,
+qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int path, int num_sms, int64_t* info) {
+  if (!info || num_sms < 0) return QLIN_ERR_INVALID_VALUE;
+  if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;
+  qlin_status_t st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_ERR_UNSUPPORTED_SHAPE;  // an empty call launches nothing
+  if (num_sms == 0) {
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != QLIN_OK) return st;
+    num_sms = d->num_sms;
+  }
+  Dispatch dp;
+  if (op == QLIN_OP_W4A16_GEMM) {
+    if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+    st = dispatch_w4(M, N, K, G, path, num_sms, &dp);
+  } else if (op == QLIN_OP_W8A8_GEMM) {
+    st = dispatch_w8(M, N, K, path, num_sms, &dp);
+  } else if (op == QLIN_OP_W8A8_BLOCK_GEMM) {
+    dp.kernel = QLIN_KERNEL_W8A8_BLOCK_TC;
+    dp.tp = plan_w8a8_block_tc(M, N, K, num_sms);
+    dp.ws = dp.tp.split.ws_bytes;
+  } else {
+    return QLIN_ERR_INVALID_VALUE;
+  }
+  if (st != QLIN_OK) return st;
+  for (int i = 0; i < 8; ++i) info[i] = 0;
+  info[0] = dp.kernel;
+  const bool tc = dp.kernel == QLIN_KERNEL_W4A16_TC || dp.kernel == QLIN_KERNEL_W8A8_TC ||
+                  dp.kernel == QLIN_KERNEL_W8A8_BLOCK_TC;
+  if (tc) {
+    info[1] = dp.tp.bn;
+    info[2] = dp.tp.wn;
+    info[3] = dp.tp.kps;
+    info[4] = dp.tp.split.splits;
+    info[6] = dp.kernel == QLIN_KERNEL_W4A16_TC && dp.tp.bn <= 128 ? 1 : 0;
+    info[7] = dp.tp.mblocks;
+  } else {
+    const int64_t tok = (dp.kernel == QLIN_KERNEL_W4A16_MMA || dp.kernel == QLIN_KERNEL_W8A8_MMA)
+                            ? (M <= 8 ? 8 : M <= 16 ? 16 : 32)
+                            : (M >= 4 ? 4 : M >= 2 ? 2 : 1);
+    info[1] = tok;
+    info[2] = kTileN;
+    info[3] = 1;
+    info[4] = dp.sp.splits;
+    info[7] = (M + tok - 1) / tok;
+  }
+  info[5] = static_cast<int64_t>(dp.ws);
+  return QLIN_OK;
+}
+
+qlin_status_t qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes, void* scales_f16,
                  void* zeros_u4, void* stream) {
   if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
-  int st = check_shape(0, N, K);
+  qlin_status_t st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   if (symmetric != 0 && symmetric != 1) return QLIN_ERR_INVALID_VALUE;
   if (!W_bf16 || !codes || !scales_f16 || !zeros_u4) return QLIN_ERR_INVALID_VALUE;
@@ -238,11 +345,11 @@ int qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric,
                                       static_cast<cudaStream_t>(stream)));
 }
 
-static int w4a16_impl(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+static qlin_status_t w4a16_impl(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                       void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const Epi& epi, void* workspace,
                       size_t ws_bytes, int path, void* stream) {
   if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
-  int st = check_shape(M, N, K);
+  qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;
   if (M == 0) return QLIN_OK;
@@ -253,67 +360,64 @@ static int w4a16_impl(const void* X_bf16, const void* codes, const void* scales_
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != QLIN_OK) return st;
-  if (path == QLIN_PATH_AUTO) path = M <= g_gemv_max_m_w4 ? QLIN_PATH_GEMV : QLIN_PATH_TC;
+  Dispatch dp;
+  st = dispatch_w4(M, N, K, G, path, d->num_sms, &dp);
+  if (st != QLIN_OK) return st;
+  if (dp.ws > 0 && (!workspace || ws_bytes < dp.ws)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
   const auto* X = static_cast<const uint16_t*>(X_bf16);
   const auto* c = static_cast<const uint8_t*>(codes);
   const auto* s = static_cast<const uint16_t*>(scales_f16);
   const auto* z = static_cast<const uint8_t*>(zeros_u4);
   auto* Y = static_cast<uint16_t*>(Y_bf16);
   auto cs = static_cast<cudaStream_t>(stream);
-  if (path == QLIN_PATH_GEMV) {
-    if (mma_path_ok(M, K)) {
-      const SplitPlan p = plan_w4a16_mma(M, N, K, d->num_sms, G);
-      if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-      return launch_status(launch_w4a16_mma(X, c, s, z, Y, M, N, K, G, p, workspace, d->err, cs, epi));
-    }
-    if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;  // the CUDA-core GEMV takes G = 128 only
-    const SplitPlan p = plan_w4a16_gemv(M, N, K, d->num_sms);
-    if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-    return launch_status(launch_w4a16_gemv(X, c, s, z, Y, M, N, K, p, workspace, cs, epi));
+  switch (dp.kernel) {
+    case QLIN_KERNEL_W4A16_MMA:
+      return launch_status(launch_w4a16_mma(X, c, s, z, Y, M, N, K, G, dp.sp, workspace, d->err, cs, epi));
+    case QLIN_KERNEL_W4A16_GEMV:
+      return launch_status(launch_w4a16_gemv(X, c, s, z, Y, M, N, K, dp.sp, workspace, cs, epi));
+    default:
+      return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, G, dp.tp, workspace, d->err, d->num_sms, cs, epi));
   }
-  const TcPlan p = plan_w4a16_tc(M, N, K, d->num_sms);
-  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_w4a16_tc(X, c, s, z, Y, M, N, K, G, p, workspace, d->err, d->num_sms, cs, epi));
 }
 
-int qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+qlin_status_t qlin_w4a16_gemm_ex(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                        void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
                        int path, void* stream) {
   return w4a16_impl(X_bf16, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, Epi{}, workspace, ws_bytes, path,
                     stream);
 }
 
-int qlin_w4a16_gemm_fused(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+qlin_status_t qlin_w4a16_gemm_fused(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                           void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const void* bias_bf16, int act,
                           void* workspace, size_t ws_bytes, int path, void* stream) {
   Epi epi;
-  const int st = make_epi(bias_bf16, act, &epi);
+  const qlin_status_t st = make_epi(bias_bf16, act, &epi);
   if (st != QLIN_OK) return st;
   return w4a16_impl(X_bf16, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, epi, workspace, ws_bytes, path, stream);
 }
 
-int qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
+qlin_status_t qlin_w4a16_gemm(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                     void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, void* workspace, size_t ws_bytes,
                     void* stream) {
   return qlin_w4a16_gemm_ex(X_bf16, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, workspace, ws_bytes,
                             QLIN_PATH_AUTO, stream);
 }
 
-int qlin_quant_act_fp8(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream) {
+qlin_status_t qlin_quant_act_fp8(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream) {
   if (M < 0 || M > kMaxM || K <= 0 || K % kGroup != 0 || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return QLIN_OK;
   if (!X_bf16 || !Xq_e4m3 || !sx) return QLIN_ERR_INVALID_VALUE;
   if (!aligned16(X_bf16) || !aligned16(Xq_e4m3) || !aligned16(sx)) return QLIN_ERR_MISALIGNED;
   DeviceState* d = nullptr;
-  int st = device_state(&d);
+  qlin_status_t st = device_state(&d);
   if (st != QLIN_OK) return st;
   return launch_status(launch_quant_act_fp8(static_cast<const uint16_t*>(X_bf16), M, K,
                                             static_cast<uint8_t*>(Xq_e4m3), sx, static_cast<cudaStream_t>(stream)));
 }
 
-int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* workspace,
+qlin_status_t qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* workspace,
                      size_t ws_bytes, void* stream) {
-  int st = check_shape(0, N, K);
+  qlin_status_t st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   if (!W_bf16 || !Wq_e4m3 || !sw || !workspace) return QLIN_ERR_INVALID_VALUE;
   if (!aligned16(W_bf16) || !aligned16(Wq_e4m3) || !aligned16(sw) || !aligned16(workspace))
@@ -327,10 +431,10 @@ int qlin_quant_w_fp8(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, fl
                                           static_cast<cudaStream_t>(stream)));
 }
 
-static int w8a8_impl(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
+static qlin_status_t w8a8_impl(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
                      int64_t M, int64_t N, int64_t K, const Epi& epi, void* workspace, size_t ws_bytes, int path,
                      void* stream) {
-  int st = check_shape(M, N, K);
+  qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;
   if (M == 0) return QLIN_OK;
@@ -341,61 +445,59 @@ static int w8a8_impl(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, 
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != QLIN_OK) return st;
-  if (path == QLIN_PATH_AUTO) path = M <= g_gemv_max_m_w8 ? QLIN_PATH_GEMV : QLIN_PATH_TC;
+  Dispatch dp;
+  st = dispatch_w8(M, N, K, path, d->num_sms, &dp);
+  if (st != QLIN_OK) return st;
+  if (dp.ws > 0 && (!workspace || ws_bytes < dp.ws)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
   const auto* xq = static_cast<const uint8_t*>(Xq_e4m3);
   const auto* wq = static_cast<const uint8_t*>(Wq_e4m3);
   auto* Y = static_cast<uint16_t*>(Y_bf16);
   auto cs = static_cast<cudaStream_t>(stream);
-  if (path == QLIN_PATH_GEMV) {
-    if (mma8_path_ok(M, K)) {  // register-level E4M3 MMA; split-K inside clusters, no workspace
-      const SplitPlan p = plan_w8a8_mma(M, N, K, d->num_sms);
-      return launch_status(launch_w8a8_mma(xq, sx, wq, sw, Y, M, N, K, p, d->err, cs, epi));
-    }
-    const SplitPlan p = plan_w8a8_gemv(M, N, K, d->num_sms);
-    if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-    return launch_status(launch_w8a8_gemv(xq, sx, wq, sw, Y, M, N, K, p, workspace, cs, epi));
+  switch (dp.kernel) {
+    case QLIN_KERNEL_W8A8_MMA: return launch_status(launch_w8a8_mma(xq, sx, wq, sw, Y, M, N, K, dp.sp, d->err, cs, epi));
+    case QLIN_KERNEL_W8A8_GEMV:
+      return launch_status(launch_w8a8_gemv(xq, sx, wq, sw, Y, M, N, K, dp.sp, workspace, cs, epi));
+    default:
+      return launch_status(launch_w8a8_tc(xq, sx, wq, sw, Y, M, N, K, dp.tp, workspace, d->err, d->num_sms, cs, epi));
   }
-  const TcPlan p = plan_w8a8_tc(M, N, K, d->num_sms);
-  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_w8a8_tc(xq, sx, wq, sw, Y, M, N, K, p, workspace, d->err, d->num_sms, cs, epi));
 }
 
-int qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
+qlin_status_t qlin_w8a8_fp8_gemm_ex(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
                           int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, int path,
                           void* stream) {
   return w8a8_impl(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, Epi{}, workspace, ws_bytes, path, stream);
 }
 
-int qlin_w8a8_fp8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+qlin_status_t qlin_w8a8_fp8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                              void* Y_bf16, int64_t M, int64_t N, int64_t K, const void* bias_bf16, int act,
                              void* workspace, size_t ws_bytes, int path, void* stream) {
   Epi epi;
-  const int st = make_epi(bias_bf16, act, &epi);
+  const qlin_status_t st = make_epi(bias_bf16, act, &epi);
   if (st != QLIN_OK) return st;
   return w8a8_impl(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, epi, workspace, ws_bytes, path, stream);
 }
 
-int qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
+qlin_status_t qlin_w8a8_fp8_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw, void* Y_bf16,
                        int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, void* stream) {
   return qlin_w8a8_fp8_gemm_ex(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, workspace, ws_bytes, QLIN_PATH_AUTO,
                                stream);
 }
 
-int qlin_quant_act_fp8_blocks(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream) {
+qlin_status_t qlin_quant_act_fp8_blocks(const void* X_bf16, int64_t M, int64_t K, void* Xq_e4m3, float* sx, void* stream) {
   if (M < 0 || M > kMaxM || K <= 0 || K % kGroup != 0 || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return QLIN_OK;
   if (!X_bf16 || !Xq_e4m3 || !sx) return QLIN_ERR_INVALID_VALUE;
   if (!aligned16(X_bf16) || !aligned16(Xq_e4m3) || (reinterpret_cast<uintptr_t>(sx) & 3u)) return QLIN_ERR_MISALIGNED;
   DeviceState* d = nullptr;
-  int st = device_state(&d);
+  qlin_status_t st = device_state(&d);
   if (st != QLIN_OK) return st;
   return launch_status(launch_quant_act_fp8_blocks(static_cast<const uint16_t*>(X_bf16), M, K,
                                                    static_cast<uint8_t*>(Xq_e4m3), sx,
                                                    static_cast<cudaStream_t>(stream)));
 }
 
-int qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* stream) {
-  int st = check_shape(0, N, K);
+qlin_status_t qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e4m3, float* sw, void* stream) {
+  qlin_status_t st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   if (!W_bf16 || !Wq_e4m3 || !sw) return QLIN_ERR_INVALID_VALUE;
   if (!aligned16(W_bf16) || !aligned16(Wq_e4m3) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return QLIN_ERR_MISALIGNED;
@@ -406,10 +508,10 @@ int qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, void* Wq_e
                                                  static_cast<uint8_t*>(Wq_e4m3), sw, static_cast<cudaStream_t>(stream)));
 }
 
-int qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                              void* stream) {
-  int st = check_shape(M, N, K);
+  qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (M == 0) return QLIN_OK;
   if (!Xq_e4m3 || !sx || !Wq_e4m3 || !sw || !Y_bf16) return QLIN_ERR_INVALID_VALUE;
@@ -427,18 +529,18 @@ int qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* W
                                             static_cast<cudaStream_t>(stream)));
 }
 
-int qlin_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+qlin_status_t qlin_selftest_wait_timeout(uint32_t limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return QLIN_ERR_INVALID_VALUE;
   DeviceState* d = nullptr;
-  int st = device_state(&d);
+  qlin_status_t st = device_state(&d);
   if (st != QLIN_OK) return st;
   return launch_status(launch_wait_timeout(static_cast<uint64_t>(limit_us) * 1000ull, d->err,
                                            static_cast<cudaStream_t>(stream)));
 }
 
-int qlin_get_device_error(void* stream) {
+qlin_status_t qlin_get_device_error(void* stream) {
   DeviceState* d = nullptr;
-  int st = device_state(&d);
+  qlin_status_t st = device_state(&d);
   if (st != QLIN_OK) return st;
   auto cs = static_cast<cudaStream_t>(stream);
   st = cuda_status(cudaStreamSynchronize(cs));
@@ -449,7 +551,7 @@ int qlin_get_device_error(void* stream) {
   const int zero = 0;
   st = cuda_status(cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice));
   if (st != QLIN_OK) return st;
-  return word;
+  return static_cast<qlin_status_t>(word);
 }
 
 }  // extern "C"

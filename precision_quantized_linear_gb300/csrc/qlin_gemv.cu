@@ -246,6 +246,8 @@ static size_t w4_gemv_smem(int mt, int kb_per_split) {
 
 static int gemv_mt(int64_t M) { return M >= 4 ? 4 : (M >= 2 ? 2 : 1); }
 
+bool gemv_m_ok(int64_t M) { return (M + gemv_mt(M) - 1) / gemv_mt(M) <= 65535; }
+
 // Split so that about two CTAs per SM stream weights, with x for one K range
 // of at most 8192/MT columns in shared memory.
 static SplitPlan plan_splits(int64_t tiles_mn, int64_t KB, int num_sms, int max_kb) {

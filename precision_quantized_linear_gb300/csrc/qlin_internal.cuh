@@ -87,7 +87,7 @@ struct SplitPlan {
 cudaError_t set_smem_once_impl(const void* kernel, int bytes, bool wide_clusters);
 // QLIN_OK for cudaSuccess; otherwise records e for qlin_last_cuda_error(),
 // clears the runtime's last-error state and returns QLIN_ERR_CUDA.
-int cuda_status(cudaError_t e);
+qlin_status_t cuda_status(cudaError_t e);
 // wide_clusters: also allow thread-block clusters of up to 16 CTAs.
 template <typename F>
 inline cudaError_t set_smem_once(F* kernel, int bytes, bool wide_clusters = false) {
@@ -105,6 +105,9 @@ cudaError_t launch_quant_w_fp8(const uint16_t* W, int64_t N, int64_t K, uint8_t*
                                int num_sms, cudaStream_t st);
 
 SplitPlan plan_w4a16_gemv(int64_t M, int64_t N, int64_t K, int num_sms);
+// The CUDA-core GEMVs launch one grid row per block of up to four tokens:
+// at most 65535 of them.
+bool gemv_m_ok(int64_t M);
 cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
                               uint16_t* Y, int64_t M, int64_t N, int64_t K, const SplitPlan& plan, void* ws,
                               cudaStream_t st, const Epi& epi = Epi{});
@@ -161,7 +164,7 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, int* err, cudaStream_t st);
 
 // SM count of the current device after the library's device checks
 // (returns a qlin status).
-int device_num_sms(int* out);
+qlin_status_t device_num_sms(int* out);
 // Device address of the current device's error word (valid after device_num_sms succeeded).
 int* device_error_word();
 

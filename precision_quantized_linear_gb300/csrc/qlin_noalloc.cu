@@ -23,7 +23,7 @@ static void* g_noalloc_ptr[64] = {};
 // Device address of the scratch array on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address must come from
 // cudaGetSymbolAddress, called once per device with that device current.
-static int noalloc_scratch(void** out) {
+static qlin_status_t noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QLIN_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -40,7 +40,7 @@ static int noalloc_scratch(void** out) {
 
 using namespace qlin;
 
-extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, const void* scales_f16,
+extern "C" qlin_status_t qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, const void* scales_f16,
                                        const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
                                        void* stream) {
   if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
@@ -54,10 +54,11 @@ extern "C" int qlin_w4a16_gemv_noalloc(const void* X_bf16, const void* codes, co
                       reinterpret_cast<uintptr_t>(Y_bf16);
   if (a & 15u) return QLIN_ERR_MISALIGNED;
   int num_sms = 0;
-  int st = device_num_sms(&num_sms);
+  qlin_status_t st = device_num_sms(&num_sms);
   if (st != QLIN_OK) return st;
   // same kernel choice as qlin_w4a16_gemm_ex(..., QLIN_PATH_GEMV, ...)
   const bool mma = mma_path_ok(M, K);
+  if (!mma && !gemv_m_ok(M)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   const SplitPlan plan = mma ? plan_w4a16_mma(M, N, K, num_sms) : plan_w4a16_gemv(M, N, K, num_sms);
   if (plan.ws_bytes > kNoAllocScratchBytes) return QLIN_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;

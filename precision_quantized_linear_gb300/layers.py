@@ -69,7 +69,7 @@ class W4A16Linear:
         M = X_bf16.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=X_bf16.device)
-        buf, nb = self.ws.get(qlin_workspace_size(OP_W4A16_GEMM, M, self.N, self.K))
+        buf, nb = self.ws.get(qlin_workspace_size(OP_W4A16_GEMM, M, self.N, self.K, self.G))
         if self.bias is None and act == ACT_NONE:
             qlin_w4a16_gemm_ex(_as_u16(X_bf16), self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N,
                                self.K, self.G, buf, nb, path, stream)

@@ -90,3 +90,39 @@ def test_fp8_and_pack_reject_bad_arguments(lib):
     assert lib.qlin_pack_w4(16, 128, 128, 128, 2, 16, 16, 16, None) == 1
     assert lib.qlin_pack_w4(16, 128, 128, 48, 0, 16, 16, 16, None) == 2
     assert lib.qlin_quant_w_fp8(16, 128, 128, 16, 16, None, 0, None) == 1
+
+
+# The dispatch query plans without a device when given an SM count.
+def test_plan_query_without_device(lib):
+    p = q.qlin_plan_info(q.OP_W4A16_GEMM, 2048, 28672, 4096, 128, q.PATH_TC, 152)
+    assert p["kernel"] == q.KERNEL_W4A16_TC and p["tokens_per_tile"] == 256 and p["a_in_tmem"] == 0
+    assert p["token_blocks"] == 8 and p["splits"] == 1 and p["ws_bytes"] == 0
+    p = q.qlin_plan_info(q.OP_W4A16_GEMM, 128, 14336, 4096, 128, q.PATH_TC, 152)
+    assert p["tokens_per_tile"] == 128 and p["a_in_tmem"] == 1
+    p = q.qlin_plan_info(q.OP_W8A8_GEMM, 8192, 4096, 14336, 128, q.PATH_AUTO, 152)
+    assert p["kernel"] == q.KERNEL_W8A8_TC and p["tokens_per_tile"] == 256
+    p = q.qlin_plan_info(q.OP_W8A8_BLOCK_GEMM, 256, 28672, 4096, 128, q.PATH_AUTO, 152)
+    assert p["kernel"] == q.KERNEL_W8A8_BLOCK_TC and p["rows_per_tile"] == 256
+    # a split K range always has a workspace of counters + FP32 partial sums
+    p = q.qlin_plan_info(q.OP_W4A16_GEMM, 64, 4096, 14336, 128, q.PATH_TC, 152)
+    tiles = (4096 // 128) * p["token_blocks"]
+    assert p["splits"] > 1 and p["ws_bytes"] == (tiles * 4 + 255) // 256 * 256 + 4 * p["splits"] * 64 * 4096
+    # the CUDA-core GEMV (K % 256 != 0) keeps its split-K sums in the workspace
+    p = q.qlin_plan_info(q.OP_W4A16_GEMM, 4, 6144, 4224, 128, q.PATH_GEMV, 152)
+    assert p["kernel"] == q.KERNEL_W4A16_GEMV and p["splits"] > 1 and p["ws_bytes"] > 0
+
+
+def test_plan_query_rejects_what_the_call_rejects(lib):
+    info = (ctypes.c_int64 * 8)()
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4, 100, 4096, 128, 0, 152, info) == 2     # N % 128
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4, 128, 4096, 48, 0, 152, info) == 2      # G
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4, 128, 4096, 128, 5, 152, info) == 1     # path
+    assert lib.qlin_plan_info(99, 4, 128, 4096, 128, 0, 152, info) == 1                  # op
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 0, 128, 4096, 128, 0, 152, info) == 2     # empty call
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4, 128, 4096, 128, 0, 152, None) == 1
+    # the CUDA-core GEMVs launch one grid row per 4 tokens: at most 65535 rows
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4 * 65535, 128, 4224, 128, q.PATH_GEMV, 152, info) == 0
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4 * 65535 + 1, 128, 4224, 128, q.PATH_GEMV, 152, info) == 2
+    assert lib.qlin_plan_info(q.OP_W8A8_GEMM, 4 * 65535 + 1, 128, 4224, 128, q.PATH_GEMV, 152, info) == 2
+    # G = 32 / 64 are tensor-core only when K % 256 != 0
+    assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4, 128, 4224, 64, q.PATH_GEMV, 152, info) == 2

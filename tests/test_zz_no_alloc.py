@@ -3,10 +3,18 @@
 Some callers cannot allocate device memory when they run a layer (a runtime
 that forbids allocation after start-up, code inside a memory pool it does not
 own, a host with a fixed footprint).  qlin_w4a16_gemv_noalloc serves them with
-a fixed scratch array inside the library instead of a caller workspace.  This
-file checks, through the C ABI, that two calls in a row give the same output
-as the workspace-taking GEMV, within the parity tolerance used everywhere
-else.  It is collected last so that a stop-at-first-failure run has already
+a fixed scratch array inside the library instead of a caller workspace.
+
+The array is only used when the call runs the CUDA-core GEMV (K % 256 != 0)
+with its K range split: the cases below are chosen so, and the dispatch query
+confirms it (split count > 1 and a non-zero workspace that the array stands in
+for).  Each output is compared with the oracle element by element and, bit
+for bit, with the workspace-taking call (the same kernel with the same split
+order).  Different shapes run back to back, twice each, so every call finds the
+array holding the previous call's counters and partial sums.  The K % 256 == 0
+cases run the tensor-core small-M kernel, which needs no scratch at all.
+
+This file is collected last, so that a stop-at-first-failure run has already
 run every other test; it also passes alone in a fresh process.
 """
 import numpy as np
@@ -18,38 +26,65 @@ import precision_quantized_linear_gb300 as q
 from precision_quantized_linear_gb300 import synthetic as syn
 from precision_quantized_linear_gb300.layers import W4A16Linear
 
+from _parity import check_w4, host_f64, to_dev
+
 pytestmark = pytest.mark.gpu
 
-TOL = 2e-3
+# (M, N, K): K % 256 != 0 -> CUDA-core GEMV with its partial sums in the array
+SCRATCH_CASES = [(1, 4096, 4224), (4, 6144, 4224), (16, 4096, 4224), (3, 512, 4224)]
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (4, 4096, 14336), (16, 28672, 4096), (3, 512, 512)])
-def test_noalloc_matches_workspace_gemv(M, N, K):
+def _need_gpu():
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     q.build()
-    Wh = syn.make_weight(N, K, seed=M + N)
-    Xh = syn.make_act(M, K, seed=M + K + 1)
-    W = torch.from_numpy(Wh.view(np.int16)).cuda()
-    X = torch.from_numpy(Xh.view(np.int16)).cuda()
-    lin = W4A16Linear(W)
-    ref = lin(X, path=q.PATH_GEMV).float()
-    # the tolerance's scale: ||x_m|| * ||deq(w_n)|| (dequantised rows from the oracle)
-    xn = torch.from_numpy(np.linalg.norm(syn.bf16_bits_to_f32(Xh).astype(np.float64), axis=1)).cuda()
-    wn = torch.from_numpy(np.linalg.norm(oracle.dequant_w4(oracle.quantize_w4(Wh)), axis=1)).cuda()
+
+
+def _case(M, N, K, seed):
+    W = syn.make_weight(N, K, seed=seed)
+    X = syn.make_act(M, K, seed=seed + 1)
+    return W, X, oracle.quantize_w4(W), W4A16Linear(to_dev(W))
+
+
+def test_noalloc_scratch_path_matches_oracle_and_workspace_call():
+    _need_gpu()
+    cases = []
+    for i, (M, N, K) in enumerate(SCRATCH_CASES):
+        plan = q.qlin_plan_info(q.OP_W4A16_GEMM, M, N, K, 128, q.PATH_GEMV)
+        assert plan["kernel"] == q.KERNEL_W4A16_GEMV and plan["splits"] > 1 and plan["ws_bytes"] > 0, plan
+        W, X, wq, lin = _case(M, N, K, seed=900 + i)
+        ref = lin(to_dev(X), path=q.PATH_GEMV).clone()   # the same kernel with a caller workspace
+        cases.append((M, N, K, X, wq, lin, ref))
+    torch.cuda.synchronize()
+    for _ in range(2):                                   # each shape twice, all shapes back to back
+        for M, N, K, X, wq, lin, ref in cases:
+            Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            q.qlin_w4a16_gemv_noalloc(to_dev(X), lin.codes, lin.scales, lin.zeros, Y.view(torch.int16), M, N, K,
+                                      128)
+            torch.cuda.synchronize()
+            assert torch.equal(Y, ref), (M, N, K)       # same kernel, same split order: identical bits
+            check_w4(host_f64(Y), X, wq, full=True, tm=16, seed=M)
+    assert q.qlin_get_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 28672, 4096)])
+def test_noalloc_tensor_core_kernel_matches_oracle(M, N, K):
+    _need_gpu()
+    plan = q.qlin_plan_info(q.OP_W4A16_GEMM, M, N, K, 128, q.PATH_GEMV)
+    assert plan["kernel"] == q.KERNEL_W4A16_MMA and plan["ws_bytes"] == 0
+    W, X, wq, lin = _case(M, N, K, seed=M + N)
+    ref = lin(to_dev(X), path=q.PATH_GEMV)
     for _ in range(2):
         Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-        q.qlin_w4a16_gemv_noalloc(X, lin.codes, lin.scales, lin.zeros, Y.view(torch.int16), M, N, K, 128)
-        err = ((Y.double() - ref.double()).abs() / (xn[:, None] * wn[None, :])).max().item()
-        assert err <= TOL
-        assert torch.equal(Y.float(), ref)       # same kernel, same split order: identical bits
+        q.qlin_w4a16_gemv_noalloc(to_dev(X), lin.codes, lin.scales, lin.zeros, Y.view(torch.int16), M, N, K, 128)
+        torch.cuda.synchronize()
+        assert torch.equal(Y, ref)
+        check_w4(host_f64(Y), X, wq, full=True, tm=16, seed=M)
     assert q.qlin_get_device_error() == 0
 
 
 def test_noalloc_rejects_oversize():
-    if not torch.cuda.is_available():
-        pytest.skip("needs a GPU")
-    q.build()
+    _need_gpu()
     t = torch.zeros(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(q.QlinError) as e:       # K % 256 != 0: the CUDA-core GEMV needs ~15.7 MiB of partial sums
         q.qlin_w4a16_gemv_noalloc(t, t, t, t, t, 16, 16384, 28800, 128)
