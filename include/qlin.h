@@ -77,6 +77,7 @@ typedef enum {
 #define QLIN_OP_W8A8_GEMM 2
 #define QLIN_OP_QUANT_W_FP8 3
 #define QLIN_OP_W8A8_BLOCK_GEMM 4
+#define QLIN_OP_MXFP8_GEMM 5
 
 /* Activation of the fused output epilogue (qlin_*_gemm_fused). */
 #define QLIN_ACT_NONE 0
@@ -251,6 +252,45 @@ qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, con
                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                              void* stream);
 
+/* ---- MXFP8 (the OCP Microscaling format that [LP] S10 names; [VQ] S2: the
+ * MXFP8 W8A8 path runs on Blackwell only): E4M3 elements in blocks of 32
+ * consecutive values along K, each block with one power-of-two scale 2^e
+ * stored as an E8M0 byte e + 127.  e = floor(log2 amax) - 8 (8 being the
+ * exponent of E4M3's largest normal, 448 = 1.75 x 2^8), clamped to
+ * [-127, 127]; an all-zero block takes e = -127; elements are
+ * E4M3(v / 2^e), round to nearest even, saturating at +-448.  The product
+ * applies both block scales on the tensor cores (tcgen05 kind::mxf8f6f4 with
+ * hardware block scaling): no promotion pass.
+ *
+ * Scale layout ("scale atoms", the form the tensor cores take them in):
+ * for a tensor of R rows, ceil(R/128) x (K/128) atoms of 512 bytes, atom
+ * (R0, c) at byte ((R0 * (K/128)) + c) * 512 covering rows 128 R0 .. +127
+ * and columns 128 c .. +127.  Row r of the atom (r = row % 128) holds the
+ * scales of its four 32-column blocks kk = 0..3 in the four bytes
+ * 16 (r % 32) + 4 (r / 32) + kk.  Atom rows past R are 0. */
+
+/* Bytes of the scale atoms of an R x K tensor: ceil(R/128) * 128 * K / 32.
+ * K % 128 == 0, R >= 0. */
+qlin_status_t qlin_mx_scale_bytes(int64_t R, int64_t K, size_t* bytes);
+
+/* Quantise X [R][K] BF16 to MXFP8: codes [R][K] E4M3 (16-byte aligned) and
+ * scales in the atom layout above (qlin_mx_scale_bytes bytes, 16-byte aligned).
+ * Used for the weights (R = N, once at load) and the activations (R = M, per
+ * call).  K % 128 == 0.  Asynchronous, no workspace. */
+qlin_status_t qlin_quant_mxfp8(const void* X_bf16, int64_t R, int64_t K, void* codes_e4m3, void* scales_e8m0,
+                               void* stream);
+
+/* MXFP8 linear layer: Y[m][n] = bf16( sum_b 2^(xs[m][b]-127) 2^(ws[n][b]-127)
+ * sum_{k in block b} e4m3(Xq[m][k]) e4m3(Wq[n][k]) ), b over the 32-column
+ * blocks, accumulated in FP32 on the tensor cores.  Xq / xs from
+ * qlin_quant_mxfp8 of the activations, Wq / ws of the weights.  Shapes as
+ * qlin_w8a8_fp8_gemm (N % 128 == 0, K % 128 == 0); workspace:
+ * qlin_workspace_size(QLIN_OP_MXFP8_GEMM, ...) bytes (0 when the K range is
+ * not split), zero-filled, left zero-filled.  Deterministic. */
+qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3, const void* ws_e8m0,
+                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                              void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QLIN_OK, or the first error a kernel recorded since the last call. */
 qlin_status_t qlin_get_device_error(void* stream);
@@ -299,12 +339,14 @@ int qlin_gemv_max_m(int op);
 #define QLIN_KERNEL_W8A8_GEMV 5   /* small-M W8A8 on the CUDA cores (K % 256 != 0) */
 #define QLIN_KERNEL_W8A8_TC 6     /* W8A8 TMA + tcgen05 kind::f8f6f4 */
 #define QLIN_KERNEL_W8A8_BLOCK_TC 7 /* block-scaled W8A8 on tcgen05 with FP32 promotion */
+#define QLIN_KERNEL_MXFP8_TC 8    /* MXFP8 on tcgen05 kind::mxf8f6f4 with hardware block scaling */
 
 /*
  * Dispatch query (for tests and measurement tools; launches nothing, reads
  * no device memory): the kernel and tiling a call of `op`
- * (QLIN_OP_W4A16_GEMM, QLIN_OP_W8A8_GEMM or QLIN_OP_W8A8_BLOCK_GEMM) with
- * these sizes and `path` (QLIN_PATH_*; ignored by the block-scaled GEMM)
+ * (QLIN_OP_W4A16_GEMM, QLIN_OP_W8A8_GEMM, QLIN_OP_W8A8_BLOCK_GEMM or
+ * QLIN_OP_MXFP8_GEMM) with these sizes and `path` (QLIN_PATH_*; ignored by
+ * the block-scaled and MXFP8 GEMMs)
  * would launch.  num_sms is the SM count to plan for, 0 for the current
  * device's (the small-M kernels always read the current device's cluster
  * occupancy).  Writes 8 values:

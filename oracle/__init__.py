@@ -415,6 +415,31 @@ def mx_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return tab[codes] * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)
 
 
+def mx_scales_atoms(scales: np.ndarray) -> np.ndarray:
+    """The MX scales [R][K/32] in the "scale atom" layout the library's MXFP8 calls
+    take, written from its description: atoms of 512 bytes, atom (R0, c) at
+    ((R0 * (K/128)) + c) * 512 for rows 128 R0 .. +127 and columns 128 c .. +127;
+    row r (mod 128) keeps the scales of its 32-column blocks kk = 0..3 at
+    16 (r % 32) + 4 (r / 32) + kk; rows past R are 0.  Flat uint8 array."""
+    sc = np.asarray(scales, dtype=np.uint8)
+    R, nb = sc.shape
+    assert nb % 4 == 0
+    nc = nb // 4
+    nr = (R + 127) // 128
+    out = np.zeros(nr * nc * 512, np.uint8)
+    for r in range(R):
+        r0, rr = divmod(r, 128)
+        for c in range(nc):
+            base = (r0 * nc + c) * 512 + 16 * (rr % 32) + 4 * (rr // 32)
+            out[base:base + 4] = sc[r, 4 * c:4 * c + 4]
+    return out
+
+
+def w8a8_mx_full(Xq, xs, Wq, ws) -> np.ndarray:
+    """Y = dequant(Xq, xs) . dequant(Wq, ws)^T in double (dense product of the MX-dequantised operands)."""
+    return gemm_nt_f64(np.ascontiguousarray(mx_dequant(Xq, xs)), np.ascontiguousarray(mx_dequant(Wq, ws)))
+
+
 def w8a8_mx_at(Xq, xs, Wq, ws, ms, ns) -> np.ndarray:
     """Y[m_i, n_i] = sum over 32-blocks of both block scales times the block's E4M3 dot product, in double."""
     Xq = np.ascontiguousarray(Xq, dtype=np.uint8)

@@ -29,13 +29,14 @@ __all__ = [
     "qlin_w4a16_gemm_fused", "qlin_w8a8_fp8_gemm_fused",
     "PACK_FORMAT_VERSION", "qlin_plan_info", "PLAN_FIELDS",
     "KERNEL_W4A16_MMA", "KERNEL_W4A16_GEMV", "KERNEL_W4A16_TC", "KERNEL_W8A8_MMA", "KERNEL_W8A8_GEMV",
-    "KERNEL_W8A8_TC", "KERNEL_W8A8_BLOCK_TC",
+    "KERNEL_W8A8_TC", "KERNEL_W8A8_BLOCK_TC", "KERNEL_MXFP8_TC", "OP_MXFP8_GEMM",
+    "qlin_mx_scale_bytes", "qlin_quant_mxfp8", "qlin_mxfp8_gemm",
 ]
 
-OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM = 1, 2, 3, 4
+OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM, OP_MXFP8_GEMM = 1, 2, 3, 4, 5
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 (KERNEL_W4A16_MMA, KERNEL_W4A16_GEMV, KERNEL_W4A16_TC, KERNEL_W8A8_MMA, KERNEL_W8A8_GEMV, KERNEL_W8A8_TC,
- KERNEL_W8A8_BLOCK_TC) = 1, 2, 3, 4, 5, 6, 7
+ KERNEL_W8A8_BLOCK_TC, KERNEL_MXFP8_TC) = 1, 2, 3, 4, 5, 6, 7, 8
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = 0, 1, 2, 3
 PACK_FORMAT_VERSION = 2
 
@@ -71,6 +72,9 @@ _SIGS = {
     "qlin_quant_act_fp8_blocks": [_p, _i64, _i64, _p, _p, _p],
     "qlin_quant_w_fp8_blocks": [_p, _i64, _i64, _p, _p, _p],
     "qlin_w8a8_fp8_block_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
+    "qlin_mx_scale_bytes": [_i64, _i64, ctypes.POINTER(_sz)],
+    "qlin_quant_mxfp8": [_p, _i64, _i64, _p, _p, _p],
+    "qlin_mxfp8_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
 }
 
 
@@ -241,6 +245,22 @@ def qlin_w8a8_fp8_block_gemm(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, st
     return _check(load().qlin_w8a8_fp8_block_gemm(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
                                                   _ptr(workspace), ws_bytes, _stream(stream)),
                   "qlin_w8a8_fp8_block_gemm")
+
+
+def qlin_mx_scale_bytes(R: int, K: int) -> int:
+    b = _sz()
+    _check(load().qlin_mx_scale_bytes(R, K, ctypes.byref(b)), "qlin_mx_scale_bytes")
+    return b.value
+
+
+def qlin_quant_mxfp8(X, R, K, codes, scales, stream=None):
+    return _check(load().qlin_quant_mxfp8(_ptr(X), R, K, _ptr(codes), _ptr(scales), _stream(stream)),
+                  "qlin_quant_mxfp8")
+
+
+def qlin_mxfp8_gemm(Xq, xs, Wq, ws_sf, Y, M, N, K, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_mxfp8_gemm(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws_sf), _ptr(Y), M, N, K,
+                                         _ptr(workspace), ws_bytes, _stream(stream)), "qlin_mxfp8_gemm")
 
 
 def qlin_get_device_error(stream=None) -> int:

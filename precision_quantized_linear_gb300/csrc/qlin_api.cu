@@ -272,6 +272,7 @@ qlin_status_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, int G
     case QLIN_OP_W8A8_BLOCK_GEMM:
       *bytes = M == 0 ? 0 : plan_w8a8_block_tc(M, N, K, d->num_sms).split.ws_bytes;
       return QLIN_OK;
+    case QLIN_OP_MXFP8_GEMM: *bytes = M == 0 ? 0 : plan_mxfp8_tc(M, N, K, d->num_sms).split.ws_bytes; return QLIN_OK;
     default: return QLIN_ERR_INVALID_VALUE;
   }
 }
@@ -298,6 +299,10 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
     dp.kernel = QLIN_KERNEL_W8A8_BLOCK_TC;
     dp.tp = plan_w8a8_block_tc(M, N, K, num_sms);
     dp.ws = dp.tp.split.ws_bytes;
+  } else if (op == QLIN_OP_MXFP8_GEMM) {
+    dp.kernel = QLIN_KERNEL_MXFP8_TC;
+    dp.tp = plan_mxfp8_tc(M, N, K, num_sms);
+    dp.ws = dp.tp.split.ws_bytes;
   } else {
     return QLIN_ERR_INVALID_VALUE;
   }
@@ -305,7 +310,7 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
   for (int i = 0; i < 8; ++i) info[i] = 0;
   info[0] = dp.kernel;
   const bool tc = dp.kernel == QLIN_KERNEL_W4A16_TC || dp.kernel == QLIN_KERNEL_W8A8_TC ||
-                  dp.kernel == QLIN_KERNEL_W8A8_BLOCK_TC;
+                  dp.kernel == QLIN_KERNEL_W8A8_BLOCK_TC || dp.kernel == QLIN_KERNEL_MXFP8_TC;
   if (tc) {
     info[1] = dp.tp.bn;
     info[2] = dp.tp.wn;
@@ -527,6 +532,48 @@ qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, con
                                             static_cast<const uint8_t*>(Wq_e4m3), sw, static_cast<uint16_t*>(Y_bf16),
                                             M, N, K, p, workspace, d->err, d->num_sms,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_mx_scale_bytes(int64_t R, int64_t K, size_t* bytes) {
+  if (!bytes) return QLIN_ERR_INVALID_VALUE;
+  if (R < 0 || R > kMaxM * 64 || K <= 0 || K % kGroup != 0 || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  *bytes = static_cast<size_t>((R + 127) / 128 * 128 * (K / 32));
+  return QLIN_OK;
+}
+
+qlin_status_t qlin_quant_mxfp8(const void* X_bf16, int64_t R, int64_t K, void* codes_e4m3, void* scales_e8m0,
+                               void* stream) {
+  if (R < 0 || R > kMaxM * 64 || K <= 0 || K % kGroup != 0 || K > (int64_t(1) << 31)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (R == 0) return QLIN_OK;
+  if (!X_bf16 || !codes_e4m3 || !scales_e8m0) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(X_bf16) || !aligned16(codes_e4m3) || !aligned16(scales_e8m0)) return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  qlin_status_t st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_quant_mxfp8(static_cast<const uint16_t*>(X_bf16), R, K,
+                                          static_cast<uint8_t*>(codes_e4m3), static_cast<uint8_t*>(scales_e8m0),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3, const void* ws_e8m0,
+                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  qlin_status_t st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  if (!Xq_e4m3 || !xs_e8m0 || !Wq_e4m3 || !ws_e8m0 || !Y_bf16) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(Xq_e4m3) || !aligned16(xs_e8m0) || !aligned16(Wq_e4m3) || !aligned16(ws_e8m0) ||
+      !aligned16(Y_bf16) || (workspace && !aligned16(workspace)))
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  const TcPlan p = plan_mxfp8_tc(M, N, K, d->num_sms);
+  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_mxfp8_tc(static_cast<const uint8_t*>(Xq_e4m3), static_cast<const uint8_t*>(xs_e8m0),
+                                       static_cast<const uint8_t*>(Wq_e4m3), static_cast<const uint8_t*>(ws_e8m0),
+                                       static_cast<uint16_t*>(Y_bf16), M, N, K, p, workspace, d->err, d->num_sms,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 qlin_status_t qlin_selftest_wait_timeout(uint32_t limit_us, void* stream) {

@@ -155,6 +155,14 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                                  int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
                                  cudaStream_t st);
+// MXFP8: E4M3 operands with E8M0 scales per 32 columns, in scale atoms
+// [rows / 128][K / 128][512 B] (see qlin_quant_mxfp8).
+TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t* Wq, const uint8_t* ws_sf,
+                            uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
+                            int num_sms, cudaStream_t st);
+cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t st);
 cudaError_t launch_quant_act_fp8_blocks(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx,
                                         cudaStream_t st);
 cudaError_t launch_quant_w_fp8_blocks(const uint16_t* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,

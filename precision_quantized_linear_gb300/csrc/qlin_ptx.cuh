@@ -307,6 +307,29 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// Same for E4M3 operands with hardware block scaling (MXFP8): every 32-element
+// K step of row m of A is multiplied by 2^(e - 127) of the E8M0 byte read from
+// TMEM lane m, column sfa_tmem + m / 32, byte `a_id` of the instruction
+// descriptor; column n of B likewise from lane n % 32 (the same in each lane
+// quadrant), column sfb_tmem + n / 32, byte `b_id`.
+__device__ __forceinline__ void mma_mx8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 512-byte shared-memory atom of 32 rows x 16 bytes into TMEM lanes
+// 32q + r, columns taddr .. taddr + 3, for each lane quadrant q (row r's four
+// 32-bit words go to the four columns).  In issue order with this thread's MMAs.
+__device__ __forceinline__ void tc_cp_atom(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -362,6 +385,26 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
   d |= static_cast<uint64_t>(1) << 46;                     // descriptor version for tcgen05
   d |= static_cast<uint64_t>(2) << 61;                     // swizzle mode: 128-byte
   return d;
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte atom without swizzle: 8-row
+// core matrices of 128 contiguous bytes, 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_atom(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFF) >> 4);  // start address
+  d |= static_cast<uint64_t>(128 >> 4) << 32;              // stride byte offset: next 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                     // descriptor version for tcgen05
+  return d;                                                // swizzle mode 0: none
+}
+
+// Instruction descriptor of the block-scaled E4M3 MMA (M = 128): E8M0 scales,
+// K-major A and B, FP32 accumulator; a_id / b_id pick the scale byte (0..3).
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t mma_n, uint32_t a_id, uint32_t b_id) {
+  return (b_id << 4)                 // scale byte of B
+         | ((mma_n >> 3) << 17)      // N / 8
+         | (1u << 23)                // scale type: E8M0
+         | ((128u >> 4) << 24)       // M / 16
+         | (a_id << 29);             // scale byte of A
 }
 
 // Instruction descriptor: dense, FP32 accumulator, K-major A and B.

@@ -311,4 +311,62 @@ cudaError_t launch_quant_w_fp8_blocks(const uint16_t* W, int64_t N, int64_t K, u
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ MXFP8
+
+// MX block scale of a 32-element block ([LP] S10, OCP Microscaling v1.0):
+// e = floor(log2 amax) - 8 (8: exponent of E4M3's largest normal), clamped to
+// [-127, 127]; -127 for an all-zero block.  Read from the exponent field: an
+// FP32 subnormal amax (below 2^-126) lies below the clamp.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (eb == 0) return -127;
+  const int e = eb - 127 - 8;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// One warp per (row r, 128 columns): lane l holds columns 4l .. 4l+3, a block
+// of 32 columns is a segment of 8 lanes.  Codes are E4M3(v * 2^-e) -- the
+// power-of-two scaling is exact, so this is v / 2^e rounded once, to nearest
+// even with saturation.  The four scale bytes of the 128 columns go to one
+// 32-bit word of the scale atom: row r of atom (r / 128, k / 128) holds its
+// word at byte 16 (r % 32) + 4 ((r % 128) / 32); rows past R (the atom's
+// padding) get 0.
+__global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint16_t* __restrict__ X, int64_t R, int64_t K,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nc = K / 128;
+  const int64_t rows = (R + 127) / 128 * 128;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= rows * nc) return;  // whole warps only
+  const int64_t r = item / nc, c = item % nc;
+  uint32_t e8 = 0;
+  if (r < R) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(X + r * K + c * 128 + 4 * lane);
+    const float v[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = seg_max(amax, 8);
+    const int e = amax == 0.0f ? -127 : mx_exponent(amax);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e in [-127, 119]
+    const uint32_t lo = e4m3x2(v[0] * inv, v[1] * inv), hi = e4m3x2(v[2] * inv, v[3] * inv);
+    *reinterpret_cast<uint32_t*>(codes + r * K + c * 128 + 4 * lane) = lo | (hi << 16);
+    e8 = static_cast<uint32_t>(e + 127);
+  }
+  // bytes kk = 0..3 of the word from lanes 0, 8, 16, 24
+  uint32_t word = (e8 & 0xFFu) << (8 * (lane >> 3));
+  word |= __shfl_xor_sync(0xffffffffu, word, 8);
+  word |= __shfl_xor_sync(0xffffffffu, word, 16);
+  if (lane == 0) {
+    uint8_t* atom = scales + ((r / 128) * nc + c) * 512;
+    *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+  }
+}
+
+cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t st) {
+  const int64_t warps = (R + 127) / 128 * 128 * (K / 128);
+  const int64_t blocks = (warps + 7) / 8;
+  quant_mxfp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, R, K, codes, scales);
+  return cudaGetLastError();
+}
+
 }  // namespace qlin

@@ -40,7 +40,7 @@ namespace qlin {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kSmemBudget = 225 * 1024;
 
-template <int BN, bool W4, int KPS, bool BS = false, int WN = 128>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool MX = false>
 struct TcCfg {
   static constexpr int kBlkBytes = 128;                         // bytes of one row of a K block
   static constexpr int kCols = W4 ? 64 : 128;                   // K columns per block
@@ -52,8 +52,12 @@ struct TcCfg {
   static constexpr int kScaleOff = KPS * kXBlk + KPS * kWBlk;   // scales, then zero-points (W4A16)
   static constexpr int kZeroOff = kScaleOff + kGroupsMax * 256;
   static constexpr int kMetaBytes = W4 ? ((kGroupsMax * 320 + 1023) / 1024) * 1024 : 0;
-  static constexpr int kStage = KPS * kXBlk + KPS * kWBlk + kMetaBytes;
-  static constexpr int kTxBase = KPS * kXBlk + KPS * kWBlk;    // plus 320 bytes per group loaded
+  // MXFP8: the E8M0 scale atoms of the stage's K block (512 bytes of weight
+  // scales, then 512 of token scales), copied into TMEM by the MMA thread
+  static constexpr int kSfOff = KPS * kXBlk + KPS * kWBlk + kMetaBytes;
+  static constexpr int kSfBytes = MX ? 1024 : 0;
+  static constexpr int kStage = KPS * kXBlk + KPS * kWBlk + kMetaBytes + kSfBytes;
+  static constexpr int kTxBase = KPS * kXBlk + KPS * kWBlk + kSfBytes;  // W4A16: plus 320 bytes per group loaded
   // dequantised BF16 weight tiles: in TMEM (tcgen05.st, read by the MMA as
   // its A operand) when the accumulators leave room, else in shared memory
   static constexpr bool kATmem = W4 && BN <= 128;
@@ -81,7 +85,12 @@ struct TcCfg {
   // block scaling keeps up to four K-block partial products in flight
   static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : 2;
   static constexpr int kAColBase = 2 * BN;                      // first TMEM column of the A slots
-  static constexpr int kTmemNeed = kAccBufs * BN + (kATmem ? kAStages * kASlotCols : 0);
+  // MXFP8 scale factors in TMEM: a ring of kSfSlots K blocks, four columns of
+  // weight scales and four of token scales each (see mma_mx8)
+  static constexpr int kSfSlots = MX ? 4 : 0;
+  static constexpr int kSfaCol = kAccBufs * BN;
+  static constexpr int kSfbCol = kSfaCol + 4 * kSfSlots;
+  static constexpr int kTmemNeed = kAccBufs * BN + (kATmem ? kAStages * kASlotCols : 0) + 8 * kSfSlots;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                  : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kDqWarps = W4 ? 8 : 0;
@@ -100,6 +109,7 @@ struct TcCfg {
   static_assert(kTmemNeed <= 512, "TMEM budget");
   static_assert(!BS || (!W4 && BN <= 128), "block scaling: E4M3 operands, at most 128 tokens (running sums in registers)");
   static_assert(WN == 128 || (kTokM && WN == 256), "256-row weight tiles only token-major");
+  static_assert(!MX || (!W4 && !BS && BN >= 32 && BN <= 128), "MXFP8: E4M3 operands, 32..128 tokens per tile");
 };
 
 struct TcArgs {
@@ -108,6 +118,8 @@ struct TcArgs {
   const uint8_t* zeros;
   const float* sx;
   const float* sw;  // W8A8 block scaling: sx = [K/128][M], sw = [N/128][K/128]
+  const uint8_t* sfa;  // MXFP8: E8M0 scale atoms of the weights, [N/128][K/128][512 B]
+  const uint8_t* sfb;  // MXFP8: E8M0 scale atoms of the tokens, [ceil(M/128)][K/128][512 B]
   uint16_t* Y;
   float* partials;
   uint32_t* counters;
@@ -177,12 +189,13 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
   return r;
 }
 
-// EPI: the output epilogue (bias, activation) of the *_gemm_fused calls is compiled in
-template <int BN, bool W4, int KPS, bool BS, int WN, bool EPI>
-__global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
+// EPI: the output epilogue (bias, activation) of the *_gemm_fused calls is compiled in;
+// MX: E4M3 operands with E8M0 block scales applied by the MMA (MXFP8)
+template <int BN, bool W4, int KPS, bool BS, int WN, bool EPI, bool MX = false>
+__global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX>::kMaxRegs))
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ TcArgs a) {
-  using C = TcCfg<BN, W4, KPS, BS, WN>;
+  using C = TcCfg<BN, W4, KPS, BS, WN, MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -263,6 +276,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
           for (int h = 0; h < WN / kTileN; ++h)  // one box of 128 rows per scale block
             tma_load_2d_hint(st + C::kXBlk + h * kTileN * C::kBlkBytes, &tmap_w, &full[s], kb * C::kCols,
                              un.nt * WN + h * kTileN, pol_stream);
+          if constexpr (MX)  // the weight tile's scale atom of this K block
+            bulk_load(st + C::kSfOff, a.sfa + (static_cast<int64_t>(un.nt) * KB + kb) * 512, 512, &full[s]);
         }
       };
       auto load_x = [&](int s, const Unit& un, int j) {
@@ -271,6 +286,9 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
 #pragma unroll
         for (int i = 0; i < KPS; ++i)
           tma_load_2d_hint(st + i * C::kXBlk, &tmap_x, &full[s], (kb + i) * C::kCols, un.mb * BN, pol_keep);
+        if constexpr (MX)  // the scale atom of the 128 tokens holding this token block
+          bulk_load(st + C::kSfOff + 512, a.sfb + ((static_cast<int64_t>(un.mb) * BN / 128) * KB + kb) * 512, 512,
+                    &full[s]);
       };
       int it = 0;
       // phase 1: weights of the first ring pass
@@ -337,6 +355,47 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
           mma_commit(&empty[s]);
           mma_commit(&acc_full[pb]);
         }
+      }
+      if (!ok) {
+        set_error(a.err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+      }
+    } else if (lane == 0 && MX) {
+      // MXFP8: per K block, copy its two scale atoms into the next TMEM slot
+      // of the ring (in issue order with the MMAs), then four MMAs of 32
+      // columns, k-step kk taking byte kk of each scale word
+      int it = 0, ua = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++ua) {
+        const Unit un = unit_of(a, u, KB);
+        const int acc = ua & 1;
+        if (!mbar_wait(&acc_empty[acc], ((ua >> 1) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + acc * C::kAccCols;
+        const uint32_t tok_col = static_cast<uint32_t>((un.mb * BN) % 128) / 32;  // this block's tokens in the atom
+        for (int j = 0; j < un.nkb && ok; ++j, ++it) {
+          const int s = it % C::kStages;
+          if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t slot = static_cast<uint32_t>(it % C::kSfSlots) * 4;
+          const uint32_t t_sfa = tmem_base + C::kSfaCol + slot, t_sfb = tmem_base + C::kSfbCol + slot;
+          const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
+          tc_cp_atom(t_sfa, sdesc_atom(st_u32 + C::kSfOff));
+          tc_cp_atom(t_sfb, sdesc_atom(st_u32 + C::kSfOff + 512));
+          const uint32_t a_addr = st_u32 + C::kXBlk, b_addr = st_u32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mx8(tmem_d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc_mx(BN, kk, kk), t_sfa,
+                    t_sfb + tok_col, (j | kk) != 0);
+          mma_commit(&empty[s]);
+        }
+        mma_commit(&acc_full[acc]);
       }
       if (!ok) {
         set_error(a.err, QLIN_ERR_TIMEOUT);
@@ -517,7 +576,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
     grid_dep_wait();  // outputs and the workspace may still be in use by the previous kernel
     const int t = threadIdx.x - C::kEpiWarp0 * 32;  // 0 .. kEpiWarps * 32 - 1
     const int quad = warp & 3;                       // TMEM lane quadrant of this warp
-    const float s_w = (W4 || BS) ? 1.0f : *a.sw;
+    const float s_w = (W4 || BS || MX) ? 1.0f : *a.sw;
     int ua = 0;
     uint32_t epi_n = 0;  // staging boxes used so far
     int kbi = 0;         // K blocks promoted so far (block scaling)
@@ -802,7 +861,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
             for (int i = 0; i < 16; ++i) {
               const int64_t m = mbase + c0 + i;
               const float x = have ? __uint_as_float(v[i]) : 0.0f;
-              o[i] = W4 ? x : (m < a.M ? (x * __ldg(a.sx + m)) * s_w : 0.0f);
+              o[i] = (W4 || MX) ? x : (m < a.M ? (x * __ldg(a.sx + m)) * s_w : 0.0f);
             }
             if constexpr (EPI) epi_run(a.epi.act, o, bias_n);
 #pragma unroll
@@ -848,7 +907,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN>::kMaxRegs))
                   __stcg(p + static_cast<int64_t>(i) * a.N, 0.0f);
                 }
             }
-            if constexpr (!W4) {
+            if constexpr (!W4 && !MX) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const int64_t m = mbase + c0 + i;
@@ -1031,6 +1090,15 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bo
 
 TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 64, true); }
 TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false); }
+// MXFP8 runs on the E4M3 tile plan with 32 to 128 tokens per tile: a token
+// tile then starts on a 32-token boundary of its scale atom (the MMA reads a
+// tile's token scales from whole TMEM columns of 32 lanes), and two
+// accumulators of 128 columns leave room for the scale-factor ring.
+TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
+  TcPlan p = plan_tc(M, N, K, num_sms, 128, false, 128);
+  if (p.bn < 32) p.bn = 32;  // the same single token block for M <= 16
+  return p;
+}
 // Block scaling keeps the running sums of a 128-token tile in registers.  With
 // 128-token tiles the weight tile is 256 rows (two scale blocks) when N allows
 // and there are still enough tiles for every SM: a wider MMA moves fewer
@@ -1042,11 +1110,11 @@ TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   return plan_tc(M, N, K, num_sms, 128, false, 128, wn, false);
 }
 
-template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = false>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = false, bool MX = false>
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
                              const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
-  using C = TcCfg<BN, W4, KPS, BS, WN>;
-  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI>, C::kSmemBytes);
+  using C = TcCfg<BN, W4, KPS, BS, WN, MX>;
+  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI, MX>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   args.counters = static_cast<uint32_t*>(ws);
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.split.tiles)) : nullptr;
@@ -1073,7 +1141,7 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI>, tx, tw, ty, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI, MX>, tx, tw, ty, args);
 }
 
 template <bool W4, bool EPI>
@@ -1140,6 +1208,29 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
   a.epi = epi;
   return (epi.bias || epi.act) ? launch_tc_bn<false, true>(tx, tw, ty, a, plan, ws, num_sms, st)
                                 : launch_tc_bn<false, false>(tx, tw, ty, a, plan, ws, num_sms, st);
+}
+
+cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t* Wq, const uint8_t* ws_sf,
+                            uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
+                            int num_sms, cudaStream_t st) {
+  CUtensorMap tx, tw, ty;
+  if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, K, N, K, 128, 128)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, N * 2, kTileN, 16, false))
+    return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.sfa = ws_sf;
+  a.sfb = xs;
+  a.Y = Y;
+  a.err = err;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  switch (plan.bn) {
+    case 32: return launch_tc<32, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 64: return launch_tc<64, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default: return launch_tc<128, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+  }
 }
 
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,

@@ -12,7 +12,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (ACT_NONE, OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_pack_w4,
+from . import (ACT_NONE, OP_MXFP8_GEMM, OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO,
+               qlin_mx_scale_bytes, qlin_mxfp8_gemm, qlin_pack_w4, qlin_quant_mxfp8,
                qlin_quant_act_fp8, qlin_quant_act_fp8_blocks, qlin_quant_w_fp8, qlin_quant_w_fp8_blocks,
                qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w4a16_gemm_fused, qlin_w8a8_fp8_block_gemm,
                qlin_w8a8_fp8_gemm_ex, qlin_w8a8_fp8_gemm_fused, qlin_workspace_size)
@@ -151,3 +152,38 @@ class W8A8BlockLinear:
     def __call__(self, X_bf16, Y=None, stream=None):
         Xq, sx = self.quant_act(X_bf16, stream=stream)
         return self.gemm(Xq, sx, Y, stream)
+
+
+class MXFP8Linear:
+    """MXFP8 W8A8: E4M3 weights and activations with E8M0 scales per 32 columns,
+    both block scales applied by the tensor cores."""
+
+    def __init__(self, W_bf16: torch.Tensor, stream=None):
+        N, K = W_bf16.shape
+        self.N, self.K = N, K
+        dev = W_bf16.device
+        self.Wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        self.ws_sf = torch.empty(qlin_mx_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+        qlin_quant_mxfp8(_as_u16(W_bf16.contiguous()), N, K, self.Wq, self.ws_sf, stream)
+        self.ws = Workspace(dev)
+
+    def quant_act(self, X_bf16: torch.Tensor, Xq=None, xs=None, stream=None):
+        M, K = X_bf16.shape
+        if Xq is None:
+            Xq = torch.empty((M, K), dtype=torch.uint8, device=X_bf16.device)
+        if xs is None:
+            xs = torch.empty(max(qlin_mx_scale_bytes(M, K), 16), dtype=torch.uint8, device=X_bf16.device)
+        qlin_quant_mxfp8(_as_u16(X_bf16), M, K, Xq, xs, stream)
+        return Xq, xs
+
+    def gemm(self, Xq, xs, Y=None, stream=None):
+        M = Xq.shape[0]
+        if Y is None:
+            Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
+        buf, nb = self.ws.get(qlin_workspace_size(OP_MXFP8_GEMM, M, self.N, self.K))
+        qlin_mxfp8_gemm(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        return Y
+
+    def __call__(self, X_bf16, Y=None, stream=None):
+        Xq, xs = self.quant_act(X_bf16, stream=stream)
+        return self.gemm(Xq, xs, Y, stream)

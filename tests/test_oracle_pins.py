@@ -608,3 +608,35 @@ def test_mxfp8_product_applies_each_block_scale_to_its_own_block():
     got = oracle.w8a8_mx_at(Xq, xs, Wq, ws, ms, ns)
     want = (oracle.mx_dequant(Xq, xs) @ oracle.mx_dequant(Wq, ws).T)[ms, ns]  # dense product of the dequantised operands
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=0)
+
+
+def test_mx_scale_atoms_feed_each_row_its_own_scales():
+    """The atom layout, read back the way the tensor cores take it: the 512-byte
+    atom as 32 rows of four 32-bit words, copied to lane r (of every lane
+    quadrant); row m of the operand reads lane m % 32, word m // 32, byte kk."""
+    R, K = 200, 256                                          # a partial second row atom, two column atoms
+    rng = np.random.default_rng(21)
+    scales = rng.integers(1, 255, (R, K // 32)).astype(np.uint8)
+    atoms = oracle.mx_scales_atoms(scales)
+    assert atoms.size == 2 * 2 * 512
+    nc = K // 128
+    for m in range(R):
+        for c in range(nc):
+            atom = atoms[((m // 128) * nc + c) * 512:((m // 128) * nc + c + 1) * 512].reshape(32, 4, 4)
+            mm = m % 128
+            assert list(atom[mm % 32, mm // 32]) == list(scales[m, 4 * c:4 * c + 4])
+    pad = atoms[(1 * nc) * 512:].reshape(nc, 32, 4, 4)        # rows 200..255 of the second row atom are 0
+    for c in range(nc):
+        for mm in range(R - 128, 128):
+            assert not pad[c, mm % 32, mm // 32].any()
+
+
+def test_mx_full_product_equals_the_per_element_loops():
+    rng = np.random.default_rng(22)
+    X = (rng.standard_normal((5, 256)) * np.exp2(rng.integers(-5, 5, (5, 8)).repeat(32, axis=1))).astype(np.float32)
+    W = (rng.standard_normal((7, 256)) * np.exp2(rng.integers(-5, 5, (7, 8)).repeat(32, axis=1))).astype(np.float32)
+    Xq, xs = oracle.quant_mxfp8_rows(_bf16_bits(X))
+    Wq, ws = oracle.quant_mxfp8_rows(_bf16_bits(W))
+    full = oracle.w8a8_mx_full(Xq, xs, Wq, ws)
+    ms, ns = np.repeat(np.arange(5), 7), np.tile(np.arange(7), 5)
+    np.testing.assert_allclose(full[ms, ns], oracle.w8a8_mx_at(Xq, xs, Wq, ws, ms, ns), rtol=1e-12, atol=0)
