@@ -378,13 +378,18 @@ def measure_prefill(peaks, l2):
 
     import precision_quantized_linear_gb300 as q
     from precision_quantized_linear_gb300 import synthetic as syn
-    from precision_quantized_linear_gb300.layers import W8A8Linear
+    from precision_quantized_linear_gb300.layers import MXFP8Linear, W8A8Linear
 
     p8 = 2.0 * peaks["bf16_tflops_sustained"]
-    rows = []
+    rows, mx_rows = [], []
     for K, N in [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]:
-        lin = W8A8Linear(torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda())
-        sets = [lin.Wq] + [lin.Wq.clone() for _ in range(rotation(N * K, l2) - 1)]
+        Wd = torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda()
+        lin = W8A8Linear(Wd)
+        linmx = MXFP8Linear(Wd)
+        del Wd
+        nrot = rotation(N * K, l2)
+        sets = [lin.Wq] + [lin.Wq.clone() for _ in range(nrot - 1)]
+        mxsets = [(linmx.Wq, linmx.ws_sf)] + [(linmx.Wq.clone(), linmx.ws_sf.clone()) for _ in range(nrot - 1)]
         for M in (2048, 8192):
             X = torch.from_numpy(syn.make_act(M, K, seed=M + 7, token_outlier_frac=0.001).view(np.int16)).cuda()
             Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
@@ -401,16 +406,35 @@ def measure_prefill(peaks, l2):
             rows.append({"K": K, "N": N, "M": M, "us": round(us, 2), "TFLOPS": round(flops / (us * 1e-6) / 1e12, 1),
                          "frac": round(t_roof / us, 3), "quant_us": round(qus, 2),
                          "TFLOPS_with_quant": round(flops / ((us + qus) * 1e-6) / 1e12, 1)})
+            # MXFP8 (E8M0 scales per 32 columns applied by the tensor cores) on the same operands
+            Xmq, xms = linmx.quant_act(X)
+            nbm = q.qlin_workspace_size(q.OP_MXFP8_GEMM, M, N, K)
+            wsm = torch.zeros(max(nbm, 256), dtype=torch.uint8, device="cuda")
+            usm = time_launches([lambda st, wq=wq, wsf=wsf: q.qlin_mxfp8_gemm(Xmq, xms, wq, wsf, Y, M, N, K, wsm,
+                                                                             wsm.numel(), st) for (wq, wsf) in mxsets])
+            qusm = time_launches([lambda st: q.qlin_quant_mxfp8(X, M, K, Xmq, xms, st)])
+            alg_mx = w8_alg_bytes(M, N, K) + (M + N) * K // 32
+            t_roof = max(flops / (p8 * 1e12), alg_mx / (peaks["hbm_gbs"] * 1e9)) * 1e6
+            mx_rows.append({"K": K, "N": N, "M": M, "us": round(usm, 2),
+                            "TFLOPS": round(flops / (usm * 1e-6) / 1e12, 1), "frac": round(t_roof / usm, 3),
+                            "quant_us": round(qusm, 2)})
             assert q.qlin_get_device_error() == 0
-            del X, Y, Xq, sx, ws
-        del lin, sets
+            del X, Y, Xq, sx, ws, Xmq, xms, wsm
+        del lin, sets, linmx, mxsets
         torch.cuda.empty_cache()
-    tot_flops = sum(2 * r["M"] * r["N"] * r["K"] for r in rows)
-    tot_us = sum(r["us"] for r in rows)
+
+    def total(rs):
+        f = sum(2 * r["M"] * r["N"] * r["K"] for r in rs)
+        t = sum(r["us"] for r in rs)
+        return round(f / (t * 1e-6) / 1e12, 1), round(f / (t * 1e-6) / 1e12 / p8, 3)
+    tf, fr = total(rows)
+    tfm, frm = total(mx_rows)
     return {"workload": "W8A8 FP8 prefill M=2048/8192 on the Llama-3-8B shapes (tcgen05 kind::f8f6f4)",
             "peak_tflops": round(p8, 1), "peak_source": "measured bf16 sustained x 2 (nominal FP8/BF16 ratio)",
-            "TFLOPS": round(tot_flops / (tot_us * 1e-6) / 1e12, 1),
-            "frac": round(tot_flops / (tot_us * 1e-6) / 1e12 / p8, 3), "cases": rows}
+            "TFLOPS": tf, "frac": fr, "cases": rows,
+            "mxfp8": {"workload": "MXFP8 (E8M0 scale per 32 columns, hardware block scaling, tcgen05 "
+                                  "kind::mxf8f6f4) on the same shapes and M", "TFLOPS": tfm, "frac": frm,
+                      "cases": mx_rows}}
 
 
 def measure_crossover(peaks, l2):

@@ -94,6 +94,8 @@ def _load():
         lib.orc_w4a16_at.restype = None
         lib.orc_w4a16_at.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int,
                                      _p, _p, _i64, _p]
+        lib.orc_w4a8_at.restype = None
+        lib.orc_w4a8_at.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _i64, _p]
         lib.orc_w8a8_at.restype = None
         lib.orc_w8a8_at.argtypes = [_p, _p, _p, ctypes.c_float, _i64, _i64, _i64,
                                     _p, _p, _i64, _p]
@@ -278,6 +280,29 @@ def w8a8_at(Xq, sx, Wq, sw, ms, ns) -> np.ndarray:
     ns = np.ascontiguousarray(ns, dtype=np.int64)
     out = np.empty(ms.shape, np.float64)
     _load().orc_w8a8_at(_ptr(Xq), _ptr(sx), _ptr(Wq), float(sw), M, N, K,
+                        _ptr(ms), _ptr(ns), ms.size, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- W4A8
+
+def w4a8_full(Xq, sx, wq: W4Quant) -> np.ndarray:
+    """[LP] S1 W4A8: Y = (diag(sx) dec(Xq)) . deq(W)^T in double, deq(W) = s (q - z)
+    of the INT4 quantiser and Xq / sx of the per-token E4M3 quantiser."""
+    A = e4m3_table()[np.asarray(Xq, np.uint8)] * np.asarray(sx, np.float64)[:, None]
+    return gemm_nt_f64(np.ascontiguousarray(A), dequant_w4(wq))
+
+
+def w4a8_at(Xq, sx, wq: W4Quant, ms, ns) -> np.ndarray:
+    """Y[m_i, n_i] of w4a8_full for sampled pairs, each a plain loop over K in C."""
+    Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    M, K = Xq.shape
+    N = wq.q.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape, np.float64)
+    _load().orc_w4a8_at(_ptr(Xq), _ptr(sx), _ptr(wq.q), _ptr(wq.s), _ptr(wq.z), M, N, K, wq.G,
                         _ptr(ms), _ptr(ns), ms.size, _ptr(out))
     return out
 

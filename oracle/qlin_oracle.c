@@ -446,6 +446,31 @@ void orc_w4a16_at(const uint16_t *X, const uint8_t *q, const uint16_t *s, const 
     }
 }
 
+/* W4A8 ([LP] S1: INT4 weights, FP8 activations, FP32 accumulation, BF16
+ * output): the INT4 weights of the W4A16 quantiser (x_hat = s (q - z) per
+ * group) times the per-token E4M3 activations (sx[m] e4m3(Xq[m][k])):
+ * Y[m][n] = sum_k sx[m] e4m3(Xq[m][k]) * s[n][k/G] (q[n][k] - z[n][k/G]),
+ * in double, for sampled (m, n). */
+void orc_w4a8_at(const uint8_t *Xq, const float *sx, const uint8_t *q, const uint16_t *s, const uint8_t *z,
+                 int64_t M, int64_t N, int64_t K, int G,
+                 const int64_t *ms, const int64_t *ns, int64_t cnt, double *out)
+{
+    int64_t ng = K / G;
+    (void)M;
+    (void)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < cnt; i++) {
+        int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            double x = (double)sx[m] * orc_e4m3_to_f64(Xq[m * K + k]);
+            double w = orc_f16_to_f64(s[n * ng + k / G]) * ((double)q[n * K + k] - (double)z[n * ng + k / G]);
+            acc += x * w;
+        }
+        out[i] = acc;
+    }
+}
+
 /* W8A8: Y[m][n] = sx[m] * sw * sum_k e4m3(Xq[m][k]) * e4m3(Wq[n][k]).   */
 void orc_w8a8_at(const uint8_t *Xq, const float *sx, const uint8_t *Wq, float sw,
                  int64_t M, int64_t N, int64_t K,

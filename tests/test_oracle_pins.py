@@ -640,3 +640,58 @@ def test_mx_full_product_equals_the_per_element_loops():
     full = oracle.w8a8_mx_full(Xq, xs, Wq, ws)
     ms, ns = np.repeat(np.arange(5), 7), np.tile(np.arange(7), 5)
     np.testing.assert_allclose(full[ms, ns], oracle.w8a8_mx_at(Xq, xs, Wq, ws, ms, ns), rtol=1e-12, atol=0)
+
+
+# ---- W4A8 ([LP] S1 precision manifest: INT4 weights, FP8 activations, FP32 accumulate)
+
+def _w4a8_case(M, N, K, seed):
+    W = syn.make_weight(N, K, seed=seed)
+    X = syn.make_act(M, K, seed=seed + 1, token_outlier_frac=0.2)
+    wq = oracle.quantize_w4(W)
+    Xq, sx = oracle.quant_fp8_rows(X)
+    return wq, Xq, sx
+
+
+def test_w4a8_full_equals_the_per_element_loops():
+    wq, Xq, sx = _w4a8_case(5, 256, 384, 31)
+    full = oracle.w4a8_full(Xq, sx, wq)
+    ms, ns = np.repeat(np.arange(5), 9), np.tile(np.arange(0, 256, 29), 5)
+    np.testing.assert_allclose(full[ms, ns], oracle.w4a8_at(Xq, sx, wq, ms, ns), rtol=1e-12, atol=1e-300)
+
+
+def test_w4a8_reduces_to_w4a16_on_fp8_exact_activations():
+    # activations whose values are E4M3 codes times a unit scale are exact in BF16:
+    # the W4A8 product must then be the (pinned) W4A16 product of those values
+    rng = np.random.default_rng(32)
+    codes = rng.integers(0, 256, (3, 256)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38            # no NaN codes
+    vals = oracle.e4m3_table()[codes].astype(np.float32)
+    xb = syn.f32_to_bf16_bits(vals)
+    assert np.array_equal(syn.bf16_bits_to_f32(xb), vals)
+    wq = oracle.quantize_w4(syn.make_weight(128, 256, seed=33))
+    sx = np.ones(3, np.float32)
+    np.testing.assert_array_equal(oracle.w4a8_full(codes, sx, wq), oracle.w4a16_full(xb, wq))
+
+
+def test_w4a8_token_scale_enters_its_row_linearly():
+    wq, Xq, sx = _w4a8_case(4, 128, 256, 34)
+    base = oracle.w4a8_full(Xq, sx, wq)
+    sx2 = sx.copy()
+    sx2[2] *= 4.0                                    # power of two: exact
+    got = oracle.w4a8_full(Xq, sx2, wq)
+    np.testing.assert_array_equal(got[2], 4.0 * base[2])
+    np.testing.assert_array_equal(np.delete(got, 2, 0), np.delete(base, 2, 0))
+
+
+def test_w4a8_brute_force_triple_loop():
+    wq, Xq, sx = _w4a8_case(2, 128, 128, 35)
+    tab = oracle.e4m3_table()
+    deq = oracle.dequant_w4(wq)
+    want = np.zeros((2, 128))
+    for m in range(2):
+        for n in range(128):
+            acc = 0.0
+            for k in range(128):
+                acc += float(sx[m]) * tab[Xq[m, k]] * deq[n, k]
+            want[m, n] = acc
+    np.testing.assert_allclose(oracle.w4a8_full(Xq, sx, wq), want, rtol=1e-12, atol=1e-300)
