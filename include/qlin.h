@@ -78,6 +78,7 @@ typedef enum {
 #define QLIN_OP_QUANT_W_FP8 3
 #define QLIN_OP_W8A8_BLOCK_GEMM 4
 #define QLIN_OP_MXFP8_GEMM 5
+#define QLIN_OP_W4A8_GEMM 6
 
 /* Activation of the fused output epilogue (qlin_*_gemm_fused). */
 #define QLIN_ACT_NONE 0
@@ -252,6 +253,23 @@ qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, con
                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                              void* stream);
 
+/*
+ * W4A8 linear layer ([LP] S1 precision manifest "W4A8: INT4 weights, INT8/FP8
+ * activations -> accumulate FP32 -> output BF16"; S20 QServe W4A8): the packed
+ * INT4 weights of qlin_pack_w4 (G = 128) times the per-token E4M3 activations
+ * of qlin_quant_act_fp8,
+ *     Y[m][n] = bf16( sx[m] * sum_g s[n][g] * sum_{k in g} e4m3(Xq[m][k]) (q[n][k] - z[n][g]) ),
+ * the inner sums accumulated in FP32 on the tensor cores (tcgen05
+ * kind::f8f6f4; q - z, an integer in [-15, 15], is exact in E4M3) and each
+ * group's partial product promoted with its FP16 scale in FP32.
+ * Requires G == 128; shapes and alignment as qlin_w4a16_gemm (sx 4-byte
+ * aligned); workspace: qlin_workspace_size(QLIN_OP_W4A8_GEMM, ...) bytes (0
+ * when the K range is not split), zero-filled, left zero-filled.  Deterministic.
+ */
+qlin_status_t qlin_w4a8_gemm(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,
+                             const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
+                             void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- MXFP8 (the OCP Microscaling format that [LP] S10 names; [VQ] S2: the
  * MXFP8 W8A8 path runs on Blackwell only): E4M3 elements in blocks of 32
  * consecutive values along K, each block with one power-of-two scale 2^e
@@ -340,13 +358,14 @@ int qlin_gemv_max_m(int op);
 #define QLIN_KERNEL_W8A8_TC 6     /* W8A8 TMA + tcgen05 kind::f8f6f4 */
 #define QLIN_KERNEL_W8A8_BLOCK_TC 7 /* block-scaled W8A8 on tcgen05 with FP32 promotion */
 #define QLIN_KERNEL_MXFP8_TC 8    /* MXFP8 on tcgen05 kind::mxf8f6f4 with hardware block scaling */
+#define QLIN_KERNEL_W4A8_TC 9     /* W4A8: INT4 -> E4M3 dequantisation, tcgen05 kind::f8f6f4, group promotion */
 
 /*
  * Dispatch query (for tests and measurement tools; launches nothing, reads
  * no device memory): the kernel and tiling a call of `op`
- * (QLIN_OP_W4A16_GEMM, QLIN_OP_W8A8_GEMM, QLIN_OP_W8A8_BLOCK_GEMM or
- * QLIN_OP_MXFP8_GEMM) with these sizes and `path` (QLIN_PATH_*; ignored by
- * the block-scaled and MXFP8 GEMMs)
+ * (QLIN_OP_W4A16_GEMM, QLIN_OP_W8A8_GEMM, QLIN_OP_W8A8_BLOCK_GEMM,
+ * QLIN_OP_MXFP8_GEMM or QLIN_OP_W4A8_GEMM) with these sizes and `path`
+ * (QLIN_PATH_*; ignored by the block-scaled, MXFP8 and W4A8 GEMMs)
  * would launch.  num_sms is the SM count to plan for, 0 for the current
  * device's (the small-M kernels always read the current device's cluster
  * occupancy).  Writes 8 values:

@@ -30,13 +30,14 @@ __all__ = [
     "PACK_FORMAT_VERSION", "qlin_plan_info", "PLAN_FIELDS",
     "KERNEL_W4A16_MMA", "KERNEL_W4A16_GEMV", "KERNEL_W4A16_TC", "KERNEL_W8A8_MMA", "KERNEL_W8A8_GEMV",
     "KERNEL_W8A8_TC", "KERNEL_W8A8_BLOCK_TC", "KERNEL_MXFP8_TC", "OP_MXFP8_GEMM",
-    "qlin_mx_scale_bytes", "qlin_quant_mxfp8", "qlin_mxfp8_gemm",
+    "qlin_mx_scale_bytes", "qlin_quant_mxfp8", "qlin_mxfp8_gemm", "qlin_w4a8_gemm", "OP_W4A8_GEMM",
+    "KERNEL_W4A8_TC",
 ]
 
-OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM, OP_MXFP8_GEMM = 1, 2, 3, 4, 5
+OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM, OP_MXFP8_GEMM, OP_W4A8_GEMM = 1, 2, 3, 4, 5, 6
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 (KERNEL_W4A16_MMA, KERNEL_W4A16_GEMV, KERNEL_W4A16_TC, KERNEL_W8A8_MMA, KERNEL_W8A8_GEMV, KERNEL_W8A8_TC,
- KERNEL_W8A8_BLOCK_TC, KERNEL_MXFP8_TC) = 1, 2, 3, 4, 5, 6, 7, 8
+ KERNEL_W8A8_BLOCK_TC, KERNEL_MXFP8_TC, KERNEL_W4A8_TC) = 1, 2, 3, 4, 5, 6, 7, 8, 9
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = 0, 1, 2, 3
 PACK_FORMAT_VERSION = 2
 
@@ -73,6 +74,7 @@ _SIGS = {
     "qlin_quant_w_fp8_blocks": [_p, _i64, _i64, _p, _p, _p],
     "qlin_w8a8_fp8_block_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
     "qlin_mx_scale_bytes": [_i64, _i64, ctypes.POINTER(_sz)],
+    "qlin_w4a8_gemm": [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _sz, _p],
     "qlin_quant_mxfp8": [_p, _i64, _i64, _p, _p, _p],
     "qlin_mxfp8_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
 }
@@ -245,6 +247,11 @@ def qlin_w8a8_fp8_block_gemm(Xq, sx, Wq, sw, Y, M, N, K, workspace, ws_bytes, st
     return _check(load().qlin_w8a8_fp8_block_gemm(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
                                                   _ptr(workspace), ws_bytes, _stream(stream)),
                   "qlin_w8a8_fp8_block_gemm")
+
+
+def qlin_w4a8_gemm(Xq, sx, codes, scales, zeros, Y, M, N, K, G, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_w4a8_gemm(_ptr(Xq), _ptr(sx), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(Y), M, N,
+                                        K, G, _ptr(workspace), ws_bytes, _stream(stream)), "qlin_w4a8_gemm")
 
 
 def qlin_mx_scale_bytes(R: int, K: int) -> int:

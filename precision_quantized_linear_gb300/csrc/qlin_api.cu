@@ -273,6 +273,10 @@ qlin_status_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, int G
       *bytes = M == 0 ? 0 : plan_w8a8_block_tc(M, N, K, d->num_sms).split.ws_bytes;
       return QLIN_OK;
     case QLIN_OP_MXFP8_GEMM: *bytes = M == 0 ? 0 : plan_mxfp8_tc(M, N, K, d->num_sms).split.ws_bytes; return QLIN_OK;
+    case QLIN_OP_W4A8_GEMM:
+      if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+      *bytes = M == 0 ? 0 : plan_w4a8_tc(M, N, K, d->num_sms).split.ws_bytes;
+      return QLIN_OK;
     default: return QLIN_ERR_INVALID_VALUE;
   }
 }
@@ -299,6 +303,11 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
     dp.kernel = QLIN_KERNEL_W8A8_BLOCK_TC;
     dp.tp = plan_w8a8_block_tc(M, N, K, num_sms);
     dp.ws = dp.tp.split.ws_bytes;
+  } else if (op == QLIN_OP_W4A8_GEMM) {
+    if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
+    dp.kernel = QLIN_KERNEL_W4A8_TC;
+    dp.tp = plan_w4a8_tc(M, N, K, num_sms);
+    dp.ws = dp.tp.split.ws_bytes;
   } else if (op == QLIN_OP_MXFP8_GEMM) {
     dp.kernel = QLIN_KERNEL_MXFP8_TC;
     dp.tp = plan_mxfp8_tc(M, N, K, num_sms);
@@ -310,13 +319,14 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
   for (int i = 0; i < 8; ++i) info[i] = 0;
   info[0] = dp.kernel;
   const bool tc = dp.kernel == QLIN_KERNEL_W4A16_TC || dp.kernel == QLIN_KERNEL_W8A8_TC ||
-                  dp.kernel == QLIN_KERNEL_W8A8_BLOCK_TC || dp.kernel == QLIN_KERNEL_MXFP8_TC;
+                  dp.kernel == QLIN_KERNEL_W8A8_BLOCK_TC || dp.kernel == QLIN_KERNEL_MXFP8_TC ||
+                  dp.kernel == QLIN_KERNEL_W4A8_TC;
   if (tc) {
     info[1] = dp.tp.bn;
     info[2] = dp.tp.wn;
     info[3] = dp.tp.kps;
     info[4] = dp.tp.split.splits;
-    info[6] = dp.kernel == QLIN_KERNEL_W4A16_TC && dp.tp.bn <= 128 ? 1 : 0;
+    info[6] = (dp.kernel == QLIN_KERNEL_W4A16_TC && dp.tp.bn <= 128) || dp.kernel == QLIN_KERNEL_W4A8_TC ? 1 : 0;
     info[7] = dp.tp.mblocks;
   } else {
     const int64_t tok = (dp.kernel == QLIN_KERNEL_W4A16_MMA || dp.kernel == QLIN_KERNEL_W8A8_MMA)
@@ -532,6 +542,28 @@ qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, con
                                             static_cast<const uint8_t*>(Wq_e4m3), sw, static_cast<uint16_t*>(Y_bf16),
                                             M, N, K, p, workspace, d->err, d->num_sms,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_w4a8_gemm(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,
+                             const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;  // one quantisation group per 128-column K block
+  qlin_status_t st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  if (!Xq_e4m3 || !sx || !codes || !scales_f16 || !zeros_u4 || !Y_bf16) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(Xq_e4m3) || !aligned16(codes) || !aligned16(scales_f16) || !aligned16(zeros_u4) ||
+      !aligned16(Y_bf16) || (workspace && !aligned16(workspace)) || (reinterpret_cast<uintptr_t>(sx) & 3u))
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  const TcPlan p = plan_w4a8_tc(M, N, K, d->num_sms);
+  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_w4a8_tc(static_cast<const uint8_t*>(Xq_e4m3), sx, static_cast<const uint8_t*>(codes),
+                                      static_cast<const uint16_t*>(scales_f16), static_cast<const uint8_t*>(zeros_u4),
+                                      static_cast<uint16_t*>(Y_bf16), M, N, K, p, workspace, d->err, d->num_sms,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 qlin_status_t qlin_mx_scale_bytes(int64_t R, int64_t K, size_t* bytes) {

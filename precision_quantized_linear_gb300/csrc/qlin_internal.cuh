@@ -155,6 +155,11 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                                  int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
                                  cudaStream_t st);
+// W4A8: packed INT4 weights (G = 128) dequantised to E4M3, times per-token E4M3 activations.
+TcPlan plan_w4a8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_w4a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* codes, const uint16_t* scales,
+                           const uint8_t* zeros, uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan,
+                           void* ws, int* err, int num_sms, cudaStream_t st);
 // MXFP8: E4M3 operands with E8M0 scales per 32 columns, in scale atoms
 // [rows / 128][K / 128][512 B] (see qlin_quant_mxfp8).
 TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms);

@@ -40,15 +40,18 @@ namespace qlin {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kSmemBudget = 225 * 1024;
 
-template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool MX = false>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool MX = false, bool A8 = false>
 struct TcCfg {
   static constexpr int kBlkBytes = 128;                         // bytes of one row of a K block
-  static constexpr int kCols = W4 ? 64 : 128;                   // K columns per block
+  // K columns per block: 64 for W4A16 (one packed code tile), 128 for E4M3
+  // operands; W4A8 takes two code tiles (one quantisation group) per block
+  static constexpr int kCols = (W4 && !A8) ? 64 : 128;
   static constexpr int kXBlk = BN * kBlkBytes;                  // token tile of one K block
-  static constexpr int kWBlk = W4 ? 4096 : WN * kBlkBytes;      // packed codes / E4M3 tile of one K block
+  static constexpr int kWBlk = W4 ? (A8 ? 8192 : 4096) : WN * kBlkBytes;  // packed codes / E4M3 tile of one K block
   // group scales and zero-points of a stage: room for G = 32 (two groups per
-  // 64-column block); G = 64 / 128 use the front of each region
-  static constexpr int kGroupsMax = W4 ? 2 * KPS : 0;
+  // 64-column block); G = 64 / 128 use the front of each region; W4A8: one
+  // group (G = 128) per block
+  static constexpr int kGroupsMax = W4 ? (A8 ? KPS : 2 * KPS) : 0;
   static constexpr int kScaleOff = KPS * kXBlk + KPS * kWBlk;   // scales, then zero-points (W4A16)
   static constexpr int kZeroOff = kScaleOff + kGroupsMax * 256;
   static constexpr int kMetaBytes = W4 ? ((kGroupsMax * 320 + 1023) / 1024) * 1024 : 0;
@@ -61,7 +64,9 @@ struct TcCfg {
   // dequantised BF16 weight tiles: in TMEM (tcgen05.st, read by the MMA as
   // its A operand) when the accumulators leave room, else in shared memory
   static constexpr bool kATmem = W4 && BN <= 128;
-  static constexpr int kAStages = W4 ? (kATmem ? 8 : 4) : 0;  // A slots (one 64-column block each)
+  // A slots: one K block each (W4A16: 64 BF16 columns, W4A8: 128 E4M3 columns,
+  // both 32 TMEM columns of a 128-lane slot)
+  static constexpr int kAStages = W4 ? (kATmem ? 8 : 4) : 0;
   static constexpr int kAStage = (W4 && !kATmem) ? 128 * kBlkBytes : 0;  // shared-memory bytes per slot
   static constexpr int kASlotCols = 32;                         // TMEM columns per slot (64 BF16 per lane)
   // output staging: two boxes of 16 tokens x 128 rows of BF16 for the tensor stores
@@ -82,9 +87,9 @@ struct TcCfg {
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kAccCols = kTokM ? WN : BN;              // one accumulator
   // accumulators in TMEM: two (one unit while the epilogue drains the other);
-  // block scaling keeps up to four K-block partial products in flight
-  static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : 2;
-  static constexpr int kAColBase = 2 * BN;                      // first TMEM column of the A slots
+  // block scaling and W4A8 keep up to four K-block partial products in flight
+  static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : (A8 ? 4 : 2);
+  static constexpr int kAColBase = kAccBufs * BN;               // first TMEM column of the A slots
   // MXFP8 scale factors in TMEM: a ring of kSfSlots K blocks, four columns of
   // weight scales and four of token scales each (see mma_mx8)
   static constexpr int kSfSlots = MX ? 4 : 0;
@@ -110,6 +115,7 @@ struct TcCfg {
   static_assert(!BS || (!W4 && BN <= 128), "block scaling: E4M3 operands, at most 128 tokens (running sums in registers)");
   static_assert(WN == 128 || (kTokM && WN == 256), "256-row weight tiles only token-major");
   static_assert(!MX || (!W4 && !BS && BN >= 32 && BN <= 128), "MXFP8: E4M3 operands, 32..128 tokens per tile");
+  static_assert(!A8 || (W4 && !BS && !MX && BN <= 64), "W4A8: packed INT4 weights, at most 64 tokens per tile");
 };
 
 struct TcArgs {
@@ -190,12 +196,13 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
 }
 
 // EPI: the output epilogue (bias, activation) of the *_gemm_fused calls is compiled in;
-// MX: E4M3 operands with E8M0 block scales applied by the MMA (MXFP8)
-template <int BN, bool W4, int KPS, bool BS, int WN, bool EPI, bool MX = false>
-__global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX>::kMaxRegs))
+// MX: E4M3 operands with E8M0 block scales applied by the MMA (MXFP8);
+// A8: packed INT4 weights (W4 = true) dequantised to E4M3 times E4M3 tokens (W4A8)
+template <int BN, bool W4, int KPS, bool BS, int WN, bool EPI, bool MX = false, bool A8 = false>
+__global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ TcArgs a) {
-  using C = TcCfg<BN, W4, KPS, BS, WN, MX>;
+  using C = TcCfg<BN, W4, KPS, BS, WN, MX, A8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -255,7 +262,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX>::kMaxRegs))
       const int64_t ng = W4 ? a.K / a.G : 0;  // groups per weight row (W4A16)
       // groups whose scales a stage loads: those of its KPS blocks (a G = 128
       // group spans two blocks, so a one-block stage loads the group it is in)
-      const int gps = W4 ? (KPS * 64 >= a.G ? KPS * 64 / a.G : 1) : 0;
+      const int gps = W4 ? (KPS * C::kCols >= a.G ? KPS * C::kCols / a.G : 1) : 0;
       const uint32_t tx_bytes = C::kTxBase + gps * 320;
       // weights never depend on the previous kernel: the first pass over the
       // ring is filled with weight tiles before waiting for that kernel; the
@@ -264,9 +271,10 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX>::kMaxRegs))
         uint8_t* st = ring + s * C::kStage;
         const int kb = un.kb0 + j * KPS;
         if constexpr (W4) {
-          const int64_t g0 = (static_cast<int64_t>(kb) * 64) >> (31 - __clz(a.G));
-          bulk_load_hint(st + KPS * C::kXBlk, a.codes + (static_cast<int64_t>(un.nt) * KB + kb) * 4096,
-                         KPS * 4096, &full[s], pol_stream);
+          const int64_t g0 = (static_cast<int64_t>(kb) * C::kCols) >> (31 - __clz(a.G));
+          const int64_t tpb = C::kCols / 64;  // packed code tiles per K block
+          bulk_load_hint(st + KPS * C::kXBlk, a.codes + (static_cast<int64_t>(un.nt) * KB * tpb + kb * tpb) * 4096,
+                         KPS * C::kWBlk, &full[s], pol_stream);
           bulk_load(st + C::kScaleOff, a.scales + (static_cast<int64_t>(un.nt) * ng + g0) * kTileN, gps * 256,
                     &full[s]);
           bulk_load(st + C::kZeroOff, a.zeros + (static_cast<int64_t>(un.nt) * ng + g0) * (kTileN / 2), gps * 64,
@@ -401,6 +409,47 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX>::kMaxRegs))
         set_error(a.err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
       }
+    } else if (lane == 0 && A8) {
+      // W4A8: every K block (one quantisation group) goes to its own partial
+      // product in one of kAccBufs TMEM buffers, A = the block's E4M3 (q - z)
+      // written into a TMEM slot by the dequantisation warps; the epilogue
+      // applies the group scale
+      constexpr uint32_t idesc = idesc_make(0, 0, 128, BN);
+      int it = 0, ait = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        const Unit un = unit_of(a, u, KB);
+        for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
+          const int s = it % C::kStages;
+          if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
+            ok = false;
+            break;
+          }
+#pragma unroll 1
+          for (int i = 0; i < KPS; ++i, ++ait) {
+            const int ai = ait % C::kAStages, pb = ait % C::kAccBufs;
+            if (!mbar_wait(&a_full[ai], (ait / C::kAStages) & 1, kWaitLimitNs, &s_abort) ||
+                !mbar_wait(&acc_empty[pb], ((ait / C::kAccBufs) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = tmem_base + C::kAColBase + ai * C::kASlotCols;
+            const uint32_t b_addr = smem_u32(ring + s * C::kStage + i * C::kXBlk);
+            const uint32_t tmem_d = tmem_base + pb * C::kAccCols;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // 32 bytes of K per MMA = 8 TMEM columns of A
+              mma_f8_tmem_a(tmem_d, a_addr + kk * 8, sdesc_sw128(b_addr + kk * 32), idesc, kk != 0);
+            mma_commit(&a_empty[ai]);
+            mma_commit(&acc_full[pb]);
+          }
+          mma_commit(&empty[s]);
+        }
+      }
+      if (!ok) {
+        set_error(a.err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+      }
     } else if (lane == 0) {
       constexpr uint32_t idesc = W4 ? idesc_make(1, 1, 128, BN) : idesc_make(0, 0, 128, BN);
       int it = 0, ait = 0, ua = 0;
@@ -458,8 +507,82 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX>::kMaxRegs))
       }
     }
   } else if (warp < C::kEpiWarp0) {
-    // ---------------------------------------------------------------- dequantisation (W4A16)
-    if constexpr (W4) {
+    // ---------------------------------------------------------------- dequantisation (W4A8)
+    if constexpr (W4 && A8) {
+      // The two groups of four warps take the K blocks (128 columns = one
+      // quantisation group) in turn; the warp of TMEM lane quadrant q turns rows
+      // 32q..32q+31 into E4M3 (q - z): integers in [-15, 15], exact in E4M3.
+      // A nibble pair becomes FP16x2 (1024 + q) with one LOP3, (q - z) with one
+      // HSUB2 and an E4M3 pair with one CVT; the 128 columns go to the slot in
+      // natural order, four per TMEM column.
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;
+      const int grp = (warp - 2) >> 2;
+      int it = 0, ait = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        const Unit un = unit_of(a, u, KB);
+        for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
+          const int s = it % C::kStages;
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort))) {
+            ok = false;
+            break;
+          }
+          const uint32_t sts = smem_u32(ring + s * C::kStage);
+#pragma unroll 1
+          for (int i = 0; i < KPS; ++i, ++ait) {
+            const bool mine = (ait & 1) == grp;
+            const int ai = ait % C::kAStages;
+            uint4 c[4];  // records of row r: code tile 0 halves 0, 1, then code tile 1 halves 0, 1
+            uint32_t zoff = 0;
+            if (mine) {
+              if (!__all_sync(0xffffffffu,
+                              mbar_wait(&a_empty[ai], ((ait / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
+                ok = false;
+                break;
+              }
+#pragma unroll
+              for (int rec = 0; rec < 4; ++rec) c[rec] = lds128(sts + KPS * C::kXBlk + i * 8192 + rec * 2048 + r * 16);
+              const uint32_t zb = lds8(sts + C::kZeroOff + i * 64 + r / 2);
+              zoff = (0x6400u + ((r & 1) ? (zb >> 4) : (zb & 15u))) * 0x10001u;  // FP16x2 (1024 + z)
+            }
+            if (i == KPS - 1) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
+            }
+            if (!mine) continue;
+            tc_fence_after();
+#pragma unroll
+            for (int rec = 0; rec < 4; ++rec) {
+              const uint32_t w[4] = {c[rec].x, c[rec].y, c[rec].z, c[rec].w};
+              uint32_t e[4][4];  // e[t][g8]: E4M3 of columns 8 g8 + 2t (low byte) and 8 g8 + 2t + 1
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8)
+                  e[t][g8] = e4m3x2_of_f16x2(hsub2_bits(((w[t] >> (4 * g8)) & 0x000F000Fu) | 0x64006400u, zoff));
+              uint32_t v[8];  // TMEM column 2 g8 + j of the record: columns 8 g8 + 4 j .. + 3
+#pragma unroll
+              for (int g8 = 0; g8 < 4; ++g8)
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) v[2 * g8 + jj] = e[2 * jj][g8] | (e[2 * jj + 1][g8] << 16);
+              tmem_st8(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
+                           rec * 8,
+                       v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[ai]);
+          }
+        }
+      }
+      if (!ok) {
+        set_error(a.err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+      }
+    } else if constexpr (W4) {
+      // ------------------------------------------------------------ dequantisation (W4A16)
       // Two groups of four warps take the 64-column blocks in turn (group g the
       // blocks with ait % 2 == g), so that two blocks are dequantised at once;
       // within a group, the warp of TMEM lane quadrant q does rows 32q..32q+31,
@@ -581,7 +704,106 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX>::kMaxRegs))
     uint32_t epi_n = 0;  // staging boxes used so far
     int kbi = 0;         // K blocks promoted so far (block scaling)
     for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++ua) {
-      if constexpr (C::kTokM) {
+      if constexpr (A8) {
+        // ---- W4A8: every K block's partial product is promoted with the group
+        // scale of this thread's weight row (TMEM lane quad * 32 + lane),
+        // r[c] += P[c] * s[n][g], in K-block order; then y = r * sx[m]
+        const Unit un = unit_of(a, u, KB);
+        const int row = quad * 32 + lane;
+        const int64_t n = static_cast<int64_t>(un.nt) * kTileN + row;
+        const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
+        const bool direct = a.splits == 1;
+        const uint16_t* sp = a.scales + static_cast<int64_t>(un.nt) * KB * kTileN + row;  // [group][128 rows]
+        float sn = un.nkb > 0 ? __half2float(__ushort_as_half(__ldg(sp + static_cast<int64_t>(un.kb0) * kTileN))) : 0.0f;
+        float rr[BN];
+#pragma unroll
+        for (int c = 0; c < BN; ++c) rr[c] = 0.0f;
+        bool have = true;
+        for (int j = 0; j < un.nkb; ++j, ++kbi) {
+          const int pb = kbi % C::kAccBufs;
+          const float f = sn;
+          if (j + 1 < un.nkb)  // the next group's scale while this one is promoted
+            sn = __half2float(__ushort_as_half(__ldg(sp + static_cast<int64_t>(un.kb0 + j + 1) * kTileN)));
+          if (have && !__all_sync(0xffffffffu, mbar_wait(&acc_full[pb], (kbi / C::kAccBufs) & 1, kWaitLimitNs,
+                                                           &s_abort))) {
+            have = false;
+            set_error(a.err, QLIN_ERR_TIMEOUT);
+            s_abort = 1;
+          }
+          if (!have) continue;
+          tc_fence_after();
+          const uint32_t tmem_d = tmem_base + pb * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+          constexpr int kChunk = 16;  // columns per TMEM load: the running sums already hold up to 64 registers
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += kChunk) {
+            uint32_t v[kChunk / 16][16];
+#pragma unroll
+            for (int q = 0; q < kChunk / 16; ++q) tmem_ld16(tmem_d + c0 + q * 16, v[q]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < kChunk / 16; ++q) reg_fence16(v[q]);
+            if (c0 + kChunk == BN) {  // all of the buffer is in registers: it may take the next K block
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[pb]);
+            }
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) rr[c0 + c] = fmaf(__uint_as_float(v[c >> 4][c & 15]), f, rr[c0 + c]);
+          }
+        }
+        // the token scales are applied where the values are written, 16 tokens at a time
+        if (direct) {
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            if (mbase + c0 < a.M) {  // the same for the four warps: they skip the barriers together
+              uint16_t* box = reinterpret_cast<uint16_t*>(epi_box + (epi_n & 1) * C::kEpiBox);
+              if (t == 0) bulk_wait_read<1>();
+              named_bar_epi();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int64_t m = mbase + c0 + i;
+                box[i * kTileN + row] = m < a.M ? to_bf16(rr[c0 + i] * __ldg(a.sx + m)) : uint16_t(0);
+              }
+              fence_proxy_async_smem();
+              named_bar_epi();
+              if (t == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(mbase + c0));
+              ++epi_n;
+            }
+          }
+        } else {
+          if (have) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c) {
+              const int64_t m = mbase + c;
+              if (m < a.M) __stcg(a.partials + (static_cast<int64_t>(un.split) * a.M + m) * a.N + n, rr[c] * __ldg(a.sx + m));
+            }
+          }
+          // last-arriver reduction of the K ranges, in split order (deterministic)
+          __threadfence();
+          named_bar_epi();
+          const int64_t tile = static_cast<int64_t>(un.mb) * a.ntiles + un.nt;
+          if (t == 0) s_last = !s_abort && (atomicAdd(a.counters + tile, 1u) == static_cast<uint32_t>(a.splits - 1));
+          named_bar_epi();
+          if (s_last) {
+            __threadfence();
+#pragma unroll 1
+            for (int c = 0; c < BN; ++c) {
+              const int64_t m = mbase + c;
+              if (m >= a.M) break;
+              float acc_v = 0.0f;
+              for (int sp2 = 0; sp2 < a.splits; ++sp2) {  // read and clear: the workspace is left zero-filled
+                float* p = a.partials + (static_cast<int64_t>(sp2) * a.M + m) * a.N + n;
+                acc_v += __ldcg(p);
+                __stcg(p, 0.0f);
+              }
+              a.Y[m * a.N + n] = to_bf16(acc_v);
+            }
+            if (t == 0) a.counters[tile] = 0u;
+          }
+          named_bar_epi();
+        }
+        continue;
+      } else if constexpr (C::kTokM) {
         // ---- block scaling, token-major: thread = token m (TMEM lane quad * 32 +
         // lane), columns [cbase, cbase + 64) of the weight tile; every K block's
         // partial product is promoted as r[c] += P[c] * (sx[kb][m] * sw[nt][kb])
@@ -1094,6 +1316,11 @@ TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_
 // tile then starts on a 32-token boundary of its scale atom (the MMA reads a
 // tile's token scales from whole TMEM columns of 32 lanes), and two
 // accumulators of 128 columns leave room for the scale-factor ring.
+// W4A8: K blocks of 128 columns (one quantisation group, two code tiles) and
+// at most 64 tokens per tile (the promotion keeps a row's running sums in
+// registers); the E4M3 tile plan with those limits.
+TcPlan plan_w4a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false, 64); }
+
 TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   TcPlan p = plan_tc(M, N, K, num_sms, 128, false, 128);
   if (p.bn < 32) p.bn = 32;  // the same single token block for M <= 16
@@ -1110,11 +1337,11 @@ TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   return plan_tc(M, N, K, num_sms, 128, false, 128, wn, false);
 }
 
-template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = false, bool MX = false>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = false, bool MX = false, bool A8 = false>
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
                              const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
-  using C = TcCfg<BN, W4, KPS, BS, WN, MX>;
-  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI, MX>, C::kSmemBytes);
+  using C = TcCfg<BN, W4, KPS, BS, WN, MX, A8>;
+  cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI, MX, A8>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   args.counters = static_cast<uint32_t*>(ws);
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + counters_bytes(plan.split.tiles)) : nullptr;
@@ -1126,7 +1353,7 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
   {
     const double l2_half = 63.0 * 1024 * 1024;  // half of the 126 MB L2
     const double wb = static_cast<double>(args.N) * static_cast<double>(args.K) * (W4 ? 0.51953125 : 1.0);
-    const double xb = static_cast<double>(args.M) * static_cast<double>(args.K) * (W4 ? 2.0 : 1.0);
+    const double xb = static_cast<double>(args.M) * static_cast<double>(args.K) * ((W4 && !A8) ? 2.0 : 1.0);
     args.mb_fast = (wb > l2_half && xb < wb) ? 1 : 0;
     args.x_keep = xb <= l2_half / 2 ? 1 : 0;
   }
@@ -1141,7 +1368,7 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI, MX>, tx, tw, ty, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI, MX, A8>, tx, tw, ty, args);
 }
 
 template <bool W4, bool EPI>
@@ -1208,6 +1435,31 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
   a.epi = epi;
   return (epi.bias || epi.act) ? launch_tc_bn<false, true>(tx, tw, ty, a, plan, ws, num_sms, st)
                                 : launch_tc_bn<false, false>(tx, tw, ty, a, plan, ws, num_sms, st);
+}
+
+cudaError_t launch_w4a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* codes, const uint16_t* scales,
+                           const uint8_t* zeros, uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan,
+                           void* ws, int* err, int num_sms, cudaStream_t st) {
+  CUtensorMap tx, ty;
+  if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, N * 2, kTileN, 16, false))
+    return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.codes = codes;
+  a.scales = scales;
+  a.zeros = zeros;
+  a.G = kGroup;
+  a.sx = sx;
+  a.Y = Y;
+  a.err = err;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  switch (plan.bn) {
+    case 16: return launch_tc<16, true, 1, false, 128, false, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
+    case 32: return launch_tc<32, true, 1, false, 128, false, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
+    default: return launch_tc<64, true, 1, false, 128, false, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
+  }
 }
 
 cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t* Wq, const uint8_t* ws_sf,

@@ -12,8 +12,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (ACT_NONE, OP_MXFP8_GEMM, OP_QUANT_W_FP8, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO,
-               qlin_mx_scale_bytes, qlin_mxfp8_gemm, qlin_pack_w4, qlin_quant_mxfp8,
+from . import (ACT_NONE, OP_MXFP8_GEMM, OP_QUANT_W_FP8, OP_W4A8_GEMM, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM,
+               OP_W8A8_GEMM, PATH_AUTO, qlin_mx_scale_bytes, qlin_mxfp8_gemm, qlin_pack_w4, qlin_quant_mxfp8,
+               qlin_w4a8_gemm,
                qlin_quant_act_fp8, qlin_quant_act_fp8_blocks, qlin_quant_w_fp8, qlin_quant_w_fp8_blocks,
                qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w4a16_gemm_fused, qlin_w8a8_fp8_block_gemm,
                qlin_w8a8_fp8_gemm_ex, qlin_w8a8_fp8_gemm_fused, qlin_workspace_size)
@@ -78,6 +79,36 @@ class W4A16Linear:
             qlin_w4a16_gemm_fused(_as_u16(X_bf16), self.codes, self.scales, self.zeros, Y.view(torch.int16), M,
                                   self.N, self.K, self.G, self.bias, act, buf, nb, path, stream)
         return Y
+
+
+class W4A8Linear(W4A16Linear):
+    """W4A8: the packed INT4 weights of W4A16Linear (G = 128) times per-token E4M3
+    activations from the fused amax quantiser."""
+
+    def __init__(self, W_bf16: torch.Tensor, symmetric: bool = False, stream=None):
+        super().__init__(W_bf16, G=128, symmetric=symmetric, stream=stream)
+
+    def quant_act(self, X_bf16: torch.Tensor, Xq=None, sx=None, stream=None):
+        M, K = X_bf16.shape
+        if Xq is None:
+            Xq = torch.empty((M, K), dtype=torch.uint8, device=X_bf16.device)
+        if sx is None:
+            sx = torch.empty(max(M, 1), dtype=torch.float32, device=X_bf16.device)
+        qlin_quant_act_fp8(_as_u16(X_bf16), M, K, Xq, sx, stream)
+        return Xq, sx
+
+    def gemm(self, Xq, sx, Y=None, stream=None):
+        M = Xq.shape[0]
+        if Y is None:
+            Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
+        buf, nb = self.ws.get(qlin_workspace_size(OP_W4A8_GEMM, M, self.N, self.K, 128))
+        qlin_w4a8_gemm(Xq, sx, self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N, self.K, 128, buf,
+                       nb, stream)
+        return Y
+
+    def __call__(self, X_bf16, Y=None, stream=None):
+        Xq, sx = self.quant_act(X_bf16, stream=stream)
+        return self.gemm(Xq, sx, Y, stream)
 
 
 class W8A8Linear:
