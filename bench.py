@@ -470,8 +470,16 @@ def measure_crossover(peaks, l2):
                 q.qlin_quant_act_fp8(X, M, K, Xq, sx, st)
                 q.qlin_w8a8_fp8_gemm(Xq, sx, wq, lin8.sw, Y, M, N, K, ws, ws.numel(), st)
             us8 = time_launches([lambda st, wq=wq: w8(st, wq) for wq in sets8])
+            nb48 = q.qlin_workspace_size(q.OP_W4A8_GEMM, M, N, K)
+            ws48 = torch.zeros(max(nb48, 256), dtype=torch.uint8, device="cuda")
+
+            def w48(st, c, s, z):
+                q.qlin_quant_act_fp8(X, M, K, Xq, sx, st)
+                q.qlin_w4a8_gemm(Xq, sx, c, s, z, Y, M, N, K, 128, ws48, ws48.numel(), st)
+            us48 = time_launches([lambda st, c=c, s=s, z=z: w48(st, c, s, z) for (c, s, z) in sets4])
             rows.append({"K": K, "N": N, "M": M, "variant": "w4", "us": us4})
             rows.append({"K": K, "N": N, "M": M, "variant": "w8", "us": us8})
+            rows.append({"K": K, "N": N, "M": M, "variant": "w4a8", "us": us48})
             assert q.qlin_get_device_error() == 0
         del lin4, lin8, sets4, sets8
         torch.cuda.empty_cache()
@@ -479,6 +487,10 @@ def measure_crossover(peaks, l2):
                                 quant_in_w8=True)
     summary["how"] = ("W8A8 time = qlin_quant_act_fp8 + qlin_w8a8_fp8_gemm; both through the default dispatch; "
                       "roofline with the measured HBM and BF16 peaks, FP8 = 2 x BF16")
+    summary["w4a8_us"] = {"%dx%d" % (K, N): {str(r["M"]): round(r["us"], 2) for r in rows
+                                              if (r["K"], r["N"]) == (K, N) and r["variant"] == "w4a8"}
+                          for K, N in [(4096, 14336), (14336, 4096)]}
+    summary["w4a8_how"] = "W4A8 time = qlin_quant_act_fp8 + qlin_w4a8_gemm (INT4 weights, E4M3 tokens)"
     return summary
 
 
@@ -695,7 +707,7 @@ def run_sweep(args):
 
     import precision_quantized_linear_gb300 as q
     from precision_quantized_linear_gb300 import synthetic as syn
-    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8BlockLinear, W8A8Linear
+    from precision_quantized_linear_gb300.layers import W4A8Linear, W4A16Linear, W8A8BlockLinear, W8A8Linear
 
     torch.cuda.set_device(0)
     q.build()
@@ -712,7 +724,8 @@ def run_sweep(args):
     if args.sweep == "crossover":
         shapes = [(4096, 14336), (14336, 4096)]
         plan = [("w4", M) for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)] + \
-               [("w8", M) for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)]
+               [("w8", M) for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)] + \
+               [("w4a8", M) for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512)]
     elif args.sweep == "prefill":
         shapes = [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]
         plan = [("w8", M) for M in (2048, 8192)] + [("w4", M) for M in (2048, 8192)]
@@ -770,6 +783,22 @@ def run_sweep(args):
                            TFLOPS=round(flops / (us * 1e-6) / 1e12, 2), roof_us=round(t_roof, 2),
                            roof_frac=round(t_roof / us, 3),
                            bound="hbm" if alg / (bw * 1e9) > flops / (p16 * 1e12) else "tensor")
+            elif v == "w4a8":
+                lin48 = W4A8Linear.__new__(W4A8Linear)
+                lin48.N, lin48.K, lin48.G = N, K, 128
+                nb = q.qlin_workspace_size(q.OP_W4A8_GEMM, M, N, K)
+                ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+                q.qlin_quant_act_fp8(X, M, K, Xq, sx)
+                fns = [lambda st, c=c, s=s, z=z: q.qlin_w4a8_gemm(Xq, sx, c, s, z, Y, M, N, K, 128, ws, ws.numel(), st)
+                       for (c, s, z) in sets4]
+                us = time_launches(fns)
+                qus = time_launches([lambda st: q.qlin_quant_act_fp8(X, M, K, Xq, sx, st)])
+                alg = w4_alg_bytes(M, N, K) - M * K
+                t_roof = max(flops / (p8_use * 1e12), alg / (bw * 1e9)) * 1e6
+                row.update(us=round(us, 2), quant_us=round(qus, 2), weight_GBps=round(w4b / (us * 1e-6) / 1e9, 1),
+                           TFLOPS=round(flops / (us * 1e-6) / 1e12, 2), roof_us=round(t_roof, 2),
+                           roof_frac=round(t_roof / us, 3),
+                           bound="hbm" if alg / (bw * 1e9) > flops / (p8_use * 1e12) else "tensor")
             elif v == "w8b":
                 nb = q.qlin_workspace_size(q.OP_W8A8_BLOCK_GEMM, M, N, K)
                 ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")

@@ -40,8 +40,10 @@
  *  - M = 0 is a valid empty call: it returns QLIN_OK and launches nothing.
  *
  * Eligibility ([LP] S24): device sm_103 (compute capability 10.3);
- * G in {32, 64, 128} (the CUDA-core GEMV that serves small M when K % 256 != 0
- * and qlin_w4a16_gemv_noalloc take G = 128 only); N % 128 == 0; K % 128 == 0;
+ * G in {32, 64, 128}, or G == K for per-channel scales (one group spanning
+ * the row, [LP] S4 "per-channel"); the CUDA-core GEMV that serves small M
+ * when K % 256 != 0, qlin_w4a16_gemv_noalloc and qlin_w4a8_gemm take G = 128
+ * only; N % 128 == 0; K % 128 == 0;
  * 1 <= N, K; 0 <= M <= 2^24, and M <= 262140 (4 x 65535 token blocks of its
  * launch grid) wherever a call runs the CUDA-core GEMV (QLIN_PATH_GEMV with
  * K % 256 != 0, and qlin_w4a16_gemv_noalloc in that case); larger M returns
@@ -148,7 +150,9 @@ qlin_status_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, int G
  *          ((n/128)*(K/G) + g) * 128 + n%128.
  *   zeros  (N*K/(2G) bytes): nibble of (n, g) in byte
  *          ((n/128)*(K/G) + g) * 64 + (n%128)/2, low nibble for even n.
- *  Requires G in {32, 64, 128}, N % 128 == 0, K % 128 == 0.
+ *  Requires G in {32, 64, 128} or G == K (per-channel: K/G = 1 scale and
+ *  zero-point per row, found from the row's range over all of K), N % 128 ==
+ *  0, K % 128 == 0.
  */
 qlin_status_t qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes,
                  void* scales_f16, void* zeros_u4, void* stream);

@@ -203,10 +203,11 @@ def pack_canonical(wq: W4Quant):
 
 
 def pack_tile(wq: W4Quant):
-    """Tile layout, format version 2 (128 x 64 tiles, G = 32, 64 or 128): codes, scales, zeros as flat arrays."""
+    """Tile layout, format version 2 (128 x 64 tiles, G = 32, 64, 128, or K for one
+    group per row): codes, scales, zeros as flat arrays."""
     N, K = wq.q.shape
     G = wq.G
-    assert G in (32, 64, 128) and N % 128 == 0 and K % 128 == 0
+    assert (G in (32, 64, 128) or G == K) and N % 128 == 0 and K % 128 == 0
     codes = np.empty((N * K // 2,), np.uint8)
     scales = np.empty((N * K // G,), np.uint16)
     zeros = np.empty((N * K // G // 2,), np.uint8)

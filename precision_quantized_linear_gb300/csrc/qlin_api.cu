@@ -144,8 +144,10 @@ qlin_status_t cuda_status(cudaError_t e) {
 
 static qlin_status_t launch_status(cudaError_t e) { return cuda_status(e); }
 
-// W4A16 quantisation groups the kernels take ([LP] S4 per-group, S5 b_eff = 4 + 16 / G)
-static bool group_ok(int G) { return G == 32 || G == 64 || G == 128; }
+// W4A16 quantisation groups the kernels take ([LP] S4 per-group, S5 b_eff =
+// 4 + 16 / G): 32, 64 or 128 columns, or G == K, one group per row ([LP] S4
+// "per-channel")
+static bool group_ok(int G, int64_t K) { return G == 32 || G == 64 || G == 128 || (G > 0 && G == K); }
 
 // Validated output epilogue of the *_fused calls.
 static qlin_status_t make_epi(const void* bias_bf16, int act, Epi* epi) {
@@ -182,7 +184,7 @@ int qlin_gemv_max_m(int op) { return op == QLIN_OP_W8A8_GEMM ? g_gemv_max_m_w8 :
 
 qlin_status_t qlin_w4_packed_sizes(int64_t N, int64_t K, int G, size_t* codes, size_t* scales, size_t* zeros) {
   if (!codes || !scales || !zeros) return QLIN_ERR_INVALID_VALUE;
-  if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (!group_ok(G, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   qlin_status_t st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   *codes = static_cast<size_t>(N * K / 2);
@@ -264,7 +266,7 @@ qlin_status_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, int G
   if (st != QLIN_OK) return st;
   switch (op) {
     case QLIN_OP_W4A16_GEMM:
-      if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+      if (!group_ok(G, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
       *bytes = M == 0 ? 0 : ws_w4(M, N, K, G, d->num_sms);
       return QLIN_OK;
     case QLIN_OP_W8A8_GEMM: *bytes = M == 0 ? 0 : ws_w8(M, N, K, d->num_sms); return QLIN_OK;
@@ -295,7 +297,7 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
   }
   Dispatch dp;
   if (op == QLIN_OP_W4A16_GEMM) {
-    if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+    if (!group_ok(G, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
     st = dispatch_w4(M, N, K, G, path, num_sms, &dp);
   } else if (op == QLIN_OP_W8A8_GEMM) {
     st = dispatch_w8(M, N, K, path, num_sms, &dp);
@@ -344,7 +346,7 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
 
 qlin_status_t qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int symmetric, void* codes, void* scales_f16,
                  void* zeros_u4, void* stream) {
-  if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (!group_ok(G, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   qlin_status_t st = check_shape(0, N, K);
   if (st != QLIN_OK) return st;
   if (symmetric != 0 && symmetric != 1) return QLIN_ERR_INVALID_VALUE;
@@ -363,7 +365,7 @@ qlin_status_t qlin_pack_w4(const void* W_bf16, int64_t N, int64_t K, int G, int 
 static qlin_status_t w4a16_impl(const void* X_bf16, const void* codes, const void* scales_f16, const void* zeros_u4,
                       void* Y_bf16, int64_t M, int64_t N, int64_t K, int G, const Epi& epi, void* workspace,
                       size_t ws_bytes, int path, void* stream) {
-  if (!group_ok(G)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (!group_ok(G, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
   qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (path < QLIN_PATH_AUTO || path > QLIN_PATH_TC) return QLIN_ERR_INVALID_VALUE;

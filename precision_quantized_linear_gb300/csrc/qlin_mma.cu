@@ -113,7 +113,10 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
 }
 
 // NT: n8 token blocks, M <= 8 * NT (NT = 1, 2, 4); EPI: bias / activation
-// epilogue; G: quantisation group (32, 64, 128 columns)
+// epilogue; G: quantisation group (32, 64, 128 columns), or 256 for per-channel
+// scales (one group spanning K, folded once per 256-column stage: the fold is
+// linear, so per-stage folds with the row's one scale and zero-point sum to
+// the single fold over K)
 template <int NT, bool EPI, int G>
 __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma_kernel(
     const uint16_t* __restrict__ X, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
   const int s0 = split * stages_per_split;
   const int nst = static_cast<int>(imin64(KS, s0 + stages_per_split)) - s0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ngK = K / G;
+  const int64_t ngK = G == 256 ? 1 : K / G;  // groups per weight row
   const int64_t KB = K / kTileK;
   const int mrows = static_cast<int>(imin64(M, C::kTok));
 
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT>::kMinBlocks) w4a16_mma
     uint8_t* st = ring + (i % C::kStages) * C::kStage;
     uint64_t* bar = &full[i % C::kStages];
     const int64_t kb = static_cast<int64_t>(s0 + i) * 4;  // first 64-column block
-    const int64_t g0 = kb * 64 / G;  // first group
+    const int64_t g0 = G == 256 ? 0 : kb * 64 / G;  // first group
     mbar_arrive_expect_tx(bar, tx);
     bulk_load(st, codes + (static_cast<int64_t>(nt) * KB + kb) * 4096, kMmaCodeBytes, bar);
     bulk_load(st + kMmaMetaOff, scales + (static_cast<int64_t>(nt) * ngK + g0) * kTileN, C::kGps * 256, bar);
@@ -550,6 +553,7 @@ static int active_clusters(int ntb, int cs) {
 
 SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms, int G) {
   (void)num_sms;  // the cluster occupancy table already counts the SMs
+  if (G != 32 && G != 64 && G != 128) G = 256;  // per-channel scales (G == K): the 256-column instantiation
   SplitPlan p;
   const int64_t tiles = N / kTileN;
   const int64_t KS = K / kMmaStageCols;
@@ -566,7 +570,7 @@ SplitPlan plan_w4a16_mma(int64_t M, int64_t N, int64_t K, int num_sms, int G) {
     if (s != c) continue;
     const int cs = static_cast<int>(s);
     const int64_t fit = G == 32 ? active_clusters<32>(ntb, cs) : G == 64 ? active_clusters<64>(ntb, cs)
-                                                               : active_clusters<128>(ntb, cs);
+                      : G == 256 ? active_clusters<256>(ntb, cs) : active_clusters<128>(ntb, cs);
     if (fit <= 0) continue;
     const int64_t waves = (tiles + fit - 1) / fit;
     const double conc = static_cast<double>((tiles < fit ? tiles : fit) * s);  // CTAs running together
@@ -624,7 +628,8 @@ cudaError_t launch_w4a16_mma(const uint16_t* X, const uint8_t* codes, const uint
   auto by_group = [&](auto nt, auto ep) {
     if (G == 32) return go(nt, ep, std::integral_constant<int, 32>{});
     if (G == 64) return go(nt, ep, std::integral_constant<int, 64>{});
-    return go(nt, ep, std::integral_constant<int, 128>{});
+    if (G == 128) return go(nt, ep, std::integral_constant<int, 128>{});
+    return go(nt, ep, std::integral_constant<int, 256>{});  // per-channel: G == K
   };
   auto by_epi = [&](auto nt) { return fused ? by_group(nt, std::true_type{}) : by_group(nt, std::false_type{}); };
   if (M <= 8) return by_epi(std::integral_constant<int, 1>{});

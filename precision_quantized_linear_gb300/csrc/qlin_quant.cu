@@ -48,12 +48,86 @@ __device__ __forceinline__ float seg_max(float v, int seg) {
 // columns 4u, 4u+1 go to word 2(u%2) and 4u+2, 4u+3 to word 2(u%2)+1, both at
 // nibble positions u/2 and u/2 + 4, so each word is the OR of the lanes u,
 // u^2, u^4, u^6.
+// Scale and zero-point of one group from its range ([LP] S2-S3): lo, hi
+// include 0; s = fp16((hi - lo) / 15) (symmetric: fp16(amax / 7)); a scale
+// that rounds to 0 stores 1 and zero-point 0 (symmetric: 8).
+__device__ __forceinline__ void group_params(float lo, float hi, float amax, int symmetric, __half& s16, float& sc,
+                                             int& zp) {
+  const float s32 = symmetric ? __fdiv_rn(amax, 7.0f) : __fdiv_rn(hi - lo, 15.0f);
+  s16 = __float2half_rn(s32);
+  sc = __half2float(s16);
+  if (sc == 0.0f) {  // degenerate group: s = 1, logical zero-point 0
+    s16 = __float2half_rn(1.0f);
+    sc = 1.0f;
+    zp = symmetric ? 8 : 0;
+  } else if (symmetric) {
+    zp = 8;
+  } else {
+    float zf = rintf(__fdiv_rn(-lo, sc));
+    zf = fminf(fmaxf(zf, 0.0f), 15.0f);
+    zp = static_cast<int>(zf);
+  }
+}
+
+// Per-channel scales ([LP] S4 "per-channel": one group spanning the row): one
+// CTA per pair of rows reduces each row's range over all of K and writes the
+// two scales and their zero-point byte (tile layout with K / G = 1).
+__global__ void __launch_bounds__(256) row_range_kernel(const uint16_t* __restrict__ W, int64_t K, int symmetric,
+                                                        uint16_t* __restrict__ scales, uint8_t* __restrict__ zeros,
+                                                        int* err) {
+  __shared__ float red[3][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t zbyte = 0;
+  for (int sub = 0; sub < 2; ++sub) {
+    const int64_t n = blockIdx.x * 2 + sub;
+    const uint2* row = reinterpret_cast<const uint2*>(W + n * K);
+    float lo = 0.0f, hi = 0.0f, amax = 0.0f;
+    for (int64_t i = threadIdx.x; i < K / 4; i += 256) {
+      const uint2 raw = row[i];
+      const float v[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo = fminf(lo, v[j]);
+        hi = fmaxf(hi, v[j]);
+        amax = fmaxf(amax, fabsf(v[j]));
+      }
+    }
+    lo = warp_min(lo);
+    hi = warp_max(hi);
+    amax = warp_max(amax);
+    if (lane == 0) {
+      red[0][warp] = lo;
+      red[1][warp] = hi;
+      red[2][warp] = amax;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < 8; ++w) {
+        lo = fminf(lo, red[0][w]);
+        hi = fmaxf(hi, red[1][w]);
+        amax = fmaxf(amax, red[2][w]);
+      }
+      __half s16;
+      float sc;
+      int zp;
+      group_params(lo, hi, amax, symmetric, s16, sc, zp);
+      if (isinf(sc)) set_error(err, QLIN_ERR_INVALID_VALUE);
+      scales[(n / kTileN) * kTileN + n % kTileN] = __half_as_ushort(s16);
+      zbyte |= static_cast<uint32_t>(zp) << (4 * sub);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) zeros[(blockIdx.x * 2 / kTileN) * (kTileN / 2) + (blockIdx.x * 2 % kTileN) / 2] = zbyte;
+}
+
 __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict__ W, int64_t N, int64_t K,
                                                       int G, int symmetric, uint8_t* __restrict__ codes,
                                                       uint16_t* __restrict__ scales, uint8_t* __restrict__ zeros,
                                                       int* err) {
   const int lane = threadIdx.x & 31;
-  const int seg = G / 4;                    // lanes per group
+  // G == K beyond 128 columns: per-channel scales, already written by row_range_kernel
+  const bool pc = G > 128;
+  const int seg = pc ? 32 : G / 4;          // lanes per group (within a 128-column chunk)
   const int64_t ng = K / 128;               // chunks per row
   const int64_t ngk = K / G;                // groups per row
   const int64_t total = (N / 2) * ng;
@@ -69,32 +143,27 @@ __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict
       const int r = static_cast<int>(n % kTileN);
       const uint2 raw = *reinterpret_cast<const uint2*>(W + n * K + g * kGroup + 4 * lane);
       const float v[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-      float lo = 0.0f, hi = 0.0f, amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        lo = fminf(lo, v[i]);
-        hi = fmaxf(hi, v[i]);
-        amax = fmaxf(amax, fabsf(v[i]));
-      }
-      lo = seg_min(lo, seg);
-      hi = seg_max(hi, seg);
-      amax = seg_max(amax, seg);
-      const float s32 = symmetric ? __fdiv_rn(amax, 7.0f) : __fdiv_rn(hi - lo, 15.0f);
-      __half s16 = __float2half_rn(s32);
-      float sc = __half2float(s16);
+      __half s16;
+      float sc;
       int zp;
-      if (sc == 0.0f) {  // degenerate group: s = 1, logical zero-point 0
-        s16 = __float2half_rn(1.0f);
-        sc = 1.0f;
-        zp = symmetric ? 8 : 0;
-      } else if (symmetric) {
-        zp = 8;
+      if (pc) {  // the row's scale and zero-point from the range pass
+        s16 = __ushort_as_half(scales[nb * kTileN + r]);
+        sc = __half2float(s16);
+        zp = static_cast<int>((zeros[nb * (kTileN / 2) + r / 2] >> (4 * (r & 1))) & 15u);
       } else {
-        float zf = rintf(__fdiv_rn(-lo, sc));
-        zf = fminf(fmaxf(zf, 0.0f), 15.0f);
-        zp = static_cast<int>(zf);
+        float lo = 0.0f, hi = 0.0f, amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lo = fminf(lo, v[i]);
+          hi = fmaxf(hi, v[i]);
+          amax = fmaxf(amax, fabsf(v[i]));
+        }
+        lo = seg_min(lo, seg);
+        hi = seg_max(hi, seg);
+        amax = seg_max(amax, seg);
+        group_params(lo, hi, amax, symmetric, s16, sc, zp);
+        if (isinf(sc) && lane == 0) set_error(err, QLIN_ERR_INVALID_VALUE);
       }
-      if (isinf(sc) && lane == 0) set_error(err, QLIN_ERR_INVALID_VALUE);
       uint32_t cq[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -123,13 +192,14 @@ __global__ void __launch_bounds__(256) pack_w4_kernel(const uint16_t* __restrict
         *reinterpret_cast<uint2*>(codes + (nb * (K / kTileK) + kb) * 4096 + h * 2048 + r * 16 + u * 8) =
             make_uint2(wa, wb);
       }
+      if (pc) continue;  // scales and zero-points are in place
       const int64_t gg = g * (128 / G) + lane / seg;  // group of this lane's segment
       if (lane % seg == 0) {
         scales[(nb * ngk + gg) * kTileN + r] = __half_as_ushort(s16);
         zbyte |= static_cast<uint32_t>(zp) << (4 * sub);
       }
     }
-    if (lane % seg == 0)
+    if (!pc && lane % seg == 0)
       zeros[(nb * ngk + g * (128 / G) + lane / seg) * (kTileN / 2) + ((pair * 2) % kTileN) / 2] =
           static_cast<uint8_t>(zbyte);
   }
@@ -140,6 +210,11 @@ cudaError_t launch_pack_w4(const uint16_t* W, int64_t N, int64_t K, int G, int s
   const int64_t items = (N / 2) * (K / 128);
   const int64_t want = (items + 7) / 8;
   const int blocks = static_cast<int>(want < static_cast<int64_t>(num_sms) * 16 ? want : num_sms * 16);
+  if (G > 128) {  // per-channel: the row ranges first
+    row_range_kernel<<<static_cast<unsigned>(N / 2), 256, 0, st>>>(W, K, symmetric, scales, zeros, err);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   pack_w4_kernel<<<blocks, 256, 0, st>>>(W, N, K, G, symmetric, codes, scales, zeros, err);
   return cudaGetLastError();
 }

@@ -138,7 +138,8 @@ struct TcArgs {
   int units;         // ntiles * mblocks * splits
   int mb_fast;       // unit order: token block fastest (weights streamed once) or weight tile fastest
   int x_keep;        // keep activation tiles in L2 (evict-last) when they are small
-  int G;             // W4A16 quantisation group (32, 64, 128)
+  int G;             // W4A16 quantisation group (32, 64, 128, or K for per-channel scales)
+  int gshift;        // log2 G; 31 for per-channel scales, so that every column maps to group 0
   Epi epi;           // output epilogue (bias, activation); not used by block scaling
 };
 
@@ -271,7 +272,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         uint8_t* st = ring + s * C::kStage;
         const int kb = un.kb0 + j * KPS;
         if constexpr (W4) {
-          const int64_t g0 = (static_cast<int64_t>(kb) * C::kCols) >> (31 - __clz(a.G));
+          const int64_t g0 = (static_cast<int64_t>(kb) * C::kCols) >> a.gshift;
           const int64_t tpb = C::kCols / 64;  // packed code tiles per K block
           bulk_load_hint(st + KPS * C::kXBlk, a.codes + (static_cast<int64_t>(un.nt) * KB * tpb + kb * tpb) * 4096,
                          KPS * C::kWBlk, &full[s], pol_stream);
@@ -688,7 +689,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
       };
       if (a.G == 32) dq_loop(std::integral_constant<int, 5>{});
       else if (a.G == 64) dq_loop(std::integral_constant<int, 6>{});
-      else dq_loop(std::integral_constant<int, 7>{});
+      else if (a.G == 128) dq_loop(std::integral_constant<int, 7>{});
+      else dq_loop(std::integral_constant<int, 31>{});  // per-channel (G == K): the group index is always 0
       if (!ok) {
         set_error(a.err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
@@ -1406,6 +1408,7 @@ cudaError_t launch_w4a16_tc(const uint16_t* X, const uint8_t* codes, const uint1
   a.scales = scales;
   a.zeros = zeros;
   a.G = G;
+  a.gshift = G == 32 ? 5 : G == 64 ? 6 : G == 128 ? 7 : 31;
   a.Y = Y;
   a.err = err;
   a.M = M;
@@ -1449,6 +1452,7 @@ cudaError_t launch_w4a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* co
   a.scales = scales;
   a.zeros = zeros;
   a.G = kGroup;
+  a.gshift = 7;
   a.sx = sx;
   a.Y = Y;
   a.err = err;

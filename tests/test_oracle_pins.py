@@ -695,3 +695,33 @@ def test_w4a8_brute_force_triple_loop():
                 acc += float(sx[m]) * tab[Xq[m, k]] * deq[n, k]
             want[m, n] = acc
     np.testing.assert_allclose(oracle.w4a8_full(Xq, sx, wq), want, rtol=1e-12, atol=1e-300)
+
+
+# ---- per-channel W4 scales ([LP] S4 "per-channel": one scale spanning the row, G = K)
+
+def test_per_channel_equals_per_group_when_every_group_spans_the_row_range():
+    # each row repeats one 128-column pattern: every group has the row's min / max,
+    # so one group over K and groups of 128 give the same scale, zero-point and codes
+    rng = np.random.default_rng(41)
+    pat = (rng.standard_normal((128, 128)) * 0.02).astype(np.float32)
+    W = syn.f32_to_bf16_bits(np.tile(pat, (1, 8)))          # [128, 1024]
+    pc = oracle.quantize_w4(W, G=1024)
+    pg = oracle.quantize_w4(W, G=128)
+    assert pc.s.shape == (128, 1) and pg.s.shape == (128, 8)
+    assert np.array_equal(pc.q, pg.q)
+    assert (pg.s == pc.s).all() and (pg.z == pc.z).all()
+
+
+def test_per_channel_scale_closed_form():
+    W = syn.make_weight(256, 2048, seed=42)
+    wq = oracle.quantize_w4(W, G=2048)
+    w = syn.bf16_bits_to_f32(W)
+    lo = np.minimum(w.min(axis=1), 0.0).astype(np.float32)
+    hi = np.maximum(w.max(axis=1), 0.0).astype(np.float32)
+    s16 = ((hi - lo) / np.float32(15.0)).astype(np.float32).astype(np.float16)   # binary32 divide, RNE to binary16
+    assert np.array_equal(wq.s[:, 0], s16.view(np.uint16))
+    deq = oracle.dequant_w4(wq)
+    sc = s16.astype(np.float64)[:, None]
+    assert (np.abs(deq - w) <= sc / 2 * (1 + 2.0 ** -20)).all()   # round-trip bound inside the range
+    c, s, z = oracle.pack_tile(wq)
+    assert np.array_equal(s.reshape(2, 128), wq.s[:, 0].reshape(2, 128))       # one scale per row, tile order
