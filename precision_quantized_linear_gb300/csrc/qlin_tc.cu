@@ -58,17 +58,21 @@ struct TcCfg {
   // MXFP8: the E8M0 scale atoms of the stage's K block (512 bytes of weight
   // scales, then 512 of token scales), copied into TMEM by the MMA thread
   static constexpr int kSfOff = KPS * kXBlk + KPS * kWBlk + kMetaBytes;
-  static constexpr int kSfBytes = MX ? 1024 : 0;
+  static constexpr int kSfbAtoms = BN > 128 ? 2 : 1;                // token atoms of a tile
+  static constexpr int kSfBytes = MX ? ((512 * (1 + kSfbAtoms) + 1023) / 1024) * 1024 : 0;
   static constexpr int kStage = KPS * kXBlk + KPS * kWBlk + kMetaBytes + kSfBytes;
-  static constexpr int kTxBase = KPS * kXBlk + KPS * kWBlk + kSfBytes;  // W4A16: plus 320 bytes per group loaded
+  static constexpr int kTxBase = KPS * kXBlk + KPS * kWBlk + (MX ? 512 * (1 + kSfbAtoms) : 0);  // W4A16: plus 320 B per group
   // dequantised BF16 weight tiles: in TMEM (tcgen05.st, read by the MMA as
   // its A operand) when the accumulators leave room, else in shared memory
   static constexpr bool kATmem = W4 && BN <= 128;
-  // A slots: one K block each (W4A16: 64 BF16 columns, W4A8: 128 E4M3 columns,
-  // both 32 TMEM columns of a 128-lane slot)
-  static constexpr int kAStages = W4 ? (kATmem ? 8 : 4) : 0;
+  // A slots: W4A16 in TMEM hands the MMA two 64-column blocks per slot (64
+  // TMEM columns), so that the issuing thread's fixed cost per hand-off (a
+  // barrier wait, a fence, a commit) is paid once per 128 columns; W4A8 one
+  // 128-column E4M3 block (32 columns); the shared-memory path one 64-column block
+  static constexpr int kSlotBlocks = (kATmem && !A8) ? 2 : 1;
+  static constexpr int kAStages = W4 ? (kATmem ? (A8 ? 8 : 4) : 4) : 0;
   static constexpr int kAStage = (W4 && !kATmem) ? 128 * kBlkBytes : 0;  // shared-memory bytes per slot
-  static constexpr int kASlotCols = 32;                         // TMEM columns per slot (64 BF16 per lane)
+  static constexpr int kASlotCols = 32 * kSlotBlocks;           // TMEM columns per slot (64 BF16 per lane and block)
   // output staging: two boxes of 16 tokens x 128 rows of BF16 for the tensor stores
   // Block scaling with 128-token tiles runs token-major: the token tile is the
   // MMA's A operand (TMEM lane = token) and the weight tile of WN rows (one or
@@ -88,14 +92,16 @@ struct TcCfg {
   static constexpr int kAccCols = kTokM ? WN : BN;              // one accumulator
   // accumulators in TMEM: two (one unit while the epilogue drains the other);
   // block scaling and W4A8 keep up to four K-block partial products in flight
-  static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : (A8 ? 4 : 2);
+  // MXFP8 with 256-token tiles keeps one (the scale-factor ring takes the rest of TMEM)
+  static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : A8 ? 4 : (MX && BN == 256) ? 1 : 2;
   static constexpr int kAColBase = kAccBufs * BN;               // first TMEM column of the A slots
   // MXFP8 scale factors in TMEM: a ring of kSfSlots K blocks, four columns of
   // weight scales and four of token scales each (see mma_mx8)
   static constexpr int kSfSlots = MX ? 4 : 0;
   static constexpr int kSfaCol = kAccBufs * BN;
-  static constexpr int kSfbCol = kSfaCol + 4 * kSfSlots;
-  static constexpr int kTmemNeed = kAccBufs * BN + (kATmem ? kAStages * kASlotCols : 0) + 8 * kSfSlots;
+  static constexpr int kSfbCol = kSfaCol + 4 * kSfSlots;  // token scales: 4 columns per atom and slot
+  static constexpr int kTmemNeed =
+      kAccBufs * BN + (kATmem ? kAStages * kASlotCols : 0) + 4 * kSfSlots * (1 + kSfbAtoms);
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                  : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kDqWarps = W4 ? 8 : 0;
@@ -114,8 +120,9 @@ struct TcCfg {
   static_assert(kTmemNeed <= 512, "TMEM budget");
   static_assert(!BS || (!W4 && BN <= 128), "block scaling: E4M3 operands, at most 128 tokens (running sums in registers)");
   static_assert(WN == 128 || (kTokM && WN == 256), "256-row weight tiles only token-major");
-  static_assert(!MX || (!W4 && !BS && BN >= 32 && BN <= 128), "MXFP8: E4M3 operands, 32..128 tokens per tile");
+  static_assert(!MX || (!W4 && !BS && BN >= 32), "MXFP8: E4M3 operands, at least 32 tokens per tile");
   static_assert(!A8 || (W4 && !BS && !MX && BN <= 64), "W4A8: packed INT4 weights, at most 64 tokens per tile");
+  static_assert(kSlotBlocks == 1 || KPS % 2 == 0, "two-block slots need an even number of blocks per stage");
 };
 
 struct TcArgs {
@@ -295,9 +302,16 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
 #pragma unroll
         for (int i = 0; i < KPS; ++i)
           tma_load_2d_hint(st + i * C::kXBlk, &tmap_x, &full[s], (kb + i) * C::kCols, un.mb * BN, pol_keep);
-        if constexpr (MX)  // the scale atom of the 128 tokens holding this token block
-          bulk_load(st + C::kSfOff + 512, a.sfb + ((static_cast<int64_t>(un.mb) * BN / 128) * KB + kb) * 512, 512,
-                    &full[s]);
+        if constexpr (MX) {  // the scale atom(s) of the 128 tokens holding this token block
+          const int64_t natoms = (a.M + 127) / 128;  // atoms the caller's buffer holds
+#pragma unroll
+          for (int t = 0; t < C::kSfbAtoms; ++t) {
+            // a 256-token tile past the last atom takes that atom again: its
+            // tokens are beyond M (zero rows, outputs never written)
+            const int64_t atom = imin64(static_cast<int64_t>(un.mb) * BN / 128 + t, natoms - 1);
+            bulk_load(st + C::kSfOff + 512 * (1 + t), a.sfb + (atom * KB + kb) * 512, 512, &full[s]);
+          }
+        }
       };
       int it = 0;
       // phase 1: weights of the first ring pass
@@ -377,8 +391,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++ua) {
         const Unit un = unit_of(a, u, KB);
-        const int acc = ua & 1;
-        if (!mbar_wait(&acc_empty[acc], ((ua >> 1) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+        const int acc = ua % C::kAccBufs;
+        if (!mbar_wait(&acc_empty[acc], ((ua / C::kAccBufs) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
           ok = false;
           break;
         }
@@ -392,11 +406,14 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
             break;
           }
           tc_fence_after();
-          const uint32_t slot = static_cast<uint32_t>(it % C::kSfSlots) * 4;
-          const uint32_t t_sfa = tmem_base + C::kSfaCol + slot, t_sfb = tmem_base + C::kSfbCol + slot;
+          const uint32_t slot = static_cast<uint32_t>(it % C::kSfSlots);
+          const uint32_t t_sfa = tmem_base + C::kSfaCol + slot * 4;
+          const uint32_t t_sfb = tmem_base + C::kSfbCol + slot * 4 * C::kSfbAtoms;
           const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
           tc_cp_atom(t_sfa, sdesc_atom(st_u32 + C::kSfOff));
-          tc_cp_atom(t_sfb, sdesc_atom(st_u32 + C::kSfOff + 512));
+#pragma unroll
+          for (int t = 0; t < C::kSfbAtoms; ++t)  // tokens 128 t .. read columns 4 t ..
+            tc_cp_atom(t_sfb + 4 * t, sdesc_atom(st_u32 + C::kSfOff + 512 * (1 + t)));
           const uint32_t a_addr = st_u32 + C::kXBlk, b_addr = st_u32;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -451,14 +468,62 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         set_error(a.err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
       }
+    } else if (lane == 0 && C::kSlotBlocks == 2) {
+      // W4A16 with A in TMEM: per slot (two 64-column blocks) one barrier wait,
+      // eight MMAs with the B descriptors stepped by 32 bytes, one commit
+      constexpr uint32_t idesc = idesc_make(1, 1, 128, BN);
+      int it = 0, pit = 0, ua = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++ua) {
+        const Unit un = unit_of(a, u, KB);
+        const int acc = ua % C::kAccBufs;
+        if (!mbar_wait(&acc_empty[acc], ((ua / C::kAccBufs) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + acc * C::kAccCols;
+        for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
+          const int s = it % C::kStages;
+          if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
+#pragma unroll
+          for (int ip = 0; ip < KPS / 2; ++ip, ++pit) {
+            const int ai = pit % C::kAStages;
+            if (!mbar_wait(&a_full[ai], (pit / C::kAStages) & 1, kWaitLimitNs, &s_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_slot = tmem_base + C::kAColBase + ai * C::kASlotCols;
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+              const uint64_t bd = sdesc_sw128(st_u32 + (2 * ip + blk) * C::kXBlk);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)  // 16 BF16 of K per MMA: 8 TMEM columns of A, 32 bytes of B
+                mma_f16_tmem_a(tmem_d, a_slot + blk * 32 + kk * 8, bd + 2 * kk, idesc, (j | ip | blk | kk) != 0);
+            }
+            mma_commit(&a_empty[ai]);
+          }
+          mma_commit(&empty[s]);
+        }
+        mma_commit(&acc_full[acc]);  // arrives when this unit's MMAs are done
+      }
+      if (!ok) {
+        set_error(a.err, QLIN_ERR_TIMEOUT);
+        s_abort = 1;
+      }
     } else if (lane == 0) {
       constexpr uint32_t idesc = W4 ? idesc_make(1, 1, 128, BN) : idesc_make(0, 0, 128, BN);
       int it = 0, ait = 0, ua = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++ua) {
         const Unit un = unit_of(a, u, KB);
-        const int acc = ua & 1;
-        if (!mbar_wait(&acc_empty[acc], ((ua >> 1) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
+        const int acc = ua % C::kAccBufs;
+        if (!mbar_wait(&acc_empty[acc], ((ua / C::kAccBufs) & 1) ^ 1, kWaitLimitNs, &s_abort)) {
           ok = false;
           break;
         }
@@ -640,30 +705,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
                 if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
               }
               if (!mine) continue;
-              if constexpr (C::kATmem) {
-                // lane r of the slot holds row r: 32 columns x two BF16 = the 64 columns of the block
-                tc_fence_after();
-  #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[h]);
-                  const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[h]);
-                  const uint32_t words[4] = {c[h].x, c[h].y, c[h].z, c[h].w};
-                  uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
-  #pragma unroll
-                  for (int t = 0; t < 4; ++t) {
-                    const uint4 d = dequant8(words[t], zoff, s2);
-                    v[t] = d.x;
-                    v[4 + t] = d.y;
-                    v[8 + t] = d.z;
-                    v[12 + t] = d.w;
-                  }
-                  tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
-                                h * 16,
-                            v);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-              } else {
+              {
                 uint8_t* arow = aring + ai * C::kAStage + r * 128;
   #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -687,10 +729,98 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
           }
         }
       };
-      if (a.G == 32) dq_loop(std::integral_constant<int, 5>{});
-      else if (a.G == 64) dq_loop(std::integral_constant<int, 6>{});
-      else if (a.G == 128) dq_loop(std::integral_constant<int, 7>{});
-      else dq_loop(std::integral_constant<int, 31>{});  // per-channel (G == K): the group index is always 0
+      // A in TMEM: a group takes two consecutive blocks (one slot) in turn;
+      // lane r of the slot holds row r, 32 columns x two BF16 per block
+      auto dq_pairs = [&](auto gconst) {
+        constexpr int gshift = decltype(gconst)::value;  // log2 G (31: per-channel)
+        int pit = 0;
+        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+          const Unit un = unit_of(a, u, KB);
+          for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
+            const int s = it % C::kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort))) {
+              ok = false;
+              break;
+            }
+            const uint32_t sts = smem_u32(ring + s * C::kStage);
+            const int kb = un.kb0 + j * KPS;
+#pragma unroll
+            for (int ip = 0; ip < KPS / 2; ++ip, ++pit) {
+              const bool mine = (pit & 1) == grp;
+              const int ai = pit % C::kAStages;
+              uint4 c[2][2];
+              float scale[2][2] = {}, zq[2][2] = {};  // [block][32-column half]
+              if (mine) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&a_empty[ai], ((pit / C::kAStages) & 1) ^ 1, kWaitLimitNs, &s_abort))) {
+                  ok = false;
+                  break;
+                }
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                  const int i = 2 * ip + blk;
+                  c[blk][0] = lds128(sts + KPS * C::kXBlk + i * 4096 + r * 16);         // columns 0..31
+                  c[blk][1] = lds128(sts + KPS * C::kXBlk + i * 4096 + 2048 + r * 16);  // columns 32..63
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && gshift > 5) {  // G >= 64: both halves in one group
+                      scale[blk][1] = scale[blk][0];
+                      zq[blk][1] = zq[blk][0];
+                      break;
+                    }
+                    const int gi = (((kb + i) * 64 + h * 32) >> gshift) - ((kb * 64) >> gshift);
+                    scale[blk][h] = __half2float(
+                        __ushort_as_half(static_cast<unsigned short>(lds16(sts + C::kScaleOff + gi * 256 + r * 2))));
+                    const uint32_t zb = lds8(sts + C::kZeroOff + gi * 64 + r / 2);
+                    zq[blk][h] = static_cast<float>((r & 1) ? (zb >> 4) : (zb & 15u));
+                  }
+                }
+              }
+              if (ip == KPS / 2 - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);  // this warp has read all of the stage it needs
+              }
+              if (!mine) continue;
+              tc_fence_after();
+#pragma unroll
+              for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const __nv_bfloat162 zoff = __float2bfloat162_rn(128.0f + zq[blk][h]);
+                  const __nv_bfloat162 s2 = __float2bfloat162_rn(scale[blk][h]);
+                  const uint32_t words[4] = {c[blk][h].x, c[blk][h].y, c[blk][h].z, c[blk][h].w};
+                  uint32_t v[16];  // v[p] = columns 2p, 2p+1 of the half; pair p = 4i + t is word t, position i
+#pragma unroll
+                  for (int t = 0; t < 4; ++t) {
+                    const uint4 d = dequant8(words[t], zoff, s2);
+                    v[t] = d.x;
+                    v[4 + t] = d.y;
+                    v[8 + t] = d.z;
+                    v[12 + t] = d.w;
+                  }
+                  tmem_st16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase + ai * C::kASlotCols +
+                                blk * 32 + h * 16,
+                            v);
+                }
+              tmem_st_wait();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&a_full[ai]);
+            }
+          }
+        }
+      };
+      if constexpr (C::kATmem) {
+        if (a.G == 32) dq_pairs(std::integral_constant<int, 5>{});
+        else if (a.G == 64) dq_pairs(std::integral_constant<int, 6>{});
+        else if (a.G == 128) dq_pairs(std::integral_constant<int, 7>{});
+        else dq_pairs(std::integral_constant<int, 31>{});  // per-channel (G == K): the group index is always 0
+      } else {
+        if (a.G == 32) dq_loop(std::integral_constant<int, 5>{});
+        else if (a.G == 64) dq_loop(std::integral_constant<int, 6>{});
+        else if (a.G == 128) dq_loop(std::integral_constant<int, 7>{});
+        else dq_loop(std::integral_constant<int, 31>{});  // per-channel (G == K): the group index is always 0
+      }
       if (!ok) {
         set_error(a.err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
@@ -1045,12 +1175,13 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         continue;
       }
       const Unit un = unit_of(a, u, KB);
-      const int acc = ua & 1;
+      const int acc = ua % C::kAccBufs;
       const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
       const float bias_n = EPI ? epi_bias(a.epi, n) : 0.0f;  // loaded while the MMAs run
       // A warp whose wait gave up skips this unit's data but keeps taking part
       // in the named barriers below, so that they always see all 128 threads.
-      const bool have = __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (ua >> 1) & 1, kWaitLimitNs, &s_abort));
+      const bool have =
+          __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (ua / C::kAccBufs) & 1, kWaitLimitNs, &s_abort));
       if (!have) {
         set_error(a.err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
@@ -1191,19 +1322,20 @@ static int pick_bn(int64_t M) {
 }
 
 // Cost of a unit on one SM in cycles at 2.07 GHz, measured on GB300 per token
-// tile (64 / 128 / 256 tokens) with the split count forced: cycles per K block
-// (64 columns W4A16, 128 E4M3), a start-up and drain cost paid once per CTA,
-// and the split-K fix-up of a unit (partial sums written, the last arriver's
-// reduction), which grows with the tile and, by half again per extra split,
-// with the split count.
+// tile: cycles per K block (64 columns W4A16, 128 E4M3), a start-up and drain
+// cost paid once per CTA, and the split-K fix-up of a unit (partial sums
+// written, the last arriver's reduction), which grows with the tile and, by
+// half again per extra split, with the split count.  W4A16 (16 .. 256 tokens)
+// from one unit per SM at three depths of K, a linear fit; E4M3 (64 .. 256)
+// with the split count forced.
 struct TcCost {
   double kb, once, fix;
 };
 static TcCost tc_cost(bool w4, int bn) {
-  const int i = bn >= 256 ? 2 : bn >= 128 ? 1 : 0;
-  static const double kb8[3] = {590, 594, 657}, once8[3] = {10.5e3, 15e3, 24.5e3};
-  static const double kb4[3] = {713, 906, 924}, once4[3] = {11e3, 8.9e3, 16.7e3};
-  static const double fix[3] = {23e3, 40e3, 70e3};
+  const int i = bn >= 256 ? 4 : bn >= 128 ? 3 : bn >= 64 ? 2 : bn >= 32 ? 1 : 0;
+  static const double kb8[5] = {590, 590, 590, 594, 657}, once8[5] = {10.5e3, 10.5e3, 10.5e3, 15e3, 24.5e3};
+  static const double kb4[5] = {539, 541, 597, 616, 927}, once4[5] = {13.1e3, 13e3, 15.1e3, 17.4e3, 24e3};
+  static const double fix[5] = {12e3, 16e3, 23e3, 40e3, 70e3};
   return TcCost{w4 ? kb4[i] : kb8[i], w4 ? once4[i] : once8[i], fix[i]};
 }
 
@@ -1217,9 +1349,12 @@ static void plan_tc_joint(TcPlan& p, int64_t M, int64_t N, int64_t K, int num_sm
   const double ybytes = 2.0 * static_cast<double>(M) * static_cast<double>(N);
   double best = 1e30;
   const int top = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
-  for (int bn = top; bn >= 64; bn /= 2) {
+  const int low = w4 ? 16 : 64;  // W4A16 plans every token tile this way
+  for (int bn = top; bn >= low; bn /= 2) {
     const TcCost cost = tc_cost(w4, bn);
-    const int kps = (w4 && bn <= 64 && KB % 2 == 0) ? 2 : 1;
+    // A in TMEM (BN <= 128): slots of two blocks; narrow tiles four blocks per
+    // stage, so that a stage still carries enough bytes
+    const int kps = (w4 && bn <= 32 && KB % 4 == 0) ? 4 : (w4 && bn <= 128) ? 2 : 1;
     const int64_t KS = KB / kps;
     const int64_t mblocks = (M + bn - 1) / bn;
     const int64_t tiles = (N / kTileN) * mblocks;
@@ -1256,7 +1391,7 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bo
   TcPlan p;
   p.bn = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
   p.wn = tile_n;
-  if (joint && p.bn >= 64 && tile_n == kTileN) {
+  if (joint && (p.bn >= 64 || w4) && tile_n == kTileN) {
     plan_tc_joint(p, M, N, K, num_sms, cols, w4, max_bn);
     return p;
   }
@@ -1268,7 +1403,7 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bo
   // in flight per SM
   p.kps = 1;
   if (w4 && p.bn <= 32 && KB % 4 == 0) p.kps = 4;
-  else if (w4 && p.bn <= 64 && KB % 2 == 0) p.kps = 2;
+  else if (w4 && p.bn <= 128) p.kps = 2;  // A in TMEM: slots of two blocks (K % 128 == 0 makes KB even)
   const int64_t KS = KB / p.kps;  // stages along K
   // Split K by a small cost model: the time of a split count c is the larger
   // of the memory time (all bytes at the HBM rate, or one unit's bytes at a
@@ -1314,17 +1449,17 @@ static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bo
 
 TcPlan plan_w4a16_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 64, true); }
 TcPlan plan_w8a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false); }
-// MXFP8 runs on the E4M3 tile plan with 32 to 128 tokens per tile: a token
-// tile then starts on a 32-token boundary of its scale atom (the MMA reads a
-// tile's token scales from whole TMEM columns of 32 lanes), and two
-// accumulators of 128 columns leave room for the scale-factor ring.
 // W4A8: K blocks of 128 columns (one quantisation group, two code tiles) and
 // at most 64 tokens per tile (the promotion keeps a row's running sums in
 // registers); the E4M3 tile plan with those limits.
 TcPlan plan_w4a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_tc(M, N, K, num_sms, 128, false, 64); }
 
+// MXFP8 runs on the E4M3 tile plan with at least 32 tokens per tile: a token
+// tile then starts on a 32-token boundary of its scale atom (the MMA reads a
+// tile's token scales from whole TMEM columns of 32 lanes).  256-token tiles
+// keep one accumulator: two would leave no TMEM for the scale-factor ring.
 TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
-  TcPlan p = plan_tc(M, N, K, num_sms, 128, false, 128);
+  TcPlan p = plan_tc(M, N, K, num_sms, 128, false, 256);
   if (p.bn < 32) p.bn = 32;  // the same single token block for M <= 16
   return p;
 }
@@ -1382,7 +1517,7 @@ static cudaError_t launch_tc_bn(const CUtensorMap& tx, const CUtensorMap& tw, co
     if (plan.bn == 32) return plan.kps == 4 ? launch_tc<32, true, 4, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st)
                                             : launch_tc<32, true, 2, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
     if (plan.bn == 64) return launch_tc<64, true, 2, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
-    if (plan.bn == 128) return launch_tc<128, true, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    if (plan.bn == 128) return launch_tc<128, true, 2, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
     return launch_tc<256, true, 1, false, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
   } else {
     switch (plan.bn) {
@@ -1485,7 +1620,8 @@ cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t*
   switch (plan.bn) {
     case 32: return launch_tc<32, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
     case 64: return launch_tc<64, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    default: return launch_tc<128, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 128: return launch_tc<128, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default: return launch_tc<256, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
   }
 }
 

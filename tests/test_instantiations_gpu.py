@@ -41,24 +41,25 @@ def _plan(op, M, N, K, path):
 # (id, M, N, K, act, expected plan fields) -- W4A16 on QLIN_PATH_TC:
 # tc_gemm_kernel<BN, W4 = true, KPS, BS = false, WN = 128, EPI = act != none>
 W4_TC = [
-    ("bn16_kps4", 16, 512, 1024, NONE, dict(tokens_per_tile=16, kblocks_per_stage=4, a_in_tmem=1)),
-    ("bn16_kps2", 9, 512, 4224, NONE, dict(tokens_per_tile=16, kblocks_per_stage=2)),
-    ("bn32_kps4", 32, 512, 1024, NONE, dict(tokens_per_tile=32, kblocks_per_stage=4)),
-    ("bn32_kps2", 24, 512, 4224, NONE, dict(tokens_per_tile=32, kblocks_per_stage=2)),
-    ("bn64", 64, 4096, 4096, NONE, dict(tokens_per_tile=64, kblocks_per_stage=2, splits=1)),
-    ("bn64_split", 64, 4096, 14336, NONE, dict(tokens_per_tile=64, splits=4)),
-    ("bn128", 128, 14336, 4096, NONE, dict(tokens_per_tile=128, kblocks_per_stage=1, a_in_tmem=1, splits=1)),
-    ("bn128_split", 200, 4096, 14336, NONE, dict(tokens_per_tile=128, splits=2)),
-    ("bn256", 512, 14336, 4096, NONE, dict(tokens_per_tile=256, a_in_tmem=0, splits=1)),
-    ("bn256_split", 512, 4096, 14336, NONE, dict(tokens_per_tile=256, a_in_tmem=0, splits=2)),
+    ("bn16_kps4", 16, 512, 1024, NONE, dict(tokens_per_tile=16, kblocks_per_stage=4, a_in_tmem=1, splits=1)),
+    ("bn16_kps4_split", 1, 512, 4096, NONE, dict(tokens_per_tile=16, kblocks_per_stage=4, splits=2)),
+    ("bn16_kps2", 9, 512, 4224, NONE, dict(tokens_per_tile=16, kblocks_per_stage=2, splits=3)),
+    ("bn32_kps4", 20, 512, 1024, NONE, dict(tokens_per_tile=32, kblocks_per_stage=4)),
+    ("bn32_kps4_split", 20, 6144, 4096, NONE, dict(tokens_per_tile=32, kblocks_per_stage=4, splits=2)),
+    ("bn32_kps2", 20, 6144, 4224, NONE, dict(tokens_per_tile=32, kblocks_per_stage=2, splits=2)),
+    ("bn64", 40, 14336, 1024, NONE, dict(tokens_per_tile=64, kblocks_per_stage=2, splits=1)),
+    ("bn64_split", 40, 6144, 8192, NONE, dict(tokens_per_tile=64, splits=3)),
+    ("bn128", 300, 4096, 1024, NONE, dict(tokens_per_tile=128, kblocks_per_stage=2, a_in_tmem=1, splits=1)),
+    ("bn128_split", 100, 6144, 14336, NONE, dict(tokens_per_tile=128, kblocks_per_stage=2, splits=3)),
+    ("bn256", 160, 14336, 4096, NONE, dict(tokens_per_tile=256, kblocks_per_stage=1, a_in_tmem=0, splits=1)),
     ("bn16_kps4_epi", 5, 512, 1024, SILU, dict(tokens_per_tile=16, kblocks_per_stage=4)),
     ("bn16_kps2_epi", 3, 512, 4224, GELU, dict(tokens_per_tile=16, kblocks_per_stage=2)),
-    ("bn32_kps4_epi", 20, 512, 1024, GELU, dict(tokens_per_tile=32, kblocks_per_stage=4)),
-    ("bn32_kps2_epi", 32, 512, 4224, SILU, dict(tokens_per_tile=32, kblocks_per_stage=2)),
-    ("bn64_split_epi", 64, 4096, 14336, SILU, dict(tokens_per_tile=64, splits=4)),
-    ("bn128_epi", 128, 14336, 4096, GELU, dict(tokens_per_tile=128, splits=1)),
-    ("bn256_epi", 512, 14336, 4096, SILU, dict(tokens_per_tile=256, splits=1)),
-    ("bn256_split_epi", 512, 4096, 14336, GELU, dict(tokens_per_tile=256, splits=2)),
+    ("bn32_kps4_epi", 20, 6144, 4096, GELU, dict(tokens_per_tile=32, kblocks_per_stage=4, splits=2)),
+    ("bn32_kps2_epi", 20, 6144, 4224, SILU, dict(tokens_per_tile=32, kblocks_per_stage=2)),
+    ("bn64_split_epi", 40, 6144, 8192, SILU, dict(tokens_per_tile=64, splits=3)),
+    ("bn128_epi", 300, 4096, 1024, GELU, dict(tokens_per_tile=128, kblocks_per_stage=2)),
+    ("bn128_split_epi", 100, 6144, 14336, SILU, dict(tokens_per_tile=128, splits=3)),
+    ("bn256_epi", 160, 14336, 4096, SILU, dict(tokens_per_tile=256, splits=1)),
 ]
 
 

@@ -57,8 +57,10 @@ GEMM_CASES = [
     ("bn64_split", 64, 4096, 14336, 64, 2),
     ("bn64_ragged", 300, 512, 1024, 64, 1),
     ("bn128", 128, 14336, 4096, 128, 1),
-    ("bn128_prefill", 2048, 4096, 4096, 128, 1),
-    ("bn128_prefill_gateup", 2048, 28672, 4096, 128, 1),
+    ("bn128_ragged", 300, 4096, 4096, 128, 1),
+    ("bn256_prefill", 2048, 4096, 4096, 256, 1),
+    ("bn256_prefill_gateup", 2048, 28672, 4096, 256, 1),
+    ("bn256_odd_atoms", 300, 14336, 4096, 256, 1),   # 3 token atoms: the last tile's second atom is past M
 ]
 
 
