@@ -160,3 +160,17 @@ def test_w8a8_block_tc_instantiation(case):
             wd = tab[Wq_r[ns]] * np.repeat(ws.astype(np.float64), 128, axis=1)
             check(Y[np.ix_(ms, ns)], ref, np.linalg.norm(xd, axis=1), np.linalg.norm(wd, axis=1), 0,
                   "tile m%d n%d" % (ms[0], ns[0]))
+
+
+@pytest.mark.parametrize("M", [1, 3, 7])
+def test_w8a8_gemv_k_not_256(M):
+    # K % 256 != 0 on the small-M path: the CUDA-core E4M3 GEMV with its split-K sums in the workspace
+    N, K = 512, 4224
+    plan = _plan(q.OP_W8A8_GEMM, M, N, K, q.PATH_GEMV)
+    assert plan["kernel"] == q.KERNEL_W8A8_GEMV
+    W = syn.make_weight(N, K, seed=M + 70)
+    X = syn.make_act(M, K, seed=M + 71)
+    Xq, sx = oracle.quant_fp8_rows(X)
+    Wq, sw = oracle.quant_fp8_tensor(W)
+    Y = host_f64(W8A8Linear(to_dev(W))(to_dev(X), path=q.PATH_GEMV))
+    check_w8(Y, Xq, sx, Wq, sw, full=True, tm=16, seed=M)
