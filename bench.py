@@ -850,7 +850,7 @@ def run_case(args):
 
     import precision_quantized_linear_gb300 as q
     from precision_quantized_linear_gb300 import synthetic as syn
-    from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8BlockLinear, W8A8Linear
+    from precision_quantized_linear_gb300.layers import MXFP8Linear, W4A8Linear, W4A16Linear, W8A8BlockLinear, W8A8Linear
 
     torch.cuda.set_device(0)
     q.build()
@@ -862,6 +862,14 @@ def run_case(args):
     if args.case == "w4a16":
         lin = W4A16Linear(W)
         fn = lambda: lin(X, path=path)  # noqa: E731
+    elif args.case == "w4a8":
+        lin = W4A8Linear(W)
+        Xq, sx = lin.quant_act(X)
+        fn = lambda: lin.gemm(Xq, sx)  # noqa: E731
+    elif args.case == "mxfp8":
+        lin = MXFP8Linear(W)
+        Xq, xs = lin.quant_act(X)
+        fn = lambda: lin.gemm(Xq, xs)  # noqa: E731
     elif args.case == "w8a8b":
         lin = W8A8BlockLinear(W)
         Xq, sx = lin.quant_act(X)
@@ -894,7 +902,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweeps", action="store_true", help="decode line only (no prefill / crossover objects)")
-    ap.add_argument("--case", default=None, choices=["w4a16", "w8a8", "w8a8b"])
+    ap.add_argument("--case", default=None, choices=["w4a16", "w8a8", "w8a8b", "w4a8", "mxfp8"])
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--N", type=int, default=28672)
     ap.add_argument("--K", type=int, default=4096)

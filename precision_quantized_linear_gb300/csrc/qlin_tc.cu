@@ -159,16 +159,18 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
-// Eight columns of one 32-bit code word -> four BF16 pairs bf16(s) (q - z);
-// component i is the pair in nibble positions i and i + 4.  Word t of a
-// 32-column record holds pairs (columns 8i + 2t, +1) for i = 0..3.
+// Eight columns of one 32-bit code word -> four BF16 pairs bf16(bf16(s) (q - z)):
+// the caller rounds the FP16 group scale to BF16 once (s2), (q - z) is exact,
+// and the product is rounded to BF16; component i is the pair in nibble
+// positions i and i + 4.  Word t of a 32-column record holds pairs (columns
+// 8i + 2t, +1) for i = 0..3.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 zoff, __nv_bfloat162 s2) {
   uint32_t o[4];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const uint32_t v = ((w >> (4 * t)) & 0x000F000Fu) | 0x43004300u;  // BF16x2 (128 + q)
     __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v);
-    b = __hmul2(__hsub2(b, zoff), s2);  // (q - z) is exact; the product is rounded once
+    b = __hmul2(__hsub2(b, zoff), s2);  // (q - z) is exact; the product with bf16(s) is rounded once
     o[t] = bf16x2_bits(b);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
