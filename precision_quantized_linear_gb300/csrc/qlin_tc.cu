@@ -408,7 +408,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
             break;
           }
           tc_fence_after();
-          const uint32_t slot = static_cast<uint32_t>(it % C::kSfSlots);
+          const uint32_t slot = static_cast<uint32_t>(C::kSfSlots ? it % C::kSfSlots : 0);
           const uint32_t t_sfa = tmem_base + C::kSfaCol + slot * 4;
           const uint32_t t_sfb = tmem_base + C::kSfbCol + slot * 4 * C::kSfbAtoms;
           const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
