@@ -10,8 +10,10 @@ follows (see ``qlin_oracle.c`` for the list):
   [LP] "Low-precision LLM inference: FP8/INT8/INT4/FP4 kernels and
        calibration" -- S2 uniform quantisation, S3 symmetric/asymmetric,
        S4 granularity, S5 effective bits, S7 E4M3, S8 FP8 current scaling,
-       S10 MX block formats (MXFP8 after the OCP Microscaling spec v1.0,
-       ``quant_mxfp8_rows`` below), S22 accumulator precision, S23/S24 fused
+       S10 FP4 E2M1 and the block formats (MXFP8 and MXFP4 after the OCP
+       Microscaling spec v1.0, NVFP4 after its vendor's two-level recipe:
+       ``quant_mxfp8_rows``, ``quant_mxfp4_rows``, ``quant_nvfp4_rows``
+       below), S22 accumulator precision, S23/S24 fused
        bias / activation epilogue (``epilogue`` below).
   [TP] "Quantization throughput by batch size: why W4A16 is overtaken by
        W8A8" -- the arithmetic-intensity roofline (``roofline_*`` below).
@@ -99,6 +101,21 @@ def _load():
         lib.orc_w8a8_at.restype = None
         lib.orc_w8a8_at.argtypes = [_p, _p, _p, ctypes.c_float, _i64, _i64, _i64,
                                     _p, _p, _i64, _p]
+        lib.orc_e2m1_to_f64.restype = ctypes.c_double
+        lib.orc_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.orc_f32_to_e2m1_rn_sat.restype = ctypes.c_uint8
+        lib.orc_f32_to_e2m1_rn_sat.argtypes = [ctypes.c_float]
+        lib.orc_quant_mxfp4_rows.restype = None
+        lib.orc_quant_mxfp4_rows.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.orc_w4a4_mx_at.restype = None
+        lib.orc_w4a4_mx_at.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _i64, _p]
+        lib.orc_nvfp4_global_scale.restype = ctypes.c_float
+        lib.orc_nvfp4_global_scale.argtypes = [_p, _i64]
+        lib.orc_quant_nvfp4_rows.restype = None
+        lib.orc_quant_nvfp4_rows.argtypes = [_p, _i64, _i64, ctypes.c_float, _p, _p]
+        lib.orc_w4a4_nv_at.restype = None
+        lib.orc_w4a4_nv_at.argtypes = [_p, _p, ctypes.c_float, _p, _p, ctypes.c_float, _i64, _i64, _i64,
+                                       _p, _p, _i64, _p]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_set_num_threads.restype = None
         lib.orc_set_num_threads.argtypes = [ctypes.c_int]
@@ -478,4 +495,121 @@ def w8a8_mx_at(Xq, xs, Wq, ws, ms, ns) -> np.ndarray:
     ns = np.ascontiguousarray(ns, dtype=np.int64)
     out = np.empty(ms.shape, np.float64)
     _load().orc_w8a8_mx_at(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws), M, N, K, _ptr(ms), _ptr(ns), ms.size, _ptr(out))
+    return out
+
+
+# ---- FP4 ([LP] S10): E2M1 elements, MXFP4 and NVFP4 block formats
+
+def e2m1_to_f64(c: int) -> float:
+    return _load().orc_e2m1_to_f64(c)
+
+
+def f32_to_e2m1(x: float) -> int:
+    """binary32 -> E2M1 code: nearest magnitude, ties to the even code, saturating at 6, sign kept."""
+    return _load().orc_f32_to_e2m1_rn_sat(x)
+
+
+def e2m1_table() -> np.ndarray:
+    """The 16 E2M1 codes' values (bit 3 the sign)."""
+    return np.array([e2m1_to_f64(c) for c in range(16)], np.float64)
+
+
+def pack_fp4(codes: np.ndarray) -> np.ndarray:
+    """Two E2M1 codes per byte along a row: column 2i in the low nibble, 2i + 1 in the high one."""
+    c = np.asarray(codes, np.uint8)
+    assert c.shape[-1] % 2 == 0
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_fp4(packed: np.ndarray) -> np.ndarray:
+    p = np.asarray(packed, np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.uint8)
+    out[..., 0::2] = p & 15
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def quant_mxfp4_rows(X_bf16: np.ndarray):
+    """MXFP4 (OCP MX v1.0, named in [LP] S10): per row, blocks of 32 elements share a
+    power-of-two scale 2^e (E8M0 byte e + 127, e = floor(log2 amax) - 2, clamped to
+    [-127, 127]); codes E2M1(v / 2^e), nearest, ties to even, saturating.  Returns codes
+    [R][K] (one per byte) and scales [R][K/32] uint8."""
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    R, K = X.shape
+    assert K % 32 == 0
+    codes = np.empty((R, K), np.uint8)
+    scales = np.empty((R, K // 32), np.uint8)
+    _load().orc_quant_mxfp4_rows(_ptr(X), R, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mxfp4_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """e2m1(code) * 2^(scale - 127) per 32-block, in double."""
+    return e2m1_table()[codes] * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)
+
+
+def w4a4_mx_full(Xq, xs, Wq, ws) -> np.ndarray:
+    """Y = mxfp4_dequant(Xq, xs) . mxfp4_dequant(Wq, ws)^T in double."""
+    return gemm_nt_f64(np.ascontiguousarray(mxfp4_dequant(Xq, xs)), np.ascontiguousarray(mxfp4_dequant(Wq, ws)))
+
+
+def w4a4_mx_at(Xq, xs, Wq, ws, ms, ns) -> np.ndarray:
+    """Y[m_i, n_i] = sum over 32-blocks of both block scales times the block's E2M1 dot product, in double."""
+    Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    xs = np.ascontiguousarray(xs, dtype=np.uint8)
+    ws = np.ascontiguousarray(ws, dtype=np.uint8)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape, np.float64)
+    _load().orc_w4a4_mx_at(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws), M, N, K, _ptr(ms), _ptr(ns), ms.size, _ptr(out))
+    return out
+
+
+def nvfp4_global_scale(X_bf16: np.ndarray) -> float:
+    """NVFP4 per-tensor scale: amax(|X|) / (6 * 448) as a binary32 division; 1.0 when that is 0."""
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    return float(np.float32(_load().orc_nvfp4_global_scale(_ptr(X), X.size)))
+
+
+def quant_nvfp4_rows(X_bf16: np.ndarray, sg: float):
+    """NVFP4 ([LP] S10 names it; the vendor's two-level recipe): blocks of 16 along a
+    row, block scale sb = E4M3(amax_b / (6 sg)), codes E2M1(v / (sb sg)), each step one
+    binary32 operation; a block whose scale is 0 stores code 0.  Returns codes [R][K]
+    (one per byte) and scales [R][K/16] (E4M3 codes)."""
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    R, K = X.shape
+    assert K % 16 == 0
+    codes = np.empty((R, K), np.uint8)
+    scales = np.empty((R, K // 16), np.uint8)
+    _load().orc_quant_nvfp4_rows(_ptr(X), R, K, float(sg), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def nvfp4_dequant(codes: np.ndarray, scales: np.ndarray, sg: float) -> np.ndarray:
+    """e2m1(code) * e4m3(sb) * sg per 16-block, in double."""
+    return e2m1_table()[codes] * np.repeat(e4m3_table()[scales], 16, axis=1) * float(np.float32(sg))
+
+
+def w4a4_nv_full(Xq, xs, sgx, Wq, ws, sgw) -> np.ndarray:
+    """Y = nvfp4_dequant(Xq, xs, sgx) . nvfp4_dequant(Wq, ws, sgw)^T in double."""
+    return gemm_nt_f64(np.ascontiguousarray(nvfp4_dequant(Xq, xs, sgx)),
+                       np.ascontiguousarray(nvfp4_dequant(Wq, ws, sgw)))
+
+
+def w4a4_nv_at(Xq, xs, sgx, Wq, ws, sgw, ms, ns) -> np.ndarray:
+    """Y[m_i, n_i] = sgx sgw * sum over 16-blocks of both E4M3 block scales times the block's E2M1 dot product."""
+    Xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    xs = np.ascontiguousarray(xs, dtype=np.uint8)
+    ws = np.ascontiguousarray(ws, dtype=np.uint8)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(ms.shape, np.float64)
+    _load().orc_w4a4_nv_at(_ptr(Xq), _ptr(xs), float(sgx), _ptr(Wq), _ptr(ws), float(sgw), M, N, K,
+                           _ptr(ms), _ptr(ns), ms.size, _ptr(out))
     return out

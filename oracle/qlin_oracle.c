@@ -519,16 +519,19 @@ int orc_num_threads(void)
 /* E4M3(v / X), round to nearest even, saturating at +-448.             */
 /* ------------------------------------------------------------------ */
 
-static int mx_exponent(float amax)
+/* emax: exponent of the element type's largest normal (E4M3 8, E2M1 2) */
+static int mx_exponent_of(float amax, int emax)
 {
     if (amax == 0.0f) return -127;
     int ex;
     frexpf(amax, &ex);          /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
-    int e = (ex - 1) - 8;
+    int e = (ex - 1) - emax;
     if (e < -127) e = -127;
     if (e > 127) e = 127;
     return e;
 }
+
+static int mx_exponent(float amax) { return mx_exponent_of(amax, 8); }
 
 /* X [R][K] bf16 -> codes [R][K] e4m3 and scales [R][K/32] e8m0 */
 void orc_quant_mxfp8_rows(const uint16_t *X, int64_t R, int64_t K, uint8_t *codes, uint8_t *scales)
@@ -567,5 +570,153 @@ void orc_w8a8_mx_at(const uint8_t *Xq, const uint8_t *xs, const uint8_t *Wq, con
             acc += part * ldexp(1.0, (int)xs[m * (K / 32) + b] - 127) * ldexp(1.0, (int)ws[n * (K / 32) + b] - 127);
         }
         out[i] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* FP4 E2M1 ([LP] S10: 1 sign, 2 exponent and 1 mantissa bit).  With    */
+/* the exponent bias 1 the eight magnitudes are 0, 0.5 (the subnormal), */
+/* 1, 1.5, 2, 3, 4 and 6; the format has no infinity and no NaN.        */
+/* ------------------------------------------------------------------ */
+
+double orc_e2m1_to_f64(uint8_t c)
+{
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 3;
+    int m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* binary32 -> E2M1: the nearest of the eight magnitudes, a tie going to the
+ * even code (mantissa bit 0); above 6 (infinity included) the result
+ * saturates to 6.  The sign bit is kept, also when the result is 0. */
+uint8_t orc_f32_to_e2m1_rn_sat(float x)
+{
+    uint8_t sign = signbit(x) ? 8 : 0;
+    double a = fabs((double)x);
+    if (a >= 6.0)                /* 6 and beyond (infinity too): the largest magnitude */
+        return sign | 7;
+    int best = 0;
+    for (int c = 1; c < 8; c++) {
+        double d = fabs(a - orc_e2m1_to_f64((uint8_t)c));
+        double db = fabs(a - orc_e2m1_to_f64((uint8_t)best));
+        if (d < db || (d == db && (c & 1) == 0))
+            best = c;
+    }
+    return sign | (uint8_t)best;
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 (the OCP MX specification's FP4 block format, named in [LP]    */
+/* S10): the MXFP8 recipe above with E2M1 elements -- blocks of 32 along */
+/* a row share 2^e (E8M0 byte e + 127), e = floor(log2 amax) - 2, 2      */
+/* being the exponent of E2M1's largest normal (6 = 1.5 * 2^2), clamped  */
+/* to [-127, 127], -127 for an all-zero block; each element becomes      */
+/* E2M1(v / 2^e).  Codes are returned one per byte (0..15).             */
+/* ------------------------------------------------------------------ */
+
+void orc_quant_mxfp4_rows(const uint16_t *X, int64_t R, int64_t K, uint8_t *codes, uint8_t *scales)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; r++) {
+        for (int64_t b = 0; b < K / 32; b++) {
+            float amax = 0.0f;
+            for (int64_t k = b * 32; k < b * 32 + 32; k++) {
+                float a = fabsf(bf16_to_f32(X[r * K + k]));
+                if (a > amax) amax = a;
+            }
+            int e = mx_exponent_of(amax, 2);
+            scales[r * (K / 32) + b] = (uint8_t)(e + 127);
+            double xs = ldexp(1.0, e);
+            for (int64_t k = b * 32; k < b * 32 + 32; k++)
+                codes[r * K + k] = orc_f32_to_e2m1_rn_sat((float)((double)bf16_to_f32(X[r * K + k]) / xs));
+        }
+    }
+}
+
+/* Y[m][n] = sum over 32-blocks b of 2^(xs[m][b]-127) 2^(ws[n][b]-127)
+ *           * sum_{k in b} e2m1(Xq[m][k]) e2m1(Wq[n][k]), in double, for sampled (m, n);
+ * codes one per byte */
+void orc_w4a4_mx_at(const uint8_t *Xq, const uint8_t *xs, const uint8_t *Wq, const uint8_t *ws,
+                    int64_t M, int64_t N, int64_t K, const int64_t *ms, const int64_t *ns, int64_t cnt, double *out)
+{
+    (void)M; (void)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < cnt; i++) {
+        int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t b = 0; b < K / 32; b++) {
+            double part = 0.0;
+            for (int64_t k = b * 32; k < b * 32 + 32; k++)
+                part += orc_e2m1_to_f64(Xq[m * K + k]) * orc_e2m1_to_f64(Wq[n * K + k]);
+            acc += part * ldexp(1.0, (int)xs[m * (K / 32) + b] - 127) * ldexp(1.0, (int)ws[n * (K / 32) + b] - 127);
+        }
+        out[i] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* NVFP4 ([LP] S10 names it as a vendor recipe on the same E2M1         */
+/* elements with its own block size and scale hierarchy; the reading    */
+/* here is that vendor's published two-level recipe): a per-tensor FP32 */
+/* scale sg = amax(|X|) / (6 * 448) (1 when that is 0), blocks of 16    */
+/* along a row with an E4M3 block scale sb = E4M3(amax_b / (6 sg))      */
+/* (round to nearest even, saturating), elements E2M1(v / (sb sg)); a   */
+/* block whose scale rounds to 0 stores code 0 for every element.       */
+/* Every step is one binary32 operation, so both sides of a comparison  */
+/* take the same rounding decisions.                                    */
+/* ------------------------------------------------------------------ */
+
+float orc_nvfp4_global_scale(const uint16_t *X, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; i++) {
+        float a = fabsf(bf16_to_f32(X[i]));
+        if (a > amax) amax = a;
+    }
+    float sg = amax / 2688.0f;   /* 6 (E2M1's largest) * 448 (E4M3's largest) */
+    return sg == 0.0f ? 1.0f : sg;
+}
+
+/* X [R][K] bf16 -> codes [R][K] (one E2M1 code per byte), scales [R][K/16] E4M3 */
+void orc_quant_nvfp4_rows(const uint16_t *X, int64_t R, int64_t K, float sg, uint8_t *codes, uint8_t *scales)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; r++) {
+        for (int64_t b = 0; b < K / 16; b++) {
+            float amax = 0.0f;
+            for (int64_t k = b * 16; k < b * 16 + 16; k++) {
+                float a = fabsf(bf16_to_f32(X[r * K + k]));
+                if (a > amax) amax = a;
+            }
+            float d6 = 6.0f * sg;
+            float q = amax / d6;
+            uint8_t sc = orc_f32_to_e4m3_rn_sat(q);
+            scales[r * (K / 16) + b] = sc;
+            float den = (float)orc_e4m3_to_f64(sc) * sg;
+            for (int64_t k = b * 16; k < b * 16 + 16; k++)
+                codes[r * K + k] = sc == 0 ? 0 : orc_f32_to_e2m1_rn_sat(bf16_to_f32(X[r * K + k]) / den);
+        }
+    }
+}
+
+/* Y[m][n] = sgx sgw * sum over 16-blocks b of e4m3(xs[m][b]) e4m3(ws[n][b])
+ *           * sum_{k in b} e2m1(Xq[m][k]) e2m1(Wq[n][k]), in double, for sampled (m, n) */
+void orc_w4a4_nv_at(const uint8_t *Xq, const uint8_t *xs, float sgx, const uint8_t *Wq, const uint8_t *ws, float sgw,
+                    int64_t M, int64_t N, int64_t K, const int64_t *ms, const int64_t *ns, int64_t cnt, double *out)
+{
+    (void)M; (void)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < cnt; i++) {
+        int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t b = 0; b < K / 16; b++) {
+            double part = 0.0;
+            for (int64_t k = b * 16; k < b * 16 + 16; k++)
+                part += orc_e2m1_to_f64(Xq[m * K + k]) * orc_e2m1_to_f64(Wq[n * K + k]);
+            acc += part * orc_e4m3_to_f64(xs[m * (K / 16) + b]) * orc_e4m3_to_f64(ws[n * (K / 16) + b]);
+        }
+        out[i] = acc * (double)sgx * (double)sgw;
     }
 }

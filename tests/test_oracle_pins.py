@@ -725,3 +725,154 @@ def test_per_channel_scale_closed_form():
     assert (np.abs(deq - w) <= sc / 2 * (1 + 2.0 ** -20)).all()   # round-trip bound inside the range
     c, s, z = oracle.pack_tile(wq)
     assert np.array_equal(s.reshape(2, 128), wq.s[:, 0].reshape(2, 128))       # one scale per row, tile order
+
+
+# ---- FP4 ([LP] S10): E2M1 = 1 sign, 2 exponent and 1 mantissa bit; MXFP4 and NVFP4 blocks
+
+def test_e2m1_values_are_the_ocp_table():
+    # the OCP MX specification's E2M1 table: largest normal 6, smallest normal 1, one subnormal 0.5
+    want = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    tab = oracle.e2m1_table()
+    assert list(tab[:8]) == want
+    assert list(-tab[8:]) == want and np.signbit(tab[8:]).all()
+    # every E2M1 value is exact in E4M3 (2 exponent bits and 1 mantissa bit fit in 4 and 3)
+    e4 = oracle.e4m3_table()
+    for v in want:
+        assert e4[oracle.f32_to_e4m3(v)] == v
+
+
+def test_e2m1_rounding_nearest_ties_even_saturating():
+    tab = oracle.e2m1_table()
+    ties = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0}   # midpoints: even code
+    for x, v in ties.items():
+        assert tab[oracle.f32_to_e2m1(x)] == v and tab[oracle.f32_to_e2m1(-x)] == -v
+    for x in (6.0, 6.5, 7.99, 1e30, float("inf")):
+        assert oracle.f32_to_e2m1(x) == 7 and oracle.f32_to_e2m1(-x) == 15
+    assert oracle.f32_to_e2m1(-0.1) == 8 and oracle.f32_to_e2m1(0.0) == 0     # the sign survives a zero result
+    rng = np.random.default_rng(31)
+    grid = tab[:8]
+    for x in rng.uniform(-7.0, 7.0, 5000).astype(np.float32):            # brute force: a nearest value
+        q = tab[oracle.f32_to_e2m1(float(x))]
+        assert abs(float(x) - q) <= np.abs(abs(float(x)) - grid).min()
+        assert q == 0 or np.sign(q) == np.sign(x)
+
+
+def test_fp4_packing_puts_the_even_column_in_the_low_nibble():
+    codes = np.array([[1, 2, 15, 8, 0, 7]], np.uint8)
+    packed = oracle.pack_fp4(codes)
+    assert list(packed[0]) == [0x21, 0x8F, 0x70]
+    assert np.array_equal(oracle.unpack_fp4(packed), codes)
+
+
+def test_mxfp4_shared_exponent_at_closed_form_points():
+    rows = np.zeros((5, 32), np.float32)
+    rows[0, 0] = 1.0                      # floor(log2 1) = 0 -> e = -2 (byte 125); 1 / 2^-2 = 4: code 6
+    rows[1, :2] = [7.0, 5.0]              # e = 0 (byte 127); 7 saturates to 6 (code 7); 5 is a tie: 4 (code 6)
+    rows[3, 0] = 2.0 ** -126              # e would be -128: clamped to -127 (byte 0); 2^-126 / 2^-127 = 2: code 4
+    rows[4, :2] = [-3.0, 0.75]            # e = -1 (byte 126); -3 / 0.5 = -6 (code 15); 0.75 / 0.5 = 1.5 (code 3)
+    codes, scales = oracle.quant_mxfp4_rows(_bf16_bits(rows))
+    assert list(scales[:, 0]) == [125, 127, 0, 0, 126]
+    assert codes[0, 0] == 6 and list(codes[1, :2]) == [7, 6] and not codes[2].any()
+    assert codes[3, 0] == 4 and list(codes[4, :2]) == [15, 3]
+    deq = oracle.mxfp4_dequant(codes, scales)
+    assert deq[0, 0] == 1.0 and deq[1, 0] == 6.0 and deq[1, 1] == 4.0 and deq[3, 0] == 2.0 ** -126
+    assert deq[4, 0] == -3.0 and deq[4, 1] == 0.75
+
+
+def test_mxfp4_round_trip_error_bound():
+    rng = np.random.default_rng(32)
+    X = (rng.standard_normal((16, 256)) * np.exp2(rng.integers(-20, 20, (16, 1)))).astype(np.float32)
+    Xb = _bf16_bits(X)
+    v = syn.bf16_bits_to_f32(Xb).astype(np.float64)
+    codes, scales = oracle.quant_mxfp4_rows(Xb)
+    deq = oracle.mxfp4_dequant(codes, scales)
+    step = np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)   # X = 2^e of each element
+    sat = np.abs(v) > 6.0 * step
+    # one mantissa bit: half a spacing is at most a quarter of the value; below 1 X the spacing is X / 2
+    ok = np.abs(v - deq) <= 0.25 * np.abs(v) + 0.25 * step
+    assert ok[~sat].all()
+    assert (np.abs(deq[sat]) == 6.0 * step[sat]).all() and (np.abs(v[sat]) < 8.0 * step[sat]).all()
+    amax = np.abs(v).reshape(16, 8, 32).max(axis=2)                      # every block's amax lands in [4, 8) X
+    sc = np.ldexp(1.0, scales.astype(np.int64) - 127)
+    assert ((amax >= 4.0 * sc) & (amax < 8.0 * sc)).all()
+
+
+def test_mxfp4_product_applies_each_block_scale_to_its_own_block():
+    rng = np.random.default_rng(33)
+    X = (rng.standard_normal((6, 128)) * np.exp2(rng.integers(-6, 6, (6, 4)).repeat(32, axis=1))).astype(np.float32)
+    W = (rng.standard_normal((8, 128)) * np.exp2(rng.integers(-6, 6, (8, 4)).repeat(32, axis=1))).astype(np.float32)
+    Xq, xs = oracle.quant_mxfp4_rows(_bf16_bits(X))
+    Wq, ws = oracle.quant_mxfp4_rows(_bf16_bits(W))
+    ms, ns = np.repeat(np.arange(6), 8), np.tile(np.arange(8), 6)
+    got = oracle.w4a4_mx_at(Xq, xs, Wq, ws, ms, ns)
+    want = (oracle.mxfp4_dequant(Xq, xs) @ oracle.mxfp4_dequant(Wq, ws).T)[ms, ns]
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(oracle.w4a4_mx_full(Xq, xs, Wq, ws)[ms, ns], got, rtol=1e-12, atol=0)
+
+
+def test_nvfp4_global_scale():
+    X = np.zeros((2, 16), np.float32)
+    assert oracle.nvfp4_global_scale(_bf16_bits(X)) == 1.0                 # all zero: 1
+    X[1, 3] = -2688.0
+    assert oracle.nvfp4_global_scale(_bf16_bits(X)) == 1.0                 # 2688 = 6 * 448
+    X[1, 3] = 1.0
+    assert oracle.nvfp4_global_scale(_bf16_bits(X)) == float(np.float32(1.0) / np.float32(2688.0))
+
+
+def test_nvfp4_two_level_scales_at_closed_form_points():
+    X = np.zeros((2, 32), np.float32)
+    X[0, 0] = 2688.0                      # sg = 1; block 0: sb = 2688 / 6 = 448 (0x7E), 2688 / 448 = 6 (code 7)
+    X[0, 16:20] = [6.0, 3.0, -1.5, 0.25]  # block 1: sb = 1 (0x38); codes 7, 5, 11 (-1.5), 0 (0.25: tie -> 0)
+    X[1, 0:2] = [1.25, 0.5]               # sb = E4M3(1.25 / 6 = 0.2083) = 0.203125 (0x25): 1.25 / sb = 6.15 -> 6
+                                          # (code 7, saturated); 0.5 / sb = 2.46 -> 2 (code 4); block 1 all zero
+    Xb = _bf16_bits(X)
+    sg = oracle.nvfp4_global_scale(Xb)
+    assert sg == 1.0
+    codes, scales = oracle.quant_nvfp4_rows(Xb, sg)
+    assert scales.tolist() == [[0x7E, 0x38], [0x25, 0x00]]
+    assert codes[0, 0] == 7 and list(codes[0, 16:20]) == [7, 5, 11, 0]
+    assert list(codes[1, :2]) == [7, 4] and not codes[1, 16:].any()
+    deq = oracle.nvfp4_dequant(codes, scales, sg)
+    assert deq[0, 0] == 2688.0 and deq[1, 0] == 6 * 0.203125 and deq[1, 1] == 2 * 0.203125
+    # a tensor amax of 1: sg = 1/2688 in binary32, the block scale lands on 448 and the element on 6
+    Y = np.zeros((1, 16), np.float32)
+    Y[0, 0] = 1.0
+    sgy = oracle.nvfp4_global_scale(_bf16_bits(Y))
+    c, s = oracle.quant_nvfp4_rows(_bf16_bits(Y), sgy)
+    assert s[0, 0] == 0x7E and c[0, 0] == 7
+
+
+def test_nvfp4_round_trip_error_bound():
+    rng = np.random.default_rng(34)
+    X = (rng.standard_normal((16, 256)) * np.exp2(rng.integers(-8, 8, (16, 16)).repeat(16, axis=1))).astype(np.float32)
+    Xb = _bf16_bits(X)
+    v = syn.bf16_bits_to_f32(Xb).astype(np.float64)
+    sg = oracle.nvfp4_global_scale(Xb)
+    assert sg == float(np.float32(np.float32(np.abs(v).max()) / np.float32(2688.0)))
+    codes, scales = oracle.quant_nvfp4_rows(Xb, sg)
+    deq = oracle.nvfp4_dequant(codes, scales, sg)
+    e4 = oracle.e4m3_table()
+    sb = e4[scales]
+    amax = np.abs(v).reshape(16, 16, 16).max(axis=2)
+    t = amax / (6.0 * sg)
+    normal = t >= 2.0 ** -6                  # E4M3 normal range: the block scale is within 2^-4 of amax / (6 sg)
+    assert (np.abs(sb - t)[normal] <= 2.0 ** -4 * t[normal] * (1 + 1e-6)).all()
+    step = np.repeat(sb * sg, 16, axis=1)     # the element's unit
+    sat = np.abs(v) > 6.0 * step
+    ok = np.abs(v - deq) <= 0.25 * np.abs(v) + 0.25 * step + 1e-6 * np.abs(v)   # 1e-6: binary32 v / (sb sg)
+    assert ok[~sat].all()
+    assert (np.abs(deq[sat]) == 6.0 * step[sat]).all()
+
+
+def test_nvfp4_product_equals_the_per_block_loops():
+    rng = np.random.default_rng(35)
+    X = (rng.standard_normal((5, 128)) * np.exp2(rng.integers(-5, 5, (5, 8)).repeat(16, axis=1))).astype(np.float32)
+    W = (rng.standard_normal((7, 128)) * np.exp2(rng.integers(-5, 5, (7, 8)).repeat(16, axis=1))).astype(np.float32)
+    sgx, sgw = oracle.nvfp4_global_scale(_bf16_bits(X)), oracle.nvfp4_global_scale(_bf16_bits(W))
+    Xq, xs = oracle.quant_nvfp4_rows(_bf16_bits(X), sgx)
+    Wq, ws = oracle.quant_nvfp4_rows(_bf16_bits(W), sgw)
+    ms, ns = np.repeat(np.arange(5), 7), np.tile(np.arange(7), 5)
+    got = oracle.w4a4_nv_at(Xq, xs, sgx, Wq, ws, sgw, ms, ns)
+    want = (oracle.nvfp4_dequant(Xq, xs, sgx) @ oracle.nvfp4_dequant(Wq, ws, sgw).T)[ms, ns]
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(oracle.w4a4_nv_full(Xq, xs, sgx, Wq, ws, sgw)[ms, ns], got, rtol=1e-12, atol=0)
