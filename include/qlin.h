@@ -81,6 +81,8 @@ typedef enum {
 #define QLIN_OP_W8A8_BLOCK_GEMM 4
 #define QLIN_OP_MXFP8_GEMM 5
 #define QLIN_OP_W4A8_GEMM 6
+#define QLIN_OP_MXFP4_GEMM 7
+#define QLIN_OP_NVFP4_GEMM 8
 
 /* Activation of the fused output epilogue (qlin_*_gemm_fused). */
 #define QLIN_ACT_NONE 0
@@ -313,6 +315,74 @@ qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const vo
                               void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                               void* stream);
 
+/* ---- FP4 ([LP] S10: the E2M1 element -- 1 sign, 2 exponent and 1 mantissa
+ * bit, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 -- in the two block formats that
+ * page tells apart).  Codes are packed two per byte along K, column 2i in the
+ * low nibble, so an [R][K] tensor takes R * K / 2 bytes.  Conversion to E2M1
+ * rounds to nearest even and saturates at +-6.  K % 256 == 0 in every FP4
+ * call; R (and M) need not be a multiple of anything.
+ *
+ * MXFP4 (the OCP MX specification's FP4 format): blocks of 32 along K share
+ * an E8M0 scale 2^e, e = floor(log2 amax) - 2 (2 being the exponent of E2M1's
+ * largest normal, 6 = 1.5 x 2^2), clamped to [-127, 127], -127 for an all-zero
+ * block; elements E2M1(v / 2^e).  Scales in the MXFP8 atom layout above
+ * (qlin_mx_scale_bytes(R, K) bytes).
+ *
+ * NVFP4 (the vendor's two-level recipe on the same element): one FP32 scale
+ * per tensor, sg = amax(|X|) / (6 x 448) (1 when that is 0); blocks of 16
+ * along K with an E4M3 scale sb = E4M3(amax_b / (6 sg)) (nearest even,
+ * saturating); elements E2M1(v / (sb sg)), each step one binary32 operation;
+ * a block whose scale is 0 stores code 0 in every element.  Scales in atoms
+ * of four 16-column blocks: for R rows, ceil(R/128) x (K/64) atoms of 512
+ * bytes, atom (R0, c) at byte ((R0 * (K/64)) + c) * 512 covering rows
+ * 128 R0 .. +127 and columns 64 c .. +63, row r's scales kk = 0..3 at bytes
+ * 16 (r % 32) + 4 ((r % 128) / 32) + kk; atom rows past R are 0. */
+
+/* Bytes of the NVFP4 scale atoms of an R x K tensor: ceil(R/128) * 128 * K / 16.
+ * K % 256 == 0, R >= 0. */
+qlin_status_t qlin_nvfp4_scale_bytes(int64_t R, int64_t K, size_t* bytes);
+
+/* Quantise X [R][K] BF16 to MXFP4: codes [R][K/2] packed E2M1 (16-byte
+ * aligned) and scales in the MXFP8 atom layout (qlin_mx_scale_bytes(R, K)
+ * bytes, 16-byte aligned).  Weights once at load (R = N), activations per call
+ * (R = M).  Asynchronous, no workspace. */
+qlin_status_t qlin_quant_mxfp4(const void* X_bf16, int64_t R, int64_t K, void* codes_e2m1, void* scales_e8m0,
+                               void* stream);
+
+/* NVFP4 per-tensor scale of the n BF16 values at X (16-byte aligned,
+ * n % 8 == 0, n >= 1) into the device float *sg (4-byte aligned): a memset, an
+ * amax reduction and a one-thread kernel on `stream`; nothing is copied to the
+ * host. */
+qlin_status_t qlin_nvfp4_tensor_scale(const void* X_bf16, int64_t n, float* sg, void* stream);
+
+/* Quantise X [R][K] BF16 to NVFP4 with the per-tensor scale at device address
+ * sg (read by the kernel, so it may come from qlin_nvfp4_tensor_scale on the
+ * same stream): codes [R][K/2] packed E2M1, scales in the NVFP4 atom layout
+ * (qlin_nvfp4_scale_bytes(R, K) bytes); all 16-byte aligned.  Asynchronous. */
+qlin_status_t qlin_quant_nvfp4(const void* X_bf16, int64_t R, int64_t K, const float* sg, void* codes_e2m1,
+                               void* scales_e4m3, void* stream);
+
+/* MXFP4 linear layer: Y[m][n] = bf16( sum_b 2^(xs[m][b]-127) 2^(ws[n][b]-127)
+ * sum_{k in block b} e2m1(Xq[m][k]) e2m1(Wq[n][k]) ), b over the 32-column
+ * blocks, accumulated in FP32 on the tensor cores (tcgen05 kind::mxf4 with
+ * hardware block scaling).  Xq / xs from qlin_quant_mxfp4 of the activations,
+ * Wq / ws of the weights.  N % 128 == 0, K % 256 == 0; workspace:
+ * qlin_workspace_size(QLIN_OP_MXFP4_GEMM, ...) bytes (0 when the K range is
+ * not split), zero-filled, left zero-filled.  Deterministic. */
+qlin_status_t qlin_mxfp4_gemm(const void* Xq_e2m1, const void* xs_e8m0, const void* Wq_e2m1, const void* ws_e8m0,
+                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/* NVFP4 linear layer: Y[m][n] = bf16( sgx sgw sum_b e4m3(xs[m][b]) e4m3(ws[n][b])
+ * sum_{k in block b} e2m1(Xq[m][k]) e2m1(Wq[n][k]) ), b over the 16-column
+ * blocks; the block scales are applied by the tensor cores (tcgen05
+ * kind::mxf4nvf4), the FP32 product sgx * sgw in the epilogue.  sgx / sgw are
+ * device pointers to the two per-tensor scales, read by the kernel.  Shapes,
+ * workspace (QLIN_OP_NVFP4_GEMM) and determinism as qlin_mxfp4_gemm. */
+qlin_status_t qlin_nvfp4_gemm(const void* Xq_e2m1, const void* xs_e4m3, const float* sgx, const void* Wq_e2m1,
+                              const void* ws_e4m3, const float* sgw, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QLIN_OK, or the first error a kernel recorded since the last call. */
 qlin_status_t qlin_get_device_error(void* stream);
@@ -363,13 +433,16 @@ int qlin_gemv_max_m(int op);
 #define QLIN_KERNEL_W8A8_BLOCK_TC 7 /* block-scaled W8A8 on tcgen05 with FP32 promotion */
 #define QLIN_KERNEL_MXFP8_TC 8    /* MXFP8 on tcgen05 kind::mxf8f6f4 with hardware block scaling */
 #define QLIN_KERNEL_W4A8_TC 9     /* W4A8: INT4 -> E4M3 dequantisation, tcgen05 kind::f8f6f4, group promotion */
+#define QLIN_KERNEL_MXFP4_TC 10   /* MXFP4 on tcgen05 kind::mxf4 with hardware block scaling */
+#define QLIN_KERNEL_NVFP4_TC 11   /* NVFP4 on tcgen05 kind::mxf4nvf4 with hardware block scaling */
 
 /*
  * Dispatch query (for tests and measurement tools; launches nothing, reads
  * no device memory): the kernel and tiling a call of `op`
  * (QLIN_OP_W4A16_GEMM, QLIN_OP_W8A8_GEMM, QLIN_OP_W8A8_BLOCK_GEMM,
- * QLIN_OP_MXFP8_GEMM or QLIN_OP_W4A8_GEMM) with these sizes and `path`
- * (QLIN_PATH_*; ignored by the block-scaled, MXFP8 and W4A8 GEMMs)
+ * QLIN_OP_MXFP8_GEMM, QLIN_OP_W4A8_GEMM, QLIN_OP_MXFP4_GEMM or
+ * QLIN_OP_NVFP4_GEMM) with these sizes and `path` (QLIN_PATH_*; ignored by
+ * the block-scaled, MX, FP4 and W4A8 GEMMs)
  * would launch.  num_sms is the SM count to plan for, 0 for the current
  * device's (the small-M kernels always read the current device's cluster
  * occupancy).  Writes 8 values:

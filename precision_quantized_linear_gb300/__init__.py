@@ -31,13 +31,16 @@ __all__ = [
     "KERNEL_W4A16_MMA", "KERNEL_W4A16_GEMV", "KERNEL_W4A16_TC", "KERNEL_W8A8_MMA", "KERNEL_W8A8_GEMV",
     "KERNEL_W8A8_TC", "KERNEL_W8A8_BLOCK_TC", "KERNEL_MXFP8_TC", "OP_MXFP8_GEMM",
     "qlin_mx_scale_bytes", "qlin_quant_mxfp8", "qlin_mxfp8_gemm", "qlin_w4a8_gemm", "OP_W4A8_GEMM",
-    "KERNEL_W4A8_TC",
+    "KERNEL_W4A8_TC", "OP_MXFP4_GEMM", "OP_NVFP4_GEMM", "KERNEL_MXFP4_TC", "KERNEL_NVFP4_TC",
+    "qlin_nvfp4_scale_bytes", "qlin_quant_mxfp4", "qlin_nvfp4_tensor_scale", "qlin_quant_nvfp4", "qlin_mxfp4_gemm",
+    "qlin_nvfp4_gemm",
 ]
 
 OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM, OP_MXFP8_GEMM, OP_W4A8_GEMM = 1, 2, 3, 4, 5, 6
+OP_MXFP4_GEMM, OP_NVFP4_GEMM = 7, 8
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 (KERNEL_W4A16_MMA, KERNEL_W4A16_GEMV, KERNEL_W4A16_TC, KERNEL_W8A8_MMA, KERNEL_W8A8_GEMV, KERNEL_W8A8_TC,
- KERNEL_W8A8_BLOCK_TC, KERNEL_MXFP8_TC, KERNEL_W4A8_TC) = 1, 2, 3, 4, 5, 6, 7, 8, 9
+ KERNEL_W8A8_BLOCK_TC, KERNEL_MXFP8_TC, KERNEL_W4A8_TC, KERNEL_MXFP4_TC, KERNEL_NVFP4_TC) = range(1, 12)
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = 0, 1, 2, 3
 PACK_FORMAT_VERSION = 2
 
@@ -77,6 +80,12 @@ _SIGS = {
     "qlin_w4a8_gemm": [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _sz, _p],
     "qlin_quant_mxfp8": [_p, _i64, _i64, _p, _p, _p],
     "qlin_mxfp8_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
+    "qlin_nvfp4_scale_bytes": [_i64, _i64, ctypes.POINTER(_sz)],
+    "qlin_quant_mxfp4": [_p, _i64, _i64, _p, _p, _p],
+    "qlin_nvfp4_tensor_scale": [_p, _i64, _p, _p],
+    "qlin_quant_nvfp4": [_p, _i64, _i64, _p, _p, _p, _p],
+    "qlin_mxfp4_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
+    "qlin_nvfp4_gemm": [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
 }
 
 
@@ -268,6 +277,36 @@ def qlin_quant_mxfp8(X, R, K, codes, scales, stream=None):
 def qlin_mxfp8_gemm(Xq, xs, Wq, ws_sf, Y, M, N, K, workspace, ws_bytes, stream=None):
     return _check(load().qlin_mxfp8_gemm(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws_sf), _ptr(Y), M, N, K,
                                          _ptr(workspace), ws_bytes, _stream(stream)), "qlin_mxfp8_gemm")
+
+
+def qlin_nvfp4_scale_bytes(R: int, K: int) -> int:
+    b = _sz()
+    _check(load().qlin_nvfp4_scale_bytes(R, K, ctypes.byref(b)), "qlin_nvfp4_scale_bytes")
+    return b.value
+
+
+def qlin_quant_mxfp4(X, R, K, codes, scales, stream=None):
+    return _check(load().qlin_quant_mxfp4(_ptr(X), R, K, _ptr(codes), _ptr(scales), _stream(stream)),
+                  "qlin_quant_mxfp4")
+
+
+def qlin_nvfp4_tensor_scale(X, n, sg, stream=None):
+    return _check(load().qlin_nvfp4_tensor_scale(_ptr(X), n, _ptr(sg), _stream(stream)), "qlin_nvfp4_tensor_scale")
+
+
+def qlin_quant_nvfp4(X, R, K, sg, codes, scales, stream=None):
+    return _check(load().qlin_quant_nvfp4(_ptr(X), R, K, _ptr(sg), _ptr(codes), _ptr(scales), _stream(stream)),
+                  "qlin_quant_nvfp4")
+
+
+def qlin_mxfp4_gemm(Xq, xs, Wq, ws_sf, Y, M, N, K, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_mxfp4_gemm(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws_sf), _ptr(Y), M, N, K,
+                                         _ptr(workspace), ws_bytes, _stream(stream)), "qlin_mxfp4_gemm")
+
+
+def qlin_nvfp4_gemm(Xq, xs, sgx, Wq, ws_sf, sgw, Y, M, N, K, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_nvfp4_gemm(_ptr(Xq), _ptr(xs), _ptr(sgx), _ptr(Wq), _ptr(ws_sf), _ptr(sgw), _ptr(Y),
+                                         M, N, K, _ptr(workspace), ws_bytes, _stream(stream)), "qlin_nvfp4_gemm")
 
 
 def qlin_get_device_error(stream=None) -> int:

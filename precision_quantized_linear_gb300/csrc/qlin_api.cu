@@ -15,6 +15,7 @@ namespace qlin {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxM = int64_t(1) << 24;
+constexpr int64_t kFp4K = 256;  // K granularity of the FP4 calls
 
 // Error word of each device (first error wins; cleared by qlin_get_device_error).
 __device__ int g_error_word;
@@ -275,6 +276,11 @@ qlin_status_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, int G
       *bytes = M == 0 ? 0 : plan_w8a8_block_tc(M, N, K, d->num_sms).split.ws_bytes;
       return QLIN_OK;
     case QLIN_OP_MXFP8_GEMM: *bytes = M == 0 ? 0 : plan_mxfp8_tc(M, N, K, d->num_sms).split.ws_bytes; return QLIN_OK;
+    case QLIN_OP_MXFP4_GEMM:
+    case QLIN_OP_NVFP4_GEMM:
+      if (K % kFp4K != 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
+      *bytes = M == 0 ? 0 : plan_fp4_tc(M, N, K, d->num_sms).split.ws_bytes;
+      return QLIN_OK;
     case QLIN_OP_W4A8_GEMM:
       if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;
       *bytes = M == 0 ? 0 : plan_w4a8_tc(M, N, K, d->num_sms).split.ws_bytes;
@@ -314,6 +320,11 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
     dp.kernel = QLIN_KERNEL_MXFP8_TC;
     dp.tp = plan_mxfp8_tc(M, N, K, num_sms);
     dp.ws = dp.tp.split.ws_bytes;
+  } else if (op == QLIN_OP_MXFP4_GEMM || op == QLIN_OP_NVFP4_GEMM) {
+    if (K % kFp4K != 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
+    dp.kernel = op == QLIN_OP_MXFP4_GEMM ? QLIN_KERNEL_MXFP4_TC : QLIN_KERNEL_NVFP4_TC;
+    dp.tp = plan_fp4_tc(M, N, K, num_sms);
+    dp.ws = dp.tp.split.ws_bytes;
   } else {
     return QLIN_ERR_INVALID_VALUE;
   }
@@ -322,7 +333,8 @@ qlin_status_t qlin_plan_info(int op, int64_t M, int64_t N, int64_t K, int G, int
   info[0] = dp.kernel;
   const bool tc = dp.kernel == QLIN_KERNEL_W4A16_TC || dp.kernel == QLIN_KERNEL_W8A8_TC ||
                   dp.kernel == QLIN_KERNEL_W8A8_BLOCK_TC || dp.kernel == QLIN_KERNEL_MXFP8_TC ||
-                  dp.kernel == QLIN_KERNEL_W4A8_TC;
+                  dp.kernel == QLIN_KERNEL_W4A8_TC || dp.kernel == QLIN_KERNEL_MXFP4_TC ||
+                  dp.kernel == QLIN_KERNEL_NVFP4_TC;
   if (tc) {
     info[1] = dp.tp.bn;
     info[2] = dp.tp.wn;
@@ -608,6 +620,96 @@ qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const vo
                                        static_cast<const uint8_t*>(Wq_e4m3), static_cast<const uint8_t*>(ws_e8m0),
                                        static_cast<uint16_t*>(Y_bf16), M, N, K, p, workspace, d->err, d->num_sms,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+// ---- FP4: packed E2M1, K % 256 == 0 (one 128-byte TMA box = 256 columns per K block)
+
+static bool fp4_rows_ok(int64_t R, int64_t K) {
+  return R >= 0 && R <= kMaxM * 64 && K > 0 && K % kFp4K == 0 && K <= (int64_t(1) << 31);
+}
+
+qlin_status_t qlin_nvfp4_scale_bytes(int64_t R, int64_t K, size_t* bytes) {
+  if (!bytes) return QLIN_ERR_INVALID_VALUE;
+  if (!fp4_rows_ok(R, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  *bytes = static_cast<size_t>((R + 127) / 128 * 128 * (K / 16));
+  return QLIN_OK;
+}
+
+qlin_status_t qlin_quant_mxfp4(const void* X_bf16, int64_t R, int64_t K, void* codes_e2m1, void* scales_e8m0,
+                               void* stream) {
+  if (!fp4_rows_ok(R, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (R == 0) return QLIN_OK;
+  if (!X_bf16 || !codes_e2m1 || !scales_e8m0) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(X_bf16) || !aligned16(codes_e2m1) || !aligned16(scales_e8m0)) return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  qlin_status_t st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_quant_mxfp4(static_cast<const uint16_t*>(X_bf16), R, K,
+                                          static_cast<uint8_t*>(codes_e2m1), static_cast<uint8_t*>(scales_e8m0),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_nvfp4_tensor_scale(const void* X_bf16, int64_t n, float* sg, void* stream) {
+  if (n <= 0 || n % 8 != 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (!X_bf16 || !sg) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(X_bf16) || (reinterpret_cast<uintptr_t>(sg) & 3u) != 0) return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  qlin_status_t st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_nvfp4_tensor_scale(static_cast<const uint16_t*>(X_bf16), n, sg, d->num_sms,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_quant_nvfp4(const void* X_bf16, int64_t R, int64_t K, const float* sg, void* codes_e2m1,
+                               void* scales_e4m3, void* stream) {
+  if (!fp4_rows_ok(R, K)) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (R == 0) return QLIN_OK;
+  if (!X_bf16 || !sg || !codes_e2m1 || !scales_e4m3) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(X_bf16) || !aligned16(codes_e2m1) || !aligned16(scales_e4m3) ||
+      (reinterpret_cast<uintptr_t>(sg) & 3u) != 0)
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  qlin_status_t st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  return launch_status(launch_quant_nvfp4(static_cast<const uint16_t*>(X_bf16), R, K, sg,
+                                          static_cast<uint8_t*>(codes_e2m1), static_cast<uint8_t*>(scales_e4m3),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+static qlin_status_t fp4_gemm(const void* Xq, const void* xs, const float* sgx, const void* Wq, const void* ws_sf,
+                              const float* sgw, bool nv, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  qlin_status_t st = check_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (K % kFp4K != 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return QLIN_OK;
+  if (!Xq || !xs || !Wq || !ws_sf || !Y_bf16 || (nv && (!sgx || !sgw))) return QLIN_ERR_INVALID_VALUE;
+  if (!aligned16(Xq) || !aligned16(xs) || !aligned16(Wq) || !aligned16(ws_sf) || !aligned16(Y_bf16) ||
+      (workspace && !aligned16(workspace)) ||
+      (nv && ((reinterpret_cast<uintptr_t>(sgx) & 3u) != 0 || (reinterpret_cast<uintptr_t>(sgw) & 3u) != 0)))
+    return QLIN_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != QLIN_OK) return st;
+  const TcPlan p = plan_fp4_tc(M, N, K, d->num_sms);
+  if (p.split.ws_bytes > 0 && (!workspace || ws_bytes < p.split.ws_bytes)) return QLIN_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_fp4_tc(static_cast<const uint8_t*>(Xq), static_cast<const uint8_t*>(xs), sgx,
+                                     static_cast<const uint8_t*>(Wq), static_cast<const uint8_t*>(ws_sf), sgw,
+                                     static_cast<uint16_t*>(Y_bf16), M, N, K, nv, p, workspace, d->err, d->num_sms,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_mxfp4_gemm(const void* Xq_e2m1, const void* xs_e8m0, const void* Wq_e2m1, const void* ws_e8m0,
+                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  return fp4_gemm(Xq_e2m1, xs_e8m0, nullptr, Wq_e2m1, ws_e8m0, nullptr, false, Y_bf16, M, N, K, workspace, ws_bytes,
+                  stream);
+}
+
+qlin_status_t qlin_nvfp4_gemm(const void* Xq_e2m1, const void* xs_e4m3, const float* sgx, const void* Wq_e2m1,
+                              const void* ws_e4m3, const float* sgw, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  return fp4_gemm(Xq_e2m1, xs_e4m3, sgx, Wq_e2m1, ws_e4m3, sgw, true, Y_bf16, M, N, K, workspace, ws_bytes, stream);
 }
 
 qlin_status_t qlin_selftest_wait_timeout(uint32_t limit_us, void* stream) {

@@ -168,6 +168,18 @@ cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t*
                             int num_sms, cudaStream_t st);
 cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t st);
+// FP4: packed E2M1 operands (two per byte, K / 2 bytes per row) with MXFP4
+// (E8M0 per 32 columns) or NVFP4 (E4M3 per 16 columns and an FP32 per-tensor
+// scale sgx / sgw) scale atoms; see qlin_quant_mxfp4 / qlin_quant_nvfp4.
+TcPlan plan_fp4_tc(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_fp4_tc(const uint8_t* Xq, const uint8_t* xs, const float* sgx, const uint8_t* Wq,
+                          const uint8_t* ws_sf, const float* sgw, uint16_t* Y, int64_t M, int64_t N, int64_t K,
+                          bool nv, const TcPlan& plan, void* ws, int* err, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_mxfp4(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t st);
+cudaError_t launch_nvfp4_tensor_scale(const uint16_t* X, int64_t n, float* sg, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_nvfp4(const uint16_t* X, int64_t R, int64_t K, const float* sg, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t st);
 cudaError_t launch_quant_act_fp8_blocks(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx,
                                         cudaStream_t st);
 cudaError_t launch_quant_w_fp8_blocks(const uint16_t* W, int64_t N, int64_t K, uint8_t* Wq, float* sw,

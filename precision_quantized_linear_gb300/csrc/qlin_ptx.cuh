@@ -334,6 +334,34 @@ __device__ __forceinline__ void mma_mx8(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// Block-scaled FP4 MMA, M = 128, K = 64 E2M1 elements (32 bytes) per operand
+// row: MXFP4 (kind::mxf4, an E8M0 scale per 32 elements: two scale bytes per
+// row, idesc ids 0 or 2) and NVFP4 (kind::mxf4nvf4, an E4M3 scale per 16
+// elements: four bytes, id 0).  Row m of A reads its scales from TMEM lane m,
+// column sfa_tmem + m / 32; token n of B from lane n % 32 of every lane
+// quadrant, column sfb_tmem + n / 32.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copy a 512-byte shared-memory atom of 32 rows x 16 bytes into TMEM lanes
 // 32q + r, columns taddr .. taddr + 3, for each lane quadrant q (row r's four
 // 32-bit words go to the four columns).  In issue order with this thread's MMAs.
@@ -436,6 +464,18 @@ __host__ __device__ constexpr uint32_t idesc_mx(uint32_t mma_n, uint32_t a_id, u
   return (b_id << 4)                 // scale byte of B
          | ((mma_n >> 3) << 17)      // N / 8
          | (1u << 23)                // scale type: E8M0
+         | ((128u >> 4) << 24)       // M / 16
+         | (a_id << 29);             // scale byte of A
+}
+
+// Instruction descriptor of the block-scaled FP4 MMAs (M = 128): E2M1 A and
+// B (format code 1), K-major; e8m0 = 1 for E8M0 scales (MXFP4), 0 for E4M3
+// (NVFP4); a_id / b_id pick the first scale byte of each row's word.
+__host__ __device__ constexpr uint32_t idesc_f4(uint32_t mma_n, uint32_t a_id, uint32_t b_id, uint32_t e8m0) {
+  return (b_id << 4)                 // scale byte of B
+         | (1u << 7) | (1u << 10)    // A and B: E2M1
+         | ((mma_n >> 3) << 17)      // N / 8
+         | (e8m0 << 23)              // scale type
          | ((128u >> 4) << 24)       // M / 16
          | (a_id << 29);             // scale byte of A
 }

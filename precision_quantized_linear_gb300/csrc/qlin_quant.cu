@@ -444,4 +444,178 @@ cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t*
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ FP4 (E2M1)
+
+// Eight floats -> eight E2M1 codes, rounded to nearest even with saturation
+// at +-6 (cvt.rn.satfinite.e2m1x2), two per byte with the even element in the
+// low nibble: one 32-bit word.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Eight BF16 columns of one 16-byte load
+__device__ __forceinline__ void bf16x8(uint4 raw, float (&v)[8]) {
+  v[0] = bf16_lo(raw.x);
+  v[1] = bf16_hi(raw.x);
+  v[2] = bf16_lo(raw.y);
+  v[3] = bf16_hi(raw.y);
+  v[4] = bf16_lo(raw.z);
+  v[5] = bf16_hi(raw.z);
+  v[6] = bf16_lo(raw.w);
+  v[7] = bf16_hi(raw.w);
+}
+
+// MXFP4 ([LP] S10, OCP Microscaling v1.0): one warp per (row r, 256 columns);
+// lane l holds columns 8l .. 8l+7, a block of 32 columns is a segment of four
+// lanes.  e = floor(log2 amax) - 2 (2: exponent of E2M1's largest normal,
+// 6 = 1.5 x 2^2), clamped to [-127, 127], -127 for an all-zero block; codes
+// E2M1(v * 2^-e) (the power-of-two scaling is exact).  The 256 columns fill
+// two scale atoms: the word of atom 2c + h (h = lane / 16) holds the scale
+// bytes of lanes 16h, +4, +8, +12; rows past R write only their atom words (0).
+__global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __restrict__ X, int64_t R, int64_t K,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nc = K / 256;
+  const int64_t rows = (R + 127) / 128 * 128;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= rows * nc) return;  // whole warps only
+  const int64_t r = item / nc, c = item % nc;
+  uint32_t e8 = 0;
+  if (r < R) {
+    float v[8];
+    bf16x8(*reinterpret_cast<const uint4*>(X + r * K + c * 256 + 8 * lane), v);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = seg_max(amax, 4);
+    const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // 0: zero or below 2^-126
+    int e = eb == 0 ? -127 : eb - 127 - 2;
+    e = e < -127 ? -127 : e;
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e in [-127, 125]
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= inv;
+    *reinterpret_cast<uint32_t*>(codes + r * (K / 2) + c * 128 + 4 * lane) = e2m1x8(v);
+    e8 = static_cast<uint32_t>(e + 127);
+  }
+  uint32_t word = (e8 & 0xFFu) << (8 * ((lane >> 2) & 3));
+  word |= __shfl_xor_sync(0xffffffffu, word, 4);
+  word |= __shfl_xor_sync(0xffffffffu, word, 8);
+  if ((lane & 15) == 0) {
+    uint8_t* atom = scales + ((r / 128) * (K / 128) + 2 * c + (lane >> 4)) * 512;
+    *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+  }
+}
+
+cudaError_t launch_quant_mxfp4(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t st) {
+  const int64_t warps = (R + 127) / 128 * 128 * (K / 256);
+  const int64_t blocks = (warps + 7) / 8;
+  quant_mxfp4_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, R, K, codes, scales);
+  return cudaGetLastError();
+}
+
+// NVFP4 per-tensor scale sg = amax(|X|) / (6 x 448), 1 when that is 0.  The
+// amax is reduced into the output word as FP32 bits (non-negative floats
+// order like their bit patterns), which a one-thread kernel then turns into sg.
+__global__ void __launch_bounds__(256) amax_bits_kernel(const uint16_t* __restrict__ X, int64_t n8,
+                                                        unsigned* __restrict__ out) {
+  float amax = 0.0f;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float v[8];
+    bf16x8(reinterpret_cast<const uint4*>(X)[i], v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  }
+  amax = seg_max(amax, 32);
+  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(amax));
+}
+
+__global__ void nvfp4_scale_finish_kernel(float* sg) {
+  const float amax = __uint_as_float(*reinterpret_cast<const unsigned*>(sg));
+  const float s = __fdiv_rn(amax, 2688.0f);
+  *sg = s == 0.0f ? 1.0f : s;
+}
+
+cudaError_t launch_nvfp4_tensor_scale(const uint16_t* X, int64_t n, float* sg, int num_sms, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(sg, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  const int64_t n8 = n / 8;
+  int64_t blocks = (n8 + 255) / 256;
+  if (blocks > 4LL * num_sms) blocks = 4LL * num_sms;
+  if (blocks < 1) blocks = 1;
+  amax_bits_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, n8, reinterpret_cast<unsigned*>(sg));
+  nvfp4_scale_finish_kernel<<<1, 1, 0, st>>>(sg);
+  return cudaGetLastError();
+}
+
+// E4M3 code -> its value (exact through FP16; the code in both bytes, so
+// either half of the result holds it)
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(code * 0x0101u)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// NVFP4 ([LP] S10 names it; the vendor's two-level recipe): one warp per
+// (row r, 256 columns), lane l holds columns 8l .. 8l+7, a block of 16 columns
+// is a pair of lanes.  Block scale sb = E4M3(amax_b / (6 sg)) (RNE, saturating),
+// elements E2M1(v / (sb sg)); each step is one IEEE binary32 operation
+// (__fmul_rn / __fdiv_rn); a block whose scale is 0 stores code 0.  The 256
+// columns fill four scale atoms (64 columns each): the word of atom 4c + a
+// (a = lane / 8) holds the scale bytes of lanes 8a, +2, +4, +6.
+__global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __restrict__ X, int64_t R, int64_t K,
+                                                          const float* __restrict__ sgp, uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nc = K / 256;
+  const int64_t rows = (R + 127) / 128 * 128;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= rows * nc) return;  // whole warps only
+  const int64_t r = item / nc, c = item % nc;
+  uint32_t sc = 0;
+  if (r < R) {
+    const float sg = __ldg(sgp);
+    float v[8];
+    bf16x8(*reinterpret_cast<const uint4*>(X + r * K + c * 256 + 8 * lane), v);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = seg_max(amax, 2);
+    sc = e4m3x2(__fdiv_rn(amax, __fmul_rn(6.0f, sg)), 0.0f) & 0xFFu;
+    uint32_t q = 0;
+    if (sc != 0) {
+      const float den = __fmul_rn(e4m3_value(sc), sg);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(v[i], den);
+      q = e2m1x8(v);
+    }
+    *reinterpret_cast<uint32_t*>(codes + r * (K / 2) + c * 128 + 4 * lane) = q;
+  }
+  uint32_t word = sc << (8 * ((lane >> 1) & 3));
+  word |= __shfl_xor_sync(0xffffffffu, word, 2);
+  word |= __shfl_xor_sync(0xffffffffu, word, 4);
+  if ((lane & 7) == 0) {
+    uint8_t* atom = scales + ((r / 128) * (K / 64) + 4 * c + (lane >> 3)) * 512;
+    *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+  }
+}
+
+cudaError_t launch_quant_nvfp4(const uint16_t* X, int64_t R, int64_t K, const float* sg, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t st) {
+  const int64_t warps = (R + 127) / 128 * 128 * (K / 256);
+  const int64_t blocks = (warps + 7) / 8;
+  quant_nvfp4_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, R, K, sg, codes, scales);
+  return cudaGetLastError();
+}
+
 }  // namespace qlin

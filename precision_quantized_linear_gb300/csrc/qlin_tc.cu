@@ -40,12 +40,23 @@ namespace qlin {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr int kSmemBudget = 225 * 1024;
 
-template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool MX = false, bool A8 = false>
+// Block-scaled formats whose scales the MMA applies (template argument MX)
+constexpr int kMxNone = 0;
+constexpr int kMxF8 = 1;  // MXFP8: E4M3 elements, E8M0 scale per 32 (kind::mxf8f6f4, scale_vec::1X)
+constexpr int kMxF4 = 2;  // MXFP4: E2M1 elements, E8M0 scale per 32 (kind::mxf4, scale_vec::2X)
+constexpr int kNvF4 = 3;  // NVFP4: E2M1 elements, E4M3 scale per 16 (kind::mxf4nvf4, scale_vec::4X)
+
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, int MX = kMxNone, bool A8 = false>
 struct TcCfg {
+  static constexpr bool kF4 = MX == kMxF4 || MX == kNvF4;     // E2M1 operands, two per byte
   static constexpr int kBlkBytes = 128;                         // bytes of one row of a K block
   // K columns per block: 64 for W4A16 (one packed code tile), 128 for E4M3
-  // operands; W4A8 takes two code tiles (one quantisation group) per block
-  static constexpr int kCols = (W4 && !A8) ? 64 : 128;
+  // operands, 256 for E2M1; W4A8 takes two code tiles (one quantisation
+  // group) per block
+  static constexpr int kCols = kF4 ? 256 : (W4 && !A8) ? 64 : 128;
+  // TMA column step of a K block, in elements of the tensor map (BF16 for
+  // W4A16 activations, bytes otherwise)
+  static constexpr int kTmaX = (W4 && !A8) ? 64 : 128;
   static constexpr int kXBlk = BN * kBlkBytes;                  // token tile of one K block
   static constexpr int kWBlk = W4 ? (A8 ? 8192 : 4096) : WN * kBlkBytes;  // packed codes / E4M3 tile of one K block
   // group scales and zero-points of a stage: room for G = 32 (two groups per
@@ -55,13 +66,17 @@ struct TcCfg {
   static constexpr int kScaleOff = KPS * kXBlk + KPS * kWBlk;   // scales, then zero-points (W4A16)
   static constexpr int kZeroOff = kScaleOff + kGroupsMax * 256;
   static constexpr int kMetaBytes = W4 ? ((kGroupsMax * 320 + 1023) / 1024) * 1024 : 0;
-  // MXFP8: the E8M0 scale atoms of the stage's K block (512 bytes of weight
-  // scales, then 512 of token scales), copied into TMEM by the MMA thread
+  // Block-scaled formats: the scale atoms of the stage's K block (kSfK
+  // atoms of weight scales, then kSfK per 128 tokens), copied into TMEM by
+  // the MMA thread.  An atom holds four scales of 128 rows: 128 columns of
+  // MXFP8, 128 of MXFP4 (two per 256-column block), 64 of NVFP4 (four)
+  static constexpr int kSfK = MX == kNvF4 ? 4 : MX == kMxF4 ? 2 : 1;
   static constexpr int kSfOff = KPS * kXBlk + KPS * kWBlk + kMetaBytes;
   static constexpr int kSfbAtoms = BN > 128 ? 2 : 1;                // token atoms of a tile
-  static constexpr int kSfBytes = MX ? ((512 * (1 + kSfbAtoms) + 1023) / 1024) * 1024 : 0;
+  static constexpr int kSfBytes = MX ? ((512 * kSfK * (1 + kSfbAtoms) + 1023) / 1024) * 1024 : 0;
   static constexpr int kStage = KPS * kXBlk + KPS * kWBlk + kMetaBytes + kSfBytes;
-  static constexpr int kTxBase = KPS * kXBlk + KPS * kWBlk + (MX ? 512 * (1 + kSfbAtoms) : 0);  // W4A16: plus 320 B per group
+  static constexpr int kTxBase =
+      KPS * kXBlk + KPS * kWBlk + (MX ? 512 * kSfK * (1 + kSfbAtoms) : 0);  // W4A16: plus 320 B per group
   // dequantised BF16 weight tiles: in TMEM (tcgen05.st, read by the MMA as
   // its A operand) when the accumulators leave room, else in shared memory
   static constexpr bool kATmem = W4 && BN <= 128;
@@ -92,16 +107,17 @@ struct TcCfg {
   static constexpr int kAccCols = kTokM ? WN : BN;              // one accumulator
   // accumulators in TMEM: two (one unit while the epilogue drains the other);
   // block scaling and W4A8 keep up to four K-block partial products in flight
-  // MXFP8 with 256-token tiles keeps one (the scale-factor ring takes the rest of TMEM)
+  // block-scaled formats with 256-token tiles keep one (the scale-factor ring takes the rest of TMEM)
   static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : A8 ? 4 : (MX && BN == 256) ? 1 : 2;
   static constexpr int kAColBase = kAccBufs * BN;               // first TMEM column of the A slots
-  // MXFP8 scale factors in TMEM: a ring of kSfSlots K blocks, four columns of
-  // weight scales and four of token scales each (see mma_mx8)
+  // Block scale factors in TMEM: a ring of kSfSlots K blocks, four columns
+  // per atom (see mma_mx8, mma_mxf4): kSfK atoms of weight scales and
+  // kSfK x kSfbAtoms of token scales per slot
   static constexpr int kSfSlots = MX ? 4 : 0;
   static constexpr int kSfaCol = kAccBufs * BN;
-  static constexpr int kSfbCol = kSfaCol + 4 * kSfSlots;  // token scales: 4 columns per atom and slot
+  static constexpr int kSfbCol = kSfaCol + 4 * kSfK * kSfSlots;
   static constexpr int kTmemNeed =
-      kAccBufs * BN + (kATmem ? kAStages * kASlotCols : 0) + 4 * kSfSlots * (1 + kSfbAtoms);
+      kAccBufs * BN + (kATmem ? kAStages * kASlotCols : 0) + 4 * kSfSlots * kSfK * (1 + kSfbAtoms);
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                  : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kDqWarps = W4 ? 8 : 0;
@@ -120,7 +136,12 @@ struct TcCfg {
   static_assert(kTmemNeed <= 512, "TMEM budget");
   static_assert(!BS || (!W4 && BN <= 128), "block scaling: E4M3 operands, at most 128 tokens (running sums in registers)");
   static_assert(WN == 128 || (kTokM && WN == 256), "256-row weight tiles only token-major");
-  static_assert(!MX || (!W4 && !BS && BN >= 32), "MXFP8: E4M3 operands, at least 32 tokens per tile");
+  static_assert(!MX || (!W4 && !BS && BN >= 32), "block-scaled formats: 8- or 4-bit float operands, at least 32 tokens per tile");
+  // The FP4 MMAs (scale_vec::2X / 4X) take scale addresses a multiple of four
+  // TMEM columns above the 32-column-aligned scale region; a 64-token tile
+  // would start two columns into its token atom (32-token tiles run only as the
+  // single token block of M <= 32, checked by the host)
+  static_assert(!kF4 || BN != 64, "FP4: 32 (one token block), 128 or 256 tokens per tile");
   static_assert(!A8 || (W4 && !BS && !MX && BN <= 64), "W4A8: packed INT4 weights, at most 64 tokens per tile");
   static_assert(kSlotBlocks == 1 || KPS % 2 == 0, "two-block slots need an even number of blocks per stage");
 };
@@ -131,8 +152,9 @@ struct TcArgs {
   const uint8_t* zeros;
   const float* sx;
   const float* sw;  // W8A8 block scaling: sx = [K/128][M], sw = [N/128][K/128]
-  const uint8_t* sfa;  // MXFP8: E8M0 scale atoms of the weights, [N/128][K/128][512 B]
-  const uint8_t* sfb;  // MXFP8: E8M0 scale atoms of the tokens, [ceil(M/128)][K/128][512 B]
+  const uint8_t* sfa;  // block-scaled formats: scale atoms of the weights, [N/128][K atoms][512 B]
+  const uint8_t* sfb;  // block-scaled formats: scale atoms of the tokens, [ceil(M/128)][K atoms][512 B]
+                       // (NVFP4: sx / sw point at the two FP32 per-tensor scales)
   uint16_t* Y;
   float* partials;
   uint32_t* counters;
@@ -206,9 +228,9 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& a, int u, int64_t KB) {
 }
 
 // EPI: the output epilogue (bias, activation) of the *_gemm_fused calls is compiled in;
-// MX: E4M3 operands with E8M0 block scales applied by the MMA (MXFP8);
+// MX: block-scaled operands whose scales the MMA applies (kMxF8, kMxF4, kNvF4);
 // A8: packed INT4 weights (W4 = true) dequantised to E4M3 times E4M3 tokens (W4A8)
-template <int BN, bool W4, int KPS, bool BS, int WN, bool EPI, bool MX = false, bool A8 = false>
+template <int BN, bool W4, int KPS, bool BS, int WN, bool EPI, int MX = kMxNone, bool A8 = false>
 __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ TcArgs a) {
@@ -292,10 +314,11 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         } else {
 #pragma unroll
           for (int h = 0; h < WN / kTileN; ++h)  // one box of 128 rows per scale block
-            tma_load_2d_hint(st + C::kXBlk + h * kTileN * C::kBlkBytes, &tmap_w, &full[s], kb * C::kCols,
+            tma_load_2d_hint(st + C::kXBlk + h * kTileN * C::kBlkBytes, &tmap_w, &full[s], kb * C::kTmaX,
                              un.nt * WN + h * kTileN, pol_stream);
-          if constexpr (MX)  // the weight tile's scale atom of this K block
-            bulk_load(st + C::kSfOff, a.sfa + (static_cast<int64_t>(un.nt) * KB + kb) * 512, 512, &full[s]);
+          if constexpr (MX != kMxNone)  // the weight tile's scale atoms of this K block
+            bulk_load(st + C::kSfOff, a.sfa + (static_cast<int64_t>(un.nt) * KB + kb) * (512 * C::kSfK),
+                      512 * C::kSfK, &full[s]);
         }
       };
       auto load_x = [&](int s, const Unit& un, int j) {
@@ -303,15 +326,16 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         const int kb = un.kb0 + j * KPS;
 #pragma unroll
         for (int i = 0; i < KPS; ++i)
-          tma_load_2d_hint(st + i * C::kXBlk, &tmap_x, &full[s], (kb + i) * C::kCols, un.mb * BN, pol_keep);
-        if constexpr (MX) {  // the scale atom(s) of the 128 tokens holding this token block
+          tma_load_2d_hint(st + i * C::kXBlk, &tmap_x, &full[s], (kb + i) * C::kTmaX, un.mb * BN, pol_keep);
+        if constexpr (MX != kMxNone) {  // the scale atoms of the 128 tokens holding this token block
           const int64_t natoms = (a.M + 127) / 128;  // atoms the caller's buffer holds
 #pragma unroll
           for (int t = 0; t < C::kSfbAtoms; ++t) {
             // a 256-token tile past the last atom takes that atom again: its
             // tokens are beyond M (zero rows, outputs never written)
             const int64_t atom = imin64(static_cast<int64_t>(un.mb) * BN / 128 + t, natoms - 1);
-            bulk_load(st + C::kSfOff + 512 * (1 + t), a.sfb + (atom * KB + kb) * 512, 512, &full[s]);
+            bulk_load(st + C::kSfOff + 512 * C::kSfK * (1 + t), a.sfb + (atom * KB + kb) * (512 * C::kSfK),
+                      512 * C::kSfK, &full[s]);
           }
         }
       };
@@ -385,10 +409,12 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         set_error(a.err, QLIN_ERR_TIMEOUT);
         s_abort = 1;
       }
-    } else if (lane == 0 && MX) {
-      // MXFP8: per K block, copy its two scale atoms into the next TMEM slot
-      // of the ring (in issue order with the MMAs), then four MMAs of 32
-      // columns, k-step kk taking byte kk of each scale word
+    } else if (lane == 0 && MX != kMxNone) {
+      // Block-scaled formats: per K block, copy its scale atoms into the next
+      // TMEM slot of the ring (in issue order with the MMAs), then four MMAs
+      // of 32 bytes of K.  MXFP8: k-step kk takes byte kk of each scale word;
+      // MXFP4 (64 columns per step): atom kk / 2, bytes 2 (kk % 2) and +1;
+      // NVFP4 (64 columns): atom kk, bytes 0..3
       int it = 0, ua = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++ua) {
@@ -409,18 +435,33 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
           }
           tc_fence_after();
           const uint32_t slot = static_cast<uint32_t>(C::kSfSlots ? it % C::kSfSlots : 0);
-          const uint32_t t_sfa = tmem_base + C::kSfaCol + slot * 4;
-          const uint32_t t_sfb = tmem_base + C::kSfbCol + slot * 4 * C::kSfbAtoms;
+          const uint32_t t_sfa = tmem_base + C::kSfaCol + slot * 4 * C::kSfK;
+          const uint32_t t_sfb = tmem_base + C::kSfbCol + slot * 4 * C::kSfK * C::kSfbAtoms;
           const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
-          tc_cp_atom(t_sfa, sdesc_atom(st_u32 + C::kSfOff));
 #pragma unroll
-          for (int t = 0; t < C::kSfbAtoms; ++t)  // tokens 128 t .. read columns 4 t ..
-            tc_cp_atom(t_sfb + 4 * t, sdesc_atom(st_u32 + C::kSfOff + 512 * (1 + t)));
+          for (int c = 0; c < C::kSfK; ++c) {
+            tc_cp_atom(t_sfa + 4 * c, sdesc_atom(st_u32 + C::kSfOff + 512 * c));
+#pragma unroll
+            for (int t = 0; t < C::kSfbAtoms; ++t)  // K atom c, tokens 128 t ..: columns 4 (c kSfbAtoms + t) ..
+              tc_cp_atom(t_sfb + 4 * (c * C::kSfbAtoms + t),
+                         sdesc_atom(st_u32 + C::kSfOff + 512 * C::kSfK * (1 + t) + 512 * c));
+          }
           const uint32_t a_addr = st_u32 + C::kXBlk, b_addr = st_u32;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_mx8(tmem_d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc_mx(BN, kk, kk), t_sfa,
-                    t_sfb + tok_col, (j | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(a_addr + kk * 32), bd = sdesc_sw128(b_addr + kk * 32);
+            const uint32_t accum = (j | kk) != 0;
+            if constexpr (MX == kMxF8) {
+              mma_mx8(tmem_d, ad, bd, idesc_mx(BN, kk, kk), t_sfa, t_sfb + tok_col, accum);
+            } else if constexpr (MX == kMxF4) {
+              const uint32_t c = kk >> 1, id = 2 * (kk & 1);
+              mma_mxf4(tmem_d, ad, bd, idesc_f4(BN, id, id, 1), t_sfa + 4 * c, t_sfb + 4 * c * C::kSfbAtoms + tok_col,
+                       accum);
+            } else {
+              mma_nvf4(tmem_d, ad, bd, idesc_f4(BN, 0, 0, 0), t_sfa + 4 * kk,
+                       t_sfb + 4 * kk * C::kSfbAtoms + tok_col, accum);
+            }
+          }
           mma_commit(&empty[s]);
         }
         mma_commit(&acc_full[acc]);
@@ -834,6 +875,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
     const int t = threadIdx.x - C::kEpiWarp0 * 32;  // 0 .. kEpiWarps * 32 - 1
     const int quad = warp & 3;                       // TMEM lane quadrant of this warp
     const float s_w = (W4 || BS || MX) ? 1.0f : *a.sw;
+    const float s_nv = MX == kNvF4 ? __ldg(a.sx) * __ldg(a.sw) : 1.0f;  // NVFP4: the two per-tensor scales
     int ua = 0;
     uint32_t epi_n = 0;  // staging boxes used so far
     int kbi = 0;         // K blocks promoted so far (block scaling)
@@ -1218,7 +1260,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
             for (int i = 0; i < 16; ++i) {
               const int64_t m = mbase + c0 + i;
               const float x = have ? __uint_as_float(v[i]) : 0.0f;
-              o[i] = (W4 || MX) ? x : (m < a.M ? (x * __ldg(a.sx + m)) * s_w : 0.0f);
+              o[i] = W4 ? x : MX ? (MX == kNvF4 ? x * s_nv : x) : (m < a.M ? (x * __ldg(a.sx + m)) * s_w : 0.0f);
             }
             if constexpr (EPI) epi_run(a.epi.act, o, bias_n);
 #pragma unroll
@@ -1270,6 +1312,9 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
                 const int64_t m = mbase + c0 + i;
                 acc_v[i] = m < a.M ? (acc_v[i] * __ldg(a.sx + m)) * s_w : 0.0f;
               }
+            } else if constexpr (MX == kNvF4) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc_v[i] *= s_nv;
             }
             if constexpr (EPI) epi_run(a.epi.act, acc_v, bias_n);
 #pragma unroll
@@ -1344,14 +1389,16 @@ static TcCost tc_cost(bool w4, int bn) {
 // Token tile and split count for M > 32 (tiles of 64 tokens or more), chosen
 // together to minimise max(memory time, rounds of units x unit cost + once).
 // Ties keep the wider tile (fewer re-reads of the weights).
-static void plan_tc_joint(TcPlan& p, int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn) {
+static void plan_tc_joint(TcPlan& p, int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn,
+                          int min_bn) {
   const int64_t KB = K / cols;
   const double wbytes = static_cast<double>(N) * static_cast<double>(K) * (w4 ? 0.51953125 : 1.0);
   const double xbytes = static_cast<double>(M) * static_cast<double>(K) * (w4 ? 2.0 : 1.0);
   const double ybytes = 2.0 * static_cast<double>(M) * static_cast<double>(N);
   double best = 1e30;
-  const int top = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
-  const int low = w4 ? 16 : 64;  // W4A16 plans every token tile this way
+  int top = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
+  if (top < min_bn) top = min_bn;
+  const int low = std::max(w4 ? 16 : 64, min_bn);  // W4A16 plans every token tile this way
   for (int bn = top; bn >= low; bn /= 2) {
     const TcCost cost = tc_cost(w4, bn);
     // A in TMEM (BN <= 128): slots of two blocks; narrow tiles four blocks per
@@ -1389,12 +1436,12 @@ static void plan_tc_joint(TcPlan& p, int64_t M, int64_t N, int64_t K, int num_sm
 }
 
 static TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int num_sms, int cols, bool w4, int max_bn = 256,
-                      int tile_n = kTileN, bool joint = true) {
+                      int tile_n = kTileN, bool joint = true, int min_bn = 0) {
   TcPlan p;
   p.bn = pick_bn(M) < max_bn ? pick_bn(M) : max_bn;
   p.wn = tile_n;
   if (joint && (p.bn >= 64 || w4) && tile_n == kTileN) {
-    plan_tc_joint(p, M, N, K, num_sms, cols, w4, max_bn);
+    plan_tc_joint(p, M, N, K, num_sms, cols, w4, max_bn, min_bn);
     return p;
   }
   p.mblocks = (M + p.bn - 1) / p.bn;
@@ -1465,6 +1512,14 @@ TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   if (p.bn < 32) p.bn = 32;  // the same single token block for M <= 16
   return p;
 }
+// FP4 (MXFP4, NVFP4): a K block of 256 E2M1 columns is 128 bytes per row,
+// the bytes and K blocks of an E4M3 problem of K / 2 columns; the MXFP8 plan
+// of that problem, without 64-token tiles (see TcCfg): one 32-token block up
+// to 32 tokens, 128- or 256-token tiles beyond.
+TcPlan plan_fp4_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
+  if (M <= 32) return plan_mxfp8_tc(M, N, K / 2, num_sms);
+  return plan_tc(M, N, K / 2, num_sms, 128, false, 256, kTileN, true, 128);
+}
 // Block scaling keeps the running sums of a 128-token tile in registers.  With
 // 128-token tiles the weight tile is 256 rows (two scale blocks) when N allows
 // and there are still enough tiles for every SM: a wider MMA moves fewer
@@ -1476,7 +1531,7 @@ TcPlan plan_w8a8_block_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   return plan_tc(M, N, K, num_sms, 128, false, 128, wn, false);
 }
 
-template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = false, bool MX = false, bool A8 = false>
+template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = false, int MX = kMxNone, bool A8 = false>
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
                              const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   using C = TcCfg<BN, W4, KPS, BS, WN, MX, A8>;
@@ -1491,8 +1546,8 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
   args.units = static_cast<int>(plan.split.tiles * plan.split.splits);
   {
     const double l2_half = 63.0 * 1024 * 1024;  // half of the 126 MB L2
-    const double wb = static_cast<double>(args.N) * static_cast<double>(args.K) * (W4 ? 0.51953125 : 1.0);
-    const double xb = static_cast<double>(args.M) * static_cast<double>(args.K) * ((W4 && !A8) ? 2.0 : 1.0);
+    const double wb = static_cast<double>(args.N) * static_cast<double>(args.K) * (W4 ? 0.51953125 : C::kF4 ? 0.5 : 1.0);
+    const double xb = static_cast<double>(args.M) * static_cast<double>(args.K) * ((W4 && !A8) ? 2.0 : C::kF4 ? 0.5 : 1.0);
     args.mb_fast = (wb > l2_half && xb < wb) ? 1 : 0;
     args.x_keep = xb <= l2_half / 2 ? 1 : 0;
   }
@@ -1620,11 +1675,49 @@ cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t*
   a.N = N;
   a.K = K;
   switch (plan.bn) {
-    case 32: return launch_tc<32, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 64: return launch_tc<64, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 128: return launch_tc<128, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    default: return launch_tc<256, false, 1, false, 128, false, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 32: return launch_tc<32, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 64: return launch_tc<64, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 128: return launch_tc<128, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default: return launch_tc<256, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
   }
+}
+
+template <int MX>
+static cudaError_t launch_fp4_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const TcArgs& a,
+                                 const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
+  switch (plan.bn) {
+    case 32:  // only as the single token block: its scales start at column 0 of the token atom
+      if (plan.mblocks != 1) return cudaErrorInvalidValue;
+      return launch_tc<32, false, 1, false, 128, false, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 128: return launch_tc<128, false, 1, false, 128, false, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 256: return launch_tc<256, false, 1, false, 128, false, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// MXFP4 (sgx == sgw == nullptr) and NVFP4: packed E2M1 operands, K / 2 bytes per row
+cudaError_t launch_fp4_tc(const uint8_t* Xq, const uint8_t* xs, const float* sgx, const uint8_t* Wq,
+                          const uint8_t* ws_sf, const float* sgw, uint16_t* Y, int64_t M, int64_t N, int64_t K,
+                          bool nv, const TcPlan& plan, void* ws, int* err, int num_sms, cudaStream_t st) {
+  CUtensorMap tx, tw, ty;
+  if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K / 2, M, K / 2, 128, plan.bn))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, K / 2, N, K / 2, 128, 128))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, N * 2, kTileN, 16, false))
+    return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.sfa = ws_sf;
+  a.sfb = xs;
+  a.sx = sgx;
+  a.sw = sgw;
+  a.Y = Y;
+  a.err = err;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  return nv ? launch_fp4_bn<kNvF4>(tx, tw, ty, a, plan, ws, num_sms, st)
+            : launch_fp4_bn<kMxF4>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,

@@ -12,9 +12,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (ACT_NONE, OP_MXFP8_GEMM, OP_QUANT_W_FP8, OP_W4A8_GEMM, OP_W4A16_GEMM, OP_W8A8_BLOCK_GEMM,
-               OP_W8A8_GEMM, PATH_AUTO, qlin_mx_scale_bytes, qlin_mxfp8_gemm, qlin_pack_w4, qlin_quant_mxfp8,
-               qlin_w4a8_gemm,
+from . import (ACT_NONE, OP_MXFP4_GEMM, OP_MXFP8_GEMM, OP_NVFP4_GEMM, OP_QUANT_W_FP8, OP_W4A8_GEMM, OP_W4A16_GEMM,
+               OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_mx_scale_bytes, qlin_mxfp4_gemm, qlin_mxfp8_gemm,
+               qlin_nvfp4_gemm, qlin_nvfp4_scale_bytes, qlin_nvfp4_tensor_scale, qlin_pack_w4, qlin_quant_mxfp4,
+               qlin_quant_mxfp8, qlin_quant_nvfp4, qlin_w4a8_gemm,
                qlin_quant_act_fp8, qlin_quant_act_fp8_blocks, qlin_quant_w_fp8, qlin_quant_w_fp8_blocks,
                qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w4a16_gemm_fused, qlin_w8a8_fp8_block_gemm,
                qlin_w8a8_fp8_gemm_ex, qlin_w8a8_fp8_gemm_fused, qlin_workspace_size)
@@ -218,3 +219,85 @@ class MXFP8Linear:
     def __call__(self, X_bf16, Y=None, stream=None):
         Xq, xs = self.quant_act(X_bf16, stream=stream)
         return self.gemm(Xq, xs, Y, stream)
+
+
+class MXFP4Linear:
+    """MXFP4 W4A4: E2M1 weights and activations (two per byte) with E8M0 scales
+    per 32 columns, both block scales applied by the tensor cores."""
+
+    def __init__(self, W_bf16: torch.Tensor, stream=None):
+        N, K = W_bf16.shape
+        self.N, self.K = N, K
+        dev = W_bf16.device
+        self.Wq = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+        self.ws_sf = torch.empty(qlin_mx_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+        qlin_quant_mxfp4(_as_u16(W_bf16.contiguous()), N, K, self.Wq, self.ws_sf, stream)
+        self.ws = Workspace(dev)
+
+    def quant_act(self, X_bf16: torch.Tensor, Xq=None, xs=None, stream=None):
+        M, K = X_bf16.shape
+        if Xq is None:
+            Xq = torch.empty((M, K // 2), dtype=torch.uint8, device=X_bf16.device)
+        if xs is None:
+            xs = torch.empty(max(qlin_mx_scale_bytes(M, K), 16), dtype=torch.uint8, device=X_bf16.device)
+        qlin_quant_mxfp4(_as_u16(X_bf16), M, K, Xq, xs, stream)
+        return Xq, xs
+
+    def gemm(self, Xq, xs, Y=None, stream=None):
+        M = Xq.shape[0]
+        if Y is None:
+            Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
+        buf, nb = self.ws.get(qlin_workspace_size(OP_MXFP4_GEMM, M, self.N, self.K))
+        qlin_mxfp4_gemm(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        return Y
+
+    def __call__(self, X_bf16, Y=None, stream=None):
+        Xq, xs = self.quant_act(X_bf16, stream=stream)
+        return self.gemm(Xq, xs, Y, stream)
+
+
+class NVFP4Linear:
+    """NVFP4 W4A4: E2M1 weights and activations with E4M3 scales per 16 columns
+    and one FP32 scale per tensor; the block scales are applied by the tensor
+    cores, the two tensor scales in the epilogue.  The activations' tensor scale
+    is computed on the device for every call (an amax reduction before the
+    quantiser)."""
+
+    def __init__(self, W_bf16: torch.Tensor, stream=None):
+        N, K = W_bf16.shape
+        self.N, self.K = N, K
+        dev = W_bf16.device
+        W = _as_u16(W_bf16.contiguous())
+        self.sgw = torch.empty(4, dtype=torch.float32, device=dev)
+        qlin_nvfp4_tensor_scale(W, N * K, self.sgw, stream)
+        self.Wq = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+        self.ws_sf = torch.empty(qlin_nvfp4_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+        qlin_quant_nvfp4(W, N, K, self.sgw, self.Wq, self.ws_sf, stream)
+        self.ws = Workspace(dev)
+
+    def quant_act(self, X_bf16: torch.Tensor, Xq=None, xs=None, sgx=None, stream=None):
+        M, K = X_bf16.shape
+        dev = X_bf16.device
+        if Xq is None:
+            Xq = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+        if xs is None:
+            xs = torch.empty(max(qlin_nvfp4_scale_bytes(M, K), 16), dtype=torch.uint8, device=dev)
+        if sgx is None:
+            sgx = torch.empty(4, dtype=torch.float32, device=dev)
+        X = _as_u16(X_bf16)
+        qlin_nvfp4_tensor_scale(X, M * K, sgx, stream)
+        qlin_quant_nvfp4(X, M, K, sgx, Xq, xs, stream)
+        return Xq, xs, sgx
+
+    def gemm(self, Xq, xs, sgx, Y=None, stream=None):
+        M = Xq.shape[0]
+        if Y is None:
+            Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
+        buf, nb = self.ws.get(qlin_workspace_size(OP_NVFP4_GEMM, M, self.N, self.K))
+        qlin_nvfp4_gemm(Xq, xs, sgx, self.Wq, self.ws_sf, self.sgw, Y.view(torch.int16), M, self.N, self.K, buf, nb,
+                        stream)
+        return Y
+
+    def __call__(self, X_bf16, Y=None, stream=None):
+        Xq, xs, sgx = self.quant_act(X_bf16, stream=stream)
+        return self.gemm(Xq, xs, sgx, Y, stream)

@@ -126,3 +126,29 @@ def test_plan_query_rejects_what_the_call_rejects(lib):
     assert lib.qlin_plan_info(q.OP_W8A8_GEMM, 4 * 65535 + 1, 128, 4224, 128, q.PATH_GEMV, 152, info) == 2
     # G = 32 / 64 are tensor-core only when K % 256 != 0
     assert lib.qlin_plan_info(q.OP_W4A16_GEMM, 4, 128, 4224, 64, q.PATH_GEMV, 152, info) == 2
+
+
+def test_fp4_plans_and_size_queries_without_device(lib):
+    # FP4 K blocks are 256 columns (128 bytes): the plan of an E4M3 problem of K / 2 columns
+    for op, kern in ((q.OP_MXFP4_GEMM, q.KERNEL_MXFP4_TC), (q.OP_NVFP4_GEMM, q.KERNEL_NVFP4_TC)):
+        p = q.qlin_plan_info(op, 2048, 28672, 4096, 128, q.PATH_AUTO, 152)
+        assert p["kernel"] == kern and p["tokens_per_tile"] == 256 and p["splits"] == 1
+        p8 = q.qlin_plan_info(q.OP_MXFP8_GEMM, 40, 512, 14336, 128, q.PATH_AUTO, 152)
+        p4 = q.qlin_plan_info(op, 40, 512, 28672, 128, q.PATH_AUTO, 152)
+        assert (p4["tokens_per_tile"], p4["splits"], p4["ws_bytes"]) == (p8["tokens_per_tile"], p8["splits"],
+                                                                          p8["ws_bytes"])
+        assert q.qlin_plan_info(op, 1, 512, 1024, 128, q.PATH_AUTO, 152)["tokens_per_tile"] == 32
+    info = (ctypes.c_int64 * 8)()
+    assert lib.qlin_plan_info(q.OP_MXFP4_GEMM, 4, 128, 384, 128, 0, 152, info) == 2      # K % 256
+    assert lib.qlin_plan_info(q.OP_NVFP4_GEMM, 4, 128, 384, 128, 0, 152, info) == 2
+    # scale bytes: MXFP4 shares the MXFP8 atoms (K / 32 scales per row), NVFP4 K / 16 per row
+    assert q.qlin_mx_scale_bytes(200, 512) == 256 * 512 // 32
+    assert q.qlin_nvfp4_scale_bytes(200, 512) == 256 * 512 // 16
+    b = ctypes.c_size_t()
+    assert lib.qlin_nvfp4_scale_bytes(1, 384, ctypes.byref(b)) == 2
+    # argument checks before any device work
+    assert lib.qlin_quant_mxfp4(16, 1, 384, 16, 16, None) == 2
+    assert lib.qlin_quant_nvfp4(16, 1, 256, None, 16, 16, None) == 1
+    assert lib.qlin_nvfp4_tensor_scale(16, 12, 16, None) == 2
+    assert lib.qlin_mxfp4_gemm(16, 16, 16, 16, 16, 1, 128, 384, None, 0, None) == 2
+    assert lib.qlin_nvfp4_gemm(16, 16, None, 16, 16, 16, 16, 1, 128, 256, None, 0, None) == 1
