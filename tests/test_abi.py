@@ -133,11 +133,16 @@ def test_fp4_plans_and_size_queries_without_device(lib):
     for op, kern in ((q.OP_MXFP4_GEMM, q.KERNEL_MXFP4_TC), (q.OP_NVFP4_GEMM, q.KERNEL_NVFP4_TC)):
         p = q.qlin_plan_info(op, 2048, 28672, 4096, 128, q.PATH_AUTO, 152)
         assert p["kernel"] == kern and p["tokens_per_tile"] == 256 and p["splits"] == 1
-        p8 = q.qlin_plan_info(q.OP_MXFP8_GEMM, 40, 512, 14336, 128, q.PATH_AUTO, 152)
-        p4 = q.qlin_plan_info(op, 40, 512, 28672, 128, q.PATH_AUTO, 152)
+        p8 = q.qlin_plan_info(q.OP_MXFP8_GEMM, 8, 4096, 7168, 128, q.PATH_AUTO, 152)
+        p4 = q.qlin_plan_info(op, 8, 4096, 14336, 128, q.PATH_AUTO, 152)
         assert (p4["tokens_per_tile"], p4["splits"], p4["ws_bytes"]) == (p8["tokens_per_tile"], p8["splits"],
                                                                           p8["ws_bytes"])
+        assert p4["tokens_per_tile"] == 32 and p4["splits"] > 1
         assert q.qlin_plan_info(op, 1, 512, 1024, 128, q.PATH_AUTO, 152)["tokens_per_tile"] == 32
+        # no 64-token FP4 tiles: from 33 tokens the tile is 128 or 256, and a 32-token tile is one token block
+        for M in (33, 40, 64, 65, 100, 300, 2048):
+            for N, K in ((512, 1024), (512, 28672), (4096, 4096), (14336, 8192)):
+                assert q.qlin_plan_info(op, M, N, K, 128, q.PATH_AUTO, 152)["tokens_per_tile"] in (128, 256)
     info = (ctypes.c_int64 * 8)()
     assert lib.qlin_plan_info(q.OP_MXFP4_GEMM, 4, 128, 384, 128, 0, 152, info) == 2      # K % 256
     assert lib.qlin_plan_info(q.OP_NVFP4_GEMM, 4, 128, 384, 128, 0, 152, info) == 2
