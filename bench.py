@@ -378,14 +378,17 @@ def measure_prefill(peaks, l2):
 
     import precision_quantized_linear_gb300 as q
     from precision_quantized_linear_gb300 import synthetic as syn
-    from precision_quantized_linear_gb300.layers import MXFP8Linear, W8A8Linear
+    from precision_quantized_linear_gb300.layers import MXFP4Linear, MXFP8Linear, NVFP4Linear, W8A8Linear
 
     p8 = 2.0 * peaks["bf16_tflops_sustained"]
+    p4 = 6.0 * peaks["bf16_tflops_sustained"]   # nominal dense FP4 / BF16 = 13.5 / 2.25
     rows, mx_rows = [], []
+    f4_rows = {"mxfp4": [], "nvfp4": []}
     for K, N in [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]:
         Wd = torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda()
         lin = W8A8Linear(Wd)
         linmx = MXFP8Linear(Wd)
+        lin4 = {"mxfp4": MXFP4Linear(Wd), "nvfp4": NVFP4Linear(Wd)}
         del Wd
         nrot = rotation(N * K, l2)
         sets = [lin.Wq] + [lin.Wq.clone() for _ in range(nrot - 1)]
@@ -418,9 +421,36 @@ def measure_prefill(peaks, l2):
             mx_rows.append({"K": K, "N": N, "M": M, "us": round(usm, 2),
                             "TFLOPS": round(flops / (usm * 1e-6) / 1e12, 1), "frac": round(t_roof / usm, 3),
                             "quant_us": round(qusm, 2)})
+            # FP4 (E2M1 with hardware block scaling): MXFP4 (kind::mxf4), NVFP4 (kind::mxf4nvf4)
+            for fmt, l4 in lin4.items():
+                ops = l4.quant_act(X)
+                op = q.OP_MXFP4_GEMM if fmt == "mxfp4" else q.OP_NVFP4_GEMM
+                nb4 = q.qlin_workspace_size(op, M, N, K)
+                ws4 = torch.zeros(max(nb4, 256), dtype=torch.uint8, device="cuda")
+                wsets = [(l4.Wq, l4.ws_sf)] + [(l4.Wq.clone(), l4.ws_sf.clone()) for _ in range(nrot - 1)]
+                if fmt == "mxfp4":
+                    calls = [lambda st, wq=wq, wsf=wsf: q.qlin_mxfp4_gemm(ops[0], ops[1], wq, wsf, Y, M, N, K, ws4,
+                                                                         ws4.numel(), st) for (wq, wsf) in wsets]
+                    qcall = [lambda st: q.qlin_quant_mxfp4(X, M, K, ops[0], ops[1], st)]
+                    sf_bytes = (M + N) * K // 32
+                else:
+                    calls = [lambda st, wq=wq, wsf=wsf: q.qlin_nvfp4_gemm(ops[0], ops[1], ops[2], wq, wsf, l4.sgw, Y, M,
+                                                                         N, K, ws4, ws4.numel(), st)
+                             for (wq, wsf) in wsets]
+                    qcall = [lambda st: (q.qlin_nvfp4_tensor_scale(X, M * K, ops[2], st),
+                                         q.qlin_quant_nvfp4(X, M, K, ops[2], ops[0], ops[1], st))]
+                    sf_bytes = (M + N) * K // 16
+                us4 = time_launches(calls)
+                qus4 = time_launches(qcall)
+                alg4 = (M + N) * K // 2 + sf_bytes + 2 * M * N
+                t_roof = max(flops / (p4 * 1e12), alg4 / (peaks["hbm_gbs"] * 1e9)) * 1e6
+                f4_rows[fmt].append({"K": K, "N": N, "M": M, "us": round(us4, 2),
+                                     "TFLOPS": round(flops / (us4 * 1e-6) / 1e12, 1), "frac": round(t_roof / us4, 3),
+                                     "quant_us": round(qus4, 2)})
+                del ops, ws4, wsets, calls, qcall
             assert q.qlin_get_device_error() == 0
             del X, Y, Xq, sx, ws, Xmq, xms, wsm
-        del lin, sets, linmx, mxsets
+        del lin, sets, linmx, mxsets, lin4
         torch.cuda.empty_cache()
 
     def total(rs):
@@ -429,12 +459,26 @@ def measure_prefill(peaks, l2):
         return round(f / (t * 1e-6) / 1e12, 1), round(f / (t * 1e-6) / 1e12 / p8, 3)
     tf, fr = total(rows)
     tfm, frm = total(mx_rows)
+    f4 = {}
+    for fmt, rs in f4_rows.items():
+        f = sum(2 * r["M"] * r["N"] * r["K"] for r in rs)
+        t = sum(r["us"] for r in rs)
+        f4[fmt] = {"TFLOPS": round(f / (t * 1e-6) / 1e12, 1), "frac": round(f / (t * 1e-6) / 1e12 / p4, 3),
+                   "cases": rs}
+    f4["mxfp4"]["workload"] = ("MXFP4 (E2M1, E8M0 scale per 32 columns, hardware block scaling, tcgen05 kind::mxf4) "
+                               "on the same shapes and M")
+    f4["nvfp4"]["workload"] = ("NVFP4 (E2M1, E4M3 scale per 16 columns + FP32 tensor scales, tcgen05 "
+                               "kind::mxf4nvf4) on the same shapes and M; quant_us includes the tensor-scale reduction")
+    for v in f4.values():
+        v["peak_tflops"] = round(p4, 1)
+        v["peak_source"] = "measured bf16 sustained x 6 (nominal dense FP4/BF16 ratio)"
     return {"workload": "W8A8 FP8 prefill M=2048/8192 on the Llama-3-8B shapes (tcgen05 kind::f8f6f4)",
             "peak_tflops": round(p8, 1), "peak_source": "measured bf16 sustained x 2 (nominal FP8/BF16 ratio)",
             "TFLOPS": tf, "frac": fr, "cases": rows,
             "mxfp8": {"workload": "MXFP8 (E8M0 scale per 32 columns, hardware block scaling, tcgen05 "
                                   "kind::mxf8f6f4) on the same shapes and M", "TFLOPS": tfm, "frac": frm,
-                      "cases": mx_rows}}
+                      "cases": mx_rows},
+            "mxfp4": f4["mxfp4"], "nvfp4": f4["nvfp4"]}
 
 
 def measure_crossover(peaks, l2):
