@@ -94,9 +94,14 @@ struct TcCfg {
   // two 128-row scale blocks) its B operand, so the promotion factor
   // sx[kb][m] * sw[n / 128][kb] is one scalar per thread and 128 columns.
   static constexpr bool kTokM = BS && BN == 128;
+  // Block-scaled formats with 256-token tiles have a single accumulator: the
+  // epilogue drains it into registers (BF16 pairs) and hands it back before
+  // writing, so that the next unit's MMAs overlap the stores
+  static constexpr bool kEarly = MX && BN == 256;
   // epilogue warps: four (one per TMEM lane quadrant); with block scaling and
-  // at least 32 tokens, eight, two per quadrant, each taking half the columns
-  static constexpr int kEpiWarps = (BS && BN >= 32) ? 8 : 4;
+  // at least 32 tokens, or the early drain, eight, two per quadrant, each
+  // taking half the columns
+  static constexpr int kEpiWarps = ((BS && BN >= 32) || kEarly) ? 8 : 4;
   static constexpr int kEpiHalves = kEpiWarps / 4;
   static constexpr int kEpiBox = 16 * kTileN * 2;
   static constexpr int kEpiBoxes = kTokM ? 0 : 2 * kEpiHalves;  // token-major writes rows straight to Y
@@ -1217,6 +1222,66 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
           named_bar(1, kAll);
         }
         continue;
+      } else if constexpr (C::kEarly) {
+        // ---- single 256-token accumulator (block-scaled formats, never split
+        // along K: see the planners): warp (quadrant, half) owns TMEM lanes
+        // quad * 32.. and tokens [128 half, 128 half + 128); it reads all 128
+        // columns as BF16 pairs (64 registers), hands the accumulator back,
+        // then writes them through the staging boxes
+        const Unit un = unit_of(a, u, KB);
+        const int half = t >> 7, th = t & 127;
+        const int cbase = half * 128;
+        const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
+        const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
+        const bool have =
+            __all_sync(0xffffffffu, mbar_wait(&acc_full[0], ua & 1, kWaitLimitNs, &s_abort));
+        if (!have) {
+          set_error(a.err, QLIN_ERR_TIMEOUT);
+          s_abort = 1;
+        }
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + cbase + (static_cast<uint32_t>(quad * 32) << 16);
+        uint32_t pk[64];  // BF16 pairs: tokens cbase + 2i (low half), + 1
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t v[2][16];
+          if (have) {
+            tmem_ld16(tmem_d + c0, v[0]);
+            tmem_ld16(tmem_d + c0 + 16, v[1]);
+            tmem_ld_wait();
+            reg_fence16(v[0]);
+            reg_fence16(v[1]);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = have ? __uint_as_float(v[i >> 3][(2 * i) & 15]) * s_nv : 0.0f;
+            const float x1 = have ? __uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * s_nv : 0.0f;
+            pk[c0 / 2 + i] = bf16x2_bits(__floats2bfloat162_rn(x0, x1));  // x0 in the low half
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[0]);  // the next unit's MMAs may start
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+          const int64_t m0 = mbase + cbase + c0;
+          if (m0 < a.M) {  // the same for the 128 threads of this half: they skip the barriers together
+            uint16_t* box = reinterpret_cast<uint16_t*>(epi_box + (half * 2 + (epi_n & 1)) * C::kEpiBox);
+            if (th == 0) bulk_wait_read<1>();
+            named_bar(2 + half, 128);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t w = pk[(c0 + i) >> 1];
+              box[i * kTileN + quad * 32 + lane] =
+                  m0 + i < a.M ? static_cast<uint16_t>((i & 1) ? (w >> 16) : (w & 0xFFFFu)) : uint16_t(0);
+            }
+            fence_proxy_async_smem();
+            named_bar(2 + half, 128);
+            if (th == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(m0));
+            ++epi_n;
+          }
+        }
+        continue;
       }
       const Unit un = unit_of(a, u, KB);
       const int acc = ua % C::kAccBufs;
@@ -1509,6 +1574,7 @@ TcPlan plan_w4a8_tc(int64_t M, int64_t N, int64_t K, int num_sms) { return plan_
 // keep one accumulator: two would leave no TMEM for the scale-factor ring.
 TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   TcPlan p = plan_tc(M, N, K, num_sms, 128, false, 256);
+  if (p.bn == 256 && p.split.splits > 1) p = plan_tc(M, N, K, num_sms, 128, false, 128);  // 256: never split
   if (p.bn < 32) p.bn = 32;  // the same single token block for M <= 16
   return p;
 }
@@ -1518,7 +1584,9 @@ TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
 // to 32 tokens, 128- or 256-token tiles beyond.
 TcPlan plan_fp4_tc(int64_t M, int64_t N, int64_t K, int num_sms) {
   if (M <= 32) return plan_mxfp8_tc(M, N, K / 2, num_sms);
-  return plan_tc(M, N, K / 2, num_sms, 128, false, 256, kTileN, true, 128);
+  TcPlan p = plan_tc(M, N, K / 2, num_sms, 128, false, 256, kTileN, true, 128);
+  if (p.bn == 256 && p.split.splits > 1) p = plan_tc(M, N, K / 2, num_sms, 128, false, 128, kTileN, true, 128);
+  return p;
 }
 // Block scaling keeps the running sums of a 128-token tile in registers.  With
 // 128-token tiles the weight tile is 256 rows (two scale blocks) when N allows
@@ -1535,6 +1603,7 @@ template <int BN, bool W4, int KPS, bool BS = false, int WN = 128, bool EPI = fa
 static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, TcArgs args,
                              const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   using C = TcCfg<BN, W4, KPS, BS, WN, MX, A8>;
+  if (C::kEarly && plan.split.splits != 1) return cudaErrorInvalidValue;  // its epilogue writes Y directly
   cudaError_t e = set_smem_once(tc_gemm_kernel<BN, W4, KPS, BS, WN, EPI, MX, A8>, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   args.counters = static_cast<uint32_t*>(ws);
