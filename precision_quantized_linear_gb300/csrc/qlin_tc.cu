@@ -115,10 +115,12 @@ struct TcCfg {
   // block-scaled formats with 256-token tiles keep one (the scale-factor ring takes the rest of TMEM)
   static constexpr int kAccBufs = BS ? (512 / kAccCols < 4 ? 512 / kAccCols : 4) : A8 ? 4 : (MX && BN == 256) ? 1 : 2;
   static constexpr int kAColBase = kAccBufs * BN;               // first TMEM column of the A slots
-  // Block scale factors in TMEM: a ring of kSfSlots K blocks, four columns
-  // per atom (see mma_mx8, mma_mxf4): kSfK atoms of weight scales and
-  // kSfK x kSfbAtoms of token scales per slot
-  static constexpr int kSfSlots = MX ? 4 : 0;
+  // Block scale factors in TMEM: one slot per pipeline stage (the scale warp
+  // fills slot s once stage s has landed, and the producer refills stage s
+  // only after the MMAs that read slot s are done), four columns per atom (see
+  // mma_mx8, mma_mxf4): kSfK atoms of weight scales and kSfK x kSfbAtoms of
+  // token scales per slot
+  static constexpr int kSfSlots = MX ? kStages : 0;
   static constexpr int kSfaCol = kAccBufs * BN;
   static constexpr int kSfbCol = kSfaCol + 4 * kSfK * kSfSlots;
   static constexpr int kTmemNeed =
@@ -126,7 +128,8 @@ struct TcCfg {
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                  : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kDqWarps = W4 ? 8 : 0;
-  static constexpr int kEpiWarp0 = 2 + kDqWarps;
+  static constexpr int kSfWarps = MX ? 1 : 0;  // block-scaled formats: the warp that copies scales into TMEM
+  static constexpr int kEpiWarp0 = 2 + kDqWarps + kSfWarps;
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
   // Register cap per thread.  Each of the SM's four sub-partitions holds 16 K
   // registers and takes every fourth warp, so the cap is set by the
@@ -253,7 +256,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
   uint64_t* a_empty = a_full + C::kAStages;    // [kAStages] MMA -> dequant
   uint64_t* acc_full = a_empty + C::kAStages;  // [kAccBufs] MMA -> epilogue
   uint64_t* acc_empty = acc_full + C::kAccBufs;  // [kAccBufs] epilogue -> MMA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + C::kAccBufs);
+  uint64_t* sf_full = acc_empty + C::kAccBufs;   // [kSfSlots] scale warp -> MMA (scales of stage s in TMEM)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + C::kSfSlots);
   __shared__ int s_last;
   __shared__ volatile int s_abort;  // set by the first role whose wait gave up
 
@@ -273,6 +277,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], C::kEpiWarps);
     }
+    for (int i = 0; i < C::kSfSlots; ++i) mbar_init(&sf_full[i], 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -415,9 +420,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         s_abort = 1;
       }
     } else if (lane == 0 && MX != kMxNone) {
-      // Block-scaled formats: per K block, copy its scale atoms into the next
-      // TMEM slot of the ring (in issue order with the MMAs), then four MMAs
-      // of 32 bytes of K.  MXFP8: k-step kk takes byte kk of each scale word;
+      // Block-scaled formats: per K block, once the scale warp has copied its
+      // scale atoms into the stage's TMEM slot, four MMAs of 32 bytes of K.  MXFP8: k-step kk takes byte kk of each scale word;
       // MXFP4 (64 columns per step): atom kk / 2, bytes 2 (kk % 2) and +1;
       // NVFP4 (64 columns): atom kk, bytes 0..3
       int it = 0, ua = 0;
@@ -434,23 +438,15 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         const uint32_t tok_col = static_cast<uint32_t>((un.mb * BN) % 128) / 32;  // this block's tokens in the atom
         for (int j = 0; j < un.nkb && ok; ++j, ++it) {
           const int s = it % C::kStages;
-          if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
+          // the stage has landed and the scale warp's copies of its scales are done
+          if (!mbar_wait(&sf_full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t slot = static_cast<uint32_t>(C::kSfSlots ? it % C::kSfSlots : 0);
-          const uint32_t t_sfa = tmem_base + C::kSfaCol + slot * 4 * C::kSfK;
-          const uint32_t t_sfb = tmem_base + C::kSfbCol + slot * 4 * C::kSfK * C::kSfbAtoms;
+          const uint32_t t_sfa = tmem_base + C::kSfaCol + s * 4 * C::kSfK;
+          const uint32_t t_sfb = tmem_base + C::kSfbCol + s * 4 * C::kSfK * C::kSfbAtoms;
           const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
-#pragma unroll
-          for (int c = 0; c < C::kSfK; ++c) {
-            tc_cp_atom(t_sfa + 4 * c, sdesc_atom(st_u32 + C::kSfOff + 512 * c));
-#pragma unroll
-            for (int t = 0; t < C::kSfbAtoms; ++t)  // K atom c, tokens 128 t ..: columns 4 (c kSfbAtoms + t) ..
-              tc_cp_atom(t_sfb + 4 * (c * C::kSfbAtoms + t),
-                         sdesc_atom(st_u32 + C::kSfOff + 512 * C::kSfK * (1 + t) + 512 * c));
-          }
           const uint32_t a_addr = st_u32 + C::kXBlk, b_addr = st_u32;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -621,6 +617,44 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
       }
     }
   } else if (warp < C::kEpiWarp0) {
+    if constexpr (MX != kMxNone) {
+      // ------------------------------------------------------------ scale warp (block-scaled formats)
+      // Per K block: wait for the stage, copy its scale atoms from shared
+      // memory into the stage's TMEM slot (tcgen05.cp), and commit the copies
+      // to sf_full[s].  Slot s is free again when the producer refills stage
+      // s: that happens only after the MMAs that read the slot are done.
+      if (lane == 0) {
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+          const Unit un = unit_of(a, u, KB);
+          for (int j = 0; j < un.nkb; ++j, ++it) {
+            const int s = it % C::kStages;
+            if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t t_sfa = tmem_base + C::kSfaCol + s * 4 * C::kSfK;
+            const uint32_t t_sfb = tmem_base + C::kSfbCol + s * 4 * C::kSfK * C::kSfbAtoms;
+            const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
+#pragma unroll
+            for (int c = 0; c < C::kSfK; ++c) {
+              tc_cp_atom(t_sfa + 4 * c, sdesc_atom(st_u32 + C::kSfOff + 512 * c));
+#pragma unroll
+              for (int t = 0; t < C::kSfbAtoms; ++t)  // K atom c, tokens 128 t ..: columns 4 (c kSfbAtoms + t) ..
+                tc_cp_atom(t_sfb + 4 * (c * C::kSfbAtoms + t),
+                           sdesc_atom(st_u32 + C::kSfOff + 512 * C::kSfK * (1 + t) + 512 * c));
+            }
+            mma_commit(&sf_full[s]);  // arrives when the copies are done
+          }
+        }
+        if (!ok) {
+          set_error(a.err, QLIN_ERR_TIMEOUT);
+          s_abort = 1;
+        }
+      }
+    }
     // ---------------------------------------------------------------- dequantisation (W4A8)
     if constexpr (W4 && A8) {
       // The two groups of four warps take the K blocks (128 columns = one
