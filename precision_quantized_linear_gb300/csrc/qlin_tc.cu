@@ -206,11 +206,13 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 zoff, __nv_
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Work unit u -> (n tile, token block, K range).  When the weights fit in L2
-// the weight tile varies fastest (the weights stay resident and each
-// activation block is streamed once); otherwise tiles are taken in groups of
-// kRasterN weight tiles x every token block, token block fastest, so that the
-// activations stay resident and each weight tile is streamed once.
+// Work unit u -> (n tile, token block, K range).  The larger operand is
+// streamed once and the smaller kept resident: when the activations are the
+// smaller, tiles are taken in groups of kRasterN weight tiles x every token
+// block, token block fastest, so that each weight tile is read from HBM once
+// (its token blocks run at the same time); otherwise the weight tile varies
+// fastest.  Weights that would fit in L2 are not assumed to stay there: the
+// BF16 output streams through L2 as well (at 2048 tokens x 28672 rows, 117 MB).
 constexpr int kRasterN = 16;
 struct Unit {
   int nt, mb, split, kb0, nkb;
@@ -1651,7 +1653,7 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
     const double l2_half = 63.0 * 1024 * 1024;  // half of the 126 MB L2
     const double wb = static_cast<double>(args.N) * static_cast<double>(args.K) * (W4 ? 0.51953125 : C::kF4 ? 0.5 : 1.0);
     const double xb = static_cast<double>(args.M) * static_cast<double>(args.K) * ((W4 && !A8) ? 2.0 : C::kF4 ? 0.5 : 1.0);
-    args.mb_fast = (wb > l2_half && xb < wb) ? 1 : 0;
+    args.mb_fast = xb < wb ? 1 : 0;
     args.x_keep = xb <= l2_half / 2 ? 1 : 0;
   }
   const int grid = args.units < num_sms ? args.units : num_sms;
