@@ -894,7 +894,8 @@ def run_case(args):
 
     import precision_quantized_linear_gb300 as q
     from precision_quantized_linear_gb300 import synthetic as syn
-    from precision_quantized_linear_gb300.layers import MXFP8Linear, W4A8Linear, W4A16Linear, W8A8BlockLinear, W8A8Linear
+    from precision_quantized_linear_gb300.layers import (MXFP4Linear, MXFP8Linear, NVFP4Linear, W4A8Linear, W4A16Linear,
+                                                          W8A8BlockLinear, W8A8Linear)
 
     torch.cuda.set_device(0)
     q.build()
@@ -914,6 +915,14 @@ def run_case(args):
         lin = MXFP8Linear(W)
         Xq, xs = lin.quant_act(X)
         fn = lambda: lin.gemm(Xq, xs)  # noqa: E731
+    elif args.case == "mxfp4":
+        lin = MXFP4Linear(W)
+        Xq, xs = lin.quant_act(X)
+        fn = lambda: lin.gemm(Xq, xs)  # noqa: E731
+    elif args.case == "nvfp4":
+        lin = NVFP4Linear(W)
+        Xq, xs, sgx = lin.quant_act(X)
+        fn = lambda: lin.gemm(Xq, xs, sgx)  # noqa: E731
     elif args.case == "w8a8b":
         lin = W8A8BlockLinear(W)
         Xq, sx = lin.quant_act(X)
@@ -946,7 +955,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweeps", action="store_true", help="decode line only (no prefill / crossover objects)")
-    ap.add_argument("--case", default=None, choices=["w4a16", "w8a8", "w8a8b", "w4a8", "mxfp8"])
+    ap.add_argument("--case", default=None, choices=["w4a16", "w8a8", "w8a8b", "w4a8", "mxfp8", "mxfp4",
+                                                          "nvfp4"])
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--N", type=int, default=28672)
     ap.add_argument("--K", type=int, default=4096)
