@@ -279,11 +279,49 @@ __global__ void __launch_bounds__(THREADS) quant_act_fp8_kernel(const uint16_t* 
   for (int64_t i = threadIdx.x; i < n8; i += THREADS) out[i] = quant8(row[i], s);
 }
 
+// The same with the row held in registers: each thread loads its ITEMS
+// 16-byte pieces of the row at once (K <= THREADS * 8 * ITEMS), so a CTA has
+// the whole row in flight, and quantises from registers after the block
+// reduction.  Small CTAs let an SM keep many rows in flight.
+template <int THREADS, int ITEMS>
+__global__ void __launch_bounds__(THREADS) quant_act_fp8_reg_kernel(const uint16_t* __restrict__ X, int64_t K,
+                                                                    uint8_t* __restrict__ Xq, float* __restrict__ sx) {
+  __shared__ float red[32];
+  const int64_t m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(X + m * K);
+  const int n8 = static_cast<int>(K / 8);
+  uint4 v[ITEMS];
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j) {
+    const int i = threadIdx.x + j * THREADS;
+    v[j] = i < n8 ? row[i] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float a = 0.0f;
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j) a = amax8(v[j], a);
+  a = block_max<THREADS>(a, red);
+  const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+  if (threadIdx.x == 0) sx[m] = s;
+  uint2* out = reinterpret_cast<uint2*>(Xq + m * K);
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j) {
+    const int i = threadIdx.x + j * THREADS;
+    if (i < n8) out[i] = quant8(v[j], s);
+  }
+}
+
 cudaError_t launch_quant_act_fp8(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* sx, cudaStream_t st) {
-  if (K >= 4096)
-    quant_act_fp8_kernel<512><<<static_cast<unsigned>(M), 512, 0, st>>>(X, K, Xq, sx);
+  const unsigned g = static_cast<unsigned>(M);
+  if (K <= 4096)
+    quant_act_fp8_reg_kernel<128, 4><<<g, 128, 0, st>>>(X, K, Xq, sx);
+  else if (K <= 8192)
+    quant_act_fp8_reg_kernel<128, 8><<<g, 128, 0, st>>>(X, K, Xq, sx);
+  else if (K <= 16384)
+    quant_act_fp8_reg_kernel<256, 8><<<g, 256, 0, st>>>(X, K, Xq, sx);
+  else if (K <= 32768)
+    quant_act_fp8_reg_kernel<512, 8><<<g, 512, 0, st>>>(X, K, Xq, sx);
   else
-    quant_act_fp8_kernel<128><<<static_cast<unsigned>(M), 128, 0, st>>>(X, K, Xq, sx);
+    quant_act_fp8_kernel<512><<<g, 512, 0, st>>>(X, K, Xq, sx);
   return cudaGetLastError();
 }
 
@@ -388,6 +426,11 @@ cudaError_t launch_quant_w_fp8_blocks(const uint16_t* W, int64_t N, int64_t K, u
 
 // ------------------------------------------------------------------ MXFP8
 
+// Items (a row's 128- or 256-column chunk) per warp in the MX / FP4
+// quantisers: a warp issues all of their loads before the arithmetic, so that
+// an SM keeps enough bytes in flight to stream at the HBM rate.
+constexpr int kMxItems = 4;
+
 // MX block scale of a 32-element block ([LP] S10, OCP Microscaling v1.0):
 // e = floor(log2 amax) - 8 (8: exponent of E4M3's largest normal), clamped to
 // [-127, 127]; -127 for an all-zero block.  Read from the exponent field: an
@@ -399,8 +442,8 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// One warp per (row r, 128 columns): lane l holds columns 4l .. 4l+3, a block
-// of 32 columns is a segment of 8 lanes.  Codes are E4M3(v * 2^-e) -- the
+// A warp per kMxItems consecutive (row r, 128 columns) items: lane l holds
+// columns 4l .. 4l+3, a block of 32 columns is a segment of 8 lanes.  Codes are E4M3(v * 2^-e) -- the
 // power-of-two scaling is exact, so this is v / 2^e rounded once, to nearest
 // even with saturation.  The four scale bytes of the 128 columns go to one
 // 32-bit word of the scale atom: row r of atom (r / 128, k / 128) holds its
@@ -410,35 +453,57 @@ __global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint16_t* __rest
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const int lane = threadIdx.x & 31;
   const int64_t nc = K / 128;
-  const int64_t rows = (R + 127) / 128 * 128;
-  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (item >= rows * nc) return;  // whole warps only
-  const int64_t r = item / nc, c = item % nc;
-  uint32_t e8 = 0;
-  if (r < R) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(X + r * K + c * 128 + 4 * lane);
-    const float v[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    amax = seg_max(amax, 8);
-    const int e = amax == 0.0f ? -127 : mx_exponent(amax);
-    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e in [-127, 119]
-    const uint32_t lo = e4m3x2(v[0] * inv, v[1] * inv), hi = e4m3x2(v[2] * inv, v[3] * inv);
-    *reinterpret_cast<uint32_t*>(codes + r * K + c * 128 + 4 * lane) = lo | (hi << 16);
-    e8 = static_cast<uint32_t>(e + 127);
+  const int64_t total = (R + 127) / 128 * 128 * nc;  // items: (row, 128 columns), padding rows included
+  const int64_t item0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kMxItems;
+  if (item0 >= total) return;  // whole warps only
+  // all of this warp's loads first, so that kMxItems of them are in flight
+  // item0 + u is row rr[u], chunk cc[u]: one division per warp, then a carry
+  int64_t rr[kMxItems], cc[kMxItems];
+  rr[0] = item0 / nc;
+  cc[0] = item0 - rr[0] * nc;
+#pragma unroll
+  for (int u = 1; u < kMxItems; ++u) {
+    const bool wrap = cc[u - 1] + 1 == nc;
+    cc[u] = wrap ? 0 : cc[u - 1] + 1;
+    rr[u] = wrap ? rr[u - 1] + 1 : rr[u - 1];
   }
-  // bytes kk = 0..3 of the word from lanes 0, 8, 16, 24
-  uint32_t word = (e8 & 0xFFu) << (8 * (lane >> 3));
-  word |= __shfl_xor_sync(0xffffffffu, word, 8);
-  word |= __shfl_xor_sync(0xffffffffu, word, 16);
-  if (lane == 0) {
-    uint8_t* atom = scales + ((r / 128) * nc + c) * 512;
-    *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+  uint2 raw[kMxItems];
+#pragma unroll
+  for (int u = 0; u < kMxItems; ++u) {
+    const int64_t item = item0 + u, r = rr[u], c = cc[u];
+    raw[u] = (item < total && r < R) ? *reinterpret_cast<const uint2*>(X + r * K + c * 128 + 4 * lane) : make_uint2(0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < kMxItems; ++u) {
+    const int64_t item = item0 + u;
+    if (item >= total) break;  // the same for the whole warp
+    const int64_t r = rr[u], c = cc[u];
+    uint32_t e8 = 0;
+    if (r < R) {
+      const float v[4] = {bf16_lo(raw[u].x), bf16_hi(raw[u].x), bf16_lo(raw[u].y), bf16_hi(raw[u].y)};
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      amax = seg_max(amax, 8);
+      const int e = amax == 0.0f ? -127 : mx_exponent(amax);
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e in [-127, 119]
+      const uint32_t lo = e4m3x2(v[0] * inv, v[1] * inv), hi = e4m3x2(v[2] * inv, v[3] * inv);
+      *reinterpret_cast<uint32_t*>(codes + r * K + c * 128 + 4 * lane) = lo | (hi << 16);
+      e8 = static_cast<uint32_t>(e + 127);
+    }
+    // bytes kk = 0..3 of the word from lanes 0, 8, 16, 24
+    uint32_t word = (e8 & 0xFFu) << (8 * (lane >> 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 8);
+    word |= __shfl_xor_sync(0xffffffffu, word, 16);
+    if (lane == 0) {
+      uint8_t* atom = scales + ((r / 128) * nc + c) * 512;
+      *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+    }
   }
 }
 
 cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t st) {
-  const int64_t warps = (R + 127) / 128 * 128 * (K / 128);
+  const int64_t items = (R + 127) / 128 * 128 * (K / 128);
+  const int64_t warps = (items + kMxItems - 1) / kMxItems;
   const int64_t blocks = (warps + 7) / 8;
   quant_mxfp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, R, K, codes, scales);
   return cudaGetLastError();
@@ -474,8 +539,8 @@ __device__ __forceinline__ void bf16x8(uint4 raw, float (&v)[8]) {
   v[7] = bf16_hi(raw.w);
 }
 
-// MXFP4 ([LP] S10, OCP Microscaling v1.0): one warp per (row r, 256 columns);
-// lane l holds columns 8l .. 8l+7, a block of 32 columns is a segment of four
+// MXFP4 ([LP] S10, OCP Microscaling v1.0): a warp per kMxItems consecutive
+// (row r, 256 columns) items; lane l holds columns 8l .. 8l+7, a block of 32 columns is a segment of four
 // lanes.  e = floor(log2 amax) - 2 (2: exponent of E2M1's largest normal,
 // 6 = 1.5 x 2^2), clamped to [-127, 127], -127 for an all-zero block; codes
 // E2M1(v * 2^-e) (the power-of-two scaling is exact).  The 256 columns fill
@@ -485,40 +550,62 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint16_t* __rest
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const int lane = threadIdx.x & 31;
   const int64_t nc = K / 256;
-  const int64_t rows = (R + 127) / 128 * 128;
-  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (item >= rows * nc) return;  // whole warps only
-  const int64_t r = item / nc, c = item % nc;
-  uint32_t e8 = 0;
-  if (r < R) {
-    float v[8];
-    bf16x8(*reinterpret_cast<const uint4*>(X + r * K + c * 256 + 8 * lane), v);
-    float amax = 0.0f;
+  const int64_t total = (R + 127) / 128 * 128 * nc;  // items: (row, 256 columns), padding rows included
+  const int64_t item0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kMxItems;
+  if (item0 >= total) return;  // whole warps only
+  // item0 + u is row rr[u], chunk cc[u]: one division per warp, then a carry
+  int64_t rr[kMxItems], cc[kMxItems];
+  rr[0] = item0 / nc;
+  cc[0] = item0 - rr[0] * nc;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = seg_max(amax, 4);
-    const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // 0: zero or below 2^-126
-    int e = eb == 0 ? -127 : eb - 127 - 2;
-    e = e < -127 ? -127 : e;
-    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e in [-127, 125]
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] *= inv;
-    *reinterpret_cast<uint32_t*>(codes + r * (K / 2) + c * 128 + 4 * lane) = e2m1x8(v);
-    e8 = static_cast<uint32_t>(e + 127);
+  for (int u = 1; u < kMxItems; ++u) {
+    const bool wrap = cc[u - 1] + 1 == nc;
+    cc[u] = wrap ? 0 : cc[u - 1] + 1;
+    rr[u] = wrap ? rr[u - 1] + 1 : rr[u - 1];
   }
-  uint32_t word = (e8 & 0xFFu) << (8 * ((lane >> 2) & 3));
-  word |= __shfl_xor_sync(0xffffffffu, word, 4);
-  word |= __shfl_xor_sync(0xffffffffu, word, 8);
-  if ((lane & 15) == 0) {
-    uint8_t* atom = scales + ((r / 128) * (K / 128) + 2 * c + (lane >> 4)) * 512;
-    *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+  uint4 raw[kMxItems];
+#pragma unroll
+  for (int u = 0; u < kMxItems; ++u) {
+    const int64_t item = item0 + u, r = rr[u], c = cc[u];
+    raw[u] = (item < total && r < R) ? *reinterpret_cast<const uint4*>(X + r * K + c * 256 + 8 * lane)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < kMxItems; ++u) {
+    const int64_t item = item0 + u;
+    if (item >= total) break;  // the same for the whole warp
+    const int64_t r = rr[u], c = cc[u];
+    uint32_t e8 = 0;
+    if (r < R) {
+      float v[8];
+      bf16x8(raw[u], v);
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      amax = seg_max(amax, 4);
+      const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // 0: zero or below 2^-126
+      int e = eb == 0 ? -127 : eb - 127 - 2;
+      e = e < -127 ? -127 : e;
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e in [-127, 125]
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] *= inv;
+      *reinterpret_cast<uint32_t*>(codes + r * (K / 2) + c * 128 + 4 * lane) = e2m1x8(v);
+      e8 = static_cast<uint32_t>(e + 127);
+    }
+    uint32_t word = (e8 & 0xFFu) << (8 * ((lane >> 2) & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    word |= __shfl_xor_sync(0xffffffffu, word, 8);
+    if ((lane & 15) == 0) {
+      uint8_t* atom = scales + ((r / 128) * (K / 128) + 2 * c + (lane >> 4)) * 512;
+      *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+    }
   }
 }
 
 cudaError_t launch_quant_mxfp4(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t st) {
-  const int64_t warps = (R + 127) / 128 * 128 * (K / 256);
-  const int64_t blocks = (warps + 7) / 8;
+  const int64_t items = (R + 127) / 128 * 128 * (K / 256);
+  const int64_t blocks = ((items + kMxItems - 1) / kMxItems + 7) / 8;
   quant_mxfp4_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, R, K, codes, scales);
   return cudaGetLastError();
 }
@@ -566,8 +653,8 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
-// NVFP4 ([LP] S10 names it; the vendor's two-level recipe): one warp per
-// (row r, 256 columns), lane l holds columns 8l .. 8l+7, a block of 16 columns
+// NVFP4 ([LP] S10 names it; the vendor's two-level recipe): a warp per
+// kMxItems consecutive (row r, 256 columns) items, lane l holds columns 8l .. 8l+7, a block of 16 columns
 // is a pair of lanes.  Block scale sb = E4M3(amax_b / (6 sg)) (RNE, saturating),
 // elements E2M1(v / (sb sg)); each step is one IEEE binary32 operation
 // (__fmul_rn / __fdiv_rn); a block whose scale is 0 stores code 0.  The 256
@@ -578,42 +665,64 @@ __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __rest
                                                           uint8_t* __restrict__ scales) {
   const int lane = threadIdx.x & 31;
   const int64_t nc = K / 256;
-  const int64_t rows = (R + 127) / 128 * 128;
-  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (item >= rows * nc) return;  // whole warps only
-  const int64_t r = item / nc, c = item % nc;
-  uint32_t sc = 0;
-  if (r < R) {
-    const float sg = __ldg(sgp);
-    float v[8];
-    bf16x8(*reinterpret_cast<const uint4*>(X + r * K + c * 256 + 8 * lane), v);
-    float amax = 0.0f;
+  const int64_t total = (R + 127) / 128 * 128 * nc;  // items: (row, 256 columns), padding rows included
+  const int64_t item0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kMxItems;
+  if (item0 >= total) return;  // whole warps only
+  // item0 + u is row rr[u], chunk cc[u]: one division per warp, then a carry
+  int64_t rr[kMxItems], cc[kMxItems];
+  rr[0] = item0 / nc;
+  cc[0] = item0 - rr[0] * nc;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = seg_max(amax, 2);
-    sc = e4m3x2(__fdiv_rn(amax, __fmul_rn(6.0f, sg)), 0.0f) & 0xFFu;
-    uint32_t q = 0;
-    if (sc != 0) {
-      const float den = __fmul_rn(e4m3_value(sc), sg);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(v[i], den);
-      q = e2m1x8(v);
-    }
-    *reinterpret_cast<uint32_t*>(codes + r * (K / 2) + c * 128 + 4 * lane) = q;
+  for (int u = 1; u < kMxItems; ++u) {
+    const bool wrap = cc[u - 1] + 1 == nc;
+    cc[u] = wrap ? 0 : cc[u - 1] + 1;
+    rr[u] = wrap ? rr[u - 1] + 1 : rr[u - 1];
   }
-  uint32_t word = sc << (8 * ((lane >> 1) & 3));
-  word |= __shfl_xor_sync(0xffffffffu, word, 2);
-  word |= __shfl_xor_sync(0xffffffffu, word, 4);
-  if ((lane & 7) == 0) {
-    uint8_t* atom = scales + ((r / 128) * (K / 64) + 4 * c + (lane >> 3)) * 512;
-    *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+  uint4 raw[kMxItems];
+#pragma unroll
+  for (int u = 0; u < kMxItems; ++u) {
+    const int64_t item = item0 + u, r = rr[u], c = cc[u];
+    raw[u] = (item < total && r < R) ? *reinterpret_cast<const uint4*>(X + r * K + c * 256 + 8 * lane)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const float sg = __ldg(sgp);
+#pragma unroll
+  for (int u = 0; u < kMxItems; ++u) {
+    const int64_t item = item0 + u;
+    if (item >= total) break;  // the same for the whole warp
+    const int64_t r = rr[u], c = cc[u];
+    uint32_t sc = 0;
+    if (r < R) {
+      float v[8];
+      bf16x8(raw[u], v);
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      amax = seg_max(amax, 2);
+      sc = e4m3x2(__fdiv_rn(amax, __fmul_rn(6.0f, sg)), 0.0f) & 0xFFu;
+      uint32_t qv = 0;
+      if (sc != 0) {
+        const float den = __fmul_rn(e4m3_value(sc), sg);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(v[i], den);
+        qv = e2m1x8(v);
+      }
+      *reinterpret_cast<uint32_t*>(codes + r * (K / 2) + c * 128 + 4 * lane) = qv;
+    }
+    uint32_t word = sc << (8 * ((lane >> 1) & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    if ((lane & 7) == 0) {
+      uint8_t* atom = scales + ((r / 128) * (K / 64) + 4 * c + (lane >> 3)) * 512;
+      *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
+    }
   }
 }
 
 cudaError_t launch_quant_nvfp4(const uint16_t* X, int64_t R, int64_t K, const float* sg, uint8_t* codes,
                                uint8_t* scales, cudaStream_t st) {
-  const int64_t warps = (R + 127) / 128 * 128 * (K / 256);
-  const int64_t blocks = (warps + 7) / 8;
+  const int64_t items = (R + 127) / 128 * 128 * (K / 256);
+  const int64_t blocks = ((items + kMxItems - 1) / kMxItems + 7) / 8;
   quant_nvfp4_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, R, K, sg, codes, scales);
   return cudaGetLastError();
 }
