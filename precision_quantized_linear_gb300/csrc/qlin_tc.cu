@@ -128,7 +128,10 @@ struct TcCfg {
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                  : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kDqWarps = W4 ? 8 : 0;
-  static constexpr int kSfWarps = MX ? 1 : 0;  // block-scaled formats: the warp that copies scales into TMEM
+  // block-scaled formats: the warps that copy scales into TMEM; NVFP4 (12
+  // atom copies per K block at 256 tokens) splits them over two, weight atoms
+  // on the first, token atoms on the second
+  static constexpr int kSfWarps = MX == kNvF4 ? 2 : MX ? 1 : 0;
   static constexpr int kEpiWarp0 = 2 + kDqWarps + kSfWarps;
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
   // Register cap per thread.  Each of the SM's four sub-partitions holds 16 K
@@ -279,7 +282,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], C::kEpiWarps);
     }
-    for (int i = 0; i < C::kSfSlots; ++i) mbar_init(&sf_full[i], 1);
+    for (int i = 0; i < C::kSfSlots; ++i) mbar_init(&sf_full[i], C::kSfWarps);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -620,10 +623,10 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
     }
   } else if (warp < C::kEpiWarp0) {
     if constexpr (MX != kMxNone) {
-      // ------------------------------------------------------------ scale warp (block-scaled formats)
+      // ------------------------------------------------------------ scale warps (block-scaled formats)
       // Per K block: wait for the stage, copy its scale atoms from shared
       // memory into the stage's TMEM slot (tcgen05.cp), and commit the copies
-      // to sf_full[s].  Slot s is free again when the producer refills stage
+      // to sf_full[s] (one arrival per scale warp).  Slot s is free again when the producer refills stage
       // s: that happens only after the MMAs that read the slot are done.
       if (lane == 0) {
         int it = 0;
@@ -640,15 +643,18 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
             const uint32_t t_sfa = tmem_base + C::kSfaCol + s * 4 * C::kSfK;
             const uint32_t t_sfb = tmem_base + C::kSfbCol + s * 4 * C::kSfK * C::kSfbAtoms;
             const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
+            const int sfw = warp - 2 - C::kDqWarps;  // which scale warp (0 .. kSfWarps - 1)
 #pragma unroll
             for (int c = 0; c < C::kSfK; ++c) {
-              tc_cp_atom(t_sfa + 4 * c, sdesc_atom(st_u32 + C::kSfOff + 512 * c));
+              if (C::kSfWarps == 1 || sfw == 0) tc_cp_atom(t_sfa + 4 * c, sdesc_atom(st_u32 + C::kSfOff + 512 * c));
+              if (C::kSfWarps == 1 || sfw == 1) {
 #pragma unroll
-              for (int t = 0; t < C::kSfbAtoms; ++t)  // K atom c, tokens 128 t ..: columns 4 (c kSfbAtoms + t) ..
-                tc_cp_atom(t_sfb + 4 * (c * C::kSfbAtoms + t),
-                           sdesc_atom(st_u32 + C::kSfOff + 512 * C::kSfK * (1 + t) + 512 * c));
+                for (int t = 0; t < C::kSfbAtoms; ++t)  // K atom c, tokens 128 t ..: columns 4 (c kSfbAtoms + t) ..
+                  tc_cp_atom(t_sfb + 4 * (c * C::kSfbAtoms + t),
+                             sdesc_atom(st_u32 + C::kSfOff + 512 * C::kSfK * (1 + t) + 512 * c));
+              }
             }
-            mma_commit(&sf_full[s]);  // arrives when the copies are done
+            mma_commit(&sf_full[s]);  // arrives when this warp's copies are done
           }
         }
         if (!ok) {
