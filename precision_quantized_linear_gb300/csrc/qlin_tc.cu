@@ -413,9 +413,10 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
           // weight-major: A = weight tile, B = token tile; token-major: swapped
           const uint32_t a_addr = smem_u32(ring + s * C::kStage + (C::kTokM ? 0 : C::kXBlk));
           const uint32_t b_addr = smem_u32(ring + s * C::kStage + (C::kTokM ? C::kXBlk : 0));
+          const uint64_t ad0 = sdesc_sw128(a_addr), bd0 = sdesc_sw128(b_addr);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8(tmem_d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc, kk != 0);
+          for (int kk = 0; kk < 4; ++kk)  // 32 bytes of K per step: start address + 2 (16-byte units)
+            mma_f8(tmem_d, ad0 + 2 * kk, bd0 + 2 * kk, idesc, kk != 0);
           mma_commit(&empty[s]);
           mma_commit(&acc_full[pb]);
         }
@@ -452,10 +453,10 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
           const uint32_t t_sfa = tmem_base + C::kSfaCol + s * 4 * C::kSfK;
           const uint32_t t_sfb = tmem_base + C::kSfbCol + s * 4 * C::kSfK * C::kSfbAtoms;
           const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
-          const uint32_t a_addr = st_u32 + C::kXBlk, b_addr = st_u32;
+          const uint64_t ad0 = sdesc_sw128(st_u32 + C::kXBlk), bd0 = sdesc_sw128(st_u32);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(a_addr + kk * 32), bd = sdesc_sw128(b_addr + kk * 32);
+            const uint64_t ad = ad0 + 2 * kk, bd = bd0 + 2 * kk;  // 32 bytes of K per step
             const uint32_t accum = (j | kk) != 0;
             if constexpr (MX == kMxF8) {
               mma_mx8(tmem_d, ad, bd, idesc_mx(BN, kk, kk), t_sfa, t_sfb + tok_col, accum);
@@ -502,11 +503,11 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
             }
             tc_fence_after();
             const uint32_t a_addr = tmem_base + C::kAColBase + ai * C::kASlotCols;
-            const uint32_t b_addr = smem_u32(ring + s * C::kStage + i * C::kXBlk);
+            const uint64_t bd0 = sdesc_sw128(smem_u32(ring + s * C::kStage + i * C::kXBlk));
             const uint32_t tmem_d = tmem_base + pb * C::kAccCols;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // 32 bytes of K per MMA = 8 TMEM columns of A
-              mma_f8_tmem_a(tmem_d, a_addr + kk * 8, sdesc_sw128(b_addr + kk * 32), idesc, kk != 0);
+              mma_f8_tmem_a(tmem_d, a_addr + kk * 8, bd0 + 2 * kk, idesc, kk != 0);
             mma_commit(&a_empty[ai]);
             mma_commit(&acc_full[pb]);
           }
@@ -598,17 +599,20 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
               a_addr = smem_u32(ring + s * C::kStage + KPS * C::kXBlk);
             }
             tc_fence_after();
-            const uint32_t b_addr = smem_u32(ring + s * C::kStage + i * C::kXBlk);
+            // descriptors of the first k-step; a step of 32 bytes of K adds 2 to
+            // the start address (16-byte units, bits 0..13; shared addresses < 256 KB)
+            const uint64_t bd0 = sdesc_sw128(smem_u32(ring + s * C::kStage + i * C::kXBlk));
+            const uint64_t ad0 = C::kATmem ? 0 : sdesc_sw128(a_addr);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per MMA
-              const uint64_t bd = sdesc_sw128(b_addr + kk * 32);
+              const uint64_t bd = bd0 + 2 * kk;
               const uint32_t accum = (j | i | kk) != 0;
               if constexpr (C::kATmem)
                 mma_f16_tmem_a(tmem_d, a_addr + kk * 8, bd, idesc, accum);  // 16 BF16 of K = 8 columns
               else if constexpr (W4)
-                mma_f16(tmem_d, sdesc_sw128(a_addr + kk * 32), bd, idesc, accum);
+                mma_f16(tmem_d, ad0 + 2 * kk, bd, idesc, accum);
               else
-                mma_f8(tmem_d, sdesc_sw128(a_addr + kk * 32), bd, idesc, accum);
+                mma_f8(tmem_d, ad0 + 2 * kk, bd, idesc, accum);
             }
             if constexpr (W4) mma_commit(&a_empty[ai]);
           }
@@ -626,8 +630,9 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
       // ------------------------------------------------------------ scale warps (block-scaled formats)
       // Per K block: wait for the stage, copy its scale atoms from shared
       // memory into the stage's TMEM slot (tcgen05.cp), and commit the copies
-      // to sf_full[s] (one arrival per scale warp).  Slot s is free again when the producer refills stage
-      // s: that happens only after the MMAs that read the slot are done.
+      // to sf_full[s] (one arrival per scale warp).  Slot s is free again when
+      // the producer refills stage s: that happens only after the MMAs that
+      // read the slot are done.
       if (lane == 0) {
         int it = 0;
         bool ok = true;
