@@ -534,11 +534,10 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + acc * C::kAccCols;
         for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
+          // No wait on full[s]: the dequantisation group that filled a slot of
+          // this stage waited on full[s] before arriving on a_full, so the
+          // a_full wait below already orders these MMAs after the stage's copies
           const int s = it % C::kStages;
-          if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
-            ok = false;
-            break;
-          }
           const uint32_t st_u32 = smem_u32(ring + s * C::kStage);
 #pragma unroll
           for (int ip = 0; ip < KPS / 2; ++ip, ++pit) {
@@ -581,7 +580,9 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         const uint32_t tmem_d = tmem_base + acc * C::kAccCols;
         for (int j = 0; j < un.nkb / KPS && ok; ++j, ++it) {
           const int s = it % C::kStages;
-          if (!mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
+          // W4A16: the a_full wait below orders the MMAs after the stage's
+          // copies (its dequantisation group waited on full[s] first)
+          if (!W4 && !mbar_wait(&full[s], (it / C::kStages) & 1, kWaitLimitNs, &s_abort)) {
             ok = false;
             break;
           }
