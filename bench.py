@@ -833,7 +833,8 @@ def run_sweep(args):
         plan = [("w8", M) for M in (2048, 8192)] + [("w4", M) for M in (2048, 8192)]
     elif args.sweep == "70b":
         shapes = [(8192, 10240), (8192, 8192), (8192, 57344), (28672, 8192)]
-        plan = [("w4", M) for M in (1, 64, 256)] + [("w8", M) for M in (256, 4096)]
+        plan = [("w4", M) for M in (1, 64, 256)] + [("w8", M) for M in (256, 4096)] + \
+               [("w4a8", M) for M in (1, 64, 256)]
     elif args.sweep == "epilogue":  # fused bias + SiLU / GELU beside the plain calls
         shapes = [(4096, 4096), (4096, 28672)]
         plan = [(v, M) for M in (1, 16, 256, 2048) for v in ("w4", "w4:silu", "w4:gelu", "w8", "w8:silu")]
@@ -868,7 +869,7 @@ def run_sweep(args):
             sx = torch.empty(M, dtype=torch.float32, device="cuda")
             row = {"K": K, "N": N, "M": M, "variant": v + (":bias+" + actname if actname else "")}
             flops = 2 * M * N * K
-            if v.startswith("w4"):
+            if v in ("w4", "w4gemv", "w4tc"):
                 path = {"w4": q.PATH_AUTO, "w4gemv": q.PATH_GEMV, "w4tc": q.PATH_TC}[v]
                 nb = q.qlin_workspace_size(q.OP_W4A16_GEMM, M, N, K)
                 ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")

@@ -5,7 +5,7 @@ activations of qlin_quant_act_fp8; the oracle's reference is the fp64 product of
 the dequantised operands (sx[m] e4m3(Xq) and s (q - z)).  Bar:
     |Y - Y_ref| <= 2e-3 * ||X_deq[m, :]||_2 * ||W_deq[n, :]||_2
 on every element up to 32 tokens (and on the crossover shapes up to 512),
-on whole tiles beyond.  Each case asserts through the dispatch query which token
+on whole tiles beyond; the Llama-3-70B layers at M = 1, 64 and 256.  Each case asserts through the dispatch query which token
 tile and split count it reaches.
 """
 import numpy as np
@@ -90,6 +90,19 @@ def test_w4a8_crossover_shapes(K, N):
     lin = W4A8Linear(to_dev(W))
     for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):
         _run(M, N, K, seed=M + 41, full=True, W=W, wq=wq, lin=lin)
+
+
+@pytest.mark.parametrize("K,N", [(8192, 10240), (8192, 8192), (8192, 57344), (28672, 8192)])
+def test_w4a8_llama70b(K, N):
+    """The Llama-3-70B layers at the W4A16 batch points (M = 1, 64, 256): every
+    element at one token, whole tiles beyond."""
+    W = syn.make_weight(N, K, seed=11 * K + N)
+    wq = oracle.quantize_w4(W)
+    lin = W4A8Linear(to_dev(W))
+    for M in (1, 64, 256):
+        _run(M, N, K, seed=M + 53, full=M == 1, W=W, wq=wq, lin=lin)
+    del lin
+    torch.cuda.empty_cache()
 
 
 def test_w4a8_deterministic_and_workspace_left_zero():
