@@ -426,6 +426,18 @@ cudaError_t launch_quant_w_fp8_blocks(const uint16_t* W, int64_t N, int64_t K, u
 
 // ------------------------------------------------------------------ MXFP8
 
+// Eight BF16 columns of one 16-byte load
+__device__ __forceinline__ void bf16x8(uint4 raw, float (&v)[8]) {
+  v[0] = bf16_lo(raw.x);
+  v[1] = bf16_hi(raw.x);
+  v[2] = bf16_lo(raw.y);
+  v[3] = bf16_hi(raw.y);
+  v[4] = bf16_lo(raw.z);
+  v[5] = bf16_hi(raw.z);
+  v[6] = bf16_lo(raw.w);
+  v[7] = bf16_hi(raw.w);
+}
+
 // Items (a row's 128- or 256-column chunk) per warp in the MX / FP4
 // quantisers: a warp issues all of their loads before the arithmetic, so that
 // an SM keeps enough bytes in flight to stream at the HBM rate.
@@ -442,59 +454,71 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// A warp per kMxItems consecutive (row r, 128 columns) items: lane l holds
-// columns 4l .. 4l+3, a block of 32 columns is a segment of 8 lanes.  Codes are E4M3(v * 2^-e) -- the
-// power-of-two scaling is exact, so this is v / 2^e rounded once, to nearest
-// even with saturation.  The four scale bytes of the 128 columns go to one
-// 32-bit word of the scale atom: row r of atom (r / 128, k / 128) holds its
-// word at byte 16 (r % 32) + 4 ((r % 128) / 32); rows past R (the atom's
-// padding) get 0.
+// A warp per kMxItems consecutive (row r, 256 columns) items: lane l holds
+// columns 8l .. 8l+7 (one 16-byte load), a block of 32 columns is a segment of
+// four lanes, and lanes 16h .. 16h+15 are K block 2c + h.  When K is an odd
+// number of 128-column blocks, the last item of a row has only its first half.
+// Codes are E4M3(v * 2^-e) -- the power-of-two scaling is exact, so this is
+// v / 2^e rounded once, to nearest even with saturation.  The four scale bytes
+// of a 128-column block go to one 32-bit word of the scale atom: row r of atom
+// (r / 128, k / 128) holds its word at byte 16 (r % 32) + 4 ((r % 128) / 32);
+// rows past R (the atom's padding) get 0.
 __global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint16_t* __restrict__ X, int64_t R, int64_t K,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const int lane = threadIdx.x & 31;
-  const int64_t nc = K / 128;
-  const int64_t total = (R + 127) / 128 * 128 * nc;  // items: (row, 128 columns), padding rows included
+  const int64_t nkb = K / 128, nc = (nkb + 1) / 2;
+  const int64_t total = (R + 127) / 128 * 128 * nc;  // items: (row, 256 columns), padding rows included
   const int64_t item0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kMxItems;
   if (item0 >= total) return;  // whole warps only
-  // all of this warp's loads first, so that kMxItems of them are in flight
+  // all of this warp's loads first, so that kMxItems of them are in flight;
   // item0 + u is row rr[u], chunk cc[u]: one division per warp, then a carry
-  int64_t rr[kMxItems], cc[kMxItems];
-  rr[0] = item0 / nc;
-  cc[0] = item0 - rr[0] * nc;
+  // (rows < 2^31 and chunks < 2^23, as the call checks: 32-bit indices keep
+  // the warp's state in registers)
+  int rr[kMxItems], cc[kMxItems];
+  rr[0] = static_cast<int>(item0 / nc);
+  cc[0] = static_cast<int>(item0 - static_cast<int64_t>(rr[0]) * nc);
 #pragma unroll
   for (int u = 1; u < kMxItems; ++u) {
     const bool wrap = cc[u - 1] + 1 == nc;
     cc[u] = wrap ? 0 : cc[u - 1] + 1;
     rr[u] = wrap ? rr[u - 1] + 1 : rr[u - 1];
   }
-  uint2 raw[kMxItems];
+  const int half = lane >> 4;
+  uint4 raw[kMxItems];
 #pragma unroll
   for (int u = 0; u < kMxItems; ++u) {
     const int64_t item = item0 + u, r = rr[u], c = cc[u];
-    raw[u] = (item < total && r < R) ? *reinterpret_cast<const uint2*>(X + r * K + c * 128 + 4 * lane) : make_uint2(0u, 0u);
+    raw[u] = (item < total && r < R && 2 * c + half < nkb)
+                 ? *reinterpret_cast<const uint4*>(X + r * K + c * 256 + 8 * lane)
+                 : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
   for (int u = 0; u < kMxItems; ++u) {
     const int64_t item = item0 + u;
     if (item >= total) break;  // the same for the whole warp
     const int64_t r = rr[u], c = cc[u];
+    const bool mine = 2 * c + half < nkb;  // this lane's K block exists
     uint32_t e8 = 0;
     if (r < R) {
-      const float v[4] = {bf16_lo(raw[u].x), bf16_hi(raw[u].x), bf16_lo(raw[u].y), bf16_hi(raw[u].y)};
-      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-      amax = seg_max(amax, 8);
+      float v[8];
+      bf16x8(raw[u], v);
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      amax = seg_max(amax, 4);
       const int e = amax == 0.0f ? -127 : mx_exponent(amax);
       const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, e in [-127, 119]
-      const uint32_t lo = e4m3x2(v[0] * inv, v[1] * inv), hi = e4m3x2(v[2] * inv, v[3] * inv);
-      *reinterpret_cast<uint32_t*>(codes + r * K + c * 128 + 4 * lane) = lo | (hi << 16);
+      const uint32_t w0 = e4m3x2(v[0] * inv, v[1] * inv) | (e4m3x2(v[2] * inv, v[3] * inv) << 16);
+      const uint32_t w1 = e4m3x2(v[4] * inv, v[5] * inv) | (e4m3x2(v[6] * inv, v[7] * inv) << 16);
+      if (mine) *reinterpret_cast<uint2*>(codes + r * K + c * 256 + 8 * lane) = make_uint2(w0, w1);
       e8 = static_cast<uint32_t>(e + 127);
     }
-    // bytes kk = 0..3 of the word from lanes 0, 8, 16, 24
-    uint32_t word = (e8 & 0xFFu) << (8 * (lane >> 3));
+    // bytes kk = 0..3 of K block 2c + h's word from lanes 16h, +4, +8, +12
+    uint32_t word = (e8 & 0xFFu) << (8 * ((lane >> 2) & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
     word |= __shfl_xor_sync(0xffffffffu, word, 8);
-    word |= __shfl_xor_sync(0xffffffffu, word, 16);
-    if (lane == 0) {
-      uint8_t* atom = scales + ((r / 128) * nc + c) * 512;
+    if ((lane & 15) == 0 && mine) {
+      uint8_t* atom = scales + ((r / 128) * nkb + 2 * c + half) * 512;
       *reinterpret_cast<uint32_t*>(atom + 16 * (r % 32) + 4 * ((r % 128) / 32)) = word;
     }
   }
@@ -502,7 +526,7 @@ __global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint16_t* __rest
 
 cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t st) {
-  const int64_t items = (R + 127) / 128 * 128 * (K / 128);
+  const int64_t items = (R + 127) / 128 * 128 * ((K / 128 + 1) / 2);
   const int64_t warps = (items + kMxItems - 1) / kMxItems;
   const int64_t blocks = (warps + 7) / 8;
   quant_mxfp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(X, R, K, codes, scales);
@@ -525,18 +549,6 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
       : "=r"(r)
       : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
   return r;
-}
-
-// Eight BF16 columns of one 16-byte load
-__device__ __forceinline__ void bf16x8(uint4 raw, float (&v)[8]) {
-  v[0] = bf16_lo(raw.x);
-  v[1] = bf16_hi(raw.x);
-  v[2] = bf16_lo(raw.y);
-  v[3] = bf16_hi(raw.y);
-  v[4] = bf16_lo(raw.z);
-  v[5] = bf16_hi(raw.z);
-  v[6] = bf16_lo(raw.w);
-  v[7] = bf16_hi(raw.w);
 }
 
 // MXFP4 ([LP] S10, OCP Microscaling v1.0): a warp per kMxItems consecutive

@@ -34,7 +34,7 @@ def _lib():
     assert q.qlin_get_device_error() == 0
 
 
-@pytest.mark.parametrize("R,K", [(1, 128), (7, 512), (300, 4096), (4096, 4096), (129, 14336)])
+@pytest.mark.parametrize("R,K", [(1, 128), (7, 512), (33, 384), (300, 4096), (4096, 4096), (129, 14336)])
 def test_quant_mxfp8_bit_exact(R, K):
     X = syn.make_act(R, K, seed=R + K, token_outlier_frac=0.01)
     X[0, :32] = 0                                 # an all-zero block: scale code 0
