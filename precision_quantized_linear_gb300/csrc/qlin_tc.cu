@@ -178,6 +178,8 @@ struct TcArgs {
   int units;         // ntiles * mblocks * splits
   int mb_fast;       // unit order: token block fastest (weights streamed once) or weight tile fastest
   int x_keep;        // keep activation tiles in L2 (evict-last) when they are small
+  int w_keep;        // keep weight tiles in L2 (evict-last): with the weight tile fastest, each one is
+                     // read again by every later token block; otherwise they are streamed (evict-first)
   int G;             // W4A16 quantisation group (32, 64, 128, or K for per-channel scales)
   int gshift;        // log2 G; 31 for per-channel scales, so that every column maps to group 0
   Epi epi;           // output epilogue (bias, activation); not used by block scaling
@@ -304,7 +306,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_stream = a.w_keep ? policy_evict_last() : policy_evict_first();  // weight tiles
       const uint64_t pol_keep = a.x_keep ? policy_evict_last() : policy_evict_normal();
       const int64_t ng = W4 ? a.K / a.G : 0;  // groups per weight row (W4A16)
       // groups whose scales a stage loads: those of its KPS blocks (a G = 128
@@ -1667,6 +1669,7 @@ static cudaError_t launch_tc(const CUtensorMap& tx, const CUtensorMap& tw, const
     const double xb = static_cast<double>(args.M) * static_cast<double>(args.K) * ((W4 && !A8) ? 2.0 : C::kF4 ? 0.5 : 1.0);
     args.mb_fast = xb < wb ? 1 : 0;
     args.x_keep = xb <= l2_half / 2 ? 1 : 0;
+    args.w_keep = !args.mb_fast && args.mblocks > 1 && wb <= l2_half ? 1 : 0;
   }
   const int grid = args.units < num_sms ? args.units : num_sms;
   cudaLaunchConfig_t cfg = {};
