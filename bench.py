@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 LAYERS_8B = [("qkv", 4096, 6144), ("o_proj", 4096, 4096), ("gate_up", 4096, 28672), ("down", 14336, 4096)]
 MS_DECODE = (1, 4, 16)
 ROTATE = 5
+NOMINAL_HBM_GBS = 8000.0  # the part's nominal HBM3e rate (~8 TB/s), reported beside the measured peak
 WORKLOAD = "llama3-8b W4A16 decode layers (qkv/o/gate_up/down) at M=1,4,16"
 
 
@@ -334,6 +335,23 @@ def run_ours(args):
         t = a.elapsed_time(b) / (5 * ROTATE)
         per_m_gbs[str(M)] = round(pass_bytes / (t * 1e-3) / 1e9, 1)
 
+    # single-launch latency: one call outside any graph (launch amortisation is
+    # what the graphs above measure without): an event, one call through the
+    # C ABI on an idle stream, an event; median of 50, per layer at M = 1
+    latency_us = {}
+    for L in layers:
+        samples = []
+        for i in range(50):
+            a, b = make_event(False), make_event(False)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                issue([(1, L, i % ROTATE)])
+                b.record(stream)
+            torch.cuda.synchronize()
+            samples.append(a.elapsed_time(b) * 1e3)
+        latency_us[L["name"]] = round(float(np.median(samples)), 2)
+
     e2e = run_e2e(args, layers, xs, ys, ws, flat, stream, world)
     extra = {}
     if not args.no_sweeps and world == 1:
@@ -359,12 +377,15 @@ def run_ours(args):
                          (ROTATE, ROTATE, (ROTATE - 1) * pass_bytes / 1e6, (ROTATE - 1) * pass_bytes / l2),
                    "timing": "CUDA graph per step, CUDA events on the launching stream around the timed steps"},
         "per_M_weight_gbs": per_m_gbs,
+        "single_launch_us_m1": latency_us,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": traffic_per_launch,
                      "traffic_note": "bytes per launch, scaled from one ncu capture (M=1, 4096x28672) by "
                                      "algorithmic bytes",
-                     "peak_source": peaks["source"], "launches_timed": len(calls) * args.steps,
+                     "peak_source": peaks["source"],
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "nominal_peak": NOMINAL_HBM_GBS, "launches_timed": len(calls) * args.steps,
                      "ms_per_launch": round(launch_ms, 5), "share_of_step": 1.0},
         "gpu_launches": len(calls) * args.steps,
         "clocks": clk,
