@@ -84,7 +84,8 @@ typedef enum {
 #define QLIN_OP_MXFP4_GEMM 7
 #define QLIN_OP_NVFP4_GEMM 8
 
-/* Activation of the fused output epilogue (qlin_*_gemm_fused). */
+/* Activation of the fused output epilogue (qlin_*_gemm_fused: W4A16, W8A8,
+ * W4A8, MXFP8, MXFP4 and NVFP4; not the block-scaled FP8 GEMM). */
 #define QLIN_ACT_NONE 0
 #define QLIN_ACT_RELU 1 /* max(v, 0)                                   */
 #define QLIN_ACT_SILU 2 /* v / (1 + exp(-v))                           */
@@ -276,6 +277,14 @@ qlin_status_t qlin_w4a8_gemm(const void* Xq_e4m3, const float* sx, const void* c
                              const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
                              void* workspace, size_t ws_bytes, void* stream);
 
+/* W4A8 with the fused output epilogue of qlin_w4a16_gemm_fused ([LP] S23,
+ * S24): Y[m][n] = bf16( act( y[m][n] + bias[n] ) ), y the FP32 value that
+ * qlin_w4a8_gemm rounds; bias BF16 [N] (NULL: none, else 16-byte aligned),
+ * act one of QLIN_ACT_*.  Everything else as qlin_w4a8_gemm. */
+qlin_status_t qlin_w4a8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,
+                                   const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
+                                   const void* bias_bf16, int act, void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- MXFP8 (the OCP Microscaling format that [LP] S10 names; [VQ] S2: the
  * MXFP8 W8A8 path runs on Blackwell only): E4M3 elements in blocks of 32
  * consecutive values along K, each block with one power-of-two scale 2^e
@@ -314,6 +323,13 @@ qlin_status_t qlin_quant_mxfp8(const void* X_bf16, int64_t R, int64_t K, void* c
 qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3, const void* ws_e8m0,
                               void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                               void* stream);
+
+/* MXFP8 with the fused output epilogue: Y[m][n] = bf16( act( y[m][n] +
+ * bias[n] ) ), y the FP32 value qlin_mxfp8_gemm rounds; bias and act as in
+ * qlin_w4a16_gemm_fused.  Everything else as qlin_mxfp8_gemm. */
+qlin_status_t qlin_mxfp8_gemm_fused(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3,
+                                    const void* ws_e8m0, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                                    const void* bias_bf16, int act, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---- FP4 ([LP] S10: the E2M1 element -- 1 sign, 2 exponent and 1 mantissa
  * bit, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 -- in the two block formats that
@@ -373,6 +389,12 @@ qlin_status_t qlin_mxfp4_gemm(const void* Xq_e2m1, const void* xs_e8m0, const vo
                               void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                               void* stream);
 
+/* MXFP4 with the fused output epilogue (bias and act as in
+ * qlin_w4a16_gemm_fused, applied to the FP32 value qlin_mxfp4_gemm rounds). */
+qlin_status_t qlin_mxfp4_gemm_fused(const void* Xq_e2m1, const void* xs_e8m0, const void* Wq_e2m1,
+                                    const void* ws_e8m0, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                                    const void* bias_bf16, int act, void* workspace, size_t ws_bytes, void* stream);
+
 /* NVFP4 linear layer: Y[m][n] = bf16( sgx sgw sum_b e4m3(xs[m][b]) e4m3(ws[n][b])
  * sum_{k in block b} e2m1(Xq[m][k]) e2m1(Wq[n][k]) ), b over the 16-column
  * blocks; the block scales are applied by the tensor cores (tcgen05
@@ -382,6 +404,14 @@ qlin_status_t qlin_mxfp4_gemm(const void* Xq_e2m1, const void* xs_e8m0, const vo
 qlin_status_t qlin_nvfp4_gemm(const void* Xq_e2m1, const void* xs_e4m3, const float* sgx, const void* Wq_e2m1,
                               const void* ws_e4m3, const float* sgw, void* Y_bf16, int64_t M, int64_t N, int64_t K,
                               void* workspace, size_t ws_bytes, void* stream);
+
+/* NVFP4 with the fused output epilogue: Y[m][n] = bf16( act( y[m][n] +
+ * bias[n] ) ), y the FP32 value qlin_nvfp4_gemm rounds (after sgx * sgw);
+ * bias and act as in qlin_w4a16_gemm_fused. */
+qlin_status_t qlin_nvfp4_gemm_fused(const void* Xq_e2m1, const void* xs_e4m3, const float* sgx, const void* Wq_e2m1,
+                                    const void* ws_e4m3, const float* sgw, void* Y_bf16, int64_t M, int64_t N,
+                                    int64_t K, const void* bias_bf16, int act, void* workspace, size_t ws_bytes,
+                                    void* stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QLIN_OK, or the first error a kernel recorded since the last call. */

@@ -33,7 +33,8 @@ __all__ = [
     "qlin_mx_scale_bytes", "qlin_quant_mxfp8", "qlin_mxfp8_gemm", "qlin_w4a8_gemm", "OP_W4A8_GEMM",
     "KERNEL_W4A8_TC", "OP_MXFP4_GEMM", "OP_NVFP4_GEMM", "KERNEL_MXFP4_TC", "KERNEL_NVFP4_TC",
     "qlin_nvfp4_scale_bytes", "qlin_quant_mxfp4", "qlin_nvfp4_tensor_scale", "qlin_quant_nvfp4", "qlin_mxfp4_gemm",
-    "qlin_nvfp4_gemm",
+    "qlin_nvfp4_gemm", "qlin_w4a8_gemm_fused", "qlin_mxfp8_gemm_fused", "qlin_mxfp4_gemm_fused",
+    "qlin_nvfp4_gemm_fused",
 ]
 
 OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM, OP_MXFP8_GEMM, OP_W4A8_GEMM = 1, 2, 3, 4, 5, 6
@@ -86,6 +87,10 @@ _SIGS = {
     "qlin_quant_nvfp4": [_p, _i64, _i64, _p, _p, _p, _p],
     "qlin_mxfp4_gemm": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
     "qlin_nvfp4_gemm": [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _sz, _p],
+    "qlin_w4a8_gemm_fused": [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _int, _p, _sz, _p],
+    "qlin_mxfp8_gemm_fused": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _p],
+    "qlin_mxfp4_gemm_fused": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _p],
+    "qlin_nvfp4_gemm_fused": [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _p],
 }
 
 
@@ -307,6 +312,30 @@ def qlin_mxfp4_gemm(Xq, xs, Wq, ws_sf, Y, M, N, K, workspace, ws_bytes, stream=N
 def qlin_nvfp4_gemm(Xq, xs, sgx, Wq, ws_sf, sgw, Y, M, N, K, workspace, ws_bytes, stream=None):
     return _check(load().qlin_nvfp4_gemm(_ptr(Xq), _ptr(xs), _ptr(sgx), _ptr(Wq), _ptr(ws_sf), _ptr(sgw), _ptr(Y),
                                          M, N, K, _ptr(workspace), ws_bytes, _stream(stream)), "qlin_nvfp4_gemm")
+
+
+def qlin_w4a8_gemm_fused(Xq, sx, codes, scales, zeros, Y, M, N, K, G, bias, act, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_w4a8_gemm_fused(_ptr(Xq), _ptr(sx), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(Y),
+                                              M, N, K, G, _ptr(bias), act, _ptr(workspace), ws_bytes,
+                                              _stream(stream)), "qlin_w4a8_gemm_fused")
+
+
+def qlin_mxfp8_gemm_fused(Xq, xs, Wq, ws_sf, Y, M, N, K, bias, act, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_mxfp8_gemm_fused(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws_sf), _ptr(Y), M, N, K,
+                                               _ptr(bias), act, _ptr(workspace), ws_bytes, _stream(stream)),
+                  "qlin_mxfp8_gemm_fused")
+
+
+def qlin_mxfp4_gemm_fused(Xq, xs, Wq, ws_sf, Y, M, N, K, bias, act, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_mxfp4_gemm_fused(_ptr(Xq), _ptr(xs), _ptr(Wq), _ptr(ws_sf), _ptr(Y), M, N, K,
+                                               _ptr(bias), act, _ptr(workspace), ws_bytes, _stream(stream)),
+                  "qlin_mxfp4_gemm_fused")
+
+
+def qlin_nvfp4_gemm_fused(Xq, xs, sgx, Wq, ws_sf, sgw, Y, M, N, K, bias, act, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_nvfp4_gemm_fused(_ptr(Xq), _ptr(xs), _ptr(sgx), _ptr(Wq), _ptr(ws_sf), _ptr(sgw),
+                                               _ptr(Y), M, N, K, _ptr(bias), act, _ptr(workspace), ws_bytes,
+                                               _stream(stream)), "qlin_nvfp4_gemm_fused")
 
 
 def qlin_get_device_error(stream=None) -> int:

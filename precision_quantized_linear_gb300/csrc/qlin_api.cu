@@ -558,9 +558,9 @@ qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, con
                                             static_cast<cudaStream_t>(stream)));
 }
 
-qlin_status_t qlin_w4a8_gemm(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,
-                             const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
-                             void* workspace, size_t ws_bytes, void* stream) {
+static qlin_status_t w4a8_impl(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,
+                               const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
+                               const Epi& epi, void* workspace, size_t ws_bytes, void* stream) {
   if (G != kGroup) return QLIN_ERR_UNSUPPORTED_SHAPE;  // one quantisation group per 128-column K block
   qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
@@ -577,7 +577,22 @@ qlin_status_t qlin_w4a8_gemm(const void* Xq_e4m3, const float* sx, const void* c
   return launch_status(launch_w4a8_tc(static_cast<const uint8_t*>(Xq_e4m3), sx, static_cast<const uint8_t*>(codes),
                                       static_cast<const uint16_t*>(scales_f16), static_cast<const uint8_t*>(zeros_u4),
                                       static_cast<uint16_t*>(Y_bf16), M, N, K, p, workspace, d->err, d->num_sms,
-                                      static_cast<cudaStream_t>(stream)));
+                                      static_cast<cudaStream_t>(stream), epi));
+}
+
+qlin_status_t qlin_w4a8_gemm(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,
+                             const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  return w4a8_impl(Xq_e4m3, sx, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, Epi{}, workspace, ws_bytes, stream);
+}
+
+qlin_status_t qlin_w4a8_gemm_fused(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,
+                                   const void* zeros_u4, void* Y_bf16, int64_t M, int64_t N, int64_t K, int G,
+                                   const void* bias_bf16, int act, void* workspace, size_t ws_bytes, void* stream) {
+  Epi epi;
+  const qlin_status_t st = make_epi(bias_bf16, act, &epi);
+  if (st != QLIN_OK) return st;
+  return w4a8_impl(Xq_e4m3, sx, codes, scales_f16, zeros_u4, Y_bf16, M, N, K, G, epi, workspace, ws_bytes, stream);
 }
 
 qlin_status_t qlin_mx_scale_bytes(int64_t R, int64_t K, size_t* bytes) {
@@ -601,9 +616,9 @@ qlin_status_t qlin_quant_mxfp8(const void* X_bf16, int64_t R, int64_t K, void* c
                                           static_cast<cudaStream_t>(stream)));
 }
 
-qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3, const void* ws_e8m0,
-                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
-                              void* stream) {
+static qlin_status_t mxfp8_impl(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3, const void* ws_e8m0,
+                                void* Y_bf16, int64_t M, int64_t N, int64_t K, const Epi& epi, void* workspace,
+                                size_t ws_bytes, void* stream) {
   qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (M == 0) return QLIN_OK;
@@ -619,7 +634,22 @@ qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const vo
   return launch_status(launch_mxfp8_tc(static_cast<const uint8_t*>(Xq_e4m3), static_cast<const uint8_t*>(xs_e8m0),
                                        static_cast<const uint8_t*>(Wq_e4m3), static_cast<const uint8_t*>(ws_e8m0),
                                        static_cast<uint16_t*>(Y_bf16), M, N, K, p, workspace, d->err, d->num_sms,
-                                       static_cast<cudaStream_t>(stream)));
+                                       static_cast<cudaStream_t>(stream), epi));
+}
+
+qlin_status_t qlin_mxfp8_gemm(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3, const void* ws_e8m0,
+                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  return mxfp8_impl(Xq_e4m3, xs_e8m0, Wq_e4m3, ws_e8m0, Y_bf16, M, N, K, Epi{}, workspace, ws_bytes, stream);
+}
+
+qlin_status_t qlin_mxfp8_gemm_fused(const void* Xq_e4m3, const void* xs_e8m0, const void* Wq_e4m3,
+                                    const void* ws_e8m0, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                                    const void* bias_bf16, int act, void* workspace, size_t ws_bytes, void* stream) {
+  Epi epi;
+  const qlin_status_t st = make_epi(bias_bf16, act, &epi);
+  if (st != QLIN_OK) return st;
+  return mxfp8_impl(Xq_e4m3, xs_e8m0, Wq_e4m3, ws_e8m0, Y_bf16, M, N, K, epi, workspace, ws_bytes, stream);
 }
 
 // ---- FP4: packed E2M1, K % 256 == 0 (one 128-byte TMA box = 256 columns per K block)
@@ -678,7 +708,7 @@ qlin_status_t qlin_quant_nvfp4(const void* X_bf16, int64_t R, int64_t K, const f
 
 static qlin_status_t fp4_gemm(const void* Xq, const void* xs, const float* sgx, const void* Wq, const void* ws_sf,
                               const float* sgw, bool nv, void* Y_bf16, int64_t M, int64_t N, int64_t K,
-                              void* workspace, size_t ws_bytes, void* stream) {
+                              const Epi& epi, void* workspace, size_t ws_bytes, void* stream) {
   qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (K % kFp4K != 0) return QLIN_ERR_UNSUPPORTED_SHAPE;
@@ -696,20 +726,42 @@ static qlin_status_t fp4_gemm(const void* Xq, const void* xs, const float* sgx, 
   return launch_status(launch_fp4_tc(static_cast<const uint8_t*>(Xq), static_cast<const uint8_t*>(xs), sgx,
                                      static_cast<const uint8_t*>(Wq), static_cast<const uint8_t*>(ws_sf), sgw,
                                      static_cast<uint16_t*>(Y_bf16), M, N, K, nv, p, workspace, d->err, d->num_sms,
-                                     static_cast<cudaStream_t>(stream)));
+                                     static_cast<cudaStream_t>(stream), epi));
 }
 
 qlin_status_t qlin_mxfp4_gemm(const void* Xq_e2m1, const void* xs_e8m0, const void* Wq_e2m1, const void* ws_e8m0,
                               void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                               void* stream) {
-  return fp4_gemm(Xq_e2m1, xs_e8m0, nullptr, Wq_e2m1, ws_e8m0, nullptr, false, Y_bf16, M, N, K, workspace, ws_bytes,
-                  stream);
+  return fp4_gemm(Xq_e2m1, xs_e8m0, nullptr, Wq_e2m1, ws_e8m0, nullptr, false, Y_bf16, M, N, K, Epi{}, workspace,
+                  ws_bytes, stream);
+}
+
+qlin_status_t qlin_mxfp4_gemm_fused(const void* Xq_e2m1, const void* xs_e8m0, const void* Wq_e2m1,
+                                    const void* ws_e8m0, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                                    const void* bias_bf16, int act, void* workspace, size_t ws_bytes, void* stream) {
+  Epi epi;
+  const qlin_status_t st = make_epi(bias_bf16, act, &epi);
+  if (st != QLIN_OK) return st;
+  return fp4_gemm(Xq_e2m1, xs_e8m0, nullptr, Wq_e2m1, ws_e8m0, nullptr, false, Y_bf16, M, N, K, epi, workspace,
+                  ws_bytes, stream);
 }
 
 qlin_status_t qlin_nvfp4_gemm(const void* Xq_e2m1, const void* xs_e4m3, const float* sgx, const void* Wq_e2m1,
                               const void* ws_e4m3, const float* sgw, void* Y_bf16, int64_t M, int64_t N, int64_t K,
                               void* workspace, size_t ws_bytes, void* stream) {
-  return fp4_gemm(Xq_e2m1, xs_e4m3, sgx, Wq_e2m1, ws_e4m3, sgw, true, Y_bf16, M, N, K, workspace, ws_bytes, stream);
+  return fp4_gemm(Xq_e2m1, xs_e4m3, sgx, Wq_e2m1, ws_e4m3, sgw, true, Y_bf16, M, N, K, Epi{}, workspace, ws_bytes,
+                  stream);
+}
+
+qlin_status_t qlin_nvfp4_gemm_fused(const void* Xq_e2m1, const void* xs_e4m3, const float* sgx, const void* Wq_e2m1,
+                                    const void* ws_e4m3, const float* sgw, void* Y_bf16, int64_t M, int64_t N,
+                                    int64_t K, const void* bias_bf16, int act, void* workspace, size_t ws_bytes,
+                                    void* stream) {
+  Epi epi;
+  const qlin_status_t st = make_epi(bias_bf16, act, &epi);
+  if (st != QLIN_OK) return st;
+  return fp4_gemm(Xq_e2m1, xs_e4m3, sgx, Wq_e2m1, ws_e4m3, sgw, true, Y_bf16, M, N, K, epi, workspace, ws_bytes,
+                  stream);
 }
 
 qlin_status_t qlin_selftest_wait_timeout(uint32_t limit_us, void* stream) {

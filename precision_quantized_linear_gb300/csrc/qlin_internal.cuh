@@ -159,13 +159,13 @@ cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8
 TcPlan plan_w4a8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w4a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* codes, const uint16_t* scales,
                            const uint8_t* zeros, uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan,
-                           void* ws, int* err, int num_sms, cudaStream_t st);
+                           void* ws, int* err, int num_sms, cudaStream_t st, const Epi& epi);
 // MXFP8: E4M3 operands with E8M0 scales per 32 columns, in scale atoms
 // [rows / 128][K / 128][512 B] (see qlin_quant_mxfp8).
 TcPlan plan_mxfp8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t* Wq, const uint8_t* ws_sf,
                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
-                            int num_sms, cudaStream_t st);
+                            int num_sms, cudaStream_t st, const Epi& epi);
 cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t st);
 // FP4: packed E2M1 operands (two per byte, K / 2 bytes per row) with MXFP4
@@ -174,7 +174,8 @@ cudaError_t launch_quant_mxfp8(const uint16_t* X, int64_t R, int64_t K, uint8_t*
 TcPlan plan_fp4_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_fp4_tc(const uint8_t* Xq, const uint8_t* xs, const float* sgx, const uint8_t* Wq,
                           const uint8_t* ws_sf, const float* sgw, uint16_t* Y, int64_t M, int64_t N, int64_t K,
-                          bool nv, const TcPlan& plan, void* ws, int* err, int num_sms, cudaStream_t st);
+                          bool nv, const TcPlan& plan, void* ws, int* err, int num_sms, cudaStream_t st,
+                          const Epi& epi);
 cudaError_t launch_quant_mxfp4(const uint16_t* X, int64_t R, int64_t K, uint8_t* codes, uint8_t* scales,
                                cudaStream_t st);
 cudaError_t launch_nvfp4_tensor_scale(const uint16_t* X, int64_t n, float* sg, int num_sms, cudaStream_t st);

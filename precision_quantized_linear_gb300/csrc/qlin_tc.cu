@@ -944,6 +944,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         const int64_t n = static_cast<int64_t>(un.nt) * kTileN + row;
         const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
         const bool direct = a.splits == 1;
+        const float bias_n = EPI ? epi_bias(a.epi, n) : 0.0f;
         const uint16_t* sp = a.scales + static_cast<int64_t>(un.nt) * KB * kTileN + row;  // [group][128 rows]
         float sn = un.nkb > 0 ? __half2float(__ushort_as_half(__ldg(sp + static_cast<int64_t>(un.kb0) * kTileN))) : 0.0f;
         float rr[BN];
@@ -993,7 +994,9 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const int64_t m = mbase + c0 + i;
-                box[i * kTileN + row] = m < a.M ? to_bf16(rr[c0 + i] * __ldg(a.sx + m)) : uint16_t(0);
+                float v = m < a.M ? rr[c0 + i] * __ldg(a.sx + m) : 0.0f;
+                if constexpr (EPI) v = epi_act(a.epi.act, v, bias_n);
+                box[i * kTileN + row] = m < a.M ? to_bf16(v) : uint16_t(0);
               }
               fence_proxy_async_smem();
               named_bar_epi();
@@ -1027,6 +1030,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
                 acc_v += __ldcg(p);
                 __stcg(p, 0.0f);
               }
+              if constexpr (EPI) acc_v = epi_act(a.epi.act, acc_v, bias_n);
               a.Y[m * a.N + n] = to_bf16(acc_v);
             }
             if (t == 0) a.counters[tile] = 0u;
@@ -1281,8 +1285,9 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         const Unit un = unit_of(a, u, KB);
         const int half = t >> 7, th = t & 127;
         const int cbase = half * 128;
-        const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
         const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
+        // bias of this thread's row (TMEM lane quad * 32 + lane), loaded while the MMAs run
+        const float bias_n = EPI ? epi_bias(a.epi, static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane) : 0.0f;
         const bool have =
             __all_sync(0xffffffffu, mbar_wait(&acc_full[0], ua & 1, kWaitLimitNs, &s_abort));
         if (!have) {
@@ -1304,8 +1309,12 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float x0 = have ? __uint_as_float(v[i >> 3][(2 * i) & 15]) * s_nv : 0.0f;
-            const float x1 = have ? __uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * s_nv : 0.0f;
+            float x0 = have ? __uint_as_float(v[i >> 3][(2 * i) & 15]) * s_nv : 0.0f;
+            float x1 = have ? __uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * s_nv : 0.0f;
+            if constexpr (EPI) {
+              x0 = epi_act(a.epi.act, x0, bias_n);
+              x1 = epi_act(a.epi.act, x1, bias_n);
+            }
             pk[c0 / 2 + i] = bf16x2_bits(__floats2bfloat162_rn(x0, x1));  // x0 in the low half
           }
         }
@@ -1752,9 +1761,19 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
                                 : launch_tc_bn<false, false>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
+template <bool EPI>
+static cudaError_t launch_w4a8_bn(const CUtensorMap& tx, const CUtensorMap& ty, const TcArgs& a, const TcPlan& plan,
+                                  void* ws, int num_sms, cudaStream_t st) {
+  switch (plan.bn) {
+    case 16: return launch_tc<16, true, 1, false, 128, EPI, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
+    case 32: return launch_tc<32, true, 1, false, 128, EPI, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
+    default: return launch_tc<64, true, 1, false, 128, EPI, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
+  }
+}
+
 cudaError_t launch_w4a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* codes, const uint16_t* scales,
                            const uint8_t* zeros, uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan,
-                           void* ws, int* err, int num_sms, cudaStream_t st) {
+                           void* ws, int* err, int num_sms, cudaStream_t st, const Epi& epi) {
   CUtensorMap tx, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, N * 2, kTileN, 16, false))
@@ -1771,16 +1790,25 @@ cudaError_t launch_w4a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* co
   a.M = M;
   a.N = N;
   a.K = K;
+  a.epi = epi;
+  return (epi.bias || epi.act) ? launch_w4a8_bn<true>(tx, ty, a, plan, ws, num_sms, st)
+                                : launch_w4a8_bn<false>(tx, ty, a, plan, ws, num_sms, st);
+}
+
+template <bool EPI>
+static cudaError_t launch_mxfp8_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const TcArgs& a,
+                                   const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   switch (plan.bn) {
-    case 16: return launch_tc<16, true, 1, false, 128, false, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
-    case 32: return launch_tc<32, true, 1, false, 128, false, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
-    default: return launch_tc<64, true, 1, false, 128, false, false, true>(tx, tx, ty, a, plan, ws, num_sms, st);
+    case 32: return launch_tc<32, false, 1, false, 128, EPI, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 64: return launch_tc<64, false, 1, false, 128, EPI, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 128: return launch_tc<128, false, 1, false, 128, EPI, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default: return launch_tc<256, false, 1, false, 128, EPI, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
   }
 }
 
 cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t* Wq, const uint8_t* ws_sf,
                             uint16_t* Y, int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err,
-                            int num_sms, cudaStream_t st) {
+                            int num_sms, cudaStream_t st, const Epi& epi) {
   CUtensorMap tx, tw, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, K, N, K, 128, 128)) return cudaErrorInvalidValue;
@@ -1794,23 +1822,20 @@ cudaError_t launch_mxfp8_tc(const uint8_t* Xq, const uint8_t* xs, const uint8_t*
   a.M = M;
   a.N = N;
   a.K = K;
-  switch (plan.bn) {
-    case 32: return launch_tc<32, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 64: return launch_tc<64, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 128: return launch_tc<128, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
-    default: return launch_tc<256, false, 1, false, 128, false, kMxF8>(tx, tw, ty, a, plan, ws, num_sms, st);
-  }
+  a.epi = epi;
+  return (epi.bias || epi.act) ? launch_mxfp8_bn<true>(tx, tw, ty, a, plan, ws, num_sms, st)
+                                : launch_mxfp8_bn<false>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
-template <int MX>
+template <int MX, bool EPI>
 static cudaError_t launch_fp4_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const TcArgs& a,
                                  const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
   switch (plan.bn) {
     case 32:  // only as the single token block: its scales start at column 0 of the token atom
       if (plan.mblocks != 1) return cudaErrorInvalidValue;
-      return launch_tc<32, false, 1, false, 128, false, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 128: return launch_tc<128, false, 1, false, 128, false, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 256: return launch_tc<256, false, 1, false, 128, false, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
+      return launch_tc<32, false, 1, false, 128, EPI, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 128: return launch_tc<128, false, 1, false, 128, EPI, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 256: return launch_tc<256, false, 1, false, 128, EPI, MX>(tx, tw, ty, a, plan, ws, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1818,7 +1843,8 @@ static cudaError_t launch_fp4_bn(const CUtensorMap& tx, const CUtensorMap& tw, c
 // MXFP4 (sgx == sgw == nullptr) and NVFP4: packed E2M1 operands, K / 2 bytes per row
 cudaError_t launch_fp4_tc(const uint8_t* Xq, const uint8_t* xs, const float* sgx, const uint8_t* Wq,
                           const uint8_t* ws_sf, const float* sgw, uint16_t* Y, int64_t M, int64_t N, int64_t K,
-                          bool nv, const TcPlan& plan, void* ws, int* err, int num_sms, cudaStream_t st) {
+                          bool nv, const TcPlan& plan, void* ws, int* err, int num_sms, cudaStream_t st,
+                          const Epi& epi) {
   CUtensorMap tx, tw, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K / 2, M, K / 2, 128, plan.bn))
     return cudaErrorInvalidValue;
@@ -1836,8 +1862,12 @@ cudaError_t launch_fp4_tc(const uint8_t* Xq, const uint8_t* xs, const float* sgx
   a.M = M;
   a.N = N;
   a.K = K;
-  return nv ? launch_fp4_bn<kNvF4>(tx, tw, ty, a, plan, ws, num_sms, st)
-            : launch_fp4_bn<kMxF4>(tx, tw, ty, a, plan, ws, num_sms, st);
+  a.epi = epi;
+  if (epi.bias || epi.act)
+    return nv ? launch_fp4_bn<kNvF4, true>(tx, tw, ty, a, plan, ws, num_sms, st)
+              : launch_fp4_bn<kMxF4, true>(tx, tw, ty, a, plan, ws, num_sms, st);
+  return nv ? launch_fp4_bn<kNvF4, false>(tx, tw, ty, a, plan, ws, num_sms, st)
+            : launch_fp4_bn<kMxF4, false>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,

@@ -5,8 +5,9 @@ reuse") and runs ``qlin_w4a16_gemm`` per call; ``W8A8Linear`` quantises the
 weights to E4M3 once and runs the fused per-token activation quantiser plus
 ``qlin_w8a8_fp8_gemm`` per call.  A layer built with a bias, or called with an
 activation, runs the ``*_gemm_fused`` calls instead: bias and activation are
-applied where the kernel writes Y.  Device memory comes from torch; every
-computation is a libqlin kernel.
+applied where the kernel writes Y (every layer here but the block-scaled FP8
+one takes them).  Device memory comes from torch; every computation is a
+libqlin kernel.
 """
 from __future__ import annotations
 
@@ -15,7 +16,8 @@ import torch
 from . import (ACT_NONE, OP_MXFP4_GEMM, OP_MXFP8_GEMM, OP_NVFP4_GEMM, OP_QUANT_W_FP8, OP_W4A8_GEMM, OP_W4A16_GEMM,
                OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_mx_scale_bytes, qlin_mxfp4_gemm, qlin_mxfp8_gemm,
                qlin_nvfp4_gemm, qlin_nvfp4_scale_bytes, qlin_nvfp4_tensor_scale, qlin_pack_w4, qlin_quant_mxfp4,
-               qlin_quant_mxfp8, qlin_quant_nvfp4, qlin_w4a8_gemm,
+               qlin_quant_mxfp8, qlin_quant_nvfp4, qlin_w4a8_gemm, qlin_w4a8_gemm_fused, qlin_mxfp8_gemm_fused,
+               qlin_mxfp4_gemm_fused, qlin_nvfp4_gemm_fused,
                qlin_quant_act_fp8, qlin_quant_act_fp8_blocks, qlin_quant_w_fp8, qlin_quant_w_fp8_blocks,
                qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w4a16_gemm_fused, qlin_w8a8_fp8_block_gemm,
                qlin_w8a8_fp8_gemm_ex, qlin_w8a8_fp8_gemm_fused, qlin_workspace_size)
@@ -86,8 +88,8 @@ class W4A8Linear(W4A16Linear):
     """W4A8: the packed INT4 weights of W4A16Linear (G = 128) times per-token E4M3
     activations from the fused amax quantiser."""
 
-    def __init__(self, W_bf16: torch.Tensor, symmetric: bool = False, stream=None):
-        super().__init__(W_bf16, G=128, symmetric=symmetric, stream=stream)
+    def __init__(self, W_bf16: torch.Tensor, symmetric: bool = False, stream=None, bias=None):
+        super().__init__(W_bf16, G=128, symmetric=symmetric, stream=stream, bias=bias)
 
     def quant_act(self, X_bf16: torch.Tensor, Xq=None, sx=None, stream=None):
         M, K = X_bf16.shape
@@ -98,18 +100,22 @@ class W4A8Linear(W4A16Linear):
         qlin_quant_act_fp8(_as_u16(X_bf16), M, K, Xq, sx, stream)
         return Xq, sx
 
-    def gemm(self, Xq, sx, Y=None, stream=None):
+    def gemm(self, Xq, sx, Y=None, stream=None, act: int = ACT_NONE):
         M = Xq.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
         buf, nb = self.ws.get(qlin_workspace_size(OP_W4A8_GEMM, M, self.N, self.K, 128))
-        qlin_w4a8_gemm(Xq, sx, self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N, self.K, 128, buf,
-                       nb, stream)
+        if self.bias is None and act == ACT_NONE:
+            qlin_w4a8_gemm(Xq, sx, self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N, self.K, 128,
+                           buf, nb, stream)
+        else:
+            qlin_w4a8_gemm_fused(Xq, sx, self.codes, self.scales, self.zeros, Y.view(torch.int16), M, self.N, self.K,
+                                 128, self.bias, act, buf, nb, stream)
         return Y
 
-    def __call__(self, X_bf16, Y=None, stream=None):
+    def __call__(self, X_bf16, Y=None, stream=None, act: int = ACT_NONE):
         Xq, sx = self.quant_act(X_bf16, stream=stream)
-        return self.gemm(Xq, sx, Y, stream)
+        return self.gemm(Xq, sx, Y, stream, act)
 
 
 class W8A8Linear:
@@ -190,9 +196,10 @@ class MXFP8Linear:
     """MXFP8 W8A8: E4M3 weights and activations with E8M0 scales per 32 columns,
     both block scales applied by the tensor cores."""
 
-    def __init__(self, W_bf16: torch.Tensor, stream=None):
+    def __init__(self, W_bf16: torch.Tensor, stream=None, bias=None):
         N, K = W_bf16.shape
         self.N, self.K = N, K
+        self.bias = _bias_bf16(bias, N)
         dev = W_bf16.device
         self.Wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
         self.ws_sf = torch.empty(qlin_mx_scale_bytes(N, K), dtype=torch.uint8, device=dev)
@@ -208,26 +215,31 @@ class MXFP8Linear:
         qlin_quant_mxfp8(_as_u16(X_bf16), M, K, Xq, xs, stream)
         return Xq, xs
 
-    def gemm(self, Xq, xs, Y=None, stream=None):
+    def gemm(self, Xq, xs, Y=None, stream=None, act: int = ACT_NONE):
         M = Xq.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
         buf, nb = self.ws.get(qlin_workspace_size(OP_MXFP8_GEMM, M, self.N, self.K))
-        qlin_mxfp8_gemm(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        if self.bias is None and act == ACT_NONE:
+            qlin_mxfp8_gemm(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        else:
+            qlin_mxfp8_gemm_fused(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, self.bias, act,
+                                  buf, nb, stream)
         return Y
 
-    def __call__(self, X_bf16, Y=None, stream=None):
+    def __call__(self, X_bf16, Y=None, stream=None, act: int = ACT_NONE):
         Xq, xs = self.quant_act(X_bf16, stream=stream)
-        return self.gemm(Xq, xs, Y, stream)
+        return self.gemm(Xq, xs, Y, stream, act)
 
 
 class MXFP4Linear:
     """MXFP4 W4A4: E2M1 weights and activations (two per byte) with E8M0 scales
     per 32 columns, both block scales applied by the tensor cores."""
 
-    def __init__(self, W_bf16: torch.Tensor, stream=None):
+    def __init__(self, W_bf16: torch.Tensor, stream=None, bias=None):
         N, K = W_bf16.shape
         self.N, self.K = N, K
+        self.bias = _bias_bf16(bias, N)
         dev = W_bf16.device
         self.Wq = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
         self.ws_sf = torch.empty(qlin_mx_scale_bytes(N, K), dtype=torch.uint8, device=dev)
@@ -243,17 +255,21 @@ class MXFP4Linear:
         qlin_quant_mxfp4(_as_u16(X_bf16), M, K, Xq, xs, stream)
         return Xq, xs
 
-    def gemm(self, Xq, xs, Y=None, stream=None):
+    def gemm(self, Xq, xs, Y=None, stream=None, act: int = ACT_NONE):
         M = Xq.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
         buf, nb = self.ws.get(qlin_workspace_size(OP_MXFP4_GEMM, M, self.N, self.K))
-        qlin_mxfp4_gemm(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        if self.bias is None and act == ACT_NONE:
+            qlin_mxfp4_gemm(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        else:
+            qlin_mxfp4_gemm_fused(Xq, xs, self.Wq, self.ws_sf, Y.view(torch.int16), M, self.N, self.K, self.bias, act,
+                                  buf, nb, stream)
         return Y
 
-    def __call__(self, X_bf16, Y=None, stream=None):
+    def __call__(self, X_bf16, Y=None, stream=None, act: int = ACT_NONE):
         Xq, xs = self.quant_act(X_bf16, stream=stream)
-        return self.gemm(Xq, xs, Y, stream)
+        return self.gemm(Xq, xs, Y, stream, act)
 
 
 class NVFP4Linear:
@@ -263,9 +279,10 @@ class NVFP4Linear:
     is computed on the device for every call (an amax reduction before the
     quantiser)."""
 
-    def __init__(self, W_bf16: torch.Tensor, stream=None):
+    def __init__(self, W_bf16: torch.Tensor, stream=None, bias=None):
         N, K = W_bf16.shape
         self.N, self.K = N, K
+        self.bias = _bias_bf16(bias, N)
         dev = W_bf16.device
         W = _as_u16(W_bf16.contiguous())
         self.sgw = torch.empty(4, dtype=torch.float32, device=dev)
@@ -289,15 +306,19 @@ class NVFP4Linear:
         qlin_quant_nvfp4(X, M, K, sgx, Xq, xs, stream)
         return Xq, xs, sgx
 
-    def gemm(self, Xq, xs, sgx, Y=None, stream=None):
+    def gemm(self, Xq, xs, sgx, Y=None, stream=None, act: int = ACT_NONE):
         M = Xq.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
         buf, nb = self.ws.get(qlin_workspace_size(OP_NVFP4_GEMM, M, self.N, self.K))
-        qlin_nvfp4_gemm(Xq, xs, sgx, self.Wq, self.ws_sf, self.sgw, Y.view(torch.int16), M, self.N, self.K, buf, nb,
-                        stream)
+        if self.bias is None and act == ACT_NONE:
+            qlin_nvfp4_gemm(Xq, xs, sgx, self.Wq, self.ws_sf, self.sgw, Y.view(torch.int16), M, self.N, self.K, buf,
+                            nb, stream)
+        else:
+            qlin_nvfp4_gemm_fused(Xq, xs, sgx, self.Wq, self.ws_sf, self.sgw, Y.view(torch.int16), M, self.N, self.K,
+                                  self.bias, act, buf, nb, stream)
         return Y
 
-    def __call__(self, X_bf16, Y=None, stream=None):
+    def __call__(self, X_bf16, Y=None, stream=None, act: int = ACT_NONE):
         Xq, xs, sgx = self.quant_act(X_bf16, stream=stream)
-        return self.gemm(Xq, xs, sgx, Y, stream)
+        return self.gemm(Xq, xs, sgx, Y, stream, act)

@@ -1,6 +1,7 @@
 """GPU parity of the fused output epilogue (bias + activation) against the oracle.
 
-Y = bf16(act(acc + bias[n])) on every kernel path of both GEMMs.  Bar: the
+Y = bf16(act(acc + bias[n])) on every kernel path of the W4A16 and W8A8 GEMMs,
+and on every tile kind of the MXFP8, MXFP4, NVFP4 and W4A8 GEMMs.  Bar: the
 GEMM bound carried through the activation (slope <= 1.13 for GELU, 1.10 for
 SiLU, 1 for ReLU) plus the BF16 rounding of the output:
     |Y - Y_ref| <= 1.13 * 2e-3 * ||X_deq[m]|| * ||W_deq[n]|| + 2^-8 |Y_ref|
@@ -12,7 +13,10 @@ import torch
 import oracle
 import precision_quantized_linear_gb300 as q
 from precision_quantized_linear_gb300 import synthetic as syn
-from precision_quantized_linear_gb300.layers import W4A16Linear, W8A8Linear
+from precision_quantized_linear_gb300.layers import (MXFP4Linear, MXFP8Linear, NVFP4Linear, W4A8Linear, W4A16Linear,
+                                                      W8A8Linear)
+
+from _parity import blocks, w4_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -100,3 +104,66 @@ def test_fused_rejects_bad_arguments():
         q.qlin_w4a16_gemm_fused(X.view(torch.int16), lin.codes, lin.scales, lin.zeros, Y.view(torch.int16), M, N, K,
                                 128, b[1:].data_ptr(), q.ACT_RELU, None, 0, q.PATH_AUTO)
     assert e.value.status == 3  # QLIN_ERR_MISALIGNED: bias not 16-byte aligned
+
+
+# ------------------------------------------------------------------ block formats and W4A8
+# The same epilogue on the MXFP8, MXFP4, NVFP4 and W4A8 GEMMs, on every tile
+# kind they plan: the single token block of up to 32 tokens, 64- / 128-token
+# tiles, split K ranges (the reduction applies it), and the 256-token tiles of
+# the block formats, whose epilogue drains the single accumulator into
+# registers before writing.  (M, N, K, activation, bias); the dispatch query
+# asserts the tile each case is meant to reach.
+FMT_CASES = [(16, 512, 1024, q.ACT_SILU, True), (100, 512, 1024, q.ACT_GELU, True),
+             (8, 512, 14336, q.ACT_RELU, False), (2048, 4096, 4096, q.ACT_NONE, True)]
+FMT_OPS = {"mxfp8": q.OP_MXFP8_GEMM, "mxfp4": q.OP_MXFP4_GEMM, "nvfp4": q.OP_NVFP4_GEMM, "w4a8": q.OP_W4A8_GEMM}
+
+
+def _fmt_oracle(fmt, X, W):
+    """(reference of rows ms x columns ns, X dequantised row norms, W dequantised norms of rows ns)."""
+    if fmt == "mxfp8":
+        Xq, xs = oracle.quant_mxfp8_rows(X)
+        Wq, ws = oracle.quant_mxfp8_rows(W)
+        xn = np.linalg.norm(oracle.mx_dequant(Xq, xs), axis=1)
+        return (lambda ms, ns: oracle.w8a8_mx_full(Xq[ms], xs[ms], Wq[ns], ws[ns]), xn,
+                lambda ns: np.linalg.norm(oracle.mx_dequant(Wq[ns], ws[ns]), axis=1))
+    if fmt == "mxfp4":
+        Xq, xs = oracle.quant_mxfp4_rows(X)
+        Wq, ws = oracle.quant_mxfp4_rows(W)
+        xn = np.linalg.norm(oracle.mxfp4_dequant(Xq, xs), axis=1)
+        return (lambda ms, ns: oracle.w4a4_mx_full(Xq[ms], xs[ms], Wq[ns], ws[ns]), xn,
+                lambda ns: np.linalg.norm(oracle.mxfp4_dequant(Wq[ns], ws[ns]), axis=1))
+    if fmt == "nvfp4":
+        sgx, sgw = oracle.nvfp4_global_scale(X), oracle.nvfp4_global_scale(W)
+        Xq, xs = oracle.quant_nvfp4_rows(X, sgx)
+        Wq, ws = oracle.quant_nvfp4_rows(W, sgw)
+        xn = np.linalg.norm(oracle.nvfp4_dequant(Xq, xs, sgx), axis=1)
+        return (lambda ms, ns: oracle.w4a4_nv_full(Xq[ms], xs[ms], sgx, Wq[ns], ws[ns], sgw), xn,
+                lambda ns: np.linalg.norm(oracle.nvfp4_dequant(Wq[ns], ws[ns], sgw), axis=1))
+    Xq, sx = oracle.quant_fp8_rows(X)
+    wq = oracle.quantize_w4(W)
+    xn = np.linalg.norm(oracle.e4m3_table()[Xq] * sx.astype(np.float64)[:, None], axis=1)
+    return (lambda ms, ns: oracle.w4a8_full(Xq[ms], sx[ms], w4_rows(wq, ns)), xn,
+            lambda ns: np.linalg.norm(oracle.dequant_w4(w4_rows(wq, ns)), axis=1))
+
+
+@pytest.mark.parametrize("fmt", list(FMT_OPS))
+@pytest.mark.parametrize("case", FMT_CASES, ids=["m%d_n%d_k%d" % c[:3] for c in FMT_CASES])
+def test_block_formats_fused_epilogue(fmt, case):
+    M, N, K, act, with_bias = case
+    plan = q.qlin_plan_info(FMT_OPS[fmt], M, N, K)
+    want = {16: 16 if fmt == "w4a8" else 32, 100: 64 if fmt in ("w4a8", "mxfp8") else 128,
+            8: 16 if fmt == "w4a8" else 32, 2048: 64 if fmt == "w4a8" else 256}[M]
+    assert plan["tokens_per_tile"] == want and (plan["splits"] > 1) == (K == 14336), plan
+    seed = M + N + K + act + len(fmt)
+    W = syn.make_weight(N, K, seed=seed)
+    X = syn.make_act(M, K, seed=seed + 1, token_outlier_frac=0.01)
+    bias = _bias(N, seed=seed + 2) if with_bias else None
+    dbias = to_dev(bias).view(torch.bfloat16) if bias is not None else None
+    dW, dX = to_dev(W).view(torch.bfloat16), to_dev(X).view(torch.bfloat16)
+    lin = {"mxfp8": MXFP8Linear, "mxfp4": MXFP4Linear, "nvfp4": NVFP4Linear, "w4a8": W4A8Linear}[fmt](dW, bias=dbias)
+    Y = lin(dX, act=act).float().cpu().numpy().astype(np.float64)
+    ref, xn, wn_of = _fmt_oracle(fmt, X, W)
+    sel = [(np.arange(M), np.arange(N))] if M * N <= 1 << 16 else blocks(M, N, plan["tokens_per_tile"], 128, seed)
+    for ms, ns in sel:
+        Yref = oracle.epilogue(ref(ms, ns), None if bias is None else bias[ns], act)
+        check(Y[np.ix_(ms, ns)], Yref, xn[ms], wn_of(ns))
