@@ -84,8 +84,7 @@ typedef enum {
 #define QLIN_OP_MXFP4_GEMM 7
 #define QLIN_OP_NVFP4_GEMM 8
 
-/* Activation of the fused output epilogue (qlin_*_gemm_fused: W4A16, W8A8,
- * W4A8, MXFP8, MXFP4 and NVFP4; not the block-scaled FP8 GEMM). */
+/* Activation of the fused output epilogue (qlin_*_gemm_fused, every GEMM). */
 #define QLIN_ACT_NONE 0
 #define QLIN_ACT_RELU 1 /* max(v, 0)                                   */
 #define QLIN_ACT_SILU 2 /* v / (1 + exp(-v))                           */
@@ -259,6 +258,14 @@ qlin_status_t qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, 
 qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
                              void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
                              void* stream);
+
+/* Block-scaled FP8 with the fused output epilogue: Y[m][n] = bf16( act(
+ * y[m][n] + bias[n] ) ), y the FP32 value qlin_w8a8_fp8_block_gemm rounds;
+ * bias and act as in qlin_w4a16_gemm_fused. */
+qlin_status_t qlin_w8a8_fp8_block_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3,
+                                             const float* sw, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                                             const void* bias_bf16, int act, void* workspace, size_t ws_bytes,
+                                             void* stream);
 
 /*
  * W4A8 linear layer ([LP] S1 precision manifest "W4A8: INT4 weights, INT8/FP8

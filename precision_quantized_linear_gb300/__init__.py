@@ -34,7 +34,7 @@ __all__ = [
     "KERNEL_W4A8_TC", "OP_MXFP4_GEMM", "OP_NVFP4_GEMM", "KERNEL_MXFP4_TC", "KERNEL_NVFP4_TC",
     "qlin_nvfp4_scale_bytes", "qlin_quant_mxfp4", "qlin_nvfp4_tensor_scale", "qlin_quant_nvfp4", "qlin_mxfp4_gemm",
     "qlin_nvfp4_gemm", "qlin_w4a8_gemm_fused", "qlin_mxfp8_gemm_fused", "qlin_mxfp4_gemm_fused",
-    "qlin_nvfp4_gemm_fused",
+    "qlin_nvfp4_gemm_fused", "qlin_w8a8_fp8_block_gemm_fused",
 ]
 
 OP_W4A16_GEMM, OP_W8A8_GEMM, OP_QUANT_W_FP8, OP_W8A8_BLOCK_GEMM, OP_MXFP8_GEMM, OP_W4A8_GEMM = 1, 2, 3, 4, 5, 6
@@ -91,6 +91,7 @@ _SIGS = {
     "qlin_mxfp8_gemm_fused": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _p],
     "qlin_mxfp4_gemm_fused": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _p],
     "qlin_nvfp4_gemm_fused": [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _p],
+    "qlin_w8a8_fp8_block_gemm_fused": [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, _int, _p, _sz, _p],
 }
 
 
@@ -353,3 +354,9 @@ def qlin_w4a16_gemv_noalloc(X, codes, scales, zeros, Y, M, N, K, G, stream=None)
     argument, nothing allocated): for callers that cannot allocate device memory."""
     return _check(load().qlin_w4a16_gemv_noalloc(_ptr(X), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(Y), M, N, K,
                                                  G, _stream(stream)), "qlin_w4a16_gemv_noalloc")
+
+
+def qlin_w8a8_fp8_block_gemm_fused(Xq, sx, Wq, sw, Y, M, N, K, bias, act, workspace, ws_bytes, stream=None):
+    return _check(load().qlin_w8a8_fp8_block_gemm_fused(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(Y), M, N, K,
+                                                        _ptr(bias), act, _ptr(workspace), ws_bytes,
+                                                        _stream(stream)), "qlin_w8a8_fp8_block_gemm_fused")

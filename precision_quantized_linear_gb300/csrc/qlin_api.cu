@@ -537,9 +537,9 @@ qlin_status_t qlin_quant_w_fp8_blocks(const void* W_bf16, int64_t N, int64_t K, 
                                                  static_cast<uint8_t*>(Wq_e4m3), sw, static_cast<cudaStream_t>(stream)));
 }
 
-qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
-                             void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
-                             void* stream) {
+static qlin_status_t w8a8_block_impl(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                                     void* Y_bf16, int64_t M, int64_t N, int64_t K, const Epi& epi, void* workspace,
+                                     size_t ws_bytes, void* stream) {
   qlin_status_t st = check_shape(M, N, K);
   if (st != QLIN_OK) return st;
   if (M == 0) return QLIN_OK;
@@ -555,7 +555,23 @@ qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, con
   return launch_status(launch_w8a8_block_tc(static_cast<const uint8_t*>(Xq_e4m3), sx,
                                             static_cast<const uint8_t*>(Wq_e4m3), sw, static_cast<uint16_t*>(Y_bf16),
                                             M, N, K, p, workspace, d->err, d->num_sms,
-                                            static_cast<cudaStream_t>(stream)));
+                                            static_cast<cudaStream_t>(stream), epi));
+}
+
+qlin_status_t qlin_w8a8_fp8_block_gemm(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3, const float* sw,
+                             void* Y_bf16, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  return w8a8_block_impl(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, Epi{}, workspace, ws_bytes, stream);
+}
+
+qlin_status_t qlin_w8a8_fp8_block_gemm_fused(const void* Xq_e4m3, const float* sx, const void* Wq_e4m3,
+                                             const float* sw, void* Y_bf16, int64_t M, int64_t N, int64_t K,
+                                             const void* bias_bf16, int act, void* workspace, size_t ws_bytes,
+                                             void* stream) {
+  Epi epi;
+  const qlin_status_t st = make_epi(bias_bf16, act, &epi);
+  if (st != QLIN_OK) return st;
+  return w8a8_block_impl(Xq_e4m3, sx, Wq_e4m3, sw, Y_bf16, M, N, K, epi, workspace, ws_bytes, stream);
 }
 
 static qlin_status_t w4a8_impl(const void* Xq_e4m3, const float* sx, const void* codes, const void* scales_f16,

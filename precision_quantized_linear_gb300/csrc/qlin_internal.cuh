@@ -154,7 +154,7 @@ cudaError_t launch_w8a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq
 // FP8 block scaling: sx = [K/128][M], sw = [N/128][K/128] FP32 block scales.
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                                  int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
-                                 cudaStream_t st);
+                                 cudaStream_t st, const Epi& epi);
 // W4A8: packed INT4 weights (G = 128) dequantised to E4M3, times per-token E4M3 activations.
 TcPlan plan_w4a8_tc(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_w4a8_tc(const uint8_t* Xq, const float* sx, const uint8_t* codes, const uint16_t* scales,

@@ -182,7 +182,7 @@ struct TcArgs {
                      // read again by every later token block; otherwise they are streamed (evict-first)
   int G;             // W4A16 quantisation group (32, 64, 128, or K for per-channel scales)
   int gshift;        // log2 G; 31 for per-channel scales, so that every column maps to group 0
-  Epi epi;           // output epilogue (bias, activation); not used by block scaling
+  Epi epi;           // output epilogue (bias, activation) of the *_fused calls
 };
 
 __device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
@@ -1103,6 +1103,10 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
             uint4* yrow = reinterpret_cast<uint4*>(a.Y + m * a.N + n0);
 #pragma unroll
             for (int c = 0; c < kCw; c += 8) {
+              if constexpr (EPI) {  // bias of columns n0 + c .. (one weight row each)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[c + i] = epi_apply(a.epi, r[c + i], n0 + c + i);
+              }
               uint32_t w[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i)
@@ -1136,6 +1140,12 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
                   acc_v.w += x.w;
                   __stcg(pp, make_float4(0.0f, 0.0f, 0.0f, 0.0f));
                 }
+                if constexpr (EPI) {
+                  acc_v.x = epi_apply(a.epi, acc_v.x, n0 + c);
+                  acc_v.y = epi_apply(a.epi, acc_v.y, n0 + c + 1);
+                  acc_v.z = epi_apply(a.epi, acc_v.z, n0 + c + 2);
+                  acc_v.w = epi_apply(a.epi, acc_v.w, n0 + c + 3);
+                }
                 const uint32_t lo = static_cast<uint32_t>(to_bf16(acc_v.x)) | (static_cast<uint32_t>(to_bf16(acc_v.y)) << 16);
                 const uint32_t hi = static_cast<uint32_t>(to_bf16(acc_v.z)) | (static_cast<uint32_t>(to_bf16(acc_v.w)) << 16);
                 *reinterpret_cast<uint2*>(a.Y + m * a.N + n0 + c) = make_uint2(lo, hi);
@@ -1160,6 +1170,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
         const int64_t n = static_cast<int64_t>(un.nt) * kTileN + quad * 32 + lane;
         const int64_t mbase = static_cast<int64_t>(un.mb) * BN;
         const bool direct = a.splits == 1;
+        const float bias_n = EPI ? epi_bias(a.epi, n) : 0.0f;
         // thread te < BN stages the factor of token mbase + te; the next K
         // block's factor is loaded while the current one is promoted
         const int64_t mt = mbase + te;
@@ -1225,7 +1236,8 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
               if (th == 0) bulk_wait_read<1>();
               named_bar(2 + half, 128);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) box[i * kTileN + quad * 32 + lane] = to_bf16(r[c0 + i]);
+              for (int i = 0; i < 16; ++i)
+                box[i * kTileN + quad * 32 + lane] = to_bf16(EPI ? epi_act(a.epi.act, r[c0 + i], bias_n) : r[c0 + i]);
               fence_proxy_async_smem();
               named_bar(2 + half, 128);
               if (th == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(m0));
@@ -1268,7 +1280,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const int64_t m = mbase + c0 + i;
-                if (m < a.M) a.Y[m * a.N + n] = to_bf16(acc_v[i]);
+                if (m < a.M) a.Y[m * a.N + n] = to_bf16(EPI ? epi_act(a.epi.act, acc_v[i], bias_n) : acc_v[i]);
               }
             }
             if (te == 0) a.counters[tile] = 0u;
@@ -1870,9 +1882,22 @@ cudaError_t launch_fp4_tc(const uint8_t* Xq, const uint8_t* xs, const float* sgx
             : launch_fp4_bn<kMxF4, false>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
+template <bool EPI>
+static cudaError_t launch_block_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const TcArgs& a,
+                                   const TcPlan& plan, void* ws, int num_sms, cudaStream_t st) {
+  switch (plan.bn) {
+    case 16: return launch_tc<16, false, 1, true, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 32: return launch_tc<32, false, 1, true, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    case 64: return launch_tc<64, false, 1, true, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+    default:
+      return plan.wn == 256 ? launch_tc<128, false, 1, true, 256, EPI>(tx, tw, ty, a, plan, ws, num_sms, st)
+                            : launch_tc<128, false, 1, true, 128, EPI>(tx, tw, ty, a, plan, ws, num_sms, st);
+  }
+}
+
 cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, uint16_t* Y,
                                  int64_t M, int64_t N, int64_t K, const TcPlan& plan, void* ws, int* err, int num_sms,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, const Epi& epi) {
   CUtensorMap tx, tw, ty;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Xq, K, M, K, 128, plan.bn)) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, K, N, K, 128, 128)) return cudaErrorInvalidValue;
@@ -1886,14 +1911,9 @@ cudaError_t launch_w8a8_block_tc(const uint8_t* Xq, const float* sx, const uint8
   a.M = M;
   a.N = N;
   a.K = K;
-  switch (plan.bn) {
-    case 16: return launch_tc<16, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 32: return launch_tc<32, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    case 64: return launch_tc<64, false, 1, true>(tx, tw, ty, a, plan, ws, num_sms, st);
-    default:
-      return plan.wn == 256 ? launch_tc<128, false, 1, true, 256>(tx, tw, ty, a, plan, ws, num_sms, st)
-                            : launch_tc<128, false, 1, true, 128>(tx, tw, ty, a, plan, ws, num_sms, st);
-  }
+  a.epi = epi;
+  return (epi.bias || epi.act) ? launch_block_bn<true>(tx, tw, ty, a, plan, ws, num_sms, st)
+                                : launch_block_bn<false>(tx, tw, ty, a, plan, ws, num_sms, st);
 }
 
 }  // namespace qlin

@@ -5,9 +5,8 @@ reuse") and runs ``qlin_w4a16_gemm`` per call; ``W8A8Linear`` quantises the
 weights to E4M3 once and runs the fused per-token activation quantiser plus
 ``qlin_w8a8_fp8_gemm`` per call.  A layer built with a bias, or called with an
 activation, runs the ``*_gemm_fused`` calls instead: bias and activation are
-applied where the kernel writes Y (every layer here but the block-scaled FP8
-one takes them).  Device memory comes from torch; every computation is a
-libqlin kernel.
+applied where the kernel writes Y (every layer here takes them).  Device
+memory comes from torch; every computation is a libqlin kernel.
 """
 from __future__ import annotations
 
@@ -17,7 +16,7 @@ from . import (ACT_NONE, OP_MXFP4_GEMM, OP_MXFP8_GEMM, OP_NVFP4_GEMM, OP_QUANT_W
                OP_W8A8_BLOCK_GEMM, OP_W8A8_GEMM, PATH_AUTO, qlin_mx_scale_bytes, qlin_mxfp4_gemm, qlin_mxfp8_gemm,
                qlin_nvfp4_gemm, qlin_nvfp4_scale_bytes, qlin_nvfp4_tensor_scale, qlin_pack_w4, qlin_quant_mxfp4,
                qlin_quant_mxfp8, qlin_quant_nvfp4, qlin_w4a8_gemm, qlin_w4a8_gemm_fused, qlin_mxfp8_gemm_fused,
-               qlin_mxfp4_gemm_fused, qlin_nvfp4_gemm_fused,
+               qlin_mxfp4_gemm_fused, qlin_nvfp4_gemm_fused, qlin_w8a8_fp8_block_gemm_fused,
                qlin_quant_act_fp8, qlin_quant_act_fp8_blocks, qlin_quant_w_fp8, qlin_quant_w_fp8_blocks,
                qlin_w4_packed_sizes, qlin_w4a16_gemm_ex, qlin_w4a16_gemm_fused, qlin_w8a8_fp8_block_gemm,
                qlin_w8a8_fp8_gemm_ex, qlin_w8a8_fp8_gemm_fused, qlin_workspace_size)
@@ -161,9 +160,10 @@ class W8A8Linear:
 class W8A8BlockLinear:
     """FP8 W8A8 with block scaling: 128 x 128 weight blocks, 1 x 128 activation blocks."""
 
-    def __init__(self, W_bf16: torch.Tensor, stream=None):
+    def __init__(self, W_bf16: torch.Tensor, stream=None, bias=None):
         N, K = W_bf16.shape
         self.N, self.K = N, K
+        self.bias = _bias_bf16(bias, N)
         dev = W_bf16.device
         self.Wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
         self.sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
@@ -179,17 +179,21 @@ class W8A8BlockLinear:
         qlin_quant_act_fp8_blocks(_as_u16(X_bf16), M, K, Xq, sx, stream)
         return Xq, sx
 
-    def gemm(self, Xq, sx, Y=None, stream=None):
+    def gemm(self, Xq, sx, Y=None, stream=None, act: int = ACT_NONE):
         M = Xq.shape[0]
         if Y is None:
             Y = torch.empty((M, self.N), dtype=torch.bfloat16, device=Xq.device)
         buf, nb = self.ws.get(qlin_workspace_size(OP_W8A8_BLOCK_GEMM, M, self.N, self.K))
-        qlin_w8a8_fp8_block_gemm(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        if self.bias is None and act == ACT_NONE:
+            qlin_w8a8_fp8_block_gemm(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, buf, nb, stream)
+        else:
+            qlin_w8a8_fp8_block_gemm_fused(Xq, sx, self.Wq, self.sw, Y.view(torch.int16), M, self.N, self.K, self.bias,
+                                           act, buf, nb, stream)
         return Y
 
-    def __call__(self, X_bf16, Y=None, stream=None):
+    def __call__(self, X_bf16, Y=None, stream=None, act: int = ACT_NONE):
         Xq, sx = self.quant_act(X_bf16, stream=stream)
-        return self.gemm(Xq, sx, Y, stream)
+        return self.gemm(Xq, sx, Y, stream, act)
 
 
 class MXFP8Linear:

@@ -14,7 +14,7 @@ import oracle
 import precision_quantized_linear_gb300 as q
 from precision_quantized_linear_gb300 import synthetic as syn
 from precision_quantized_linear_gb300.layers import (MXFP4Linear, MXFP8Linear, NVFP4Linear, W4A8Linear, W4A16Linear,
-                                                      W8A8Linear)
+                                                      W8A8BlockLinear, W8A8Linear)
 
 from _parity import blocks, w4_rows
 
@@ -115,7 +115,12 @@ def test_fused_rejects_bad_arguments():
 # asserts the tile each case is meant to reach.
 FMT_CASES = [(16, 512, 1024, q.ACT_SILU, True), (100, 512, 1024, q.ACT_GELU, True),
              (8, 512, 14336, q.ACT_RELU, False), (2048, 4096, 4096, q.ACT_NONE, True)]
-FMT_OPS = {"mxfp8": q.OP_MXFP8_GEMM, "mxfp4": q.OP_MXFP4_GEMM, "nvfp4": q.OP_NVFP4_GEMM, "w4a8": q.OP_W4A8_GEMM}
+FMT_OPS = {"mxfp8": q.OP_MXFP8_GEMM, "mxfp4": q.OP_MXFP4_GEMM, "nvfp4": q.OP_NVFP4_GEMM, "w4a8": q.OP_W4A8_GEMM,
+           "w8a8b": q.OP_W8A8_BLOCK_GEMM}
+# token tile each (format, M) of FMT_CASES is planned onto
+FMT_TILE = {"mxfp8": {16: 32, 100: 64, 8: 32, 2048: 256}, "mxfp4": {16: 32, 100: 128, 8: 32, 2048: 256},
+            "nvfp4": {16: 32, 100: 128, 8: 32, 2048: 256}, "w4a8": {16: 16, 100: 64, 8: 16, 2048: 64},
+            "w8a8b": {16: 16, 100: 128, 8: 16, 2048: 128}}
 
 
 def _fmt_oracle(fmt, X, W):
@@ -139,6 +144,15 @@ def _fmt_oracle(fmt, X, W):
         xn = np.linalg.norm(oracle.nvfp4_dequant(Xq, xs, sgx), axis=1)
         return (lambda ms, ns: oracle.w4a4_nv_full(Xq[ms], xs[ms], sgx, Wq[ns], ws[ns], sgw), xn,
                 lambda ns: np.linalg.norm(oracle.nvfp4_dequant(Wq[ns], ws[ns], sgw), axis=1))
+    if fmt == "w8a8b":  # 1 x 128 token blocks (sx [K/128][M]), 128 x 128 weight blocks (sw [N/128][K/128])
+        tab = oracle.e4m3_table()
+        Xq, sx = oracle.quant_fp8_act_blocks(X)
+        Wq, sw = oracle.quant_fp8_weight_blocks(W)
+        xn = np.linalg.norm(tab[Xq] * np.repeat(sx.T.astype(np.float64), 128, axis=1), axis=1)
+        swr = lambda ns: sw[ns[0] // 128: ns[-1] // 128 + 1]  # the scale rows of whole 128-row tiles ns
+        return (lambda ms, ns: oracle.w8a8_blocks_full(Xq[ms], sx[:, ms], Wq[ns], swr(ns)), xn,
+                lambda ns: np.linalg.norm(tab[Wq[ns]] * np.repeat(np.repeat(swr(ns).astype(np.float64), 128, axis=0),
+                                                                 128, axis=1), axis=1))
     Xq, sx = oracle.quant_fp8_rows(X)
     wq = oracle.quantize_w4(W)
     xn = np.linalg.norm(oracle.e4m3_table()[Xq] * sx.astype(np.float64)[:, None], axis=1)
@@ -151,19 +165,35 @@ def _fmt_oracle(fmt, X, W):
 def test_block_formats_fused_epilogue(fmt, case):
     M, N, K, act, with_bias = case
     plan = q.qlin_plan_info(FMT_OPS[fmt], M, N, K)
-    want = {16: 16 if fmt == "w4a8" else 32, 100: 64 if fmt in ("w4a8", "mxfp8") else 128,
-            8: 16 if fmt == "w4a8" else 32, 2048: 64 if fmt == "w4a8" else 256}[M]
-    assert plan["tokens_per_tile"] == want and (plan["splits"] > 1) == (K == 14336), plan
+    assert plan["tokens_per_tile"] == FMT_TILE[fmt][M] and (plan["splits"] > 1) == (K == 14336), plan
     seed = M + N + K + act + len(fmt)
     W = syn.make_weight(N, K, seed=seed)
     X = syn.make_act(M, K, seed=seed + 1, token_outlier_frac=0.01)
     bias = _bias(N, seed=seed + 2) if with_bias else None
     dbias = to_dev(bias).view(torch.bfloat16) if bias is not None else None
     dW, dX = to_dev(W).view(torch.bfloat16), to_dev(X).view(torch.bfloat16)
-    lin = {"mxfp8": MXFP8Linear, "mxfp4": MXFP4Linear, "nvfp4": NVFP4Linear, "w4a8": W4A8Linear}[fmt](dW, bias=dbias)
+    lin = {"mxfp8": MXFP8Linear, "mxfp4": MXFP4Linear, "nvfp4": NVFP4Linear, "w4a8": W4A8Linear,
+           "w8a8b": W8A8BlockLinear}[fmt](dW, bias=dbias)
     Y = lin(dX, act=act).float().cpu().numpy().astype(np.float64)
     ref, xn, wn_of = _fmt_oracle(fmt, X, W)
     sel = [(np.arange(M), np.arange(N))] if M * N <= 1 << 16 else blocks(M, N, plan["tokens_per_tile"], 128, seed)
     for ms, ns in sel:
         Yref = oracle.epilogue(ref(ms, ns), None if bias is None else bias[ns], act)
         check(Y[np.ix_(ms, ns)], Yref, xn[ms], wn_of(ns))
+
+
+def test_block_scaled_fused_epilogue_token_major_split():
+    """Block-scaled FP8 at 128 tokens runs token-major (thread = token, bias per
+    column); with two K ranges the reduction applies the epilogue."""
+    M, N, K, act = 100, 512, 14336, q.ACT_SILU
+    plan = q.qlin_plan_info(q.OP_W8A8_BLOCK_GEMM, M, N, K)
+    assert (plan["tokens_per_tile"], plan["splits"]) == (128, 2), plan
+    W = syn.make_weight(N, K, seed=91)
+    X = syn.make_act(M, K, seed=92, token_outlier_frac=0.01)
+    bias = _bias(N, seed=93)
+    lin = W8A8BlockLinear(to_dev(W).view(torch.bfloat16), bias=to_dev(bias).view(torch.bfloat16))
+    Y = lin(to_dev(X).view(torch.bfloat16), act=act).float().cpu().numpy().astype(np.float64)
+    ref, xn, wn_of = _fmt_oracle("w8a8b", X, W)
+    ns = np.arange(N)
+    check(Y, oracle.epilogue(ref(np.arange(M), ns), bias, act), xn, wn_of(ns))
+
