@@ -681,9 +681,10 @@ __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint16_t* __rest
   const int64_t item0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kMxItems;
   if (item0 >= total) return;  // whole warps only
   // item0 + u is row rr[u], chunk cc[u]: one division per warp, then a carry
-  int64_t rr[kMxItems], cc[kMxItems];
-  rr[0] = item0 / nc;
-  cc[0] = item0 - rr[0] * nc;
+  // (32-bit: rows < 2^31 and chunks < 2^23, as the call checks)
+  int rr[kMxItems], cc[kMxItems];
+  rr[0] = static_cast<int>(item0 / nc);
+  cc[0] = static_cast<int>(item0 - static_cast<int64_t>(rr[0]) * nc);
 #pragma unroll
   for (int u = 1; u < kMxItems; ++u) {
     const bool wrap = cc[u - 1] + 1 == nc;

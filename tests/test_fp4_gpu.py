@@ -86,6 +86,41 @@ def test_quant_nvfp4_bit_exact(R, K):
     assert np.array_equal(atoms.cpu().numpy(), oracle.mx_scales_atoms(scales_r))
 
 
+def test_quant_nvfp4_rounding_ties():
+    """Quotients v / (sb sg) exactly on the E2M1 rounding midpoints (0.25, 0.75,
+    1.25, 1.75, 2.5, 3.5, 5: ties to even) and one BF16 step either side of
+    them, with block scales 1, 0.5 and 448 and the tensor scale 1: the
+    quantiser's codes against the oracle's."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    K = 256
+    rows = []
+    for den in (1.0, 0.5, 2.0):            # block amax 6 den -> E4M3 scale den (exact), tensor scale 1
+        for off in (-1, 0, 1):             # BF16 steps off the midpoint
+            v = (mids * den).astype(np.float32)
+            b = syn.f32_to_bf16_bits(v).astype(np.int32) + off
+            blk = np.concatenate([syn.f32_to_bf16_bits(np.array([6.0 * den], np.float32)).astype(np.int32), b,
+                                  b | 0x8000, [0]]).astype(np.uint16)   # amax, the 7 values, their negatives, 0
+            row = np.zeros(K, np.uint16)
+            row[:16] = blk
+            row[16:32] = blk ^ 0x8000
+            rows.append(row)
+    X = np.stack(rows)
+    X[0, 64] = syn.f32_to_bf16_bits(np.array([2688.0], np.float32))[0]   # tensor amax 2688: sg = 1
+    R = X.shape[0]
+    Xd = to_dev(X)
+    sg = torch.empty(4, dtype=torch.float32, device="cuda")
+    q.qlin_nvfp4_tensor_scale(Xd, R * K, sg)
+    codes = torch.empty((R, K // 2), dtype=torch.uint8, device="cuda")
+    atoms = torch.empty((q.qlin_nvfp4_scale_bytes(R, K),), dtype=torch.uint8, device="cuda")
+    q.qlin_quant_nvfp4(Xd, R, K, sg, codes, atoms)
+    torch.cuda.synchronize()
+    sg_r = oracle.nvfp4_global_scale(X)
+    assert np.float32(sg_r) == np.float32(1.0)
+    codes_r, scales_r = oracle.quant_nvfp4_rows(X, sg_r)
+    assert np.array_equal(codes.cpu().numpy(), oracle.pack_fp4(codes_r))
+    assert np.array_equal(atoms.cpu().numpy(), oracle.mx_scales_atoms(scales_r))
+
+
 # (id, M, N, K, token tile, split count)
 GEMM_CASES = [
     ("bn32_m1", 1, 512, 1024, 32, 1),
