@@ -92,6 +92,32 @@ def test_fp8_and_pack_reject_bad_arguments(lib):
     assert lib.qlin_quant_w_fp8(16, 128, 128, 16, 16, None, 0, None) == 1
 
 
+def test_fused_calls_reject_bad_epilogue_arguments(lib):
+    """Every *_gemm_fused call checks its activation and bias before anything
+    else (no device needed); an empty call launches nothing."""
+    calls = {
+        "qlin_w4a16_gemm_fused": lambda b, a, M=1: lib.qlin_w4a16_gemm_fused(16, 16, 16, 16, 16, M, 128, 128, 128, b, a,
+                                                                             None, 0, 0, None),
+        "qlin_w8a8_fp8_gemm_fused": lambda b, a, M=1: lib.qlin_w8a8_fp8_gemm_fused(16, 16, 16, 16, 16, M, 128, 128, b,
+                                                                                   a, None, 0, 0, None),
+        "qlin_w8a8_fp8_block_gemm_fused": lambda b, a, M=1: lib.qlin_w8a8_fp8_block_gemm_fused(
+            16, 16, 16, 16, 16, M, 128, 128, b, a, None, 0, None),
+        "qlin_w4a8_gemm_fused": lambda b, a, M=1: lib.qlin_w4a8_gemm_fused(16, 16, 16, 16, 16, 16, M, 128, 128, 128, b,
+                                                                           a, None, 0, None),
+        "qlin_mxfp8_gemm_fused": lambda b, a, M=1: lib.qlin_mxfp8_gemm_fused(16, 16, 16, 16, 16, M, 128, 128, b, a,
+                                                                             None, 0, None),
+        "qlin_mxfp4_gemm_fused": lambda b, a, M=1: lib.qlin_mxfp4_gemm_fused(16, 16, 16, 16, 16, M, 128, 256, b, a,
+                                                                             None, 0, None),
+        "qlin_nvfp4_gemm_fused": lambda b, a, M=1: lib.qlin_nvfp4_gemm_fused(16, 16, 16, 16, 16, 16, 16, M, 128, 256,
+                                                                             b, a, None, 0, None),
+    }
+    for name, call in calls.items():
+        assert call(None, q.ACT_GELU + 1) == 1, name    # unknown activation
+        assert call(None, -1) == 1, name
+        assert call(24, q.ACT_SILU) == 3, name          # bias not 16-byte aligned
+        assert call(16, q.ACT_RELU, M=0) == 0, name     # empty call
+
+
 # The dispatch query plans without a device when given an SM count.
 def test_plan_query_without_device(lib):
     p = q.qlin_plan_info(q.OP_W4A16_GEMM, 2048, 28672, 4096, 128, q.PATH_TC, 152)
