@@ -61,7 +61,7 @@ def w8_alg_bytes(M, N, K):
 # for M = 1, K = 4096, N = 28672, against that launch's algorithmic bytes.  The
 # traffic of a bench launch is scaled from it by its algorithmic bytes (traffic grows
 # in proportion: the weights are streamed once).
-TRAFFIC_CAPTURE = {"kernel": "w4a16_mma_splitk", "dram_bytes": 61064448 + 15360,
+TRAFFIC_CAPTURE = {"kernel": "w4a16_mma_splitk", "dram_bytes": 61064448 + 8448,
                    "alg_bytes": 28672 * 4096 // 2 + 2 * 28672 * 32 + 28672 * 32 // 2 + 2 * 4096 + 2 * 28672}
 
 
