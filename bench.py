@@ -57,7 +57,7 @@ def w8_alg_bytes(M, N, K):
 
 
 # DRAM traffic of the small-M W4A16 kernel from one ncu capture (profiles/
-# w4a16_mma_splitk_m1_gateup_4096x28672.md): dram__bytes_read.sum + dram__bytes_write.sum
+# w4a16_decode_llama8b_launch_list.md): dram__bytes_read.sum + dram__bytes_write.sum
 # for M = 1, K = 4096, N = 28672, against that launch's algorithmic bytes.  The
 # traffic of a bench launch is scaled from it by its algorithmic bytes (traffic grows
 # in proportion: the weights are streamed once).
