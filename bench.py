@@ -966,6 +966,46 @@ def run_sweep(args):
         torch.cuda.empty_cache()
     if args.sweep == "crossover":
         print(json.dumps(crossover_summary(results, p16, p8_use, bw)), flush=True)
+    if args.sweep == "epilogue":
+        sweep_epilogue_blocks(l2)
+
+
+def sweep_epilogue_blocks(l2):
+    """The fused bias + SiLU epilogue of the block formats, W4A8 and block-scaled
+    FP8 against their plain GEMMs (activations quantised once, outside the timing;
+    weight copies rotated past L2)."""
+    import torch
+
+    import precision_quantized_linear_gb300 as q
+    from precision_quantized_linear_gb300 import synthetic as syn
+    from precision_quantized_linear_gb300.layers import (MXFP4Linear, MXFP8Linear, NVFP4Linear, W4A8Linear,
+                                                          W8A8BlockLinear)
+    K, N = 4096, 28672
+    W = torch.from_numpy(syn.make_weight(N, K, seed=K + N).view(np.int16)).cuda().view(torch.bfloat16)
+    bias = torch.from_numpy(syn.make_act(1, N, seed=N)[0].view(np.int16)).cuda().view(torch.bfloat16)
+    kinds = {"mxfp8": (MXFP8Linear, 1.0), "mxfp4": (MXFP4Linear, 0.5), "nvfp4": (NVFP4Linear, 0.5),
+             "w4a8": (W4A8Linear, 0.51953125), "w8a8b": (W8A8BlockLinear, 1.0)}
+    for name, (cls, bpw) in kinds.items():
+        copies = max(1, int(np.ceil(3 * l2 / (bpw * N * K))))
+        lins = [cls(W, bias=bias) for _ in range(copies)]
+        for M in (16, 256, 2048):
+            X = torch.from_numpy(syn.make_act(M, K, seed=M + 7).view(np.int16)).cuda().view(torch.bfloat16)
+            ops = lins[0].quant_act(X)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            row = {"K": K, "N": N, "M": M, "variant": name}
+            for act, key in ((q.ACT_NONE, "us_bias"), (q.ACT_SILU, "us_bias_silu")):
+                row[key] = round(time_launches([lambda st, l=l: l.gemm(*ops, Y=Y, stream=st, act=act) for l in lins]), 2)
+            saved = [l.bias for l in lins]
+            for l in lins:
+                l.bias = None
+            row["us_plain"] = round(time_launches([lambda st, l=l: l.gemm(*ops, Y=Y, stream=st) for l in lins]), 2)
+            for l, b in zip(lins, saved):
+                l.bias = b
+            row["cost_silu"] = "%+.0f %%" % (100.0 * (row["us_bias_silu"] / row["us_plain"] - 1.0))
+            assert q.qlin_get_device_error() == 0
+            print(json.dumps(row), flush=True)
+        del lins
+        torch.cuda.empty_cache()
 
 
 def run_case(args):

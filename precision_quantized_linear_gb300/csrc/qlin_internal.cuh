@@ -48,6 +48,18 @@ __device__ __forceinline__ float epi_act(int act, float v, float b) {
   }
 }
 __device__ __forceinline__ float epi_apply(const Epi& e, float v, int64_t n) { return epi_act(e.act, v, epi_bias(e, n)); }
+// act(v + b) as a called function, for epilogue loops that are unrolled over
+// many outputs (the block-format, block-scaled and W4A8 kernels): one copy of
+// each activation's code serves every output, where inlining it per output
+// would multiply the kernel's code many times over
+static __device__ __noinline__ float epi_act_call(int act, float v) { return epi_act(act, v, 0.0f); }
+// act(v + b) with the addition inline and the activation called only when one is set
+__device__ __forceinline__ float epi_sparse(int act, float v, float b) {
+  v += b;
+  return act == QLIN_ACT_NONE ? v : epi_act_call(act, v);
+}
+// the same for output column n
+__device__ __forceinline__ float epi_cols(const Epi& e, float v, int64_t n) { return epi_sparse(e.act, v, epi_bias(e, n)); }
 // act(o[i] + b) for a run of values of one output column: one branch on the
 // activation for the whole run, so that each loop stays straight-line code
 template <int L>

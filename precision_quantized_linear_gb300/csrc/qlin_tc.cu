@@ -1105,7 +1105,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
             for (int c = 0; c < kCw; c += 8) {
               if constexpr (EPI) {  // bias of columns n0 + c .. (one weight row each)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) r[c + i] = epi_apply(a.epi, r[c + i], n0 + c + i);
+                for (int i = 0; i < 8; ++i) r[c + i] = epi_cols(a.epi, r[c + i], n0 + c + i);
               }
               uint32_t w[4];
 #pragma unroll
@@ -1141,10 +1141,10 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
                   __stcg(pp, make_float4(0.0f, 0.0f, 0.0f, 0.0f));
                 }
                 if constexpr (EPI) {
-                  acc_v.x = epi_apply(a.epi, acc_v.x, n0 + c);
-                  acc_v.y = epi_apply(a.epi, acc_v.y, n0 + c + 1);
-                  acc_v.z = epi_apply(a.epi, acc_v.z, n0 + c + 2);
-                  acc_v.w = epi_apply(a.epi, acc_v.w, n0 + c + 3);
+                  acc_v.x = epi_cols(a.epi, acc_v.x, n0 + c);
+                  acc_v.y = epi_cols(a.epi, acc_v.y, n0 + c + 1);
+                  acc_v.z = epi_cols(a.epi, acc_v.z, n0 + c + 2);
+                  acc_v.w = epi_cols(a.epi, acc_v.w, n0 + c + 3);
                 }
                 const uint32_t lo = static_cast<uint32_t>(to_bf16(acc_v.x)) | (static_cast<uint32_t>(to_bf16(acc_v.y)) << 16);
                 const uint32_t hi = static_cast<uint32_t>(to_bf16(acc_v.z)) | (static_cast<uint32_t>(to_bf16(acc_v.w)) << 16);
@@ -1237,7 +1237,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
               named_bar(2 + half, 128);
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                box[i * kTileN + quad * 32 + lane] = to_bf16(EPI ? epi_act(a.epi.act, r[c0 + i], bias_n) : r[c0 + i]);
+                box[i * kTileN + quad * 32 + lane] = to_bf16(EPI ? epi_sparse(a.epi.act, r[c0 + i], bias_n) : r[c0 + i]);
               fence_proxy_async_smem();
               named_bar(2 + half, 128);
               if (th == 0) tma_store_2d(&tmap_y, box, un.nt * kTileN, static_cast<int>(m0));
@@ -1280,7 +1280,7 @@ __global__ void __maxnreg__((TcCfg<BN, W4, KPS, BS, WN, MX, A8>::kMaxRegs))
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const int64_t m = mbase + c0 + i;
-                if (m < a.M) a.Y[m * a.N + n] = to_bf16(EPI ? epi_act(a.epi.act, acc_v[i], bias_n) : acc_v[i]);
+                if (m < a.M) a.Y[m * a.N + n] = to_bf16(EPI ? epi_sparse(a.epi.act, acc_v[i], bias_n) : acc_v[i]);
               }
             }
             if (te == 0) a.counters[tile] = 0u;
